@@ -1,0 +1,202 @@
+/*
+ * gpt2.h -- C ABI of the GB300 (sm_103a) GPT-2 training-step library (libgpt2.so).
+ *
+ * One process-global model instance (the llm.c pages drive a single
+ * `GPT2 model` from main; these calls follow that page's gpt2_build /
+ * gpt2_forward / gpt2_zero_grad / gpt2_backward / gpt2_update / gpt2_free
+ * sequence, llm.c "train_gpt2.cu", sections gpt2_forward .. gpt2_free).
+ *
+ * Conventions for every call:
+ *  - Integer-returning calls return GPT2_OK (0) or a negative GPT2_ERR_* code;
+ *    gpt2_last_error() then holds a one-line description. No call exits the
+ *    process or prints.
+ *  - The library owns all model memory (parameters, gradients, AdamW state,
+ *    activations) on the current CUDA device, and allocates nothing per step.
+ *  - Work is enqueued on the library's stream (gpt2_set_stream); calls that
+ *    return host values synchronise that stream, the others are asynchronous.
+ *  - Parameter layout: one flat array of 16 tensors in the order
+ *      wte(Vp,C) wpe(maxT,C) ln1w(L,C) ln1b(L,C) qkvw(L,3C,C) qkvb(L,3C)
+ *      attprojw(L,C,C) attprojb(L,C) ln2w(L,C) ln2b(L,C) fcw(L,4C,C) fcb(L,4C)
+ *      fcprojw(L,C,4C) fcprojb(L,C) lnfw(C) lnfb(C)
+ *    (llm.c "train_gpt2.cu", ParameterTensors / fill_in_parameter_sizes).
+ *    Weight matrices are (out, in) row-major, as nn.Linear stores them.
+ */
+#ifndef GPT2_GB300_H
+#define GPT2_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define GPT2_OK 0
+#define GPT2_ERR_CONFIG (-1)         /* invalid model dimensions or unsupported mode */
+#define GPT2_ERR_STATE (-2)          /* call out of order (no model, backward before forward, ...) */
+#define GPT2_ERR_SHAPE (-3)          /* B or T differs from the first forward, or T > maxT */
+#define GPT2_ERR_TOKEN (-4)          /* a token or target id outside [0, V) */
+#define GPT2_ERR_ALIGN (-5)          /* pointer or leading dimension not 16-byte aligned */
+#define GPT2_ERR_CUDA (-6)           /* a CUDA runtime/driver call failed */
+#define GPT2_ERR_NOMEM (-7)          /* device or pinned-host allocation failed */
+#define GPT2_ERR_ARG (-8)            /* NULL pointer or out-of-range scalar argument */
+#define GPT2_ERR_DEVICE_TIMEOUT (-9) /* a bounded in-kernel wait gave up; results are invalid */
+
+/* precision modes for gpt2_init_ex */
+#define GPT2_FP32 0 /* fp32 parameters, gradients and activations (llm.c train_gpt2_fp32.cu) */
+#define GPT2_BF16 1 /* bf16 parameters, gradients and activations; fp32 master weights and AdamW
+                       moments (llm.c train_gpt2.cu, default floatX and use_master_weights) */
+
+/* Create the model with seeded random initial weights in bf16 mixed precision on
+ * the tensor cores (the llm.c page's default build). Equivalent to
+ * gpt2_init_ex(L, C, NH, V, Vp, maxT, seed, GPT2_BF16, 1).
+ *  L >= 0 layers, C channels (C % NH == 0, head size C/NH in {16, 32, 64, 128}, C % 8 == 0),
+ *  V <= Vp vocabulary (Vp % 8 == 0), maxT >= 1 positions.
+ * Initial weights: wte, wpe, qkvw, fcw ~ N(0, 0.02); attprojw, fcprojw ~ N(0, 0.02/sqrt(2L));
+ * biases 0; LayerNorm gains 1, shifts 0; wte rows [V, Vp) are 0. Replaces any
+ * previous model. Errors: GPT2_ERR_CONFIG, GPT2_ERR_NOMEM, GPT2_ERR_CUDA. */
+int gpt2_init(int L, int C, int NH, int V, int Vp, int maxT, unsigned long long seed);
+
+/* As gpt2_init with an explicit precision (GPT2_FP32 / GPT2_BF16) and
+ * tensor_cores: 1 = tcgen05 tensor-core GEMMs and attention (bf16 only),
+ * 0 = SIMT FP32-FMA kernels ("-f 0", TF32 off, in llm.c train_gpt2.cu main). */
+int gpt2_init_ex(int L, int C, int NH, int V, int Vp, int maxT, unsigned long long seed,
+                 int precision, int tensor_cores);
+
+/* Use `stream` (a cudaStream_t, e.g. torch.cuda.current_stream().cuda_stream)
+ * for all further work; NULL selects the library's own stream. */
+int gpt2_set_stream(void* stream);
+
+/* Forward pass (llm.c "train_gpt2.cu", gpt2_forward). tokens/targets are HOST
+ * int32 arrays of B*T ids in [0, V); targets may be NULL (then no loss and the
+ * call returns -1.0f, as on the page). The first forward fixes B and T
+ * (later calls must use the same B, T <= maxT). Returns the mean loss over
+ * the B*T positions (synchronises the stream), or NaN on error (see
+ * gpt2_last_error). Ids are validated on the host before any work is enqueued. */
+float gpt2_forward(const int* tokens, const int* targets, int B, int T);
+
+/* Forward pass on DEVICE-resident int32 tokens/targets (B*T each; targets may
+ * be NULL). Fully asynchronous: the mean loss is written to the device float
+ * *d_mean_loss (may be NULL). Ids outside [0, V) are clamped to 0 on the device
+ * and reported as GPT2_ERR_TOKEN by the next gpt2_sync(). */
+int gpt2_forward_device(const int* d_tokens, const int* d_targets, int B, int T,
+                        float* d_mean_loss);
+
+/* Set every parameter gradient to zero (llm.c gpt2_zero_grad). */
+int gpt2_zero_grad(void);
+
+/* Gradient accumulation over k >= 1 micro-steps: the next forwards seed the
+ * backward with dloss = 1/(k*B*T) instead of the page's 1/(B*T). */
+int gpt2_set_grad_accum(int k);
+
+/* Backward pass of the last forward (llm.c gpt2_backward). Parameter
+ * gradients ACCUMULATE (+=); activation gradients are overwritten, except the
+ * residual-stream gradient to which each LayerNorm backward adds.
+ * GPT2_ERR_STATE if the last forward had no targets. */
+int gpt2_backward(void);
+
+/* AdamW update of every parameter (llm.c gpt2_update / adamw_kernel3):
+ * m = b1 m + (1-b1) g; v = b2 v + (1-b2) g^2; mhat = m/(1-b1^step); vhat = v/(1-b2^step);
+ * theta -= lr (mhat/(sqrt(vhat)+eps) + wd theta). step >= 1. In GPT2_BF16 the fp32
+ * master copy is updated and rounded (nearest-even) into the bf16 parameters. */
+int gpt2_adamw(float lr, float beta1, float beta2, float eps, float weight_decay, int step);
+
+/* Wait for the stream; report GPT2_ERR_DEVICE_TIMEOUT / GPT2_ERR_TOKEN raised by kernels. */
+int gpt2_sync(void);
+
+/* Introspection (host fp32 copies, flat order above; all synchronise). */
+size_t gpt2_num_params(void);
+int gpt2_param_sizes(size_t out[16]);
+int gpt2_get_params(float* host);       /* current parameters (bf16 widened to fp32) */
+int gpt2_set_params(const float* host); /* also resets the fp32 master copy and AdamW moments */
+int gpt2_get_grads(float* host);
+int gpt2_get_master(float* host);       /* fp32 master weights (GPT2_BF16 only) */
+int gpt2_get_losses(float* host);       /* per-position losses of the last forward, B*T */
+
+/* Activation read-out for tests: which = GPT2_ACT_*, layer in [0, L) where it applies.
+ * Copies the tensor (widened to fp32) to host and returns its element count
+ * through *n (may be NULL). */
+#define GPT2_ACT_ENCODED 0   /* (B,T,C) */
+#define GPT2_ACT_LN1 1       /* (L,B,T,C) */
+#define GPT2_ACT_QKV 2       /* (L,B,T,3C) */
+#define GPT2_ACT_ATTY 4      /* (L,B,T,C) */
+#define GPT2_ACT_RESIDUAL2 5 /* (L,B,T,C) */
+#define GPT2_ACT_LN2 6       /* (L,B,T,C) */
+#define GPT2_ACT_FCH 7       /* (L,B,T,4C) */
+#define GPT2_ACT_FCH_GELU 8  /* (L,B,T,4C) */
+#define GPT2_ACT_RESIDUAL3 9 /* (L,B,T,C) */
+#define GPT2_ACT_LNF 10      /* (B,T,C) */
+#define GPT2_ACT_LOGITS 11   /* (B,T,Vp): logits after forward without targets, dlogits after one with targets */
+#define GPT2_ACT_LSE 18      /* (L,B,NH,T) fp32 attention log-sum-exp */
+int gpt2_get_activation(int which, int layer, float* host, size_t* n);
+
+/* Release all device memory held by the model. */
+int gpt2_free(void);
+
+/* Text of the last error (static storage, never NULL). */
+const char* gpt2_last_error(void);
+
+/* ---- kernel timing (CUDA events around each launch, for roofline reporting) ----
+ * family: 0 GEMM, 1 attention forward, 2 attention backward, 3 LayerNorm forward,
+ * 4 LayerNorm backward, 5 classifier softmax-CE, 6 AdamW, 7 encoder, 8 other.
+ * gpt2_timing_begin(max_launches) starts recording (events are preallocated);
+ * gpt2_timing_end() synchronises and totals; gpt2_timing_get returns, per family,
+ * total milliseconds, launch count and algorithmic work (FLOPs for GEMM and
+ * attention families, bytes for the others). */
+int gpt2_timing_begin(int max_launches);
+int gpt2_timing_end(void);
+int gpt2_timing_get(int family, double* total_ms, long long* launches, double* work);
+
+/* ---- standalone fused operator ----
+ * out = softmax_row( gelu_tanh( x . W^T + b ) ) (POPCORNBENCH "fused Linear +
+ * GELU + Softmax" problem statement: nn.Linear then GELU then softmax over dim 1).
+ * x: DEVICE fp32 (M,K) row-major; W: DEVICE fp32 (N,K) row-major (nn.Linear
+ * layout); b: DEVICE fp32 (N); out: DEVICE fp32 (M,N) row-major, caller-owned.
+ * The GEMM runs on the TF32 tensor cores (fp32 accumulate). x, W and out must
+ * be 16-byte aligned with K % 4 == 0 and N % 4 == 0 (else GPT2_ERR_ALIGN);
+ * M, K, N >= 1 (else GPT2_ERR_ARG). Asynchronous on `stream` (a cudaStream_t,
+ * NULL = legacy default stream). The first call on a device allocates its
+ * scratch (per-row softmax partials, grown as needed and kept until exit). */
+int fused_linear_bias_gelu_softmax(const float* x, const float* W, const float* b, float* out,
+                                   int M, int K, int N, void* stream);
+
+/* ---- kernel-level entry points (DEVICE pointers, asynchronous on `stream`) ----
+ * gpt2_gemm: D[M,N] = A[M,K] . B[N,K]^T with the step's fused epilogues.
+ *  dtype GPT2_FP32 / GPT2_BF16 is the element type of A, B, D, bias, aux, D2;
+ *  tensor_cores = 1 selects the tcgen05 kernel (bf16: kind::f16; fp32: kind::tf32,
+ *  K-major operands only), 0 the SIMT FP32-FMA kernel.
+ *  Storage: a_kmajor ? A(m,k) = A[m*lda + k] : A[k*lda + m];
+ *           b_kmajor ? B(n,k) = B[n*ldb + k] : B[k*ldb + n];  D(m,n) = D[m*ldd + n].
+ *  epilogue: 0 D = acc (+ bias[n]); 1 D = acc + bias[n], D2 = gelu(D) (same ldd);
+ *            2 D = acc + bias[n] + aux(m,n); 3 D = acc * gelu'(aux(m,n)); 4 D += acc.
+ *  (llm.c "train_gpt2.cu": matmul_forward_cublaslt, matmul_backward, gelu_forward,
+ *  gelu_backward, residual_forward.) bias may be NULL. Tensor-core path needs
+ *  16-byte aligned pointers and leading dimensions and N % (16/elem) == 0, else
+ *  GPT2_ERR_ALIGN. */
+int gpt2_gemm(int dtype, int tensor_cores, int epilogue, const void* A, long long lda, int a_kmajor,
+              const void* B, long long ldb, int b_kmajor, void* D, long long ldd, const void* bias,
+              const void* aux, long long ldaux, void* D2, int M, int N, int K, void* stream);
+
+/* Causal attention forward over a fused (B,T,3,NH,HS) qkv: out (B,T,NH*HS) and
+ * lse (B,NH,T) fp32 natural-log sum of exp of the scaled scores (llm.c
+ * attention_forward with softmax_forward_kernel5, scale 1/sqrt(HS)).
+ * HS = C/NH in {16,32,64,128}; bf16 with tensor_cores and HS == 64 uses the
+ * tensor-core flash kernel, everything else the SIMT kernel. */
+int gpt2_attention_forward(int dtype, int tensor_cores, const void* qkv, void* out, float* lse,
+                           int B, int T, int C, int NH, void* stream);
+
+/* Its backward: dqkv (B,T,3C) is written (llm.c attention_backward with
+ * softmax_autoregressive_backward_kernel); scratch_D is B*NH*T floats. */
+int gpt2_attention_backward(int dtype, int tensor_cores, const void* dout, const void* qkv,
+                            const void* out, const float* lse, void* dqkv, float* scratch_D, int B,
+                            int T, int C, int NH, void* stream);
+
+/* Synchronise the device and report (then clear) the error word of the
+ * stand-alone entry points: GPT2_ERR_DEVICE_TIMEOUT if a bounded wait expired. */
+int gpt2_device_status(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif

@@ -1,0 +1,39 @@
+"""The C ABI library builds for sm_103a, loads without a GPU, and exports every
+function that include/*.h declares."""
+import ctypes
+import glob
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", src, re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.mark.skipif(shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                    reason="no CUDA toolkit")
+def test_library_exports_every_declared_symbol():
+    from transformer_lm_gb300 import build
+    path = build.build()
+    lib = ctypes.CDLL(path)
+    names = _declared_functions()
+    assert len(names) >= 25, names
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_declares_the_same_names():
+    from transformer_lm_gb300 import gpt2
+    names = set(_declared_functions())
+    assert names == set(gpt2._SIGS), names ^ set(gpt2._SIGS)

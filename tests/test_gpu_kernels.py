@@ -1,0 +1,126 @@
+"""Kernel-level parity against the oracle: every GEMM operand layout and
+epilogue (tcgen05 bf16, SIMT fp32 and bf16), and causal attention forward and
+backward (tensor-core flash kernels and SIMT), on shapes that span several
+tiles and end in ragged tails."""
+import numpy as np
+import pytest
+
+import oracle
+from transformer_lm_gb300 import inputs
+from transformer_lm_gb300 import gpt2 as G
+from tests.gpu_util import dev, host, empty, rel_to_max, max_rel_floor
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(200, 136, 72), (256, 512, 128), (130, 264, 1000), (1024, 768, 768), (64, 8, 16)]
+
+
+def _operands(M, N, K, seed, bf16):
+    A = inputs.normal(seed, 1, M * K).reshape(M, K).astype(np.float32)
+    B = inputs.normal(seed, 2, N * K, 0.05).reshape(N, K).astype(np.float32)
+    bias = inputs.normal(seed, 3, N, 0.5).astype(np.float32)
+    aux = inputs.normal(seed, 4, M * N).reshape(M, N).astype(np.float32)
+    D0 = inputs.normal(seed, 5, M * N, 0.3).reshape(M, N).astype(np.float32)
+    if bf16:
+        A, B, bias, aux, D0 = (inputs.round_to_bf16(x) for x in (A, B, bias, aux, D0))
+    return A, B, bias, aux, D0
+
+
+def _ref(epi, A, B, bias, aux, D0):
+    acc = oracle.matmul_forward(A, B, None)
+    if epi == "store":
+        return acc + bias, None
+    if epi == "gelu":
+        pre = acc + bias
+        return pre, oracle.gelu_forward(pre)
+    if epi == "resid":
+        return acc + bias + aux, None
+    if epi == "gelu_bwd":
+        return oracle.gelu_backward(aux, acc), None
+    if epi == "accum":
+        return D0.astype(np.float64) + acc, None
+    raise ValueError(epi)
+
+
+MODES = [("bf16", 1), ("bf16", 0), ("f32", 0)]
+
+
+@pytest.mark.parametrize("mode", MODES, ids=lambda m: f"{m[0]}-tc{m[1]}")
+@pytest.mark.parametrize("a_km,b_km", [(1, 1), (1, 0), (0, 0), (0, 1)])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_gemm_layouts_match_oracle(mode, a_km, b_km, shape):
+    dt, tc = mode
+    M, N, K = shape
+    bf16 = dt == "bf16"
+    A, B, bias, aux, D0 = _operands(M, N, K, 7 + M + N + K, bf16)
+    ref, _ = _ref("store", A, B, bias, aux, D0)
+    dA = dev(A if a_km else A.T, dt)
+    dB = dev(B if b_km else B.T, dt)
+    D = empty((M, N), dt)
+    G.gpt2_gemm(G.GPT2_BF16 if bf16 else G.GPT2_FP32, tc, "store", dA, K if a_km else M, a_km, dB,
+                K if b_km else N, b_km, D, N, bias=dev(bias, dt), M=M, N=N, K=K)
+    G.gpt2_device_status()
+    err = rel_to_max(host(D), ref)
+    assert err < (8e-3 if bf16 else 1e-5), err
+
+
+@pytest.mark.parametrize("mode", MODES, ids=lambda m: f"{m[0]}-tc{m[1]}")
+@pytest.mark.parametrize("epi", ["gelu", "resid", "gelu_bwd", "accum"])
+def test_gemm_epilogues_match_oracle(mode, epi):
+    dt, tc = mode
+    bf16 = dt == "bf16"
+    M, N, K = 300, 392, 200
+    A, B, bias, aux, D0 = _operands(M, N, K, 99, bf16)
+    ref, ref2 = _ref(epi, A, B, bias, aux, D0)
+    D = dev(D0, dt) if epi == "accum" else empty((M, N), dt)
+    D2 = empty((M, N), dt) if epi == "gelu" else None
+    G.gpt2_gemm(G.GPT2_BF16 if bf16 else G.GPT2_FP32, tc, epi, dev(A, dt), K, 1, dev(B.T, dt), N, 0,
+                D, N, bias=dev(bias, dt), aux=dev(aux, dt), ldaux=N, D2=D2, M=M, N=N, K=K)
+    G.gpt2_device_status()
+    tol = 1e-2 if bf16 else 1e-5
+    assert rel_to_max(host(D), ref) < tol
+    if D2 is not None:
+        assert rel_to_max(host(D2), ref2) < tol
+
+
+@pytest.mark.parametrize("B,T,C,NH,dt,tc", [
+    (2, 64, 128, 2, "bf16", 1), (2, 130, 128, 2, "bf16", 1), (1, 1, 128, 2, "bf16", 1),
+    (2, 256, 256, 4, "bf16", 1), (3, 17, 128, 2, "bf16", 1),
+    (2, 70, 64, 4, "f32", 0), (2, 33, 128, 2, "f32", 0), (1, 40, 64, 2, "bf16", 0)])
+def test_attention_forward_backward_match_oracle(B, T, C, NH, dt, tc):
+    bf16 = dt == "bf16"
+    qkv = inputs.normal(5 + T, 1, B * T * 3 * C).astype(np.float32)
+    dout = inputs.normal(5 + T, 2, B * T * C, 0.1).astype(np.float32)
+    if bf16:
+        qkv, dout = inputs.round_to_bf16(qkv), inputs.round_to_bf16(dout)
+    ref_out, att = oracle.attention_forward(qkv, B, T, C, NH)
+    ref_dqkv = oracle.attention_backward(dout, qkv, att, B, T, C, NH)
+    prec = G.GPT2_BF16 if bf16 else G.GPT2_FP32
+    d_qkv = dev(qkv, dt)
+    out = empty((B * T * C,), dt)
+    import torch
+    lse = torch.zeros(B * NH * T, dtype=torch.float32, device="cuda")
+    G.gpt2_attention_forward(prec, tc, d_qkv, out, lse, B, T, C, NH)
+    dqkv = empty((B * T * 3 * C,), dt)
+    Dsc = torch.zeros(B * NH * T, dtype=torch.float32, device="cuda")
+    G.gpt2_attention_backward(prec, tc, dev(dout, dt), d_qkv, out, lse, dqkv, Dsc, B, T, C, NH)
+    G.gpt2_device_status()
+    tol = 2e-2 if bf16 else 1e-5
+    assert rel_to_max(host(out), ref_out) < tol
+    got = host(dqkv).reshape(B, T, 3, C)
+    ref = ref_dqkv.reshape(B, T, 3, C)
+    for part in range(3):
+        assert rel_to_max(got[:, :, part], ref[:, :, part]) < (3e-2 if bf16 else 1e-5), part
+
+
+def test_fused_op_small_shapes_match_oracle():
+    import torch
+    for (M, K, N) in [(130, 72, 264), (256, 512, 1000), (1, 4, 4)]:
+        x, W, b = inputs.fused_op_inputs(M, K, N, seed=3)
+        ref = oracle.fused_linear_bias_gelu_softmax(x, W, b)
+        out = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+        G.fused_linear_bias_gelu_softmax(dev(x), dev(W), dev(b), out, M, K, N)
+        G.gpt2_device_status()
+        y = host(out)
+        np.testing.assert_allclose(y.sum(1), 1.0, atol=1e-5)
+        assert max_rel_floor(y, ref, 0.0) < 2e-2, (M, K, N, max_rel_floor(y, ref, 0.0))

@@ -1,0 +1,266 @@
+"""Whole-step parity of the CUDA path against the oracle (through the C ABI).
+
+Tolerances:
+  fp32 path: loss within 1e-5 relative; every gradient and post-AdamW
+             parameter within 1e-3 of max(|ref|, 1e-5) elementwise.
+  bf16 path: loss within 2e-2 absolute; per-tensor gradient cosine >= 0.99.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from transformer_lm_gb300 import inputs
+from transformer_lm_gb300 import gpt2 as G
+from tests.gpu_util import max_rel_floor, cosine
+
+pytestmark = pytest.mark.gpu
+
+
+def _split(flat, d):
+    out, off = {}, 0
+    for name, s in zip(inputs.PARAM_NAMES, inputs.param_sizes(d)):
+        out[name] = flat[off:off + s]
+        off += s
+    return out
+
+
+def _oracle_step(d, params, tok, tgt, k=1):
+    B, T = tok.shape
+    m = oracle.Model(d.L, d.C, d.NH, d.V, d.Vp, d.maxT, B, T)
+    loss = m.forward(params.astype(np.float64), tok, tgt, grad_accum_k=k)
+    grads = np.zeros(params.size)
+    m.backward(grads)
+    return m, loss, grads
+
+
+def _init(d, prec, tc, params):
+    G.gpt2_init_ex(d.L, d.C, d.NH, d.V, d.Vp, d.maxT, 1, prec, tc)
+    G.gpt2_set_params(params)
+
+
+# ----------------------------------------------------------------------------- fp32 (config 0)
+def test_tiny_fp32_step_matches_oracle():
+    d = inputs.TINY
+    B, T = 2, 32
+    params = inputs.gpt2_params(d, 1337, perturb=True)
+    tok = inputs.tokens(42, 1, B, T, d.V)
+    tgt = inputs.tokens(42, 2, B, T, d.V)
+    m, ref_loss, ref_g = _oracle_step(d, params, tok, tgt)
+    _init(d, G.GPT2_FP32, 0, params)
+    G.gpt2_zero_grad()
+    loss = G.gpt2_forward(tok, tgt, B, T)
+    assert abs(loss - ref_loss) <= 1e-5 * abs(ref_loss), (loss, ref_loss)
+    np.testing.assert_allclose(G.gpt2_get_losses(B * T), m.act("losses"), rtol=1e-5)
+    G.gpt2_backward()
+    g = G.gpt2_get_grads()
+    for name in inputs.PARAM_NAMES:
+        err = max_rel_floor(_split(g, d)[name], _split(ref_g, d)[name], 1e-5)
+        assert err <= 1e-3, (name, err)
+    G.gpt2_adamw(1e-3, 0.9, 0.999, 1e-8, 0.0, 1)
+    p = G.gpt2_get_params()
+    ref_p = params.astype(np.float64)
+    mm, vv = np.zeros_like(ref_p), np.zeros_like(ref_p)
+    oracle.adamw(ref_p, ref_g, mm, vv, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1)
+    for name in inputs.PARAM_NAMES:
+        err = max_rel_floor(_split(p, d)[name], _split(ref_p, d)[name], 1e-5)
+        assert err <= 1e-3, (name, err)
+    G.gpt2_free()
+
+
+def test_tiny_fp32_activations_match_oracle():
+    d = inputs.TINY
+    B, T = 2, 32
+    params = inputs.gpt2_params(d, 7, perturb=True)
+    tok = inputs.tokens(7, 1, B, T, d.V)
+    tgt = inputs.tokens(7, 2, B, T, d.V)
+    m = oracle.Model(d.L, d.C, d.NH, d.V, d.Vp, d.maxT, B, T)
+    m.forward(params.astype(np.float64), tok, tgt)
+    _init(d, G.GPT2_FP32, 0, params)
+    G.gpt2_forward(tok, None, B, T)  # no targets: the logits stay in place
+    for name in ["encoded", "lnf", "logits"]:
+        err = max_rel_floor(G.gpt2_get_activation(name), m.act(name), 1e-3)
+        assert err < 1e-4, (name, err)
+    for l in range(d.L):
+        for name in ["ln1", "qkv", "atty", "residual2", "ln2", "fch", "fch_gelu", "residual3"]:
+            err = max_rel_floor(G.gpt2_get_activation(name, l), m.act(name, l), 1e-3)
+            assert err < 1e-4, (name, l, err)
+    G.gpt2_free()
+
+
+def test_fp32_adamw_multi_step_with_weight_decay_matches_oracle():
+    d = inputs.TINY
+    B, T = 2, 16
+    params = inputs.gpt2_params(d, 3, perturb=True)
+    tok = inputs.tokens(3, 1, B, T, d.V)
+    tgt = inputs.tokens(3, 2, B, T, d.V)
+    _init(d, G.GPT2_FP32, 0, params)
+    ref_p = params.astype(np.float64)
+    mm, vv = np.zeros_like(ref_p), np.zeros_like(ref_p)
+    for step in range(1, 4):
+        _, ref_loss, ref_g = _oracle_step(d, ref_p, tok, tgt)
+        G.gpt2_zero_grad()
+        loss = G.gpt2_forward(tok, tgt, B, T)
+        G.gpt2_backward()
+        G.gpt2_adamw(1e-3, 0.9, 0.95, 1e-8, 0.1, step)
+        oracle.adamw(ref_p, ref_g, mm, vv, 1e-3, 0.9, 0.95, 1e-8, 0.1, step)
+        assert abs(loss - ref_loss) <= 1e-5 * abs(ref_loss), (step, loss, ref_loss)
+    err = max_rel_floor(G.gpt2_get_params(), ref_p, 1e-5)
+    assert err <= 1e-3, err
+    G.gpt2_free()
+
+
+def test_grad_accumulation_equals_double_batch_fp32():
+    d = inputs.TINY
+    B, T = 2, 16
+    params = inputs.gpt2_params(d, 8, perturb=True)
+    tok = inputs.tokens(8, 1, 2 * B, T, d.V)
+    tgt = inputs.tokens(8, 2, 2 * B, T, d.V)
+    _, _, ref_g = _oracle_step(d, params, tok, tgt)
+    _init(d, G.GPT2_FP32, 0, params)
+    G.gpt2_zero_grad()
+    G.gpt2_set_grad_accum(2)
+    for half in (slice(0, B), slice(B, 2 * B)):
+        G.gpt2_forward(tok[half], tgt[half], B, T)
+        G.gpt2_backward()
+    g = G.gpt2_get_grads()
+    assert max_rel_floor(g, ref_g, 1e-5) <= 1e-3
+    G.gpt2_free()
+
+
+# ----------------------------------------------------------------------------- bf16
+SMALL_BF16 = inputs.GPT2Dims(L=2, C=128, NH=2, V=1000, Vp=1024, maxT=256)
+
+
+@pytest.mark.parametrize("tc", [1, 0])
+def test_bf16_step_matches_oracle(tc):
+    d = SMALL_BF16
+    B, T = 2, 192
+    params = inputs.round_to_bf16(inputs.gpt2_params(d, 11, perturb=True))
+    tok = inputs.tokens(11, 1, B, T, d.V)
+    tgt = inputs.tokens(11, 2, B, T, d.V)
+    m, ref_loss, ref_g = _oracle_step(d, params, tok, tgt)
+    _init(d, G.GPT2_BF16, tc, params)
+    assert np.array_equal(G.gpt2_get_params(), params)
+    G.gpt2_zero_grad()
+    loss = G.gpt2_forward(tok, tgt, B, T)
+    assert abs(loss - ref_loss) <= 2e-2, (loss, ref_loss)
+    G.gpt2_backward()
+    G.gpt2_sync()
+    g = G.gpt2_get_grads()
+    for name in inputs.PARAM_NAMES:
+        c = cosine(_split(g, d)[name], _split(ref_g, d)[name])
+        assert c >= 0.99, (name, c)
+    # master weights follow the oracle's update direction
+    G.gpt2_adamw(6e-4, 0.9, 0.95, 1e-8, 0.1, 1)
+    master = G.gpt2_get_master()
+    ref_p = params.astype(np.float64)
+    mm, vv = np.zeros_like(ref_p), np.zeros_like(ref_p)
+    oracle.adamw(ref_p, ref_g, mm, vv, 6e-4, 0.9, 0.95, 1e-8, 0.1, 1)
+    assert cosine(master - params, ref_p - params) >= 0.99
+    G.gpt2_free()
+
+
+def test_bf16_grad_accumulation_is_exact_and_deterministic():
+    """Two k=2 micro-steps on the same batch equal one k=1 step bit for bit
+    (the power-of-two dloss scale is exact), and repeated runs are identical."""
+    d = SMALL_BF16
+    B, T = 2, 128
+    params = inputs.round_to_bf16(inputs.gpt2_params(d, 12, perturb=True))
+    tok = inputs.tokens(12, 1, B, T, d.V)
+    tgt = inputs.tokens(12, 2, B, T, d.V)
+    _init(d, G.GPT2_BF16, 1, params)
+    G.gpt2_zero_grad()
+    G.gpt2_forward(tok, tgt, B, T)
+    G.gpt2_backward()
+    g1 = G.gpt2_get_grads()
+    G.gpt2_zero_grad()
+    G.gpt2_forward(tok, tgt, B, T)
+    G.gpt2_backward()
+    assert np.array_equal(G.gpt2_get_grads(), g1)
+    G.gpt2_zero_grad()
+    G.gpt2_set_grad_accum(2)
+    for _ in range(2):
+        G.gpt2_forward(tok, tgt, B, T)
+        G.gpt2_backward()
+    assert np.array_equal(G.gpt2_get_grads(), g1)
+    G.gpt2_free()
+
+
+def test_device_input_forward_matches_host_input_forward():
+    import torch
+    d = SMALL_BF16
+    B, T = 2, 64
+    params = inputs.round_to_bf16(inputs.gpt2_params(d, 13, perturb=True))
+    tok = inputs.tokens(13, 1, B, T, d.V)
+    tgt = inputs.tokens(13, 2, B, T, d.V)
+    _init(d, G.GPT2_BF16, 1, params)
+    l_host = G.gpt2_forward(tok, tgt, B, T)
+    dt, dg = torch.from_numpy(tok).cuda(), torch.from_numpy(tgt).cuda()
+    dl = torch.zeros(1, device="cuda")
+    G.gpt2_forward_device(dt, dg, B, T, dl)
+    G.gpt2_sync()
+    assert float(dl.item()) == l_host
+    G.gpt2_free()
+
+
+def test_init_distribution():
+    d = inputs.GPT2Dims(L=2, C=256, NH=4, V=1000, Vp=1024, maxT=64)
+    G.gpt2_init(d.L, d.C, d.NH, d.V, d.Vp, d.maxT, 1337)
+    p = _split(G.gpt2_get_params(), d)
+    wte = p["wte"].reshape(d.Vp, d.C)
+    assert np.all(wte[d.V:] == 0)
+    assert abs(wte[:d.V].std() - 0.02) < 1e-3 and abs(wte[:d.V].mean()) < 1e-3
+    assert abs(p["fcprojw"].std() - 0.02 / math.sqrt(2 * d.L)) < 5e-4
+    assert np.all(p["ln1w"] == 1) and np.all(p["lnfb"] == 0) and np.all(p["qkvb"] == 0)
+    G.gpt2_free()
+
+
+# ----------------------------------------------------------------------------- errors
+def test_host_side_faults_are_reported_not_fatal():
+    d = inputs.TINY
+    with pytest.raises(G.GPT2Error) as e:
+        G.gpt2_init_ex(2, 60, 4, 512, 512, 32, 1, G.GPT2_FP32, 0)
+    assert e.value.code == -1
+    with pytest.raises(G.GPT2Error):
+        G.gpt2_init_ex(2, 64, 4, 512, 500, 32, 1, G.GPT2_FP32, 0)
+    G.gpt2_init_ex(d.L, d.C, d.NH, d.V, d.Vp, d.maxT, 1, G.GPT2_FP32, 0)
+    with pytest.raises(G.GPT2Error) as e:
+        G.gpt2_backward()
+    assert e.value.code == -2
+    tok = inputs.tokens(1, 1, 2, 16, d.V)
+    bad = tok.copy()
+    bad[1, 3] = d.V
+    with pytest.raises(G.GPT2Error) as e:
+        G.gpt2_forward(bad, tok, 2, 16)
+    assert e.value.code == -4
+    with pytest.raises(G.GPT2Error) as e:
+        G.gpt2_forward(inputs.tokens(1, 1, 1, 64, d.V), None, 1, 64)
+    assert e.value.code == -3
+    G.gpt2_forward(tok, tok, 2, 16)
+    with pytest.raises(G.GPT2Error) as e:
+        G.gpt2_forward(tok[:1], tok[:1], 1, 16)
+    assert e.value.code == -3
+    G.gpt2_forward(tok, None, 2, 16)
+    with pytest.raises(G.GPT2Error) as e:
+        G.gpt2_backward()
+    assert e.value.code == -2
+    with pytest.raises(G.GPT2Error):
+        G.gpt2_adamw(1e-3, 0.9, 0.999, 1e-8, 0.0, 0)
+    G.gpt2_free()
+
+
+def test_device_token_out_of_range_is_flagged():
+    import torch
+    d = inputs.TINY
+    G.gpt2_init_ex(d.L, d.C, d.NH, d.V, d.Vp, d.maxT, 1, G.GPT2_FP32, 0)
+    tok = inputs.tokens(1, 1, 2, 16, d.V)
+    bad = tok.copy()
+    bad[0, 0] = -5
+    G.gpt2_forward_device(torch.from_numpy(bad).cuda(), torch.from_numpy(tok).cuda(), 2, 16)
+    with pytest.raises(G.GPT2Error) as e:
+        G.gpt2_sync()
+    assert e.value.code == -4
+    G.gpt2_sync()  # the flag was cleared
+    G.gpt2_free()

@@ -1,0 +1,102 @@
+// internal.h -- launchers shared between the translation units of libgpt2.so.
+// Host-side declarations only; no torch types anywhere.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+// device-side error bits, read by the host after a synchronisation
+#define DEVERR_TIMEOUT 1u
+#define DEVERR_TOKEN 2u
+
+namespace gk {
+
+// element type of parameters/activations
+enum DType { DT_F32 = 0, DT_BF16 = 1 };
+
+// GEMM epilogues, applied to the fp32 accumulator acc[m][n]:
+//  EPI_STORE     D = acc (+ bias[n])
+//  EPI_GELU      D = acc + bias[n] (pre-activation), D2 = gelu(D)
+//  EPI_RESID     D = acc + bias[n] + aux[m][n]           (residual add)
+//  EPI_GELU_BWD  D = acc * gelu'(aux[m][n])                (GELU backward)
+//  EPI_ACCUM     D = D + acc                               (parameter-gradient +=)
+//  EPI_GELU_PART D = gelu(acc + bias[n]); part[m][tile] = (max, sum exp(D - max)) over the tile
+enum Epi { EPI_STORE = 0, EPI_GELU = 1, EPI_RESID = 2, EPI_GELU_BWD = 3, EPI_ACCUM = 4,
+           EPI_GELU_PART = 5 };
+
+// D[M,N] = A[M,K] . B[N,K]^T with operands given by their storage order:
+//  a_kmajor: A(m,k) = A[m*lda + k], else A(m,k) = A[k*lda + m]
+//  b_kmajor: B(n,k) = B[n*ldb + k], else B(n,k) = B[k*ldb + n]
+//  D(m,n) = D[m*ldd + n]; aux(m,n) = aux[m*ldaux + n]
+struct GemmParams {
+    const void* A; long long lda; int a_kmajor;
+    const void* B; long long ldb; int b_kmajor;
+    void* D; long long ldd;
+    const void* bias;
+    const void* aux; long long ldaux;
+    void* D2;
+    float* part; int part_ld;  // EPI_GELU_PART: float2 partials, part_ld tiles per row
+    int M, N, K;
+    int epi;
+};
+
+// SIMT (FP32 FMA) GEMM, dtype = element type of A, B, D, bias, aux.
+int gemm_simt(const GemmParams& p, DType dt, cudaStream_t s);
+
+// tcgen05 tensor-core GEMM: DT_BF16 -> kind::f16 (bf16 in, fp32 accumulate);
+// DT_F32 -> kind::tf32. err: device error word (bounded waits).
+// Returns 0, or a negative GPT2_ERR_* code for unsupported shapes/alignment.
+int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err);
+// tile width (columns) the tensor-core GEMM uses for EPI_GELU_PART
+int gemm_tc_part_tile_n();
+
+// ---- memory-bound kernels (kernels.cu) ----
+void launch_copy_tokens(const int* src, int* dst, int n, int V, unsigned int* err, cudaStream_t s);
+void launch_encoder_forward(DType dt, void* out, const int* tok, const void* wte, const void* wpe,
+                            int B, int T, int C, cudaStream_t s);
+// deterministic: dwpe[t] += sum_b dout[b,t]; dwte[tok] += sum over positions in position order
+void launch_encoder_backward(DType dt, void* dwte, void* dwpe, const void* dout, const int* tok,
+                             int B, int T, int C, int Vp, int* ws_counts, int* ws_offsets,
+                             int* ws_cursor, int* ws_order, int* ws_sorted, cudaStream_t s);
+void launch_layernorm_forward(DType dt, void* out, float* mean, float* rstd, const void* inp,
+                              const void* w, const void* b, int N, int C, cudaStream_t s);
+// dinp (+= if accumulate else =), dw += sum, db += sum (two-stage, deterministic).
+// ws: fp32 scratch of at least layernorm_backward_ws_floats(C) floats.
+void launch_layernorm_backward(DType dt, void* dinp, void* dw, void* db, const void* dout,
+                               const void* inp, const void* w, const float* mean,
+                               const float* rstd, int N, int C, int accumulate, float* ws,
+                               cudaStream_t s);
+size_t layernorm_backward_ws_floats(int C);
+// dbias[n] += sum_m dout[m][n] (two-stage, deterministic)
+void launch_colsum_accum(DType dt, void* dbias, const void* dout, int M, int N, float* ws,
+                         cudaStream_t s);
+size_t colsum_ws_floats(int N);
+// logits (BT, Vp) -> dlogits in place; losses[BT] fp32
+void launch_classifier(DType dt, void* logits, float* losses, const int* targets, int BT, int V,
+                       int Vp, float dloss, cudaStream_t s);
+void launch_mean(const float* x, int n, float* out, cudaStream_t s);
+void launch_adamw(DType dt, void* params, float* master, const void* grads, float* m, float* v,
+                  size_t n, float lr, float b1, float b2, float c1, float c2, float eps, float wd,
+                  cudaStream_t s);
+void launch_zero(void* p, size_t bytes, cudaStream_t s);
+void launch_init_normal(DType dt, void* p, size_t n, float stddev, unsigned long long seed,
+                        unsigned long long stream_id, cudaStream_t s);
+void launch_fill(DType dt, void* p, size_t n, float value, cudaStream_t s);
+void launch_to_f32(DType dt, float* dst, const void* src, size_t n, cudaStream_t s);
+void launch_from_f32(DType dt, void* dst, const float* src, size_t n, cudaStream_t s);
+// out = softmax over each row of a (M,N) fp32 tile-partial GELU output (fused operator pass 2)
+void launch_softmax_finish(float* y, const float* part, int M, int N, int tiles, cudaStream_t s);
+
+// ---- attention (attention.cu) ----
+// qkv (B,T,3C) -> out (B,T,C), lse (B,NH,T) fp32 natural-log sum of exp of the scaled scores
+void launch_attention_forward(DType dt, int tensor_cores, void* out, float* lse, const void* qkv,
+                              int B, int T, int C, int NH, cudaStream_t s);
+// dqkv (B,T,3C) written; D scratch (B,NH,T) fp32
+void launch_attention_backward(DType dt, int tensor_cores, void* dqkv, const void* dout,
+                               const void* qkv, const void* out, const float* lse, float* D,
+                               int B, int T, int C, int NH, cudaStream_t s);
+
+int num_sms();
+
+}  // namespace gk

@@ -1,0 +1,845 @@
+// kernels.cu -- memory-bound kernels of the GPT-2 training step (sm_103a).
+//
+// Each kernel streams its tensors with 16-byte vector accesses, keeps
+// reductions deterministic (fixed-order two-stage sums instead of float
+// atomics), and sizes its grid from the SM count.
+//
+// Page references are to llm.c "train_gpt2.cu" (the mixed-precision CUDA
+// training step) unless stated otherwise.
+#include "common.cuh"
+#include "internal.h"
+
+#include <math.h>
+
+namespace gk {
+
+int num_sms() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 1;
+    }
+    return n;
+}
+
+static inline unsigned int grid_for(size_t work, int block, int per_sm = 8) {
+    size_t g = (work + block - 1) / block;
+    size_t cap = (size_t)num_sms() * per_sm;
+    if (g > cap) g = cap;
+    if (g < 1) g = 1;
+    return (unsigned int)g;
+}
+
+// ------------------------------------------------------------------ tokens
+// Copies device token ids into the model's buffer; ids outside [0, V) are
+// replaced by 0 (so no later gather leaves its table) and flagged.
+__global__ void copy_tokens_k(const int* __restrict__ src, int* __restrict__ dst, int n, int V,
+                              unsigned int* err) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        int t = src[i];
+        if (t < 0 || t >= V) {
+            atomicOr(err, DEVERR_TOKEN);
+            t = 0;
+        }
+        dst[i] = t;
+    }
+}
+
+void launch_copy_tokens(const int* src, int* dst, int n, int V, unsigned int* err, cudaStream_t s) {
+    copy_tokens_k<<<grid_for(n, 256), 256, 0, s>>>(src, dst, n, V, err);
+}
+
+// ------------------------------------------------------------------ encoder
+// encoder_forward_kernel2/3: out[b,t,:] = wte[tok[b,t],:] + wpe[t,:]
+template <typename T>
+__global__ void encoder_forward_k(T* __restrict__ out, const int* __restrict__ tok,
+                                  const T* __restrict__ wte, const T* __restrict__ wpe, int BT,
+                                  int Tn, int C) {
+    constexpr int VEC = Vec16<T>::N;
+    const int cv = C / VEC;
+    const size_t nvec = (size_t)BT * cv;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec;
+         i += (size_t)gridDim.x * blockDim.x) {
+        int bt = (int)(i / cv);
+        int c = (int)(i % cv) * VEC;
+        int t = bt % Tn;
+        Vec16<T> a = ld16(wte + (size_t)tok[bt] * C + c);
+        Vec16<T> p = ld16(wpe + (size_t)t * C + c);
+        Vec16<T> o;
+#pragma unroll
+        for (int k = 0; k < VEC; k++) o.v[k] = from_f<T>(to_f(a.v[k]) + to_f(p.v[k]));
+        st16(out + (size_t)bt * C + c, o);
+    }
+}
+
+void launch_encoder_forward(DType dt, void* out, const int* tok, const void* wte, const void* wpe,
+                            int B, int T, int C, cudaStream_t s) {
+    size_t work = (size_t)B * T * C / (dt == DT_BF16 ? 8 : 4);
+    unsigned g = grid_for(work, 256);
+    if (dt == DT_BF16)
+        encoder_forward_k<bf16><<<g, 256, 0, s>>>((bf16*)out, tok, (const bf16*)wte,
+                                                  (const bf16*)wpe, B * T, T, C);
+    else
+        encoder_forward_k<float><<<g, 256, 0, s>>>((float*)out, tok, (const float*)wte,
+                                                   (const float*)wpe, B * T, T, C);
+}
+
+// encoder_backward_kernel, made deterministic.
+// dwpe[t,:] += sum over b of dout[b,t,:] (fixed b order).
+template <typename T>
+__global__ void encoder_backward_wpe_k(T* __restrict__ dwpe, const T* __restrict__ dout, int B,
+                                       int Tn, int C) {
+    constexpr int VEC = Vec16<T>::N;
+    const int cv = C / VEC;
+    const int nvec = Tn * cv;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += gridDim.x * blockDim.x) {
+        int t = i / cv, c = (i % cv) * VEC;
+        float acc[VEC];
+#pragma unroll
+        for (int k = 0; k < VEC; k++) acc[k] = 0.f;
+        for (int b = 0; b < B; b++) {
+            Vec16<T> d = ld16(dout + ((size_t)b * Tn + t) * C + c);
+#pragma unroll
+            for (int k = 0; k < VEC; k++) acc[k] += to_f(d.v[k]);
+        }
+        T* dst = dwpe + (size_t)t * C + c;
+        Vec16<T> w = ld16(dst);
+#pragma unroll
+        for (int k = 0; k < VEC; k++) w.v[k] = from_f<T>(to_f(w.v[k]) + acc[k]);
+        st16(dst, w);
+    }
+}
+
+// token histogram (integer atomics: the counts are exact whatever the order)
+__global__ void token_count_k(const int* __restrict__ tok, int n, int* counts) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+        atomicAdd(&counts[tok[i]], 1);
+}
+
+// single-block exclusive scan: offsets[v] = sum_{u<v} counts[u], offsets[Vp] = total;
+// cursor[v] = offsets[v]
+__global__ void __launch_bounds__(1024) token_scan_k(const int* __restrict__ counts, int Vp,
+                                                     int* __restrict__ offsets,
+                                                     int* __restrict__ cursor) {
+    __shared__ int warp_tot[32];
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int per = (Vp + nt - 1) / nt;
+    const int lo = min(Vp, tid * per), hi = min(Vp, lo + per);
+    int local = 0;
+    for (int v = lo; v < hi; v++) local += counts[v];
+    // inclusive scan of `local` across the block
+    int lane = tid & 31, warp = tid >> 5;
+    int x = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = (lane < nt / 32) ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        warp_tot[lane] = w;  // inclusive warp totals
+    }
+    __syncthreads();
+    int base = (warp > 0 ? warp_tot[warp - 1] : 0) + x - local;  // exclusive prefix of this thread
+    for (int v = lo; v < hi; v++) {
+        offsets[v] = base;
+        cursor[v] = base;
+        base += counts[v];
+    }
+    if (tid == nt - 1) offsets[Vp] = base;
+}
+
+__global__ void token_scatter_k(const int* __restrict__ tok, int n, int* cursor,
+                                int* __restrict__ order) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        int slot = atomicAdd(&cursor[tok[i]], 1);
+        order[slot] = i;
+    }
+}
+
+// place each position at its rank (ascending position) inside its token's bucket
+__global__ void token_rank_k(const int* __restrict__ tok, const int* __restrict__ offsets,
+                             const int* __restrict__ order, int n, int* __restrict__ sorted) {
+    for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < n; s += gridDim.x * blockDim.x) {
+        int pos = order[s];
+        int v = tok[pos];
+        int lo = offsets[v], hi = offsets[v + 1];
+        int rank = 0;
+        for (int j = lo; j < hi; j++) rank += (order[j] < pos);
+        sorted[lo + rank] = pos;
+    }
+}
+
+// one warp per vocabulary row: dwte[v,:] += sum of dout rows of its positions, ascending
+template <typename T>
+__global__ void encoder_backward_wte_k(T* __restrict__ dwte, const T* __restrict__ dout,
+                                       const int* __restrict__ offsets,
+                                       const int* __restrict__ sorted, int Vp, int C) {
+    constexpr int VEC = Vec16<T>::N;
+    constexpr int CH = 4;  // vectors per lane per pass
+    const int warps = blockDim.x / 32;
+    const int v = blockIdx.x * warps + threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    if (v >= Vp) return;
+    const int lo = offsets[v], hi = offsets[v + 1];
+    if (lo == hi) return;
+    const int cv = C / VEC;
+    for (int c0 = 0; c0 < cv; c0 += 32 * CH) {
+        float acc[CH][VEC];
+#pragma unroll
+        for (int j = 0; j < CH; j++)
+#pragma unroll
+            for (int k = 0; k < VEC; k++) acc[j][k] = 0.f;
+        for (int s = lo; s < hi; s++) {
+            const T* row = dout + (size_t)sorted[s] * C;
+#pragma unroll
+            for (int j = 0; j < CH; j++) {
+                int vi = c0 + lane + 32 * j;
+                if (vi < cv) {
+                    Vec16<T> d = ld16(row + vi * VEC);
+#pragma unroll
+                    for (int k = 0; k < VEC; k++) acc[j][k] += to_f(d.v[k]);
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < CH; j++) {
+            int vi = c0 + lane + 32 * j;
+            if (vi < cv) {
+                T* dst = dwte + (size_t)v * C + vi * VEC;
+                Vec16<T> w = ld16(dst);
+#pragma unroll
+                for (int k = 0; k < VEC; k++) w.v[k] = from_f<T>(to_f(w.v[k]) + acc[j][k]);
+                st16(dst, w);
+            }
+        }
+    }
+}
+
+void launch_zero(void* p, size_t bytes, cudaStream_t s);
+
+void launch_encoder_backward(DType dt, void* dwte, void* dwpe, const void* dout, const int* tok,
+                             int B, int T, int C, int Vp, int* ws_counts, int* ws_offsets,
+                             int* ws_cursor, int* ws_order, int* ws_sorted, cudaStream_t s) {
+    const int n = B * T;
+    const int VEC = dt == DT_BF16 ? 8 : 4;
+    unsigned g = grid_for((size_t)T * C / VEC, 256);
+    if (dt == DT_BF16)
+        encoder_backward_wpe_k<bf16><<<g, 256, 0, s>>>((bf16*)dwpe, (const bf16*)dout, B, T, C);
+    else
+        encoder_backward_wpe_k<float><<<g, 256, 0, s>>>((float*)dwpe, (const float*)dout, B, T, C);
+    launch_zero(ws_counts, sizeof(int) * (size_t)Vp, s);
+    token_count_k<<<grid_for(n, 256), 256, 0, s>>>(tok, n, ws_counts);
+    token_scan_k<<<1, 1024, 0, s>>>(ws_counts, Vp, ws_offsets, ws_cursor);
+    token_scatter_k<<<grid_for(n, 256), 256, 0, s>>>(tok, n, ws_cursor, ws_order);
+    token_rank_k<<<grid_for(n, 256), 256, 0, s>>>(tok, ws_offsets, ws_order, n, ws_sorted);
+    unsigned gw = (unsigned)((Vp + 7) / 8);
+    if (dt == DT_BF16)
+        encoder_backward_wte_k<bf16><<<gw, 256, 0, s>>>((bf16*)dwte, (const bf16*)dout, ws_offsets,
+                                                        ws_sorted, Vp, C);
+    else
+        encoder_backward_wte_k<float><<<gw, 256, 0, s>>>((float*)dwte, (const float*)dout,
+                                                         ws_offsets, ws_sorted, Vp, C);
+}
+
+// ------------------------------------------------------------------ LayerNorm
+// layernorm_forward_kernel3: one warp per row, the row held in registers;
+// mean, biased variance, rstd = 1/sqrt(var + 1e-5), y = (x - mean) rstd w + b.
+// mean/rstd are kept in fp32.
+template <typename T, int MAXV>
+__global__ void layernorm_forward_k(T* __restrict__ out, float* __restrict__ mean,
+                                    float* __restrict__ rstd, const T* __restrict__ inp,
+                                    const T* __restrict__ w, const T* __restrict__ b, int N,
+                                    int C) {
+    constexpr int VEC = Vec16<T>::N;
+    const int warps = blockDim.x / 32;
+    const int row = blockIdx.x * warps + threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    if (row >= N) return;
+    const int cv = C / VEC;
+    const T* x = inp + (size_t)row * C;
+    float xs[MAXV][VEC];
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < MAXV; j++) {
+        int vi = lane + 32 * j;
+        if (vi < cv) {
+            Vec16<T> a = ld16(x + vi * VEC);
+#pragma unroll
+            for (int k = 0; k < VEC; k++) {
+                xs[j][k] = to_f(a.v[k]);
+                s += xs[j][k];
+            }
+        }
+    }
+    const float m = warp_sum(s) / C;
+    float var = 0.f;
+#pragma unroll
+    for (int j = 0; j < MAXV; j++) {
+        int vi = lane + 32 * j;
+        if (vi < cv) {
+#pragma unroll
+            for (int k = 0; k < VEC; k++) {
+                float d = xs[j][k] - m;
+                var += d * d;
+            }
+        }
+    }
+    var = warp_sum(var) / C;
+    const float r = rsqrtf(var + 1e-5f);
+    T* y = out + (size_t)row * C;
+#pragma unroll
+    for (int j = 0; j < MAXV; j++) {
+        int vi = lane + 32 * j;
+        if (vi < cv) {
+            Vec16<T> wv = ld16(w + vi * VEC), bv = ld16(b + vi * VEC), o;
+#pragma unroll
+            for (int k = 0; k < VEC; k++)
+                o.v[k] = from_f<T>((xs[j][k] - m) * r * to_f(wv.v[k]) + to_f(bv.v[k]));
+            st16(y + vi * VEC, o);
+        }
+    }
+    if (lane == 0) {
+        mean[row] = m;
+        rstd[row] = r;
+    }
+}
+
+static int maxv_for(int cv) {
+    int per = (cv + 31) / 32;
+    return per <= 1 ? 1 : per <= 2 ? 2 : per <= 4 ? 4 : 8;
+}
+
+void launch_layernorm_forward(DType dt, void* out, float* mean, float* rstd, const void* inp,
+                              const void* w, const void* b, int N, int C, cudaStream_t s) {
+    const int VEC = dt == DT_BF16 ? 8 : 4;
+    const int mv = maxv_for(C / VEC);
+    const int block = 256, rows = block / 32;
+    unsigned g = (unsigned)((N + rows - 1) / rows);
+#define LNF(TT, MV)                                                                            \
+    layernorm_forward_k<TT, MV><<<g, block, 0, s>>>((TT*)out, mean, rstd, (const TT*)inp,        \
+                                                    (const TT*)w, (const TT*)b, N, C)
+    if (dt == DT_BF16) {
+        if (mv == 1) LNF(bf16, 1); else if (mv == 2) LNF(bf16, 2); else if (mv == 4) LNF(bf16, 4); else LNF(bf16, 8);
+    } else {
+        if (mv == 1) LNF(float, 1); else if (mv == 2) LNF(float, 2); else if (mv == 4) LNF(float, 4); else LNF(float, 8);
+    }
+#undef LNF
+}
+
+// layernorm_backward_kernel6, deterministic and with += for every output:
+//   nhat = (x - mean) rstd, g = w * dy,
+//   dx (+)= rstd (g - mean_c(g) - nhat mean_c(g nhat)),
+//   dw += sum_rows nhat dy, db += sum_rows dy.
+// Stage 1: each block walks rows with its warps, keeps per-column partial
+// sums in registers, folds its warps in a fixed order and writes one partial
+// row per block to ws. Stage 2 sums the partial rows in block order.
+constexpr int LNB_BLOCK = 256;
+
+template <typename T, int MAXV>
+__global__ void __launch_bounds__(LNB_BLOCK) layernorm_backward_k(
+    T* __restrict__ dinp, float* __restrict__ ws, const T* __restrict__ dout,
+    const T* __restrict__ inp, const T* __restrict__ w, const float* __restrict__ mean,
+    const float* __restrict__ rstd, int N, int C, int accumulate) {
+    constexpr int VEC = Vec16<T>::N;
+    extern __shared__ float sm[];  // [2][C]
+    const int warps = blockDim.x / 32;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    const int cv = C / VEC;
+    float pdw[MAXV][VEC], pdb[MAXV][VEC], wr[MAXV][VEC];
+#pragma unroll
+    for (int j = 0; j < MAXV; j++) {
+        int vi = lane + 32 * j;
+        Vec16<T> wv;
+        if (vi < cv) wv = ld16(w + vi * VEC);
+#pragma unroll
+        for (int k = 0; k < VEC; k++) {
+            pdw[j][k] = 0.f;
+            pdb[j][k] = 0.f;
+            wr[j][k] = vi < cv ? to_f(wv.v[k]) : 0.f;
+        }
+    }
+    for (int row = blockIdx.x * warps + warp; row < N; row += gridDim.x * warps) {
+        const T* x = inp + (size_t)row * C;
+        const T* dy = dout + (size_t)row * C;
+        const float mu = mean[row], rs = rstd[row];
+        float nh[MAXV][VEC], d[MAXV][VEC];
+        float gsum = 0.f, gnsum = 0.f;
+#pragma unroll
+        for (int j = 0; j < MAXV; j++) {
+            int vi = lane + 32 * j;
+            if (vi < cv) {
+                Vec16<T> xv = ld16(x + vi * VEC), dv = ld16(dy + vi * VEC);
+#pragma unroll
+                for (int k = 0; k < VEC; k++) {
+                    nh[j][k] = (to_f(xv.v[k]) - mu) * rs;
+                    d[j][k] = to_f(dv.v[k]);
+                    float g = wr[j][k] * d[j][k];
+                    gsum += g;
+                    gnsum += g * nh[j][k];
+                }
+            }
+        }
+        gsum = warp_sum(gsum) / C;
+        gnsum = warp_sum(gnsum) / C;
+        T* dx = dinp + (size_t)row * C;
+#pragma unroll
+        for (int j = 0; j < MAXV; j++) {
+            int vi = lane + 32 * j;
+            if (vi < cv) {
+                Vec16<T> o;
+                if (accumulate) o = ld16(dx + vi * VEC);
+#pragma unroll
+                for (int k = 0; k < VEC; k++) {
+                    float g = wr[j][k] * d[j][k];
+                    float val = rs * (g - gsum - nh[j][k] * gnsum);
+                    o.v[k] = from_f<T>(accumulate ? to_f(o.v[k]) + val : val);
+                    pdw[j][k] += nh[j][k] * d[j][k];
+                    pdb[j][k] += d[j][k];
+                }
+                st16(dx + vi * VEC, o);
+            }
+        }
+    }
+    // fold the warps' partials in warp order
+    for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) sm[c] = 0.f;
+    __syncthreads();
+    for (int wi = 0; wi < warps; wi++) {
+        if (warp == wi) {
+#pragma unroll
+            for (int j = 0; j < MAXV; j++) {
+                int vi = lane + 32 * j;
+                if (vi < cv) {
+#pragma unroll
+                    for (int k = 0; k < VEC; k++) {
+                        sm[vi * VEC + k] += pdw[j][k];
+                        sm[C + vi * VEC + k] += pdb[j][k];
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+    float* dst = ws + (size_t)blockIdx.x * 2 * C;
+    for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) dst[c] = sm[c];
+}
+
+template <typename T>
+__global__ void layernorm_param_reduce_k(T* __restrict__ dw, T* __restrict__ db,
+                                         const float* __restrict__ ws, int P, int C) {
+    int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= C) return;
+    float sw = 0.f, sb = 0.f;
+    for (int p = 0; p < P; p++) {
+        sw += ws[(size_t)p * 2 * C + c];
+        sb += ws[(size_t)p * 2 * C + C + c];
+    }
+    dw[c] = from_f<T>(to_f(dw[c]) + sw);
+    db[c] = from_f<T>(to_f(db[c]) + sb);
+}
+
+static int lnb_blocks(int N) {
+    int rows_per_block = LNB_BLOCK / 32;
+    int g = (N + rows_per_block - 1) / rows_per_block;
+    int cap = 2 * num_sms();
+    return g < cap ? (g < 1 ? 1 : g) : cap;
+}
+
+size_t layernorm_backward_ws_floats(int C) { return (size_t)2 * num_sms() * 2 * C; }
+
+void launch_layernorm_backward(DType dt, void* dinp, void* dw, void* db, const void* dout,
+                               const void* inp, const void* w, const float* mean,
+                               const float* rstd, int N, int C, int accumulate, float* ws,
+                               cudaStream_t s) {
+    const int VEC = dt == DT_BF16 ? 8 : 4;
+    const int mv = maxv_for(C / VEC);
+    const int P = lnb_blocks(N);
+    const size_t smem = sizeof(float) * 2 * C;
+#define LNB(TT, MV)                                                                          \
+    layernorm_backward_k<TT, MV><<<P, LNB_BLOCK, smem, s>>>((TT*)dinp, ws, (const TT*)dout,  \
+                                                            (const TT*)inp, (const TT*)w,     \
+                                                            mean, rstd, N, C, accumulate)
+    if (dt == DT_BF16) {
+        if (mv == 1) LNB(bf16, 1); else if (mv == 2) LNB(bf16, 2); else if (mv == 4) LNB(bf16, 4); else LNB(bf16, 8);
+        layernorm_param_reduce_k<bf16><<<(C + 255) / 256, 256, 0, s>>>((bf16*)dw, (bf16*)db, ws, P, C);
+    } else {
+        if (mv == 1) LNB(float, 1); else if (mv == 2) LNB(float, 2); else if (mv == 4) LNB(float, 4); else LNB(float, 8);
+        layernorm_param_reduce_k<float><<<(C + 255) / 256, 256, 0, s>>>((float*)dw, (float*)db, ws, P, C);
+    }
+#undef LNB
+}
+
+// ------------------------------------------------------------------ bias gradient
+// matmul_backward_bias_kernel4 read with +=: dbias[n] += sum over rows of dout[:, n].
+// Stage 1: block (x: 32*VEC columns, y: a slab of rows), 8 warps stride the
+// slab, warps folded in order; stage 2 sums the slabs in order.
+constexpr int CS_SLABS = 64;
+
+template <typename T>
+__global__ void __launch_bounds__(256) colsum_partial_k(float* __restrict__ ws,
+                                                        const T* __restrict__ dout, int M, int N,
+                                                        int rows_per_slab) {
+    constexpr int VEC = Vec16<T>::N;
+    __shared__ float sm[8][32 * VEC];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    const int col = (blockIdx.x * 32 + lane) * VEC;
+    const int r0 = blockIdx.y * rows_per_slab;
+    const int r1 = min(M, r0 + rows_per_slab);
+    float acc[VEC];
+#pragma unroll
+    for (int k = 0; k < VEC; k++) acc[k] = 0.f;
+    if (col < N) {
+        for (int r = r0 + warp; r < r1; r += 8) {
+            Vec16<T> d = ld16(dout + (size_t)r * N + col);
+#pragma unroll
+            for (int k = 0; k < VEC; k++) acc[k] += to_f(d.v[k]);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < VEC; k++) sm[warp][lane * VEC + k] = acc[k];
+    __syncthreads();
+    for (int c = threadIdx.x; c < 32 * VEC; c += blockDim.x) {
+        float sacc = 0.f;
+        for (int wi = 0; wi < 8; wi++) sacc += sm[wi][c];
+        int gc = blockIdx.x * 32 * VEC + c;
+        if (gc < N) ws[(size_t)blockIdx.y * N + gc] = sacc;
+    }
+}
+
+template <typename T>
+__global__ void colsum_final_k(T* __restrict__ dbias, const float* __restrict__ ws, int R, int N) {
+    int n = blockIdx.x * blockDim.x + threadIdx.x;
+    if (n >= N) return;
+    float sacc = 0.f;
+    for (int r = 0; r < R; r++) sacc += ws[(size_t)r * N + n];
+    dbias[n] = from_f<T>(to_f(dbias[n]) + sacc);
+}
+
+size_t colsum_ws_floats(int N) { return (size_t)CS_SLABS * N; }
+
+void launch_colsum_accum(DType dt, void* dbias, const void* dout, int M, int N, float* ws,
+                         cudaStream_t s) {
+    const int VEC = dt == DT_BF16 ? 8 : 4;
+    int R = (M + 7) / 8;
+    if (R > CS_SLABS) R = CS_SLABS;
+    if (R < 1) R = 1;
+    int rps = (M + R - 1) / R;
+    R = (M + rps - 1) / rps;
+    dim3 grid((N + 32 * VEC - 1) / (32 * VEC), R);
+    if (dt == DT_BF16) {
+        colsum_partial_k<bf16><<<grid, 256, 0, s>>>(ws, (const bf16*)dout, M, N, rps);
+        colsum_final_k<bf16><<<(N + 255) / 256, 256, 0, s>>>((bf16*)dbias, ws, R, N);
+    } else {
+        colsum_partial_k<float><<<grid, 256, 0, s>>>(ws, (const float*)dout, M, N, rps);
+        colsum_final_k<float><<<(N + 255) / 256, 256, 0, s>>>((float*)dbias, ws, R, N);
+    }
+}
+
+// ------------------------------------------------------------------ classifier
+// fused_classifier_kernel3: per row, softmax over the first V logits,
+// loss = log(sum exp(l - max)) + max - l[target], and the logits are replaced
+// by dlogits = (p - 1[i == target]) * dloss; the padded columns [V, Vp) get 0.
+// Pass 1 reads the row once (online max/sum per 16-byte vector); pass 2
+// re-reads it (an L2 hit: each block's row is only ~100 KB) and writes.
+constexpr int CLS_BLOCK = 512;
+
+template <typename T>
+__global__ void __launch_bounds__(CLS_BLOCK) classifier_k(T* __restrict__ logits,
+                                                          float* __restrict__ losses,
+                                                          const int* __restrict__ targets, int V,
+                                                          int Vp, float dloss) {
+    constexpr int VEC = Vec16<T>::N;
+    __shared__ float s_max[32], s_sum[32];
+    __shared__ float s_tlogit;
+    const int row = blockIdx.x;
+    T* x = logits + (size_t)row * Vp;
+    const int tgt = targets[row];
+    if (threadIdx.x == 0) s_tlogit = to_f(x[tgt]);
+    const int nvec = Vp / VEC;
+    float m = -INFINITY, sum = 0.f;
+    for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+        Vec16<T> a = ld16(x + (size_t)vi * VEC);
+        float f[VEC];
+        float lm = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < VEC; k++) {
+            f[k] = (vi * VEC + k < V) ? to_f(a.v[k]) : -INFINITY;
+            lm = fmaxf(lm, f[k]);
+        }
+        if (lm == -INFINITY) continue;
+        float nm = fmaxf(m, lm);
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < VEC; k++) acc += expf(f[k] - nm);
+        sum = sum * expf(m - nm) + acc;
+        m = nm;
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x / 32, nw = blockDim.x / 32;
+    float wm = warp_max(m);
+    if (lane == 0) s_max[warp] = wm;
+    __syncthreads();
+    float bm = warp_max(lane < nw ? s_max[lane] : -INFINITY);
+    float ws = warp_sum(m == -INFINITY ? 0.f : sum * expf(m - bm));
+    if (lane == 0) s_sum[warp] = ws;
+    __syncthreads();
+    const float bs = warp_sum(lane < nw ? s_sum[lane] : 0.f);
+    if (threadIdx.x == 0) losses[row] = logf(bs) + bm - s_tlogit;
+    const float inv = 1.f / bs;
+    for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+        Vec16<T> a = ld16(x + (size_t)vi * VEC), o;
+#pragma unroll
+        for (int k = 0; k < VEC; k++) {
+            int i = vi * VEC + k;
+            float d = 0.f;
+            if (i < V) {
+                float p = expf(to_f(a.v[k]) - bm) * inv;
+                d = (p - (i == tgt ? 1.f : 0.f)) * dloss;
+            }
+            o.v[k] = from_f<T>(d);
+        }
+        st16_cs(x + (size_t)vi * VEC, o);
+    }
+}
+
+void launch_classifier(DType dt, void* logits, float* losses, const int* targets, int BT, int V,
+                       int Vp, float dloss, cudaStream_t s) {
+    if (dt == DT_BF16)
+        classifier_k<bf16><<<BT, CLS_BLOCK, 0, s>>>((bf16*)logits, losses, targets, V, Vp, dloss);
+    else
+        classifier_k<float><<<BT, CLS_BLOCK, 0, s>>>((float*)logits, losses, targets, V, Vp, dloss);
+}
+
+// mean of n floats in a fixed order (single block)
+__global__ void __launch_bounds__(1024) mean_k(const float* __restrict__ x, int n,
+                                               float* __restrict__ out) {
+    __shared__ float sw[32];
+    float s = 0.f;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) s += x[i];
+    s = warp_sum(s);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x / 32;
+    if (lane == 0) sw[warp] = s;
+    __syncthreads();
+    if (warp == 0) {
+        float t = lane < (int)(blockDim.x / 32) ? sw[lane] : 0.f;
+        t = warp_sum(t);
+        if (lane == 0) out[0] = t / (float)n;
+    }
+}
+
+void launch_mean(const float* x, int n, float* out, cudaStream_t s) {
+    mean_k<<<1, 1024, 0, s>>>(x, n, out);
+}
+
+// ------------------------------------------------------------------ AdamW
+// adamw_kernel3 (master-weight path) / train_gpt2_fp32.cu adamw_kernel2:
+// m = b1 m + (1-b1) g, v = b2 v + (1-b2) g^2, theta -= lr (mhat/(sqrt(vhat)+eps) + wd theta).
+template <typename T>
+DEVI float adamw_one(float g, float& m, float& v, float theta, float lr, float b1, float b2,
+                     float c1, float c2, float eps, float wd) {
+    m = fmaf(b1, m - g, g);          // b1 m + (1 - b1) g
+    v = fmaf(b2, v - g * g, g * g);  // b2 v + (1 - b2) g^2
+    float mh = m / c1, vh = v / c2;
+    return theta - lr * (mh / (sqrtf(vh) + eps) + wd * theta);
+}
+
+template <typename T>
+__global__ void adamw_k(T* __restrict__ params, float* __restrict__ master,
+                        const T* __restrict__ grads, float* __restrict__ mst,
+                        float* __restrict__ vst, size_t n, float lr, float b1, float b2, float c1,
+                        float c2, float eps, float wd) {
+    const size_t stride = (size_t)gridDim.x * blockDim.x * 4;
+    for (size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4; i < n; i += stride) {
+        if (i + 4 <= n) {
+            float4 m4 = __ldcs(reinterpret_cast<const float4*>(mst + i));
+            float4 v4 = __ldcs(reinterpret_cast<const float4*>(vst + i));
+            float g[4], th[4];
+            if constexpr (sizeof(T) == 2) {
+                uint2 graw = __ldcs(reinterpret_cast<const uint2*>(grads + i));
+                const bf16* gb = reinterpret_cast<const bf16*>(&graw);
+#pragma unroll
+                for (int k = 0; k < 4; k++) g[k] = to_f(gb[k]);
+            } else {
+                float4 g4 = __ldcs(reinterpret_cast<const float4*>(grads + i));
+                g[0] = g4.x; g[1] = g4.y; g[2] = g4.z; g[3] = g4.w;
+            }
+            if (master) {
+                float4 t4 = __ldcs(reinterpret_cast<const float4*>(master + i));
+                th[0] = t4.x; th[1] = t4.y; th[2] = t4.z; th[3] = t4.w;
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; k++) th[k] = to_f(params[i + k]);
+            }
+            float mm[4] = {m4.x, m4.y, m4.z, m4.w}, vv[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+            for (int k = 0; k < 4; k++)
+                th[k] = adamw_one<T>(g[k], mm[k], vv[k], th[k], lr, b1, b2, c1, c2, eps, wd);
+            __stcs(reinterpret_cast<float4*>(mst + i), make_float4(mm[0], mm[1], mm[2], mm[3]));
+            __stcs(reinterpret_cast<float4*>(vst + i), make_float4(vv[0], vv[1], vv[2], vv[3]));
+            if (master)
+                __stcs(reinterpret_cast<float4*>(master + i), make_float4(th[0], th[1], th[2], th[3]));
+            if constexpr (sizeof(T) == 2) {
+                uint2 praw;
+                bf16* pb = reinterpret_cast<bf16*>(&praw);
+#pragma unroll
+                for (int k = 0; k < 4; k++) pb[k] = from_f<bf16>(th[k]);
+                __stcs(reinterpret_cast<uint2*>(params + i), praw);
+            } else {
+                __stcs(reinterpret_cast<float4*>(params + i), make_float4(th[0], th[1], th[2], th[3]));
+            }
+        } else {
+            for (size_t j = i; j < n; j++) {
+                float mm = mst[j], vv = vst[j];
+                float th = master ? master[j] : to_f(params[j]);
+                th = adamw_one<T>(to_f(grads[j]), mm, vv, th, lr, b1, b2, c1, c2, eps, wd);
+                mst[j] = mm;
+                vst[j] = vv;
+                if (master) master[j] = th;
+                params[j] = from_f<T>(th);
+            }
+        }
+    }
+}
+
+void launch_adamw(DType dt, void* params, float* master, const void* grads, float* m, float* v,
+                  size_t n, float lr, float b1, float b2, float c1, float c2, float eps, float wd,
+                  cudaStream_t s) {
+    unsigned g = grid_for((n + 3) / 4, 256, 8);
+    if (dt == DT_BF16)
+        adamw_k<bf16><<<g, 256, 0, s>>>((bf16*)params, master, (const bf16*)grads, m, v, n, lr, b1,
+                                        b2, c1, c2, eps, wd);
+    else
+        adamw_k<float><<<g, 256, 0, s>>>((float*)params, master, (const float*)grads, m, v, n, lr,
+                                         b1, b2, c1, c2, eps, wd);
+}
+
+// ------------------------------------------------------------------ utilities
+__global__ void zero_k(int4* __restrict__ p, size_t n16, char* __restrict__ tail, size_t ntail) {
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i < n16; i += (size_t)gridDim.x * blockDim.x) p[i] = make_int4(0, 0, 0, 0);
+    if (blockIdx.x == 0 && threadIdx.x < ntail) tail[threadIdx.x] = 0;
+}
+
+void launch_zero(void* p, size_t bytes, cudaStream_t s) {
+    if (bytes == 0) return;
+    // p is at least 256-byte aligned (every buffer comes from cudaMalloc offsets of 256)
+    size_t n16 = bytes / 16, ntail = bytes % 16;
+    zero_k<<<grid_for(n16 ? n16 : 1, 256, 8), 256, 0, s>>>((int4*)p, n16, (char*)p + n16 * 16, ntail);
+}
+
+// counter-based normal generator for the initial weights: SplitMix64 output
+// function over (seed, stream, index), Box-Muller on two 32-bit halves.
+DEVI unsigned long long splitmix64(unsigned long long z) {
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+template <typename T>
+__global__ void init_normal_k(T* __restrict__ p, size_t n, float stddev, unsigned long long seed,
+                              unsigned long long stream_id) {
+    const unsigned long long base = seed * 0x9E3779B97F4A7C15ull + (stream_id << 40);
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x) {
+        unsigned long long z = splitmix64(base + i);
+        float u1 = ((float)(unsigned)(z >> 40) + 0.5f) * (1.0f / 16777216.0f);
+        float u2 = ((float)(unsigned)((z >> 8) & 0xFFFFFFu) + 0.5f) * (1.0f / 16777216.0f);
+        float r = sqrtf(-2.0f * logf(u1));
+        p[i] = from_f<T>(stddev * r * cospif(2.0f * u2));
+    }
+}
+
+template <typename T>
+__global__ void fill_k(T* __restrict__ p, size_t n, float value) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x)
+        p[i] = from_f<T>(value);
+}
+
+void launch_init_normal(DType dt, void* p, size_t n, float stddev, unsigned long long seed,
+                        unsigned long long stream_id, cudaStream_t s) {
+    unsigned g = grid_for(n, 256, 16);
+    if (dt == DT_BF16) init_normal_k<bf16><<<g, 256, 0, s>>>((bf16*)p, n, stddev, seed, stream_id);
+    else init_normal_k<float><<<g, 256, 0, s>>>((float*)p, n, stddev, seed, stream_id);
+}
+
+void launch_fill(DType dt, void* p, size_t n, float value, cudaStream_t s) {
+    unsigned g = grid_for(n, 256, 16);
+    if (dt == DT_BF16) fill_k<bf16><<<g, 256, 0, s>>>((bf16*)p, n, value);
+    else fill_k<float><<<g, 256, 0, s>>>((float*)p, n, value);
+}
+
+template <typename T>
+__global__ void to_f32_k(float* __restrict__ dst, const T* __restrict__ src, size_t n) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x)
+        dst[i] = to_f(src[i]);
+}
+template <typename T>
+__global__ void from_f32_k(T* __restrict__ dst, const float* __restrict__ src, size_t n) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x)
+        dst[i] = from_f<T>(src[i]);
+}
+
+void launch_to_f32(DType dt, float* dst, const void* src, size_t n, cudaStream_t s) {
+    unsigned g = grid_for(n, 256, 16);
+    if (dt == DT_BF16) to_f32_k<bf16><<<g, 256, 0, s>>>(dst, (const bf16*)src, n);
+    else to_f32_k<float><<<g, 256, 0, s>>>(dst, (const float*)src, n);
+}
+void launch_from_f32(DType dt, void* dst, const float* src, size_t n, cudaStream_t s) {
+    unsigned g = grid_for(n, 256, 16);
+    if (dt == DT_BF16) from_f32_k<bf16><<<g, 256, 0, s>>>((bf16*)dst, src, n);
+    else from_f32_k<float><<<g, 256, 0, s>>>((float*)dst, src, n);
+}
+
+// ------------------------------------------------------------------ fused operator, pass 2
+// Each row of y holds gelu(x W^T + b); part[row][t] = (max, sum exp(y - max)) of
+// column tile t. Combine the tile partials, then y <- exp(y - max) / sum in place.
+__global__ void __launch_bounds__(256) softmax_finish_k(float* __restrict__ y,
+                                                        const float2* __restrict__ part, int N,
+                                                        int tiles) {
+    __shared__ float s_m, s_inv;
+    const int row = blockIdx.x;
+    if (threadIdx.x < 32) {
+        float m = -INFINITY;
+        for (int t = threadIdx.x; t < tiles; t += 32) m = fmaxf(m, part[(size_t)row * tiles + t].x);
+        m = warp_max(m);
+        float s = 0.f;
+        for (int t = threadIdx.x; t < tiles; t += 32) {
+            float2 p = part[(size_t)row * tiles + t];
+            s += p.y * expf(p.x - m);
+        }
+        s = warp_sum(s);
+        if (threadIdx.x == 0) {
+            s_m = m;
+            s_inv = 1.f / s;
+        }
+    }
+    __syncthreads();
+    const float m = s_m, inv = s_inv;
+    float* yr = y + (size_t)row * N;
+    const int nv = N / 4;
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+        float4 v = reinterpret_cast<float4*>(yr)[i];
+        v.x = expf(v.x - m) * inv;
+        v.y = expf(v.y - m) * inv;
+        v.z = expf(v.z - m) * inv;
+        v.w = expf(v.w - m) * inv;
+        __stcs(reinterpret_cast<float4*>(yr) + i, v);
+    }
+}
+
+void launch_softmax_finish(float* y, const float* part, int M, int N, int tiles, cudaStream_t s) {
+    softmax_finish_k<<<M, 256, 0, s>>>(y, (const float2*)part, N, tiles);
+}
+
+}  // namespace gk

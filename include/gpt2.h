@@ -110,6 +110,7 @@ int gpt2_param_sizes(size_t out[16]);
 int gpt2_get_params(float* host);       /* current parameters (bf16 widened to fp32) */
 int gpt2_set_params(const float* host); /* also resets the fp32 master copy and AdamW moments */
 int gpt2_get_grads(float* host);
+int gpt2_set_grads(const float* host);  /* overwrite the gradients (e.g. to drive gpt2_adamw alone) */
 int gpt2_get_master(float* host);       /* fp32 master weights (GPT2_BF16 only) */
 int gpt2_get_losses(float* host);       /* per-position losses of the last forward, B*T */
 
@@ -136,6 +137,10 @@ int gpt2_free(void);
 /* Text of the last error (static storage, never NULL). */
 const char* gpt2_last_error(void);
 
+/* Code (GPT2_ERR_*) of the last error; lets callers of gpt2_forward, which
+ * signals failure with NaN, tell the causes apart. */
+int gpt2_last_status(void);
+
 /* ---- kernel timing (CUDA events around each launch, for roofline reporting) ----
  * family: 0 GEMM, 1 attention forward, 2 attention backward, 3 LayerNorm forward,
  * 4 LayerNorm backward, 5 classifier softmax-CE, 6 AdamW, 7 encoder, 8 other.
@@ -146,6 +151,10 @@ const char* gpt2_last_error(void);
 int gpt2_timing_begin(int max_launches);
 int gpt2_timing_end(void);
 int gpt2_timing_get(int family, double* total_ms, long long* launches, double* work);
+
+/* Number of CUDA kernels this library has launched in this process (all entry
+ * points, counted on the host at launch). */
+long long gpt2_launch_count(void);
 
 /* ---- standalone fused operator ----
  * out = softmax_row( gelu_tanh( x . W^T + b ) ) (POPCORNBENCH "fused Linear +

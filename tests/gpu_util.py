@@ -29,10 +29,12 @@ def max_rel_floor(got, ref, floor):
     return float(np.max(np.abs(got - ref) / np.maximum(np.abs(ref), floor))) if ref.size else 0.0
 
 
-def rel_to_max(got, ref):
+def rel_to_max(got, ref, floor=1e-6):
+    """max |got - ref| / max(max|ref|, floor): an all-zero reference (e.g. the
+    exact dQ of a one-position sequence) is compared in absolute terms."""
     got = np.asarray(got, dtype=np.float64).reshape(-1)
     ref = np.asarray(ref, dtype=np.float64).reshape(-1)
-    return float(np.max(np.abs(got - ref)) / max(np.max(np.abs(ref)), 1e-30))
+    return float(np.max(np.abs(got - ref)) / max(np.max(np.abs(ref)), floor))
 
 
 def cosine(a, b):

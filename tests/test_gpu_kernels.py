@@ -45,6 +45,16 @@ def _ref(epi, A, B, bias, aux, D0):
 MODES = [("bf16", 1), ("bf16", 0), ("f32", 0)]
 
 
+def _stored(X, kmajor):
+    """Storage of logical X[rows, K]: K-major = X itself, MN-major = X^T; the
+    leading dimension is padded to a multiple of 8 elements (16 bytes)."""
+    S = X if kmajor else X.T
+    ld = (S.shape[1] + 7) // 8 * 8
+    P = np.zeros((S.shape[0], ld), dtype=np.float32)
+    P[:, :S.shape[1]] = S
+    return P, ld
+
+
 @pytest.mark.parametrize("mode", MODES, ids=lambda m: f"{m[0]}-tc{m[1]}")
 @pytest.mark.parametrize("a_km,b_km", [(1, 1), (1, 0), (0, 0), (0, 1)])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
@@ -54,11 +64,11 @@ def test_gemm_layouts_match_oracle(mode, a_km, b_km, shape):
     bf16 = dt == "bf16"
     A, B, bias, aux, D0 = _operands(M, N, K, 7 + M + N + K, bf16)
     ref, _ = _ref("store", A, B, bias, aux, D0)
-    dA = dev(A if a_km else A.T, dt)
-    dB = dev(B if b_km else B.T, dt)
+    sA, lda = _stored(A, a_km)
+    sB, ldb = _stored(B, b_km)
     D = empty((M, N), dt)
-    G.gpt2_gemm(G.GPT2_BF16 if bf16 else G.GPT2_FP32, tc, "store", dA, K if a_km else M, a_km, dB,
-                K if b_km else N, b_km, D, N, bias=dev(bias, dt), M=M, N=N, K=K)
+    G.gpt2_gemm(G.GPT2_BF16 if bf16 else G.GPT2_FP32, tc, "store", dev(sA, dt), lda, a_km,
+                dev(sB, dt), ldb, b_km, D, N, bias=dev(bias, dt), M=M, N=N, K=K)
     G.gpt2_device_status()
     err = rel_to_max(host(D), ref)
     assert err < (8e-3 if bf16 else 1e-5), err

@@ -579,6 +579,7 @@ static void simt_backward(void* dqkv, const void* dout, const void* qkv, const f
 
 void launch_attention_forward(DType dt, int tensor_cores, void* out, float* lse, const void* qkv,
                               int B, int T, int C, int NH, cudaStream_t s) {
+    note_launch(1);
     const int HS = C / NH;
     if (dt == DT_BF16 && tensor_cores && HS == 64) {
         dim3 grid((T + fa::BLK - 1) / fa::BLK, B * NH);
@@ -593,6 +594,7 @@ void launch_attention_forward(DType dt, int tensor_cores, void* out, float* lse,
 void launch_attention_backward(DType dt, int tensor_cores, void* dqkv, const void* dout,
                                const void* qkv, const void* out, const float* lse, float* D,
                                int B, int T, int C, int NH, cudaStream_t s) {
+    note_launch(3);
     const int HS = C / NH;
     const int n = B * NH * T;
     if (dt == DT_BF16)

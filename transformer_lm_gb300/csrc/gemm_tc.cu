@@ -506,6 +506,7 @@ static int launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const tc::Arg
             return GPT2_ERR_CUDA;
         attr_done = true;
     }
+    note_launch(1);
     tc::gemm_tc_k<BN, KIND, EPI><<<grid, tc::NUM_THREADS, C::SMEM_BYTES, s>>>(ta, tb, a);
     return GPT2_OK;
 }

@@ -22,8 +22,10 @@ using namespace gk;
 namespace {
 
 char g_err[512] = "no error";
+int g_status = GPT2_OK;
 
 int fail(int code, const char* fmt, ...) {
+    g_status = code;
     va_list ap;
     va_start(ap, fmt);
     vsnprintf(g_err, sizeof(g_err), fmt, ap);
@@ -426,6 +428,10 @@ extern "C" {
 
 const char* gpt2_last_error(void) { return g_err; }
 
+int gpt2_last_status(void) { return g_status; }
+
+long long gpt2_launch_count(void) { return launch_count(); }
+
 int gpt2_init_ex(int L, int C, int NH, int V, int Vp, int maxT, unsigned long long seed,
                  int precision, int tensor_cores) {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -650,6 +656,22 @@ int gpt2_set_params(const float* host) {
     }
     cudaFree(tmp);
     if (e != cudaSuccess) return fail(GPT2_ERR_CUDA, "set_params: %s", cudaGetErrorString(e));
+    return GPT2_OK;
+}
+
+int gpt2_set_grads(const float* host) {
+    TRY(check_model());
+    if (!host) return fail(GPT2_ERR_ARG, "host is NULL");
+    Model* m = g;
+    float* tmp = nullptr;
+    CUDA_TRY(cudaMalloc(&tmp, m->nparams * 4 + 16));
+    cudaError_t e = cudaMemcpyAsync(tmp, host, m->nparams * 4, cudaMemcpyHostToDevice, m->stream);
+    if (e == cudaSuccess) {
+        launch_from_f32(m->dt, m->grads, tmp, m->nparams, m->stream);
+        e = cudaStreamSynchronize(m->stream);
+    }
+    cudaFree(tmp);
+    if (e != cudaSuccess) return fail(GPT2_ERR_CUDA, "set_grads: %s", cudaGetErrorString(e));
     return GPT2_OK;
 }
 

@@ -11,6 +11,8 @@
 
 #include <math.h>
 
+#include <atomic>
+
 namespace gk {
 
 int num_sms() {
@@ -23,6 +25,10 @@ int num_sms() {
     }
     return n;
 }
+
+static std::atomic<long long> g_launches{0};
+void note_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+long long launch_count() { return g_launches.load(std::memory_order_relaxed); }
 
 static inline unsigned int grid_for(size_t work, int block, int per_sm = 8) {
     size_t g = (work + block - 1) / block;
@@ -48,6 +54,7 @@ __global__ void copy_tokens_k(const int* __restrict__ src, int* __restrict__ dst
 }
 
 void launch_copy_tokens(const int* src, int* dst, int n, int V, unsigned int* err, cudaStream_t s) {
+    note_launch(1);
     copy_tokens_k<<<grid_for(n, 256), 256, 0, s>>>(src, dst, n, V, err);
 }
 
@@ -76,6 +83,7 @@ __global__ void encoder_forward_k(T* __restrict__ out, const int* __restrict__ t
 
 void launch_encoder_forward(DType dt, void* out, const int* tok, const void* wte, const void* wpe,
                             int B, int T, int C, cudaStream_t s) {
+    note_launch(1);
     size_t work = (size_t)B * T * C / (dt == DT_BF16 ? 8 : 4);
     unsigned g = grid_for(work, 256);
     if (dt == DT_BF16)
@@ -230,6 +238,7 @@ void launch_zero(void* p, size_t bytes, cudaStream_t s);
 void launch_encoder_backward(DType dt, void* dwte, void* dwpe, const void* dout, const int* tok,
                              int B, int T, int C, int Vp, int* ws_counts, int* ws_offsets,
                              int* ws_cursor, int* ws_order, int* ws_sorted, cudaStream_t s) {
+    note_launch(6);
     const int n = B * T;
     const int VEC = dt == DT_BF16 ? 8 : 4;
     unsigned g = grid_for((size_t)T * C / VEC, 256);
@@ -321,6 +330,7 @@ static int maxv_for(int cv) {
 
 void launch_layernorm_forward(DType dt, void* out, float* mean, float* rstd, const void* inp,
                               const void* w, const void* b, int N, int C, cudaStream_t s) {
+    note_launch(1);
     const int VEC = dt == DT_BF16 ? 8 : 4;
     const int mv = maxv_for(C / VEC);
     const int block = 256, rows = block / 32;
@@ -460,6 +470,7 @@ void launch_layernorm_backward(DType dt, void* dinp, void* dw, void* db, const v
                                const void* inp, const void* w, const float* mean,
                                const float* rstd, int N, int C, int accumulate, float* ws,
                                cudaStream_t s) {
+    note_launch(2);
     const int VEC = dt == DT_BF16 ? 8 : 4;
     const int mv = maxv_for(C / VEC);
     const int P = lnb_blocks(N);
@@ -528,6 +539,7 @@ size_t colsum_ws_floats(int N) { return (size_t)CS_SLABS * N; }
 
 void launch_colsum_accum(DType dt, void* dbias, const void* dout, int M, int N, float* ws,
                          cudaStream_t s) {
+    note_launch(2);
     const int VEC = dt == DT_BF16 ? 8 : 4;
     int R = (M + 7) / 8;
     if (R > CS_SLABS) R = CS_SLABS;
@@ -612,6 +624,7 @@ __global__ void __launch_bounds__(CLS_BLOCK) classifier_k(T* __restrict__ logits
 
 void launch_classifier(DType dt, void* logits, float* losses, const int* targets, int BT, int V,
                        int Vp, float dloss, cudaStream_t s) {
+    note_launch(1);
     if (dt == DT_BF16)
         classifier_k<bf16><<<BT, CLS_BLOCK, 0, s>>>((bf16*)logits, losses, targets, V, Vp, dloss);
     else
@@ -636,6 +649,7 @@ __global__ void __launch_bounds__(1024) mean_k(const float* __restrict__ x, int 
 }
 
 void launch_mean(const float* x, int n, float* out, cudaStream_t s) {
+    note_launch(1);
     mean_k<<<1, 1024, 0, s>>>(x, n, out);
 }
 
@@ -712,6 +726,7 @@ __global__ void adamw_k(T* __restrict__ params, float* __restrict__ master,
 void launch_adamw(DType dt, void* params, float* master, const void* grads, float* m, float* v,
                   size_t n, float lr, float b1, float b2, float c1, float c2, float eps, float wd,
                   cudaStream_t s) {
+    note_launch(1);
     unsigned g = grid_for((n + 3) / 4, 256, 8);
     if (dt == DT_BF16)
         adamw_k<bf16><<<g, 256, 0, s>>>((bf16*)params, master, (const bf16*)grads, m, v, n, lr, b1,
@@ -730,6 +745,7 @@ __global__ void zero_k(int4* __restrict__ p, size_t n16, char* __restrict__ tail
 
 void launch_zero(void* p, size_t bytes, cudaStream_t s) {
     if (bytes == 0) return;
+    note_launch(1);
     // p is at least 256-byte aligned (every buffer comes from cudaMalloc offsets of 256)
     size_t n16 = bytes / 16, ntail = bytes % 16;
     zero_k<<<grid_for(n16 ? n16 : 1, 256, 8), 256, 0, s>>>((int4*)p, n16, (char*)p + n16 * 16, ntail);
@@ -766,12 +782,14 @@ __global__ void fill_k(T* __restrict__ p, size_t n, float value) {
 
 void launch_init_normal(DType dt, void* p, size_t n, float stddev, unsigned long long seed,
                         unsigned long long stream_id, cudaStream_t s) {
+    note_launch(1);
     unsigned g = grid_for(n, 256, 16);
     if (dt == DT_BF16) init_normal_k<bf16><<<g, 256, 0, s>>>((bf16*)p, n, stddev, seed, stream_id);
     else init_normal_k<float><<<g, 256, 0, s>>>((float*)p, n, stddev, seed, stream_id);
 }
 
 void launch_fill(DType dt, void* p, size_t n, float value, cudaStream_t s) {
+    note_launch(1);
     unsigned g = grid_for(n, 256, 16);
     if (dt == DT_BF16) fill_k<bf16><<<g, 256, 0, s>>>((bf16*)p, n, value);
     else fill_k<float><<<g, 256, 0, s>>>((float*)p, n, value);
@@ -791,11 +809,13 @@ __global__ void from_f32_k(T* __restrict__ dst, const float* __restrict__ src, s
 }
 
 void launch_to_f32(DType dt, float* dst, const void* src, size_t n, cudaStream_t s) {
+    note_launch(1);
     unsigned g = grid_for(n, 256, 16);
     if (dt == DT_BF16) to_f32_k<bf16><<<g, 256, 0, s>>>(dst, (const bf16*)src, n);
     else to_f32_k<float><<<g, 256, 0, s>>>(dst, (const float*)src, n);
 }
 void launch_from_f32(DType dt, void* dst, const float* src, size_t n, cudaStream_t s) {
+    note_launch(1);
     unsigned g = grid_for(n, 256, 16);
     if (dt == DT_BF16) from_f32_k<bf16><<<g, 256, 0, s>>>((bf16*)dst, src, n);
     else from_f32_k<float><<<g, 256, 0, s>>>((float*)dst, src, n);
@@ -839,6 +859,7 @@ __global__ void __launch_bounds__(256) softmax_finish_k(float* __restrict__ y,
 }
 
 void launch_softmax_finish(float* y, const float* part, int M, int N, int tiles, cudaStream_t s) {
+    note_launch(1);
     softmax_finish_k<<<M, 256, 0, s>>>(y, (const float2*)part, N, tiles);
 }
 

@@ -62,11 +62,13 @@ _SIGS = {
     "gpt2_get_params": (_i, [_fp]),
     "gpt2_set_params": (_i, [_fp]),
     "gpt2_get_grads": (_i, [_fp]),
+    "gpt2_set_grads": (_i, [_fp]),
     "gpt2_get_master": (_i, [_fp]),
     "gpt2_get_losses": (_i, [_fp]),
     "gpt2_get_activation": (_i, [_i, _i, _fp, ctypes.POINTER(_sz)]),
     "gpt2_free": (_i, []),
     "gpt2_last_error": (ctypes.c_char_p, []),
+    "gpt2_last_status": (_i, []),
     "gpt2_timing_begin": (_i, [_i]),
     "gpt2_timing_end": (_i, []),
     "gpt2_timing_get": (_i, [_i, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_ll),
@@ -77,6 +79,7 @@ _SIGS = {
     "gpt2_attention_forward": (_i, [_i, _i, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "gpt2_attention_backward": (_i, [_i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "gpt2_device_status": (_i, []),
+    "gpt2_launch_count": (_ll, []),
 }
 
 
@@ -139,7 +142,7 @@ def gpt2_forward(tokens, targets, B, T) -> float:
     tgt = None if targets is None else _ints(targets)
     loss = lib().gpt2_forward(_as_ip(tok), _as_ip(tgt), B, T)
     if np.isnan(loss):
-        raise GPT2Error("gpt2_forward", -1, gpt2_last_error())
+        raise GPT2Error("gpt2_forward", int(lib().gpt2_last_status()), gpt2_last_error())
     return float(loss)
 
 
@@ -199,6 +202,13 @@ def gpt2_get_grads() -> np.ndarray:
     out = _host_f32(gpt2_num_params())
     _check("gpt2_get_grads", lib().gpt2_get_grads(out.ctypes.data_as(_fp)))
     return out
+
+
+def gpt2_set_grads(grads) -> None:
+    a = np.ascontiguousarray(grads, dtype=np.float32).reshape(-1)
+    if a.size != gpt2_num_params():
+        raise ValueError(f"expected {gpt2_num_params()} gradients, got {a.size}")
+    _check("gpt2_set_grads", lib().gpt2_set_grads(a.ctypes.data_as(_fp)))
 
 
 def gpt2_get_master() -> np.ndarray:
@@ -269,6 +279,10 @@ def gpt2_attention_backward(dtype, tensor_cores, dout, qkv, out, lse, dqkv, scra
     _check("gpt2_attention_backward",
            lib().gpt2_attention_backward(dtype, tensor_cores, ptr(dout), ptr(qkv), ptr(out),
                                          ptr(lse), ptr(dqkv), ptr(scratch_D), B, T, C, NH, stream))
+
+
+def gpt2_launch_count() -> int:
+    return int(lib().gpt2_launch_count())
 
 
 def gpt2_device_status() -> None:

@@ -169,6 +169,25 @@ long long gpt2_launch_count(void);
 int fused_linear_bias_gelu_softmax(const float* x, const float* W, const float* b, float* out,
                                    int M, int K, int N, void* stream);
 
+/* Allocation-free variant of fused_linear_bias_gelu_softmax (no counterpart in
+ * the paper: it exists for callers that cannot let a library allocate device
+ * memory -- processes whose own pool allocator owns all device memory, where a
+ * cudaMalloc behind its back can fail or fragment the pool, and loops that
+ * cannot take the device-wide synchronisation a cudaMalloc may imply).
+ * Same arguments, result and errors as fused_linear_bias_gelu_softmax; it calls
+ * no cudaMalloc/cudaFree or other allocating routine. Its per-row softmax
+ * partials live in a static device array of 1 MiB that every GPU loading the
+ * library holds until exit, which limits M * ceil(N/256) to 131072 (e.g.
+ * M = 1024 rows with N up to 32768); larger sizes return GPT2_ERR_ARG with a
+ * message in gpt2_last_error(). Every call shares that array and leaves its
+ * contents behind (nothing needs clearing: each call writes every partial it
+ * reads); calls whose GPU work overlaps race on it. The first call on a device
+ * (with that device current) looks up the array's device address; make that
+ * first call before any stream capture. An expired in-kernel wait is reported
+ * by gpt2_device_status(). */
+int fused_linear_bias_gelu_softmax_noalloc(const float* x, const float* W, const float* b,
+                                           float* out, int M, int K, int N, void* stream);
+
 /* ---- kernel-level entry points (DEVICE pointers, asynchronous on `stream`) ----
  * gpt2_gemm: D[M,N] = A[M,K] . B[N,K]^T with the step's fused epilogues.
  *  dtype GPT2_FP32 / GPT2_BF16 is the element type of A, B, D, bias, aux, D2;

@@ -423,6 +423,15 @@ int to_host_f32(Model* m, float* host, const void* src, size_t n, DType dt) {
 
 }  // namespace
 
+int gk::set_error(int code, const char* fmt, ...) {
+    g_status = code;
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
 // =================================================================== C ABI
 extern "C" {
 

@@ -98,6 +98,8 @@ void launch_attention_backward(DType dt, int tensor_cores, void* dqkv, const voi
                                int B, int T, int C, int NH, cudaStream_t s);
 
 int num_sms();
+// records the library's last error (text and GPT2_ERR_* code); returns code
+int set_error(int code, const char* fmt, ...);
 // host-side count of kernel launches made by this library (for benchmark reporting)
 void note_launch(int n);
 long long launch_count();

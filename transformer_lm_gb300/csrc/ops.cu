@@ -47,6 +47,8 @@ bool al16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 }  // namespace
 
+static int noalloc_err_of(int dev, unsigned int* bits);
+
 extern "C" {
 
 int fused_linear_bias_gelu_softmax(const float* x, const float* W, const float* b, float* out,
@@ -142,16 +144,133 @@ int gpt2_attention_backward(int dtype, int tensor_cores, const void* dout, const
 int gpt2_device_status(void) {
     int dev;
     if (current_device(&dev) != GPT2_OK) return GPT2_ERR_CUDA;
-    unsigned int* err = err_word(dev);
-    if (!err) return GPT2_ERR_NOMEM;
-    unsigned int h = 0;
     if (cudaDeviceSynchronize() != cudaSuccess) return GPT2_ERR_CUDA;
-    if (cudaMemcpy(&h, err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return GPT2_ERR_CUDA;
-    if (h) {
-        cudaMemset(err, 0, 4);
-        if (h & DEVERR_TIMEOUT) return GPT2_ERR_DEVICE_TIMEOUT;
+    unsigned int h = 0;
+    // the allocation-free variant's word (only once it has been set up here)
+    if (noalloc_err_of(dev, &h) != GPT2_OK) return GPT2_ERR_CUDA;
+    // the shared word of the allocating entry points; none exists until one of
+    // them ran on this device, and then nothing can have been recorded
+    unsigned int* err = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(ops_mu);
+        err = dev_err[dev];
+    }
+    if (err) {
+        unsigned int h2 = 0;
+        if (cudaMemcpy(&h2, err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return GPT2_ERR_CUDA;
+        if (h2) cudaMemset(err, 0, 4);
+        h |= h2;
+    }
+    if (h & DEVERR_TIMEOUT) return GPT2_ERR_DEVICE_TIMEOUT;
+    return GPT2_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of fused_linear_bias_gelu_softmax.
+//
+// Some callers cannot let a library call cudaMalloc: processes that hand all
+// device memory to their own pool allocator up front (a cudaMalloc behind the
+// pool's back can fail or fragment that memory), and loops that cannot take
+// the device-wide synchronisation cudaMalloc may imply. For them the per-row
+// softmax partials live in the file-scope device array below, reserved when
+// the library is loaded and held by every device that loads it until exit.
+//
+// Limits and sharing: at most NOALLOC_MAX_PARTIALS (row, 256-column tile)
+// pairs, i.e. M * ceil(N / 256) <= 131072 (1 MiB of float2). Every call uses
+// the same array and leaves the previous call's partials in it; nothing needs
+// clearing because the GEMM epilogue writes every partial a call reads.
+// Calls whose GPU work overlaps (different streams, no ordering between them)
+// race on the array and give wrong results.
+// Set-up: the first call on a device, with that device current, looks up the
+// array's device address (cudaGetSymbolAddress); that first call should come
+// before any stream capture.
+// ---------------------------------------------------------------------------
+
+}  // extern "C"
+
+#define NOALLOC_MAX_PARTIALS (1 << 17)
+
+static __device__ __align__(256) float2 g_noalloc_part[NOALLOC_MAX_PARTIALS];
+// bounded-wait timeout bits of the allocation-free variant (starts at zero)
+static __device__ __align__(256) unsigned int g_noalloc_err[64];
+
+namespace {
+struct NoAllocDevice {
+    bool ready = false;
+    float* part = nullptr;
+    unsigned int* err = nullptr;
+};
+NoAllocDevice noalloc_dev[kMaxDevices];
+}  // namespace
+
+// Host code cannot use the arrays' names as device addresses: look the
+// addresses up once per device (with that device current) and pass them on.
+static int noalloc_setup(int dev, NoAllocDevice* out) {
+    std::lock_guard<std::mutex> lk(ops_mu);
+    if (!noalloc_dev[dev].ready) {
+        void* part = nullptr;
+        void* err = nullptr;
+        if (cudaGetSymbolAddress(&part, g_noalloc_part) != cudaSuccess) return GPT2_ERR_CUDA;
+        if (cudaGetSymbolAddress(&err, g_noalloc_err) != cudaSuccess) return GPT2_ERR_CUDA;
+        noalloc_dev[dev].part = (float*)part;
+        noalloc_dev[dev].err = (unsigned int*)err;
+        noalloc_dev[dev].ready = true;
+    }
+    *out = noalloc_dev[dev];
+    return GPT2_OK;
+}
+
+// reads (and clears) the variant's timeout bits; 0 if it was never set up on dev
+static int noalloc_err_of(int dev, unsigned int* bits) {
+    *bits = 0;
+    bool ready;
+    {
+        std::lock_guard<std::mutex> lk(ops_mu);
+        ready = noalloc_dev[dev].ready;
+    }
+    if (!ready) return GPT2_OK;
+    if (cudaMemcpyFromSymbol(bits, g_noalloc_err, sizeof(unsigned int)) != cudaSuccess)
+        return GPT2_ERR_CUDA;
+    if (*bits) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_noalloc_err, &zero, sizeof(unsigned int)) != cudaSuccess)
+            return GPT2_ERR_CUDA;
     }
     return GPT2_OK;
 }
 
-}  // extern "C"
+extern "C" int fused_linear_bias_gelu_softmax_noalloc(const float* x, const float* W,
+                                                      const float* b, float* out, int M, int K,
+                                                      int N, void* stream) {
+    if (!x || !W || !b || !out) return gk::set_error(GPT2_ERR_ARG, "fused op (no-alloc): NULL pointer");
+    if (M < 1 || K < 1 || N < 1)
+        return gk::set_error(GPT2_ERR_ARG, "fused op (no-alloc): M, K, N must be >= 1");
+    if (!al16(x) || !al16(W) || !al16(b) || !al16(out) || K % 4 || N % 4)
+        return gk::set_error(GPT2_ERR_ALIGN,
+                             "fused op (no-alloc): pointers must be 16-byte aligned, K and N multiples of 4");
+    const int tile_n = gemm_tc_part_tile_n();
+    const long long tiles = (N + tile_n - 1) / tile_n;
+    if ((long long)M * tiles > NOALLOC_MAX_PARTIALS)
+        return gk::set_error(GPT2_ERR_ARG,
+                             "fused op (no-alloc): M * ceil(N/256) = %lld exceeds the static scratch "
+                             "limit of %d",
+                             (long long)M * tiles, NOALLOC_MAX_PARTIALS);
+    int dev;
+    if (current_device(&dev) != GPT2_OK) return gk::set_error(GPT2_ERR_CUDA, "no current device");
+    NoAllocDevice d;
+    if (noalloc_setup(dev, &d) != GPT2_OK)
+        return gk::set_error(GPT2_ERR_CUDA, "fused op (no-alloc): cudaGetSymbolAddress failed");
+    cudaStream_t s = (cudaStream_t)stream;
+    GemmParams p = {};
+    p.A = x; p.lda = K; p.a_kmajor = 1;
+    p.B = W; p.ldb = K; p.b_kmajor = 1;
+    p.D = out; p.ldd = N; p.bias = b;
+    p.part = d.part; p.part_ld = (int)tiles;
+    p.M = M; p.N = N; p.K = K; p.epi = EPI_GELU_PART;
+    int rc = gemm_tc(p, DT_F32, s, d.err);
+    if (rc != GPT2_OK) return gk::set_error(rc, "fused op (no-alloc): GEMM launch rejected");
+    launch_softmax_finish(out, d.part, M, N, (int)tiles, s);
+    if (cudaGetLastError() != cudaSuccess)
+        return gk::set_error(GPT2_ERR_CUDA, "fused op (no-alloc): launch failed");
+    return GPT2_OK;
+}

@@ -74,6 +74,7 @@ _SIGS = {
     "gpt2_timing_get": (_i, [_i, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_ll),
                              ctypes.POINTER(ctypes.c_double)]),
     "fused_linear_bias_gelu_softmax": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]),
+    "fused_linear_bias_gelu_softmax_noalloc": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]),
     "gpt2_gemm": (_i, [_i, _i, _i, _vp, _ll, _i, _vp, _ll, _i, _vp, _ll, _vp, _vp, _ll, _vp, _i, _i,
                        _i, _vp]),
     "gpt2_attention_forward": (_i, [_i, _i, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
@@ -258,6 +259,12 @@ def gpt2_timing_get(family: int | str):
 def fused_linear_bias_gelu_softmax(x, W, b, out, M, K, N, stream=None) -> None:
     _check("fused_linear_bias_gelu_softmax",
            lib().fused_linear_bias_gelu_softmax(ptr(x), ptr(W), ptr(b), ptr(out), M, K, N, stream))
+
+
+def fused_linear_bias_gelu_softmax_noalloc(x, W, b, out, M, K, N, stream=None) -> None:
+    _check("fused_linear_bias_gelu_softmax_noalloc",
+           lib().fused_linear_bias_gelu_softmax_noalloc(ptr(x), ptr(W), ptr(b), ptr(out), M, K, N,
+                                                        stream))
 
 
 def gpt2_gemm(dtype, tensor_cores, epilogue, A, lda, a_kmajor, B, ldb, b_kmajor, D, ldd, bias=None,

@@ -12,7 +12,9 @@ from tests.gpu_util import dev, host, empty, rel_to_max, max_rel_floor
 
 pytestmark = pytest.mark.gpu
 
-SHAPES = [(200, 136, 72), (256, 512, 128), (130, 264, 1000), (1024, 768, 768), (64, 8, 16)]
+# several tiles, ragged tails, and m-block counts that select 1, 2 and 4 CTAs per cluster
+SHAPES = [(200, 136, 72), (256, 512, 128), (130, 264, 1000), (1024, 768, 768), (64, 8, 16),
+          (512, 520, 136), (2048, 1032, 264)]
 
 
 def _operands(M, N, K, seed, bf16):
@@ -76,10 +78,12 @@ def test_gemm_layouts_match_oracle(mode, a_km, b_km, shape):
 
 @pytest.mark.parametrize("mode", MODES, ids=lambda m: f"{m[0]}-tc{m[1]}")
 @pytest.mark.parametrize("epi", ["gelu", "resid", "gelu_bwd", "accum"])
-def test_gemm_epilogues_match_oracle(mode, epi):
+@pytest.mark.parametrize("shape", [(300, 392, 200), (1024, 392, 200), (2048, 264, 520)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_gemm_epilogues_match_oracle(mode, epi, shape):
     dt, tc = mode
     bf16 = dt == "bf16"
-    M, N, K = 300, 392, 200
+    M, N, K = shape
     A, B, bias, aux, D0 = _operands(M, N, K, 99, bf16)
     ref, ref2 = _ref(epi, A, B, bias, aux, D0)
     D = dev(D0, dt) if epi == "accum" else empty((M, N), dt)

@@ -365,12 +365,14 @@ __global__ void __launch_bounds__(128) flash_fwd_k(bf16* __restrict__ out, float
     }
 }
 
-// dQ for one query block: loops over key blocks kb <= qb
+// dQ for one query block: loops over key blocks kb <= qb. Also computes
+// D_i = sum_d dO_i,d O_i,d for its rows and stores it for the dK/dV kernel.
 __global__ void __launch_bounds__(128) flash_bwd_dq_k(bf16* __restrict__ dqkv,
                                                       const bf16* __restrict__ dout,
                                                       const bf16* __restrict__ qkv,
+                                                      const bf16* __restrict__ outp,
                                                       const float* __restrict__ lse,
-                                                      const float* __restrict__ Dg, int Tn, int C,
+                                                      float* __restrict__ Dg, int Tn, int C,
                                                       int NH, float scale, float scale_log2) {
     __shared__ __align__(128) bf16 sQ[BLK * HSZ];
     __shared__ __align__(128) bf16 sdO[BLK * HSZ];
@@ -390,12 +392,31 @@ __global__ void __launch_bounds__(128) flash_bwd_dq_k(bf16* __restrict__ dqkv,
     load_tile(sV[0], Vg, 0, Tn, pitch);
     cp_commit();
     const size_t row_base = ((size_t)b * NH + h) * Tn;
+    // D for the block's 64 rows: two threads per row, 32 elements each; warp w
+    // computes exactly its own 16 rows, so the values are exchanged by shuffles
+    float dacc = 0.f;
+    {
+        const int r = threadIdx.x >> 1, half = threadIdx.x & 1;
+        const int q = qb * BLK + r;
+        if (q < Tn) {
+            const bf16* o = outp + ((size_t)b * Tn + q) * C + (size_t)h * HSZ + half * 32;
+            const bf16* g = dout + ((size_t)b * Tn + q) * C + (size_t)h * HSZ + half * 32;
+#pragma unroll
+            for (int v = 0; v < 4; v++) {
+                Vec16<bf16> ov = ld16(o + 8 * v), gv = ld16(g + 8 * v);
+#pragma unroll
+                for (int k = 0; k < 8; k++) dacc += to_f(ov.v[k]) * to_f(gv.v[k]);
+            }
+        }
+        dacc += __shfl_xor_sync(0xffffffffu, dacc, 1);
+        if (half == 0 && q < Tn) Dg[row_base + q] = dacc;
+    }
     float lse2[2], Dr[2];
 #pragma unroll
     for (int r = 0; r < 2; r++) {
         const int q = qb * BLK + warp * 16 + (lane >> 2) + 8 * r;
         lse2[r] = q < Tn ? lse[row_base + q] * LOG2E_F : 0.f;
-        Dr[r] = q < Tn ? Dg[row_base + q] : 0.f;
+        Dr[r] = __shfl_sync(0xffffffffu, dacc, 2 * ((lane >> 2) + 8 * r));
     }
     uint32_t qf[4][4], df[4][4];
     float dq[8][4];
@@ -594,24 +615,27 @@ void launch_attention_forward(DType dt, int tensor_cores, void* out, float* lse,
 void launch_attention_backward(DType dt, int tensor_cores, void* dqkv, const void* dout,
                                const void* qkv, const void* out, const float* lse, float* D,
                                int B, int T, int C, int NH, cudaStream_t s) {
-    note_launch(3);
+    
     const int HS = C / NH;
     const int n = B * NH * T;
+    if (dt == DT_BF16 && tensor_cores && HS == 64) {
+        note_launch(2);
+        dim3 grid((T + fa::BLK - 1) / fa::BLK, B * NH);
+        const float scale = 1.f / sqrtf((float)HS), scale_log2 = LOG2E_F * scale;
+        fa::flash_bwd_dq_k<<<grid, 128, 0, s>>>((bf16*)dqkv, (const bf16*)dout, (const bf16*)qkv,
+                                                (const bf16*)out, lse, D, T, C, NH, scale,
+                                                scale_log2);
+        fa::flash_bwd_dkv_k<<<grid, 128, 0, s>>>((bf16*)dqkv, (const bf16*)dout, (const bf16*)qkv,
+                                                 lse, D, T, C, NH, scale, scale_log2);
+        return;
+    }
+    note_launch(3);
     if (dt == DT_BF16)
         attn_rowdot_k<bf16><<<(n + 255) / 256, 256, 0, s>>>(D, (const bf16*)dout, (const bf16*)out,
                                                             B, T, C, NH, HS);
     else
         attn_rowdot_k<float><<<(n + 255) / 256, 256, 0, s>>>(D, (const float*)dout,
                                                              (const float*)out, B, T, C, NH, HS);
-    if (dt == DT_BF16 && tensor_cores && HS == 64) {
-        dim3 grid((T + fa::BLK - 1) / fa::BLK, B * NH);
-        const float scale = 1.f / sqrtf((float)HS), scale_log2 = LOG2E_F * scale;
-        fa::flash_bwd_dq_k<<<grid, 128, 0, s>>>((bf16*)dqkv, (const bf16*)dout, (const bf16*)qkv,
-                                                lse, D, T, C, NH, scale, scale_log2);
-        fa::flash_bwd_dkv_k<<<grid, 128, 0, s>>>((bf16*)dqkv, (const bf16*)dout, (const bf16*)qkv,
-                                                 lse, D, T, C, NH, scale, scale_log2);
-        return;
-    }
     if (dt == DT_BF16) simt_backward<bf16>(dqkv, dout, qkv, lse, D, B, T, C, NH, s);
     else simt_backward<float>(dqkv, dout, qkv, lse, D, B, T, C, NH, s);
 }

@@ -11,9 +11,15 @@
 //   warp 1      allocates TMEM; one elected thread issues tcgen05.mma
 //               (M=128, N=BN, fp32 accumulators in TMEM) and commits each
 //               stage back to the producer;
-//   warps 2..5  epilogue: tcgen05.ld the accumulator (each warp owns its
-//               32-lane TMEM quarter = 32 rows, one row per thread), apply
-//               bias / GELU / residual / GELU-backward / += and store.
+//   warps 2..9  epilogue: tcgen05.ld the accumulator (each warp reads 32 rows
+//               of its TMEM lane quarter, one row per thread, and half of the
+//               columns of every sub-tile), apply
+//               bias / GELU / residual / GELU-backward / += in 128-byte-wide
+//               column sub-tiles staged in 128B-swizzled shared memory: the
+//               residual / GELU input / += operand arrives by TMA load
+//               (prefetched one sub-tile ahead) and results leave by TMA
+//               store, so no thread touches global memory row by row and the
+//               ragged tails are clipped by the tensor maps.
 // Two TMEM accumulators let the epilogue of tile i overlap the MMAs of tile
 // i+1. Every mbarrier wait is bounded in time; on expiry the CTA records
 // DEVERR_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and exits.
@@ -25,6 +31,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <stdlib.h>
+
 #include <mutex>
 #include <type_traits>
 
@@ -33,22 +41,33 @@ namespace tc {
 
 constexpr int BM = 128;
 constexpr int ROWB = 128;  // bytes of K held per shared-memory row (one swizzle span)
-constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARPS = 8;  // two per TMEM lane quarter, each owning half of a sub-tile's columns
+constexpr int EPI_THREADS = 32 * EPI_WARPS;
+constexpr int NUM_THREADS = 64 + EPI_THREADS;
+constexpr int GROUP_M = 16;  // m-blocks per rasterisation group (L2 locality of A and B)
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
 
-template <int BN> struct Cfg {
+constexpr int EPI_BUFS = 2;               // epilogue staging buffers
+constexpr int EPI_BUF_BYTES = BM * ROWB;  // 128 rows x 128 bytes
+
+// CG = CTAs per MMA: 1 (tcgen05 cta_group::1, 128 x BN tiles) or 2 (a CTA
+// pair runs cta_group::2 MMAs on 256 x BN tiles; each CTA holds 128 rows of A
+// and BN/2 rows of B in its shared memory and its 128 accumulator rows in TMEM)
+template <int BN, int CG> struct Cfg {
     static constexpr int A_BYTES = BM * ROWB;
-    static constexpr int B_BYTES = BN * ROWB;
+    static constexpr int B_BYTES = (BN / CG) * ROWB;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int STAGES = (192 * 1024) / STAGE_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+    static constexpr int BAR_BYTES = 256 + 1024;  // barriers, flags, per-row softmax partials
+    static constexpr int SMEM_BYTES =
+        STAGES * STAGE_BYTES + EPI_BUFS * EPI_BUF_BYTES + BAR_BYTES + 1024;
 };
 
 struct Args {
     int M, N, K;
     int num_m, num_n, num_kb;
+    int cg;  // CTAs per MMA (1 or 2)
     int a_mn, b_mn;
     void* D;
     long long ldd;
@@ -61,6 +80,7 @@ struct Args {
     unsigned int* err;
 };
 
+// ------------------------------------------------------------------ PTX wrappers
 // ------------------------------------------------------------------ PTX wrappers
 DEVI uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -123,43 +143,105 @@ DEVI void tma_load_2d(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int x, 
         : "memory");
 }
 
-DEVI void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
-                 "r"(ncols)
+// cta_group::2 form: the bytes land in this CTA's shared memory while the
+// completion is signalled on `bar`, which may be the pair leader's barrier
+// (a shared::cluster address)
+DEVI void tma_load_2d_pair(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+DEVI uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+DEVI void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+// address of the same shared variable in CTA `rank` of the cluster
+DEVI uint32_t mapa_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+DEVI void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
 }
-DEVI void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+
+// tcgen05 allocation, with the .cta_group every tcgen05 instruction of the
+// kernel shares (for 2, one warp of each CTA of the pair issues it)
+template <int CG> DEVI void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+    if constexpr (CG == 1)
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
+                     "r"(ncols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
+                     "r"(ncols)
+                     : "memory");
 }
-DEVI void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
+template <int CG> DEVI void tmem_relinquish() {
+    if constexpr (CG == 1)
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    else
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+template <int CG> DEVI void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    if constexpr (CG == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                     : "memory");
 }
 DEVI void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 DEVI void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-DEVI void umma_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
+// arrive on `bar` once all MMAs issued so far by this thread have completed;
+// for a pair, on the barrier at that offset in both CTAs
+template <int CG> DEVI void umma_commit(uint32_t bar) {
+    if constexpr (CG == 1)
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+            : "memory");
+    else
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+            " [%0], %1;" ::"r"(bar),
+            "h"((uint16_t)3)
+            : "memory");
+}
+// local-only completion (drain on abort)
+template <int CG> DEVI void umma_commit_local(uint32_t bar) {
+    if constexpr (CG == 1)
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+            : "memory");
+    else
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+            : "memory");
 }
 
 // KIND 0: kind::f16 with bf16 operands; KIND 1: kind::tf32
-template <int KIND>
+#define UMMA_ASM(GROUP, KINDS)                                                            \
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"                        \
+                 "tcgen05.mma.cta_group::" GROUP ".kind::" KINDS " [%0], %1, %2, %3, p;\n\t}\n" ::"r"( \
+                     d_tmem),                                                             \
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)                             \
+                 : "memory")
+template <int KIND, int CG>
 DEVI void umma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
-    if constexpr (KIND == 0) {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
-            : "memory");
-    } else {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
-            : "memory");
-    }
+    if constexpr (KIND == 0 && CG == 1) UMMA_ASM("1", "f16");
+    else if constexpr (KIND == 0) UMMA_ASM("2", "f16");
+    else if constexpr (CG == 1) UMMA_ASM("1", "tf32");
+    else UMMA_ASM("2", "tf32");
 }
+#undef UMMA_ASM
 
 // 32 lanes x 32 consecutive fp32 columns; the wait is inside the same asm
 // statement so no use of the registers can be scheduled before it.
@@ -176,6 +258,30 @@ DEVI void tmem_ld32(uint32_t taddr, float (&r)[32]) {
           "=r"(u[26]), "=r"(u[27]), "=r"(u[28]), "=r"(u[29]), "=r"(u[30]), "=r"(u[31])
         : "r"(taddr)
         : "memory");
+}
+
+DEVI void tmem_ld16(uint32_t taddr, float (&r)[16]) {
+    uint32_t* u = reinterpret_cast<uint32_t*>(r);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]),
+          "=r"(u[7]), "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]),
+          "=r"(u[14]), "=r"(u[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// tile order: groups of GROUP_M consecutive m-blocks (m-block pairs for
+// cta_group::2) sweep all n-blocks before the next group starts
+DEVI void tile_coords(int st, int num_mg, int num_n, int group, int& mg, int& nb) {
+    const int per_group = group * num_n;
+    const int g = st / per_group, idx = st - g * per_group;
+    const int first = g * group;
+    const int gm = min(group, num_mg - first);
+    mg = first + idx % gm;
+    nb = idx / gm;
 }
 
 // Shared-memory matrix descriptor (tcgen05): start address, leading and
@@ -209,104 +315,135 @@ DEVI uint32_t idesc(int a_mn, int b_mn, int M, int N) {
     return d;
 }
 
+
+DEVI void tma_store_2d(const CUtensorMap* tm, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+DEVI void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N> DEVI void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+DEVI void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+DEVI void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// barrier 1 among the epilogue threads
+DEVI void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(EPI_THREADS) : "memory"); }
+
 // ------------------------------------------------------------------ epilogue
+// One 128-byte-wide column sub-tile (SUBN columns) of one row: the thread's
+// accumulator values v[], its row `rl` inside the tile, and the staging
+// buffers (128 rows x 128 bytes, 16-byte chunk k of row r at chunk k ^ (r & 7)).
+// buf0 holds the TMA-loaded operand (residual, GELU input or the current D)
+// and receives the result; buf1 receives the second output of EPI_GELU.
 template <typename T, int EPI>
-DEVI void epilogue_chunk(const Args& a, int row, int n0, const float (&v)[32], float& pmax,
-                         float& psum) {
+DEVI void epilogue_subtile(const Args& a, const float* v, uint8_t* buf0, uint8_t* buf1, int rl,
+                           int row, int n0s, int kbeg, float& pmax, float& psum) {
     constexpr int VEC = Vec16<T>::N;
-    T* D = (T*)a.D + (size_t)row * a.ldd;
     const T* bias = (const T*)a.bias;
 #pragma unroll
-    for (int j = 0; j < 32; j += VEC) {
-        const int n = n0 + j;
-        if (n >= a.N) break;
+    for (int kk = 0; kk < 4; kk++) {
+        const int k = kbeg + kk;  // 16-byte chunk of the 128-byte row
+        const int off = rl * ROWB + ((k ^ (rl & 7)) << 4);
+        const int n = n0s + k * VEC;
+        const bool colok = n < a.N;
         float x[VEC];
 #pragma unroll
-        for (int k = 0; k < VEC; k++) x[k] = v[j + k];
+        for (int e = 0; e < VEC; e++) x[e] = v[kk * VEC + e];
         if constexpr (EPI == EPI_STORE || EPI == EPI_GELU || EPI == EPI_RESID ||
                       EPI == EPI_GELU_PART) {
-            if (bias) {
-                Vec16<T> b = ld16(bias + n);
+            if (bias && colok) {
+                Vec16<T> bb = ld16(bias + n);
 #pragma unroll
-                for (int k = 0; k < VEC; k++) x[k] += to_f(b.v[k]);
+                for (int e = 0; e < VEC; e++) x[e] += to_f(bb.v[e]);
             }
         }
         Vec16<T> o;
         if constexpr (EPI == EPI_STORE) {
 #pragma unroll
-            for (int k = 0; k < VEC; k++) o.v[k] = from_f<T>(x[k]);
-            st16(D + n, o);
+            for (int e = 0; e < VEC; e++) o.v[e] = from_f<T>(x[e]);
         } else if constexpr (EPI == EPI_GELU) {
             Vec16<T> g;
 #pragma unroll
-            for (int k = 0; k < VEC; k++) {
-                o.v[k] = from_f<T>(x[k]);
-                g.v[k] = from_f<T>(gelu_fwd(to_f(o.v[k])));
+            for (int e = 0; e < VEC; e++) {
+                o.v[e] = from_f<T>(x[e]);
+                g.v[e] = from_f<T>(sizeof(T) == 2 ? gelu_fwd_fast(to_f(o.v[e])) : gelu_fwd(to_f(o.v[e])));
             }
-            st16(D + n, o);
-            st16((T*)a.D2 + (size_t)row * a.ldd + n, g);
-        } else if constexpr (EPI == EPI_RESID) {
-            Vec16<T> r = ld16((const T*)a.aux + (size_t)row * a.ldaux + n);
+            *reinterpret_cast<int4*>(buf1 + off) = *reinterpret_cast<const int4*>(&g);
+        } else if constexpr (EPI == EPI_RESID || EPI == EPI_GELU_BWD || EPI == EPI_ACCUM) {
+            Vec16<T> r;
+            *reinterpret_cast<int4*>(&r) = *reinterpret_cast<const int4*>(buf0 + off);
 #pragma unroll
-            for (int k = 0; k < VEC; k++) o.v[k] = from_f<T>(x[k] + to_f(r.v[k]));
-            st16(D + n, o);
-        } else if constexpr (EPI == EPI_GELU_BWD) {
-            Vec16<T> r = ld16((const T*)a.aux + (size_t)row * a.ldaux + n);
-#pragma unroll
-            for (int k = 0; k < VEC; k++) o.v[k] = from_f<T>(x[k] * gelu_grad(to_f(r.v[k])));
-            st16(D + n, o);
-        } else if constexpr (EPI == EPI_ACCUM) {
-            Vec16<T> r = ld16(D + n);
-#pragma unroll
-            for (int k = 0; k < VEC; k++) o.v[k] = from_f<T>(to_f(r.v[k]) + x[k]);
-            st16(D + n, o);
+            for (int e = 0; e < VEC; e++) {
+                const float rv = to_f(r.v[e]);
+                if constexpr (EPI == EPI_RESID) o.v[e] = from_f<T>(x[e] + rv);
+                else if constexpr (EPI == EPI_GELU_BWD)
+                    o.v[e] = from_f<T>(x[e] * (sizeof(T) == 2 ? gelu_grad_fast(rv) : gelu_grad(rv)));
+                else o.v[e] = from_f<T>(rv + x[e]);
+            }
         } else if constexpr (EPI == EPI_GELU_PART) {
             float cm = pmax;
 #pragma unroll
-            for (int k = 0; k < VEC; k++) {
-                x[k] = gelu_fwd(x[k]);
-                cm = fmaxf(cm, x[k]);
+            for (int e = 0; e < VEC; e++) {
+                x[e] = gelu_fwd(x[e]);
+                cm = fmaxf(cm, x[e]);
             }
-            float s = 0.f;
 #pragma unroll
-            for (int k = 0; k < VEC; k++) {
-                o.v[k] = from_f<T>(x[k]);
-                s += expf(x[k] - cm);
+            for (int e = 0; e < VEC; e++) o.v[e] = from_f<T>(x[e]);
+            if (colok && row < a.M) {
+                float s = 0.f;
+#pragma unroll
+                for (int e = 0; e < VEC; e++) s += expf(x[e] - cm);
+                psum = psum * expf(pmax - cm) + s;
+                pmax = cm;
             }
-            psum = psum * expf(pmax - cm) + s;
-            pmax = cm;
-            st16(D + n, o);
         }
+        *reinterpret_cast<int4*>(buf0 + off) = *reinterpret_cast<const int4*>(&o);
     }
 }
 
 // ------------------------------------------------------------------ kernel
-template <int BN, int KIND, int EPI>
+template <int BN, int KIND, int EPI, int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_k(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-              const __grid_constant__ Args args) {
-    using C = Cfg<BN>;
+              const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
+              const __grid_constant__ CUtensorMap tmX, const __grid_constant__ Args args) {
+    using C = Cfg<BN, CG>;
     using T = typename std::conditional<KIND == 0, bf16, float>::type;
     constexpr int KE = ROWB / (int)sizeof(T);  // K elements per stage
     constexpr int UK = KIND == 0 ? 16 : 8;     // K elements per MMA
     constexpr int KSTEPS = KE / UK;            // MMAs per stage (4)
+    constexpr int SUBN = ROWB / (int)sizeof(T);  // epilogue sub-tile width (columns)
+    constexpr int NSUB = BN / SUBN;
+    constexpr int BNC = BN / CG;               // rows of B this CTA holds
+    constexpr bool HAS_AUX = EPI == EPI_RESID || EPI == EPI_GELU_BWD || EPI == EPI_ACCUM;
+    constexpr int OUTS = EPI == EPI_GELU ? 2 : 1;  // staging buffers per sub-tile
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - raw);
-    const uint32_t bars = base + C::STAGES * C::STAGE_BYTES;
-    uint8_t* bars_ptr = base_ptr + C::STAGES * C::STAGE_BYTES;
+    const uint32_t ebuf = base + C::STAGES * C::STAGE_BYTES;
+    uint8_t* ebuf_ptr = base_ptr + C::STAGES * C::STAGE_BYTES;
+    const uint32_t bars = ebuf + EPI_BUFS * EPI_BUF_BYTES;
+    uint8_t* bars_ptr = ebuf_ptr + EPI_BUFS * EPI_BUF_BYTES;
     auto full = [&](int s) { return bars + 8u * s; };
     auto empty = [&](int s) { return bars + 8u * (C::STAGES + s); };
     auto tfull = [&](int a) { return bars + 8u * (2 * C::STAGES + a); };
     auto tempty = [&](int a) { return bars + 8u * (2 * C::STAGES + 2 + a); };
     const uint32_t drain = bars + 8u * (2 * C::STAGES + 4);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars_ptr + 8 * (2 * C::STAGES + 5));
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars_ptr + 8 * (2 * C::STAGES + 5) + 4);
-    int* n_issued_smem = reinterpret_cast<int*>(bars_ptr + 8 * (2 * C::STAGES + 6));
+    auto auxfull = [&](int b) { return bars + 8u * (2 * C::STAGES + 5 + b); };
+    constexpr int NBARS = 2 * C::STAGES + 5 + EPI_BUFS;
+    static_assert(8 * NBARS + 16 <= 256, "barrier area");
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars_ptr + 8 * NBARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars_ptr + 8 * NBARS + 4);
+    int* n_issued_smem = reinterpret_cast<int*>(bars_ptr + 8 * NBARS + 8);
+    volatile int* epi_abort = reinterpret_cast<volatile int*>(bars_ptr + 8 * NBARS + 12);
+    float2* row_part = reinterpret_cast<float2*>(bars_ptr + 256);  // [BM] softmax partials
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    const int rank = CG == 2 ? (int)(cluster_rank() & 1u) : 0;  // 0: pair leader (issues MMAs)
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; s++) {
             mbar_init(full(s), 1);
@@ -314,51 +451,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int a = 0; a < 2; a++) {
             mbar_init(tfull(a), 1);
-            mbar_init(tempty(a), 128);
+            mbar_init(tempty(a), CG);  // one arrival from each CTA's epilogue
         }
         mbar_init(drain, 1);
+        for (int b = 0; b < EPI_BUFS; b++) mbar_init(auxfull(b), 1);
         *abort_flag = 0;
         *n_issued_smem = 0;
+        *epi_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc<CG>(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish<CG>();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if constexpr (CG == 2) cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
     const uint32_t tmem_base = *tmem_slot;
-    const int num_tiles = args.num_m * args.num_n;
+    // a pair of CTAs takes an m-block pair (rows m0 .. m0+255) of one n-block
+    const int num_mg = (args.num_m + CG - 1) / CG;
+    const int num_super = num_mg * args.num_n;
+    const int group = GROUP_M / CG;
+    const int cid = (int)blockIdx.x / CG, ncl = (int)gridDim.x / CG;
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------- TMA producer
+            // ---------------- TMA producer (both CTAs of a pair)
             int stage = 0, n_issued = 0;
             uint32_t phase = 0;
-            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-                const int m0 = (tile % args.num_m) * BM, n0 = (tile / args.num_m) * BN;
+            for (int st = cid; st < num_super; st += ncl) {
+                int mg, nbk;
+                tile_coords(st, num_mg, args.num_n, group, mg, nbk);
+                const int m0 = (mg * CG + rank) * BM, n0 = nbk * BN;
                 bool ok = true;
                 for (int kb = 0; kb < args.num_kb; kb++) {
                     if (!mbar_wait(empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
                     const uint32_t sa = base + stage * C::STAGE_BYTES;
                     const uint32_t sb = sa + C::A_BYTES;
-                    mbar_expect_tx(full(stage), C::STAGE_BYTES);
                     const int k0 = kb * KE;
+                    uint32_t bar = full(stage);
+                    if constexpr (CG == 2) bar = mapa_rank(bar, 0);  // completions go to the leader
+                    if (rank == 0) mbar_expect_tx(full(stage), CG * C::STAGE_BYTES);
+                    auto load = [&](uint32_t dst, const CUtensorMap* tm, int x, int y) {
+                        if constexpr (CG == 1) tma_load_2d(dst, tm, bar, x, y);
+                        else tma_load_2d_pair(dst, tm, bar, x, y);
+                    };
                     if (!args.a_mn) {
-                        tma_load_2d(sa, &tmA, full(stage), k0, m0);
+                        load(sa, &tmA, k0, m0);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < BM / KE; j++)
-                            tma_load_2d(sa + j * KE * ROWB, &tmA, full(stage), m0 + j * KE, k0);
+                        for (int j = 0; j < BM / KE; j++) load(sa + j * KE * ROWB, &tmA, m0 + j * KE, k0);
                     }
+                    // this CTA's BN/CG rows of B
                     if (!args.b_mn) {
-                        tma_load_2d(sb, &tmB, full(stage), k0, n0);
+                        load(sb, &tmB, k0, n0 + rank * BNC);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < BN / KE; j++)
-                            tma_load_2d(sb + j * KE * ROWB, &tmB, full(stage), n0 + j * KE, k0);
+                        for (int j = 0; j < BNC / KE; j++)
+                            load(sb + j * KE * ROWB, &tmB, n0 + rank * BNC + j * KE, k0);
                     }
                     ++n_issued;
                     if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
@@ -368,12 +520,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             *n_issued_smem = n_issued;
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer
-            const uint32_t id = idesc<KIND>(args.a_mn, args.b_mn, BM, BN);
+        if (lane == 0 && rank == 0) {
+            // ---------------- MMA issuer (the pair leader)
+            const uint32_t id = idesc<KIND>(args.a_mn, args.b_mn, BM * CG, BN);
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
-            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            for (int st = cid; st < num_super; st += ncl) {
                 if (!mbar_wait(tempty(acc), acc_phase ^ 1u, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(acc * BN);
@@ -391,71 +543,162 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint64_t db = args.b_mn
                                                 ? sdesc(sb + k * UK * ROWB, KE * ROWB, 1024)
                                                 : sdesc(sb + k * UK * (int)sizeof(T), 16, 1024);
-                        umma<KIND>(d, da, db, id, (kb | k) ? 1u : 0u);
+                        umma<KIND, CG>(d, da, db, id, (kb | k) ? 1u : 0u);
                     }
-                    umma_commit(empty(stage));
+                    umma_commit<CG>(empty(stage));  // frees the stage in every CTA of the pair
                     if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                umma_commit(tfull(acc));
+                umma_commit<CG>(tfull(acc));
                 if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             }
         }
     } else {
-        // ---------------- epilogue warps 2..5
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        // ---------------- epilogue warps 2..9
+        // Every epilogue thread runs every iteration (the named barriers stay
+        // matched); after an expired wait the work is skipped, not the loop.
+        const int q = warp & 3;         // TMEM lane quarter this warp may access
+        const int hh = (warp - 2) >> 2;  // which half of each sub-tile's columns
+        const int rl = q * 32 + lane;
+        const bool elected = warp == 2 && lane == 0;
+        constexpr int HALF = SUBN / 2;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            const int mb = tile % args.num_m, nb = tile / args.num_m;
-            const int m0 = mb * BM, n0 = nb * BN;
+        int u = 0;  // sub-tile counter: staging buffer rotation and aux barrier phases
+        bool aborted = false;
+        int last_aux_u[EPI_BUFS];  // latest aux load per buffer (elected thread)
+        for (int b = 0; b < EPI_BUFS; b++) last_aux_u[b] = -1;
+        if constexpr (HAS_AUX) {
+            if (elected && cid < num_super) {
+                int mg, nbk;
+                tile_coords(cid, num_mg, args.num_n, group, mg, nbk);
+                mbar_expect_tx(auxfull(0), EPI_BUF_BYTES);
+                tma_load_2d(ebuf, &tmX, auxfull(0), nbk * BN, (mg * CG + rank) * BM);
+                last_aux_u[0] = 0;
+            }
+        }
+        for (int st = cid; st < num_super; st += ncl) {
+            int mg, nb;
+            tile_coords(st, num_mg, args.num_n, group, mg, nb);
+            const int m0 = (mg * CG + rank) * BM, n0 = nb * BN;
             int ok = 1;
-            if (lane == 0) ok = mbar_wait(tfull(acc), acc_phase, abort_flag) ? 1 : 0;
+            if (lane == 0 && !aborted) ok = mbar_wait(tfull(acc), acc_phase, abort_flag) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            tc_fence_after();
-            const int row = m0 + q * 32 + lane;
+            if (!ok) {
+                aborted = true;
+                *epi_abort = 1;
+            }
+            if (!aborted) tc_fence_after();
+            const int row = m0 + rl;
             float pmax = -INFINITY, psum = 0.f;
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
-                float v[32];
-                tmem_ld32(tmem_base + (uint32_t)(acc * BN + c) + ((uint32_t)(q * 32) << 16), v);
-                if (row < args.M && n0 + c < args.N)
-                    epilogue_chunk<T, EPI>(args, row, n0 + c, v, pmax, psum);
+            for (int j = 0; j < NSUB; j++, u++) {
+                const int b0 = (u * OUTS) % EPI_BUFS;
+                if (elected && !aborted) {
+                    if constexpr (HAS_AUX) {
+                        // prefetch the next sub-tile's operand into the next buffer
+                        int nt = st, nj = j + 1;
+                        if (nj == NSUB) { nt = st + ncl; nj = 0; }
+                        if (nt < num_super) {
+                            const int nb1 = (u + 1) % EPI_BUFS;
+                            int nmg, nnb;
+                            tile_coords(nt, num_mg, args.num_n, group, nmg, nnb);
+                            // the store that last read buffer nb1 is done
+                            bulk_wait_read<EPI_BUFS - 2>();
+                            mbar_expect_tx(auxfull(nb1), EPI_BUF_BYTES);
+                            tma_load_2d(ebuf + nb1 * EPI_BUF_BYTES, &tmX, auxfull(nb1),
+                                        nnb * BN + nj * SUBN, (nmg * CG + rank) * BM);
+                            last_aux_u[nb1] = u + 1;
+                        }
+                        if (!mbar_wait(auxfull(b0), (uint32_t)((u / EPI_BUFS) & 1), abort_flag)) {
+                            aborted = true;
+                            *epi_abort = 1;
+                        }
+                    } else {
+                        bulk_wait_read<EPI_BUFS / OUTS - 1>();  // buffers b0.. are free again
+                    }
+                }
+                epi_bar();  // operands landed / buffers free
+                int ab = aborted || *epi_abort;
+                ab = __shfl_sync(0xffffffffu, ab, 0);
+                aborted = ab != 0;
+                if (!aborted) {
+                    float v[HALF];
+                    const uint32_t taddr = tmem_base + (uint32_t)(acc * BN + j * SUBN + hh * HALF) +
+                                           ((uint32_t)(q * 32) << 16);
+                    if constexpr (HALF == 32) tmem_ld32(taddr, v);
+                    else tmem_ld16(taddr, v);
+                    epilogue_subtile<T, EPI>(args, v, ebuf_ptr + b0 * EPI_BUF_BYTES,
+                                             ebuf_ptr + ((b0 + 1) % EPI_BUFS) * EPI_BUF_BYTES, rl, row,
+                                             n0 + j * SUBN, hh * 4, pmax, psum);
+                }
+                fence_async_smem();
+                epi_bar();  // staging written
+                if (elected && !aborted) {
+                    tma_store_2d(&tmD, ebuf + b0 * EPI_BUF_BYTES, n0 + j * SUBN, m0);
+                    if constexpr (EPI == EPI_GELU)
+                        tma_store_2d(&tmD2, ebuf + (b0 + 1) * EPI_BUF_BYTES, n0 + j * SUBN, m0);
+                    bulk_commit();
+                }
             }
             if constexpr (EPI == EPI_GELU_PART) {
-                if (row < args.M)
+                // merge the two column halves of the row, then one partial per (row, tile)
+                if (hh == 1) row_part[rl] = make_float2(pmax, psum);
+                epi_bar();
+                if (hh == 0 && row < args.M && !aborted) {
+                    const float2 o = row_part[rl];
+                    const float m = fmaxf(pmax, o.x);
+                    float sum = 0.f;
+                    if (pmax != -INFINITY) sum += psum * expf(pmax - m);
+                    if (o.x != -INFINITY) sum += o.y * expf(o.x - m);
                     reinterpret_cast<float2*>(args.part)[(size_t)row * args.part_ld + nb] =
-                        make_float2(pmax, psum);
+                        make_float2(m, sum);
+                }
             }
-            tc_fence_before();
-            mbar_arrive(tempty(acc));
+            // this CTA's accumulator rows are read: release them to the leader's MMA
+            if (!aborted) tc_fence_before();
+            epi_bar();
+            if (elected) {
+                if constexpr (CG == 1) mbar_arrive(tempty(acc));
+                else mbar_arrive_cluster(mapa_rank(tempty(acc), 0));
+            }
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+        if (elected) {
+            bulk_wait_all();
+            if (aborted) {
+                for (int b = 0; b < EPI_BUFS; b++)
+                    if (last_aux_u[b] >= 0)
+                        mbar_wait_drain(auxfull(b), (uint32_t)((last_aux_u[b] / EPI_BUFS) & 1));
+            }
         }
     }
 
     __syncthreads();
-    if (*abort_flag) {
+    if (*abort_flag || *epi_abort) {
         // drain: wait for every TMA copy this CTA issued, and for all MMAs issued so far
         if (threadIdx.x == 0) {
             const int n_issued = *n_issued_smem;
-            for (int s = 0; s < C::STAGES; s++) {
-                if (n_issued > s) {
-                    const int last = s + ((n_issued - 1 - s) / C::STAGES) * C::STAGES;
-                    mbar_wait_drain(full(s), (uint32_t)((last / C::STAGES) & 1));
+            if (rank == 0) {
+                for (int s = 0; s < C::STAGES; s++) {
+                    if (n_issued > s) {
+                        const int last = s + ((n_issued - 1 - s) / C::STAGES) * C::STAGES;
+                        mbar_wait_drain(full(s), (uint32_t)((last / C::STAGES) & 1));
+                    }
                 }
             }
             atomicOr(args.err, DEVERR_TIMEOUT);
         }
-        if (threadIdx.x == 32) {
-            umma_commit(drain);
+        if (threadIdx.x == 32 && rank == 0) {
+            umma_commit_local<CG>(drain);
             mbar_wait_drain(drain, 0);
         }
         __syncthreads();
     }
+    if constexpr (CG == 2) cluster_sync();  // the peer's arrivals and copies are done
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, C::TMEM_COLS);
+        tmem_dealloc<CG>(tmem_base, C::TMEM_COLS);
     }
 }
 
@@ -494,39 +737,71 @@ static bool make_map(CUtensorMap* m, const void* ptr, DType dt, uint64_t inner, 
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, int KIND, int EPI>
-static int launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const tc::Args& a, int grid,
-                     cudaStream_t s) {
-    using C = tc::Cfg<BN>;
+struct Maps {
+    CUtensorMap a, b, d, d2, x;
+};
+
+// Persistent launch: one CTA per SM, or -- for CTA pairs -- as many 2-CTA
+// clusters as can be co-resident (cudaOccupancyMaxActiveClusters).
+template <int BN, int KIND, int EPI, int CG>
+static int launch_tc(const Maps& mp, const tc::Args& a, cudaStream_t s) {
+    using C = tc::Cfg<BN, CG>;
+    auto kern = tc::gemm_tc_k<BN, KIND, EPI, CG>;
     static bool attr_done = false;
+    static int max_clusters = 0;
     if (!attr_done) {
-        if (cudaFuncSetAttribute(tc::gemm_tc_k<BN, KIND, EPI>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::SMEM_BYTES) != cudaSuccess)
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+            cudaSuccess)
             return GPT2_ERR_CUDA;
         attr_done = true;
     }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(tc::NUM_THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    const long long supers = (long long)((a.num_m + CG - 1) / CG) * a.num_n;
+    if constexpr (CG == 1) {
+        const int sms = num_sms();
+        cfg.gridDim = dim3((unsigned)(supers < sms ? supers : sms));
+    } else {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (max_clusters == 0) {
+            int n = 0;
+            cfg.gridDim = dim3(2 * 64);
+            if (cudaOccupancyMaxActiveClusters(&n, (void*)kern, &cfg) != cudaSuccess || n < 1)
+                return GPT2_ERR_CUDA;
+            max_clusters = n;
+        }
+        const long long ncl = supers < max_clusters ? supers : max_clusters;
+        cfg.gridDim = dim3((unsigned)(ncl * 2));
+    }
     note_launch(1);
-    tc::gemm_tc_k<BN, KIND, EPI><<<grid, tc::NUM_THREADS, C::SMEM_BYTES, s>>>(ta, tb, a);
+    if (cudaLaunchKernelEx(&cfg, kern, mp.a, mp.b, mp.d, mp.d2, mp.x, a) != cudaSuccess)
+        return GPT2_ERR_CUDA;
     return GPT2_OK;
 }
 
-template <int BN, int KIND>
-static int dispatch_epi(int epi, const CUtensorMap& ta, const CUtensorMap& tb, const tc::Args& a,
-                        int grid, cudaStream_t s) {
+template <int BN, int KIND, int CG>
+static int dispatch_epi(int epi, const Maps& mp, const tc::Args& a, cudaStream_t s) {
     if constexpr (KIND == 0) {
         switch (epi) {
-            case EPI_STORE: return launch_tc<BN, KIND, EPI_STORE>(ta, tb, a, grid, s);
-            case EPI_GELU: return launch_tc<BN, KIND, EPI_GELU>(ta, tb, a, grid, s);
-            case EPI_RESID: return launch_tc<BN, KIND, EPI_RESID>(ta, tb, a, grid, s);
-            case EPI_GELU_BWD: return launch_tc<BN, KIND, EPI_GELU_BWD>(ta, tb, a, grid, s);
-            case EPI_ACCUM: return launch_tc<BN, KIND, EPI_ACCUM>(ta, tb, a, grid, s);
+            case EPI_STORE: return launch_tc<BN, KIND, EPI_STORE, CG>(mp, a, s);
+            case EPI_GELU: return launch_tc<BN, KIND, EPI_GELU, CG>(mp, a, s);
+            case EPI_RESID: return launch_tc<BN, KIND, EPI_RESID, CG>(mp, a, s);
+            case EPI_GELU_BWD: return launch_tc<BN, KIND, EPI_GELU_BWD, CG>(mp, a, s);
+            case EPI_ACCUM: return launch_tc<BN, KIND, EPI_ACCUM, CG>(mp, a, s);
             default: return GPT2_ERR_CONFIG;
         }
     } else {
         switch (epi) {
-            case EPI_STORE: return launch_tc<BN, KIND, EPI_STORE>(ta, tb, a, grid, s);
-            case EPI_GELU_PART: return launch_tc<BN, KIND, EPI_GELU_PART>(ta, tb, a, grid, s);
+            case EPI_STORE: return launch_tc<BN, KIND, EPI_STORE, CG>(mp, a, s);
+            case EPI_GELU_PART: return launch_tc<BN, KIND, EPI_GELU_PART, CG>(mp, a, s);
             default: return GPT2_ERR_CONFIG;
         }
     }
@@ -546,23 +821,34 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
     if (!al16(p.A) || !al16(p.B) || !al16(p.D) || (p.lda * esz) % 16 || (p.ldb * esz) % 16 ||
         (p.ldd * esz) % 16 || p.N % vec)
         return GPT2_ERR_ALIGN;
-    if ((p.epi == EPI_RESID || p.epi == EPI_GELU_BWD) && (!al16(p.aux) || (p.ldaux * esz) % 16))
-        return GPT2_ERR_ALIGN;
+    const bool has_aux = p.epi == EPI_RESID || p.epi == EPI_GELU_BWD;
+    if (has_aux && (!p.aux || !al16(p.aux) || (p.ldaux * esz) % 16)) return GPT2_ERR_ALIGN;
     if (p.bias && !al16(p.bias)) return GPT2_ERR_ALIGN;
-    if (p.epi == EPI_GELU && !al16(p.D2)) return GPT2_ERR_ALIGN;
+    if (p.epi == EPI_GELU && (!p.D2 || !al16(p.D2))) return GPT2_ERR_ALIGN;
 
     const int sms = num_sms();
+    const long long nm = (p.M + tc::BM - 1) / tc::BM;
+    // CTA pairs (256-row MMAs, half of B per CTA) when the m-blocks pair up
+    // without much waste; GPT2_GEMM_CG=1 forces single-CTA MMAs
+    static const int force_cg = [] {
+        const char* e = getenv("GPT2_GEMM_CG");
+        return e ? atoi(e) : 0;
+    }();
+    int cg = (nm >= 2 && (nm % 2 == 0 || nm >= 8)) ? 2 : 1;
+    if (force_cg == 1) cg = 1;
     // tile width: fewer waves x narrower tiles wins; EPI_GELU_PART fixes 256
     int BN = 256;
     if (p.epi != EPI_GELU_PART) {
-        const long long nm = (p.M + tc::BM - 1) / tc::BM;
-        const long long t256 = nm * ((p.N + 255) / 256), t128 = nm * ((p.N + 127) / 128);
-        const long long c256 = ((t256 + sms - 1) / sms) * 256, c128 = ((t128 + sms - 1) / sms) * 128;
+        const long long units = cg == 2 ? sms / 2 : sms;
+        const long long nmg = (nm + cg - 1) / cg;
+        const long long t256 = nmg * ((p.N + 255) / 256), t128 = nmg * ((p.N + 127) / 128);
+        const long long c256 = ((t256 + units - 1) / units) * 256, c128 = ((t128 + units - 1) / units) * 128;
         if (c128 < c256) BN = 128;
     }
     tc::Args a;
     a.M = p.M; a.N = p.N; a.K = p.K;
-    a.num_m = (p.M + tc::BM - 1) / tc::BM;
+    a.num_m = (int)nm;
+    a.cg = cg;
     a.num_n = (p.N + BN - 1) / BN;
     a.num_kb = (p.K + KE - 1) / KE;
     a.a_mn = p.a_kmajor ? 0 : 1;
@@ -570,19 +856,25 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
     a.D = p.D; a.ldd = p.ldd; a.bias = p.bias; a.aux = p.aux; a.ldaux = p.ldaux; a.D2 = p.D2;
     a.part = p.part; a.part_ld = p.part_ld; a.err = err;
 
-    CUtensorMap ta, tb;
-    bool ok = p.a_kmajor ? make_map(&ta, p.A, dt, p.K, p.M, p.lda, KE, tc::BM)
-                         : make_map(&ta, p.A, dt, p.M, p.K, p.lda, KE, KE);
-    ok = ok && (p.b_kmajor ? make_map(&tb, p.B, dt, p.K, p.N, p.ldb, KE, BN)
-                           : make_map(&tb, p.B, dt, p.N, p.K, p.ldb, KE, KE));
+    Maps mp;
+    const int SUBN = tc::ROWB / esz;
+    bool ok = p.a_kmajor ? make_map(&mp.a, p.A, dt, p.K, p.M, p.lda, KE, tc::BM)
+                         : make_map(&mp.a, p.A, dt, p.M, p.K, p.lda, KE, KE);
+    ok = ok && (p.b_kmajor ? make_map(&mp.b, p.B, dt, p.K, p.N, p.ldb, KE, BN / cg)
+                           : make_map(&mp.b, p.B, dt, p.N, p.K, p.ldb, KE, KE));
+    ok = ok && make_map(&mp.d, p.D, dt, p.N, p.M, p.ldd, SUBN, tc::BM);
+    ok = ok && make_map(&mp.d2, p.epi == EPI_GELU ? p.D2 : p.D, dt, p.N, p.M, p.ldd, SUBN, tc::BM);
+    if (has_aux) ok = ok && make_map(&mp.x, p.aux, dt, p.N, p.M, p.ldaux, SUBN, tc::BM);
+    else ok = ok && make_map(&mp.x, p.D, dt, p.N, p.M, p.ldd, SUBN, tc::BM);  // += reads D itself
     if (!ok) return GPT2_ERR_CUDA;
-    const long long tiles = (long long)a.num_m * a.num_n;
-    const int grid = (int)(tiles < sms ? tiles : sms);
-    if (dt == DT_BF16)
-        return BN == 256 ? dispatch_epi<256, 0>(p.epi, ta, tb, a, grid, s)
-                         : dispatch_epi<128, 0>(p.epi, ta, tb, a, grid, s);
-    return BN == 256 ? dispatch_epi<256, 1>(p.epi, ta, tb, a, grid, s)
-                     : dispatch_epi<128, 1>(p.epi, ta, tb, a, grid, s);
+    if (dt == DT_BF16) {
+        if (cg == 2)
+            return BN == 256 ? dispatch_epi<256, 0, 2>(p.epi, mp, a, s) : dispatch_epi<128, 0, 2>(p.epi, mp, a, s);
+        return BN == 256 ? dispatch_epi<256, 0, 1>(p.epi, mp, a, s) : dispatch_epi<128, 0, 1>(p.epi, mp, a, s);
+    }
+    if (cg == 2)
+        return BN == 256 ? dispatch_epi<256, 1, 2>(p.epi, mp, a, s) : dispatch_epi<128, 1, 2>(p.epi, mp, a, s);
+    return BN == 256 ? dispatch_epi<256, 1, 1>(p.epi, mp, a, s) : dispatch_epi<128, 1, 1>(p.epi, mp, a, s);
 }
 
 }  // namespace gk

@@ -350,12 +350,13 @@ void launch_layernorm_forward(DType dt, void* out, float* mean, float* rstd, con
 //   nhat = (x - mean) rstd, g = w * dy,
 //   dx (+)= rstd (g - mean_c(g) - nhat mean_c(g nhat)),
 //   dw += sum_rows nhat dy, db += sum_rows dy.
-// Stage 1: each block walks rows with its warps, keeps per-column partial
-// sums in registers, folds its warps in a fixed order and writes one partial
-// row per block to ws. Stage 2 sums the partial rows in block order.
+// Stage 1: one warp per row (a row lives in registers, NV 16-byte vectors per
+// lane); per-column partial sums stay in registers across the warp's rows,
+// the block folds its warps in a fixed order and writes one partial row to ws.
+// Stage 2 (reduce_partials_k) sums the partial rows in block order.
 constexpr int LNB_BLOCK = 256;
 
-template <typename T, int MAXV>
+template <typename T, int NV>
 __global__ void __launch_bounds__(LNB_BLOCK) layernorm_backward_k(
     T* __restrict__ dinp, float* __restrict__ ws, const T* __restrict__ dout,
     const T* __restrict__ inp, const T* __restrict__ w, const float* __restrict__ mean,
@@ -365,35 +366,30 @@ __global__ void __launch_bounds__(LNB_BLOCK) layernorm_backward_k(
     const int warps = blockDim.x / 32;
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const int cv = C / VEC;
-    float pdw[MAXV][VEC], pdb[MAXV][VEC], wr[MAXV][VEC];
+    float pdw[NV][VEC], pdb[NV][VEC];
 #pragma unroll
-    for (int j = 0; j < MAXV; j++) {
-        int vi = lane + 32 * j;
-        Vec16<T> wv;
-        if (vi < cv) wv = ld16(w + vi * VEC);
+    for (int j = 0; j < NV; j++)
 #pragma unroll
         for (int k = 0; k < VEC; k++) {
             pdw[j][k] = 0.f;
             pdb[j][k] = 0.f;
-            wr[j][k] = vi < cv ? to_f(wv.v[k]) : 0.f;
         }
-    }
     for (int row = blockIdx.x * warps + warp; row < N; row += gridDim.x * warps) {
         const T* x = inp + (size_t)row * C;
         const T* dy = dout + (size_t)row * C;
         const float mu = mean[row], rs = rstd[row];
-        float nh[MAXV][VEC], d[MAXV][VEC];
+        float nh[NV][VEC], d[NV][VEC];
         float gsum = 0.f, gnsum = 0.f;
 #pragma unroll
-        for (int j = 0; j < MAXV; j++) {
-            int vi = lane + 32 * j;
+        for (int j = 0; j < NV; j++) {
+            const int vi = lane + 32 * j;
             if (vi < cv) {
-                Vec16<T> xv = ld16(x + vi * VEC), dv = ld16(dy + vi * VEC);
+                Vec16<T> xv = ld16_cs(x + vi * VEC), dv = ld16_cs(dy + vi * VEC), wv = ld16(w + vi * VEC);
 #pragma unroll
                 for (int k = 0; k < VEC; k++) {
                     nh[j][k] = (to_f(xv.v[k]) - mu) * rs;
                     d[j][k] = to_f(dv.v[k]);
-                    float g = wr[j][k] * d[j][k];
+                    const float g = to_f(wv.v[k]) * d[j][k];
                     gsum += g;
                     gnsum += g * nh[j][k];
                 }
@@ -403,15 +399,15 @@ __global__ void __launch_bounds__(LNB_BLOCK) layernorm_backward_k(
         gnsum = warp_sum(gnsum) / C;
         T* dx = dinp + (size_t)row * C;
 #pragma unroll
-        for (int j = 0; j < MAXV; j++) {
-            int vi = lane + 32 * j;
+        for (int j = 0; j < NV; j++) {
+            const int vi = lane + 32 * j;
             if (vi < cv) {
-                Vec16<T> o;
+                Vec16<T> o, wv = ld16(w + vi * VEC);
                 if (accumulate) o = ld16(dx + vi * VEC);
 #pragma unroll
                 for (int k = 0; k < VEC; k++) {
-                    float g = wr[j][k] * d[j][k];
-                    float val = rs * (g - gsum - nh[j][k] * gnsum);
+                    const float g = to_f(wv.v[k]) * d[j][k];
+                    const float val = rs * (g - gsum - nh[j][k] * gnsum);
                     o.v[k] = from_f<T>(accumulate ? to_f(o.v[k]) + val : val);
                     pdw[j][k] += nh[j][k] * d[j][k];
                     pdb[j][k] += d[j][k];
@@ -426,8 +422,8 @@ __global__ void __launch_bounds__(LNB_BLOCK) layernorm_backward_k(
     for (int wi = 0; wi < warps; wi++) {
         if (warp == wi) {
 #pragma unroll
-            for (int j = 0; j < MAXV; j++) {
-                int vi = lane + 32 * j;
+            for (int j = 0; j < NV; j++) {
+                const int vi = lane + 32 * j;
                 if (vi < cv) {
 #pragma unroll
                     for (int k = 0; k < VEC; k++) {
@@ -443,28 +439,38 @@ __global__ void __launch_bounds__(LNB_BLOCK) layernorm_backward_k(
     for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) dst[c] = sm[c];
 }
 
+// dst[c] += sum over p of ws[p][c] for c in [0, W), summed in increasing p;
+// columns [split, W) go to dst2[c - split]. One warp per (32-column group,
+// p residue mod 8), folded across the 8 warps in order.
 template <typename T>
-__global__ void layernorm_param_reduce_k(T* __restrict__ dw, T* __restrict__ db,
-                                         const float* __restrict__ ws, int P, int C) {
-    int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c >= C) return;
-    float sw = 0.f, sb = 0.f;
-    for (int p = 0; p < P; p++) {
-        sw += ws[(size_t)p * 2 * C + c];
-        sb += ws[(size_t)p * 2 * C + C + c];
+__global__ void __launch_bounds__(256) reduce_partials_k(T* __restrict__ dst, T* __restrict__ dst2,
+                                                         int split, const float* __restrict__ ws,
+                                                         int P, int W) {
+    __shared__ float part[8][33];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    const int c = blockIdx.x * 32 + lane;
+    float acc = 0.f;
+    if (c < W)
+        for (int p = warp; p < P; p += 8) acc += ws[(size_t)p * W + c];
+    part[warp][lane] = acc;
+    __syncthreads();
+    if (warp == 0 && c < W) {
+        float t = 0.f;
+#pragma unroll
+        for (int wi = 0; wi < 8; wi++) t += part[wi][lane];
+        T* o = c < split ? dst + c : dst2 + (c - split);
+        *o = from_f<T>(to_f(*o) + t);
     }
-    dw[c] = from_f<T>(to_f(dw[c]) + sw);
-    db[c] = from_f<T>(to_f(db[c]) + sb);
 }
 
 static int lnb_blocks(int N) {
-    int rows_per_block = LNB_BLOCK / 32;
-    int g = (N + rows_per_block - 1) / rows_per_block;
-    int cap = 2 * num_sms();
+    const int rows_per_block = LNB_BLOCK / 32;
+    const int g = (N + rows_per_block - 1) / rows_per_block;
+    const int cap = 4 * num_sms();
     return g < cap ? (g < 1 ? 1 : g) : cap;
 }
 
-size_t layernorm_backward_ws_floats(int C) { return (size_t)2 * num_sms() * 2 * C; }
+size_t layernorm_backward_ws_floats(int C) { return (size_t)4 * num_sms() * 2 * C; }
 
 void launch_layernorm_backward(DType dt, void* dinp, void* dw, void* db, const void* dout,
                                const void* inp, const void* w, const float* mean,
@@ -472,27 +478,35 @@ void launch_layernorm_backward(DType dt, void* dinp, void* dw, void* db, const v
                                cudaStream_t s) {
     note_launch(2);
     const int VEC = dt == DT_BF16 ? 8 : 4;
-    const int mv = maxv_for(C / VEC);
+    const int nv = (C / VEC + 31) / 32;  // 16-byte vectors per lane (C <= 256*VEC checked at init)
     const int P = lnb_blocks(N);
     const size_t smem = sizeof(float) * 2 * C;
-#define LNB(TT, MV)                                                                          \
-    layernorm_backward_k<TT, MV><<<P, LNB_BLOCK, smem, s>>>((TT*)dinp, ws, (const TT*)dout,  \
-                                                            (const TT*)inp, (const TT*)w,     \
-                                                            mean, rstd, N, C, accumulate)
-    if (dt == DT_BF16) {
-        if (mv == 1) LNB(bf16, 1); else if (mv == 2) LNB(bf16, 2); else if (mv == 4) LNB(bf16, 4); else LNB(bf16, 8);
-        layernorm_param_reduce_k<bf16><<<(C + 255) / 256, 256, 0, s>>>((bf16*)dw, (bf16*)db, ws, P, C);
-    } else {
-        if (mv == 1) LNB(float, 1); else if (mv == 2) LNB(float, 2); else if (mv == 4) LNB(float, 4); else LNB(float, 8);
-        layernorm_param_reduce_k<float><<<(C + 255) / 256, 256, 0, s>>>((float*)dw, (float*)db, ws, P, C);
+#define LNB(TT, NVV)                                                                          \
+    layernorm_backward_k<TT, NVV><<<P, LNB_BLOCK, smem, s>>>((TT*)dinp, ws, (const TT*)dout,  \
+                                                             (const TT*)inp, (const TT*)w,     \
+                                                             mean, rstd, N, C, accumulate)
+#define LNB_ALL(TT)                                                                           \
+    switch (nv) {                                                                             \
+        case 1: LNB(TT, 1); break; case 2: LNB(TT, 2); break; case 3: LNB(TT, 3); break;       \
+        case 4: LNB(TT, 4); break; case 5: LNB(TT, 5); break; case 6: LNB(TT, 6); break;       \
+        case 7: LNB(TT, 7); break; default: LNB(TT, 8); break;                                \
     }
+    const unsigned rg = (unsigned)((2 * C + 31) / 32);
+    if (dt == DT_BF16) {
+        LNB_ALL(bf16);
+        reduce_partials_k<bf16><<<rg, 256, 0, s>>>((bf16*)dw, (bf16*)db, C, ws, P, 2 * C);
+    } else {
+        LNB_ALL(float);
+        reduce_partials_k<float><<<rg, 256, 0, s>>>((float*)dw, (float*)db, C, ws, P, 2 * C);
+    }
+#undef LNB_ALL
 #undef LNB
 }
 
 // ------------------------------------------------------------------ bias gradient
 // matmul_backward_bias_kernel4 read with +=: dbias[n] += sum over rows of dout[:, n].
 // Stage 1: block (x: 32*VEC columns, y: a slab of rows), 8 warps stride the
-// slab, warps folded in order; stage 2 sums the slabs in order.
+// slab, warps folded in order; stage 2 (reduce_partials_k) sums the slabs in order.
 constexpr int CS_SLABS = 64;
 
 template <typename T>
@@ -526,15 +540,6 @@ __global__ void __launch_bounds__(256) colsum_partial_k(float* __restrict__ ws,
     }
 }
 
-template <typename T>
-__global__ void colsum_final_k(T* __restrict__ dbias, const float* __restrict__ ws, int R, int N) {
-    int n = blockIdx.x * blockDim.x + threadIdx.x;
-    if (n >= N) return;
-    float sacc = 0.f;
-    for (int r = 0; r < R; r++) sacc += ws[(size_t)r * N + n];
-    dbias[n] = from_f<T>(to_f(dbias[n]) + sacc);
-}
-
 size_t colsum_ws_floats(int N) { return (size_t)CS_SLABS * N; }
 
 void launch_colsum_accum(DType dt, void* dbias, const void* dout, int M, int N, float* ws,
@@ -547,12 +552,13 @@ void launch_colsum_accum(DType dt, void* dbias, const void* dout, int M, int N, 
     int rps = (M + R - 1) / R;
     R = (M + rps - 1) / rps;
     dim3 grid((N + 32 * VEC - 1) / (32 * VEC), R);
+    const unsigned rg = (unsigned)((N + 31) / 32);
     if (dt == DT_BF16) {
         colsum_partial_k<bf16><<<grid, 256, 0, s>>>(ws, (const bf16*)dout, M, N, rps);
-        colsum_final_k<bf16><<<(N + 255) / 256, 256, 0, s>>>((bf16*)dbias, ws, R, N);
+        reduce_partials_k<bf16><<<rg, 256, 0, s>>>((bf16*)dbias, (bf16*)dbias, N, ws, R, N);
     } else {
         colsum_partial_k<float><<<grid, 256, 0, s>>>(ws, (const float*)dout, M, N, rps);
-        colsum_final_k<float><<<(N + 255) / 256, 256, 0, s>>>((float*)dbias, ws, R, N);
+        reduce_partials_k<float><<<rg, 256, 0, s>>>((float*)dbias, (float*)dbias, N, ws, R, N);
     }
 }
 

@@ -1,0 +1,87 @@
+"""Time one kernel of libgpt2.so on synthetic inputs (for profiling and tuning).
+
+    python -m transformer_lm_gb300.kernel_bench gemm M N K [a_kmajor b_kmajor epilogue] [--reps R]
+    python -m transformer_lm_gb300.kernel_bench attention B T C NH [--reps R]
+    python -m transformer_lm_gb300.kernel_bench fused M K N [--reps R]
+
+Prints the mean CUDA-event time per launch and the throughput. Inputs are
+allocated with torch; the kernels run through the C ABI.
+"""
+from __future__ import annotations
+
+import argparse
+import sys
+
+
+def _time(fn, reps):
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def main(argv=None):
+    import torch
+
+    from transformer_lm_gb300 import gpt2 as G
+    ap = argparse.ArgumentParser()
+    ap.add_argument("kind", choices=["gemm", "attention", "fused"])
+    ap.add_argument("dims", nargs="*")
+    ap.add_argument("--reps", type=int, default=20)
+    a = ap.parse_args(argv)
+    d = a.dims
+    if a.kind == "gemm":
+        M, N, K = int(d[0]), int(d[1]), int(d[2])
+        akm = int(d[3]) if len(d) > 3 else 1
+        bkm = int(d[4]) if len(d) > 4 else 1
+        epi = d[5] if len(d) > 5 else "store"
+        A = (torch.randn(M * K, device="cuda") * 0.5).bfloat16()
+        B = (torch.randn(N * K, device="cuda") * 0.05).bfloat16()
+        D = torch.zeros(M * N, device="cuda").bfloat16()
+        D2 = torch.zeros(M * N, device="cuda").bfloat16() if epi == "gelu" else None
+        aux = torch.randn(M * N, device="cuda").bfloat16() if epi in ("resid", "gelu_bwd") else None
+        bias = torch.zeros(N, device="cuda").bfloat16()
+
+        def fn():
+            G.gpt2_gemm(G.GPT2_BF16, 1, epi, A, K if akm else M, akm, B, K if bkm else N, bkm, D, N,
+                        bias=bias, aux=aux, ldaux=N, D2=D2, M=M, N=N, K=K)
+        ms = _time(fn, a.reps)
+        print(f"gemm {M}x{N}x{K} a_kmajor={akm} b_kmajor={bkm} {epi}: {ms * 1e3:.1f} us, "
+              f"{2.0 * M * N * K / ms / 1e9:.1f} TFLOP/s")
+    elif a.kind == "attention":
+        B, T, C, NH = (int(x) for x in d[:4])
+        qkv = (torch.randn(B * T * 3 * C, device="cuda")).bfloat16()
+        out = torch.zeros(B * T * C, device="cuda").bfloat16()
+        lse = torch.zeros(B * NH * T, device="cuda")
+        dout = (torch.randn(B * T * C, device="cuda") * 0.1).bfloat16()
+        dqkv = torch.zeros(B * T * 3 * C, device="cuda").bfloat16()
+        Dsc = torch.zeros(B * NH * T, device="cuda")
+        flops = 2.0 * B * NH * T * (T + 1) * (C // NH)
+        ms_f = _time(lambda: G.gpt2_attention_forward(1, 1, qkv, out, lse, B, T, C, NH), a.reps)
+        ms_b = _time(lambda: G.gpt2_attention_backward(1, 1, dout, qkv, out, lse, dqkv, Dsc, B, T, C,
+                                                       NH), a.reps)
+        print(f"attention B={B} T={T} C={C} NH={NH}: fwd {ms_f * 1e3:.1f} us "
+              f"({flops / ms_f / 1e9:.1f} TFLOP/s), bwd {ms_b * 1e3:.1f} us "
+              f"({2 * flops / ms_b / 1e9:.1f} TFLOP/s)")
+    else:
+        M, K, N = int(d[0]), int(d[1]), int(d[2])
+        x = torch.randn(M, K, device="cuda")
+        W = torch.randn(N, K, device="cuda") / K ** 0.5
+        b = (torch.rand(N, device="cuda") - 0.5) * 0.2
+        y = torch.empty(M, N, device="cuda")
+        ms = _time(lambda: G.fused_linear_bias_gelu_softmax(x, W, b, y, M, K, N), a.reps)
+        print(f"fused {M}x{K}x{N}: {ms * 1e3:.1f} us, {2.0 * M * N * K / ms / 1e9:.1f} TFLOP/s")
+    G.gpt2_device_status()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -219,6 +219,21 @@ int gpt2_attention_backward(int dtype, int tensor_cores, const void* dout, const
                             const void* out, const float* lse, void* dqkv, float* scratch_D, int B,
                             int T, int C, int NH, void* stream);
 
+/* LayerNorm over the last dimension C of N rows (llm.c "train_gpt2.cu",
+ * layernorm_forward_kernel3): biased variance, eps 1e-5; out (N,C), mean and
+ * rstd (N) fp32. C % 8 == 0, C <= 2048 (bf16) / 1024 (fp32). */
+int gpt2_layernorm_forward(int dtype, void* out, float* mean, float* rstd, const void* inp,
+                           const void* w, const void* b, int N, int C, void* stream);
+
+/* Its backward (layernorm_backward_kernel6 with += for every output): dinp +=
+ * (or = when accumulate == 0), dw += and db += sums over the N rows, computed
+ * deterministically through `scratch` (fp32, gpt2_layernorm_backward_scratch_floats(C)
+ * floats, caller-owned). */
+size_t gpt2_layernorm_backward_scratch_floats(int C);
+int gpt2_layernorm_backward(int dtype, void* dinp, void* dw, void* db, const void* dout,
+                            const void* inp, const void* w, const float* mean, const float* rstd,
+                            int N, int C, int accumulate, float* scratch, void* stream);
+
 /* Synchronise the device and report (then clear) the error word of the
  * stand-alone entry points: GPT2_ERR_DEVICE_TIMEOUT if a bounded wait expired. */
 int gpt2_device_status(void);

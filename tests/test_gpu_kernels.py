@@ -138,3 +138,42 @@ def test_fused_op_small_shapes_match_oracle():
         y = host(out)
         np.testing.assert_allclose(y.sum(1), 1.0, atol=1e-5)
         assert max_rel_floor(y, ref, 0.0) < 2e-2, (M, K, N, max_rel_floor(y, ref, 0.0))
+
+
+@pytest.mark.parametrize("N,C,dt", [(1000, 768, "bf16"), (37, 64, "f32"), (8192, 768, "bf16"),
+                                    (300, 1024, "bf16"), (129, 1024, "f32")])
+def test_layernorm_forward_backward_match_oracle(N, C, dt):
+    import torch
+    bf16 = dt == "bf16"
+    x = inputs.normal(N + C, 1, N * C, 2.0).reshape(N, C).astype(np.float32) + 0.5
+    w = (1.0 + inputs.normal(N + C, 2, C, 0.1)).astype(np.float32)
+    b = inputs.normal(N + C, 3, C, 0.1).astype(np.float32)
+    dy = inputs.normal(N + C, 4, N * C, 0.01).reshape(N, C).astype(np.float32)
+    d0 = inputs.normal(N + C, 5, N * C, 0.01).reshape(N, C).astype(np.float32)
+    if bf16:
+        x, w, b, dy, d0 = (inputs.round_to_bf16(a) for a in (x, w, b, dy, d0))
+    ref, mean, rstd = oracle.layernorm_forward(x, w, b)
+    prec = G.GPT2_BF16 if bf16 else G.GPT2_FP32
+    out = empty((N, C), dt)
+    dmean = torch.zeros(N, device="cuda")
+    drstd = torch.zeros(N, device="cuda")
+    dx = dev(x, dt)
+    G.gpt2_layernorm_forward(prec, out, dmean, drstd, dx, dev(w, dt), dev(b, dt), N, C)
+    tol = 1e-2 if bf16 else 1e-5
+    assert rel_to_max(host(out), ref) < tol
+    np.testing.assert_allclose(host(drstd), rstd, rtol=1e-4)
+    # backward, accumulating into d0 and into nonzero dw, db
+    dinp = d0.astype(np.float64).copy()
+    dw = np.ones(C)
+    db = np.ones(C)
+    oracle.layernorm_backward(dinp, dw, db, dy, x, w, mean, rstd)
+    g_dinp = dev(d0, dt)
+    g_dw = dev(np.ones(C, dtype=np.float32), dt)
+    g_db = dev(np.ones(C, dtype=np.float32), dt)
+    scratch = torch.zeros(G.gpt2_layernorm_backward_scratch_floats(C), device="cuda")
+    G.gpt2_layernorm_backward(prec, g_dinp, g_dw, g_db, dev(dy, dt), dx, dev(w, dt), dmean, drstd, N,
+                              C, 1, scratch)
+    G.gpt2_device_status()
+    assert rel_to_max(host(g_dinp), dinp) < (2e-2 if bf16 else 1e-5)
+    assert rel_to_max(host(g_dw) - 1.0, dw - 1.0) < (2e-2 if bf16 else 1e-5)
+    assert rel_to_max(host(g_db) - 1.0, db - 1.0) < (2e-2 if bf16 else 1e-5)

@@ -362,81 +362,69 @@ __global__ void __launch_bounds__(LNB_BLOCK) layernorm_backward_k(
     const T* __restrict__ inp, const T* __restrict__ w, const float* __restrict__ mean,
     const float* __restrict__ rstd, int N, int C, int accumulate) {
     constexpr int VEC = Vec16<T>::N;
-    extern __shared__ float sm[];  // [2][C]
+    // per-warp partial sums, [warp][dw | db][k][vector]: lane-consecutive addresses
+    extern __shared__ float sm[];
     const int warps = blockDim.x / 32;
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const int cv = C / VEC;
-    float pdw[NV][VEC], pdb[NV][VEC];
-#pragma unroll
-    for (int j = 0; j < NV; j++)
-#pragma unroll
-        for (int k = 0; k < VEC; k++) {
-            pdw[j][k] = 0.f;
-            pdb[j][k] = 0.f;
-        }
+    float* mine = sm + (size_t)warp * 2 * C;
+    for (int c = lane; c < 2 * C; c += 32) mine[c] = 0.f;
+    __syncwarp();
     for (int row = blockIdx.x * warps + warp; row < N; row += gridDim.x * warps) {
         const T* x = inp + (size_t)row * C;
         const T* dy = dout + (size_t)row * C;
         const float mu = mean[row], rs = rstd[row];
-        float nh[NV][VEC], d[NV][VEC];
+        // pass 1: the two row reductions (the row stays in L1 for pass 2)
         float gsum = 0.f, gnsum = 0.f;
 #pragma unroll
         for (int j = 0; j < NV; j++) {
             const int vi = lane + 32 * j;
             if (vi < cv) {
-                Vec16<T> xv = ld16_cs(x + vi * VEC), dv = ld16_cs(dy + vi * VEC), wv = ld16(w + vi * VEC);
+                Vec16<T> xv = ld16(x + vi * VEC), dv = ld16(dy + vi * VEC), wv = ld16(w + vi * VEC);
 #pragma unroll
                 for (int k = 0; k < VEC; k++) {
-                    nh[j][k] = (to_f(xv.v[k]) - mu) * rs;
-                    d[j][k] = to_f(dv.v[k]);
-                    const float g = to_f(wv.v[k]) * d[j][k];
+                    const float g = to_f(wv.v[k]) * to_f(dv.v[k]);
                     gsum += g;
-                    gnsum += g * nh[j][k];
+                    gnsum += g * (to_f(xv.v[k]) - mu) * rs;
                 }
             }
         }
         gsum = warp_sum(gsum) / C;
         gnsum = warp_sum(gnsum) / C;
+        // pass 2: outputs and the parameter partials
         T* dx = dinp + (size_t)row * C;
 #pragma unroll
         for (int j = 0; j < NV; j++) {
             const int vi = lane + 32 * j;
             if (vi < cv) {
-                Vec16<T> o, wv = ld16(w + vi * VEC);
+                Vec16<T> xv = ld16_cs(x + vi * VEC), dv = ld16_cs(dy + vi * VEC), wv = ld16(w + vi * VEC);
+                Vec16<T> o;
                 if (accumulate) o = ld16(dx + vi * VEC);
 #pragma unroll
                 for (int k = 0; k < VEC; k++) {
-                    const float g = to_f(wv.v[k]) * d[j][k];
-                    const float val = rs * (g - gsum - nh[j][k] * gnsum);
+                    const float d = to_f(dv.v[k]);
+                    const float nh = (to_f(xv.v[k]) - mu) * rs;
+                    const float g = to_f(wv.v[k]) * d;
+                    const float val = rs * (g - gsum - nh * gnsum);
                     o.v[k] = from_f<T>(accumulate ? to_f(o.v[k]) + val : val);
-                    pdw[j][k] += nh[j][k] * d[j][k];
-                    pdb[j][k] += d[j][k];
+                    mine[k * cv + vi] += nh * d;
+                    mine[C + k * cv + vi] += d;
                 }
                 st16(dx + vi * VEC, o);
             }
         }
     }
-    // fold the warps' partials in warp order
-    for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) sm[c] = 0.f;
     __syncthreads();
-    for (int wi = 0; wi < warps; wi++) {
-        if (warp == wi) {
-#pragma unroll
-            for (int j = 0; j < NV; j++) {
-                const int vi = lane + 32 * j;
-                if (vi < cv) {
-#pragma unroll
-                    for (int k = 0; k < VEC; k++) {
-                        sm[vi * VEC + k] += pdw[j][k];
-                        sm[C + vi * VEC + k] += pdb[j][k];
-                    }
-                }
-            }
-        }
-        __syncthreads();
-    }
+    // fold the warps' slices in warp order and write this block's partial row
+    // in column order (column vi*VEC + k)
     float* dst = ws + (size_t)blockIdx.x * 2 * C;
-    for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) dst[c] = sm[c];
+    for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) {
+        const int half = c >= C, cc = c - half * C;
+        const int vi = cc / VEC, k = cc % VEC;
+        float t = 0.f;
+        for (int wi = 0; wi < warps; wi++) t += sm[(size_t)wi * 2 * C + half * C + k * cv + vi];
+        dst[c] = t;
+    }
 }
 
 // dst[c] += sum over p of ws[p][c] for c in [0, W), summed in increasing p;
@@ -463,10 +451,23 @@ __global__ void __launch_bounds__(256) reduce_partials_k(T* __restrict__ dst, T*
     }
 }
 
-static int lnb_blocks(int N) {
+// one wave: as many blocks as are resident at once (at most 4 per SM), each
+// walking rows with its warps
+template <typename T, int NV>
+static int lnb_blocks(int N, size_t smem) {
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        cudaFuncSetAttribute(layernorm_backward_k<T, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(sizeof(float) * 2 * 2048 * (LNB_BLOCK / 32)));
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, layernorm_backward_k<T, NV>, LNB_BLOCK,
+                                                          smem) != cudaSuccess || n < 1)
+            n = 1;
+        per_sm = n < 4 ? n : 4;
+    }
     const int rows_per_block = LNB_BLOCK / 32;
     const int g = (N + rows_per_block - 1) / rows_per_block;
-    const int cap = 4 * num_sms();
+    const int cap = per_sm * num_sms();
     return g < cap ? (g < 1 ? 1 : g) : cap;
 }
 
@@ -479,9 +480,10 @@ void launch_layernorm_backward(DType dt, void* dinp, void* dw, void* db, const v
     note_launch(2);
     const int VEC = dt == DT_BF16 ? 8 : 4;
     const int nv = (C / VEC + 31) / 32;  // 16-byte vectors per lane (C <= 256*VEC checked at init)
-    const int P = lnb_blocks(N);
-    const size_t smem = sizeof(float) * 2 * C;
+    const size_t smem = sizeof(float) * 2 * C * (LNB_BLOCK / 32);
+    int P = 1;
 #define LNB(TT, NVV)                                                                          \
+    P = lnb_blocks<TT, NVV>(N, smem);                                                         \
     layernorm_backward_k<TT, NVV><<<P, LNB_BLOCK, smem, s>>>((TT*)dinp, ws, (const TT*)dout,  \
                                                              (const TT*)inp, (const TT*)w,     \
                                                              mean, rstd, N, C, accumulate)

@@ -141,6 +141,29 @@ int gpt2_attention_backward(int dtype, int tensor_cores, const void* dout, const
     return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
+int gpt2_layernorm_forward(int dtype, void* out, float* mean, float* rstd, const void* inp,
+                           const void* w, const void* b, int N, int C, void* stream) {
+    if (!out || !mean || !rstd || !inp || !w || !b) return GPT2_ERR_ARG;
+    if (dtype != GPT2_FP32 && dtype != GPT2_BF16) return GPT2_ERR_CONFIG;
+    if (N < 1 || C < 8 || C % 8 || C > (dtype == GPT2_BF16 ? 2048 : 1024)) return GPT2_ERR_ARG;
+    launch_layernorm_forward(dtype == GPT2_BF16 ? DT_BF16 : DT_F32, out, mean, rstd, inp, w, b, N,
+                             C, (cudaStream_t)stream);
+    return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+}
+
+size_t gpt2_layernorm_backward_scratch_floats(int C) { return layernorm_backward_ws_floats(C); }
+
+int gpt2_layernorm_backward(int dtype, void* dinp, void* dw, void* db, const void* dout,
+                            const void* inp, const void* w, const float* mean, const float* rstd,
+                            int N, int C, int accumulate, float* scratch, void* stream) {
+    if (!dinp || !dw || !db || !dout || !inp || !w || !mean || !rstd || !scratch) return GPT2_ERR_ARG;
+    if (dtype != GPT2_FP32 && dtype != GPT2_BF16) return GPT2_ERR_CONFIG;
+    if (N < 1 || C < 8 || C % 8 || C > (dtype == GPT2_BF16 ? 2048 : 1024)) return GPT2_ERR_ARG;
+    launch_layernorm_backward(dtype == GPT2_BF16 ? DT_BF16 : DT_F32, dinp, dw, db, dout, inp, w, mean,
+                              rstd, N, C, accumulate, scratch, (cudaStream_t)stream);
+    return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+}
+
 int gpt2_device_status(void) {
     int dev;
     if (current_device(&dev) != GPT2_OK) return GPT2_ERR_CUDA;

@@ -80,6 +80,10 @@ _SIGS = {
     "gpt2_attention_forward": (_i, [_i, _i, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "gpt2_attention_backward": (_i, [_i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "gpt2_device_status": (_i, []),
+    "gpt2_layernorm_forward": (_i, [_i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp]),
+    "gpt2_layernorm_backward_scratch_floats": (_sz, [_i]),
+    "gpt2_layernorm_backward": (_i, [_i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _vp,
+                                     _vp]),
     "gpt2_launch_count": (_ll, []),
 }
 
@@ -286,6 +290,24 @@ def gpt2_attention_backward(dtype, tensor_cores, dout, qkv, out, lse, dqkv, scra
     _check("gpt2_attention_backward",
            lib().gpt2_attention_backward(dtype, tensor_cores, ptr(dout), ptr(qkv), ptr(out),
                                          ptr(lse), ptr(dqkv), ptr(scratch_D), B, T, C, NH, stream))
+
+
+def gpt2_layernorm_forward(dtype, out, mean, rstd, inp, w, b, N, C, stream=None) -> None:
+    _check("gpt2_layernorm_forward",
+           lib().gpt2_layernorm_forward(dtype, ptr(out), ptr(mean), ptr(rstd), ptr(inp), ptr(w),
+                                        ptr(b), N, C, stream))
+
+
+def gpt2_layernorm_backward_scratch_floats(C) -> int:
+    return int(lib().gpt2_layernorm_backward_scratch_floats(C))
+
+
+def gpt2_layernorm_backward(dtype, dinp, dw, db, dout, inp, w, mean, rstd, N, C, accumulate,
+                            scratch, stream=None) -> None:
+    _check("gpt2_layernorm_backward",
+           lib().gpt2_layernorm_backward(dtype, ptr(dinp), ptr(dw), ptr(db), ptr(dout), ptr(inp),
+                                         ptr(w), ptr(mean), ptr(rstd), N, C, int(accumulate),
+                                         ptr(scratch), stream))
 
 
 def gpt2_launch_count() -> int:

@@ -3,6 +3,7 @@
     python -m transformer_lm_gb300.kernel_bench gemm M N K [a_kmajor b_kmajor epilogue] [--reps R]
     python -m transformer_lm_gb300.kernel_bench attention B T C NH [--reps R]
     python -m transformer_lm_gb300.kernel_bench fused M K N [--reps R]
+    python -m transformer_lm_gb300.kernel_bench layernorm N C [--reps R]
 
 Prints the mean CUDA-event time per launch and the throughput. Inputs are
 allocated with torch; the kernels run through the C ABI.
@@ -33,7 +34,7 @@ def main(argv=None):
 
     from transformer_lm_gb300 import gpt2 as G
     ap = argparse.ArgumentParser()
-    ap.add_argument("kind", choices=["gemm", "attention", "fused"])
+    ap.add_argument("kind", choices=["gemm", "attention", "fused", "layernorm"])
     ap.add_argument("dims", nargs="*")
     ap.add_argument("--reps", type=int, default=20)
     a = ap.parse_args(argv)
@@ -71,6 +72,24 @@ def main(argv=None):
         print(f"attention B={B} T={T} C={C} NH={NH}: fwd {ms_f * 1e3:.1f} us "
               f"({flops / ms_f / 1e9:.1f} TFLOP/s), bwd {ms_b * 1e3:.1f} us "
               f"({2 * flops / ms_b / 1e9:.1f} TFLOP/s)")
+    elif a.kind == "layernorm":
+        N, C = int(d[0]), int(d[1])
+        x = torch.randn(N * C, device="cuda").bfloat16()
+        w = torch.ones(C, device="cuda").bfloat16()
+        b = torch.zeros(C, device="cuda").bfloat16()
+        y = torch.empty_like(x)
+        mean = torch.empty(N, device="cuda")
+        rstd = torch.empty(N, device="cuda")
+        dy = (torch.randn(N * C, device="cuda") * 0.01).bfloat16()
+        dx = torch.zeros_like(x)
+        dw = torch.zeros_like(w)
+        db = torch.zeros_like(b)
+        scratch = torch.zeros(G.gpt2_layernorm_backward_scratch_floats(C), device="cuda")
+        ms_f = _time(lambda: G.gpt2_layernorm_forward(1, y, mean, rstd, x, w, b, N, C), a.reps)
+        ms_b = _time(lambda: G.gpt2_layernorm_backward(1, dx, dw, db, dy, x, w, mean, rstd, N, C, 1,
+                                                       scratch), a.reps)
+        print(f"layernorm N={N} C={C}: fwd {ms_f * 1e3:.1f} us ({4.0 * N * C / ms_f / 1e6:.0f} GB/s), "
+              f"bwd {ms_b * 1e3:.1f} us ({8.0 * N * C / ms_b / 1e6:.0f} GB/s)")
     else:
         M, K, N = int(d[0]), int(d[1]), int(d[2])
         x = torch.randn(M, K, device="cuda")

@@ -598,27 +598,34 @@ static void simt_backward(void* dqkv, const void* dout, const void* qkv, const f
 #undef ATTB
 }
 
-void launch_attention_forward(DType dt, int tensor_cores, void* out, float* lse, const void* qkv,
-                              int B, int T, int C, int NH, cudaStream_t s) {
-    note_launch(1);
+int launch_attention_forward(DType dt, int tensor_cores, void* out, float* lse, const void* qkv,
+                             int B, int T, int C, int NH, cudaStream_t s, unsigned int* err) {
     const int HS = C / NH;
     if (dt == DT_BF16 && tensor_cores && HS == 64) {
+        // tcgen05 kernel; the m16n8k16 kernel remains for operands TMA cannot address
+        const int rc = launch_flash_forward_tc(out, lse, qkv, B, T, C, NH, s, err);
+        if (rc != GPT2_ERR_ALIGN) return rc;
+        note_launch(1);
         dim3 grid((T + fa::BLK - 1) / fa::BLK, B * NH);
         const float scale_log2 = LOG2E_F / sqrtf((float)HS);
         fa::flash_fwd_k<<<grid, 128, 0, s>>>((bf16*)out, lse, (const bf16*)qkv, T, C, NH, scale_log2);
-        return;
+        return GPT2_OK;
     }
+    note_launch(1);
     if (dt == DT_BF16) simt_forward<bf16>(out, lse, qkv, B, T, C, NH, s);
     else simt_forward<float>(out, lse, qkv, B, T, C, NH, s);
+    return GPT2_OK;
 }
 
-void launch_attention_backward(DType dt, int tensor_cores, void* dqkv, const void* dout,
-                               const void* qkv, const void* out, const float* lse, float* D,
-                               int B, int T, int C, int NH, cudaStream_t s) {
-    
+int launch_attention_backward(DType dt, int tensor_cores, void* dqkv, const void* dout,
+                              const void* qkv, const void* out, const float* lse, float* D, int B,
+                              int T, int C, int NH, cudaStream_t s, unsigned int* err) {
     const int HS = C / NH;
     const int n = B * NH * T;
     if (dt == DT_BF16 && tensor_cores && HS == 64) {
+        // tcgen05 kernels; the m16n8k16 kernels remain for operands TMA cannot address
+        const int rc = launch_flash_backward_tc(dqkv, dout, qkv, out, lse, D, B, T, C, NH, s, err);
+        if (rc != GPT2_ERR_ALIGN) return rc;
         note_launch(2);
         dim3 grid((T + fa::BLK - 1) / fa::BLK, B * NH);
         const float scale = 1.f / sqrtf((float)HS), scale_log2 = LOG2E_F * scale;
@@ -627,7 +634,7 @@ void launch_attention_backward(DType dt, int tensor_cores, void* dqkv, const voi
                                                 scale_log2);
         fa::flash_bwd_dkv_k<<<grid, 128, 0, s>>>((bf16*)dqkv, (const bf16*)dout, (const bf16*)qkv,
                                                  lse, D, T, C, NH, scale, scale_log2);
-        return;
+        return GPT2_OK;
     }
     note_launch(3);
     if (dt == DT_BF16)
@@ -638,6 +645,7 @@ void launch_attention_backward(DType dt, int tensor_cores, void* dqkv, const voi
                                                              (const float*)out, B, T, C, NH, HS);
     if (dt == DT_BF16) simt_backward<bf16>(dqkv, dout, qkv, lse, D, B, T, C, NH, s);
     else simt_backward<float>(dqkv, dout, qkv, lse, D, B, T, C, NH, s);
+    return GPT2_OK;
 }
 
 }  // namespace gk

@@ -1,0 +1,533 @@
+// attention_bwd_tc.cu -- causal flash attention backward on the tcgen05 tensor
+// cores (sm_103a), head size 64, bf16 operands, fp32 softmax and accumulators.
+//
+// With P = softmax(q.k / sqrt(64)) recomputed from the forward's LSE, and
+// D_i = sum_d dO_id O_id (the row dot product of the output and its grad):
+//   dV_j = sum_i P_ij dO_i
+//   dS_ij = P_ij (dO_i . v_j - D_i)
+//   dK_j = scale sum_i dS_ij q_i,   dQ_i = scale sum_j dS_ij k_j
+// (llm.c "train_gpt2.cu", attention_backward with softmax_autoregressive_
+// backward_kernel, in flash form: no T x T matrix is stored). The grads are
+// written with "=" into dqkv (B, T, 3C).
+//
+// Two kernels, neither with float atomics, so every run is bit-identical:
+//   DKV  one CTA per (128-key tile, b, h); it walks the query blocks at and
+//        after its keys, with S^T = K Q^T and dP^T = V dO^T in TMEM and
+//        dV += P^T dO, dK += dS^T Q accumulating in TMEM;
+//   DQ   one CTA per (128-query tile, b, h); it walks the key blocks at and
+//        before its queries with S = Q K^T, dP = dO V^T and dQ += dS K.
+// Roles (320 threads): warp 0 loads the streamed Q/dO (or K/V) blocks into a
+// 3-stage ring by TMA (and, for DKV, the blocks' LSE and D into shared
+// memory); one thread of warp 1 issues the MMAs; warps 2..9 form P and dS,
+// two warps per TMEM lane quarter, each on 64 of the 128 columns. S is
+// double-buffered in TMEM, so the next block's S = ... MMA overlaps the
+// current block's softmax. All waits are bounded; on expiry the CTA records
+// DEVERR_TIMEOUT, drains its copies and MMAs and frees TMEM.
+#include "common.cuh"
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+#include "gpt2.h"
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+namespace gk {
+namespace fabw {
+using namespace tc;
+
+constexpr int HSZ = 64;
+constexpr int BLK = 128;                   // rows per CTA and columns per block
+constexpr int STAGES = 3;
+constexpr int TILE = 128 * 128;            // 128 rows x 64 bf16, 128B-swizzled
+constexpr int OFF_X0 = 0;                  // fixed tiles: K, V (DKV) or Q, dO (DQ)
+constexpr int OFF_X1 = TILE;
+constexpr int OFF_Y = 2 * TILE;            // ring: stage s holds Y0 at +2s*TILE, Y1 at +(2s+1)*TILE
+constexpr int OFF_P = OFF_Y + STAGES * 2 * TILE;  // P^T (DKV), two 64-column atoms
+constexpr int OFF_DS = OFF_P + 2 * TILE;          // dS^T (DKV) or dS (DQ)
+constexpr int OFF_VEC = OFF_DS + 2 * TILE;        // per stage: -LSE*log2(e) [128], D [128]
+constexpr int OFF_BAR = OFF_VEC + STAGES * 1024;
+constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;
+constexpr int NUM_THREADS = 320;
+constexpr int TMEM_COLS = 512;  // S0 0, S1 128, dP 256, acc0 384 (dV / dQ), acc1 448 (dK)
+constexpr float LOG2E = 1.4426950408889634f;
+
+struct BwdArgs {
+    bf16* dqkv;
+    const float* lse;
+    const float* D;
+    int T, C, NH, BH, nblk;
+    float scale, scale_log2;
+    unsigned int* err;
+};
+
+template <bool DKV>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    flash_bwd_tc_k(const __grid_constant__ CUtensorMap tqkv, const __grid_constant__ CUtensorMap tdo,
+                   const __grid_constant__ BwdArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw);
+    const uint32_t bars = base + OFF_BAR;
+    uint8_t* bars_ptr = base_ptr + OFF_BAR;
+    const uint32_t fixed_full = bars;
+    auto st_full = [&](int s) { return bars + 8u * (1 + s); };
+    auto st_empty = [&](int s) { return bars + 8u * (4 + s); };
+    auto s_full = [&](int b) { return bars + 8u * (7 + b); };
+    auto s_empty = [&](int b) { return bars + 8u * (9 + b); };
+    const uint32_t dp_full = bars + 8u * 11, dp_empty = bars + 8u * 12;
+    const uint32_t p_full = bars + 8u * 13, p_empty = bars + 8u * 14;
+    const uint32_t ds_full = bars + 8u * 15, ds_empty = bars + 8u * 16;
+    const uint32_t acc_full = bars + 8u * 17, drain = bars + 8u * 18;
+    constexpr int NBARS = 19;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars_ptr + 8 * NBARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars_ptr + 8 * NBARS + 4);
+    int* n_issued_smem = reinterpret_cast<int*>(bars_ptr + 8 * NBARS + 8);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    const int T = a.T, C = a.C;
+    // heaviest tiles first across all heads: key tile 0 meets every query
+    // block, query tile nblk-1 meets every key block
+    const int grp = (int)blockIdx.x / a.BH, bh = (int)blockIdx.x % a.BH;
+    const int tile = DKV ? grp : a.nblk - 1 - grp;
+    const int b = bh / a.NH, h = bh % a.NH;
+    const int r0 = tile * BLK;
+    const int n = DKV ? a.nblk - tile : tile + 1;  // column blocks visited
+    auto col0 = [&](int u) { return (DKV ? tile + u : u) * BLK; };
+
+    if (threadIdx.x == 0) {
+        mbar_init(fixed_full, 1);
+        for (int s = 0; s < STAGES; s++) {
+            mbar_init(st_full(s), 1);
+            mbar_init(st_empty(s), 1);
+        }
+        for (int q = 0; q < 2; q++) {
+            mbar_init(s_full(q), 1);
+            mbar_init(s_empty(q), 8);
+        }
+        mbar_init(dp_full, 1);
+        mbar_init(dp_empty, 8);
+        mbar_init(p_full, 8);
+        mbar_init(p_empty, 1);
+        mbar_init(ds_full, 8);
+        mbar_init(ds_empty, 1);
+        mbar_init(acc_full, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        *n_issued_smem = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc<1>(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish<1>();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    // warp-uniform bounded wait
+    auto wait_warp = [&](uint32_t bar, uint32_t parity) {
+        int w = 1;
+        if (lane == 0) w = mbar_wait(bar, parity, abort_flag) ? 1 : 0;
+        return __shfl_sync(0xffffffffu, w, 0) != 0;
+    };
+
+    // column offsets (elements) of Q, K, V within a row of qkv
+    const int xq = h * HSZ, xk = C + h * HSZ, xv = 2 * C + h * HSZ;
+
+    if (warp == 0) {
+        // ---------------- loads
+        int issued = 0;
+        if (lane == 0) {
+            mbar_expect_tx(fixed_full, 2 * TILE);
+            if (DKV) {
+                tma_load_3d(base + OFF_X0, &tqkv, fixed_full, xk, r0, b);
+                tma_load_3d(base + OFF_X1, &tqkv, fixed_full, xv, r0, b);
+            } else {
+                tma_load_3d(base + OFF_X0, &tqkv, fixed_full, xq, r0, b);
+                tma_load_3d(base + OFF_X1, &tdo, fixed_full, h * HSZ, r0, b);
+            }
+        }
+        for (int u = 0; u < n; u++) {
+            const int st = u % STAGES;
+            if (!wait_warp(st_empty(st), (uint32_t)(((u / STAGES) & 1) ^ 1))) break;
+            const int c0 = col0(u);
+            if (DKV) {
+                // the block's LSE (as -LSE * log2 e; -inf past the sequence end,
+                // which zeroes those columns of P) and D
+                float4 nl, dd;
+                float* pn = &nl.x;
+                float* pd = &dd.x;
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const int q = c0 + lane * 4 + e;
+                    const bool in = q < T;
+                    pn[e] = in ? -a.lse[(size_t)bh * T + q] * LOG2E : -INFINITY;
+                    pd[e] = in ? a.D[(size_t)bh * T + q] : 0.f;
+                }
+                float* vec = reinterpret_cast<float*>(base_ptr + OFF_VEC + st * 1024);
+                reinterpret_cast<float4*>(vec)[lane] = nl;
+                reinterpret_cast<float4*>(vec + 128)[lane] = dd;
+                __syncwarp();
+            }
+            if (lane == 0) {
+                const uint32_t y = base + OFF_Y + st * 2 * TILE;
+                mbar_expect_tx(st_full(st), 2 * TILE);
+                if (DKV) {
+                    tma_load_3d(y, &tqkv, st_full(st), xq, c0, b);
+                    tma_load_3d(y + TILE, &tdo, st_full(st), h * HSZ, c0, b);
+                } else {
+                    tma_load_3d(y, &tqkv, st_full(st), xk, c0, b);
+                    tma_load_3d(y + TILE, &tqkv, st_full(st), xv, c0, b);
+                }
+            }
+            ++issued;
+        }
+        if (lane == 0) *n_issued_smem = issued;
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            const uint32_t idSq = idesc<0>(0, 0, BLK, BLK);  // S, dP: both operands K-major
+            const uint32_t idAcc = idesc<0>(0, 1, BLK, HSZ); // acc += (P|dS) Y: Y is MN-major
+            const uint32_t tS0 = tmem_base, tdP = tmem_base + 256;
+            const uint32_t tA0 = tmem_base + 384, tA1 = tmem_base + 448;
+            auto ybuf = [&](int u, int which) { return base + OFF_Y + (u % STAGES) * 2 * TILE + which * TILE; };
+            auto issue_qk = [&](uint32_t d, uint32_t x, uint32_t y) {
+#pragma unroll
+                for (int k = 0; k < HSZ / 16; k++)
+                    umma<0, 1>(d, sdesc(x + k * 32, 16, 1024), sdesc(y + k * 32, 16, 1024), idSq,
+                               k ? 1u : 0u);
+            };
+            auto issue_acc = [&](uint32_t d, uint32_t pa, uint32_t y, bool accumulate) {
+#pragma unroll
+                for (int k = 0; k < BLK / 16; k++)
+                    umma<0, 1>(d, sdesc(pa + (k >> 2) * TILE + (k & 3) * 32, 16, 1024),
+                               sdesc(y + k * 2048, 8192, 1024), idAcc, (accumulate || k) ? 1u : 0u);
+            };
+            auto issue_s = [&](int u) {
+                issue_qk(tS0 + (uint32_t)((u & 1) * 128), base + OFF_X0, ybuf(u, 0));
+                umma_commit<1>(s_full(u & 1));
+            };
+            auto issue_dp = [&](int u) {
+                issue_qk(tdP, base + OFF_X1, ybuf(u, 1));
+                umma_commit<1>(dp_full);
+            };
+            bool ok = mbar_wait(fixed_full, 0, abort_flag) && mbar_wait(st_full(0), 0, abort_flag);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+                issue_dp(0);
+                if (n > 1) {
+                    ok = mbar_wait(st_full(1), 0, abort_flag);
+                    if (ok) {
+                        tc_fence_after();
+                        issue_s(1);
+                    }
+                }
+            }
+            for (int u = 0; ok && u < n; u++) {
+                const uint32_t par = (uint32_t)(u & 1);
+                if (DKV) {
+                    if (!mbar_wait(p_full, par, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_acc(tA0, base + OFF_P, ybuf(u, 1), u > 0);  // dV += P^T dO
+                    umma_commit<1>(p_empty);
+                }
+                if (u + 1 < n) {
+                    if (!mbar_wait(dp_empty, par, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_dp(u + 1);
+                }
+                if (!mbar_wait(ds_full, par, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                // DKV: dK += dS^T Q; DQ: dQ += dS K
+                issue_acc(DKV ? tA1 : tA0, base + OFF_DS, ybuf(u, 0), u > 0);
+                umma_commit<1>(ds_empty);
+                umma_commit<1>(st_empty(u % STAGES));
+                if (u + 2 < n) {
+                    if (!mbar_wait(st_full((u + 2) % STAGES), (uint32_t)(((u + 2) / STAGES) & 1), abort_flag) ||
+                        !mbar_wait(s_empty(u & 1), (uint32_t)((u >> 1) & 1), abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_s(u + 2);
+                }
+            }
+            if (ok) umma_commit<1>(acc_full);
+        }
+    } else {
+        // ---------------- P and dS
+        const int qq = warp & 3;          // TMEM lane quarter
+        const int hf = (warp - 2) >> 2;   // column half
+        const int r = qq * 32 + lane;     // row within the tile
+        const int row = r0 + r;           // key (DKV) or query (DQ)
+        const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
+        const uint32_t tdP = tmem_base + lane_off + 256 + hf * 64;
+        uint8_t* pbuf = base_ptr + OFF_P + hf * TILE + r * 128;
+        uint8_t* dsbuf = base_ptr + OFF_DS + hf * TILE + r * 128;
+        const int swz = r & 7;
+        // DQ: the row's LSE and D
+        float nl_row = -INFINITY, d_row = 0.f;
+        if (!DKV && row < T) {
+            nl_row = -a.lse[(size_t)bh * T + row] * LOG2E;
+            d_row = a.D[(size_t)bh * T + row];
+        }
+        bool ok = true;
+        for (int u = 0; u < n; u++) {
+            const int sb = u & 1, st = u % STAGES;
+            const uint32_t par = (uint32_t)(u & 1);
+            if (!wait_warp(s_full(sb), (uint32_t)((u >> 1) & 1))) { ok = false; break; }
+            tc_fence_after();
+            const float* vec = reinterpret_cast<const float*>(base_ptr + OFF_VEC + st * 1024);
+            // the diagonal block: DKV sees it first, DQ last
+            const bool diag = DKV ? u == 0 : u == n - 1;
+            const int c_base = hf * 64;
+            float P[64];
+#pragma unroll
+            for (int ch = 0; ch < 2; ch++) {
+                float v[32];
+                tmem_ld32(tmem_base + lane_off + (uint32_t)(sb * 128 + c_base + ch * 32), v);
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    const int c = c_base + ch * 32 + e;
+                    float4 nl4;
+                    if (DKV) nl4 = *reinterpret_cast<const float4*>(vec + c);
+                    else nl4 = make_float4(nl_row, nl_row, nl_row, nl_row);
+                    const float* nl = &nl4.x;
+#pragma unroll
+                    for (int f = 0; f < 4; f++) {
+                        float p = ex2_approx(fmaf(v[e + f], a.scale_log2, nl[f]));
+                        // causal: query >= key
+                        if (diag) p = (DKV ? c + f >= r : c + f <= r) ? p : 0.f;
+                        P[ch * 32 + e + f] = p;
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_empty(sb));
+            if (DKV) {
+                // P^T row r, columns c_base..c_base+63 -> atom hf, bf16
+                if (!wait_warp(p_empty, par ^ 1u)) { ok = false; break; }
+#pragma unroll
+                for (int k8 = 0; k8 < 8; k8++) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        __nv_bfloat162 pr = __floats2bfloat162_rn(P[8 * k8 + 2 * e], P[8 * k8 + 2 * e + 1]);
+                        pk[e] = *reinterpret_cast<uint32_t*>(&pr);
+                    }
+                    *reinterpret_cast<uint4*>(pbuf + ((k8 ^ swz) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full);
+            }
+            if (!wait_warp(dp_full, par)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t dsk[32];
+#pragma unroll
+            for (int ch = 0; ch < 2; ch++) {
+                float v[32];
+                tmem_ld32(tdP + (uint32_t)(ch * 32), v);
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    const int c = c_base + ch * 32 + e;
+                    float4 d4;
+                    if (DKV) d4 = *reinterpret_cast<const float4*>(vec + 128 + c);
+                    else d4 = make_float4(d_row, d_row, d_row, d_row);
+                    const int j = ch * 32 + e;
+                    __nv_bfloat162 lo = __floats2bfloat162_rn(P[j] * (v[e] - d4.x), P[j + 1] * (v[e + 1] - d4.y));
+                    __nv_bfloat162 hi =
+                        __floats2bfloat162_rn(P[j + 2] * (v[e + 2] - d4.z), P[j + 3] * (v[e + 3] - d4.w));
+                    dsk[j >> 1] = *reinterpret_cast<uint32_t*>(&lo);
+                    dsk[(j >> 1) + 1] = *reinterpret_cast<uint32_t*>(&hi);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dp_empty);
+            if (!wait_warp(ds_empty, par ^ 1u)) { ok = false; break; }
+#pragma unroll
+            for (int k8 = 0; k8 < 8; k8++)
+                *reinterpret_cast<uint4*>(dsbuf + ((k8 ^ swz) << 4)) =
+                    make_uint4(dsk[4 * k8], dsk[4 * k8 + 1], dsk[4 * k8 + 2], dsk[4 * k8 + 3]);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ds_full);
+        }
+        // epilogue: DKV writes dV (half 0) and dK (half 1) rows; DQ writes
+        // half of each dQ row per warp
+        if (ok && wait_warp(acc_full, 0u)) {
+            tc_fence_after();
+            if (DKV) {
+                float v[64];
+                const uint32_t src = tmem_base + lane_off + (hf ? 448u : 384u);
+                tmem_ld32(src, *reinterpret_cast<float(*)[32]>(v));
+                tmem_ld32(src + 32, *reinterpret_cast<float(*)[32]>(v + 32));
+                if (row < T) {
+                    const float sc = hf ? a.scale : 1.f;
+                    bf16* dst = a.dqkv + ((size_t)b * T + row) * 3 * C + (hf ? xk : xv);
+#pragma unroll
+                    for (int d = 0; d < HSZ; d += 8) {
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int e = 0; e < 4; e++) {
+                            __nv_bfloat162 pr = __floats2bfloat162_rn(v[d + 2 * e] * sc, v[d + 2 * e + 1] * sc);
+                            pk[e] = *reinterpret_cast<uint32_t*>(&pr);
+                        }
+                        *reinterpret_cast<uint4*>(dst + d) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                }
+            } else {
+                float v[32];
+                tmem_ld32(tmem_base + lane_off + 384u + (uint32_t)(hf * 32), v);
+                if (row < T) {
+                    bf16* dst = a.dqkv + ((size_t)b * T + row) * 3 * C + xq + hf * 32;
+#pragma unroll
+                    for (int d = 0; d < 32; d += 8) {
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int e = 0; e < 4; e++) {
+                            __nv_bfloat162 pr =
+                                __floats2bfloat162_rn(v[d + 2 * e] * a.scale, v[d + 2 * e + 1] * a.scale);
+                            pk[e] = *reinterpret_cast<uint32_t*>(&pr);
+                        }
+                        *reinterpret_cast<uint4*>(dst + d) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                }
+            }
+        }
+    }
+
+    __syncthreads();
+    if (*abort_flag) {
+        if (threadIdx.x == 0) {
+            // let every issued copy land before the shared memory is released
+            mbar_wait_drain(fixed_full, 0);
+            const int issued = *n_issued_smem;
+            for (int s = 0; s < STAGES; s++) {
+                if (issued > s) {
+                    const int lst = s + ((issued - 1 - s) / STAGES) * STAGES;
+                    mbar_wait_drain(st_full(s), (uint32_t)((lst / STAGES) & 1));
+                }
+            }
+            atomicOr(a.err, DEVERR_TIMEOUT);
+        }
+        if (threadIdx.x == 32) {
+            umma_commit_local<1>(drain);
+            mbar_wait_drain(drain, 0);
+        }
+        __syncthreads();
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc<1>(tmem_base, TMEM_COLS);
+    }
+}
+
+// D_i = dO_i . O_i for every (b, h, i), eight threads per row (16-byte loads)
+__global__ void rowdot64_k(float* __restrict__ D, const bf16* __restrict__ dout,
+                           const bf16* __restrict__ out, int T, int C, int NH, int nrows) {
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    const int row = idx >> 3, part = idx & 7;
+    float s = 0.f;
+    if (row < nrows) {
+        const int bh = row / T, t = row % T;
+        const int b = bh / NH, h = bh % NH;
+        const size_t off = ((size_t)b * T + t) * C + (size_t)h * HSZ + part * 8;
+        const Vec16 g = ld16(dout + off), o = ld16(out + off);
+        const bf16* gp = reinterpret_cast<const bf16*>(&g);
+        const bf16* op = reinterpret_cast<const bf16*>(&o);
+#pragma unroll
+        for (int e = 0; e < 8; e++) s = fmaf(to_f(gp[e]), to_f(op[e]), s);
+    }
+    s += __shfl_xor_sync(0xffffffffu, s, 4);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    if (row < nrows && part == 0) D[row] = s;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    });
+    return fn;
+}
+
+// (B, T, width) bf16 as a 3-D tensor (width, T, B) with 64 x 128 x 1 boxes
+static int make_map(CUtensorMap* tm, const void* p, int width, int T, int B) {
+    auto fn = encode_fn();
+    if (!fn) return set_error(GPT2_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)T, (cuuint64_t)B};
+    cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)T * width * 2};
+    cuuint32_t box[3] = {HSZ, BLK, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return set_error(GPT2_ERR_CUDA, "flash backward: tensor map encoding failed");
+    return GPT2_OK;
+}
+
+template <bool DKV> static int opt_in() {
+    static bool done = false;
+    if (done) return GPT2_OK;
+    const cudaError_t e =
+        cudaFuncSetAttribute(flash_bwd_tc_k<DKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess)
+        return set_error(GPT2_ERR_CUDA, "flash backward: shared-memory opt-in failed: %s", cudaGetErrorString(e));
+    done = true;
+    return GPT2_OK;
+}
+
+}  // namespace fabw
+
+// D = rowsum(dO * O), then dQ (query tiles) and dK, dV (key tiles)
+int launch_flash_backward_tc(void* dqkv, const void* dout, const void* qkv, const void* out,
+                             const float* lse, float* D, int B, int T, int C, int NH, cudaStream_t s,
+                             unsigned int* err) {
+    using namespace fabw;
+    if ((uintptr_t)qkv % 16 || (uintptr_t)dout % 16 || (uintptr_t)out % 16 || C % 64 || C / NH != HSZ)
+        return set_error(GPT2_ERR_ALIGN, "flash backward: 16-byte aligned operands and head size 64 needed");
+    CUtensorMap tqkv, tdo;
+    int rc = make_map(&tqkv, qkv, 3 * C, T, B);
+    if (rc == GPT2_OK) rc = make_map(&tdo, dout, C, T, B);
+    if (rc == GPT2_OK) rc = opt_in<true>();
+    if (rc == GPT2_OK) rc = opt_in<false>();
+    if (rc != GPT2_OK) return rc;
+    const int nrows = B * NH * T;
+    note_launch(3);
+    rowdot64_k<<<(nrows * 8 + 255) / 256, 256, 0, s>>>(D, (const bf16*)dout, (const bf16*)out, T, C, NH,
+                                                       nrows);
+    BwdArgs a;
+    a.dqkv = (bf16*)dqkv;
+    a.lse = lse;
+    a.D = D;
+    a.T = T;
+    a.C = C;
+    a.NH = NH;
+    a.BH = B * NH;
+    a.nblk = (T + BLK - 1) / BLK;
+    a.scale = 1.f / sqrtf((float)HSZ);
+    a.scale_log2 = LOG2E * a.scale;
+    a.err = err;
+    const int grid = a.nblk * a.BH;
+    flash_bwd_tc_k<false><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tqkv, tdo, a);
+    flash_bwd_tc_k<true><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tqkv, tdo, a);
+    return GPT2_OK;
+}
+
+}  // namespace gk

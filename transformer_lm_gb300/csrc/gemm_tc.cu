@@ -25,6 +25,7 @@
 // DEVERR_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and exits.
 #include "common.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 #include "gpt2.h"
 
@@ -45,7 +46,6 @@ constexpr int EPI_WARPS = 8;  // two per TMEM lane quarter, each owning half of 
 constexpr int EPI_THREADS = 32 * EPI_WARPS;
 constexpr int NUM_THREADS = 64 + EPI_THREADS;
 constexpr int GROUP_M = 16;  // m-blocks per rasterisation group (L2 locality of A and B)
-constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
 
 constexpr int EPI_BUFS = 2;               // epilogue staging buffers
 constexpr int EPI_BUF_BYTES = BM * ROWB;  // 128 rows x 128 bytes
@@ -80,199 +80,6 @@ struct Args {
     unsigned int* err;
 };
 
-// ------------------------------------------------------------------ PTX wrappers
-// ------------------------------------------------------------------ PTX wrappers
-DEVI uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-DEVI void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-DEVI void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-DEVI void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-DEVI bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-DEVI unsigned long long globaltimer() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-// Wait for the phase with the given parity to complete. Returns false when
-// the time limit passes (and raises the CTA's abort flag) or when another
-// role has already aborted.
-DEVI bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer() - t0 > WAIT_LIMIT_NS) {
-                *abort_flag = 1;
-                return false;
-            }
-        }
-    }
-}
-// bounded wait that ignores the abort flag (used while draining)
-DEVI bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
-    const unsigned long long t0 = globaltimer();
-    while (!mbar_try_wait(bar, parity))
-        if (globaltimer() - t0 > WAIT_LIMIT_NS) return false;
-    return true;
-}
-
-DEVI void tma_load_2d(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int x, int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-// cta_group::2 form: the bytes land in this CTA's shared memory while the
-// completion is signalled on `bar`, which may be the pair leader's barrier
-// (a shared::cluster address)
-DEVI void tma_load_2d_pair(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int x, int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-DEVI uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-DEVI void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                     : "memory");
-}
-// address of the same shared variable in CTA `rank` of the cluster
-DEVI uint32_t mapa_rank(uint32_t addr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-DEVI void mbar_arrive_cluster(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-                 : "memory");
-}
-
-// tcgen05 allocation, with the .cta_group every tcgen05 instruction of the
-// kernel shares (for 2, one warp of each CTA of the pair issues it)
-template <int CG> DEVI void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
-    if constexpr (CG == 1)
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
-                     "r"(ncols)
-                     : "memory");
-    else
-        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
-                     "r"(ncols)
-                     : "memory");
-}
-template <int CG> DEVI void tmem_relinquish() {
-    if constexpr (CG == 1)
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    else
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-template <int CG> DEVI void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    if constexpr (CG == 1)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                     : "memory");
-    else
-        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                     : "memory");
-}
-DEVI void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-DEVI void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-// arrive on `bar` once all MMAs issued so far by this thread have completed;
-// for a pair, on the barrier at that offset in both CTAs
-template <int CG> DEVI void umma_commit(uint32_t bar) {
-    if constexpr (CG == 1)
-        asm volatile(
-            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-            : "memory");
-    else
-        asm volatile(
-            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-            " [%0], %1;" ::"r"(bar),
-            "h"((uint16_t)3)
-            : "memory");
-}
-// local-only completion (drain on abort)
-template <int CG> DEVI void umma_commit_local(uint32_t bar) {
-    if constexpr (CG == 1)
-        asm volatile(
-            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-            : "memory");
-    else
-        asm volatile(
-            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-            : "memory");
-}
-
-// KIND 0: kind::f16 with bf16 operands; KIND 1: kind::tf32
-#define UMMA_ASM(GROUP, KINDS)                                                            \
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"                        \
-                 "tcgen05.mma.cta_group::" GROUP ".kind::" KINDS " [%0], %1, %2, %3, p;\n\t}\n" ::"r"( \
-                     d_tmem),                                                             \
-                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)                             \
-                 : "memory")
-template <int KIND, int CG>
-DEVI void umma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
-    if constexpr (KIND == 0 && CG == 1) UMMA_ASM("1", "f16");
-    else if constexpr (KIND == 0) UMMA_ASM("2", "f16");
-    else if constexpr (CG == 1) UMMA_ASM("1", "tf32");
-    else UMMA_ASM("2", "tf32");
-}
-#undef UMMA_ASM
-
-// 32 lanes x 32 consecutive fp32 columns; the wait is inside the same asm
-// statement so no use of the registers can be scheduled before it.
-DEVI void tmem_ld32(uint32_t taddr, float (&r)[32]) {
-    uint32_t* u = reinterpret_cast<uint32_t*>(r);
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]),
-          "=r"(u[7]), "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]),
-          "=r"(u[14]), "=r"(u[15]), "=r"(u[16]), "=r"(u[17]), "=r"(u[18]), "=r"(u[19]),
-          "=r"(u[20]), "=r"(u[21]), "=r"(u[22]), "=r"(u[23]), "=r"(u[24]), "=r"(u[25]),
-          "=r"(u[26]), "=r"(u[27]), "=r"(u[28]), "=r"(u[29]), "=r"(u[30]), "=r"(u[31])
-        : "r"(taddr)
-        : "memory");
-}
-
-DEVI void tmem_ld16(uint32_t taddr, float (&r)[16]) {
-    uint32_t* u = reinterpret_cast<uint32_t*>(r);
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15}, [%16];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]),
-          "=r"(u[7]), "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]),
-          "=r"(u[14]), "=r"(u[15])
-        : "r"(taddr)
-        : "memory");
-}
-
 // tile order: groups of GROUP_M consecutive m-blocks (m-block pairs for
 // cta_group::2) sweep all n-blocks before the next group starts
 DEVI void tile_coords(int st, int num_mg, int num_n, int group, int& mg, int& nb) {
@@ -284,50 +91,6 @@ DEVI void tile_coords(int st, int num_mg, int num_n, int group, int& mg, int& nb
     nb = idx / gm;
 }
 
-// Shared-memory matrix descriptor (tcgen05): start address, leading and
-// stride byte offsets (16-byte units), the fixed 0b001 at bits 46-48, and
-// the 128-byte swizzle mode (2) at bits 61-63. Tiles are 1024-byte aligned,
-// so the base-offset field stays 0.
-DEVI uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
-}
-
-// Instruction descriptor: D fp32 (bits 4-5 = 1), A/B format (bits 7-9,
-// 10-12: bf16 = 1 for kind::f16, tf32 = 2 for kind::tf32), A/B major
-// (bits 15/16: 1 = MN-major), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-template <int KIND>
-DEVI uint32_t idesc(int a_mn, int b_mn, int M, int N) {
-    uint32_t fmt = KIND == 0 ? 1u : 2u;
-    uint32_t d = 0;
-    d |= 1u << 4;
-    d |= fmt << 7;
-    d |= fmt << 10;
-    d |= (uint32_t)a_mn << 15;
-    d |= (uint32_t)b_mn << 16;
-    d |= (uint32_t)(N >> 3) << 17;
-    d |= (uint32_t)(M >> 4) << 24;
-    return d;
-}
-
-
-DEVI void tma_store_2d(const CUtensorMap* tm, uint32_t src, int x, int y) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                     reinterpret_cast<uint64_t>(tm)),
-                 "r"(x), "r"(y), "r"(src)
-                 : "memory");
-}
-DEVI void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-template <int N> DEVI void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-DEVI void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-DEVI void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 // barrier 1 among the epilogue threads
 DEVI void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(EPI_THREADS) : "memory"); }
 

@@ -287,8 +287,12 @@ int run_forward(Model* m, bool has_targets) {
                                        (int)BT, C, s));
         TRY(gemm(m, EPI_STORE, ln1, C, 1, P(m, 4) + (size_t)l * 3 * C * C * es, C, 1, qkv, 3 * C,
                  P(m, 5) + (size_t)l * 3 * C * es, nullptr, 0, nullptr, (int)BT, 3 * C, C));
-        TIMED(FAM_ATTN_FWD, 2.0 * B * NH * (double)T * (T + 1) * (C / NH),
-              launch_attention_forward(dt, m->tc, atty, lse, qkv, B, T, C, NH, s));
+        {
+            int rc_ = GPT2_OK;
+            TIMED(FAM_ATTN_FWD, 2.0 * B * NH * (double)T * (T + 1) * (C / NH),
+                  rc_ = launch_attention_forward(dt, m->tc, atty, lse, qkv, B, T, C, NH, s, m->d_err));
+            if (rc_ != GPT2_OK) return rc_;  // the launcher recorded the reason
+        }
         TRY(gemm(m, EPI_RESID, atty, C, 1, P(m, 6) + (size_t)l * C * C * es, C, 1, res2, C,
                  P(m, 7) + (size_t)l * C * es, resid_in, C, nullptr, (int)BT, C, C));
         TIMED(FAM_LN_FWD, ln_bytes,
@@ -371,9 +375,13 @@ int run_backward(Model* m) {
         TIMED(FAM_OTHER, 1.0 * BT * C * es,
               launch_colsum_accum(dt, G(m, 7) + (size_t)l * C * es, m->dresidual, (int)BT, C, m->ws, s));
         // attention: dqkv (B,T,3C) into the 4C scratch
-        TIMED(FAM_ATTN_BWD, 4.0 * B * NH * (double)T * (T + 1) * (C / NH),
-              launch_attention_backward(dt, m->tc, m->dbt4c, m->dbtc, qkv, atty, lse, m->attn_D, B, T,
-                                        C, NH, s));
+        {
+            int rc_ = GPT2_OK;
+            TIMED(FAM_ATTN_BWD, 4.0 * B * NH * (double)T * (T + 1) * (C / NH),
+                  rc_ = launch_attention_backward(dt, m->tc, m->dbt4c, m->dbtc, qkv, atty, lse, m->attn_D,
+                                                  B, T, C, NH, s, m->d_err));
+            if (rc_ != GPT2_OK) return rc_;
+        }
         // qkv (W: 3C x C)
         TRY(gemm(m, EPI_STORE, m->dbt4c, 3 * C, 1, P(m, 4) + (size_t)l * 3 * C * C * es, C, 0, m->dbtc,
                  C, nullptr, nullptr, 0, nullptr, (int)BT, C, 3 * C));

@@ -90,12 +90,20 @@ void launch_softmax_finish(float* y, const float* part, int M, int N, int tiles,
 
 // ---- attention (attention.cu) ----
 // qkv (B,T,3C) -> out (B,T,C), lse (B,NH,T) fp32 natural-log sum of exp of the scaled scores
-void launch_attention_forward(DType dt, int tensor_cores, void* out, float* lse, const void* qkv,
-                              int B, int T, int C, int NH, cudaStream_t s);
-// dqkv (B,T,3C) written; D scratch (B,NH,T) fp32
-void launch_attention_backward(DType dt, int tensor_cores, void* dqkv, const void* dout,
-                               const void* qkv, const void* out, const float* lse, float* D,
-                               int B, int T, int C, int NH, cudaStream_t s);
+// returns 0 or a GPT2_ERR_* code; err: device error word of the bounded waits
+int launch_attention_forward(DType dt, int tensor_cores, void* out, float* lse, const void* qkv,
+                             int B, int T, int C, int NH, cudaStream_t s, unsigned int* err);
+// tcgen05 flash forward (bf16, head size 64)
+int launch_flash_forward_tc(void* out, float* lse, const void* qkv, int B, int T, int C, int NH,
+                            cudaStream_t s, unsigned int* err);
+// dqkv (B,T,3C) written; D scratch (B,NH,T) fp32; returns 0 or a GPT2_ERR_* code
+int launch_attention_backward(DType dt, int tensor_cores, void* dqkv, const void* dout,
+                              const void* qkv, const void* out, const float* lse, float* D,
+                              int B, int T, int C, int NH, cudaStream_t s, unsigned int* err);
+// tcgen05 flash backward (bf16, head size 64): D = rowsum(dO * O), then dQ, dK, dV
+int launch_flash_backward_tc(void* dqkv, const void* dout, const void* qkv, const void* out,
+                             const float* lse, float* D, int B, int T, int C, int NH, cudaStream_t s,
+                             unsigned int* err);
 
 int num_sms();
 // records the library's last error (text and GPT2_ERR_* code); returns code

@@ -26,6 +26,12 @@ unsigned int* dev_err[kMaxDevices] = {nullptr};
 float* dev_part[kMaxDevices] = {nullptr};
 size_t dev_part_bytes[kMaxDevices] = {0};
 
+// status of the launches just issued, with CUDA's message kept for gpt2_last_error
+int launch_status() {
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? GPT2_OK : set_error(GPT2_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+}
+
 int current_device(int* dev) {
     if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices) return GPT2_ERR_CUDA;
     return GPT2_OK;
@@ -85,7 +91,7 @@ int fused_linear_bias_gelu_softmax(const float* x, const float* W, const float* 
     int rc = gemm_tc(p, DT_F32, s, err);
     if (rc != GPT2_OK) return rc;
     launch_softmax_finish(out, part, M, N, tiles, s);
-    return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+    return launch_status();
 }
 
 int gpt2_gemm(int dtype, int tensor_cores, int epilogue, const void* A, long long lda, int a_kmajor,
@@ -113,7 +119,7 @@ int gpt2_gemm(int dtype, int tensor_cores, int epilogue, const void* A, long lon
         rc = gemm_simt(p, dt, (cudaStream_t)stream);
     }
     if (rc != GPT2_OK) return rc;
-    return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+    return launch_status();
 }
 
 int gpt2_attention_forward(int dtype, int tensor_cores, const void* qkv, void* out, float* lse,
@@ -123,9 +129,14 @@ int gpt2_attention_forward(int dtype, int tensor_cores, const void* qkv, void* o
     const int HS = C / NH;
     if (HS != 16 && HS != 32 && HS != 64 && HS != 128) return GPT2_ERR_CONFIG;
     if (dtype != GPT2_FP32 && dtype != GPT2_BF16) return GPT2_ERR_CONFIG;
-    launch_attention_forward(dtype == GPT2_BF16 ? DT_BF16 : DT_F32, tensor_cores, out, lse, qkv, B,
-                             T, C, NH, (cudaStream_t)stream);
-    return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+    int dev;
+    if (current_device(&dev) != GPT2_OK) return GPT2_ERR_CUDA;
+    unsigned int* err = err_word(dev);
+    if (!err) return GPT2_ERR_NOMEM;
+    const int rc = launch_attention_forward(dtype == GPT2_BF16 ? DT_BF16 : DT_F32, tensor_cores, out,
+                                            lse, qkv, B, T, C, NH, (cudaStream_t)stream, err);
+    if (rc != GPT2_OK) return rc;
+    return launch_status();
 }
 
 int gpt2_attention_backward(int dtype, int tensor_cores, const void* dout, const void* qkv,
@@ -136,9 +147,15 @@ int gpt2_attention_backward(int dtype, int tensor_cores, const void* dout, const
     const int HS = C / NH;
     if (HS != 16 && HS != 32 && HS != 64 && HS != 128) return GPT2_ERR_CONFIG;
     if (dtype != GPT2_FP32 && dtype != GPT2_BF16) return GPT2_ERR_CONFIG;
-    launch_attention_backward(dtype == GPT2_BF16 ? DT_BF16 : DT_F32, tensor_cores, dqkv, dout, qkv,
-                              out, lse, scratch_D, B, T, C, NH, (cudaStream_t)stream);
-    return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+    int dev;
+    if (current_device(&dev) != GPT2_OK) return GPT2_ERR_CUDA;
+    unsigned int* err = err_word(dev);
+    if (!err) return GPT2_ERR_NOMEM;
+    const int rc = launch_attention_backward(dtype == GPT2_BF16 ? DT_BF16 : DT_F32, tensor_cores, dqkv,
+                                             dout, qkv, out, lse, scratch_D, B, T, C, NH,
+                                             (cudaStream_t)stream, err);
+    if (rc != GPT2_OK) return rc;
+    return launch_status();
 }
 
 int gpt2_layernorm_forward(int dtype, void* out, float* mean, float* rstd, const void* inp,
@@ -148,7 +165,7 @@ int gpt2_layernorm_forward(int dtype, void* out, float* mean, float* rstd, const
     if (N < 1 || C < 8 || C % 8 || C > (dtype == GPT2_BF16 ? 2048 : 1024)) return GPT2_ERR_ARG;
     launch_layernorm_forward(dtype == GPT2_BF16 ? DT_BF16 : DT_F32, out, mean, rstd, inp, w, b, N,
                              C, (cudaStream_t)stream);
-    return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+    return launch_status();
 }
 
 size_t gpt2_layernorm_backward_scratch_floats(int C) { return layernorm_backward_ws_floats(C); }
@@ -161,7 +178,7 @@ int gpt2_layernorm_backward(int dtype, void* dinp, void* dw, void* db, const voi
     if (N < 1 || C < 8 || C % 8 || C > (dtype == GPT2_BF16 ? 2048 : 1024)) return GPT2_ERR_ARG;
     launch_layernorm_backward(dtype == GPT2_BF16 ? DT_BF16 : DT_F32, dinp, dw, db, dout, inp, w, mean,
                               rstd, N, C, accumulate, scratch, (cudaStream_t)stream);
-    return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+    return launch_status();
 }
 
 int gpt2_device_status(void) {

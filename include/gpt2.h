@@ -200,10 +200,18 @@ int fused_linear_bias_gelu_softmax_noalloc(const float* x, const float* W, const
  *  (llm.c "train_gpt2.cu": matmul_forward_cublaslt, matmul_backward, gelu_forward,
  *  gelu_backward, residual_forward.) bias may be NULL. Tensor-core path needs
  *  16-byte aligned pointers and leading dimensions and N % (16/elem) == 0, else
- *  GPT2_ERR_ALIGN. */
+ *  GPT2_ERR_ALIGN.
+ *  ws / ws_floats: optional DEVICE fp32 scratch, caller-owned, 16-byte aligned
+ *  (NULL or 0 = none). With epilogue 4, bf16 and tensor cores, a product with
+ *  fewer output tiles than the GPU has CTA slots (a weight gradient: small
+ *  M x N, long K) may split K into ranges whose fp32 partial sums go to ws
+ *  (at most ws_floats of them) and are then added to D in range order, so the
+ *  result stays deterministic. Nothing else may use ws until the call's work
+ *  on `stream` has finished. */
 int gpt2_gemm(int dtype, int tensor_cores, int epilogue, const void* A, long long lda, int a_kmajor,
               const void* B, long long ldb, int b_kmajor, void* D, long long ldd, const void* bias,
-              const void* aux, long long ldaux, void* D2, int M, int N, int K, void* stream);
+              const void* aux, long long ldaux, void* D2, int M, int N, int K, float* ws,
+              size_t ws_floats, void* stream);
 
 /* Causal attention forward over a fused (B,T,3,NH,HS) qkv: out (B,T,NH*HS) and
  * lse (B,NH,T) fp32 natural-log sum of exp of the scaled scores (llm.c

@@ -76,6 +76,32 @@ def test_gemm_layouts_match_oracle(mode, a_km, b_km, shape):
     assert err < (8e-3 if bf16 else 1e-5), err
 
 
+@pytest.mark.parametrize("shape,a_km,b_km", [((768, 768, 8192), 0, 0), ((300, 264, 4096), 0, 0),
+                                              ((1152, 384, 6144), 0, 0), ((520, 136, 3000), 1, 1)],
+                         ids=lambda x: "x".join(map(str, x)) if isinstance(x, tuple) else str(x))
+def test_gemm_split_k_accumulate_matches_oracle(shape, a_km, b_km):
+    """D += A B^T for weight-gradient shapes (few output tiles, long K) with a
+    scratch, so that K is split into ranges reduced in order; the result must
+    match the oracle and repeat bit for bit."""
+    import torch
+    M, N, K = shape
+    A, B, bias, aux, D0 = _operands(M, N, K, 21 + M + K, True)
+    ref, _ = _ref("accum", A, B, bias, aux, D0)
+    sA, lda = _stored(A, a_km)
+    sB, ldb = _stored(B, b_km)
+    dA, dB = dev(sA, "bf16"), dev(sB, "bf16")
+    ws = torch.empty(16 * M * N + 64, dtype=torch.float32, device="cuda")
+    outs = []
+    for _ in range(2):
+        D = dev(D0, "bf16")
+        G.gpt2_gemm(G.GPT2_BF16, 1, "accum", dA, lda, a_km, dB, ldb, b_km, D, N, M=M, N=N, K=K,
+                    ws=ws, ws_floats=ws.numel())
+        G.gpt2_device_status()
+        outs.append(host(D))
+    assert rel_to_max(outs[0], ref) < 1e-2
+    assert np.array_equal(outs[0], outs[1])
+
+
 @pytest.mark.parametrize("mode", MODES, ids=lambda m: f"{m[0]}-tc{m[1]}")
 @pytest.mark.parametrize("epi", ["gelu", "resid", "gelu_bwd", "accum"])
 @pytest.mark.parametrize("shape", [(300, 392, 200), (1024, 392, 200), (2048, 264, 520)],

@@ -77,6 +77,7 @@ struct Args {
     void* D2;
     float* part;
     int part_ld;
+    int splits, kb_per;  // split-K: K ranges per tile and k-blocks per range
     unsigned int* err;
 };
 
@@ -181,7 +182,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr int NSUB = BN / SUBN;
     constexpr int BNC = BN / CG;               // rows of B this CTA holds
     constexpr bool HAS_AUX = EPI == EPI_RESID || EPI == EPI_GELU_BWD || EPI == EPI_ACCUM;
-    constexpr int OUTS = EPI == EPI_GELU ? 2 : 1;  // staging buffers per sub-tile
+    // staging buffers per sub-tile: EPI_GELU's two outputs; EPI_SPLITK's fp32
+    // sub-tile is 256 bytes wide (one buffer per column half)
+    constexpr int OUTS = (EPI == EPI_GELU || EPI == EPI_SPLITK) ? 2 : 1;
+    static_assert(EPI != EPI_SPLITK || KIND == 0, "split-K partials: bf16 operands only");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -236,6 +240,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // a pair of CTAs takes an m-block pair (rows m0 .. m0+255) of one n-block
     const int num_mg = (args.num_m + CG - 1) / CG;
     const int num_super = num_mg * args.num_n;
+    // work units: K range `split` of tile `st % num_super`, split-major so that
+    // concurrent units share their K range of A and B in L2
+    const int num_units = num_super * args.splits;
     const int group = GROUP_M / CG;
     const int cid = (int)blockIdx.x / CG, ncl = (int)gridDim.x / CG;
 
@@ -244,12 +251,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // ---------------- TMA producer (both CTAs of a pair)
             int stage = 0, n_issued = 0;
             uint32_t phase = 0;
-            for (int st = cid; st < num_super; st += ncl) {
+            for (int st = cid; st < num_units; st += ncl) {
                 int mg, nbk;
-                tile_coords(st, num_mg, args.num_n, group, mg, nbk);
+                tile_coords(st % num_super, num_mg, args.num_n, group, mg, nbk);
                 const int m0 = (mg * CG + rank) * BM, n0 = nbk * BN;
+                const int kb0 = (st / num_super) * args.kb_per;
+                const int kb1 = min(args.num_kb, kb0 + args.kb_per);
                 bool ok = true;
-                for (int kb = 0; kb < args.num_kb; kb++) {
+                for (int kb = kb0; kb < kb1; kb++) {
                     if (!mbar_wait(empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
                     const uint32_t sa = base + stage * C::STAGE_BYTES;
                     const uint32_t sb = sa + C::A_BYTES;
@@ -288,12 +297,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t id = idesc<KIND>(args.a_mn, args.b_mn, BM * CG, BN);
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
-            for (int st = cid; st < num_super; st += ncl) {
+            for (int st = cid; st < num_units; st += ncl) {
                 if (!mbar_wait(tempty(acc), acc_phase ^ 1u, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+                const int kb0 = (st / num_super) * args.kb_per;
+                const int kb1 = min(args.num_kb, kb0 + args.kb_per);
                 bool ok = true;
-                for (int kb = 0; kb < args.num_kb; kb++) {
+                for (int kb = kb0; kb < kb1; kb++) {
                     if (!mbar_wait(full(stage), phase, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t sa = base + stage * C::STAGE_BYTES;
@@ -306,7 +317,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint64_t db = args.b_mn
                                                 ? sdesc(sb + k * UK * ROWB, KE * ROWB, 1024)
                                                 : sdesc(sb + k * UK * (int)sizeof(T), 16, 1024);
-                        umma<KIND, CG>(d, da, db, id, (kb | k) ? 1u : 0u);
+                        umma<KIND, CG>(d, da, db, id, (kb > kb0 || k) ? 1u : 0u);
                     }
                     umma_commit<CG>(empty(stage));  // frees the stage in every CTA of the pair
                     if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
@@ -332,17 +343,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int last_aux_u[EPI_BUFS];  // latest aux load per buffer (elected thread)
         for (int b = 0; b < EPI_BUFS; b++) last_aux_u[b] = -1;
         if constexpr (HAS_AUX) {
-            if (elected && cid < num_super) {
+            if (elected && cid < num_units) {
                 int mg, nbk;
-                tile_coords(cid, num_mg, args.num_n, group, mg, nbk);
+                tile_coords(cid % num_super, num_mg, args.num_n, group, mg, nbk);
                 mbar_expect_tx(auxfull(0), EPI_BUF_BYTES);
                 tma_load_2d(ebuf, &tmX, auxfull(0), nbk * BN, (mg * CG + rank) * BM);
                 last_aux_u[0] = 0;
             }
         }
-        for (int st = cid; st < num_super; st += ncl) {
+        for (int st = cid; st < num_units; st += ncl) {
             int mg, nb;
-            tile_coords(st, num_mg, args.num_n, group, mg, nb);
+            tile_coords(st % num_super, num_mg, args.num_n, group, mg, nb);
+            const int split = st / num_super;
             const int m0 = (mg * CG + rank) * BM, n0 = nb * BN;
             int ok = 1;
             if (lane == 0 && !aborted) ok = mbar_wait(tfull(acc), acc_phase, abort_flag) ? 1 : 0;
@@ -362,10 +374,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         // prefetch the next sub-tile's operand into the next buffer
                         int nt = st, nj = j + 1;
                         if (nj == NSUB) { nt = st + ncl; nj = 0; }
-                        if (nt < num_super) {
+                        if (nt < num_units) {
                             const int nb1 = (u + 1) % EPI_BUFS;
                             int nmg, nnb;
-                            tile_coords(nt, num_mg, args.num_n, group, nmg, nnb);
+                            tile_coords(nt % num_super, num_mg, args.num_n, group, nmg, nnb);
                             // the store that last read buffer nb1 is done
                             bulk_wait_read<EPI_BUFS - 2>();
                             mbar_expect_tx(auxfull(nb1), EPI_BUF_BYTES);
@@ -391,16 +403,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                            ((uint32_t)(q * 32) << 16);
                     if constexpr (HALF == 32) tmem_ld32(taddr, v);
                     else tmem_ld16(taddr, v);
-                    epilogue_subtile<T, EPI>(args, v, ebuf_ptr + b0 * EPI_BUF_BYTES,
-                                             ebuf_ptr + ((b0 + 1) % EPI_BUFS) * EPI_BUF_BYTES, rl, row,
-                                             n0 + j * SUBN, hh * 4, pmax, psum);
+                    if constexpr (EPI == EPI_SPLITK) {
+                        // this half's 32 fp32 columns = one 128-byte staging row
+                        uint8_t* bp = ebuf_ptr + (b0 + hh) * EPI_BUF_BYTES + rl * ROWB;
+#pragma unroll
+                        for (int k = 0; k < 8; k++)
+                            *reinterpret_cast<float4*>(bp + ((k ^ (rl & 7)) << 4)) =
+                                make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+                    } else {
+                        epilogue_subtile<T, EPI>(args, v, ebuf_ptr + b0 * EPI_BUF_BYTES,
+                                                 ebuf_ptr + ((b0 + 1) % EPI_BUFS) * EPI_BUF_BYTES, rl,
+                                                 row, n0 + j * SUBN, hh * 4, pmax, psum);
+                    }
                 }
                 fence_async_smem();
                 epi_bar();  // staging written
                 if (elected && !aborted) {
-                    tma_store_2d(&tmD, ebuf + b0 * EPI_BUF_BYTES, n0 + j * SUBN, m0);
-                    if constexpr (EPI == EPI_GELU)
-                        tma_store_2d(&tmD2, ebuf + (b0 + 1) * EPI_BUF_BYTES, n0 + j * SUBN, m0);
+                    if constexpr (EPI == EPI_SPLITK) {
+                        // (N, M, splits) fp32 map: ragged rows clip inside their own slice
+                        tma_store_3d(&tmD, ebuf + b0 * EPI_BUF_BYTES, n0 + j * SUBN, m0, split);
+                        tma_store_3d(&tmD, ebuf + (b0 + 1) * EPI_BUF_BYTES, n0 + j * SUBN + HALF, m0, split);
+                    } else {
+                        tma_store_2d(&tmD, ebuf + b0 * EPI_BUF_BYTES, n0 + j * SUBN, m0);
+                        if constexpr (EPI == EPI_GELU)
+                            tma_store_2d(&tmD2, ebuf + (b0 + 1) * EPI_BUF_BYTES, n0 + j * SUBN, m0);
+                    }
                     bulk_commit();
                 }
             }
@@ -500,6 +527,64 @@ static bool make_map(CUtensorMap* m, const void* ptr, DType dt, uint64_t inner, 
     return r == CUDA_SUCCESS;
 }
 
+// (N, M, S) fp32 map over S consecutive M x N slices (row pitch N): the
+// split-K partials; box = box_inner x box_outer x 1, 128-byte swizzle
+static bool make_map_3d_f32(CUtensorMap* m, void* ptr, int N, int M, int S, uint32_t box_inner,
+                            uint32_t box_outer) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)M, (cuuint64_t)S};
+    cuuint64_t strides[2] = {(cuuint64_t)N * 4, (cuuint64_t)M * N * 4};
+    cuuint32_t box[3] = {box_inner, box_outer, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// D[m, n] += sum over s = 0..S-1 (in order) of ws[s][m][n]; 8 columns per thread
+__global__ void __launch_bounds__(256) splitk_reduce_k(bf16* __restrict__ D, long long ldd,
+                                                       const float* __restrict__ ws, int M, int N,
+                                                       int S) {
+    const int n8 = N / 8;
+    const long long total = (long long)M * n8;
+    const size_t slice = (size_t)M * N;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int m = (int)(i / n8), c = (int)(i % n8) * 8;
+        const float* w = ws + (size_t)m * N + c;
+        float acc[8];
+        {
+            const float4 x0 = __ldcs(reinterpret_cast<const float4*>(w));
+            const float4 x1 = __ldcs(reinterpret_cast<const float4*>(w + 4));
+            acc[0] = x0.x; acc[1] = x0.y; acc[2] = x0.z; acc[3] = x0.w;
+            acc[4] = x1.x; acc[5] = x1.y; acc[6] = x1.z; acc[7] = x1.w;
+        }
+        for (int sp = 1; sp < S; sp++) {
+            const float4 x0 = __ldcs(reinterpret_cast<const float4*>(w + sp * slice));
+            const float4 x1 = __ldcs(reinterpret_cast<const float4*>(w + sp * slice + 4));
+            acc[0] += x0.x; acc[1] += x0.y; acc[2] += x0.z; acc[3] += x0.w;
+            acc[4] += x1.x; acc[5] += x1.y; acc[6] += x1.z; acc[7] += x1.w;
+        }
+        bf16* d = D + (size_t)m * ldd + c;
+        Vec16<bf16> o = ld16(d);
+#pragma unroll
+        for (int e = 0; e < 8; e++) o.v[e] = from_f<bf16>(to_f(o.v[e]) + acc[e]);
+        st16(d, o);
+    }
+}
+
+static int launch_splitk_reduce(bf16* D, long long ldd, const float* ws, int M, int N, int S,
+                                cudaStream_t s) {
+    const long long total = (long long)M * (N / 8);
+    long long blocks = (total + 255) / 256;
+    const long long cap = (long long)num_sms() * 8;
+    if (blocks > cap) blocks = cap;
+    note_launch(1);
+    splitk_reduce_k<<<(unsigned)blocks, 256, 0, s>>>(D, ldd, ws, M, N, S);
+    return GPT2_OK;
+}
+
 struct Maps {
     CUtensorMap a, b, d, d2, x;
 };
@@ -523,7 +608,7 @@ static int launch_tc(const Maps& mp, const tc::Args& a, cudaStream_t s) {
     cfg.blockDim = dim3(tc::NUM_THREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = s;
-    const long long supers = (long long)((a.num_m + CG - 1) / CG) * a.num_n;
+    const long long supers = (long long)((a.num_m + CG - 1) / CG) * a.num_n * a.splits;
     if constexpr (CG == 1) {
         const int sms = num_sms();
         cfg.gridDim = dim3((unsigned)(supers < sms ? supers : sms));
@@ -559,6 +644,7 @@ static int dispatch_epi(int epi, const Maps& mp, const tc::Args& a, cudaStream_t
             case EPI_RESID: return launch_tc<BN, KIND, EPI_RESID, CG>(mp, a, s);
             case EPI_GELU_BWD: return launch_tc<BN, KIND, EPI_GELU_BWD, CG>(mp, a, s);
             case EPI_ACCUM: return launch_tc<BN, KIND, EPI_ACCUM, CG>(mp, a, s);
+            case EPI_SPLITK: return launch_tc<BN, KIND, EPI_SPLITK, CG>(mp, a, s);
             default: return GPT2_ERR_CONFIG;
         }
     } else {
@@ -599,14 +685,18 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
     }();
     int cg = (nm >= 2 && (nm % 2 == 0 || nm >= 8)) ? 2 : 1;
     if (force_cg == 1) cg = 1;
-    // tile width: fewer waves x narrower tiles wins; EPI_GELU_PART fixes 256
-    int BN = 256;
+    // tile width: 256 (a 256 x 256 pair tile halves the operand traffic per
+    // flop of a 256 x 128 one); 128 only for narrow outputs
+    int BN = p.N <= 128 ? 128 : 256;
     if (p.epi != EPI_GELU_PART) {
-        const long long units = cg == 2 ? sms / 2 : sms;
-        const long long nmg = (nm + cg - 1) / cg;
-        const long long t256 = nmg * ((p.N + 255) / 256), t128 = nmg * ((p.N + 127) / 128);
-        const long long c256 = ((t256 + units - 1) / units) * 256, c128 = ((t128 + units - 1) / units) * 128;
-        if (c128 < c256) BN = 128;
+        // GPT2_GEMM_BN=128|256 overrides the choice (tuning)
+        static const int force_bn = [] {
+            const char* e = getenv("GPT2_GEMM_BN");
+            return e ? atoi(e) : 0;
+        }();
+        if (force_bn == 128 || force_bn == 256) BN = force_bn;
+    } else {
+        BN = 256;
     }
     tc::Args a;
     a.M = p.M; a.N = p.N; a.K = p.K;
@@ -618,6 +708,37 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
     a.b_mn = p.b_kmajor ? 0 : 1;
     a.D = p.D; a.ldd = p.ldd; a.bias = p.bias; a.aux = p.aux; a.ldaux = p.ldaux; a.D2 = p.D2;
     a.part = p.part; a.part_ld = p.part_ld; a.err = err;
+    a.splits = 1;
+    a.kb_per = a.num_kb;
+    // Split-K for "+=" products with fewer tiles than CTA slots (the weight
+    // grads): each K range writes fp32 partials to the scratch and a second
+    // kernel adds them to D in range order (deterministic). The range count
+    // minimises a cost model: waves x (k-blocks per range + 6) x 0.25 us per
+    // 256-wide k-block, plus the partials' traffic at 5 TB/s.
+    if (p.epi == EPI_ACCUM && dt == DT_BF16 && p.ws && p.ws_floats > 0) {
+        const long long units = cg == 2 ? sms / 2 : sms;
+        const long long tiles = ((nm + cg - 1) / cg) * a.num_n;
+        const double t_kb = 0.25 * BN / 256.0, mn = (double)p.M * p.N;
+        auto est = [&](int sp) {
+            const long long kbp = (a.num_kb + sp - 1) / sp;
+            const long long waves = (tiles * sp + units - 1) / units;
+            double t = (double)waves * (double)(kbp + 6) * t_kb;
+            if (sp > 1) t += (8.0 * sp * mn + 4.0 * mn) / 5e6;
+            return t;
+        };
+        int best = 1;
+        double best_t = est(1);
+        for (int sp = 2; sp <= 16; sp++) {
+            if ((a.num_kb + sp - 1) / sp < 4) break;
+            if ((double)sp * mn > (double)p.ws_floats) break;
+            const double t = est(sp);
+            if (t < best_t * 0.97) { best = sp; best_t = t; }
+        }
+        if (best > 1) {
+            a.kb_per = (a.num_kb + best - 1) / best;
+            a.splits = (a.num_kb + a.kb_per - 1) / a.kb_per;
+        }
+    }
 
     Maps mp;
     const int SUBN = tc::ROWB / esz;
@@ -625,6 +746,16 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
                          : make_map(&mp.a, p.A, dt, p.M, p.K, p.lda, KE, KE);
     ok = ok && (p.b_kmajor ? make_map(&mp.b, p.B, dt, p.K, p.N, p.ldb, KE, BN / cg)
                            : make_map(&mp.b, p.B, dt, p.N, p.K, p.ldb, KE, KE));
+    if (a.splits > 1) {
+        ok = ok && make_map_3d_f32(&mp.d, p.ws, p.N, p.M, a.splits, 32, tc::BM);
+        mp.d2 = mp.d;
+        mp.x = mp.d;
+        if (!ok) return GPT2_ERR_CUDA;
+        const int rc = cg == 2 ? dispatch_epi<256, 0, 2>(EPI_SPLITK, mp, a, s)
+                               : dispatch_epi<256, 0, 1>(EPI_SPLITK, mp, a, s);
+        if (rc != GPT2_OK) return rc;
+        return launch_splitk_reduce((bf16*)p.D, p.ldd, p.ws, p.M, p.N, a.splits, s);
+    }
     ok = ok && make_map(&mp.d, p.D, dt, p.N, p.M, p.ldd, SUBN, tc::BM);
     ok = ok && make_map(&mp.d2, p.epi == EPI_GELU ? p.D2 : p.D, dt, p.N, p.M, p.ldd, SUBN, tc::BM);
     if (has_aux) ok = ok && make_map(&mp.x, p.aux, dt, p.N, p.M, p.ldaux, SUBN, tc::BM);

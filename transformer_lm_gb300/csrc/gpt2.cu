@@ -88,6 +88,7 @@ struct Model {
     float *ln1_mean, *ln1_rstd, *ln2_mean, *ln2_rstd, *lnf_mean, *lnf_rstd, *lse, *losses, *mean_loss;
     void *dresidual, *dbtc, *dbt4c;
     float *attn_D, *ws;
+    float* gemm_ws = nullptr;  // split-K partials of the weight-gradient GEMMs
     int *enc_counts, *enc_offsets, *enc_cursor, *enc_order, *enc_sorted;
     Timing timing;
 };
@@ -131,6 +132,10 @@ int gemm(Model* m, int epi, const void* A, long long lda, int a_km, const void* 
     p.B = B; p.ldb = ldb; p.b_kmajor = b_km;
     p.D = D; p.ldd = ldd; p.bias = bias; p.aux = aux; p.ldaux = ldaux; p.D2 = D2;
     p.M = M; p.N = N; p.K = K; p.epi = epi;
+    if (m->gemm_ws) {
+        p.ws = m->gemm_ws;
+        p.ws_floats = gemm_ws_floats(m->C);
+    }
     int rc;
     int ti = tbegin(m, FAM_GEMM, 2.0 * M * N * K);
     if (m->tc) rc = gemm_tc(p, m->dt, m->stream, m->d_err);
@@ -184,6 +189,7 @@ int alloc_acts(Model* m, int B, int T) {
         {(void**)&m->mean_loss, 256}, {&m->dresidual, BT * C * es}, {&m->dbtc, BT * C * es},
         {&m->dbt4c, BT * 4 * C * es}, {(void**)&m->attn_D, (size_t)B * NH * T * 4},
         {(void**)&m->ws, 4 * std::max(layernorm_backward_ws_floats(m->C), colsum_ws_floats(4 * m->C))},
+        {(void**)&m->gemm_ws, 4 * gemm_ws_floats(m->C)},
         {(void**)&m->enc_counts, (size_t)m->Vp * 4}, {(void**)&m->enc_offsets, ((size_t)m->Vp + 1) * 4},
         {(void**)&m->enc_cursor, (size_t)m->Vp * 4}, {(void**)&m->enc_order, BT * 4},
         {(void**)&m->enc_sorted, BT * 4},

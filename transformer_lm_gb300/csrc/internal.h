@@ -23,7 +23,8 @@ enum DType { DT_F32 = 0, DT_BF16 = 1 };
 //  EPI_ACCUM     D = D + acc                               (parameter-gradient +=)
 //  EPI_GELU_PART D = gelu(acc + bias[n]); part[m][tile] = (max, sum exp(D - max)) over the tile
 enum Epi { EPI_STORE = 0, EPI_GELU = 1, EPI_RESID = 2, EPI_GELU_BWD = 3, EPI_ACCUM = 4,
-           EPI_GELU_PART = 5 };
+           EPI_GELU_PART = 5,
+           EPI_SPLITK = 6 };  // internal to gemm_tc: fp32 partial sums of one K range
 
 // D[M,N] = A[M,K] . B[N,K]^T with operands given by their storage order:
 //  a_kmajor: A(m,k) = A[m*lda + k], else A(m,k) = A[k*lda + m]
@@ -37,9 +38,13 @@ struct GemmParams {
     const void* aux; long long ldaux;
     void* D2;
     float* part; int part_ld;  // EPI_GELU_PART: float2 partials, part_ld tiles per row
+    float* ws; size_t ws_floats;  // optional fp32 scratch: lets EPI_ACCUM split K (0 = never)
     int M, N, K;
     int epi;
 };
+
+// fp32 split-K scratch the model gives its GEMMs: four (4C x C) slices
+inline size_t gemm_ws_floats(int C) { return (size_t)16 * C * C; }
 
 // SIMT (FP32 FMA) GEMM, dtype = element type of A, B, D, bias, aux.
 int gemm_simt(const GemmParams& p, DType dt, cudaStream_t s);

@@ -96,7 +96,8 @@ int fused_linear_bias_gelu_softmax(const float* x, const float* W, const float* 
 
 int gpt2_gemm(int dtype, int tensor_cores, int epilogue, const void* A, long long lda, int a_kmajor,
               const void* B, long long ldb, int b_kmajor, void* D, long long ldd, const void* bias,
-              const void* aux, long long ldaux, void* D2, int M, int N, int K, void* stream) {
+              const void* aux, long long ldaux, void* D2, int M, int N, int K, float* ws,
+              size_t ws_floats, void* stream) {
     if (!A || !B || !D) return GPT2_ERR_ARG;
     if (dtype != GPT2_FP32 && dtype != GPT2_BF16) return GPT2_ERR_CONFIG;
     if (epilogue < EPI_STORE || epilogue > EPI_ACCUM) return GPT2_ERR_ARG;
@@ -107,6 +108,8 @@ int gpt2_gemm(int dtype, int tensor_cores, int epilogue, const void* A, long lon
     p.B = B; p.ldb = ldb; p.b_kmajor = b_kmajor ? 1 : 0;
     p.D = D; p.ldd = ldd; p.bias = bias; p.aux = aux; p.ldaux = ldaux; p.D2 = D2;
     p.M = M; p.N = N; p.K = K; p.epi = epilogue;
+    if (ws && ((uintptr_t)ws & 15u)) return GPT2_ERR_ALIGN;
+    p.ws = ws; p.ws_floats = ws ? ws_floats : 0;
     const DType dt = dtype == GPT2_BF16 ? DT_BF16 : DT_F32;
     int rc;
     if (tensor_cores) {

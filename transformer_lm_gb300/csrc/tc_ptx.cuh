@@ -293,6 +293,12 @@ DEVI void tma_store_2d(const CUtensorMap* tm, uint32_t src, int x, int y) {
                  "r"(x), "r"(y), "r"(src)
                  : "memory");
 }
+DEVI void tma_store_3d(const CUtensorMap* tm, uint32_t src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(x), "r"(y), "r"(z), "r"(src)
+                 : "memory");
+}
 DEVI void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 template <int N> DEVI void bulk_wait_read() {
     asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");

@@ -76,7 +76,7 @@ _SIGS = {
     "fused_linear_bias_gelu_softmax": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]),
     "fused_linear_bias_gelu_softmax_noalloc": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]),
     "gpt2_gemm": (_i, [_i, _i, _i, _vp, _ll, _i, _vp, _ll, _i, _vp, _ll, _vp, _vp, _ll, _vp, _i, _i,
-                       _i, _vp]),
+                       _i, _vp, _sz, _vp]),
     "gpt2_attention_forward": (_i, [_i, _i, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "gpt2_attention_backward": (_i, [_i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "gpt2_device_status": (_i, []),
@@ -272,11 +272,13 @@ def fused_linear_bias_gelu_softmax_noalloc(x, W, b, out, M, K, N, stream=None) -
 
 
 def gpt2_gemm(dtype, tensor_cores, epilogue, A, lda, a_kmajor, B, ldb, b_kmajor, D, ldd, bias=None,
-              aux=None, ldaux=0, D2=None, M=0, N=0, K=0, stream=None) -> None:
+              aux=None, ldaux=0, D2=None, M=0, N=0, K=0, ws=None, ws_floats=0,
+              stream=None) -> None:
     epi = EPI[epilogue] if isinstance(epilogue, str) else epilogue
     _check("gpt2_gemm", lib().gpt2_gemm(dtype, tensor_cores, epi, ptr(A), lda, int(a_kmajor), ptr(B),
                                         ldb, int(b_kmajor), ptr(D), ldd, ptr(bias), ptr(aux), ldaux,
-                                        ptr(D2), M, N, K, stream))
+                                        ptr(D2), M, N, K, ptr(ws), ws_floats if ws is not None else 0,
+                                        stream))
 
 
 def gpt2_attention_forward(dtype, tensor_cores, qkv, out, lse, B, T, C, NH, stream=None) -> None:

@@ -231,25 +231,27 @@ def run_ours(args):
     G.gpt2_set_stream(stream.cuda_stream)
     tok = inputs.tokens(42 + rank, 1, B, T, V)
     tgt = inputs.tokens(42 + rank, 2, B, T, V)
-    d_tok = torch.from_numpy(tok).cuda()
-    d_tgt = torch.from_numpy(tgt).cuda()
+    d_tok = torch.from_numpy(tok.reshape(-1)).cuda()
+    d_tgt = torch.from_numpy(tgt.reshape(-1)).cuda()
     d_loss = torch.zeros(1, device="cuda")
     step_no = [0]
 
+    # pinned host copies of the batch for the end-to-end leg
+    h_tok = torch.from_numpy(tok.reshape(-1)).pin_memory()
+    h_tgt = torch.from_numpy(tgt.reshape(-1)).pin_memory()
+
     def device_step():
+        # forward + zero_grad + backward + AdamW; replayed from a CUDA graph
+        # once the first call has recorded it
         step_no[0] += 1
-        G.gpt2_forward_device(d_tok, d_tgt, B, T, d_loss)
-        G.gpt2_zero_grad()
-        G.gpt2_backward()
-        G.gpt2_adamw(LR, B1, B2, EPS, WD, step_no[0])
+        G.gpt2_train_step(d_tok, d_tgt, B, T, LR, B1, B2, EPS, WD, step_no[0], d_loss)
 
     def host_step():
-        step_no[0] += 1
-        loss = G.gpt2_forward(tok, tgt, B, T)
-        G.gpt2_zero_grad()
-        G.gpt2_backward()
-        G.gpt2_adamw(LR, B1, B2, EPS, WD, step_no[0])
-        return loss
+        # the batch goes up from pinned host memory and the loss comes back
+        d_tok.copy_(h_tok, non_blocking=True)
+        d_tgt.copy_(h_tgt, non_blocking=True)
+        device_step()
+        return float(d_loss.item())
 
     for _ in range(args.warmup):
         device_step()

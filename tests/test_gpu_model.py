@@ -262,6 +262,48 @@ def test_device_input_forward_matches_host_input_forward():
     G.gpt2_free()
 
 
+def test_train_step_graph_replays_match_eager_steps():
+    """gpt2_train_step (eager first call, CUDA-graph replays after) gives the
+    same parameters and losses, bit for bit, as the four calls it stands for,
+    with the learning rate changing every step and the token buffer refilled
+    in place between steps."""
+    import torch
+    d = SMALL_BF16
+    B, T = 2, 128
+    params = inputs.round_to_bf16(inputs.gpt2_params(d, 14, perturb=True))
+    batches = [(inputs.tokens(14, 2 * i + 1, B, T, d.V), inputs.tokens(14, 2 * i + 2, B, T, d.V))
+               for i in range(4)]
+    lrs = [6e-4, 3e-4, 1e-4, 5e-4]
+    dt = torch.zeros(B * T, dtype=torch.int32, device="cuda")
+    dg = torch.zeros(B * T, dtype=torch.int32, device="cuda")
+    dl = torch.zeros(1, device="cuda")
+
+    def run(use_graph):
+        _init(d, G.GPT2_BF16, 1, params)
+        losses = []
+        for i, (tok, tgt) in enumerate(batches):
+            dt.copy_(torch.from_numpy(tok.reshape(-1)))
+            dg.copy_(torch.from_numpy(tgt.reshape(-1)))
+            if use_graph:
+                G.gpt2_train_step(dt, dg, B, T, lrs[i], 0.9, 0.95, 1e-8, 0.1, i + 1, dl)
+            else:
+                G.gpt2_forward_device(dt, dg, B, T, dl)
+                G.gpt2_zero_grad()
+                G.gpt2_backward()
+                G.gpt2_adamw(lrs[i], 0.9, 0.95, 1e-8, 0.1, i + 1)
+            G.gpt2_sync()
+            losses.append(float(dl.item()))
+        out = (losses, G.gpt2_get_params(), G.gpt2_get_master())
+        G.gpt2_free()
+        return out
+
+    l_e, p_e, m_e = run(False)
+    l_g, p_g, m_g = run(True)
+    assert l_e == l_g
+    assert np.array_equal(p_e, p_g)
+    assert np.array_equal(m_e, m_g)
+
+
 def test_init_distribution():
     d = inputs.GPT2Dims(L=2, C=256, NH=4, V=1000, Vp=1024, maxT=64)
     G.gpt2_init(d.L, d.C, d.NH, d.V, d.Vp, d.maxT, 1337)

@@ -89,6 +89,15 @@ struct Model {
     void *dresidual, *dbtc, *dbt4c;
     float *attn_D, *ws;
     float* gemm_ws = nullptr;  // split-K partials of the weight-gradient GEMMs
+    // gpt2_train_step: the captured step and what it was captured for
+    float* d_hyper = nullptr;  // AdamW hyperparameters read by the replayed update
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t graph_exec = nullptr;
+    const int* g_tokens = nullptr;
+    const int* g_targets = nullptr;
+    float* g_loss = nullptr;
+    int g_B = 0, g_T = 0, g_accum = 0;
+    long long g_launches = 0;  // kernel launches one replay makes
     int *enc_counts, *enc_offsets, *enc_cursor, *enc_order, *enc_sorted;
     Timing timing;
 };
@@ -164,6 +173,9 @@ void free_model(Model* m) {
     cudaFree(m->mom_m);
     cudaFree(m->mom_v);
     cudaFree(m->d_err);
+    cudaFree(m->d_hyper);
+    if (m->graph_exec) cudaGraphExecDestroy(m->graph_exec);
+    if (m->graph) cudaGraphDestroy(m->graph);
     for (cudaEvent_t e : m->timing.ev) cudaEventDestroy(e);
     if (m->own_stream) cudaStreamDestroy(m->own_stream);
     delete m;
@@ -437,6 +449,20 @@ int to_host_f32(Model* m, float* host, const void* src, size_t n, DType dt) {
 
 }  // namespace
 
+namespace {
+int run_adamw(Model* m, float lr, float beta1, float beta2, float eps, float weight_decay, int step,
+              const float* hyper) {
+    const float c1 = 1.0f - powf(beta1, (float)step);
+    const float c2 = 1.0f - powf(beta2, (float)step);
+    const double bytes = (double)m->nparams * (m->master ? (2 * m->esz + 24) : (4.0 * 7));
+    TIMED(FAM_ADAMW, bytes,
+          launch_adamw(m->dt, m->params, m->master, m->grads, m->mom_m, m->mom_v, m->nparams, lr,
+                       beta1, beta2, c1, c2, eps, weight_decay, hyper, m->stream));
+    CUDA_TRY(cudaGetLastError());
+    return GPT2_OK;
+}
+}  // namespace
+
 int gk::set_error(int code, const char* fmt, ...) {
     g_status = code;
     va_list ap;
@@ -503,6 +529,7 @@ int gpt2_init_ex(int L, int C, int NH, int V, int Vp, int maxT, unsigned long lo
               cudaMalloc((void**)&m->mom_m, off * 4 + 256) == cudaSuccess &&
               cudaMalloc((void**)&m->mom_v, off * 4 + 256) == cudaSuccess &&
               cudaMalloc((void**)&m->d_err, 256) == cudaSuccess &&
+              cudaMalloc((void**)&m->d_hyper, 256) == cudaSuccess &&
               (precision == GPT2_FP32 || cudaMalloc((void**)&m->master, off * 4 + 256) == cudaSuccess);
     if (!ok) {
         free_model(m);
@@ -620,14 +647,75 @@ int gpt2_backward(void) {
 int gpt2_adamw(float lr, float beta1, float beta2, float eps, float weight_decay, int step) {
     TRY(check_model());
     if (step < 1) return fail(GPT2_ERR_ARG, "step=%d must be >= 1", step);
+    return run_adamw(g, lr, beta1, beta2, eps, weight_decay, step, nullptr);
+}
+
+// The whole step as CUDA graph replays. The first call with a given set of
+// buffers, shape and accumulation count runs the step eagerly (which also
+// performs every allocation and one-time set-up) and then records the same
+// launches into a graph; later calls write the AdamW hyperparameters to
+// device memory with one tiny kernel and replay the graph.
+int gpt2_train_step(const int* d_tokens, const int* d_targets, int B, int T, float lr, float beta1,
+                    float beta2, float eps, float weight_decay, int step, float* d_mean_loss) {
+    TRY(check_model());
     Model* m = g;
-    const float c1 = 1.0f - powf(beta1, (float)step);
-    const float c2 = 1.0f - powf(beta2, (float)step);
-    const double bytes = (double)m->nparams * (m->master ? (2 * m->esz + 24) : (4.0 * 7));
-    TIMED(FAM_ADAMW, bytes,
-          launch_adamw(m->dt, m->params, m->master, m->grads, m->mom_m, m->mom_v, m->nparams, lr,
-                       beta1, beta2, c1, c2, eps, weight_decay, m->stream));
-    CUDA_TRY(cudaGetLastError());
+    if (!d_tokens || !d_targets) return fail(GPT2_ERR_ARG, "tokens and targets are required");
+    if (step < 1) return fail(GPT2_ERR_ARG, "step=%d must be >= 1", step);
+    TRY(check_shape(m, B, T));
+    const bool same = m->graph_exec && m->g_tokens == d_tokens && m->g_targets == d_targets &&
+                      m->g_loss == d_mean_loss && m->g_B == B && m->g_T == T &&
+                      m->g_accum == m->grad_accum;
+    if (same && !m->timing.on) {
+        const float c1 = 1.0f - powf(beta1, (float)step), c2 = 1.0f - powf(beta2, (float)step);
+        launch_set_hyper(m->d_hyper, lr, beta1, beta2, c1, c2, eps, weight_decay, m->stream);
+        CUDA_TRY(cudaGraphLaunch(m->graph_exec, m->stream));
+        note_launch((int)m->g_launches);
+        m->fwd_done = 1;
+        m->fwd_targets = 0;
+        return GPT2_OK;
+    }
+    // eager step
+    TRY(gpt2_forward_device(d_tokens, d_targets, B, T, d_mean_loss));
+    TRY(gpt2_zero_grad());
+    TRY(gpt2_backward());
+    TRY(run_adamw(m, lr, beta1, beta2, eps, weight_decay, step, nullptr));
+    if (m->timing.on) return GPT2_OK;  // timing events are not recorded into graphs
+    // record the step for the next calls
+    if (m->graph_exec) cudaGraphExecDestroy(m->graph_exec);
+    if (m->graph) cudaGraphDestroy(m->graph);
+    m->graph_exec = nullptr;
+    m->graph = nullptr;
+    const long long l0 = launch_count();
+    CUDA_TRY(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal));
+    int rc = gpt2_forward_device(d_tokens, d_targets, B, T, d_mean_loss);
+    if (rc == GPT2_OK) rc = gpt2_zero_grad();
+    if (rc == GPT2_OK) rc = gpt2_backward();
+    if (rc == GPT2_OK) rc = run_adamw(m, lr, beta1, beta2, eps, weight_decay, step, m->d_hyper);
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamEndCapture(m->stream, &graph);
+    if (rc != GPT2_OK || e != cudaSuccess) {
+        if (graph) cudaGraphDestroy(graph);
+        cudaGetLastError();
+        return rc != GPT2_OK ? rc : fail(GPT2_ERR_CUDA, "step capture failed: %s", cudaGetErrorString(e));
+    }
+    e = cudaGraphInstantiate(&m->graph_exec, graph, 0);
+    if (e != cudaSuccess) {
+        cudaGraphDestroy(graph);
+        m->graph_exec = nullptr;
+        return fail(GPT2_ERR_CUDA, "step graph instantiation failed: %s", cudaGetErrorString(e));
+    }
+    m->graph = graph;
+    m->g_launches = launch_count() - l0;
+    m->g_tokens = d_tokens;
+    m->g_targets = d_targets;
+    m->g_loss = d_mean_loss;
+    m->g_B = B;
+    m->g_T = T;
+    m->g_accum = m->grad_accum;
+    // the capture recorded launches but ran nothing; undo its count
+    note_launch(-(int)m->g_launches);
+    m->fwd_done = 1;
+    m->fwd_targets = 0;
     return GPT2_OK;
 }
 

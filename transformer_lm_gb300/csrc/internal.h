@@ -81,9 +81,14 @@ size_t colsum_ws_floats(int N);
 void launch_classifier(DType dt, void* logits, float* losses, const int* targets, int BT, int V,
                        int Vp, float dloss, cudaStream_t s);
 void launch_mean(const float* x, int n, float* out, cudaStream_t s);
+// hyper: NULL, or device floats {lr, b1, b2, c1, c2, eps, wd} that replace the
+// by-value ones (a CUDA graph replays the launch with new values there)
 void launch_adamw(DType dt, void* params, float* master, const void* grads, float* m, float* v,
                   size_t n, float lr, float b1, float b2, float c1, float c2, float eps, float wd,
-                  cudaStream_t s);
+                  const float* hyper, cudaStream_t s);
+// writes {lr, b1, b2, c1, c2, eps, wd} to h with a one-thread kernel
+void launch_set_hyper(float* h, float lr, float b1, float b2, float c1, float c2, float eps, float wd,
+                      cudaStream_t s);
 void launch_zero(void* p, size_t bytes, cudaStream_t s);
 void launch_init_normal(DType dt, void* p, size_t n, float stddev, unsigned long long seed,
                         unsigned long long stream_id, cudaStream_t s);

@@ -427,6 +427,128 @@ __global__ void __launch_bounds__(LNB_BLOCK) layernorm_backward_k(
     }
 }
 
+// Same operation for bf16 rows of at most 32 * 8 * NV columns, built for
+// memory-level parallelism: each lane keeps its weights and its dw/db column
+// partials in registers and loads the warp's next row while it computes the
+// current one, so every warp has two rows of loads in flight and nothing is
+// read twice. The block folds its warps in order through shared memory and
+// writes one partial row to ws (reduce_partials_k sums the blocks in order).
+template <int NV>
+__global__ void __launch_bounds__(LNB_BLOCK, 1) layernorm_backward_reg_k(
+    bf16* __restrict__ dinp, float* __restrict__ ws, const bf16* __restrict__ dout,
+    const bf16* __restrict__ inp, const bf16* __restrict__ w, const float* __restrict__ mean,
+    const float* __restrict__ rstd, int N, int C, int accumulate) {
+    constexpr int VEC = 8;
+    extern __shared__ float sm[];
+    const int warps = blockDim.x / 32;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    const int cv = C / VEC;
+    float wf[NV][VEC], adw[NV][VEC], adb[NV][VEC];
+#pragma unroll
+    for (int j = 0; j < NV; j++) {
+        const int vi = lane + 32 * j;
+        Vec16<bf16> wv;
+        if (vi < cv) wv = ld16(w + vi * VEC);
+#pragma unroll
+        for (int k = 0; k < VEC; k++) {
+            wf[j][k] = vi < cv ? to_f(wv.v[k]) : 0.f;
+            adw[j][k] = 0.f;
+            adb[j][k] = 0.f;
+        }
+    }
+    const int stride = gridDim.x * warps;
+    int row = blockIdx.x * warps + warp;
+    Vec16<bf16> xa[NV], da[NV];
+    float mu = 0.f, rs = 0.f;
+    auto load_row = [&](int r, Vec16<bf16> (&xv)[NV], Vec16<bf16> (&dv)[NV], float& m, float& sd) {
+        const bf16* x = inp + (size_t)r * C;
+        const bf16* dy = dout + (size_t)r * C;
+#pragma unroll
+        for (int j = 0; j < NV; j++) {
+            const int vi = lane + 32 * j;
+            if (vi < cv) {
+                xv[j] = ld16_cs(x + vi * VEC);
+                dv[j] = ld16_cs(dy + vi * VEC);
+            }
+        }
+        m = mean[r];
+        sd = rstd[r];
+    };
+    if (row < N) load_row(row, xa, da, mu, rs);
+    while (row < N) {
+        const int nrow = row + stride;
+        Vec16<bf16> xb[NV], db2[NV];
+        float mu2 = 0.f, rs2 = 0.f;
+        if (nrow < N) load_row(nrow, xb, db2, mu2, rs2);
+        bf16* dx = dinp + (size_t)row * C;
+        Vec16<bf16> old[NV];
+        if (accumulate) {
+#pragma unroll
+            for (int j = 0; j < NV; j++)
+                if (lane + 32 * j < cv) old[j] = ld16(dx + (lane + 32 * j) * VEC);
+        }
+        float gsum = 0.f, gnsum = 0.f;
+#pragma unroll
+        for (int j = 0; j < NV; j++) {
+            if (lane + 32 * j < cv) {
+#pragma unroll
+                for (int k = 0; k < VEC; k++) {
+                    const float g = wf[j][k] * to_f(da[j].v[k]);
+                    gsum += g;
+                    gnsum += g * (to_f(xa[j].v[k]) - mu) * rs;
+                }
+            }
+        }
+        gsum = warp_sum(gsum) / C;
+        gnsum = warp_sum(gnsum) / C;
+#pragma unroll
+        for (int j = 0; j < NV; j++) {
+            const int vi = lane + 32 * j;
+            if (vi < cv) {
+                Vec16<bf16> o;
+#pragma unroll
+                for (int k = 0; k < VEC; k++) {
+                    const float d = to_f(da[j].v[k]);
+                    const float nh = (to_f(xa[j].v[k]) - mu) * rs;
+                    const float val = rs * (wf[j][k] * d - gsum - nh * gnsum);
+                    o.v[k] = from_f<bf16>(accumulate ? to_f(old[j].v[k]) + val : val);
+                    adw[j][k] += nh * d;
+                    adb[j][k] += d;
+                }
+                st16(dx + vi * VEC, o);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < NV; j++) {
+            xa[j] = xb[j];
+            da[j] = db2[j];
+        }
+        mu = mu2;
+        rs = rs2;
+        row = nrow;
+    }
+    // fold the warps in order: sm[warp][dw | db][column]
+    float* mine = sm + (size_t)warp * 2 * C;
+#pragma unroll
+    for (int j = 0; j < NV; j++) {
+        const int vi = lane + 32 * j;
+        if (vi < cv) {
+#pragma unroll
+            for (int k = 0; k < VEC; k++) {
+                mine[vi * VEC + k] = adw[j][k];
+                mine[C + vi * VEC + k] = adb[j][k];
+            }
+        }
+    }
+    __syncthreads();
+    float* dst = ws + (size_t)blockIdx.x * 2 * C;
+    for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) {
+        float t = 0.f;
+        for (int wi = 0; wi < warps; wi++) t += sm[(size_t)wi * 2 * C + c];
+        dst[c] = t;
+    }
+}
+
 // dst[c] += sum over p of ws[p][c] for c in [0, W), summed in increasing p;
 // columns [split, W) go to dst2[c - split]. One warp per (32-column group,
 // p residue mod 8), folded across the 8 warps in order.
@@ -471,6 +593,15 @@ static int lnb_blocks(int N, size_t smem) {
     return g < cap ? (g < 1 ? 1 : g) : cap;
 }
 
+template <int NV> static void lnr_opt_in(size_t smem) {
+    static size_t done = 0;
+    if (smem > done) {
+        cudaFuncSetAttribute(layernorm_backward_reg_k<NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+        done = smem;
+    }
+}
+
 size_t layernorm_backward_ws_floats(int C) { return (size_t)4 * num_sms() * 2 * C; }
 
 void launch_layernorm_backward(DType dt, void* dinp, void* dw, void* db, const void* dout,
@@ -494,7 +625,23 @@ void launch_layernorm_backward(DType dt, void* dinp, void* dw, void* db, const v
         case 7: LNB(TT, 7); break; default: LNB(TT, 8); break;                                \
     }
     const unsigned rg = (unsigned)((2 * C + 31) / 32);
-    if (dt == DT_BF16) {
+    if (dt == DT_BF16 && nv <= 4) {
+        // one block per SM: its 8 warps keep two rows of loads in flight each
+        const int rows_per_block = LNB_BLOCK / 32;
+        P = (N + rows_per_block - 1) / rows_per_block;
+        if (P > num_sms()) P = num_sms();
+        if (P < 1) P = 1;
+#define LNR(NVV)                                                                                    \
+    lnr_opt_in<NVV>(smem);                                                                           \
+    layernorm_backward_reg_k<NVV><<<P, LNB_BLOCK, smem, s>>>((bf16*)dinp, ws, (const bf16*)dout,     \
+                                                          (const bf16*)inp, (const bf16*)w, mean,   \
+                                                          rstd, N, C, accumulate)
+        switch (nv) {
+            case 1: LNR(1); break; case 2: LNR(2); break; case 3: LNR(3); break; default: LNR(4); break;
+        }
+#undef LNR
+        reduce_partials_k<bf16><<<rg, 256, 0, s>>>((bf16*)dw, (bf16*)db, C, ws, P, 2 * C);
+    } else if (dt == DT_BF16) {
         LNB_ALL(bf16);
         reduce_partials_k<bf16><<<rg, 256, 0, s>>>((bf16*)dw, (bf16*)db, C, ws, P, 2 * C);
     } else {
@@ -509,7 +656,7 @@ void launch_layernorm_backward(DType dt, void* dinp, void* dw, void* db, const v
 // matmul_backward_bias_kernel4 read with +=: dbias[n] += sum over rows of dout[:, n].
 // Stage 1: block (x: 32*VEC columns, y: a slab of rows), 8 warps stride the
 // slab, warps folded in order; stage 2 (reduce_partials_k) sums the slabs in order.
-constexpr int CS_SLABS = 64;
+constexpr int CS_SLABS = 128;
 
 template <typename T>
 __global__ void __launch_bounds__(256) colsum_partial_k(float* __restrict__ ws,
@@ -525,10 +672,20 @@ __global__ void __launch_bounds__(256) colsum_partial_k(float* __restrict__ ws,
 #pragma unroll
     for (int k = 0; k < VEC; k++) acc[k] = 0.f;
     if (col < N) {
-        for (int r = r0 + warp; r < r1; r += 8) {
-            Vec16<T> d = ld16(dout + (size_t)r * N + col);
+        const T* p = dout + col;
+        int r = r0 + warp;
+        // four independent rows per iteration keep four loads in flight per lane
+        for (; r + 24 < r1; r += 32) {
+            const Vec16<T> a = ld16_cs(p + (size_t)r * N), b = ld16_cs(p + (size_t)(r + 8) * N);
+            const Vec16<T> c = ld16_cs(p + (size_t)(r + 16) * N), d = ld16_cs(p + (size_t)(r + 24) * N);
 #pragma unroll
-            for (int k = 0; k < VEC; k++) acc[k] += to_f(d.v[k]);
+            for (int k = 0; k < VEC; k++)
+                acc[k] += (to_f(a.v[k]) + to_f(b.v[k])) + (to_f(c.v[k]) + to_f(d.v[k]));
+        }
+        for (; r < r1; r += 8) {
+            const Vec16<T> a = ld16_cs(p + (size_t)r * N);
+#pragma unroll
+            for (int k = 0; k < VEC; k++) acc[k] += to_f(a.v[k]);
         }
     }
 #pragma unroll
@@ -548,7 +705,7 @@ void launch_colsum_accum(DType dt, void* dbias, const void* dout, int M, int N, 
                          cudaStream_t s) {
     note_launch(2);
     const int VEC = dt == DT_BF16 ? 8 : 4;
-    int R = (M + 7) / 8;
+    int R = (M + 31) / 32;
     if (R > CS_SLABS) R = CS_SLABS;
     if (R < 1) R = 1;
     int rps = (M + R - 1) / R;
@@ -677,7 +834,11 @@ template <typename T>
 __global__ void adamw_k(T* __restrict__ params, float* __restrict__ master,
                         const T* __restrict__ grads, float* __restrict__ mst,
                         float* __restrict__ vst, size_t n, float lr, float b1, float b2, float c1,
-                        float c2, float eps, float wd) {
+                        float c2, float eps, float wd, const float* __restrict__ hyper) {
+    if (hyper) {  // hyperparameters from device memory (graph replays)
+        lr = hyper[0]; b1 = hyper[1]; b2 = hyper[2]; c1 = hyper[3]; c2 = hyper[4];
+        eps = hyper[5]; wd = hyper[6];
+    }
     const size_t stride = (size_t)gridDim.x * blockDim.x * 4;
     for (size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4; i < n; i += stride) {
         if (i + 4 <= n) {
@@ -733,15 +894,26 @@ __global__ void adamw_k(T* __restrict__ params, float* __restrict__ master,
 
 void launch_adamw(DType dt, void* params, float* master, const void* grads, float* m, float* v,
                   size_t n, float lr, float b1, float b2, float c1, float c2, float eps, float wd,
-                  cudaStream_t s) {
+                  const float* hyper, cudaStream_t s) {
     note_launch(1);
     unsigned g = grid_for((n + 3) / 4, 256, 8);
     if (dt == DT_BF16)
         adamw_k<bf16><<<g, 256, 0, s>>>((bf16*)params, master, (const bf16*)grads, m, v, n, lr, b1,
-                                        b2, c1, c2, eps, wd);
+                                        b2, c1, c2, eps, wd, hyper);
     else
         adamw_k<float><<<g, 256, 0, s>>>((float*)params, master, (const float*)grads, m, v, n, lr,
-                                         b1, b2, c1, c2, eps, wd);
+                                         b1, b2, c1, c2, eps, wd, hyper);
+}
+
+__global__ void set_hyper_k(float* h, float lr, float b1, float b2, float c1, float c2, float eps,
+                            float wd) {
+    h[0] = lr; h[1] = b1; h[2] = b2; h[3] = c1; h[4] = c2; h[5] = eps; h[6] = wd;
+}
+
+void launch_set_hyper(float* h, float lr, float b1, float b2, float c1, float c2, float eps, float wd,
+                      cudaStream_t s) {
+    note_launch(1);
+    set_hyper_k<<<1, 1, 0, s>>>(h, lr, b1, b2, c1, c2, eps, wd);
 }
 
 // ------------------------------------------------------------------ utilities

@@ -80,6 +80,7 @@ _SIGS = {
     "gpt2_attention_forward": (_i, [_i, _i, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "gpt2_attention_backward": (_i, [_i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "gpt2_device_status": (_i, []),
+    "gpt2_train_step": (_i, [_vp, _vp, _i, _i, _f, _f, _f, _f, _f, _i, _vp]),
     "gpt2_layernorm_forward": (_i, [_i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp]),
     "gpt2_layernorm_backward_scratch_floats": (_sz, [_i]),
     "gpt2_layernorm_backward": (_i, [_i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _vp,
@@ -170,6 +171,14 @@ def gpt2_backward() -> None:
 
 def gpt2_adamw(lr, beta1, beta2, eps, weight_decay, step) -> None:
     _check("gpt2_adamw", lib().gpt2_adamw(lr, beta1, beta2, eps, weight_decay, step))
+
+
+def gpt2_train_step(d_tokens, d_targets, B, T, lr, beta1, beta2, eps, weight_decay, step,
+                    d_mean_loss=None) -> None:
+    """Forward, zero_grad, backward and AdamW on device buffers (CUDA-graph replays)."""
+    _check("gpt2_train_step", lib().gpt2_train_step(ptr(d_tokens), ptr(d_targets), B, T, lr, beta1,
+                                                    beta2, eps, weight_decay, step,
+                                                    ptr(d_mean_loss)))
 
 
 def gpt2_sync() -> None:

@@ -128,6 +128,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_enter();  // global memory is touched only from here on
 
     // warp-uniform bounded wait
     auto wait_warp = [&](uint32_t bar, uint32_t parity) {
@@ -434,6 +435,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // D_i = dO_i . O_i for every (b, h, i), eight threads per row (16-byte loads)
 __global__ void rowdot64_k(float* __restrict__ D, const bf16* __restrict__ dout,
                            const bf16* __restrict__ out, int T, int C, int NH, int nrows) {
+    pdl_enter();
     const int idx = blockIdx.x * blockDim.x + threadIdx.x;
     const int row = idx >> 3, part = idx & 7;
     float s = 0.f;
@@ -510,8 +512,8 @@ int launch_flash_backward_tc(void* dqkv, const void* dout, const void* qkv, cons
     if (rc != GPT2_OK) return rc;
     const int nrows = B * NH * T;
     note_launch(3);
-    rowdot64_k<<<(nrows * 8 + 255) / 256, 256, 0, s>>>(D, (const bf16*)dout, (const bf16*)out, T, C, NH,
-                                                       nrows);
+    launch_pdl(rowdot64_k, dim3((nrows * 8 + 255) / 256), dim3(256), 0, s, D, (const bf16*)dout,
+               (const bf16*)out, T, C, NH, nrows);
     BwdArgs a;
     a.dqkv = (bf16*)dqkv;
     a.lse = lse;
@@ -525,8 +527,8 @@ int launch_flash_backward_tc(void* dqkv, const void* dout, const void* qkv, cons
     a.scale_log2 = LOG2E * a.scale;
     a.err = err;
     const int grid = a.nblk * a.BH;
-    flash_bwd_tc_k<false><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tqkv, tdo, a);
-    flash_bwd_tc_k<true><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tqkv, tdo, a);
+    launch_pdl(flash_bwd_tc_k<false>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, s, tqkv, tdo, a);
+    launch_pdl(flash_bwd_tc_k<true>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, s, tqkv, tdo, a);
     return GPT2_OK;
 }
 

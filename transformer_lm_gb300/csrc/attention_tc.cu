@@ -119,6 +119,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_enter();  // global memory is touched only from here on
 
     if (warp == 0) {
         if (lane == 0) {
@@ -380,7 +381,7 @@ int launch_flash_forward_tc(void* out, float* lse, const void* qkv, int B, int T
     a.err = err;
     dim3 grid((T + NQT * BQ - 1) / (NQT * BQ), B * NH);
     note_launch(1);
-    flash_fwd_tc_k<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tm, a);
+    launch_pdl(flash_fwd_tc_k, grid, dim3(NUM_THREADS), SMEM_BYTES, s, tm, a);
     return GPT2_OK;
 }
 

@@ -41,6 +41,16 @@ template <typename T> DEVI void st16_cs(T* p, const Vec16<T>& v) {
 }
 
 // ---------------------------------------------------------------- reductions
+// Programmatic dependent launch: allow the next kernel of the stream to be
+// scheduled (its prologue overlaps this kernel's tail), then wait until every
+// kernel this one depends on has finished and its writes are visible. Every
+// kernel launched through launch_pdl calls it before its first global memory
+// access; without the launch attribute both instructions do nothing.
+DEVI void pdl_enter() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 DEVI float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

@@ -237,6 +237,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     if constexpr (CG == 2) cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
     const uint32_t tmem_base = *tmem_slot;
+    pdl_enter();  // global memory is touched only from here on
     // a pair of CTAs takes an m-block pair (rows m0 .. m0+255) of one n-block
     const int num_mg = (args.num_m + CG - 1) / CG;
     const int num_super = num_mg * args.num_n;
@@ -546,6 +547,7 @@ static bool make_map_3d_f32(CUtensorMap* m, void* ptr, int N, int M, int S, uint
 __global__ void __launch_bounds__(256) splitk_reduce_k(bf16* __restrict__ D, long long ldd,
                                                        const float* __restrict__ ws, int M, int N,
                                                        int S) {
+    pdl_enter();
     const int n8 = N / 8;
     const long long total = (long long)M * n8;
     const size_t slice = (size_t)M * N;
@@ -581,7 +583,7 @@ static int launch_splitk_reduce(bf16* D, long long ldd, const float* ws, int M, 
     const long long cap = (long long)num_sms() * 8;
     if (blocks > cap) blocks = cap;
     note_launch(1);
-    splitk_reduce_k<<<(unsigned)blocks, 256, 0, s>>>(D, ldd, ws, M, N, S);
+    launch_pdl(splitk_reduce_k, dim3((unsigned)blocks), dim3(256), 0, s, D, ldd, ws, M, N, S);
     return GPT2_OK;
 }
 
@@ -604,7 +606,7 @@ static int launch_tc(const Maps& mp, const tc::Args& a, cudaStream_t s) {
         attr_done = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(tc::NUM_THREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = s;
@@ -612,6 +614,8 @@ static int launch_tc(const Maps& mp, const tc::Args& a, cudaStream_t s) {
     if constexpr (CG == 1) {
         const int sms = num_sms();
         cfg.gridDim = dim3((unsigned)(supers < sms ? supers : sms));
+        cfg.attrs = attr;
+        cfg.numAttrs = 0;
     } else {
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
@@ -628,6 +632,11 @@ static int launch_tc(const Maps& mp, const tc::Args& a, cudaStream_t s) {
         }
         const long long ncl = supers < max_clusters ? supers : max_clusters;
         cfg.gridDim = dim3((unsigned)(ncl * 2));
+    }
+    if (pdl_enabled()) {
+        attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs++;
     }
     note_launch(1);
     if (cudaLaunchKernelEx(&cfg, kern, mp.a, mp.b, mp.d, mp.d2, mp.x, a) != cudaSuccess)

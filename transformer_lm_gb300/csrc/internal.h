@@ -116,6 +116,26 @@ int launch_flash_backward_tc(void* dqkv, const void* dout, const void* qkv, cons
                              unsigned int* err);
 
 int num_sms();
+
+// Programmatic dependent launch for the step's kernels (GPT2_PDL=0 turns it
+// off): the kernel may be scheduled while the previous one drains, and waits
+// for it in pdl_enter().
+bool pdl_enabled();
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
 // records the library's last error (text and GPT2_ERR_* code); returns code
 int set_error(int code, const char* fmt, ...);
 // host-side count of kernel launches made by this library (for benchmark reporting)

@@ -10,10 +10,19 @@
 #include "internal.h"
 
 #include <math.h>
+#include <stdlib.h>
 
 #include <atomic>
 
 namespace gk {
+
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char* e = getenv("GPT2_PDL");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
 
 int num_sms() {
     static int n = 0;
@@ -43,6 +52,7 @@ static inline unsigned int grid_for(size_t work, int block, int per_sm = 8) {
 // replaced by 0 (so no later gather leaves its table) and flagged.
 __global__ void copy_tokens_k(const int* __restrict__ src, int* __restrict__ dst, int n, int V,
                               unsigned int* err) {
+    pdl_enter();
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
         int t = src[i];
         if (t < 0 || t >= V) {
@@ -55,7 +65,7 @@ __global__ void copy_tokens_k(const int* __restrict__ src, int* __restrict__ dst
 
 void launch_copy_tokens(const int* src, int* dst, int n, int V, unsigned int* err, cudaStream_t s) {
     note_launch(1);
-    copy_tokens_k<<<grid_for(n, 256), 256, 0, s>>>(src, dst, n, V, err);
+    launch_pdl(copy_tokens_k, grid_for(n, 256), 256, 0, s, src, dst, n, V, err);
 }
 
 // ------------------------------------------------------------------ encoder
@@ -64,6 +74,7 @@ template <typename T>
 __global__ void encoder_forward_k(T* __restrict__ out, const int* __restrict__ tok,
                                   const T* __restrict__ wte, const T* __restrict__ wpe, int BT,
                                   int Tn, int C) {
+    pdl_enter();
     constexpr int VEC = Vec16<T>::N;
     const int cv = C / VEC;
     const size_t nvec = (size_t)BT * cv;
@@ -87,10 +98,10 @@ void launch_encoder_forward(DType dt, void* out, const int* tok, const void* wte
     size_t work = (size_t)B * T * C / (dt == DT_BF16 ? 8 : 4);
     unsigned g = grid_for(work, 256);
     if (dt == DT_BF16)
-        encoder_forward_k<bf16><<<g, 256, 0, s>>>((bf16*)out, tok, (const bf16*)wte,
+        launch_pdl(encoder_forward_k<bf16>, g, 256, 0, s, (bf16*)out, tok, (const bf16*)wte,
                                                   (const bf16*)wpe, B * T, T, C);
     else
-        encoder_forward_k<float><<<g, 256, 0, s>>>((float*)out, tok, (const float*)wte,
+        launch_pdl(encoder_forward_k<float>, g, 256, 0, s, (float*)out, tok, (const float*)wte,
                                                    (const float*)wpe, B * T, T, C);
 }
 
@@ -99,6 +110,7 @@ void launch_encoder_forward(DType dt, void* out, const int* tok, const void* wte
 template <typename T>
 __global__ void encoder_backward_wpe_k(T* __restrict__ dwpe, const T* __restrict__ dout, int B,
                                        int Tn, int C) {
+    pdl_enter();
     constexpr int VEC = Vec16<T>::N;
     const int cv = C / VEC;
     const int nvec = Tn * cv;
@@ -122,6 +134,7 @@ __global__ void encoder_backward_wpe_k(T* __restrict__ dwpe, const T* __restrict
 
 // token histogram (integer atomics: the counts are exact whatever the order)
 __global__ void token_count_k(const int* __restrict__ tok, int n, int* counts) {
+    pdl_enter();
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
         atomicAdd(&counts[tok[i]], 1);
 }
@@ -131,6 +144,7 @@ __global__ void token_count_k(const int* __restrict__ tok, int n, int* counts) {
 __global__ void __launch_bounds__(1024) token_scan_k(const int* __restrict__ counts, int Vp,
                                                      int* __restrict__ offsets,
                                                      int* __restrict__ cursor) {
+    pdl_enter();
     __shared__ int warp_tot[32];
     const int tid = threadIdx.x, nt = blockDim.x;
     const int per = (Vp + nt - 1) / nt;
@@ -168,6 +182,7 @@ __global__ void __launch_bounds__(1024) token_scan_k(const int* __restrict__ cou
 
 __global__ void token_scatter_k(const int* __restrict__ tok, int n, int* cursor,
                                 int* __restrict__ order) {
+    pdl_enter();
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
         int slot = atomicAdd(&cursor[tok[i]], 1);
         order[slot] = i;
@@ -177,6 +192,7 @@ __global__ void token_scatter_k(const int* __restrict__ tok, int n, int* cursor,
 // place each position at its rank (ascending position) inside its token's bucket
 __global__ void token_rank_k(const int* __restrict__ tok, const int* __restrict__ offsets,
                              const int* __restrict__ order, int n, int* __restrict__ sorted) {
+    pdl_enter();
     for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < n; s += gridDim.x * blockDim.x) {
         int pos = order[s];
         int v = tok[pos];
@@ -192,6 +208,7 @@ template <typename T>
 __global__ void encoder_backward_wte_k(T* __restrict__ dwte, const T* __restrict__ dout,
                                        const int* __restrict__ offsets,
                                        const int* __restrict__ sorted, int Vp, int C) {
+    pdl_enter();
     constexpr int VEC = Vec16<T>::N;
     constexpr int CH = 4;  // vectors per lane per pass
     const int warps = blockDim.x / 32;
@@ -243,20 +260,20 @@ void launch_encoder_backward(DType dt, void* dwte, void* dwpe, const void* dout,
     const int VEC = dt == DT_BF16 ? 8 : 4;
     unsigned g = grid_for((size_t)T * C / VEC, 256);
     if (dt == DT_BF16)
-        encoder_backward_wpe_k<bf16><<<g, 256, 0, s>>>((bf16*)dwpe, (const bf16*)dout, B, T, C);
+        launch_pdl(encoder_backward_wpe_k<bf16>, g, 256, 0, s, (bf16*)dwpe, (const bf16*)dout, B, T, C);
     else
-        encoder_backward_wpe_k<float><<<g, 256, 0, s>>>((float*)dwpe, (const float*)dout, B, T, C);
+        launch_pdl(encoder_backward_wpe_k<float>, g, 256, 0, s, (float*)dwpe, (const float*)dout, B, T, C);
     launch_zero(ws_counts, sizeof(int) * (size_t)Vp, s);
-    token_count_k<<<grid_for(n, 256), 256, 0, s>>>(tok, n, ws_counts);
-    token_scan_k<<<1, 1024, 0, s>>>(ws_counts, Vp, ws_offsets, ws_cursor);
-    token_scatter_k<<<grid_for(n, 256), 256, 0, s>>>(tok, n, ws_cursor, ws_order);
-    token_rank_k<<<grid_for(n, 256), 256, 0, s>>>(tok, ws_offsets, ws_order, n, ws_sorted);
+    launch_pdl(token_count_k, grid_for(n, 256), 256, 0, s, tok, n, ws_counts);
+    launch_pdl(token_scan_k, 1, 1024, 0, s, ws_counts, Vp, ws_offsets, ws_cursor);
+    launch_pdl(token_scatter_k, grid_for(n, 256), 256, 0, s, tok, n, ws_cursor, ws_order);
+    launch_pdl(token_rank_k, grid_for(n, 256), 256, 0, s, tok, ws_offsets, ws_order, n, ws_sorted);
     unsigned gw = (unsigned)((Vp + 7) / 8);
     if (dt == DT_BF16)
-        encoder_backward_wte_k<bf16><<<gw, 256, 0, s>>>((bf16*)dwte, (const bf16*)dout, ws_offsets,
+        launch_pdl(encoder_backward_wte_k<bf16>, gw, 256, 0, s, (bf16*)dwte, (const bf16*)dout, ws_offsets,
                                                         ws_sorted, Vp, C);
     else
-        encoder_backward_wte_k<float><<<gw, 256, 0, s>>>((float*)dwte, (const float*)dout,
+        launch_pdl(encoder_backward_wte_k<float>, gw, 256, 0, s, (float*)dwte, (const float*)dout,
                                                          ws_offsets, ws_sorted, Vp, C);
 }
 
@@ -269,6 +286,7 @@ __global__ void layernorm_forward_k(T* __restrict__ out, float* __restrict__ mea
                                     float* __restrict__ rstd, const T* __restrict__ inp,
                                     const T* __restrict__ w, const T* __restrict__ b, int N,
                                     int C) {
+    pdl_enter();
     constexpr int VEC = Vec16<T>::N;
     const int warps = blockDim.x / 32;
     const int row = blockIdx.x * warps + threadIdx.x / 32;
@@ -336,7 +354,7 @@ void launch_layernorm_forward(DType dt, void* out, float* mean, float* rstd, con
     const int block = 256, rows = block / 32;
     unsigned g = (unsigned)((N + rows - 1) / rows);
 #define LNF(TT, MV)                                                                            \
-    layernorm_forward_k<TT, MV><<<g, block, 0, s>>>((TT*)out, mean, rstd, (const TT*)inp,        \
+    launch_pdl(layernorm_forward_k<TT, MV>, g, block, 0, s, (TT*)out, mean, rstd, (const TT*)inp,        \
                                                     (const TT*)w, (const TT*)b, N, C)
     if (dt == DT_BF16) {
         if (mv == 1) LNF(bf16, 1); else if (mv == 2) LNF(bf16, 2); else if (mv == 4) LNF(bf16, 4); else LNF(bf16, 8);
@@ -361,6 +379,7 @@ __global__ void __launch_bounds__(LNB_BLOCK) layernorm_backward_k(
     T* __restrict__ dinp, float* __restrict__ ws, const T* __restrict__ dout,
     const T* __restrict__ inp, const T* __restrict__ w, const float* __restrict__ mean,
     const float* __restrict__ rstd, int N, int C, int accumulate) {
+    pdl_enter();
     constexpr int VEC = Vec16<T>::N;
     // per-warp partial sums, [warp][dw | db][k][vector]: lane-consecutive addresses
     extern __shared__ float sm[];
@@ -427,7 +446,7 @@ __global__ void __launch_bounds__(LNB_BLOCK) layernorm_backward_k(
     }
 }
 
-// Same operation for bf16 rows of at most 32 * 8 * NV columns, built for
+// Same operation for bf16 rows of at most 32 * 8 * NV columns (NV <= 3), built for
 // memory-level parallelism: each lane keeps its weights and its dw/db column
 // partials in registers and loads the warp's next row while it computes the
 // current one, so every warp has two rows of loads in flight and nothing is
@@ -438,62 +457,60 @@ __global__ void __launch_bounds__(LNB_BLOCK, 1) layernorm_backward_reg_k(
     bf16* __restrict__ dinp, float* __restrict__ ws, const bf16* __restrict__ dout,
     const bf16* __restrict__ inp, const bf16* __restrict__ w, const float* __restrict__ mean,
     const float* __restrict__ rstd, int N, int C, int accumulate) {
+    pdl_enter();
     constexpr int VEC = 8;
     extern __shared__ float sm[];
     const int warps = blockDim.x / 32;
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const int cv = C / VEC;
-    float wf[NV][VEC], adw[NV][VEC], adb[NV][VEC];
+    Vec16<bf16> wv[NV];  // the lane's weights, kept packed
+    float adw[NV][VEC], adb[NV][VEC];
 #pragma unroll
     for (int j = 0; j < NV; j++) {
         const int vi = lane + 32 * j;
-        Vec16<bf16> wv;
-        if (vi < cv) wv = ld16(w + vi * VEC);
+        if (vi < cv) wv[j] = ld16(w + vi * VEC);
 #pragma unroll
         for (int k = 0; k < VEC; k++) {
-            wf[j][k] = vi < cv ? to_f(wv.v[k]) : 0.f;
             adw[j][k] = 0.f;
             adb[j][k] = 0.f;
         }
     }
     const int stride = gridDim.x * warps;
     int row = blockIdx.x * warps + warp;
-    Vec16<bf16> xa[NV], da[NV];
+    Vec16<bf16> xa[NV], da[NV], oa[NV];
     float mu = 0.f, rs = 0.f;
-    auto load_row = [&](int r, Vec16<bf16> (&xv)[NV], Vec16<bf16> (&dv)[NV], float& m, float& sd) {
+    // a row's x, dy, the current dx (the += operand) and its statistics
+    auto load_row = [&](int r, Vec16<bf16> (&xv)[NV], Vec16<bf16> (&dv)[NV], Vec16<bf16> (&ov)[NV],
+                        float& m, float& sd) {
         const bf16* x = inp + (size_t)r * C;
         const bf16* dy = dout + (size_t)r * C;
+        const bf16* dxr = dinp + (size_t)r * C;
 #pragma unroll
         for (int j = 0; j < NV; j++) {
             const int vi = lane + 32 * j;
             if (vi < cv) {
                 xv[j] = ld16_cs(x + vi * VEC);
                 dv[j] = ld16_cs(dy + vi * VEC);
+                if (accumulate) ov[j] = ld16(dxr + vi * VEC);
             }
         }
         m = mean[r];
         sd = rstd[r];
     };
-    if (row < N) load_row(row, xa, da, mu, rs);
+    if (row < N) load_row(row, xa, da, oa, mu, rs);
     while (row < N) {
         const int nrow = row + stride;
-        Vec16<bf16> xb[NV], db2[NV];
+        Vec16<bf16> xb[NV], db2[NV], ob[NV];
         float mu2 = 0.f, rs2 = 0.f;
-        if (nrow < N) load_row(nrow, xb, db2, mu2, rs2);
+        if (nrow < N) load_row(nrow, xb, db2, ob, mu2, rs2);
         bf16* dx = dinp + (size_t)row * C;
-        Vec16<bf16> old[NV];
-        if (accumulate) {
-#pragma unroll
-            for (int j = 0; j < NV; j++)
-                if (lane + 32 * j < cv) old[j] = ld16(dx + (lane + 32 * j) * VEC);
-        }
         float gsum = 0.f, gnsum = 0.f;
 #pragma unroll
         for (int j = 0; j < NV; j++) {
             if (lane + 32 * j < cv) {
 #pragma unroll
                 for (int k = 0; k < VEC; k++) {
-                    const float g = wf[j][k] * to_f(da[j].v[k]);
+                    const float g = to_f(wv[j].v[k]) * to_f(da[j].v[k]);
                     gsum += g;
                     gnsum += g * (to_f(xa[j].v[k]) - mu) * rs;
                 }
@@ -510,8 +527,8 @@ __global__ void __launch_bounds__(LNB_BLOCK, 1) layernorm_backward_reg_k(
                 for (int k = 0; k < VEC; k++) {
                     const float d = to_f(da[j].v[k]);
                     const float nh = (to_f(xa[j].v[k]) - mu) * rs;
-                    const float val = rs * (wf[j][k] * d - gsum - nh * gnsum);
-                    o.v[k] = from_f<bf16>(accumulate ? to_f(old[j].v[k]) + val : val);
+                    const float val = rs * (to_f(wv[j].v[k]) * d - gsum - nh * gnsum);
+                    o.v[k] = from_f<bf16>(accumulate ? to_f(oa[j].v[k]) + val : val);
                     adw[j][k] += nh * d;
                     adb[j][k] += d;
                 }
@@ -522,6 +539,7 @@ __global__ void __launch_bounds__(LNB_BLOCK, 1) layernorm_backward_reg_k(
         for (int j = 0; j < NV; j++) {
             xa[j] = xb[j];
             da[j] = db2[j];
+            oa[j] = ob[j];
         }
         mu = mu2;
         rs = rs2;
@@ -556,12 +574,15 @@ template <typename T>
 __global__ void __launch_bounds__(256) reduce_partials_k(T* __restrict__ dst, T* __restrict__ dst2,
                                                          int split, const float* __restrict__ ws,
                                                          int P, int W) {
+    pdl_enter();
     __shared__ float part[8][33];
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const int c = blockIdx.x * 32 + lane;
     float acc = 0.f;
-    if (c < W)
+    if (c < W) {
+#pragma unroll 8
         for (int p = warp; p < P; p += 8) acc += ws[(size_t)p * W + c];
+    }
     part[warp][lane] = acc;
     __syncthreads();
     if (warp == 0 && c < W) {
@@ -615,7 +636,7 @@ void launch_layernorm_backward(DType dt, void* dinp, void* dw, void* db, const v
     int P = 1;
 #define LNB(TT, NVV)                                                                          \
     P = lnb_blocks<TT, NVV>(N, smem);                                                         \
-    layernorm_backward_k<TT, NVV><<<P, LNB_BLOCK, smem, s>>>((TT*)dinp, ws, (const TT*)dout,  \
+    launch_pdl(layernorm_backward_k<TT, NVV>, P, LNB_BLOCK, smem, s, (TT*)dinp, ws, (const TT*)dout,  \
                                                              (const TT*)inp, (const TT*)w,     \
                                                              mean, rstd, N, C, accumulate)
 #define LNB_ALL(TT)                                                                           \
@@ -625,7 +646,7 @@ void launch_layernorm_backward(DType dt, void* dinp, void* dw, void* db, const v
         case 7: LNB(TT, 7); break; default: LNB(TT, 8); break;                                \
     }
     const unsigned rg = (unsigned)((2 * C + 31) / 32);
-    if (dt == DT_BF16 && nv <= 4) {
+    if (dt == DT_BF16 && nv <= 3) {
         // one block per SM: its 8 warps keep two rows of loads in flight each
         const int rows_per_block = LNB_BLOCK / 32;
         P = (N + rows_per_block - 1) / rows_per_block;
@@ -633,20 +654,20 @@ void launch_layernorm_backward(DType dt, void* dinp, void* dw, void* db, const v
         if (P < 1) P = 1;
 #define LNR(NVV)                                                                                    \
     lnr_opt_in<NVV>(smem);                                                                           \
-    layernorm_backward_reg_k<NVV><<<P, LNB_BLOCK, smem, s>>>((bf16*)dinp, ws, (const bf16*)dout,     \
+    launch_pdl(layernorm_backward_reg_k<NVV>, P, LNB_BLOCK, smem, s, (bf16*)dinp, ws, (const bf16*)dout,     \
                                                           (const bf16*)inp, (const bf16*)w, mean,   \
                                                           rstd, N, C, accumulate)
         switch (nv) {
-            case 1: LNR(1); break; case 2: LNR(2); break; case 3: LNR(3); break; default: LNR(4); break;
+            case 1: LNR(1); break; case 2: LNR(2); break; default: LNR(3); break;
         }
 #undef LNR
-        reduce_partials_k<bf16><<<rg, 256, 0, s>>>((bf16*)dw, (bf16*)db, C, ws, P, 2 * C);
+        launch_pdl(reduce_partials_k<bf16>, rg, 256, 0, s, (bf16*)dw, (bf16*)db, C, ws, P, 2 * C);
     } else if (dt == DT_BF16) {
         LNB_ALL(bf16);
-        reduce_partials_k<bf16><<<rg, 256, 0, s>>>((bf16*)dw, (bf16*)db, C, ws, P, 2 * C);
+        launch_pdl(reduce_partials_k<bf16>, rg, 256, 0, s, (bf16*)dw, (bf16*)db, C, ws, P, 2 * C);
     } else {
         LNB_ALL(float);
-        reduce_partials_k<float><<<rg, 256, 0, s>>>((float*)dw, (float*)db, C, ws, P, 2 * C);
+        launch_pdl(reduce_partials_k<float>, rg, 256, 0, s, (float*)dw, (float*)db, C, ws, P, 2 * C);
     }
 #undef LNB_ALL
 #undef LNB
@@ -662,6 +683,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) colsum_partial_k(float* __restrict__ ws,
                                                         const T* __restrict__ dout, int M, int N,
                                                         int rows_per_slab) {
+    pdl_enter();
     constexpr int VEC = Vec16<T>::N;
     __shared__ float sm[8][32 * VEC];
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
@@ -713,11 +735,11 @@ void launch_colsum_accum(DType dt, void* dbias, const void* dout, int M, int N, 
     dim3 grid((N + 32 * VEC - 1) / (32 * VEC), R);
     const unsigned rg = (unsigned)((N + 31) / 32);
     if (dt == DT_BF16) {
-        colsum_partial_k<bf16><<<grid, 256, 0, s>>>(ws, (const bf16*)dout, M, N, rps);
-        reduce_partials_k<bf16><<<rg, 256, 0, s>>>((bf16*)dbias, (bf16*)dbias, N, ws, R, N);
+        launch_pdl(colsum_partial_k<bf16>, grid, 256, 0, s, ws, (const bf16*)dout, M, N, rps);
+        launch_pdl(reduce_partials_k<bf16>, rg, 256, 0, s, (bf16*)dbias, (bf16*)dbias, N, ws, R, N);
     } else {
-        colsum_partial_k<float><<<grid, 256, 0, s>>>(ws, (const float*)dout, M, N, rps);
-        reduce_partials_k<float><<<rg, 256, 0, s>>>((float*)dbias, (float*)dbias, N, ws, R, N);
+        launch_pdl(colsum_partial_k<float>, grid, 256, 0, s, ws, (const float*)dout, M, N, rps);
+        launch_pdl(reduce_partials_k<float>, rg, 256, 0, s, (float*)dbias, (float*)dbias, N, ws, R, N);
     }
 }
 
@@ -734,6 +756,7 @@ __global__ void __launch_bounds__(CLS_BLOCK) classifier_k(T* __restrict__ logits
                                                           float* __restrict__ losses,
                                                           const int* __restrict__ targets, int V,
                                                           int Vp, float dloss) {
+    pdl_enter();
     constexpr int VEC = Vec16<T>::N;
     __shared__ float s_max[32], s_sum[32];
     __shared__ float s_tlogit;
@@ -791,14 +814,15 @@ void launch_classifier(DType dt, void* logits, float* losses, const int* targets
                        int Vp, float dloss, cudaStream_t s) {
     note_launch(1);
     if (dt == DT_BF16)
-        classifier_k<bf16><<<BT, CLS_BLOCK, 0, s>>>((bf16*)logits, losses, targets, V, Vp, dloss);
+        launch_pdl(classifier_k<bf16>, BT, CLS_BLOCK, 0, s, (bf16*)logits, losses, targets, V, Vp, dloss);
     else
-        classifier_k<float><<<BT, CLS_BLOCK, 0, s>>>((float*)logits, losses, targets, V, Vp, dloss);
+        launch_pdl(classifier_k<float>, BT, CLS_BLOCK, 0, s, (float*)logits, losses, targets, V, Vp, dloss);
 }
 
 // mean of n floats in a fixed order (single block)
 __global__ void __launch_bounds__(1024) mean_k(const float* __restrict__ x, int n,
                                                float* __restrict__ out) {
+    pdl_enter();
     __shared__ float sw[32];
     float s = 0.f;
     for (int i = threadIdx.x; i < n; i += blockDim.x) s += x[i];
@@ -815,7 +839,7 @@ __global__ void __launch_bounds__(1024) mean_k(const float* __restrict__ x, int 
 
 void launch_mean(const float* x, int n, float* out, cudaStream_t s) {
     note_launch(1);
-    mean_k<<<1, 1024, 0, s>>>(x, n, out);
+    launch_pdl(mean_k, 1, 1024, 0, s, x, n, out);
 }
 
 // ------------------------------------------------------------------ AdamW
@@ -835,6 +859,7 @@ __global__ void adamw_k(T* __restrict__ params, float* __restrict__ master,
                         const T* __restrict__ grads, float* __restrict__ mst,
                         float* __restrict__ vst, size_t n, float lr, float b1, float b2, float c1,
                         float c2, float eps, float wd, const float* __restrict__ hyper) {
+    pdl_enter();
     if (hyper) {  // hyperparameters from device memory (graph replays)
         lr = hyper[0]; b1 = hyper[1]; b2 = hyper[2]; c1 = hyper[3]; c2 = hyper[4];
         eps = hyper[5]; wd = hyper[6];
@@ -898,26 +923,28 @@ void launch_adamw(DType dt, void* params, float* master, const void* grads, floa
     note_launch(1);
     unsigned g = grid_for((n + 3) / 4, 256, 8);
     if (dt == DT_BF16)
-        adamw_k<bf16><<<g, 256, 0, s>>>((bf16*)params, master, (const bf16*)grads, m, v, n, lr, b1,
+        launch_pdl(adamw_k<bf16>, g, 256, 0, s, (bf16*)params, master, (const bf16*)grads, m, v, n, lr, b1,
                                         b2, c1, c2, eps, wd, hyper);
     else
-        adamw_k<float><<<g, 256, 0, s>>>((float*)params, master, (const float*)grads, m, v, n, lr,
+        launch_pdl(adamw_k<float>, g, 256, 0, s, (float*)params, master, (const float*)grads, m, v, n, lr,
                                          b1, b2, c1, c2, eps, wd, hyper);
 }
 
 __global__ void set_hyper_k(float* h, float lr, float b1, float b2, float c1, float c2, float eps,
                             float wd) {
+    pdl_enter();
     h[0] = lr; h[1] = b1; h[2] = b2; h[3] = c1; h[4] = c2; h[5] = eps; h[6] = wd;
 }
 
 void launch_set_hyper(float* h, float lr, float b1, float b2, float c1, float c2, float eps, float wd,
                       cudaStream_t s) {
     note_launch(1);
-    set_hyper_k<<<1, 1, 0, s>>>(h, lr, b1, b2, c1, c2, eps, wd);
+    launch_pdl(set_hyper_k, 1, 1, 0, s, h, lr, b1, b2, c1, c2, eps, wd);
 }
 
 // ------------------------------------------------------------------ utilities
 __global__ void zero_k(int4* __restrict__ p, size_t n16, char* __restrict__ tail, size_t ntail) {
+    pdl_enter();
     size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     for (; i < n16; i += (size_t)gridDim.x * blockDim.x) p[i] = make_int4(0, 0, 0, 0);
     if (blockIdx.x == 0 && threadIdx.x < ntail) tail[threadIdx.x] = 0;
@@ -928,7 +955,7 @@ void launch_zero(void* p, size_t bytes, cudaStream_t s) {
     note_launch(1);
     // p is at least 256-byte aligned (every buffer comes from cudaMalloc offsets of 256)
     size_t n16 = bytes / 16, ntail = bytes % 16;
-    zero_k<<<grid_for(n16 ? n16 : 1, 256, 8), 256, 0, s>>>((int4*)p, n16, (char*)p + n16 * 16, ntail);
+    launch_pdl(zero_k, grid_for(n16 ? n16 : 1, 256, 8), 256, 0, s, (int4*)p, n16, (char*)p + n16 * 16, ntail);
 }
 
 // counter-based normal generator for the initial weights: SplitMix64 output

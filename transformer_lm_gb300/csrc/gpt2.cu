@@ -89,6 +89,14 @@ struct Model {
     void *dresidual, *dbtc, *dbt4c;
     float *attn_D, *ws;
     float* gemm_ws = nullptr;  // split-K partials of the weight-gradient GEMMs
+    // LayerNorm and bias gradients as partial rows, reduced by one launch at
+    // the end of the backward (areas: 2L+1 LayerNorms [ln1 of l = 2l, ln2 of
+    // l = 2l+1, lnf = 2L], their column sums when not fused, fc and qkv biases)
+    float* gpart = nullptr;
+    PartialDesc* d_desc = nullptr;
+    int ndesc = 0, P_ln = 0, R_cs = 0;
+    bool ln_fused = false;
+    size_t ln_area = 0, cs_off = 0, fcb_off = 0, qkvb_off = 0;
     // gpt2_train_step: the captured step and what it was captured for
     float* d_hyper = nullptr;  // AdamW hyperparameters read by the replayed update
     cudaGraph_t graph = nullptr;
@@ -157,6 +165,10 @@ int gemm(Model* m, int epi, const void* A, long long lda, int a_km, const void* 
 // ------------------------------------------------------------------ lifecycle
 void free_acts(Model* m) {
     if (m->act_mem) cudaFree(m->act_mem);
+    if (m->gpart) cudaFree(m->gpart);
+    if (m->d_desc) cudaFree(m->d_desc);
+    m->gpart = nullptr;
+    m->d_desc = nullptr;
     if (m->h_pinned) cudaFreeHost(m->h_pinned);
     m->act_mem = nullptr;
     m->h_pinned = nullptr;
@@ -182,6 +194,54 @@ void free_model(Model* m) {
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+float* ln_part(const Model* m, int i) { return m->gpart + (size_t)i * m->ln_area; }
+float* cs_part(const Model* m, int i) { return m->gpart + m->cs_off + (size_t)i * m->R_cs * m->C; }
+float* fcb_part(const Model* m, int l) { return m->gpart + m->fcb_off + (size_t)l * m->R_cs * 4 * m->C; }
+float* qkvb_part(const Model* m, int l) { return m->gpart + m->qkvb_off + (size_t)l * m->R_cs * 3 * m->C; }
+
+// partial-row areas and the device table of their reductions (fixed for a B x T)
+int alloc_partials(Model* m) {
+    const int L = m->L, C = m->C;
+    const int BT = m->B * m->T;
+    const size_t es = m->esz;
+    m->ln_fused = layernorm_backward_fuses_colsum(m->dt, C);
+    m->P_ln = layernorm_backward_part_rows(m->dt, BT, C);
+    m->R_cs = colsum_part_rows(BT);
+    m->ln_area = (size_t)m->P_ln * 3 * C;
+    m->cs_off = (size_t)(2 * L + 1) * m->ln_area;
+    m->fcb_off = m->cs_off + (m->ln_fused ? 0 : (size_t)(2 * L + 1) * m->R_cs * C);
+    m->qkvb_off = m->fcb_off + (size_t)L * m->R_cs * 4 * C;
+    const size_t total = m->qkvb_off + (size_t)L * m->R_cs * 3 * C;
+    CUDA_TRY(cudaMalloc((void**)&m->gpart, total * 4 + 256));
+    std::vector<PartialDesc> d;
+    const long long lstride = m->ln_fused ? 3LL * C : 2LL * C;
+    auto add = [&](const float* part, long long pstride, int P, int width, char* dst) {
+        d.push_back(PartialDesc{part, pstride, P, width, dst});
+    };
+    // the column sums of LayerNorm i's output: the bias grad of the matmul below it
+    auto add_cs = [&](int i, char* dst) {
+        if (m->ln_fused) add(ln_part(m, i) + 2 * C, lstride, m->P_ln, C, dst);
+        else add(cs_part(m, i), C, m->R_cs, C, dst);
+    };
+    add(ln_part(m, 2 * L), lstride, m->P_ln, C, G(m, 14));
+    add(ln_part(m, 2 * L) + C, lstride, m->P_ln, C, G(m, 15));
+    if (L > 0) add_cs(2 * L, G(m, 13) + (size_t)(L - 1) * C * es);
+    for (int l = 0; l < L; l++) {
+        add(ln_part(m, 2 * l + 1), lstride, m->P_ln, C, G(m, 8) + (size_t)l * C * es);
+        add(ln_part(m, 2 * l + 1) + C, lstride, m->P_ln, C, G(m, 9) + (size_t)l * C * es);
+        add_cs(2 * l + 1, G(m, 7) + (size_t)l * C * es);
+        add(ln_part(m, 2 * l), lstride, m->P_ln, C, G(m, 2) + (size_t)l * C * es);
+        add(ln_part(m, 2 * l) + C, lstride, m->P_ln, C, G(m, 3) + (size_t)l * C * es);
+        if (l > 0) add_cs(2 * l, G(m, 13) + (size_t)(l - 1) * C * es);
+        add(fcb_part(m, l), 4LL * C, m->R_cs, 4 * C, G(m, 11) + (size_t)l * 4 * C * es);
+        add(qkvb_part(m, l), 3LL * C, m->R_cs, 3 * C, G(m, 5) + (size_t)l * 3 * C * es);
+    }
+    m->ndesc = (int)d.size();
+    CUDA_TRY(cudaMalloc((void**)&m->d_desc, d.size() * sizeof(PartialDesc) + 256));
+    CUDA_TRY(cudaMemcpy(m->d_desc, d.data(), d.size() * sizeof(PartialDesc), cudaMemcpyHostToDevice));
+    return GPT2_OK;
+}
 
 int alloc_acts(Model* m, int B, int T) {
     const size_t L = m->L, C = m->C, BT = (size_t)B * T, es = m->esz;
@@ -228,7 +288,7 @@ int alloc_acts(Model* m, int B, int T) {
     m->B = B;
     m->T = T;
     m->acts = true;
-    return GPT2_OK;
+    return alloc_partials(m);
 }
 
 int check_model() {
@@ -353,9 +413,22 @@ int run_backward(Model* m) {
     TRY(gemm(m, EPI_ACCUM, m->logits, Vp, 0, m->lnf, C, 0, G(m, 0), C, nullptr, nullptr, 0, nullptr,
              Vp, C, (int)BT));
     void* last = L == 0 ? m->encoded : act(m->residual3, L - 1, C);
-    TIMED(FAM_LN_BWD, lnb_bytes - 1.0 * BT * C * es,
-          launch_layernorm_backward(dt, m->dresidual, G(m, 14), G(m, 15), m->dbtc, last, P(m, 14),
-                                    m->lnf_mean, m->lnf_rstd, (int)BT, C, 0, m->ws, s));
+    // LayerNorm i backward into its partial area; the column sums of its output
+    // (the next-lower matmul's bias grad) come fused or from a colsum pass
+    auto ln_bwd = [&](int i, void* inp, const void* w, const float* mean, const float* rstd,
+                      int accumulate, bool need_cs) -> int {
+        int P_ = 0;
+        TIMED(FAM_LN_BWD, lnb_bytes - (accumulate ? 0.0 : 1.0 * BT * C * es),
+              P_ = launch_layernorm_backward_part(dt, m->dresidual, ln_part(m, i), m->dbtc, inp, w, mean,
+                                                  rstd, (int)BT, C, accumulate, m->ln_fused ? 1 : 0,
+                                                  m->d_err, s));
+        if (P_ != m->P_ln) return fail(GPT2_ERR_CUDA, "LayerNorm backward partial rows changed");
+        if (need_cs && !m->ln_fused)
+            TIMED(FAM_OTHER, 1.0 * BT * C * es,
+                  launch_colsum_part(dt, cs_part(m, i), m->dresidual, (int)BT, C, s));
+        return GPT2_OK;
+    };
+    TRY(ln_bwd(2 * L, last, P(m, 14), m->lnf_mean, m->lnf_rstd, 0, L > 0));
     for (int l = L - 1; l >= 0; l--) {
         void* resid_in = l == 0 ? m->encoded : act(m->residual3, l - 1, C);
         void* ln1 = act(m->ln1, l, C);
@@ -371,27 +444,22 @@ int run_backward(Model* m) {
                  m->dbt4c, 4 * C, nullptr, fch, 4 * C, nullptr, (int)BT, 4 * C, C));
         TRY(gemm(m, EPI_ACCUM, m->dresidual, C, 0, fchg, 4 * C, 0, G(m, 12) + (size_t)l * 4 * C * C * es,
                  4 * C, nullptr, nullptr, 0, nullptr, C, 4 * C, (int)BT));
-        TIMED(FAM_OTHER, 1.0 * BT * C * es,
-              launch_colsum_accum(dt, G(m, 13) + (size_t)l * C * es, m->dresidual, (int)BT, C, m->ws, s));
+        // (fcproj's bias grad: the column sums of the LayerNorm backward above)
         // fc (W: 4C x C)
         TRY(gemm(m, EPI_STORE, m->dbt4c, 4 * C, 1, P(m, 10) + (size_t)l * 4 * C * C * es, C, 0, m->dbtc,
                  C, nullptr, nullptr, 0, nullptr, (int)BT, C, 4 * C));
         TRY(gemm(m, EPI_ACCUM, m->dbt4c, 4 * C, 0, ln2, C, 0, G(m, 10) + (size_t)l * 4 * C * C * es, C,
                  nullptr, nullptr, 0, nullptr, 4 * C, C, (int)BT));
         TIMED(FAM_OTHER, 4.0 * BT * C * es,
-              launch_colsum_accum(dt, G(m, 11) + (size_t)l * 4 * C * es, m->dbt4c, (int)BT, 4 * C, m->ws, s));
-        TIMED(FAM_LN_BWD, lnb_bytes,
-              launch_layernorm_backward(dt, m->dresidual, G(m, 8) + (size_t)l * C * es,
-                                        G(m, 9) + (size_t)l * C * es, m->dbtc, res2,
-                                        P(m, 8) + (size_t)l * C * es, m->ln2_mean + l * BT,
-                                        m->ln2_rstd + l * BT, (int)BT, C, 1, m->ws, s));
+              launch_colsum_part(dt, fcb_part(m, l), m->dbt4c, (int)BT, 4 * C, s));
+        TRY(ln_bwd(2 * l + 1, res2, P(m, 8) + (size_t)l * C * es, m->ln2_mean + l * BT,
+                   m->ln2_rstd + l * BT, 1, true));
         // attention projection (W: C x C)
         TRY(gemm(m, EPI_STORE, m->dresidual, C, 1, P(m, 6) + (size_t)l * C * C * es, C, 0, m->dbtc, C,
                  nullptr, nullptr, 0, nullptr, (int)BT, C, C));
         TRY(gemm(m, EPI_ACCUM, m->dresidual, C, 0, atty, C, 0, G(m, 6) + (size_t)l * C * C * es, C,
                  nullptr, nullptr, 0, nullptr, C, C, (int)BT));
-        TIMED(FAM_OTHER, 1.0 * BT * C * es,
-              launch_colsum_accum(dt, G(m, 7) + (size_t)l * C * es, m->dresidual, (int)BT, C, m->ws, s));
+        // (attproj's bias grad: the column sums of LayerNorm 2's backward)
         // attention: dqkv (B,T,3C) into the 4C scratch
         {
             int rc_ = GPT2_OK;
@@ -406,13 +474,12 @@ int run_backward(Model* m) {
         TRY(gemm(m, EPI_ACCUM, m->dbt4c, 3 * C, 0, ln1, C, 0, G(m, 4) + (size_t)l * 3 * C * C * es, C,
                  nullptr, nullptr, 0, nullptr, 3 * C, C, (int)BT));
         TIMED(FAM_OTHER, 3.0 * BT * C * es,
-              launch_colsum_accum(dt, G(m, 5) + (size_t)l * 3 * C * es, m->dbt4c, (int)BT, 3 * C, m->ws, s));
-        TIMED(FAM_LN_BWD, lnb_bytes,
-              launch_layernorm_backward(dt, m->dresidual, G(m, 2) + (size_t)l * C * es,
-                                        G(m, 3) + (size_t)l * C * es, m->dbtc, resid_in,
-                                        P(m, 2) + (size_t)l * C * es, m->ln1_mean + l * BT,
-                                        m->ln1_rstd + l * BT, (int)BT, C, 1, m->ws, s));
+              launch_colsum_part(dt, qkvb_part(m, l), m->dbt4c, (int)BT, 3 * C, s));
+        TRY(ln_bwd(2 * l, resid_in, P(m, 2) + (size_t)l * C * es, m->ln1_mean + l * BT,
+                   m->ln1_rstd + l * BT, 1, l > 0));
     }
+    // every LayerNorm and bias grad: += its partial rows, summed in order
+    TIMED(FAM_OTHER, 0.0, launch_reduce_partials_multi(dt, m->d_desc, m->ndesc, 4 * C, s));
     TIMED(FAM_ENCODER, 2.0 * BT * C * es,
           launch_encoder_backward(dt, G(m, 0), G(m, 1), m->dresidual, m->tokens, B, T, C, Vp,
                                   m->enc_counts, m->enc_offsets, m->enc_cursor, m->enc_order,

@@ -77,6 +77,32 @@ size_t layernorm_backward_ws_floats(int C);
 void launch_colsum_accum(DType dt, void* dbias, const void* dout, int M, int N, float* ws,
                          cudaStream_t s);
 size_t colsum_ws_floats(int N);
+
+// ---- partial sums reduced once per backward ----
+// dst[c] += sum over p < P (in order) of part[p * pstride + c], c < width;
+// dst has the model's element type
+struct PartialDesc {
+    const float* part;
+    long long pstride;
+    int P, width;
+    void* dst;
+};
+// LayerNorm backward that leaves its parameter sums as partial rows
+// part[p][G*C] = [dw | db | colsum of the written dinp rows (G = 3)];
+// returns the row count P. The column sums are fused only where
+// layernorm_backward_fuses_colsum(dt, C); otherwise G = 2.
+bool layernorm_backward_fuses_colsum(DType dt, int C);
+int layernorm_backward_part_rows(DType dt, int N, int C);
+int launch_layernorm_backward_part(DType dt, void* dinp, float* part, const void* dout,
+                                   const void* inp, const void* w, const float* mean,
+                                   const float* rstd, int N, int C, int accumulate, int with_colsum,
+                                   unsigned int* err, cudaStream_t s);
+// column sums of dout (M, N) as partial rows part[R][N]; returns R
+int colsum_part_rows(int M);
+int launch_colsum_part(DType dt, float* part, const void* dout, int M, int N, cudaStream_t s);
+// one launch over a device table of descriptors
+void launch_reduce_partials_multi(DType dt, const PartialDesc* d_desc, int ndesc, int maxwidth,
+                                  cudaStream_t s);
 // logits (BT, Vp) -> dlogits in place; losses[BT] fp32
 void launch_classifier(DType dt, void* logits, float* losses, const int* targets, int BT, int V,
                        int Vp, float dloss, cudaStream_t s);

@@ -8,6 +8,7 @@
 // training step) unless stated otherwise.
 #include "common.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 #include <math.h>
 #include <stdlib.h>
@@ -567,6 +568,203 @@ __global__ void __launch_bounds__(LNB_BLOCK, 1) layernorm_backward_reg_k(
     }
 }
 
+// The same operation (bf16, C <= 768) as a persistent kernel fed by bulk
+// copies: one producer thread streams each of the CTA's rows (x, dy and, for
+// +=, the current dx) from HBM into a ring of LNQ_RING shared-memory slots with
+// cp.async.bulk, so up to LNQ_RING rows per SM are in flight; seven consumer
+// warps take the slots in turn (warp per row), keep dw / db partials in
+// registers and write dx. With `with_colsum` they also sum the written dx rows
+// by column (the bias gradient of the matmul that produced this residual-stream
+// gradient). The block folds its warps in order and writes one partial row
+// [dw | db | colsum] of G*C floats to part[blockIdx.x].
+constexpr int LNQ_RING = 20;
+constexpr int LNQ_WARPS = 7;  // consumer warps; warp LNQ_WARPS is the producer (8 warps: 2 per SM quarter)
+
+template <int NV>
+__global__ void __launch_bounds__(32 * (LNQ_WARPS + 1)) layernorm_backward_bulk_k(
+    bf16* __restrict__ dinp, float* __restrict__ part, const bf16* __restrict__ dout,
+    const bf16* __restrict__ inp, const bf16* __restrict__ w, const float* __restrict__ mean,
+    const float* __restrict__ rstd, int N, int C, int accumulate, int with_colsum,
+    unsigned int* __restrict__ err) {
+    constexpr int VEC = 8;
+    extern __shared__ __align__(128) uint8_t lnq_sm[];
+    const int rowb = C * 2, slotb = 3 * rowb;
+    uint8_t* ring = lnq_sm;
+    const uint32_t ring_s = tc::smem_u32(ring);
+    uint8_t* tail = lnq_sm + (size_t)LNQ_RING * slotb;
+    const uint32_t bars = tc::smem_u32(tail);
+    auto full = [&](int s) { return bars + 8u * s; };
+    auto empty = [&](int s) { return bars + 8u * (LNQ_RING + s); };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tail + 16 * LNQ_RING);
+    int* issued_s = reinterpret_cast<int*>(tail + 16 * LNQ_RING + 4);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < LNQ_RING; s++) {
+            tc::mbar_init(full(s), 1);
+            tc::mbar_init(empty(s), 1);
+        }
+        *abort_flag = 0;
+        *issued_s = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    pdl_enter();
+    const int nk = (N - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;  // rows of this CTA
+    const int cv = C / VEC;
+    const int G = with_colsum ? 3 : 2;
+    float adw[NV][VEC], adb[NV][VEC], acs[NV][VEC];  // consumer partial sums
+#pragma unroll
+    for (int j = 0; j < NV; j++)
+#pragma unroll
+        for (int e = 0; e < VEC; e++) adw[j][e] = adb[j][e] = acs[j][e] = 0.f;
+    if (warp == LNQ_WARPS) {
+        if (lane == 0) {
+            int issued = 0;
+            const uint32_t bytes = (uint32_t)(accumulate ? 3 * rowb : 2 * rowb);
+            for (int k = 0; k < nk; k++) {
+                const int s = k % LNQ_RING;
+                if (!tc::mbar_wait(empty(s), (uint32_t)(((k / LNQ_RING) & 1) ^ 1), abort_flag)) break;
+                const size_t r = (size_t)blockIdx.x + (size_t)k * gridDim.x;
+                const uint32_t dst = ring_s + (uint32_t)(s * slotb);
+                tc::mbar_expect_tx(full(s), bytes);
+                tc::bulk_load(dst, inp + r * C, (uint32_t)rowb, full(s));
+                tc::bulk_load(dst + rowb, dout + r * C, (uint32_t)rowb, full(s));
+                if (accumulate) tc::bulk_load(dst + 2 * rowb, dinp + r * C, (uint32_t)rowb, full(s));
+                ++issued;
+            }
+            *issued_s = issued;
+        }
+    } else {
+        Vec16<bf16> wv[NV];
+#pragma unroll
+        for (int j = 0; j < NV; j++) {
+            const int vi = lane + 32 * j;
+            if (vi < cv) wv[j] = ld16(w + vi * VEC);
+        }
+        float mu = 0.f, rs = 0.f;
+        if (warp < nk) {
+            const size_t r = (size_t)blockIdx.x + (size_t)warp * gridDim.x;
+            mu = mean[r];
+            rs = rstd[r];
+        }
+        for (int k = warp; k < nk; k += LNQ_WARPS) {
+            const size_t r = (size_t)blockIdx.x + (size_t)k * gridDim.x;
+            // the next row's statistics, a row ahead
+            float mu2 = 0.f, rs2 = 0.f;
+            if (k + LNQ_WARPS < nk) {
+                const size_t r2 = r + (size_t)LNQ_WARPS * gridDim.x;
+                mu2 = mean[r2];
+                rs2 = rstd[r2];
+            }
+            const int s = k % LNQ_RING;
+            int ok = 1;
+            if (lane == 0) ok = tc::mbar_wait(full(s), (uint32_t)((k / LNQ_RING) & 1), abort_flag) ? 1 : 0;
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            const uint8_t* slot = ring + (size_t)s * slotb;
+            Vec16<bf16> xv[NV], dv[NV], ov[NV];
+#pragma unroll
+            for (int j = 0; j < NV; j++) {
+                const int vi = lane + 32 * j;
+                if (vi < cv) {
+                    xv[j] = *reinterpret_cast<const Vec16<bf16>*>(slot + vi * 16);
+                    dv[j] = *reinterpret_cast<const Vec16<bf16>*>(slot + rowb + vi * 16);
+                    if (accumulate) ov[j] = *reinterpret_cast<const Vec16<bf16>*>(slot + 2 * rowb + vi * 16);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(empty(s));  // the slot is in registers
+            float gsum = 0.f, gnsum = 0.f;
+#pragma unroll
+            for (int j = 0; j < NV; j++) {
+                if (lane + 32 * j < cv) {
+#pragma unroll
+                    for (int e = 0; e < VEC; e++) {
+                        const float g = to_f(wv[j].v[e]) * to_f(dv[j].v[e]);
+                        gsum += g;
+                        gnsum += g * (to_f(xv[j].v[e]) - mu) * rs;
+                    }
+                }
+            }
+            gsum = warp_sum(gsum) / C;
+            gnsum = warp_sum(gnsum) / C;
+            bf16* dx = dinp + r * C;
+#pragma unroll
+            for (int j = 0; j < NV; j++) {
+                const int vi = lane + 32 * j;
+                if (vi < cv) {
+                    Vec16<bf16> o;
+#pragma unroll
+                    for (int e = 0; e < VEC; e++) {
+                        const float d = to_f(dv[j].v[e]);
+                        const float nh = (to_f(xv[j].v[e]) - mu) * rs;
+                        const float val = rs * (to_f(wv[j].v[e]) * d - gsum - nh * gnsum);
+                        o.v[e] = from_f<bf16>(accumulate ? to_f(ov[j].v[e]) + val : val);
+                        adw[j][e] += nh * d;
+                        adb[j][e] += d;
+                        acs[j][e] += to_f(o.v[e]);
+                    }
+                    st16(dx + vi * VEC, o);
+                }
+            }
+            mu = mu2;
+            rs = rs2;
+        }
+    }
+    __syncthreads();
+    if (*abort_flag) {
+        // let every issued copy land before the ring is reused or released
+        if (threadIdx.x == 32 * LNQ_WARPS) {
+            const int issued = *issued_s;
+            for (int s = 0; s < LNQ_RING && s < issued; s++) {
+                const int lst = s + ((issued - 1 - s) / LNQ_RING) * LNQ_RING;
+                tc::mbar_wait_drain(full(s), (uint32_t)((lst / LNQ_RING) & 1));
+            }
+            atomicOr(err, DEVERR_TIMEOUT);
+        }
+        __syncthreads();
+    }
+    // fold the consumer warps in order through the (now idle) ring memory
+    float* fold = reinterpret_cast<float*>(lnq_sm);  // [LNQ_WARPS][G*C]
+    if (warp < LNQ_WARPS) {
+        float* mine = fold + (size_t)warp * G * C;
+#pragma unroll
+        for (int j = 0; j < NV; j++) {
+            const int vi = lane + 32 * j;
+            if (vi < cv) {
+#pragma unroll
+                for (int e = 0; e < VEC; e++) {
+                    mine[vi * VEC + e] = adw[j][e];
+                    mine[C + vi * VEC + e] = adb[j][e];
+                    if (with_colsum) mine[2 * C + vi * VEC + e] = acs[j][e];
+                }
+            }
+        }
+    }
+    __syncthreads();
+    float* dst = part + (size_t)blockIdx.x * G * C;
+    for (int c = threadIdx.x; c < G * C; c += blockDim.x) {
+        float t = 0.f;
+        for (int wi = 0; wi < LNQ_WARPS; wi++) t += fold[(size_t)wi * G * C + c];
+        dst[c] = t;
+    }
+}
+
+// dst[c] (+)= sum over p of part[p * pstride + c] for every descriptor, summed in
+// increasing p (one launch for many parameter tensors)
+template <typename T>
+__global__ void __launch_bounds__(256) reduce_partials_multi_k(const PartialDesc* __restrict__ d) {
+    pdl_enter();
+    const PartialDesc pd = d[blockIdx.y];
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= pd.width) return;
+    const float* p = pd.part + c;
+    float acc = 0.f;
+#pragma unroll 8
+    for (int i = 0; i < pd.P; i++) acc += p[(size_t)i * pd.pstride];
+    T* o = (T*)pd.dst + c;
+    *o = from_f<T>(to_f(*o) + acc);
+}
+
 // dst[c] += sum over p of ws[p][c] for c in [0, W), summed in increasing p;
 // columns [split, W) go to dst2[c - split]. One warp per (32-column group,
 // p residue mod 8), folded across the 8 warps in order.
@@ -673,6 +871,90 @@ void launch_layernorm_backward(DType dt, void* dinp, void* dw, void* db, const v
 #undef LNB
 }
 
+// ------------------------------------------------------------------ partial-row form
+bool layernorm_backward_fuses_colsum(DType dt, int C) {
+    return dt == DT_BF16 && (C / 8 + 31) / 32 <= 3 && (C * 2) % 16 == 0;
+}
+
+int layernorm_backward_part_rows(DType dt, int N, int C) {
+    if (layernorm_backward_fuses_colsum(dt, C)) return N < num_sms() ? N : num_sms();
+    const size_t smem = sizeof(float) * 2 * C * (LNB_BLOCK / 32);
+    const int nv = (C / (dt == DT_BF16 ? 8 : 4) + 31) / 32;
+    if (dt == DT_BF16) {
+        switch (nv) {
+            case 4: return lnb_blocks<bf16, 4>(N, smem); case 5: return lnb_blocks<bf16, 5>(N, smem);
+            case 6: return lnb_blocks<bf16, 6>(N, smem); case 7: return lnb_blocks<bf16, 7>(N, smem);
+            default: return lnb_blocks<bf16, 8>(N, smem);
+        }
+    }
+    switch (nv) {
+        case 1: return lnb_blocks<float, 1>(N, smem); case 2: return lnb_blocks<float, 2>(N, smem);
+        case 3: return lnb_blocks<float, 3>(N, smem); case 4: return lnb_blocks<float, 4>(N, smem);
+        case 5: return lnb_blocks<float, 5>(N, smem); case 6: return lnb_blocks<float, 6>(N, smem);
+        case 7: return lnb_blocks<float, 7>(N, smem); default: return lnb_blocks<float, 8>(N, smem);
+    }
+}
+
+template <int NV> static size_t lnq_opt_in(int C) {
+    const size_t smem = (size_t)LNQ_RING * 3 * C * 2 + 16 * LNQ_RING + 16;
+    static size_t done = 0;
+    if (smem > done) {
+        cudaFuncSetAttribute(layernorm_backward_bulk_k<NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+        done = smem;
+    }
+    return smem;
+}
+
+int launch_layernorm_backward_part(DType dt, void* dinp, float* part, const void* dout,
+                                   const void* inp, const void* w, const float* mean,
+                                   const float* rstd, int N, int C, int accumulate, int with_colsum,
+                                   unsigned int* err, cudaStream_t s) {
+    const int P = layernorm_backward_part_rows(dt, N, C);
+    if (layernorm_backward_fuses_colsum(dt, C)) {
+        const int nv = (C / 8 + 31) / 32;
+        note_launch(1);
+#define LNQ(NVV)                                                                                 \
+    launch_pdl(layernorm_backward_bulk_k<NVV>, dim3(P), dim3(32 * (LNQ_WARPS + 1)),               \
+               lnq_opt_in<NVV>(C), s, (bf16*)dinp, part, (const bf16*)dout, (const bf16*)inp,     \
+               (const bf16*)w, mean, rstd, N, C, accumulate, with_colsum, err)
+        if (nv == 1) LNQ(1);
+        else if (nv == 2) LNQ(2);
+        else LNQ(3);
+#undef LNQ
+        return P;
+    }
+    note_launch(1);
+    const size_t smem = sizeof(float) * 2 * C * (LNB_BLOCK / 32);
+    const int nv = (C / (dt == DT_BF16 ? 8 : 4) + 31) / 32;
+#define LNB2(TT, NVV)                                                                            \
+    launch_pdl(layernorm_backward_k<TT, NVV>, dim3(P), dim3(LNB_BLOCK), smem, s, (TT*)dinp, part,  \
+               (const TT*)dout, (const TT*)inp, (const TT*)w, mean, rstd, N, C, accumulate)
+    if (dt == DT_BF16) {
+        switch (nv) {
+            case 4: LNB2(bf16, 4); break; case 5: LNB2(bf16, 5); break; case 6: LNB2(bf16, 6); break;
+            case 7: LNB2(bf16, 7); break; default: LNB2(bf16, 8); break;
+        }
+    } else {
+        switch (nv) {
+            case 1: LNB2(float, 1); break; case 2: LNB2(float, 2); break; case 3: LNB2(float, 3); break;
+            case 4: LNB2(float, 4); break; case 5: LNB2(float, 5); break; case 6: LNB2(float, 6); break;
+            case 7: LNB2(float, 7); break; default: LNB2(float, 8); break;
+        }
+    }
+#undef LNB2
+    return P;
+}
+
+void launch_reduce_partials_multi(DType dt, const PartialDesc* d_desc, int ndesc, int maxwidth,
+                                  cudaStream_t s) {
+    if (ndesc <= 0) return;
+    note_launch(1);
+    const dim3 grid((unsigned)((maxwidth + 255) / 256), (unsigned)ndesc);
+    if (dt == DT_BF16) launch_pdl(reduce_partials_multi_k<bf16>, grid, dim3(256), 0, s, d_desc);
+    else launch_pdl(reduce_partials_multi_k<float>, grid, dim3(256), 0, s, d_desc);
+}
+
 // ------------------------------------------------------------------ bias gradient
 // matmul_backward_bias_kernel4 read with +=: dbias[n] += sum over rows of dout[:, n].
 // Stage 1: block (x: 32*VEC columns, y: a slab of rows), 8 warps stride the
@@ -722,6 +1004,25 @@ __global__ void __launch_bounds__(256) colsum_partial_k(float* __restrict__ ws,
 }
 
 size_t colsum_ws_floats(int N) { return (size_t)CS_SLABS * N; }
+
+int colsum_part_rows(int M) {
+    int R = (M + 31) / 32;
+    if (R > CS_SLABS) R = CS_SLABS;
+    if (R < 1) R = 1;
+    const int rps = (M + R - 1) / R;
+    return (M + rps - 1) / rps;
+}
+
+int launch_colsum_part(DType dt, float* part, const void* dout, int M, int N, cudaStream_t s) {
+    const int R = colsum_part_rows(M);
+    const int rps = (M + R - 1) / R;
+    const int VEC = dt == DT_BF16 ? 8 : 4;
+    const dim3 grid((N + 32 * VEC - 1) / (32 * VEC), R);
+    note_launch(1);
+    if (dt == DT_BF16) launch_pdl(colsum_partial_k<bf16>, grid, dim3(256), 0, s, part, (const bf16*)dout, M, N, rps);
+    else launch_pdl(colsum_partial_k<float>, grid, dim3(256), 0, s, part, (const float*)dout, M, N, rps);
+    return R;
+}
 
 void launch_colsum_accum(DType dt, void* dbias, const void* dout, int M, int N, float* ws,
                          cudaStream_t s) {

@@ -76,6 +76,13 @@ DEVI void tma_load_2d(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int x, 
         : "memory");
 }
 
+// untiled bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0)
+DEVI void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 DEVI void tma_load_3d(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int x, int y, int z) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"

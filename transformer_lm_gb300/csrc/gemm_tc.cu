@@ -47,21 +47,28 @@ constexpr int EPI_THREADS = 32 * EPI_WARPS;
 constexpr int NUM_THREADS = 64 + EPI_THREADS;
 constexpr int GROUP_M = 16;  // m-blocks per rasterisation group (L2 locality of A and B)
 
-constexpr int EPI_BUFS = 2;               // epilogue staging buffers
-constexpr int EPI_BUF_BYTES = BM * ROWB;  // 128 rows x 128 bytes
+constexpr int EPI_BUF_BYTES = BM * ROWB;  // one epilogue staging buffer: 128 rows x 128 bytes
+// staging buffers per epilogue: the two-output and element-heavy epilogues
+// take four, so that two sub-tiles' stores (and the next operand load) stay
+// in flight while the next sub-tile is written; the rest keep two and one
+// more pipeline stage
+template <int EPI> __host__ __device__ constexpr int epi_bufs() {
+    return (EPI == EPI_GELU || EPI == EPI_GELU_BWD || EPI == EPI_SPLITK) ? 4 : 2;
+}
 
 // CG = CTAs per MMA: 1 (tcgen05 cta_group::1, 128 x BN tiles) or 2 (a CTA
 // pair runs cta_group::2 MMAs on 256 x BN tiles; each CTA holds 128 rows of A
 // and BN/2 rows of B in its shared memory and its 128 accumulator rows in TMEM)
-template <int BN, int CG> struct Cfg {
+template <int BN, int CG, int EB> struct Cfg {
     static constexpr int A_BYTES = BM * ROWB;
     static constexpr int B_BYTES = (BN / CG) * ROWB;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (192 * 1024) / STAGE_BYTES;
-    static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int BAR_BYTES = 256 + 1024;  // barriers, flags, per-row softmax partials
+    static constexpr int STAGES = (224 * 1024 - EB * EPI_BUF_BYTES - BAR_BYTES - 1024) / STAGE_BYTES;
+    static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int SMEM_BYTES =
-        STAGES * STAGE_BYTES + EPI_BUFS * EPI_BUF_BYTES + BAR_BYTES + 1024;
+        STAGES * STAGE_BYTES + EB * EPI_BUF_BYTES + BAR_BYTES + 1024;
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
 struct Args {
@@ -173,7 +180,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_k(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
               const __grid_constant__ CUtensorMap tmX, const __grid_constant__ Args args) {
-    using C = Cfg<BN, CG>;
+    constexpr int EPI_BUFS = epi_bufs<EPI>();
+    using C = Cfg<BN, CG, EPI_BUFS>;
     using T = typename std::conditional<KIND == 0, bf16, float>::type;
     constexpr int KE = ROWB / (int)sizeof(T);  // K elements per stage
     constexpr int UK = KIND == 0 ? 16 : 8;     // K elements per MMA
@@ -595,7 +603,7 @@ struct Maps {
 // clusters as can be co-resident (cudaOccupancyMaxActiveClusters).
 template <int BN, int KIND, int EPI, int CG>
 static int launch_tc(const Maps& mp, const tc::Args& a, cudaStream_t s) {
-    using C = tc::Cfg<BN, CG>;
+    using C = tc::Cfg<BN, CG, tc::epi_bufs<EPI>()>;
     auto kern = tc::gemm_tc_k<BN, KIND, EPI, CG>;
     static bool attr_done = false;
     static int max_clusters = 0;

@@ -16,10 +16,10 @@
 //        dV += P^T dO, dK += dS^T Q accumulating in TMEM;
 //   DQ   one CTA per (128-query tile, b, h); it walks the key blocks at and
 //        before its queries with S = Q K^T, dP = dO V^T and dQ += dS K.
-// Roles (320 threads): warp 0 loads the streamed Q/dO (or K/V) blocks into a
+// Roles (576 threads): warp 0 loads the streamed Q/dO (or K/V) blocks into a
 // 3-stage ring by TMA (and, for DKV, the blocks' LSE and D into shared
-// memory); one thread of warp 1 issues the MMAs; warps 2..9 form P and dS,
-// two warps per TMEM lane quarter, each on 64 of the 128 columns. S is
+// memory); one thread of warp 1 issues the MMAs; warps 2..17 form P and dS,
+// four warps per TMEM lane quarter, each on 32 of the 128 columns. S is
 // double-buffered in TMEM, so the next block's S = ... MMA overlaps the
 // current block's softmax. All waits are bounded; on expiry the CTA records
 // DEVERR_TIMEOUT, drains its copies and MMAs and frees TMEM.
@@ -38,10 +38,10 @@ namespace fabw {
 using namespace tc;
 
 constexpr int HSZ = 64;
-constexpr int BLK = 128;                   // rows per CTA and columns per block
+constexpr int BLK = 128;                   // rows per work item and columns per block
 constexpr int STAGES = 3;
 constexpr int TILE = 128 * 128;            // 128 rows x 64 bf16, 128B-swizzled
-constexpr int OFF_X0 = 0;                  // fixed tiles: K, V (DKV) or Q, dO (DQ)
+constexpr int OFF_X0 = 0;                  // fixed tiles of the current item: K, V (DKV) or Q, dO (DQ)
 constexpr int OFF_X1 = TILE;
 constexpr int OFF_Y = 2 * TILE;            // ring: stage s holds Y0 at +2s*TILE, Y1 at +(2s+1)*TILE
 constexpr int OFF_P = OFF_Y + STAGES * 2 * TILE;  // P^T (DKV), two 64-column atoms
@@ -49,7 +49,10 @@ constexpr int OFF_DS = OFF_P + 2 * TILE;          // dS^T (DKV) or dS (DQ)
 constexpr int OFF_VEC = OFF_DS + 2 * TILE;        // per stage: -LSE*log2(e) [128], D [128]
 constexpr int OFF_BAR = OFF_VEC + STAGES * 1024;
 constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;
-constexpr int NUM_THREADS = 320;
+constexpr int CW = 16;                     // compute warps (P and dS)
+constexpr int CQ = CW / 4;                 // compute warps per TMEM lane quarter
+constexpr int COLS = 128 / CQ;             // columns per compute thread
+constexpr int NUM_THREADS = 64 + 32 * CW;
 constexpr int TMEM_COLS = 512;  // S0 0, S1 128, dP 256, acc0 384 (dV / dQ), acc1 448 (dK)
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -57,11 +60,32 @@ struct BwdArgs {
     bf16* dqkv;
     const float* lse;
     const float* D;
-    int T, C, NH, BH, nblk;
+    int T, C, NH, BH, nblk, items;
     float scale, scale_log2;
     unsigned int* err;
 };
 
+// One work item: (tile, b, h), heaviest tiles first across all heads (key
+// tile 0 meets every query block, query tile nblk-1 every key block).
+struct Item {
+    int tile, bh, b, h, r0, n;
+};
+template <bool DKV> DEVI Item decode_item(const BwdArgs& a, int idx) {
+    Item it;
+    const int grp = idx / a.BH;
+    it.bh = idx % a.BH;
+    it.tile = DKV ? grp : a.nblk - 1 - grp;
+    it.b = it.bh / a.NH;
+    it.h = it.bh % a.NH;
+    it.r0 = it.tile * BLK;
+    it.n = DKV ? a.nblk - it.tile : it.tile + 1;  // column blocks visited
+    return it;
+}
+
+// Persistent: each CTA takes one item per round (a snake over the CTAs);
+// the ring, the S/dP buffers and every barrier phase run on counters global
+// to the CTA, so the next item's loads and first MMAs overlap this item's
+// last blocks and its epilogue.
 template <bool DKV>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     flash_bwd_tc_k(const __grid_constant__ CUtensorMap tqkv, const __grid_constant__ CUtensorMap tdo,
@@ -72,51 +96,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t* base_ptr = smem_raw + (base - raw);
     const uint32_t bars = base + OFF_BAR;
     uint8_t* bars_ptr = base_ptr + OFF_BAR;
-    const uint32_t fixed_full = bars;
-    auto st_full = [&](int s) { return bars + 8u * (1 + s); };
-    auto st_empty = [&](int s) { return bars + 8u * (4 + s); };
-    auto s_full = [&](int b) { return bars + 8u * (7 + b); };
-    auto s_empty = [&](int b) { return bars + 8u * (9 + b); };
-    const uint32_t dp_full = bars + 8u * 11, dp_empty = bars + 8u * 12;
-    const uint32_t p_full = bars + 8u * 13, p_empty = bars + 8u * 14;
-    const uint32_t ds_full = bars + 8u * 15, ds_empty = bars + 8u * 16;
-    const uint32_t acc_full = bars + 8u * 17, drain = bars + 8u * 18;
-    constexpr int NBARS = 19;
+    const uint32_t x_full = bars, x_empty = bars + 8u;
+    auto st_full = [&](int s) { return bars + 8u * (2 + s); };
+    auto st_empty = [&](int s) { return bars + 8u * (5 + s); };
+    auto s_full = [&](int b) { return bars + 8u * (8 + b); };
+    auto s_empty = [&](int b) { return bars + 8u * (10 + b); };
+    const uint32_t dp_full = bars + 8u * 12, dp_empty = bars + 8u * 13;
+    const uint32_t p_full = bars + 8u * 14, p_empty = bars + 8u * 15;
+    const uint32_t ds_full = bars + 8u * 16, ds_empty = bars + 8u * 17;
+    const uint32_t acc_full = bars + 8u * 18, acc_empty = bars + 8u * 19, drain = bars + 8u * 20;
+    constexpr int NBARS = 21;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars_ptr + 8 * NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars_ptr + 8 * NBARS + 4);
-    int* n_issued_smem = reinterpret_cast<int*>(bars_ptr + 8 * NBARS + 8);
+    int* n_issued_smem = reinterpret_cast<int*>(bars_ptr + 8 * NBARS + 8);   // ring loads issued
+    int* x_issued_smem = reinterpret_cast<int*>(bars_ptr + 8 * NBARS + 12);  // fixed-tile loads issued
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const int T = a.T, C = a.C;
-    // heaviest tiles first across all heads: key tile 0 meets every query
-    // block, query tile nblk-1 meets every key block
-    const int grp = (int)blockIdx.x / a.BH, bh = (int)blockIdx.x % a.BH;
-    const int tile = DKV ? grp : a.nblk - 1 - grp;
-    const int b = bh / a.NH, h = bh % a.NH;
-    const int r0 = tile * BLK;
-    const int n = DKV ? a.nblk - tile : tile + 1;  // column blocks visited
-    auto col0 = [&](int u) { return (DKV ? tile + u : u) * BLK; };
 
     if (threadIdx.x == 0) {
-        mbar_init(fixed_full, 1);
+        mbar_init(x_full, 1);
+        mbar_init(x_empty, 1);
         for (int s = 0; s < STAGES; s++) {
             mbar_init(st_full(s), 1);
             mbar_init(st_empty(s), 1);
         }
         for (int q = 0; q < 2; q++) {
             mbar_init(s_full(q), 1);
-            mbar_init(s_empty(q), 8);
+            mbar_init(s_empty(q), CW);
         }
         mbar_init(dp_full, 1);
-        mbar_init(dp_empty, 8);
-        mbar_init(p_full, 8);
+        mbar_init(dp_empty, CW);
+        mbar_init(p_full, CW);
         mbar_init(p_empty, 1);
-        mbar_init(ds_full, 8);
+        mbar_init(ds_full, CW);
         mbar_init(ds_empty, 1);
         mbar_init(acc_full, 1);
+        mbar_init(acc_empty, CW);
         mbar_init(drain, 1);
         *abort_flag = 0;
         *n_issued_smem = 0;
+        *x_issued_smem = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -130,6 +150,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
     pdl_enter();  // global memory is touched only from here on
 
+    // round t of the item walk: a snake over the CTAs (forward on even
+    // rounds, backward on odd ones) evens out the heavy-first item sizes
+    auto item_of = [&](int t) {
+        const int G = (int)gridDim.x, c = (int)blockIdx.x;
+        return t * G + ((t & 1) ? G - 1 - c : c);
+    };
+
     // warp-uniform bounded wait
     auto wait_warp = [&](uint32_t bar, uint32_t parity) {
         int w = 1;
@@ -137,58 +164,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         return __shfl_sync(0xffffffffu, w, 0) != 0;
     };
 
-    // column offsets (elements) of Q, K, V within a row of qkv
-    const int xq = h * HSZ, xk = C + h * HSZ, xv = 2 * C + h * HSZ;
-
     if (warp == 0) {
         // ---------------- loads
-        int issued = 0;
-        if (lane == 0) {
-            mbar_expect_tx(fixed_full, 2 * TILE);
-            if (DKV) {
-                tma_load_3d(base + OFF_X0, &tqkv, fixed_full, xk, r0, b);
-                tma_load_3d(base + OFF_X1, &tqkv, fixed_full, xv, r0, b);
-            } else {
-                tma_load_3d(base + OFF_X0, &tqkv, fixed_full, xq, r0, b);
-                tma_load_3d(base + OFF_X1, &tdo, fixed_full, h * HSZ, r0, b);
-            }
-        }
-        for (int u = 0; u < n; u++) {
-            const int st = u % STAGES;
-            if (!wait_warp(st_empty(st), (uint32_t)(((u / STAGES) & 1) ^ 1))) break;
-            const int c0 = col0(u);
-            if (DKV) {
-                // the block's LSE (as -LSE * log2 e; -inf past the sequence end,
-                // which zeroes those columns of P) and D
-                float4 nl, dd;
-                float* pn = &nl.x;
-                float* pd = &dd.x;
-#pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    const int q = c0 + lane * 4 + e;
-                    const bool in = q < T;
-                    pn[e] = in ? -a.lse[(size_t)bh * T + q] * LOG2E : -INFINITY;
-                    pd[e] = in ? a.D[(size_t)bh * T + q] : 0.f;
-                }
-                float* vec = reinterpret_cast<float*>(base_ptr + OFF_VEC + st * 1024);
-                reinterpret_cast<float4*>(vec)[lane] = nl;
-                reinterpret_cast<float4*>(vec + 128)[lane] = dd;
-                __syncwarp();
-            }
+        int g = 0, nx = 0;
+        bool ok = true;
+        for (int t = 0, idx = item_of(0); ok && idx < a.items; idx = item_of(++t)) {
+            const Item it = decode_item<DKV>(a, idx);
+            const int xq = it.h * HSZ, xk = C + it.h * HSZ, xv = 2 * C + it.h * HSZ;
+            if (!wait_warp(x_empty, (uint32_t)((t & 1) ^ 1))) break;
             if (lane == 0) {
-                const uint32_t y = base + OFF_Y + st * 2 * TILE;
-                mbar_expect_tx(st_full(st), 2 * TILE);
+                mbar_expect_tx(x_full, 2 * TILE);
                 if (DKV) {
-                    tma_load_3d(y, &tqkv, st_full(st), xq, c0, b);
-                    tma_load_3d(y + TILE, &tdo, st_full(st), h * HSZ, c0, b);
+                    tma_load_3d(base + OFF_X0, &tqkv, x_full, xk, it.r0, it.b);
+                    tma_load_3d(base + OFF_X1, &tqkv, x_full, xv, it.r0, it.b);
                 } else {
-                    tma_load_3d(y, &tqkv, st_full(st), xk, c0, b);
-                    tma_load_3d(y + TILE, &tqkv, st_full(st), xv, c0, b);
+                    tma_load_3d(base + OFF_X0, &tqkv, x_full, xq, it.r0, it.b);
+                    tma_load_3d(base + OFF_X1, &tdo, x_full, it.h * HSZ, it.r0, it.b);
                 }
             }
-            ++issued;
+            ++nx;
+            for (int u = 0; u < it.n; u++, g++) {
+                const int st = g % STAGES;
+                if (!wait_warp(st_empty(st), (uint32_t)(((g / STAGES) & 1) ^ 1))) { ok = false; break; }
+                const int c0 = (DKV ? it.tile + u : u) * BLK;
+                if (DKV) {
+                    // the block's LSE (as -LSE * log2 e; -inf past the sequence end,
+                    // which zeroes those columns of P) and D
+                    float4 nl, dd;
+                    float* pn = &nl.x;
+                    float* pd = &dd.x;
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const int q = c0 + lane * 4 + e;
+                        const bool in = q < T;
+                        pn[e] = in ? -a.lse[(size_t)it.bh * T + q] * LOG2E : -INFINITY;
+                        pd[e] = in ? a.D[(size_t)it.bh * T + q] : 0.f;
+                    }
+                    float* vec = reinterpret_cast<float*>(base_ptr + OFF_VEC + st * 1024);
+                    reinterpret_cast<float4*>(vec)[lane] = nl;
+                    reinterpret_cast<float4*>(vec + 128)[lane] = dd;
+                    __syncwarp();
+                }
+                if (lane == 0) {
+                    const uint32_t y = base + OFF_Y + st * 2 * TILE;
+                    mbar_expect_tx(st_full(st), 2 * TILE);
+                    if (DKV) {
+                        tma_load_3d(y, &tqkv, st_full(st), xq, c0, it.b);
+                        tma_load_3d(y + TILE, &tdo, st_full(st), it.h * HSZ, c0, it.b);
+                    } else {
+                        tma_load_3d(y, &tqkv, st_full(st), xk, c0, it.b);
+                        tma_load_3d(y + TILE, &tqkv, st_full(st), xv, c0, it.b);
+                    }
+                }
+            }
         }
-        if (lane == 0) *n_issued_smem = issued;
+        if (lane == 0) {
+            *n_issued_smem = g;
+            *x_issued_smem = nx;
+        }
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer
@@ -196,7 +229,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t idAcc = idesc<0>(0, 1, BLK, HSZ); // acc += (P|dS) Y: Y is MN-major
             const uint32_t tS0 = tmem_base, tdP = tmem_base + 256;
             const uint32_t tA0 = tmem_base + 384, tA1 = tmem_base + 448;
-            auto ybuf = [&](int u, int which) { return base + OFF_Y + (u % STAGES) * 2 * TILE + which * TILE; };
+            auto ybuf = [&](int g, int which) { return base + OFF_Y + (g % STAGES) * 2 * TILE + which * TILE; };
             auto issue_qk = [&](uint32_t d, uint32_t x, uint32_t y) {
 #pragma unroll
                 for (int k = 0; k < HSZ / 16; k++)
@@ -209,198 +242,201 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     umma<0, 1>(d, sdesc(pa + (k >> 2) * TILE + (k & 3) * 32, 16, 1024),
                                sdesc(y + k * 2048, 8192, 1024), idAcc, (accumulate || k) ? 1u : 0u);
             };
-            auto issue_s = [&](int u) {
-                issue_qk(tS0 + (uint32_t)((u & 1) * 128), base + OFF_X0, ybuf(u, 0));
-                umma_commit<1>(s_full(u & 1));
+            // S of global block g once its ring stage landed and its S buffer was read
+            auto issue_s = [&](int g) {
+                if (!mbar_wait(st_full(g % STAGES), (uint32_t)((g / STAGES) & 1), abort_flag) ||
+                    !mbar_wait(s_empty(g & 1), (uint32_t)(((g >> 1) & 1) ^ 1), abort_flag))
+                    return false;
+                tc_fence_after();
+                issue_qk(tS0 + (uint32_t)((g & 1) * 128), base + OFF_X0, ybuf(g, 0));
+                umma_commit<1>(s_full(g & 1));
+                return true;
             };
-            auto issue_dp = [&](int u) {
-                issue_qk(tdP, base + OFF_X1, ybuf(u, 1));
+            // dP of global block g once the previous dP was read
+            auto issue_dp = [&](int g) {
+                if (!mbar_wait(dp_empty, (uint32_t)((g & 1) ^ 1), abort_flag)) return false;
+                tc_fence_after();
+                issue_qk(tdP, base + OFF_X1, ybuf(g, 1));
                 umma_commit<1>(dp_full);
+                return true;
             };
-            bool ok = mbar_wait(fixed_full, 0, abort_flag) && mbar_wait(st_full(0), 0, abort_flag);
-            if (ok) {
+            int g0 = 0;
+            bool ok = true;
+            for (int t = 0, idx = item_of(0); ok && idx < a.items; idx = item_of(++t)) {
+                const int n = decode_item<DKV>(a, idx).n;
+                if (!mbar_wait(x_full, (uint32_t)(t & 1), abort_flag)) break;
                 tc_fence_after();
-                issue_s(0);
-                issue_dp(0);
-                if (n > 1) {
-                    ok = mbar_wait(st_full(1), 0, abort_flag);
-                    if (ok) {
+                ok = issue_s(g0) && issue_dp(g0);
+                if (ok && n == 1) umma_commit<1>(x_empty);  // the item's last reads of K/V (Q/dO)
+                if (ok && n > 1) ok = issue_s(g0 + 1);
+                // the previous item's accumulators have been read out
+                if (ok && !mbar_wait(acc_empty, (uint32_t)((t & 1) ^ 1), abort_flag)) ok = false;
+                if (ok) tc_fence_after();
+                for (int u = 0; ok && u < n; u++) {
+                    const int g = g0 + u;
+                    const uint32_t par = (uint32_t)(g & 1);
+                    if (DKV) {
+                        if (!mbar_wait(p_full, par, abort_flag)) { ok = false; break; }
                         tc_fence_after();
-                        issue_s(1);
+                        issue_acc(tA0, base + OFF_P, ybuf(g, 1), u > 0);  // dV += P^T dO
+                        umma_commit<1>(p_empty);
                     }
-                }
-            }
-            for (int u = 0; ok && u < n; u++) {
-                const uint32_t par = (uint32_t)(u & 1);
-                if (DKV) {
-                    if (!mbar_wait(p_full, par, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    issue_acc(tA0, base + OFF_P, ybuf(u, 1), u > 0);  // dV += P^T dO
-                    umma_commit<1>(p_empty);
-                }
-                if (u + 1 < n) {
-                    if (!mbar_wait(dp_empty, par, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    issue_dp(u + 1);
-                }
-                if (!mbar_wait(ds_full, par, abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                // DKV: dK += dS^T Q; DQ: dQ += dS K
-                issue_acc(DKV ? tA1 : tA0, base + OFF_DS, ybuf(u, 0), u > 0);
-                umma_commit<1>(ds_empty);
-                umma_commit<1>(st_empty(u % STAGES));
-                if (u + 2 < n) {
-                    if (!mbar_wait(st_full((u + 2) % STAGES), (uint32_t)(((u + 2) / STAGES) & 1), abort_flag) ||
-                        !mbar_wait(s_empty(u & 1), (uint32_t)((u >> 1) & 1), abort_flag)) {
-                        ok = false;
-                        break;
+                    if (u + 1 < n) {
+                        if (!issue_dp(g + 1)) { ok = false; break; }
+                        if (u + 2 == n) umma_commit<1>(x_empty);  // the item's last reads of X
                     }
+                    if (!mbar_wait(ds_full, par, abort_flag)) { ok = false; break; }
                     tc_fence_after();
-                    issue_s(u + 2);
+                    // DKV: dK += dS^T Q; DQ: dQ += dS K
+                    issue_acc(DKV ? tA1 : tA0, base + OFF_DS, ybuf(g, 0), u > 0);
+                    umma_commit<1>(ds_empty);
+                    umma_commit<1>(st_empty(g % STAGES));
+                    if (u + 2 < n && !issue_s(g + 2)) { ok = false; break; }
                 }
+                if (!ok) break;
+                umma_commit<1>(acc_full);
+                g0 += n;
             }
-            if (ok) umma_commit<1>(acc_full);
         }
     } else {
-        // ---------------- P and dS
-        const int qq = warp & 3;          // TMEM lane quarter
-        const int hf = (warp - 2) >> 2;   // column half
-        const int r = qq * 32 + lane;     // row within the tile
-        const int row = r0 + r;           // key (DKV) or query (DQ)
+        // ---------------- P and dS: CW warps, CQ per TMEM lane quarter, each
+        // on COLS consecutive columns of its row
+        const int qq = warp & 3;             // TMEM lane quarter
+        const int cq = (warp - 2) >> 2;      // column group
+        const int r = qq * 32 + lane;        // row within the tile
         const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
-        const uint32_t tdP = tmem_base + lane_off + 256 + hf * 64;
-        uint8_t* pbuf = base_ptr + OFF_P + hf * TILE + r * 128;
-        uint8_t* dsbuf = base_ptr + OFF_DS + hf * TILE + r * 128;
+        const int c_base = cq * COLS;
+        const uint32_t tdP = tmem_base + lane_off + 256 + c_base;
+        // this thread's COLS columns of row r: atom c_base / 64, 16-byte chunks from k8_0
+        const int k8_0 = (c_base % 64) / 8;
+        uint8_t* pbuf = base_ptr + OFF_P + (c_base / 64) * TILE + r * 128;
+        uint8_t* dsbuf = base_ptr + OFF_DS + (c_base / 64) * TILE + r * 128;
         const int swz = r & 7;
-        // DQ: the row's LSE and D
-        float nl_row = -INFINITY, d_row = 0.f;
-        if (!DKV && row < T) {
-            nl_row = -a.lse[(size_t)bh * T + row] * LOG2E;
-            d_row = a.D[(size_t)bh * T + row];
-        }
+        int g = 0;
         bool ok = true;
-        for (int u = 0; u < n; u++) {
-            const int sb = u & 1, st = u % STAGES;
-            const uint32_t par = (uint32_t)(u & 1);
-            if (!wait_warp(s_full(sb), (uint32_t)((u >> 1) & 1))) { ok = false; break; }
-            tc_fence_after();
-            const float* vec = reinterpret_cast<const float*>(base_ptr + OFF_VEC + st * 1024);
-            // the diagonal block: DKV sees it first, DQ last
-            const bool diag = DKV ? u == 0 : u == n - 1;
-            const int c_base = hf * 64;
-            float P[64];
+        for (int t = 0, idx = item_of(0); ok && idx < a.items; idx = item_of(++t)) {
+            const Item it = decode_item<DKV>(a, idx);
+            const int row = it.r0 + r;  // key (DKV) or query (DQ)
+            // DQ: the row's LSE and D
+            float nl_row = -INFINITY, d_row = 0.f;
+            if (!DKV && row < T) {
+                nl_row = -a.lse[(size_t)it.bh * T + row] * LOG2E;
+                d_row = a.D[(size_t)it.bh * T + row];
+            }
+            for (int u = 0; u < it.n; u++, g++) {
+                const int sb = g & 1, st = g % STAGES;
+                const uint32_t par = (uint32_t)(g & 1);
+                if (!wait_warp(s_full(sb), (uint32_t)((g >> 1) & 1))) { ok = false; break; }
+                tc_fence_after();
+                const float* vec = reinterpret_cast<const float*>(base_ptr + OFF_VEC + st * 1024);
+                // the diagonal block: DKV sees it first, DQ last
+                const bool diag = DKV ? u == 0 : u == it.n - 1;
+                float P[COLS];
 #pragma unroll
-            for (int ch = 0; ch < 2; ch++) {
-                float v[32];
-                tmem_ld32(tmem_base + lane_off + (uint32_t)(sb * 128 + c_base + ch * 32), v);
+                for (int ch = 0; ch < COLS / 32; ch++) {
+                    float v[32];
+                    tmem_ld32(tmem_base + lane_off + (uint32_t)(sb * 128 + c_base + ch * 32), v);
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    const int c = c_base + ch * 32 + e;
-                    float4 nl4;
-                    if (DKV) nl4 = *reinterpret_cast<const float4*>(vec + c);
-                    else nl4 = make_float4(nl_row, nl_row, nl_row, nl_row);
-                    const float* nl = &nl4.x;
+                    for (int e = 0; e < 32; e += 4) {
+                        const int c = c_base + ch * 32 + e;
+                        float4 nl4;
+                        if (DKV) nl4 = *reinterpret_cast<const float4*>(vec + c);
+                        else nl4 = make_float4(nl_row, nl_row, nl_row, nl_row);
+                        const float* nl = &nl4.x;
 #pragma unroll
-                    for (int f = 0; f < 4; f++) {
-                        float p = ex2_approx(fmaf(v[e + f], a.scale_log2, nl[f]));
-                        // causal: query >= key
-                        if (diag) p = (DKV ? c + f >= r : c + f <= r) ? p : 0.f;
-                        P[ch * 32 + e + f] = p;
+                        for (int f = 0; f < 4; f++) {
+                            float p = ex2_approx(fmaf(v[e + f], a.scale_log2, nl[f]));
+                            // causal: query >= key
+                            if (diag) p = (DKV ? c + f >= r : c + f <= r) ? p : 0.f;
+                            P[ch * 32 + e + f] = p;
+                        }
                     }
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_empty(sb));
+                if (DKV) {
+                    // P^T, bf16
+                    if (!wait_warp(p_empty, par ^ 1u)) { ok = false; break; }
+#pragma unroll
+                    for (int k = 0; k < COLS / 8; k++) {
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int e = 0; e < 4; e++) {
+                            __nv_bfloat162 pr = __floats2bfloat162_rn(P[8 * k + 2 * e], P[8 * k + 2 * e + 1]);
+                            pk[e] = *reinterpret_cast<uint32_t*>(&pr);
+                        }
+                        *reinterpret_cast<uint4*>(pbuf + (((k8_0 + k) ^ swz) << 4)) =
+                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(p_full);
+                }
+                if (!wait_warp(dp_full, par)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t dsk[COLS / 2];
+#pragma unroll
+                for (int ch = 0; ch < COLS / 32; ch++) {
+                    float v[32];
+                    tmem_ld32(tdP + (uint32_t)(ch * 32), v);
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        const int c = c_base + ch * 32 + e;
+                        float4 d4;
+                        if (DKV) d4 = *reinterpret_cast<const float4*>(vec + 128 + c);
+                        else d4 = make_float4(d_row, d_row, d_row, d_row);
+                        const int j = ch * 32 + e;
+                        __nv_bfloat162 lo =
+                            __floats2bfloat162_rn(P[j] * (v[e] - d4.x), P[j + 1] * (v[e + 1] - d4.y));
+                        __nv_bfloat162 hi =
+                            __floats2bfloat162_rn(P[j + 2] * (v[e + 2] - d4.z), P[j + 3] * (v[e + 3] - d4.w));
+                        dsk[j >> 1] = *reinterpret_cast<uint32_t*>(&lo);
+                        dsk[(j >> 1) + 1] = *reinterpret_cast<uint32_t*>(&hi);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(dp_empty);
+                if (!wait_warp(ds_empty, par ^ 1u)) { ok = false; break; }
+#pragma unroll
+                for (int k = 0; k < COLS / 8; k++)
+                    *reinterpret_cast<uint4*>(dsbuf + (((k8_0 + k) ^ swz) << 4)) =
+                        make_uint4(dsk[4 * k], dsk[4 * k + 1], dsk[4 * k + 2], dsk[4 * k + 3]);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ds_full);
             }
+            if (!ok) break;
+            // epilogue: the accumulator columns split over the column groups.
+            // DKV: [dV 64 | dK 64] at TMEM 384; DQ: dQ 64 at TMEM 384
+            if (!wait_warp(acc_full, (uint32_t)(t & 1))) { ok = false; break; }
+            tc_fence_after();
+            constexpr int W = (DKV ? 128 : 64) / CQ;  // columns per thread
+            const int a0 = cq * W;                    // first accumulator column
+            float v[W];
+#pragma unroll
+            for (int ch = 0; ch < W; ch += 16)
+                tmem_ld16(tmem_base + lane_off + 384u + (uint32_t)(a0 + ch),
+                          *reinterpret_cast<float(*)[16]>(v + ch));
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(s_empty(sb));
-            if (DKV) {
-                // P^T row r, columns c_base..c_base+63 -> atom hf, bf16
-                if (!wait_warp(p_empty, par ^ 1u)) { ok = false; break; }
+            if (lane == 0) mbar_arrive(acc_empty);  // the next item may overwrite them
+            if (row < T) {
+                const bool is_k = DKV && a0 >= 64;
+                const float sc = (!DKV || is_k) ? a.scale : 1.f;
+                const int col = DKV ? (is_k ? C + it.h * HSZ : 2 * C + it.h * HSZ) + (a0 % 64)
+                                    : it.h * HSZ + a0;
+                bf16* dst = a.dqkv + ((size_t)it.b * T + row) * 3 * C + col;
 #pragma unroll
-                for (int k8 = 0; k8 < 8; k8++) {
+                for (int d = 0; d < W; d += 8) {
                     uint32_t pk[4];
 #pragma unroll
                     for (int e = 0; e < 4; e++) {
-                        __nv_bfloat162 pr = __floats2bfloat162_rn(P[8 * k8 + 2 * e], P[8 * k8 + 2 * e + 1]);
+                        __nv_bfloat162 pr = __floats2bfloat162_rn(v[d + 2 * e] * sc, v[d + 2 * e + 1] * sc);
                         pk[e] = *reinterpret_cast<uint32_t*>(&pr);
                     }
-                    *reinterpret_cast<uint4*>(pbuf + ((k8 ^ swz) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                }
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(p_full);
-            }
-            if (!wait_warp(dp_full, par)) { ok = false; break; }
-            tc_fence_after();
-            uint32_t dsk[32];
-#pragma unroll
-            for (int ch = 0; ch < 2; ch++) {
-                float v[32];
-                tmem_ld32(tdP + (uint32_t)(ch * 32), v);
-#pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    const int c = c_base + ch * 32 + e;
-                    float4 d4;
-                    if (DKV) d4 = *reinterpret_cast<const float4*>(vec + 128 + c);
-                    else d4 = make_float4(d_row, d_row, d_row, d_row);
-                    const int j = ch * 32 + e;
-                    __nv_bfloat162 lo = __floats2bfloat162_rn(P[j] * (v[e] - d4.x), P[j + 1] * (v[e + 1] - d4.y));
-                    __nv_bfloat162 hi =
-                        __floats2bfloat162_rn(P[j + 2] * (v[e + 2] - d4.z), P[j + 3] * (v[e + 3] - d4.w));
-                    dsk[j >> 1] = *reinterpret_cast<uint32_t*>(&lo);
-                    dsk[(j >> 1) + 1] = *reinterpret_cast<uint32_t*>(&hi);
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(dp_empty);
-            if (!wait_warp(ds_empty, par ^ 1u)) { ok = false; break; }
-#pragma unroll
-            for (int k8 = 0; k8 < 8; k8++)
-                *reinterpret_cast<uint4*>(dsbuf + ((k8 ^ swz) << 4)) =
-                    make_uint4(dsk[4 * k8], dsk[4 * k8 + 1], dsk[4 * k8 + 2], dsk[4 * k8 + 3]);
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(ds_full);
-        }
-        // epilogue: DKV writes dV (half 0) and dK (half 1) rows; DQ writes
-        // half of each dQ row per warp
-        if (ok && wait_warp(acc_full, 0u)) {
-            tc_fence_after();
-            if (DKV) {
-                float v[64];
-                const uint32_t src = tmem_base + lane_off + (hf ? 448u : 384u);
-                tmem_ld32(src, *reinterpret_cast<float(*)[32]>(v));
-                tmem_ld32(src + 32, *reinterpret_cast<float(*)[32]>(v + 32));
-                if (row < T) {
-                    const float sc = hf ? a.scale : 1.f;
-                    bf16* dst = a.dqkv + ((size_t)b * T + row) * 3 * C + (hf ? xk : xv);
-#pragma unroll
-                    for (int d = 0; d < HSZ; d += 8) {
-                        uint32_t pk[4];
-#pragma unroll
-                        for (int e = 0; e < 4; e++) {
-                            __nv_bfloat162 pr = __floats2bfloat162_rn(v[d + 2 * e] * sc, v[d + 2 * e + 1] * sc);
-                            pk[e] = *reinterpret_cast<uint32_t*>(&pr);
-                        }
-                        *reinterpret_cast<uint4*>(dst + d) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    }
-                }
-            } else {
-                float v[32];
-                tmem_ld32(tmem_base + lane_off + 384u + (uint32_t)(hf * 32), v);
-                if (row < T) {
-                    bf16* dst = a.dqkv + ((size_t)b * T + row) * 3 * C + xq + hf * 32;
-#pragma unroll
-                    for (int d = 0; d < 32; d += 8) {
-                        uint32_t pk[4];
-#pragma unroll
-                        for (int e = 0; e < 4; e++) {
-                            __nv_bfloat162 pr =
-                                __floats2bfloat162_rn(v[d + 2 * e] * a.scale, v[d + 2 * e + 1] * a.scale);
-                            pk[e] = *reinterpret_cast<uint32_t*>(&pr);
-                        }
-                        *reinterpret_cast<uint4*>(dst + d) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    }
+                    *reinterpret_cast<uint4*>(dst + d) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
             }
         }
@@ -410,7 +446,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (*abort_flag) {
         if (threadIdx.x == 0) {
             // let every issued copy land before the shared memory is released
-            mbar_wait_drain(fixed_full, 0);
+            const int nx = *x_issued_smem;
+            if (nx > 0) mbar_wait_drain(x_full, (uint32_t)((nx - 1) & 1));
             const int issued = *n_issued_smem;
             for (int s = 0; s < STAGES; s++) {
                 if (issued > s) {
@@ -523,10 +560,11 @@ int launch_flash_backward_tc(void* dqkv, const void* dout, const void* qkv, cons
     a.NH = NH;
     a.BH = B * NH;
     a.nblk = (T + BLK - 1) / BLK;
+    a.items = a.nblk * a.BH;
     a.scale = 1.f / sqrtf((float)HSZ);
     a.scale_log2 = LOG2E * a.scale;
     a.err = err;
-    const int grid = a.nblk * a.BH;
+    const int grid = a.items < num_sms() ? a.items : num_sms();  // persistent
     launch_pdl(flash_bwd_tc_k<false>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, s, tqkv, tdo, a);
     launch_pdl(flash_bwd_tc_k<true>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, s, tqkv, tdo, a);
     return GPT2_OK;

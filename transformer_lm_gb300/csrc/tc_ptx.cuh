@@ -38,6 +38,19 @@ DEVI bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// the same test, but the thread may sleep (up to `ns`) until the phase
+// completes instead of returning at once: waiting warps stop taking issue slots
+DEVI bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
 DEVI unsigned long long globaltimer() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -50,8 +63,8 @@ DEVI bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if ((it & 7u) == 0) {
             if (*abort_flag) return false;
             if (globaltimer() - t0 > WAIT_LIMIT_NS) {
                 *abort_flag = 1;

@@ -11,15 +11,14 @@
 //   warp 1      allocates TMEM; one elected thread issues tcgen05.mma
 //               (M=128, N=BN, fp32 accumulators in TMEM) and commits each
 //               stage back to the producer;
-//   warps 2..9  epilogue: tcgen05.ld the accumulator (each warp reads 32 rows
-//               of its TMEM lane quarter, one row per thread, and half of the
-//               columns of every sub-tile), apply
-//               bias / GELU / residual / GELU-backward / += in 128-byte-wide
-//               column sub-tiles staged in 128B-swizzled shared memory: the
-//               residual / GELU input / += operand arrives by TMA load
-//               (prefetched one sub-tile ahead) and results leave by TMA
-//               store, so no thread touches global memory row by row and the
-//               ragged tails are clipped by the tensor maps.
+//   warps 2..9  epilogue: each warp owns the 32 rows of its TMEM lane
+//               quarter and every other 128-byte-wide column chunk of a tile
+//               (one row per thread): it tcgen05.ld's the chunk, applies bias /
+//               GELU / residual / GELU-backward / += (the operand row segment
+//               read straight from global memory), stages the result in its own
+//               4 KB 128B-swizzled buffer and writes it with its own TMA store.
+//               The warps never wait for one another inside a tile; ragged
+//               tails are clipped by the tensor maps.
 // Two TMEM accumulators let the epilogue of tile i overlap the MMAs of tile
 // i+1. Every mbarrier wait is bounded in time; on expiry the CTA records
 // DEVERR_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and exits.
@@ -47,27 +46,20 @@ constexpr int EPI_THREADS = 32 * EPI_WARPS;
 constexpr int NUM_THREADS = 64 + EPI_THREADS;
 constexpr int GROUP_M = 16;  // m-blocks per rasterisation group (L2 locality of A and B)
 
-constexpr int EPI_BUF_BYTES = BM * ROWB;  // one epilogue staging buffer: 128 rows x 128 bytes
-// staging buffers per epilogue: the two-output and element-heavy epilogues
-// take four, so that two sub-tiles' stores (and the next operand load) stay
-// in flight while the next sub-tile is written; the rest keep two and one
-// more pipeline stage
-template <int EPI> __host__ __device__ constexpr int epi_bufs() {
-    return (EPI == EPI_GELU || EPI == EPI_GELU_BWD || EPI == EPI_SPLITK) ? 4 : 2;
-}
+constexpr int STG_BYTES = 32 * ROWB;  // an epilogue warp's staging: 32 rows x 128 bytes
 
 // CG = CTAs per MMA: 1 (tcgen05 cta_group::1, 128 x BN tiles) or 2 (a CTA
 // pair runs cta_group::2 MMAs on 256 x BN tiles; each CTA holds 128 rows of A
 // and BN/2 rows of B in its shared memory and its 128 accumulator rows in TMEM)
-template <int BN, int CG, int EB> struct Cfg {
+template <int BN, int CG> struct Cfg {
     static constexpr int A_BYTES = BM * ROWB;
     static constexpr int B_BYTES = (BN / CG) * ROWB;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int EPI_BYTES = EPI_WARPS * STG_BYTES;
     static constexpr int BAR_BYTES = 256 + 1024;  // barriers, flags, per-row softmax partials
-    static constexpr int STAGES = (224 * 1024 - EB * EPI_BUF_BYTES - BAR_BYTES - 1024) / STAGE_BYTES;
+    static constexpr int STAGES = (227 * 1024 - EPI_BYTES - BAR_BYTES - 1024) / STAGE_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int SMEM_BYTES =
-        STAGES * STAGE_BYTES + EB * EPI_BUF_BYTES + BAR_BYTES + 1024;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES + 1024;
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
@@ -103,75 +95,97 @@ DEVI void tile_coords(int st, int num_mg, int num_n, int group, int& mg, int& nb
 DEVI void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(EPI_THREADS) : "memory"); }
 
 // ------------------------------------------------------------------ epilogue
-// One 128-byte-wide column sub-tile (SUBN columns) of one row: the thread's
-// accumulator values v[], its row `rl` inside the tile, and the staging
-// buffers (128 rows x 128 bytes, 16-byte chunk k of row r at chunk k ^ (r & 7)).
-// buf0 holds the TMA-loaded operand (residual, GELU input or the current D)
-// and receives the result; buf1 receives the second output of EPI_GELU.
-template <typename T, int EPI>
-DEVI void epilogue_subtile(const Args& a, const float* v, uint8_t* buf0, uint8_t* buf1, int rl,
-                           int row, int n0s, int kbeg, float& pmax, float& psum) {
-    constexpr int VEC = Vec16<T>::N;
-    const T* bias = (const T*)a.bias;
+// One 128-byte output chunk of one row: the accumulator values v[OC], the
+// chunk's first column nc, the row; the result leaves packed in o (and the
+// second output of EPI_GELU in o2). Columns past N are computed but clipped
+// by the store.
+// The operand row segment of a chunk (residual, GELU input, or D itself for
+// +=), read straight from global memory; zeros outside the matrix.
+template <typename T, int EPI, int OC>
+DEVI void load_operand(const Args& a, int row, int nc, Vec16<T> (&r)[OC * sizeof(T) / 16]) {
+    constexpr int VEC = 16 / (int)sizeof(T);
+    if constexpr (EPI == EPI_RESID || EPI == EPI_GELU_BWD || EPI == EPI_ACCUM) {
+        const T* src = EPI == EPI_ACCUM ? (const T*)a.D + (size_t)row * a.ldd
+                                        : (const T*)a.aux + (size_t)row * a.ldaux;
 #pragma unroll
-    for (int kk = 0; kk < 4; kk++) {
-        const int k = kbeg + kk;  // 16-byte chunk of the 128-byte row
-        const int off = rl * ROWB + ((k ^ (rl & 7)) << 4);
-        const int n = n0s + k * VEC;
-        const bool colok = n < a.N;
-        float x[VEC];
-#pragma unroll
-        for (int e = 0; e < VEC; e++) x[e] = v[kk * VEC + e];
-        if constexpr (EPI == EPI_STORE || EPI == EPI_GELU || EPI == EPI_RESID ||
-                      EPI == EPI_GELU_PART) {
-            if (bias && colok) {
-                Vec16<T> bb = ld16(bias + n);
-#pragma unroll
-                for (int e = 0; e < VEC; e++) x[e] += to_f(bb.v[e]);
-            }
+        for (int k = 0; k < OC / VEC; k++) {
+            if (row < a.M && nc + k * VEC < a.N)
+                *reinterpret_cast<int4*>(&r[k]) = *reinterpret_cast<const int4*>(src + nc + k * VEC);
+            else
+                *reinterpret_cast<int4*>(&r[k]) = make_int4(0, 0, 0, 0);
         }
-        Vec16<T> o;
-        if constexpr (EPI == EPI_STORE) {
-#pragma unroll
-            for (int e = 0; e < VEC; e++) o.v[e] = from_f<T>(x[e]);
-        } else if constexpr (EPI == EPI_GELU) {
-            Vec16<T> g;
-#pragma unroll
-            for (int e = 0; e < VEC; e++) {
-                o.v[e] = from_f<T>(x[e]);
-                g.v[e] = from_f<T>(sizeof(T) == 2 ? gelu_fwd_fast(to_f(o.v[e])) : gelu_fwd(to_f(o.v[e])));
-            }
-            *reinterpret_cast<int4*>(buf1 + off) = *reinterpret_cast<const int4*>(&g);
-        } else if constexpr (EPI == EPI_RESID || EPI == EPI_GELU_BWD || EPI == EPI_ACCUM) {
-            Vec16<T> r;
-            *reinterpret_cast<int4*>(&r) = *reinterpret_cast<const int4*>(buf0 + off);
-#pragma unroll
-            for (int e = 0; e < VEC; e++) {
-                const float rv = to_f(r.v[e]);
-                if constexpr (EPI == EPI_RESID) o.v[e] = from_f<T>(x[e] + rv);
-                else if constexpr (EPI == EPI_GELU_BWD)
-                    o.v[e] = from_f<T>(x[e] * (sizeof(T) == 2 ? gelu_grad_fast(rv) : gelu_grad(rv)));
-                else o.v[e] = from_f<T>(rv + x[e]);
-            }
-        } else if constexpr (EPI == EPI_GELU_PART) {
-            float cm = pmax;
-#pragma unroll
-            for (int e = 0; e < VEC; e++) {
-                x[e] = gelu_fwd(x[e]);
-                cm = fmaxf(cm, x[e]);
-            }
-#pragma unroll
-            for (int e = 0; e < VEC; e++) o.v[e] = from_f<T>(x[e]);
-            if (colok && row < a.M) {
-                float s = 0.f;
-#pragma unroll
-                for (int e = 0; e < VEC; e++) s += expf(x[e] - cm);
-                psum = psum * expf(pmax - cm) + s;
-                pmax = cm;
-            }
-        }
-        *reinterpret_cast<int4*>(buf0 + off) = *reinterpret_cast<const int4*>(&o);
     }
+}
+
+template <typename T, typename TO, int EPI, int OC>
+DEVI void epilogue_chunk(const Args& a, float (&v)[OC], const Vec16<T> (&r)[OC * sizeof(T) / 16], int row,
+                         int nc, uint32_t (&o)[32], uint32_t (&o2)[32], float& pmax, float& psum) {
+    constexpr int VEC = 16 / (int)sizeof(T);
+    const T* bias = (const T*)a.bias;
+    if constexpr (EPI == EPI_STORE || EPI == EPI_GELU || EPI == EPI_RESID || EPI == EPI_GELU_PART) {
+        if (bias) {
+#pragma unroll
+            for (int k = 0; k < OC / VEC; k++) {
+                if (nc + k * VEC < a.N) {
+                    Vec16<T> bb;
+                    *reinterpret_cast<int4*>(&bb) = __ldg(reinterpret_cast<const int4*>(bias + nc + k * VEC));
+#pragma unroll
+                    for (int e = 0; e < VEC; e++) v[k * VEC + e] += to_f(bb.v[e]);
+                }
+            }
+        }
+    }
+    if constexpr (EPI == EPI_RESID || EPI == EPI_GELU_BWD || EPI == EPI_ACCUM) {
+#pragma unroll
+        for (int k = 0; k < OC / VEC; k++)
+#pragma unroll
+            for (int e = 0; e < VEC; e++) {
+                const float rv = to_f(r[k].v[e]);
+                float& x = v[k * VEC + e];
+                if constexpr (EPI == EPI_RESID) x += rv;
+                else if constexpr (EPI == EPI_GELU_BWD) x *= sizeof(T) == 2 ? gelu_grad_fast(rv) : gelu_grad(rv);
+                else x = rv + x;
+            }
+    }
+    if constexpr (EPI == EPI_GELU_PART) {
+        float cm = pmax;
+#pragma unroll
+        for (int e = 0; e < OC; e++) {
+            v[e] = gelu_fwd(v[e]);
+            cm = fmaxf(cm, v[e]);
+        }
+        if (row < a.M) {
+            float sum = 0.f;
+#pragma unroll
+            for (int e = 0; e < OC; e++) sum += nc + e < a.N ? expf(v[e] - cm) : 0.f;
+            psum = psum * expf(pmax - cm) + sum;
+            pmax = cm;
+        }
+    }
+    if constexpr (sizeof(TO) == 4) {
+#pragma unroll
+        for (int e = 0; e < 32; e++) o[e] = __float_as_uint(v[e]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 32; e++) {
+            __nv_bfloat162 pr = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+            o[e] = *reinterpret_cast<uint32_t*>(&pr);
+            if constexpr (EPI == EPI_GELU) {
+                // GELU of the rounded pre-activation (what the backward sees)
+                const float2 f = __bfloat1622float2(pr);
+                __nv_bfloat162 gr = __floats2bfloat162_rn(gelu_fwd_fast(f.x), gelu_fwd_fast(f.y));
+                o2[e] = *reinterpret_cast<uint32_t*>(&gr);
+            }
+        }
+    }
+}
+
+// a warp's 32 staged rows: row `lane`, 16-byte chunk k at k ^ (lane & 7)
+DEVI void stage_row(uint8_t* stg, int lane, const uint32_t (&o)[32]) {
+#pragma unroll
+    for (int k = 0; k < 8; k++)
+        *reinterpret_cast<uint4*>(stg + lane * ROWB + ((k ^ (lane & 7)) << 4)) =
+            make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -179,37 +193,34 @@ template <int BN, int KIND, int EPI, int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_k(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
-              const __grid_constant__ CUtensorMap tmX, const __grid_constant__ Args args) {
-    constexpr int EPI_BUFS = epi_bufs<EPI>();
-    using C = Cfg<BN, CG, EPI_BUFS>;
+              const __grid_constant__ Args args) {
+    using C = Cfg<BN, CG>;
     using T = typename std::conditional<KIND == 0, bf16, float>::type;
     constexpr int KE = ROWB / (int)sizeof(T);  // K elements per stage
     constexpr int UK = KIND == 0 ? 16 : 8;     // K elements per MMA
     constexpr int KSTEPS = KE / UK;            // MMAs per stage (4)
-    constexpr int SUBN = ROWB / (int)sizeof(T);  // epilogue sub-tile width (columns)
-    constexpr int NSUB = BN / SUBN;
     constexpr int BNC = BN / CG;               // rows of B this CTA holds
-    constexpr bool HAS_AUX = EPI == EPI_RESID || EPI == EPI_GELU_BWD || EPI == EPI_ACCUM;
-    // staging buffers per sub-tile: EPI_GELU's two outputs; EPI_SPLITK's fp32
-    // sub-tile is 256 bytes wide (one buffer per column half)
-    constexpr int OUTS = (EPI == EPI_GELU || EPI == EPI_SPLITK) ? 2 : 1;
+    // epilogue output: fp32 for kind::tf32 and for split-K partials, else bf16;
+    // a 128-byte chunk holds OC output columns
+    constexpr bool OUT_F32 = KIND == 1 || EPI == EPI_SPLITK;
+    using TO = typename std::conditional<OUT_F32, float, bf16>::type;
+    constexpr int OC = OUT_F32 ? 32 : 64;
+    constexpr int NCH = BN / OC;
     static_assert(EPI != EPI_SPLITK || KIND == 0, "split-K partials: bf16 operands only");
-
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - raw);
     const uint32_t ebuf = base + C::STAGES * C::STAGE_BYTES;
     uint8_t* ebuf_ptr = base_ptr + C::STAGES * C::STAGE_BYTES;
-    const uint32_t bars = ebuf + EPI_BUFS * EPI_BUF_BYTES;
-    uint8_t* bars_ptr = ebuf_ptr + EPI_BUFS * EPI_BUF_BYTES;
+    const uint32_t bars = ebuf + C::EPI_BYTES;
+    uint8_t* bars_ptr = ebuf_ptr + C::EPI_BYTES;
     auto full = [&](int s) { return bars + 8u * s; };
     auto empty = [&](int s) { return bars + 8u * (C::STAGES + s); };
     auto tfull = [&](int a) { return bars + 8u * (2 * C::STAGES + a); };
     auto tempty = [&](int a) { return bars + 8u * (2 * C::STAGES + 2 + a); };
     const uint32_t drain = bars + 8u * (2 * C::STAGES + 4);
-    auto auxfull = [&](int b) { return bars + 8u * (2 * C::STAGES + 5 + b); };
-    constexpr int NBARS = 2 * C::STAGES + 5 + EPI_BUFS;
+    constexpr int NBARS = 2 * C::STAGES + 5;
     static_assert(8 * NBARS + 16 <= 256, "barrier area");
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars_ptr + 8 * NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars_ptr + 8 * NBARS + 4);
@@ -226,10 +237,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int a = 0; a < 2; a++) {
             mbar_init(tfull(a), 1);
-            mbar_init(tempty(a), CG);  // one arrival from each CTA's epilogue
+            mbar_init(tempty(a), CG * EPI_WARPS);  // one arrival per epilogue warp of each CTA
         }
         mbar_init(drain, 1);
-        for (int b = 0; b < EPI_BUFS; b++) mbar_init(auxfull(b), 1);
         *abort_flag = 0;
         *n_issued_smem = 0;
         *epi_abort = 0;
@@ -337,111 +347,84 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
     } else {
-        // ---------------- epilogue warps 2..9
-        // Every epilogue thread runs every iteration (the named barriers stay
-        // matched); after an expired wait the work is skipped, not the loop.
-        const int q = warp & 3;         // TMEM lane quarter this warp may access
-        const int hh = (warp - 2) >> 2;  // which half of each sub-tile's columns
-        const int rl = q * 32 + lane;
-        const bool elected = warp == 2 && lane == 0;
-        constexpr int HALF = SUBN / 2;
+        // ---------------- epilogue warps 2..9: a warp owns its TMEM lane
+        // quarter's 32 rows and the column chunks j = hh, hh + 2, ... of each
+        // tile; it stages a chunk in its own buffer and stores it itself.
+        // Every epilogue thread runs every tile (EPI_GELU_PART's named barrier
+        // stays matched); after an expired wait the work is skipped.
+        const int q = warp & 3;          // TMEM lane quarter this warp may access
+        const int hh = (warp - 2) >> 2;  // chunk parity
+        const int rl = q * 32 + lane;    // row within the tile
+        uint8_t* stg = ebuf_ptr + (warp - 2) * STG_BYTES;
+        const uint32_t stg_s = ebuf + (uint32_t)((warp - 2) * STG_BYTES);
         int acc = 0;
         uint32_t acc_phase = 0;
-        int u = 0;  // sub-tile counter: staging buffer rotation and aux barrier phases
         bool aborted = false;
-        int last_aux_u[EPI_BUFS];  // latest aux load per buffer (elected thread)
-        for (int b = 0; b < EPI_BUFS; b++) last_aux_u[b] = -1;
-        if constexpr (HAS_AUX) {
-            if (elected && cid < num_units) {
-                int mg, nbk;
-                tile_coords(cid % num_super, num_mg, args.num_n, group, mg, nbk);
-                mbar_expect_tx(auxfull(0), EPI_BUF_BYTES);
-                tma_load_2d(ebuf, &tmX, auxfull(0), nbk * BN, (mg * CG + rank) * BM);
-                last_aux_u[0] = 0;
-            }
-        }
+        const uint32_t tempty_leader = CG == 2 ? mapa_rank(tempty(0), 0) : 0u;
         for (int st = cid; st < num_units; st += ncl) {
             int mg, nb;
             tile_coords(st % num_super, num_mg, args.num_n, group, mg, nb);
             const int split = st / num_super;
             const int m0 = (mg * CG + rank) * BM, n0 = nb * BN;
+            const int row = m0 + rl;
+            // the first chunk's operand is read while the MMAs run
+            constexpr int NV = OC * (int)sizeof(T) / 16;
+            Vec16<T> r[NV];
+            load_operand<T, EPI, OC>(args, row, n0 + hh * OC, r);
             int ok = 1;
             if (lane == 0 && !aborted) ok = mbar_wait(tfull(acc), acc_phase, abort_flag) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) {
+            if (!ok || *epi_abort) {
                 aborted = true;
                 *epi_abort = 1;
             }
             if (!aborted) tc_fence_after();
-            const int row = m0 + rl;
             float pmax = -INFINITY, psum = 0.f;
 #pragma unroll 1
-            for (int j = 0; j < NSUB; j++, u++) {
-                const int b0 = (u * OUTS) % EPI_BUFS;
-                if (elected && !aborted) {
-                    if constexpr (HAS_AUX) {
-                        // prefetch the next sub-tile's operand into the next buffer
-                        int nt = st, nj = j + 1;
-                        if (nj == NSUB) { nt = st + ncl; nj = 0; }
-                        if (nt < num_units) {
-                            const int nb1 = (u + 1) % EPI_BUFS;
-                            int nmg, nnb;
-                            tile_coords(nt % num_super, num_mg, args.num_n, group, nmg, nnb);
-                            // the store that last read buffer nb1 is done
-                            bulk_wait_read<EPI_BUFS - 2>();
-                            mbar_expect_tx(auxfull(nb1), EPI_BUF_BYTES);
-                            tma_load_2d(ebuf + nb1 * EPI_BUF_BYTES, &tmX, auxfull(nb1),
-                                        nnb * BN + nj * SUBN, (nmg * CG + rank) * BM);
-                            last_aux_u[nb1] = u + 1;
-                        }
-                        if (!mbar_wait(auxfull(b0), (uint32_t)((u / EPI_BUFS) & 1), abort_flag)) {
-                            aborted = true;
-                            *epi_abort = 1;
-                        }
-                    } else {
-                        bulk_wait_read<EPI_BUFS / OUTS - 1>();  // buffers b0.. are free again
-                    }
-                }
-                epi_bar();  // operands landed / buffers free
-                int ab = aborted || *epi_abort;
-                ab = __shfl_sync(0xffffffffu, ab, 0);
-                aborted = ab != 0;
-                if (!aborted) {
-                    float v[HALF];
-                    const uint32_t taddr = tmem_base + (uint32_t)(acc * BN + j * SUBN + hh * HALF) +
-                                           ((uint32_t)(q * 32) << 16);
-                    if constexpr (HALF == 32) tmem_ld32(taddr, v);
-                    else tmem_ld16(taddr, v);
-                    if constexpr (EPI == EPI_SPLITK) {
-                        // this half's 32 fp32 columns = one 128-byte staging row
-                        uint8_t* bp = ebuf_ptr + (b0 + hh) * EPI_BUF_BYTES + rl * ROWB;
+            for (int j = hh; j < NCH && !aborted; j += 2) {
+                const int nc = n0 + j * OC;
+                float v[OC];
+                const uint32_t taddr = tmem_base + (uint32_t)(acc * BN + j * OC) + ((uint32_t)(q * 32) << 16);
+                if constexpr (OC == 64) tmem_ld64(taddr, v);
+                else tmem_ld32(taddr, v);
+                Vec16<T> rn[NV];  // the next chunk's operand, in flight during this one
+                if (j + 2 < NCH) load_operand<T, EPI, OC>(args, row, nc + 2 * OC, rn);
+                uint32_t o[32], o2[32];
+                epilogue_chunk<T, TO, EPI, OC>(args, v, r, row, nc, o, o2, pmax, psum);
 #pragma unroll
-                        for (int k = 0; k < 8; k++)
-                            *reinterpret_cast<float4*>(bp + ((k ^ (rl & 7)) << 4)) =
-                                make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-                    } else {
-                        epilogue_subtile<T, EPI>(args, v, ebuf_ptr + b0 * EPI_BUF_BYTES,
-                                                 ebuf_ptr + ((b0 + 1) % EPI_BUFS) * EPI_BUF_BYTES, rl,
-                                                 row, n0 + j * SUBN, hh * 4, pmax, psum);
-                    }
-                }
+                for (int k = 0; k < NV; k++) r[k] = rn[k];
+                // this warp's previous store has read the staging buffer
+                if (lane == 0) bulk_wait_read<0>();
+                __syncwarp();
+                stage_row(stg, lane, o);
                 fence_async_smem();
-                epi_bar();  // staging written
-                if (elected && !aborted) {
-                    if constexpr (EPI == EPI_SPLITK) {
-                        // (N, M, splits) fp32 map: ragged rows clip inside their own slice
-                        tma_store_3d(&tmD, ebuf + b0 * EPI_BUF_BYTES, n0 + j * SUBN, m0, split);
-                        tma_store_3d(&tmD, ebuf + (b0 + 1) * EPI_BUF_BYTES, n0 + j * SUBN + HALF, m0, split);
-                    } else {
-                        tma_store_2d(&tmD, ebuf + b0 * EPI_BUF_BYTES, n0 + j * SUBN, m0);
-                        if constexpr (EPI == EPI_GELU)
-                            tma_store_2d(&tmD2, ebuf + (b0 + 1) * EPI_BUF_BYTES, n0 + j * SUBN, m0);
-                    }
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (EPI == EPI_SPLITK) tma_store_3d(&tmD, stg_s, nc, m0 + q * 32, split);
+                    else tma_store_2d(&tmD, stg_s, nc, m0 + q * 32);
                     bulk_commit();
                 }
+                if constexpr (EPI == EPI_GELU) {
+                    if (lane == 0) bulk_wait_read<0>();
+                    __syncwarp();
+                    stage_row(stg, lane, o2);
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmD2, stg_s, nc, m0 + q * 32);
+                        bulk_commit();
+                    }
+                }
+            }
+            // this warp's accumulator rows are read: release them to the leader's MMA
+            if (!aborted) tc_fence_before();
+            __syncwarp();
+            if (lane == 0 && !aborted) {
+                if constexpr (CG == 1) mbar_arrive(tempty(acc));
+                else mbar_arrive_cluster(tempty_leader + 8u * (uint32_t)acc);
             }
             if constexpr (EPI == EPI_GELU_PART) {
-                // merge the two column halves of the row, then one partial per (row, tile)
+                // merge the two chunk parities of the row, then one partial per (row, tile)
                 if (hh == 1) row_part[rl] = make_float2(pmax, psum);
                 epi_bar();
                 if (hh == 0 && row < args.M && !aborted) {
@@ -453,24 +436,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     reinterpret_cast<float2*>(args.part)[(size_t)row * args.part_ld + nb] =
                         make_float2(m, sum);
                 }
-            }
-            // this CTA's accumulator rows are read: release them to the leader's MMA
-            if (!aborted) tc_fence_before();
-            epi_bar();
-            if (elected) {
-                if constexpr (CG == 1) mbar_arrive(tempty(acc));
-                else mbar_arrive_cluster(mapa_rank(tempty(acc), 0));
+                epi_bar();  // row_part is free for the next tile
             }
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
-        if (elected) {
-            bulk_wait_all();
-            if (aborted) {
-                for (int b = 0; b < EPI_BUFS; b++)
-                    if (last_aux_u[b] >= 0)
-                        mbar_wait_drain(auxfull(b), (uint32_t)((last_aux_u[b] / EPI_BUFS) & 1));
-            }
-        }
+        if (lane == 0) bulk_wait_all();
     }
 
     __syncthreads();
@@ -596,14 +566,14 @@ static int launch_splitk_reduce(bf16* D, long long ldd, const float* ws, int M, 
 }
 
 struct Maps {
-    CUtensorMap a, b, d, d2, x;
+    CUtensorMap a, b, d, d2;
 };
 
 // Persistent launch: one CTA per SM, or -- for CTA pairs -- as many 2-CTA
 // clusters as can be co-resident (cudaOccupancyMaxActiveClusters).
 template <int BN, int KIND, int EPI, int CG>
 static int launch_tc(const Maps& mp, const tc::Args& a, cudaStream_t s) {
-    using C = tc::Cfg<BN, CG, tc::epi_bufs<EPI>()>;
+    using C = tc::Cfg<BN, CG>;
     auto kern = tc::gemm_tc_k<BN, KIND, EPI, CG>;
     static bool attr_done = false;
     static int max_clusters = 0;
@@ -647,7 +617,7 @@ static int launch_tc(const Maps& mp, const tc::Args& a, cudaStream_t s) {
         cfg.numAttrs++;
     }
     note_launch(1);
-    if (cudaLaunchKernelEx(&cfg, kern, mp.a, mp.b, mp.d, mp.d2, mp.x, a) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, kern, mp.a, mp.b, mp.d, mp.d2, a) != cudaSuccess)
         return GPT2_ERR_CUDA;
     return GPT2_OK;
 }
@@ -758,25 +728,24 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
     }
 
     Maps mp;
-    const int SUBN = tc::ROWB / esz;
+    const int OC = tc::ROWB / esz;  // output columns per 128-byte chunk
     bool ok = p.a_kmajor ? make_map(&mp.a, p.A, dt, p.K, p.M, p.lda, KE, tc::BM)
                          : make_map(&mp.a, p.A, dt, p.M, p.K, p.lda, KE, KE);
     ok = ok && (p.b_kmajor ? make_map(&mp.b, p.B, dt, p.K, p.N, p.ldb, KE, BN / cg)
                            : make_map(&mp.b, p.B, dt, p.N, p.K, p.ldb, KE, KE));
     if (a.splits > 1) {
-        ok = ok && make_map_3d_f32(&mp.d, p.ws, p.N, p.M, a.splits, 32, tc::BM);
+        // fp32 partials: 32-column x 32-row boxes, one per epilogue warp and chunk
+        ok = ok && make_map_3d_f32(&mp.d, p.ws, p.N, p.M, a.splits, 32, 32);
         mp.d2 = mp.d;
-        mp.x = mp.d;
         if (!ok) return GPT2_ERR_CUDA;
         const int rc = cg == 2 ? dispatch_epi<256, 0, 2>(EPI_SPLITK, mp, a, s)
                                : dispatch_epi<256, 0, 1>(EPI_SPLITK, mp, a, s);
         if (rc != GPT2_OK) return rc;
         return launch_splitk_reduce((bf16*)p.D, p.ldd, p.ws, p.M, p.N, a.splits, s);
     }
-    ok = ok && make_map(&mp.d, p.D, dt, p.N, p.M, p.ldd, SUBN, tc::BM);
-    ok = ok && make_map(&mp.d2, p.epi == EPI_GELU ? p.D2 : p.D, dt, p.N, p.M, p.ldd, SUBN, tc::BM);
-    if (has_aux) ok = ok && make_map(&mp.x, p.aux, dt, p.N, p.M, p.ldaux, SUBN, tc::BM);
-    else ok = ok && make_map(&mp.x, p.D, dt, p.N, p.M, p.ldd, SUBN, tc::BM);  // += reads D itself
+    // output boxes: one 128-byte chunk x 32 rows (an epilogue warp's store)
+    ok = ok && make_map(&mp.d, p.D, dt, p.N, p.M, p.ldd, OC, 32);
+    ok = ok && make_map(&mp.d2, p.epi == EPI_GELU ? p.D2 : p.D, dt, p.N, p.M, p.ldd, OC, 32);
     if (!ok) return GPT2_ERR_CUDA;
     if (dt == DT_BF16) {
         if (cg == 2)

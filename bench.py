@@ -33,7 +33,19 @@ WORKLOAD = ("GPT-2 124M (L=12 C=768 NH=12 V=50257 Vp=50304) bf16 mixed-precision
             "(fwd+bwd+AdamW lr 6e-4 wd 0.1), B=8 T=1024")
 L, C, NH, V, Vp, MAXT = 12, 768, 12, 50257, 50304, 1024
 B, T = 8, 1024
+ACCUM = 1  # gradient-accumulation micro-steps per AdamW update
+DIMS = "GPT2_124M"
 LR, B1, B2, EPS, WD = 6e-4, 0.9, 0.95, 1e-8, 0.1
+
+
+def select_model(name: str) -> None:
+    """--model 350m: GPT-2 350M, B=16, T=1024, 4 micro-steps per update."""
+    global L, C, NH, B, ACCUM, DIMS, WORKLOAD
+    if name == "350m":
+        L, C, NH, B, ACCUM, DIMS = 24, 1024, 16, 16, 4, "GPT2_350M"
+        WORKLOAD = ("GPT-2 350M (L=24 C=1024 NH=16 V=50257 Vp=50304) bf16 mixed-precision train step "
+                    "(4 micro-steps of B=16 T=1024 with += gradient accumulation, then AdamW lr 6e-4 "
+                    "wd 0.1)")
 
 
 def model_flops_per_token() -> float:
@@ -163,7 +175,7 @@ def oracle_sample_setup(seed: int = 1337):
 
     import oracle
     from transformer_lm_gb300 import inputs
-    d = inputs.GPT2_124M
+    d = getattr(inputs, DIMS)
     params = inputs.round_to_bf16(inputs.gpt2_params(d, seed)).astype(np.float64)
     tok = inputs.tokens(42, 1, 1, ORACLE_SAMPLE_T, d.V)
     tgt = inputs.tokens(42, 2, 1, ORACLE_SAMPLE_T, d.V)
@@ -191,8 +203,8 @@ def cpu_baseline(steps: int = 1) -> dict:
     dt = time.perf_counter() - t0
     return {"value": steps * ORACLE_SAMPLE_T / dt, "unit": "tokens/s", "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": (f"full 124M model fwd+bwd on B=1 T={ORACLE_SAMPLE_T} plus AdamW over all "
-                       f"124,475,904 params, {steps} step(s), fp64, {dt:.1f} s")}
+            "sample": (f"full {DIMS[5:]} model fwd+bwd on B=1 T={ORACLE_SAMPLE_T} plus AdamW over "
+                       f"all params, {steps} step(s), fp64, {dt:.1f} s")}
 
 
 def run_reference(args):
@@ -208,8 +220,8 @@ def run_reference(args):
         oracle_sample_step(st)
     dt = time.perf_counter() - t0
     value = args.steps * ORACLE_SAMPLE_T / dt
-    sample = (f"each step: full 124M model fwd+bwd on B=1 T={ORACLE_SAMPLE_T} plus AdamW over all "
-              f"params, fp64 CPU oracle")
+    sample = (f"each step: full {DIMS[5:]} model fwd+bwd on B=1 T={ORACLE_SAMPLE_T} plus AdamW over "
+              f"all params, fp64 CPU oracle")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000.0 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -246,11 +258,13 @@ def run_ours(args):
     stream = torch.cuda.Stream()
     torch.cuda.set_stream(stream)
     G.gpt2_set_stream(stream.cuda_stream)
-    tok = inputs.tokens(42 + rank, 1, B, T, V)
-    tgt = inputs.tokens(42 + rank, 2, B, T, V)
+    G.gpt2_set_grad_accum(ACCUM)
+    # ACCUM micro-batches of B x T ids, one after another
+    tok = inputs.tokens(42 + rank, 1, ACCUM * B, T, V)
+    tgt = inputs.tokens(42 + rank, 2, ACCUM * B, T, V)
     d_tok = torch.from_numpy(tok.reshape(-1)).cuda()
     d_tgt = torch.from_numpy(tgt.reshape(-1)).cuda()
-    d_loss = torch.zeros(1, device="cuda")
+    d_loss = torch.zeros(ACCUM, device="cuda")
     step_no = [0]
 
     # pinned host copies of the batch for the end-to-end leg
@@ -268,7 +282,7 @@ def run_ours(args):
         d_tok.copy_(h_tok, non_blocking=True)
         d_tgt.copy_(h_tgt, non_blocking=True)
         device_step()
-        return float(d_loss.item())
+        return float(d_loss.cpu().mean())
 
     for _ in range(args.warmup):
         device_step()
@@ -294,12 +308,12 @@ def run_ours(args):
     ms = ev0.elapsed_time(ev1)
     ms = max_over_ranks(ms, world)
     G.gpt2_sync()
-    loss_dev = float(d_loss.item())
+    loss_dev = float(d_loss.cpu().mean())
 
     # ---- per-kernel durations: CUDA events around every launch, on the
     # library's stream, over a second pass of the same steps (kept out of
     # the timed region above because the extra event records slow the step)
-    G.gpt2_timing_begin(args.steps * 400)
+    G.gpt2_timing_begin(args.steps * 500 * ACCUM * L // 12)
     for _ in range(args.steps):
         device_step()
     G.gpt2_timing_end()
@@ -316,10 +330,10 @@ def run_ours(args):
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     G.gpt2_sync()
 
-    tokens_all = world * B * T * args.steps
+    tokens_all = world * ACCUM * B * T * args.steps
     value = tokens_all / (ms / 1000.0)
     e2e_value = tokens_all / e2e_s
-    step_flops = model_flops_per_token() * B * T
+    step_flops = model_flops_per_token() * ACCUM * B * T
 
     fam = {}
     for f in G.FAMILIES:
@@ -347,7 +361,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": T,
+        "config": {"workload": WORKLOAD, "global_batch": ACCUM * B * world, "seq_len": T,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "no flush: per-step working set (~6 GB) is larger than L2"},
         "mfu": step_flops / (ms / 1000.0 / args.steps) / (peaks["bf16_tflops_sustained"] * 1e12),
@@ -355,8 +369,8 @@ def run_ours(args):
         "model_tflop_per_step": step_flops / 1e12,
         "roofline": roofline,
         "breakdown": breakdown,
-        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": 2 * B * T * 4,
-                "d2h_bytes_per_step": 4},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": 2 * ACCUM * B * T * 4,
+                "d2h_bytes_per_step": 4 * ACCUM},
         "gpu_launches": launches,
         "clocks": clk,
         "loss": {"device_path": loss_dev, "host_path": loss_host},
@@ -379,7 +393,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--model", default="124m", choices=["124m", "350m"],
+                    help="124m: the headline workload (B=8, T=1024); 350m: B=16, T=1024, "
+                         "4 accumulation micro-steps per update")
     args = ap.parse_args()
+    select_model(args.model)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":

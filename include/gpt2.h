@@ -101,16 +101,18 @@ int gpt2_backward(void);
  * master copy is updated and rounded (nearest-even) into the bf16 parameters. */
 int gpt2_adamw(float lr, float beta1, float beta2, float eps, float weight_decay, int step);
 
-/* One whole training step on DEVICE-resident int32 tokens and targets (B*T
- * each): gpt2_forward_device, gpt2_zero_grad, gpt2_backward and gpt2_adamw in
- * that order, with the same results. The first call for a given (d_tokens,
+/* One whole training step on DEVICE-resident int32 tokens and targets:
+ * gpt2_zero_grad, then for each of the k = gpt2_set_grad_accum micro-steps
+ * gpt2_forward_device and gpt2_backward on the next B*T ids (the buffers hold
+ * k*B*T each), then gpt2_adamw, with the same results as those calls. The
+ * mean loss of micro-step i goes to d_mean_loss[i] (may be NULL). The first call for a given (d_tokens,
  * d_targets, d_mean_loss, B, T, grad-accumulation k) runs eagerly and records
  * the step's launches into a CUDA graph; later calls with the same set replay
  * the graph (the AdamW arguments may change from call to call), which removes
  * the per-launch host cost and most of the gaps between kernels. The buffers
  * are read at replay time, so refill them in place between calls. Fully
- * asynchronous on the model's stream; *d_mean_loss (may be NULL) receives the
- * mean loss. With gpt2_timing_begin active every call runs eagerly. */
+ * asynchronous on the model's stream. With gpt2_timing_begin active every call
+ * runs eagerly. */
 int gpt2_train_step(const int* d_tokens, const int* d_targets, int B, int T, float lr, float beta1,
                     float beta2, float eps, float weight_decay, int step, float* d_mean_loss);
 

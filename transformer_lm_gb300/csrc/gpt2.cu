@@ -741,10 +741,20 @@ int gpt2_train_step(const int* d_tokens, const int* d_targets, int B, int T, flo
         m->fwd_targets = 0;
         return GPT2_OK;
     }
+    // zero_grad, then k micro-steps (forward, backward) on consecutive B*T slices
+    const int k = m->grad_accum;
+    const size_t n = (size_t)B * T;
+    auto micro_steps = [&]() -> int {
+        TRY(gpt2_zero_grad());
+        for (int i = 0; i < k; i++) {
+            TRY(gpt2_forward_device(d_tokens + i * n, d_targets + i * n, B, T,
+                                    d_mean_loss ? d_mean_loss + i : nullptr));
+            TRY(gpt2_backward());
+        }
+        return GPT2_OK;
+    };
     // eager step
-    TRY(gpt2_forward_device(d_tokens, d_targets, B, T, d_mean_loss));
-    TRY(gpt2_zero_grad());
-    TRY(gpt2_backward());
+    TRY(micro_steps());
     TRY(run_adamw(m, lr, beta1, beta2, eps, weight_decay, step, nullptr));
     if (m->timing.on) return GPT2_OK;  // timing events are not recorded into graphs
     // record the step for the next calls
@@ -754,9 +764,7 @@ int gpt2_train_step(const int* d_tokens, const int* d_targets, int B, int T, flo
     m->graph = nullptr;
     const long long l0 = launch_count();
     CUDA_TRY(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal));
-    int rc = gpt2_forward_device(d_tokens, d_targets, B, T, d_mean_loss);
-    if (rc == GPT2_OK) rc = gpt2_zero_grad();
-    if (rc == GPT2_OK) rc = gpt2_backward();
+    int rc = micro_steps();
     if (rc == GPT2_OK) rc = run_adamw(m, lr, beta1, beta2, eps, weight_decay, step, m->d_hyper);
     cudaGraph_t graph = nullptr;
     cudaError_t e = cudaStreamEndCapture(m->stream, &graph);

@@ -176,11 +176,14 @@ long long gpt2_launch_count(void);
  * GELU + Softmax" problem statement: nn.Linear then GELU then softmax over dim 1).
  * x: DEVICE fp32 (M,K) row-major; W: DEVICE fp32 (N,K) row-major (nn.Linear
  * layout); b: DEVICE fp32 (N); out: DEVICE fp32 (M,N) row-major, caller-owned.
- * The GEMM runs on the TF32 tensor cores (fp32 accumulate). x, W and out must
- * be 16-byte aligned with K % 4 == 0 and N % 4 == 0 (else GPT2_ERR_ALIGN);
- * M, K, N >= 1 (else GPT2_ERR_ARG). Asynchronous on `stream` (a cudaStream_t,
- * NULL = legacy default stream). The first call on a device allocates its
- * scratch (per-row softmax partials, grown as needed and kept until exit). */
+ * The GEMM splits each fp32 operand into bf16 halves (hi, lo) and runs
+ * hi.hi + hi.lo + lo.hi on the bf16 tensor cores with fp32 accumulation
+ * (about 2^-16 relative per product; outputs within 1e-3 relative of fp64).
+ * x, W and out must be 16-byte aligned with K % 4 == 0 and N % 4 == 0 (else
+ * GPT2_ERR_ALIGN); M, K, N >= 1 (else GPT2_ERR_ARG). Asynchronous on `stream`
+ * (a cudaStream_t, NULL = legacy default stream). The first call on a device
+ * allocates its scratch (per-row softmax partials and the split operands,
+ * 6*(M+N)*K bytes; grown as needed and kept until exit). */
 int fused_linear_bias_gelu_softmax(const float* x, const float* W, const float* b, float* out,
                                    int M, int K, int N, void* stream);
 
@@ -189,8 +192,10 @@ int fused_linear_bias_gelu_softmax(const float* x, const float* W, const float* 
  * memory -- processes whose own pool allocator owns all device memory, where a
  * cudaMalloc behind its back can fail or fragment the pool, and loops that
  * cannot take the device-wide synchronisation a cudaMalloc may imply).
- * Same arguments, result and errors as fused_linear_bias_gelu_softmax; it calls
- * no cudaMalloc/cudaFree or other allocating routine. Its per-row softmax
+ * Same arguments and errors as fused_linear_bias_gelu_softmax; it calls no
+ * cudaMalloc/cudaFree or other allocating routine. Its GEMM is single-pass TF32
+ * (operands truncated to a 10-bit mantissa): elementwise error up to a few
+ * 1e-3 relative at K = 8192. Its per-row softmax
  * partials live in a static device array of 1 MiB that every GPU loading the
  * library holds until exit, which limits M * ceil(N/256) to 131072 (e.g.
  * M = 1024 rows with N up to 32768); larger sizes return GPT2_ERR_ARG with a

@@ -205,7 +205,7 @@ def test_fused_op_small_shapes_match_oracle():
         G.gpt2_device_status()
         y = host(out)
         np.testing.assert_allclose(y.sum(1), 1.0, atol=1e-5)
-        assert max_rel_floor(y, ref, 0.0) < 2e-2, (M, K, N, max_rel_floor(y, ref, 0.0))
+        assert max_rel_floor(y, ref, 0.0) < 1e-3, (M, K, N, max_rel_floor(y, ref, 0.0))
 
 
 @pytest.mark.parametrize("N,C,dt", [(1000, 768, "bf16"), (37, 64, "f32"), (8192, 768, "bf16"),

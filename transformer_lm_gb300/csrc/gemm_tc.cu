@@ -121,16 +121,18 @@ template <typename T, typename TO, int EPI, int OC>
 DEVI void epilogue_chunk(const Args& a, float (&v)[OC], const Vec16<T> (&r)[OC * sizeof(T) / 16], int row,
                          int nc, uint32_t (&o)[32], uint32_t (&o2)[32], float& pmax, float& psum) {
     constexpr int VEC = 16 / (int)sizeof(T);
-    const T* bias = (const T*)a.bias;
+    // the bias has the output's element type
+    constexpr int BV = 16 / (int)sizeof(TO);
+    const TO* bias = (const TO*)a.bias;
     if constexpr (EPI == EPI_STORE || EPI == EPI_GELU || EPI == EPI_RESID || EPI == EPI_GELU_PART) {
         if (bias) {
 #pragma unroll
-            for (int k = 0; k < OC / VEC; k++) {
-                if (nc + k * VEC < a.N) {
-                    Vec16<T> bb;
-                    *reinterpret_cast<int4*>(&bb) = __ldg(reinterpret_cast<const int4*>(bias + nc + k * VEC));
+            for (int k = 0; k < OC / BV; k++) {
+                if (nc + k * BV < a.N) {
+                    Vec16<TO> bb;
+                    *reinterpret_cast<int4*>(&bb) = __ldg(reinterpret_cast<const int4*>(bias + nc + k * BV));
 #pragma unroll
-                    for (int e = 0; e < VEC; e++) v[k * VEC + e] += to_f(bb.v[e]);
+                    for (int e = 0; e < BV; e++) v[k * BV + e] += to_f(bb.v[e]);
                 }
             }
         }
@@ -200,9 +202,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr int UK = KIND == 0 ? 16 : 8;     // K elements per MMA
     constexpr int KSTEPS = KE / UK;            // MMAs per stage (4)
     constexpr int BNC = BN / CG;               // rows of B this CTA holds
-    // epilogue output: fp32 for kind::tf32 and for split-K partials, else bf16;
+    // epilogue output: fp32 for kind::tf32, split-K partials and the fused
+    // operator's GELU tiles, else bf16;
     // a 128-byte chunk holds OC output columns
-    constexpr bool OUT_F32 = KIND == 1 || EPI == EPI_SPLITK;
+    constexpr bool OUT_F32 = KIND == 1 || EPI == EPI_SPLITK || EPI == EPI_GELU_PART;
     using TO = typename std::conditional<OUT_F32, float, bf16>::type;
     constexpr int OC = OUT_F32 ? 32 : 64;
     constexpr int NCH = BN / OC;
@@ -632,6 +635,7 @@ static int dispatch_epi(int epi, const Maps& mp, const tc::Args& a, cudaStream_t
             case EPI_GELU_BWD: return launch_tc<BN, KIND, EPI_GELU_BWD, CG>(mp, a, s);
             case EPI_ACCUM: return launch_tc<BN, KIND, EPI_ACCUM, CG>(mp, a, s);
             case EPI_SPLITK: return launch_tc<BN, KIND, EPI_SPLITK, CG>(mp, a, s);
+            case EPI_GELU_PART: return launch_tc<BN, KIND, EPI_GELU_PART, CG>(mp, a, s);
             default: return GPT2_ERR_CONFIG;
         }
     } else {
@@ -654,8 +658,11 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
     const int KE = tc::ROWB / esz;
     // tf32 operands only in K-major form
     if (dt == DT_F32 && (!p.a_kmajor || !p.b_kmajor)) return GPT2_ERR_CONFIG;
+    // the fused operator's GELU tiles (and bias) are fp32 whatever the operands
+    const DType out_dt = p.epi == EPI_GELU_PART ? DT_F32 : dt;
+    const int osz = out_dt == DT_BF16 ? 2 : 4;
     if (!al16(p.A) || !al16(p.B) || !al16(p.D) || (p.lda * esz) % 16 || (p.ldb * esz) % 16 ||
-        (p.ldd * esz) % 16 || p.N % vec)
+        (p.ldd * osz) % 16 || p.N % (16 / osz) || (dt == DT_BF16 && p.N % vec && p.epi != EPI_GELU_PART))
         return GPT2_ERR_ALIGN;
     const bool has_aux = p.epi == EPI_RESID || p.epi == EPI_GELU_BWD;
     if (has_aux && (!p.aux || !al16(p.aux) || (p.ldaux * esz) % 16)) return GPT2_ERR_ALIGN;
@@ -728,7 +735,6 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
     }
 
     Maps mp;
-    const int OC = tc::ROWB / esz;  // output columns per 128-byte chunk
     bool ok = p.a_kmajor ? make_map(&mp.a, p.A, dt, p.K, p.M, p.lda, KE, tc::BM)
                          : make_map(&mp.a, p.A, dt, p.M, p.K, p.lda, KE, KE);
     ok = ok && (p.b_kmajor ? make_map(&mp.b, p.B, dt, p.K, p.N, p.ldb, KE, BN / cg)
@@ -744,8 +750,9 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
         return launch_splitk_reduce((bf16*)p.D, p.ldd, p.ws, p.M, p.N, a.splits, s);
     }
     // output boxes: one 128-byte chunk x 32 rows (an epilogue warp's store)
-    ok = ok && make_map(&mp.d, p.D, dt, p.N, p.M, p.ldd, OC, 32);
-    ok = ok && make_map(&mp.d2, p.epi == EPI_GELU ? p.D2 : p.D, dt, p.N, p.M, p.ldd, OC, 32);
+    const int OCO = tc::ROWB / osz;
+    ok = ok && make_map(&mp.d, p.D, out_dt, p.N, p.M, p.ldd, OCO, 32);
+    ok = ok && make_map(&mp.d2, p.epi == EPI_GELU ? p.D2 : p.D, out_dt, p.N, p.M, p.ldd, OCO, 32);
     if (!ok) return GPT2_ERR_CUDA;
     if (dt == DT_BF16) {
         if (cg == 2)

@@ -121,6 +121,9 @@ void launch_init_normal(DType dt, void* p, size_t n, float stddev, unsigned long
 void launch_fill(DType dt, void* p, size_t n, float value, cudaStream_t s);
 void launch_to_f32(DType dt, float* dst, const void* src, size_t n, cudaStream_t s);
 void launch_from_f32(DType dt, void* dst, const float* src, size_t n, cudaStream_t s);
+// fp32 (rows, K) -> bf16 (rows, 3*Kp): [hi | hi | lo] (mode 0) or [hi | lo | hi] (mode 1)
+void launch_split_bf16x3(void* dst, const float* src, int rows, int K, int Kp, int mode,
+                         cudaStream_t s);
 // out = softmax over each row of a (M,N) fp32 tile-partial GELU output (fused operator pass 2)
 void launch_softmax_finish(float* y, const float* part, int M, int N, int tiles, cudaStream_t s);
 

@@ -2,10 +2,13 @@
 //
 //  * fused_linear_bias_gelu_softmax: y = softmax_row(gelu_tanh(x W^T + b))
 //    (POPCORNBENCH "fused Linear + GELU + Softmax" problem: nn.Linear, GELU,
-//    softmax over dim 1). Pass 1 is the tcgen05 TF32 GEMM whose epilogue adds
+//    softmax over dim 1). x and W are split into bf16 halves (hi, lo) and
+//    x W^T runs as hi.hi + hi.lo + lo.hi on the bf16 tensor cores (about
+//    2^-16 relative per product, fp32 accumulation); the GEMM epilogue adds
 //    the bias, applies GELU, stores the row tile and records, per row and
-//    256-column tile, (max, sum exp(v - max)). Pass 2 merges the tile
-//    partials of each row and rewrites the row as exp(v - max) / sum.
+//    256-column tile, (max, sum exp(v - max)). The last pass merges the tile
+//    partials of each row and rewrites the row as exp(v - max) / sum. The
+//    allocation-free variant keeps the single-pass TF32 GEMM.
 //  * gpt2_gemm / gpt2_attention_forward / gpt2_attention_backward: the
 //    training step's kernels exposed one at a time.
 #include "gpt2.h"
@@ -68,8 +71,13 @@ int fused_linear_bias_gelu_softmax(const float* x, const float* W, const float* 
     if (!err) return GPT2_ERR_NOMEM;
     const int tile_n = gemm_tc_part_tile_n();
     const int tiles = (N + tile_n - 1) / tile_n;
-    const size_t need = (size_t)M * tiles * 2 * sizeof(float);
-    float* part;
+    // scratch: the row-tile softmax partials, then the split operands
+    // x' (M, 3Kp) and W' (N, 3Kp) in bf16
+    const int Kp = (K + 7) / 8 * 8;
+    const size_t part_bytes = ((size_t)M * tiles * 2 * sizeof(float) + 255) / 256 * 256;
+    const size_t xs_bytes = ((size_t)M * 3 * Kp * 2 + 255) / 256 * 256;
+    const size_t need = part_bytes + xs_bytes + (size_t)N * 3 * Kp * 2;
+    char* scratch;
     {
         std::lock_guard<std::mutex> lk(ops_mu);
         if (dev_part_bytes[dev] < need) {
@@ -79,16 +87,23 @@ int fused_linear_bias_gelu_softmax(const float* x, const float* W, const float* 
             if (cudaMalloc(&dev_part[dev], need) != cudaSuccess) return GPT2_ERR_NOMEM;
             dev_part_bytes[dev] = need;
         }
-        part = dev_part[dev];
+        scratch = (char*)dev_part[dev];
     }
+    float* part = (float*)scratch;
+    void* xs = scratch + part_bytes;
+    void* ws = scratch + part_bytes + xs_bytes;
     cudaStream_t s = (cudaStream_t)stream;
+    // x W^T as hi.hi + hi.lo + lo.hi over bf16 halves of each fp32 operand, on
+    // the bf16 tensor cores (fp32 accumulation)
+    launch_split_bf16x3(xs, x, M, K, Kp, 0, s);
+    launch_split_bf16x3(ws, W, N, K, Kp, 1, s);
     GemmParams p = {};
-    p.A = x; p.lda = K; p.a_kmajor = 1;
-    p.B = W; p.ldb = K; p.b_kmajor = 1;
+    p.A = xs; p.lda = 3LL * Kp; p.a_kmajor = 1;
+    p.B = ws; p.ldb = 3LL * Kp; p.b_kmajor = 1;
     p.D = out; p.ldd = N; p.bias = b;
     p.part = part; p.part_ld = tiles;
-    p.M = M; p.N = N; p.K = K; p.epi = EPI_GELU_PART;
-    int rc = gemm_tc(p, DT_F32, s, err);
+    p.M = M; p.N = N; p.K = 3 * Kp; p.epi = EPI_GELU_PART;
+    int rc = gemm_tc(p, DT_BF16, s, err);
     if (rc != GPT2_OK) return rc;
     launch_softmax_finish(out, part, M, N, tiles, s);
     return launch_status();

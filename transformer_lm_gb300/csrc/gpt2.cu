@@ -61,6 +61,8 @@ struct Timing {
     double works[FAM_COUNT] = {0};
 };
 
+constexpr int kEvents = 16;  // fork / join events of the two-stream backward
+
 struct Model {
     int L, C, NH, V, Vp, maxT, HS;
     int prec;  // GPT2_FP32 / GPT2_BF16
@@ -76,6 +78,8 @@ struct Model {
     unsigned int* d_err = nullptr;
     cudaStream_t stream = nullptr;
     cudaStream_t own_stream = nullptr;
+    cudaStream_t side = nullptr;  // the backward's weight-gradient stream
+    cudaEvent_t ev[kEvents] = {};
     int grad_accum = 1;
     int fwd_done = 0, fwd_targets = 0;
     // activations
@@ -190,6 +194,9 @@ void free_model(Model* m) {
     if (m->graph) cudaGraphDestroy(m->graph);
     for (cudaEvent_t e : m->timing.ev) cudaEventDestroy(e);
     if (m->own_stream) cudaStreamDestroy(m->own_stream);
+    if (m->side) cudaStreamDestroy(m->side);
+    for (cudaEvent_t e : m->ev)
+        if (e) cudaEventDestroy(e);
     delete m;
 }
 
@@ -400,18 +407,60 @@ int run_forward(Model* m, bool has_targets) {
 }
 
 // ------------------------------------------------------------------ backward
+// The backward as two streams. The main stream carries the chain that feeds
+// each next step (dX products, LayerNorm backward, attention backward); the
+// weight-gradient products and the fc / qkv bias column sums go to a side
+// stream as soon as their inputs exist and are joined right before the first
+// kernel that overwrites one of those inputs. The side kernels fill the SMs the
+// main kernels leave idle in their last waves. Nothing is reordered within a
+// stream, and every tensor still receives the same += in the same order.
 int run_backward(Model* m) {
     const int B = m->B, T = m->T, C = m->C, L = m->L, NH = m->NH, Vp = m->Vp;
     const size_t BT = (size_t)B * T, es = m->esz;
     const DType dt = m->dt;
     cudaStream_t s = m->stream;
+    const bool par = m->side != nullptr && !m->timing.on;
+    cudaStream_t side = par ? m->side : s;
+    int evi = 0;
+    // a point on one stream that the other must pass before going on
+    auto edge = [&](cudaStream_t from, cudaStream_t to) -> int {
+        if (!par) return GPT2_OK;
+        cudaEvent_t e = m->ev[evi++ % kEvents];
+        CUDA_TRY(cudaEventRecord(e, from));
+        CUDA_TRY(cudaStreamWaitEvent(to, e, 0));
+        return GPT2_OK;
+    };
+    // run f with the model's launches going to the side stream
+    auto on_side = [&](auto&& f) -> int {
+        cudaStream_t keep = m->stream;
+        m->stream = side;
+        const int rc = f();
+        m->stream = keep;
+        return rc;
+    };
+    // a join: the event is recorded on the side stream now, waited on main later
+    auto mark_side = [&](cudaEvent_t& e) -> int {
+        if (!par) return GPT2_OK;
+        e = m->ev[evi++ % kEvents];
+        CUDA_TRY(cudaEventRecord(e, side));
+        return GPT2_OK;
+    };
+    auto wait_side = [&](cudaEvent_t e) -> int {
+        if (!par || !e) return GPT2_OK;
+        CUDA_TRY(cudaStreamWaitEvent(s, e, 0));
+        return GPT2_OK;
+    };
     auto act = [&](void* base, int l, size_t width) { return (char*)base + (size_t)l * BT * width * es; };
     const double lnb_bytes = 4.0 * BT * C * es + 8.0 * BT;
-    // classifier matmul: dlnf = dlogits . wte ; dwte += dlogits^T . lnf
+    // classifier matmul: dlnf = dlogits . wte (main); dwte += dlogits^T . lnf
+    // (side, joined before the encoder backward adds to dwte)
+    TRY(edge(s, side));
+    TRY(on_side([&] {
+        return gemm(m, EPI_ACCUM, m->logits, Vp, 0, m->lnf, C, 0, G(m, 0), C, nullptr, nullptr, 0,
+                    nullptr, Vp, C, (int)BT);
+    }));
     TRY(gemm(m, EPI_STORE, m->logits, Vp, 1, P(m, 0), C, 0, m->dbtc, C, nullptr, nullptr, 0, nullptr,
              (int)BT, C, Vp));
-    TRY(gemm(m, EPI_ACCUM, m->logits, Vp, 0, m->lnf, C, 0, G(m, 0), C, nullptr, nullptr, 0, nullptr,
-             Vp, C, (int)BT));
     void* last = L == 0 ? m->encoded : act(m->residual3, L - 1, C);
     // LayerNorm i backward into its partial area; the column sums of its output
     // (the next-lower matmul's bias grad) come fused or from a colsum pass
@@ -429,6 +478,7 @@ int run_backward(Model* m) {
         return GPT2_OK;
     };
     TRY(ln_bwd(2 * L, last, P(m, 14), m->lnf_mean, m->lnf_rstd, 0, L > 0));
+    cudaEvent_t qkv_done = nullptr;  // the previous layer's qkv weight grad has read dbt4c
     for (int l = L - 1; l >= 0; l--) {
         void* resid_in = l == 0 ? m->encoded : act(m->residual3, l - 1, C);
         void* ln1 = act(m->ln1, l, C);
@@ -439,28 +489,48 @@ int run_backward(Model* m) {
         void* fch = act(m->fch, l, 4 * C);
         void* fchg = act(m->fch_gelu, l, 4 * C);
         float* lse = m->lse + (size_t)l * B * NH * T;
-        // fcproj (W: C x 4C) with the GELU backward fused into the dX epilogue
+        cudaEvent_t fcproj_w = nullptr, fc_w = nullptr, attproj_w = nullptr;
+        // fcproj (W: C x 4C): dW += dresidual^T fch_gelu on the side
+        TRY(edge(s, side));
+        TRY(on_side([&] {
+            return gemm(m, EPI_ACCUM, m->dresidual, C, 0, fchg, 4 * C, 0,
+                        G(m, 12) + (size_t)l * 4 * C * C * es, 4 * C, nullptr, nullptr, 0, nullptr, C,
+                        4 * C, (int)BT);
+        }));
+        TRY(mark_side(fcproj_w));
+        // dX with the GELU backward fused into its epilogue (overwrites dbt4c)
+        TRY(wait_side(qkv_done));
         TRY(gemm(m, EPI_GELU_BWD, m->dresidual, C, 1, P(m, 12) + (size_t)l * 4 * C * C * es, 4 * C, 0,
                  m->dbt4c, 4 * C, nullptr, fch, 4 * C, nullptr, (int)BT, 4 * C, C));
-        TRY(gemm(m, EPI_ACCUM, m->dresidual, C, 0, fchg, 4 * C, 0, G(m, 12) + (size_t)l * 4 * C * C * es,
-                 4 * C, nullptr, nullptr, 0, nullptr, C, 4 * C, (int)BT));
         // (fcproj's bias grad: the column sums of the LayerNorm backward above)
-        // fc (W: 4C x C)
+        // fc (W: 4C x C): dW and the bias column sums read dbt4c, on the side
+        TRY(edge(s, side));
+        TRY(on_side([&] {
+            TRY(gemm(m, EPI_ACCUM, m->dbt4c, 4 * C, 0, ln2, C, 0, G(m, 10) + (size_t)l * 4 * C * C * es,
+                     C, nullptr, nullptr, 0, nullptr, 4 * C, C, (int)BT));
+            TIMED(FAM_OTHER, 4.0 * BT * C * es,
+                  launch_colsum_part(dt, fcb_part(m, l), m->dbt4c, (int)BT, 4 * C, m->stream));
+            return GPT2_OK;
+        }));
+        TRY(mark_side(fc_w));
         TRY(gemm(m, EPI_STORE, m->dbt4c, 4 * C, 1, P(m, 10) + (size_t)l * 4 * C * C * es, C, 0, m->dbtc,
                  C, nullptr, nullptr, 0, nullptr, (int)BT, C, 4 * C));
-        TRY(gemm(m, EPI_ACCUM, m->dbt4c, 4 * C, 0, ln2, C, 0, G(m, 10) + (size_t)l * 4 * C * C * es, C,
-                 nullptr, nullptr, 0, nullptr, 4 * C, C, (int)BT));
-        TIMED(FAM_OTHER, 4.0 * BT * C * es,
-              launch_colsum_part(dt, fcb_part(m, l), m->dbt4c, (int)BT, 4 * C, s));
+        // LayerNorm 2 backward adds into dresidual, which fcproj's dW reads
+        TRY(wait_side(fcproj_w));
         TRY(ln_bwd(2 * l + 1, res2, P(m, 8) + (size_t)l * C * es, m->ln2_mean + l * BT,
                    m->ln2_rstd + l * BT, 1, true));
-        // attention projection (W: C x C)
+        // attention projection (W: C x C): dW on the side
+        TRY(edge(s, side));
+        TRY(on_side([&] {
+            return gemm(m, EPI_ACCUM, m->dresidual, C, 0, atty, C, 0, G(m, 6) + (size_t)l * C * C * es, C,
+                        nullptr, nullptr, 0, nullptr, C, C, (int)BT);
+        }));
+        TRY(mark_side(attproj_w));
         TRY(gemm(m, EPI_STORE, m->dresidual, C, 1, P(m, 6) + (size_t)l * C * C * es, C, 0, m->dbtc, C,
                  nullptr, nullptr, 0, nullptr, (int)BT, C, C));
-        TRY(gemm(m, EPI_ACCUM, m->dresidual, C, 0, atty, C, 0, G(m, 6) + (size_t)l * C * C * es, C,
-                 nullptr, nullptr, 0, nullptr, C, C, (int)BT));
         // (attproj's bias grad: the column sums of LayerNorm 2's backward)
-        // attention: dqkv (B,T,3C) into the 4C scratch
+        // attention: dqkv (B,T,3C) into dbt4c, which fc's dW and bias sums read
+        TRY(wait_side(fc_w));
         {
             int rc_ = GPT2_OK;
             TIMED(FAM_ATTN_BWD, 4.0 * B * NH * (double)T * (T + 1) * (C / NH),
@@ -468,16 +538,25 @@ int run_backward(Model* m) {
                                                   B, T, C, NH, s, m->d_err));
             if (rc_ != GPT2_OK) return rc_;
         }
-        // qkv (W: 3C x C)
+        // qkv (W: 3C x C): dW and the bias column sums on the side
+        TRY(edge(s, side));
+        TRY(on_side([&] {
+            TRY(gemm(m, EPI_ACCUM, m->dbt4c, 3 * C, 0, ln1, C, 0, G(m, 4) + (size_t)l * 3 * C * C * es, C,
+                     nullptr, nullptr, 0, nullptr, 3 * C, C, (int)BT));
+            TIMED(FAM_OTHER, 3.0 * BT * C * es,
+                  launch_colsum_part(dt, qkvb_part(m, l), m->dbt4c, (int)BT, 3 * C, m->stream));
+            return GPT2_OK;
+        }));
+        TRY(mark_side(qkv_done));
         TRY(gemm(m, EPI_STORE, m->dbt4c, 3 * C, 1, P(m, 4) + (size_t)l * 3 * C * C * es, C, 0, m->dbtc,
                  C, nullptr, nullptr, 0, nullptr, (int)BT, C, 3 * C));
-        TRY(gemm(m, EPI_ACCUM, m->dbt4c, 3 * C, 0, ln1, C, 0, G(m, 4) + (size_t)l * 3 * C * C * es, C,
-                 nullptr, nullptr, 0, nullptr, 3 * C, C, (int)BT));
-        TIMED(FAM_OTHER, 3.0 * BT * C * es,
-              launch_colsum_part(dt, qkvb_part(m, l), m->dbt4c, (int)BT, 3 * C, s));
+        // LayerNorm 1 backward adds into dresidual, which attproj's dW reads
+        TRY(wait_side(attproj_w));
         TRY(ln_bwd(2 * l, resid_in, P(m, 2) + (size_t)l * C * es, m->ln1_mean + l * BT,
                    m->ln1_rstd + l * BT, 1, l > 0));
     }
+    // everything on the side stream is done before the sums are read
+    TRY(edge(side, s));
     // every LayerNorm and bias grad: += its partial rows, summed in order
     TIMED(FAM_OTHER, 0.0, launch_reduce_partials_multi(dt, m->d_desc, m->ndesc, 4 * C, s));
     TIMED(FAM_ENCODER, 2.0 * BT * C * es,
@@ -591,6 +670,12 @@ int gpt2_init_ex(int L, int C, int NH, int V, int Vp, int maxT, unsigned long lo
         return fail(GPT2_ERR_CUDA, "stream: %s", cudaGetErrorString(e));
     }
     m->stream = m->own_stream;
+    if (cudaStreamCreateWithFlags(&m->side, cudaStreamNonBlocking) != cudaSuccess) m->side = nullptr;
+    for (int i = 0; m->side && i < kEvents; i++)
+        if (cudaEventCreateWithFlags(&m->ev[i], cudaEventDisableTiming) != cudaSuccess) {
+            cudaStreamDestroy(m->side);  // stay on one stream
+            m->side = nullptr;
+        }
     bool ok = cudaMalloc(&m->params, off * m->esz + 256) == cudaSuccess &&
               cudaMalloc(&m->grads, off * m->esz + 256) == cudaSuccess &&
               cudaMalloc((void**)&m->mom_m, off * 4 + 256) == cudaSuccess &&

@@ -107,6 +107,14 @@ void launch_reduce_partials_multi(DType dt, const PartialDesc* d_desc, int ndesc
 void launch_classifier(DType dt, void* logits, float* losses, const int* targets, int BT, int V,
                        int Vp, float dloss, cudaStream_t s);
 void launch_mean(const float* x, int n, float* out, cudaStream_t s);
+// ranges of the flat parameter buffers one AdamW launch updates (offsets and
+// counts are multiples of 4)
+struct AdamRanges {
+    size_t off[8], n[8];
+};
+void launch_adamw_ranges(DType dt, void* params, float* master, const void* grads, float* m,
+                         float* v, const AdamRanges& r, int nranges, float lr, float b1, float b2,
+                         float c1, float c2, float eps, float wd, const float* hyper, cudaStream_t s);
 // hyper: NULL, or device floats {lr, b1, b2, c1, c2, eps, wd} that replace the
 // by-value ones (a CUDA graph replays the launch with new values there)
 void launch_adamw(DType dt, void* params, float* master, const void* grads, float* m, float* v,

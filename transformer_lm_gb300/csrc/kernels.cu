@@ -1158,13 +1158,20 @@ DEVI float adamw_one(float g, float& m, float& v, float theta, float lr, float b
 template <typename T>
 __global__ void adamw_k(T* __restrict__ params, float* __restrict__ master,
                         const T* __restrict__ grads, float* __restrict__ mst,
-                        float* __restrict__ vst, size_t n, float lr, float b1, float b2, float c1,
-                        float c2, float eps, float wd, const float* __restrict__ hyper) {
+                        float* __restrict__ vst, const AdamRanges r, float lr, float b1, float b2,
+                        float c1, float c2, float eps, float wd, const float* __restrict__ hyper) {
     pdl_enter();
     if (hyper) {  // hyperparameters from device memory (graph replays)
         lr = hyper[0]; b1 = hyper[1]; b2 = hyper[2]; c1 = hyper[3]; c2 = hyper[4];
         eps = hyper[5]; wd = hyper[6];
     }
+    // this block row's range of the flat parameter buffers
+    const size_t off = r.off[blockIdx.y], n = r.n[blockIdx.y];
+    params += off;
+    grads += off;
+    mst += off;
+    vst += off;
+    if (master) master += off;
     const size_t stride = (size_t)gridDim.x * blockDim.x * 4;
     for (size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4; i < n; i += stride) {
         if (i + 4 <= n) {
@@ -1221,14 +1228,26 @@ __global__ void adamw_k(T* __restrict__ params, float* __restrict__ master,
 void launch_adamw(DType dt, void* params, float* master, const void* grads, float* m, float* v,
                   size_t n, float lr, float b1, float b2, float c1, float c2, float eps, float wd,
                   const float* hyper, cudaStream_t s) {
+    AdamRanges r = {};
+    r.off[0] = 0;
+    r.n[0] = n;
+    launch_adamw_ranges(dt, params, master, grads, m, v, r, 1, lr, b1, b2, c1, c2, eps, wd, hyper, s);
+}
+
+void launch_adamw_ranges(DType dt, void* params, float* master, const void* grads, float* m,
+                         float* v, const AdamRanges& r, int nranges, float lr, float b1, float b2,
+                         float c1, float c2, float eps, float wd, const float* hyper, cudaStream_t s) {
+    if (nranges <= 0) return;
+    size_t nmax = 0;
+    for (int i = 0; i < nranges; i++) nmax = r.n[i] > nmax ? r.n[i] : nmax;
     note_launch(1);
-    unsigned g = grid_for((n + 3) / 4, 256, 8);
+    const dim3 grid(grid_for((nmax + 3) / 4, 256, 8), (unsigned)nranges);
     if (dt == DT_BF16)
-        launch_pdl(adamw_k<bf16>, g, 256, 0, s, (bf16*)params, master, (const bf16*)grads, m, v, n, lr, b1,
-                                        b2, c1, c2, eps, wd, hyper);
+        launch_pdl(adamw_k<bf16>, grid, dim3(256), 0, s, (bf16*)params, master, (const bf16*)grads, m, v, r,
+                   lr, b1, b2, c1, c2, eps, wd, hyper);
     else
-        launch_pdl(adamw_k<float>, g, 256, 0, s, (float*)params, master, (const float*)grads, m, v, n, lr,
-                                         b1, b2, c1, c2, eps, wd, hyper);
+        launch_pdl(adamw_k<float>, grid, dim3(256), 0, s, (float*)params, master, (const float*)grads, m, v,
+                   r, lr, b1, b2, c1, c2, eps, wd, hyper);
 }
 
 __global__ void set_hyper_k(float* h, float lr, float b1, float b2, float c1, float c2, float eps,

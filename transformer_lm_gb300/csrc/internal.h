@@ -68,10 +68,11 @@ void launch_layernorm_forward(DType dt, void* out, float* mean, float* rstd, con
                               const void* w, const void* b, int N, int C, cudaStream_t s);
 // dinp (+= if accumulate else =), dw += sum, db += sum (two-stage, deterministic).
 // ws: fp32 scratch of at least layernorm_backward_ws_floats(C) floats.
+// err: device error word of the bounded waits
 void launch_layernorm_backward(DType dt, void* dinp, void* dw, void* db, const void* dout,
                                const void* inp, const void* w, const float* mean,
                                const float* rstd, int N, int C, int accumulate, float* ws,
-                               cudaStream_t s);
+                               unsigned int* err, cudaStream_t s);
 size_t layernorm_backward_ws_floats(int C);
 // dbias[n] += sum_m dout[m][n] (two-stage, deterministic)
 void launch_colsum_accum(DType dt, void* dbias, const void* dout, int M, int N, float* ws,

@@ -447,161 +447,59 @@ __global__ void __launch_bounds__(LNB_BLOCK) layernorm_backward_k(
     }
 }
 
-// Same operation for bf16 rows of at most 32 * 8 * NV columns (NV <= 3), built for
-// memory-level parallelism: each lane keeps its weights and its dw/db column
-// partials in registers and loads the warp's next row while it computes the
-// current one, so every warp has two rows of loads in flight and nothing is
-// read twice. The block folds its warps in order through shared memory and
-// writes one partial row to ws (reduce_partials_k sums the blocks in order).
-template <int NV>
-__global__ void __launch_bounds__(LNB_BLOCK, 1) layernorm_backward_reg_k(
-    bf16* __restrict__ dinp, float* __restrict__ ws, const bf16* __restrict__ dout,
-    const bf16* __restrict__ inp, const bf16* __restrict__ w, const float* __restrict__ mean,
-    const float* __restrict__ rstd, int N, int C, int accumulate) {
-    pdl_enter();
-    constexpr int VEC = 8;
-    extern __shared__ float sm[];
-    const int warps = blockDim.x / 32;
-    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-    const int cv = C / VEC;
-    Vec16<bf16> wv[NV];  // the lane's weights, kept packed
-    float adw[NV][VEC], adb[NV][VEC];
-#pragma unroll
-    for (int j = 0; j < NV; j++) {
-        const int vi = lane + 32 * j;
-        if (vi < cv) wv[j] = ld16(w + vi * VEC);
-#pragma unroll
-        for (int k = 0; k < VEC; k++) {
-            adw[j][k] = 0.f;
-            adb[j][k] = 0.f;
-        }
-    }
-    const int stride = gridDim.x * warps;
-    int row = blockIdx.x * warps + warp;
-    Vec16<bf16> xa[NV], da[NV], oa[NV];
-    float mu = 0.f, rs = 0.f;
-    // a row's x, dy, the current dx (the += operand) and its statistics
-    auto load_row = [&](int r, Vec16<bf16> (&xv)[NV], Vec16<bf16> (&dv)[NV], Vec16<bf16> (&ov)[NV],
-                        float& m, float& sd) {
-        const bf16* x = inp + (size_t)r * C;
-        const bf16* dy = dout + (size_t)r * C;
-        const bf16* dxr = dinp + (size_t)r * C;
-#pragma unroll
-        for (int j = 0; j < NV; j++) {
-            const int vi = lane + 32 * j;
-            if (vi < cv) {
-                xv[j] = ld16_cs(x + vi * VEC);
-                dv[j] = ld16_cs(dy + vi * VEC);
-                if (accumulate) ov[j] = ld16(dxr + vi * VEC);
-            }
-        }
-        m = mean[r];
-        sd = rstd[r];
-    };
-    if (row < N) load_row(row, xa, da, oa, mu, rs);
-    while (row < N) {
-        const int nrow = row + stride;
-        Vec16<bf16> xb[NV], db2[NV], ob[NV];
-        float mu2 = 0.f, rs2 = 0.f;
-        if (nrow < N) load_row(nrow, xb, db2, ob, mu2, rs2);
-        bf16* dx = dinp + (size_t)row * C;
-        float gsum = 0.f, gnsum = 0.f;
-#pragma unroll
-        for (int j = 0; j < NV; j++) {
-            if (lane + 32 * j < cv) {
-#pragma unroll
-                for (int k = 0; k < VEC; k++) {
-                    const float g = to_f(wv[j].v[k]) * to_f(da[j].v[k]);
-                    gsum += g;
-                    gnsum += g * (to_f(xa[j].v[k]) - mu) * rs;
-                }
-            }
-        }
-        gsum = warp_sum(gsum) / C;
-        gnsum = warp_sum(gnsum) / C;
-#pragma unroll
-        for (int j = 0; j < NV; j++) {
-            const int vi = lane + 32 * j;
-            if (vi < cv) {
-                Vec16<bf16> o;
-#pragma unroll
-                for (int k = 0; k < VEC; k++) {
-                    const float d = to_f(da[j].v[k]);
-                    const float nh = (to_f(xa[j].v[k]) - mu) * rs;
-                    const float val = rs * (to_f(wv[j].v[k]) * d - gsum - nh * gnsum);
-                    o.v[k] = from_f<bf16>(accumulate ? to_f(oa[j].v[k]) + val : val);
-                    adw[j][k] += nh * d;
-                    adb[j][k] += d;
-                }
-                st16(dx + vi * VEC, o);
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < NV; j++) {
-            xa[j] = xb[j];
-            da[j] = db2[j];
-            oa[j] = ob[j];
-        }
-        mu = mu2;
-        rs = rs2;
-        row = nrow;
-    }
-    // fold the warps in order: sm[warp][dw | db][column]
-    float* mine = sm + (size_t)warp * 2 * C;
-#pragma unroll
-    for (int j = 0; j < NV; j++) {
-        const int vi = lane + 32 * j;
-        if (vi < cv) {
-#pragma unroll
-            for (int k = 0; k < VEC; k++) {
-                mine[vi * VEC + k] = adw[j][k];
-                mine[C + vi * VEC + k] = adb[j][k];
-            }
-        }
-    }
-    __syncthreads();
-    float* dst = ws + (size_t)blockIdx.x * 2 * C;
-    for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) {
-        float t = 0.f;
-        for (int wi = 0; wi < warps; wi++) t += sm[(size_t)wi * 2 * C + c];
-        dst[c] = t;
-    }
-}
-
 // The same operation (bf16, C <= 768) as a persistent kernel fed by bulk
 // copies: one producer thread streams each of the CTA's rows (x, dy and, for
 // +=, the current dx) from HBM into a ring of LNQ_RING shared-memory slots with
-// cp.async.bulk, so up to LNQ_RING rows per SM are in flight; seven consumer
-// warps take the slots in turn (warp per row), keep dw / db partials in
-// registers and write dx. With `with_colsum` they also sum the written dx rows
-// by column (the bias gradient of the matmul that produced this residual-stream
-// gradient). The block folds its warps in order and writes one partial row
-// [dw | db | colsum] of G*C floats to part[blockIdx.x].
-constexpr int LNQ_RING = 20;
-constexpr int LNQ_WARPS = 7;  // consumer warps; warp LNQ_WARPS is the producer (8 warps: 2 per SM quarter)
+// cp.async.bulk, so up to LNQ_RING rows per SM are in flight. A row is taken
+// by a group of NV warps, each lane holding one 16-byte vector (8 columns) of
+// it; the groups take the slots in turn, combine the two row sums through
+// shared memory under a named barrier, write dx, and keep the dw / db partials
+// (and, with `with_colsum`, the column sums of the written dx: the bias
+// gradient of the matmul that produced this residual-stream gradient) in
+// registers. The CTA folds its warps in order into one partial row
+// [dw | db | colsum] of G*C floats at part[blockIdx.x].
+constexpr int LNQ_RING = 10;  // ring slots
+constexpr int LNQ_SR = 4;     // consecutive rows per slot (one bulk copy per array)
+constexpr int LNQ_THREADS = 512;  // 15 consumer warps + the producer warp
+constexpr int LNQ_XCH = 16 * 2 * 4;  // exchange entries: groups x parity x warps in a group
+
+// bytes of the ring or of the fold [groups][3][C] fp32, whichever is larger
+__host__ __device__ inline size_t lnq_body_bytes(int C, int groups) {
+    const size_t ring = (size_t)LNQ_RING * LNQ_SR * 3 * C * 2, fold = (size_t)groups * 3 * C * 4;
+    return ((ring > fold ? ring : fold) + 15) / 16 * 16;
+}
 
 template <int NV>
-__global__ void __launch_bounds__(32 * (LNQ_WARPS + 1)) layernorm_backward_bulk_k(
+__global__ void __launch_bounds__(LNQ_THREADS, 1) layernorm_backward_bulk_k(
     bf16* __restrict__ dinp, float* __restrict__ part, const bf16* __restrict__ dout,
     const bf16* __restrict__ inp, const bf16* __restrict__ w, const float* __restrict__ mean,
     const float* __restrict__ rstd, int N, int C, int accumulate, int with_colsum,
     unsigned int* __restrict__ err) {
     constexpr int VEC = 8;
+    constexpr int GROUPS = (LNQ_THREADS / 32 - 1) / NV;  // row groups of NV warps
+    constexpr int CWARPS = GROUPS * NV;                    // consumer warps
+    static_assert(GROUPS <= 15 && NV <= 4, "named barriers and the exchange area");
     extern __shared__ __align__(128) uint8_t lnq_sm[];
-    const int rowb = C * 2, slotb = 3 * rowb;
+    const int rowb = C * 2, arrb = LNQ_SR * rowb, slotb = 3 * arrb;  // a slot: [x | dy | dx] x SR rows
     uint8_t* ring = lnq_sm;
     const uint32_t ring_s = tc::smem_u32(ring);
-    uint8_t* tail = lnq_sm + (size_t)LNQ_RING * slotb;
+    // the ring, later reused by the fold of the groups' partial sums
+    uint8_t* tail = lnq_sm + lnq_body_bytes(C, GROUPS);
     const uint32_t bars = tc::smem_u32(tail);
     auto full = [&](int s) { return bars + 8u * s; };
     auto empty = [&](int s) { return bars + 8u * (LNQ_RING + s); };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tail + 16 * LNQ_RING);
     int* issued_s = reinterpret_cast<int*>(tail + 16 * LNQ_RING + 4);
+    // [group][row-pair parity][warp in group]: the two rows' (sum of w dy, sum
+    // of w dy nhat), and whether that warp's wait for the slot succeeded
+    float2* xch = reinterpret_cast<float2*>(tail + 16 * LNQ_RING + 16);
+    int* xok = reinterpret_cast<int*>(tail + 16 * LNQ_RING + 16 + LNQ_XCH * 16);
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    const int producer = LNQ_THREADS / 32 - 1;
     if (threadIdx.x == 0) {
         for (int s = 0; s < LNQ_RING; s++) {
             tc::mbar_init(full(s), 1);
-            tc::mbar_init(empty(s), 1);
+            tc::mbar_init(empty(s), NV);  // one arrival per warp of the group
         }
         *abort_flag = 0;
         *issued_s = 0;
@@ -609,111 +507,135 @@ __global__ void __launch_bounds__(32 * (LNQ_WARPS + 1)) layernorm_backward_bulk_
     }
     __syncthreads();
     pdl_enter();
-    const int nk = (N - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;  // rows of this CTA
+    // this CTA's rows: a contiguous range, in slots of LNQ_SR rows
+    const int per = (N + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int r_begin = min(N, (int)blockIdx.x * per), r_end = min(N, r_begin + per);
+    const int nk = (r_end - r_begin + LNQ_SR - 1) / LNQ_SR;  // slots of this CTA
     const int cv = C / VEC;
     const int G = with_colsum ? 3 : 2;
-    float adw[NV][VEC], adb[NV][VEC], acs[NV][VEC];  // consumer partial sums
+    const int grp = warp / NV, wig = warp % NV;  // row group, warp in group
+    const int vi = wig * 32 + lane;              // this lane's vector of the row
+    const bool has = warp < CWARPS && vi < cv;
+    float adw[VEC], adb[VEC], acs[VEC];
 #pragma unroll
-    for (int j = 0; j < NV; j++)
-#pragma unroll
-        for (int e = 0; e < VEC; e++) adw[j][e] = adb[j][e] = acs[j][e] = 0.f;
-    if (warp == LNQ_WARPS) {
+    for (int e = 0; e < VEC; e++) adw[e] = adb[e] = acs[e] = 0.f;
+    if (warp == producer) {
         if (lane == 0) {
             int issued = 0;
-            const uint32_t bytes = (uint32_t)(accumulate ? 3 * rowb : 2 * rowb);
             for (int k = 0; k < nk; k++) {
                 const int s = k % LNQ_RING;
                 if (!tc::mbar_wait(empty(s), (uint32_t)(((k / LNQ_RING) & 1) ^ 1), abort_flag)) break;
-                const size_t r = (size_t)blockIdx.x + (size_t)k * gridDim.x;
+                const size_t r = (size_t)r_begin + (size_t)k * LNQ_SR;
+                const uint32_t nb = (uint32_t)(min(LNQ_SR, r_end - (int)r) * rowb);
                 const uint32_t dst = ring_s + (uint32_t)(s * slotb);
-                tc::mbar_expect_tx(full(s), bytes);
-                tc::bulk_load(dst, inp + r * C, (uint32_t)rowb, full(s));
-                tc::bulk_load(dst + rowb, dout + r * C, (uint32_t)rowb, full(s));
-                if (accumulate) tc::bulk_load(dst + 2 * rowb, dinp + r * C, (uint32_t)rowb, full(s));
+                tc::mbar_expect_tx(full(s), (accumulate ? 3u : 2u) * nb);
+                tc::bulk_load(dst, inp + r * C, nb, full(s));
+                tc::bulk_load(dst + arrb, dout + r * C, nb, full(s));
+                if (accumulate) tc::bulk_load(dst + 2 * arrb, dinp + r * C, nb, full(s));
                 ++issued;
             }
             *issued_s = issued;
         }
-    } else {
-        Vec16<bf16> wv[NV];
-#pragma unroll
-        for (int j = 0; j < NV; j++) {
-            const int vi = lane + 32 * j;
-            if (vi < cv) wv[j] = ld16(w + vi * VEC);
-        }
-        float mu = 0.f, rs = 0.f;
-        if (warp < nk) {
-            const size_t r = (size_t)blockIdx.x + (size_t)warp * gridDim.x;
-            mu = mean[r];
-            rs = rstd[r];
-        }
-        for (int k = warp; k < nk; k += LNQ_WARPS) {
-            const size_t r = (size_t)blockIdx.x + (size_t)k * gridDim.x;
-            // the next row's statistics, a row ahead
-            float mu2 = 0.f, rs2 = 0.f;
-            if (k + LNQ_WARPS < nk) {
-                const size_t r2 = r + (size_t)LNQ_WARPS * gridDim.x;
-                mu2 = mean[r2];
-                rs2 = rstd[r2];
-            }
+    } else if (warp < CWARPS) {
+        Vec16<bf16> wv;
+        if (has) wv = ld16(w + vi * VEC);
+        int par = 0;
+        bool ok_all = true;
+        for (int k = grp; ok_all && k < nk; k += GROUPS) {
             const int s = k % LNQ_RING;
             int ok = 1;
             if (lane == 0) ok = tc::mbar_wait(full(s), (uint32_t)((k / LNQ_RING) & 1), abort_flag) ? 1 : 0;
-            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            // a failed wait is acted on only after the group's barrier below, so
+            // that all of the group's warps leave together
+            if (NV == 1 && !ok) break;
             const uint8_t* slot = ring + (size_t)s * slotb;
-            Vec16<bf16> xv[NV], dv[NV], ov[NV];
+            const int r0 = r_begin + k * LNQ_SR;
+            const int nrows = min(LNQ_SR, r_end - r0);
+            // two rows at a time: their loads, sums and exchanges overlap
+            for (int i = 0; i < nrows; i += 2, par ^= 1) {
+                const int nr = min(2, nrows - i);
+                float mu[2], rs[2], g[2][VEC], nh[2][VEC];
+                Vec16<bf16> dvv[2], ovv[2];
+                float gs[2] = {0.f, 0.f}, gns[2] = {0.f, 0.f};
+                const bool use = has && ok;
 #pragma unroll
-            for (int j = 0; j < NV; j++) {
-                const int vi = lane + 32 * j;
-                if (vi < cv) {
-                    xv[j] = *reinterpret_cast<const Vec16<bf16>*>(slot + vi * 16);
-                    dv[j] = *reinterpret_cast<const Vec16<bf16>*>(slot + rowb + vi * 16);
-                    if (accumulate) ov[j] = *reinterpret_cast<const Vec16<bf16>*>(slot + 2 * rowb + vi * 16);
+                for (int q = 0; q < 2; q++) {
+                    const size_t r = (size_t)r0 + i + (q < nr ? q : 0);
+                    mu[q] = mean[r];
+                    rs[q] = rstd[r];
+                    const uint8_t* rowp = slot + (size_t)(i + (q < nr ? q : 0)) * rowb;
+                    Vec16<bf16> xv;
+                    if (use) {
+                        xv = *reinterpret_cast<const Vec16<bf16>*>(rowp + vi * 16);
+                        dvv[q] = *reinterpret_cast<const Vec16<bf16>*>(rowp + arrb + vi * 16);
+                        if (accumulate) ovv[q] = *reinterpret_cast<const Vec16<bf16>*>(rowp + 2 * arrb + vi * 16);
+                    }
+#pragma unroll
+                    for (int e = 0; e < VEC; e++) {
+                        g[q][e] = use ? to_f(wv.v[e]) * to_f(dvv[q].v[e]) : 0.f;
+                        nh[q][e] = use ? (to_f(xv.v[e]) - mu[q]) * rs[q] : 0.f;
+                        gs[q] += g[q][e];
+                        gns[q] += g[q][e] * nh[q][e];
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+                    for (int q = 0; q < 2; q++) {
+                        gs[q] += __shfl_xor_sync(0xffffffffu, gs[q], o);
+                        gns[q] += __shfl_xor_sync(0xffffffffu, gns[q], o);
+                    }
+                }
+                if (NV > 1) {
+                    // the group's warps exchange their sums and wait results
+                    // (double-buffered by row-pair parity)
+                    float4* x4 = reinterpret_cast<float4*>(xch) + ((size_t)grp * 2 + par) * NV;
+                    int* o2 = xok + ((size_t)grp * 2 + par) * NV;
+                    if (lane == 0) {
+                        x4[wig] = make_float4(gs[0], gns[0], gs[1], gns[1]);
+                        o2[wig] = ok;
+                    }
+                    asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(NV * 32) : "memory");
+                    gs[0] = gns[0] = gs[1] = gns[1] = 0.f;
+#pragma unroll
+                    for (int j2 = 0; j2 < NV; j2++) {
+                        const float4 t = x4[j2];
+                        ok_all = ok_all && o2[j2] != 0;
+                        gs[0] += t.x;
+                        gns[0] += t.y;
+                        gs[1] += t.z;
+                        gns[1] += t.w;
+                    }
+                    if (!ok_all) break;
+                }
+                if (use) {
+#pragma unroll
+                    for (int q = 0; q < 2; q++) {
+                        if (q >= nr) break;
+                        const float gm = gs[q] / C, gnm = gns[q] / C;
+                        Vec16<bf16> o;
+#pragma unroll
+                        for (int e = 0; e < VEC; e++) {
+                            const float val = rs[q] * (g[q][e] - gm - nh[q][e] * gnm);
+                            const float d = to_f(dvv[q].v[e]);
+                            o.v[e] = from_f<bf16>(accumulate ? to_f(ovv[q].v[e]) + val : val);
+                            adw[e] += nh[q][e] * d;
+                            adb[e] += d;
+                            acs[e] += to_f(o.v[e]);
+                        }
+                        st16(dinp + ((size_t)r0 + i + q) * C + vi * VEC, o);
+                    }
                 }
             }
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(empty(s));  // the slot is in registers
-            float gsum = 0.f, gnsum = 0.f;
-#pragma unroll
-            for (int j = 0; j < NV; j++) {
-                if (lane + 32 * j < cv) {
-#pragma unroll
-                    for (int e = 0; e < VEC; e++) {
-                        const float g = to_f(wv[j].v[e]) * to_f(dv[j].v[e]);
-                        gsum += g;
-                        gnsum += g * (to_f(xv[j].v[e]) - mu) * rs;
-                    }
-                }
-            }
-            gsum = warp_sum(gsum) / C;
-            gnsum = warp_sum(gnsum) / C;
-            bf16* dx = dinp + r * C;
-#pragma unroll
-            for (int j = 0; j < NV; j++) {
-                const int vi = lane + 32 * j;
-                if (vi < cv) {
-                    Vec16<bf16> o;
-#pragma unroll
-                    for (int e = 0; e < VEC; e++) {
-                        const float d = to_f(dv[j].v[e]);
-                        const float nh = (to_f(xv[j].v[e]) - mu) * rs;
-                        const float val = rs * (to_f(wv[j].v[e]) * d - gsum - nh * gnsum);
-                        o.v[e] = from_f<bf16>(accumulate ? to_f(ov[j].v[e]) + val : val);
-                        adw[j][e] += nh * d;
-                        adb[j][e] += d;
-                        acs[j][e] += to_f(o.v[e]);
-                    }
-                    st16(dx + vi * VEC, o);
-                }
-            }
-            mu = mu2;
-            rs = rs2;
+            if (lane == 0 && ok) tc::mbar_arrive(empty(s));  // this warp is done with the slot
         }
     }
     __syncthreads();
     if (*abort_flag) {
         // let every issued copy land before the ring is reused or released
-        if (threadIdx.x == 32 * LNQ_WARPS) {
+        if (threadIdx.x == 32 * producer) {
             const int issued = *issued_s;
             for (int s = 0; s < LNQ_RING && s < issued; s++) {
                 const int lst = s + ((issued - 1 - s) / LNQ_RING) * LNQ_RING;
@@ -723,28 +645,23 @@ __global__ void __launch_bounds__(32 * (LNQ_WARPS + 1)) layernorm_backward_bulk_
         }
         __syncthreads();
     }
-    // fold the consumer warps in order through the (now idle) ring memory
-    float* fold = reinterpret_cast<float*>(lnq_sm);  // [LNQ_WARPS][G*C]
-    if (warp < LNQ_WARPS) {
-        float* mine = fold + (size_t)warp * G * C;
+    // fold the row groups in order through the (now idle) ring memory:
+    // fold[group][dw | db | colsum][column]
+    float* fold = reinterpret_cast<float*>(lnq_sm);
+    if (has) {
+        float* mine = fold + (size_t)grp * G * C;
 #pragma unroll
-        for (int j = 0; j < NV; j++) {
-            const int vi = lane + 32 * j;
-            if (vi < cv) {
-#pragma unroll
-                for (int e = 0; e < VEC; e++) {
-                    mine[vi * VEC + e] = adw[j][e];
-                    mine[C + vi * VEC + e] = adb[j][e];
-                    if (with_colsum) mine[2 * C + vi * VEC + e] = acs[j][e];
-                }
-            }
+        for (int e = 0; e < VEC; e++) {
+            mine[vi * VEC + e] = adw[e];
+            mine[C + vi * VEC + e] = adb[e];
+            if (with_colsum) mine[2 * C + vi * VEC + e] = acs[e];
         }
     }
     __syncthreads();
     float* dst = part + (size_t)blockIdx.x * G * C;
     for (int c = threadIdx.x; c < G * C; c += blockDim.x) {
         float t = 0.f;
-        for (int wi = 0; wi < LNQ_WARPS; wi++) t += fold[(size_t)wi * G * C + c];
+        for (int gi = 0; gi < GROUPS; gi++) t += fold[(size_t)gi * G * C + c];
         dst[c] = t;
     }
 }
@@ -812,63 +729,21 @@ static int lnb_blocks(int N, size_t smem) {
     return g < cap ? (g < 1 ? 1 : g) : cap;
 }
 
-template <int NV> static void lnr_opt_in(size_t smem) {
-    static size_t done = 0;
-    if (smem > done) {
-        cudaFuncSetAttribute(layernorm_backward_reg_k<NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-        done = smem;
-    }
-}
-
 size_t layernorm_backward_ws_floats(int C) { return (size_t)4 * num_sms() * 2 * C; }
 
 void launch_layernorm_backward(DType dt, void* dinp, void* dw, void* db, const void* dout,
                                const void* inp, const void* w, const float* mean,
                                const float* rstd, int N, int C, int accumulate, float* ws,
-                               cudaStream_t s) {
-    note_launch(2);
-    const int VEC = dt == DT_BF16 ? 8 : 4;
-    const int nv = (C / VEC + 31) / 32;  // 16-byte vectors per lane (C <= 256*VEC checked at init)
-    const size_t smem = sizeof(float) * 2 * C * (LNB_BLOCK / 32);
-    int P = 1;
-#define LNB(TT, NVV)                                                                          \
-    P = lnb_blocks<TT, NVV>(N, smem);                                                         \
-    launch_pdl(layernorm_backward_k<TT, NVV>, P, LNB_BLOCK, smem, s, (TT*)dinp, ws, (const TT*)dout,  \
-                                                             (const TT*)inp, (const TT*)w,     \
-                                                             mean, rstd, N, C, accumulate)
-#define LNB_ALL(TT)                                                                           \
-    switch (nv) {                                                                             \
-        case 1: LNB(TT, 1); break; case 2: LNB(TT, 2); break; case 3: LNB(TT, 3); break;       \
-        case 4: LNB(TT, 4); break; case 5: LNB(TT, 5); break; case 6: LNB(TT, 6); break;       \
-        case 7: LNB(TT, 7); break; default: LNB(TT, 8); break;                                \
-    }
+                               unsigned int* err, cudaStream_t s) {
+    // partial rows [P][dw | db], then their in-order sum into dw and db
+    const int P = launch_layernorm_backward_part(dt, dinp, ws, dout, inp, w, mean, rstd, N, C,
+                                                 accumulate, 0, err, s);
+    note_launch(1);
     const unsigned rg = (unsigned)((2 * C + 31) / 32);
-    if (dt == DT_BF16 && nv <= 3) {
-        // one block per SM: its 8 warps keep two rows of loads in flight each
-        const int rows_per_block = LNB_BLOCK / 32;
-        P = (N + rows_per_block - 1) / rows_per_block;
-        if (P > num_sms()) P = num_sms();
-        if (P < 1) P = 1;
-#define LNR(NVV)                                                                                    \
-    lnr_opt_in<NVV>(smem);                                                                           \
-    launch_pdl(layernorm_backward_reg_k<NVV>, P, LNB_BLOCK, smem, s, (bf16*)dinp, ws, (const bf16*)dout,     \
-                                                          (const bf16*)inp, (const bf16*)w, mean,   \
-                                                          rstd, N, C, accumulate)
-        switch (nv) {
-            case 1: LNR(1); break; case 2: LNR(2); break; default: LNR(3); break;
-        }
-#undef LNR
+    if (dt == DT_BF16)
         launch_pdl(reduce_partials_k<bf16>, rg, 256, 0, s, (bf16*)dw, (bf16*)db, C, ws, P, 2 * C);
-    } else if (dt == DT_BF16) {
-        LNB_ALL(bf16);
-        launch_pdl(reduce_partials_k<bf16>, rg, 256, 0, s, (bf16*)dw, (bf16*)db, C, ws, P, 2 * C);
-    } else {
-        LNB_ALL(float);
+    else
         launch_pdl(reduce_partials_k<float>, rg, 256, 0, s, (float*)dw, (float*)db, C, ws, P, 2 * C);
-    }
-#undef LNB_ALL
-#undef LNB
 }
 
 // ------------------------------------------------------------------ partial-row form
@@ -896,7 +771,7 @@ int layernorm_backward_part_rows(DType dt, int N, int C) {
 }
 
 template <int NV> static size_t lnq_opt_in(int C) {
-    const size_t smem = (size_t)LNQ_RING * 3 * C * 2 + 16 * LNQ_RING + 16;
+    const size_t smem = lnq_body_bytes(C, (LNQ_THREADS / 32 - 1) / NV) + 16 * LNQ_RING + 16 + LNQ_XCH * 20;
     static size_t done = 0;
     if (smem > done) {
         cudaFuncSetAttribute(layernorm_backward_bulk_k<NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -915,7 +790,7 @@ int launch_layernorm_backward_part(DType dt, void* dinp, float* part, const void
         const int nv = (C / 8 + 31) / 32;
         note_launch(1);
 #define LNQ(NVV)                                                                                 \
-    launch_pdl(layernorm_backward_bulk_k<NVV>, dim3(P), dim3(32 * (LNQ_WARPS + 1)),               \
+    launch_pdl(layernorm_backward_bulk_k<NVV>, dim3(P), dim3(LNQ_THREADS),                       \
                lnq_opt_in<NVV>(C), s, (bf16*)dinp, part, (const bf16*)dout, (const bf16*)inp,     \
                (const bf16*)w, mean, rstd, N, C, accumulate, with_colsum, err)
         if (nv == 1) LNQ(1);
@@ -1050,7 +925,16 @@ void launch_colsum_accum(DType dt, void* dbias, const void* dout, int M, int N, 
 // by dlogits = (p - 1[i == target]) * dloss; the padded columns [V, Vp) get 0.
 // Pass 1 reads the row once (online max/sum per 16-byte vector); pass 2
 // re-reads it (an L2 hit: each block's row is only ~100 KB) and writes.
+// exp(x - m) is taken as 2^(x log2(e) - m log2(e)): one FMA and the hardware
+// ex2 per element (relative error ~2^-22).
 constexpr int CLS_BLOCK = 512;
+constexpr float CLS_LOG2E = 1.4426950408889634f;
+
+DEVI float cls_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 template <typename T>
 __global__ void __launch_bounds__(CLS_BLOCK) classifier_k(T* __restrict__ logits,
@@ -1077,11 +961,11 @@ __global__ void __launch_bounds__(CLS_BLOCK) classifier_k(T* __restrict__ logits
             lm = fmaxf(lm, f[k]);
         }
         if (lm == -INFINITY) continue;
-        float nm = fmaxf(m, lm);
+        const float nm = fmaxf(m, lm), nl = -nm * CLS_LOG2E;
         float acc = 0.f;
 #pragma unroll
-        for (int k = 0; k < VEC; k++) acc += expf(f[k] - nm);
-        sum = sum * expf(m - nm) + acc;
+        for (int k = 0; k < VEC; k++) acc += cls_exp2(fmaf(f[k], CLS_LOG2E, nl));
+        sum = sum * cls_exp2((m - nm) * CLS_LOG2E) + acc;
         m = nm;
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x / 32, nw = blockDim.x / 32;
@@ -1089,12 +973,12 @@ __global__ void __launch_bounds__(CLS_BLOCK) classifier_k(T* __restrict__ logits
     if (lane == 0) s_max[warp] = wm;
     __syncthreads();
     float bm = warp_max(lane < nw ? s_max[lane] : -INFINITY);
-    float ws = warp_sum(m == -INFINITY ? 0.f : sum * expf(m - bm));
+    float ws = warp_sum(m == -INFINITY ? 0.f : sum * cls_exp2((m - bm) * CLS_LOG2E));
     if (lane == 0) s_sum[warp] = ws;
     __syncthreads();
     const float bs = warp_sum(lane < nw ? s_sum[lane] : 0.f);
     if (threadIdx.x == 0) losses[row] = logf(bs) + bm - s_tlogit;
-    const float inv = 1.f / bs;
+    const float inv = 1.f / bs, bl = -bm * CLS_LOG2E;
     for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
         Vec16<T> a = ld16(x + (size_t)vi * VEC), o;
 #pragma unroll
@@ -1102,7 +986,7 @@ __global__ void __launch_bounds__(CLS_BLOCK) classifier_k(T* __restrict__ logits
             int i = vi * VEC + k;
             float d = 0.f;
             if (i < V) {
-                float p = expf(to_f(a.v[k]) - bm) * inv;
+                float p = cls_exp2(fmaf(to_f(a.v[k]), CLS_LOG2E, bl)) * inv;
                 d = (p - (i == tgt ? 1.f : 0.f)) * dloss;
             }
             o.v[k] = from_f<T>(d);

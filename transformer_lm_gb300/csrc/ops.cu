@@ -194,8 +194,12 @@ int gpt2_layernorm_backward(int dtype, void* dinp, void* dw, void* db, const voi
     if (!dinp || !dw || !db || !dout || !inp || !w || !mean || !rstd || !scratch) return GPT2_ERR_ARG;
     if (dtype != GPT2_FP32 && dtype != GPT2_BF16) return GPT2_ERR_CONFIG;
     if (N < 1 || C < 8 || C % 8 || C > (dtype == GPT2_BF16 ? 2048 : 1024)) return GPT2_ERR_ARG;
+    int dev;
+    if (current_device(&dev) != GPT2_OK) return GPT2_ERR_CUDA;
+    unsigned int* err = err_word(dev);
+    if (!err) return GPT2_ERR_NOMEM;
     launch_layernorm_backward(dtype == GPT2_BF16 ? DT_BF16 : DT_F32, dinp, dw, db, dout, inp, w, mean,
-                              rstd, N, C, accumulate, scratch, (cudaStream_t)stream);
+                              rstd, N, C, accumulate, scratch, err, (cudaStream_t)stream);
     return launch_status();
 }
 

@@ -137,13 +137,19 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def dist_setup():
+def dist_setup(backend: str | None = None):
+    """One process per GPU (torchrun's RANK / LOCAL_RANK / WORLD_SIZE). The
+    replicas exchange nothing on the data path: the process group only carries
+    the barriers and the max-over-ranks of the timings (NCCL on GPUs, gloo
+    when there is no GPU)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
+        import torch
         import torch.distributed as dist
-        backend = "nccl"
+        if backend is None:
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
         dist.init_process_group(backend=backend)
     return world, rank, local
 
@@ -159,9 +165,15 @@ def max_over_ranks(x: float, world: int) -> float:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, seconds: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank / seconds
 
 
 # --------------------------------------------------------------------------- CPU oracle arm
@@ -331,8 +343,8 @@ def run_ours(args):
     G.gpt2_sync()
 
     tokens_all = world * ACCUM * B * T * args.steps
-    value = tokens_all / (ms / 1000.0)
-    e2e_value = tokens_all / e2e_s
+    value = job_throughput(ACCUM * B * T * args.steps, world, ms / 1000.0)
+    e2e_value = job_throughput(ACCUM * B * T * args.steps, world, e2e_s)
     step_flops = model_flops_per_token() * ACCUM * B * T
 
     fam = {}

@@ -195,6 +195,32 @@ def test_attention_growing_scores_match_oracle(T):
     assert rel_to_max(got[:, :, 0], ref[:, :, 0]) < 1.5e-1
 
 
+@pytest.mark.parametrize("B,T,C,NH", [(10, 1024, 256, 4), (40, 300, 128, 2)])
+def test_attention_forward_many_items_per_cta(B, T, C, NH):
+    """More (b, h, 256-query) work items than SMs, so the persistent forward
+    runs several items per CTA (its Q buffers, K/V ring and TMEM regions are
+    reused across items); T=300 also has items whose second query tile is
+    empty. Output against the oracle, LSE against its definition."""
+    import torch
+    qkv = inputs.round_to_bf16(inputs.normal(40 + T, 1, B * T * 3 * C).astype(np.float32))
+    ref_out = np.concatenate([
+        oracle.attention_forward(qkv.reshape(B, -1)[b], 1, T, C, NH)[0] for b in range(B)])
+    out = empty((B * T * C,), "bf16")
+    lse = torch.zeros(B * NH * T, dtype=torch.float32, device="cuda")
+    G.gpt2_attention_forward(G.GPT2_BF16, 1, dev(qkv, "bf16"), out, lse, B, T, C, NH)
+    G.gpt2_device_status()
+    assert rel_to_max(host(out), ref_out) < 2e-2
+    x = qkv.astype(np.float64).reshape(B, T, 3, NH, C // NH)
+    mask = np.tril(np.ones((T, T), bool))
+    got_lse = host(lse).reshape(B, NH, T)
+    for b in range(B):
+        s = np.einsum("tnd,snd->nts", x[b, :, 0], x[b, :, 1]) / np.sqrt(C // NH)
+        s = np.where(mask[None], s, -np.inf)
+        mx = s.max(-1, keepdims=True)
+        ref_lse = (mx + np.log(np.exp(s - mx).sum(-1, keepdims=True)))[..., 0]
+        np.testing.assert_allclose(got_lse[b], ref_lse, atol=2e-3, rtol=1e-4)
+
+
 def test_fused_op_small_shapes_match_oracle():
     import torch
     for (M, K, N) in [(130, 72, 264), (256, 512, 1000), (1, 4, 4)]:

@@ -5,20 +5,28 @@
 // sqrt(64)) v_j and LSE_i (llm.c "train_gpt2.cu", attention_forward with
 // softmax_forward_kernel5, in flash form: no T x T matrix is stored).
 //
-// One CTA takes 256 consecutive queries of one (b, h) as two 128-row tiles
-// (one TMEM lane = one query row = one thread of its softmax warpgroup):
-//   warp 0       TMA: both Q tiles once, then K and V blocks of 128 keys into
-//                a 2-stage ring (3-D tensor map over (3C, T, B): rows past the
-//                end of a sequence read as zero);
+// Persistent: one CTA per SM. A work item is 256 consecutive queries of one
+// (b, h), taken as two 128-row tiles; items are ordered longest first (the
+// last queries see the most keys) and dealt to the CTAs in snake order, so
+// every CTA gets a similar number of key blocks. Roles (320 threads):
+//   warp 0       TMA: the two Q tiles of each item into a 2-deep buffer, the
+//                K and V blocks of 128 keys into a 4-stage ring (3-D tensor map
+//                over (3C, T, B): rows past the end of a sequence read as 0);
 //   warp 1       one thread issues the MMAs: S_t = Q_t K^T (M=128, N=128,
-//                K=64) into TMEM, then O_t = P_t V (M=128, N=64, K=128; V is
-//                the MN-major operand);
-//   warps 2..9   two softmax warpgroups, one per query tile: each thread reads
-//                its row of S from TMEM, forms exp2(s - m) and writes the bf16 P
-//                row into 128B-swizzled shared memory. O_t accumulates in TMEM
-//                across key blocks; a row's reference max m moves only when a
-//                block's max exceeds it by more than 8 (so p <= 256), and then
-//                the warp rescales its O rows in TMEM between two P.V MMAs.
+//                K=64, both operands in shared memory) and O_t += P_t V
+//                (M=128, N=64, K=128) with P_t read from tensor memory and V
+//                the MN-major operand. S_t for the next key block (or the next
+//                item) is issued as soon as the softmax threads have copied
+//                S_t into registers, so it overlaps their exponentials;
+//   warps 2..9   two softmax warpgroups, one per query tile (one TMEM lane =
+//                one query row = one thread): S row from TMEM, row max,
+//                P = exp2(s - m) written back to TMEM as bf16 pairs, and the
+//                item's epilogue O / l and LSE. A row's reference max m moves
+//                only when a block's max exceeds it by more than 8 (so p <=
+//                256); the warp then rescales its O rows in TMEM after the
+//                previous P.V has completed.
+// TMEM, 512 columns: tile t at t*256 holds S (128 fp32 columns), O (+128, 64
+// columns) and P (+192, 64 columns of bf16 pairs).
 // All waits are bounded; on expiry the CTA records DEVERR_TIMEOUT, drains its
 // copies and MMAs and frees TMEM.
 #include "common.cuh"
@@ -29,6 +37,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 namespace gk {
@@ -37,29 +46,56 @@ using namespace tc;
 
 constexpr int HSZ = 64;
 constexpr int BQ = 128;          // queries per tile
-constexpr int NQT = 2;           // query tiles per CTA
+constexpr int NQT = 2;           // query tiles per item
 constexpr int BKV = 128;         // keys per block
-constexpr int KV_STAGES = 2;
-constexpr int TILE_BYTES = 128 * 128;    // 128 rows x 128 bytes (64 bf16)
-constexpr int P_BYTES = 2 * TILE_BYTES;  // 128 queries x 128 keys, two 64-key atoms
+constexpr int KV_STAGES = 4;
+constexpr int Q_BUFS = 2;
+constexpr int TILE_BYTES = 128 * 128;  // 128 rows x 128 bytes (64 bf16)
 constexpr int NUM_THREADS = 64 + NQT * 128;
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + NQT * TILE_BYTES;
-constexpr int OFF_V = OFF_K + KV_STAGES * TILE_BYTES;
-constexpr int OFF_P = OFF_V + KV_STAGES * TILE_BYTES;
-constexpr int OFF_BAR = OFF_P + NQT * P_BYTES;
+constexpr int OFF_Q = 0;                                   // [buf][tile]
+constexpr int OFF_KV = OFF_Q + Q_BUFS * NQT * TILE_BYTES;  // [stage]: K, then V
+constexpr int OFF_BAR = OFF_KV + KV_STAGES * 2 * TILE_BYTES;
 constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
-constexpr int TMEM_COLS = 512;   // tile t: S at t*192 (128 columns), O at t*192+128 (64)
+constexpr int TMEM_COLS = 512;
+constexpr int TM_TILE = 256;  // columns per query tile
+constexpr int TM_O = 128;
+constexpr int TM_P = 192;
 constexpr float LN2_F = 0.6931471805599453f;
 constexpr float RESCALE_LOG2 = 8.f;  // lazy-rescale threshold (log2 units)
 
 struct FwdArgs {
     bf16* out;
     float* lse;
-    int T, C, NH;
+    int T, C, NH, BH;
+    int nqb, nitems;
     float scale_log2;
     unsigned int* err;
 };
+
+// item u (longest first): its (b, h), first query and key blocks per tile
+struct Item {
+    int bh, q0, n[NQT], nmax;
+};
+DEVI Item decode_item(const FwdArgs& a, int u) {
+    Item it;
+    const int qblk = a.nqb - 1 - u / a.BH;
+    it.bh = u % a.BH;
+    it.q0 = qblk * NQT * BQ;
+    it.nmax = 0;
+#pragma unroll
+    for (int t = 0; t < NQT; t++) {
+        const int qs = it.q0 + t * BQ;
+        // BQ == BKV: tile t sees key blocks 0 .. qs / BKV
+        it.n[t] = qs < a.T ? qs / BKV + 1 : 0;
+        it.nmax = max(it.nmax, it.n[t]);
+    }
+    return it;
+}
+// the r-th item of CTA c among G CTAs (snake order); -1 past the end
+DEVI int item_of(int r, int c, int G, int nitems) {
+    const int u = r * G + ((r & 1) ? G - 1 - c : c);
+    return u < nitems ? u : -1;
+}
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     flash_fwd_tc_k(const __grid_constant__ CUtensorMap tm, const __grid_constant__ FwdArgs a) {
@@ -69,45 +105,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t* base_ptr = smem_raw + (base - raw);
     const uint32_t bars = base + OFF_BAR;
     uint8_t* bars_ptr = base_ptr + OFF_BAR;
-    // barriers
-    const uint32_t qfull = bars;
-    auto kvfull = [&](int s) { return bars + 8u * (1 + s); };
-    auto kvempty = [&](int s) { return bars + 8u * (1 + KV_STAGES + s); };
-    auto sfull = [&](int t) { return bars + 8u * (1 + 2 * KV_STAGES + t); };
-    auto pfull = [&](int t) { return bars + 8u * (3 + 2 * KV_STAGES + t); };
-    auto pempty = [&](int t) { return bars + 8u * (5 + 2 * KV_STAGES + t); };
-    auto ofull = [&](int t) { return bars + 8u * (7 + 2 * KV_STAGES + t); };
-    const uint32_t drain = bars + 8u * (11 + 2 * KV_STAGES);
-    constexpr int NBARS = 12 + 2 * KV_STAGES;
+    auto qfull = [&](int q) { return bars + 8u * q; };
+    auto qempty = [&](int q) { return bars + 8u * (2 + q); };
+    auto kvfull = [&](int s) { return bars + 8u * (4 + s); };
+    auto kvempty = [&](int s) { return bars + 8u * (8 + s); };
+    auto sfull = [&](int t) { return bars + 8u * (12 + t); };
+    auto sfree = [&](int t) { return bars + 8u * (14 + t); };
+    auto pfull = [&](int t) { return bars + 8u * (16 + t); };
+    auto pempty = [&](int t) { return bars + 8u * (18 + t); };
+    auto ofull = [&](int t) { return bars + 8u * (20 + t); };
+    const uint32_t drain = bars + 8u * 22;
+    constexpr int NBARS = 23;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars_ptr + 8 * NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars_ptr + 8 * NBARS + 4);
-    int* n_issued_smem = reinterpret_cast<int*>(bars_ptr + 8 * NBARS + 8);
+    int* q_issued = reinterpret_cast<int*>(bars_ptr + 8 * NBARS + 8);    // [Q_BUFS]
+    int* kv_issued = reinterpret_cast<int*>(bars_ptr + 8 * NBARS + 16);  // [KV_STAGES]
+    static_assert(8 * NBARS + 16 + 4 * KV_STAGES <= 256, "barrier area");
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-    const int T = a.T, C = a.C;
-    const int nqb = (T + NQT * BQ - 1) / (NQT * BQ);
-    const int qblk = nqb - 1 - (int)blockIdx.x;  // the longest rows first
-    const int b = blockIdx.y / a.NH, h = blockIdx.y % a.NH;
-    const int q0 = qblk * NQT * BQ;
-    const int nkb_total = (T + BKV - 1) / BKV;
-    const int last = min((q0 + NQT * BQ - 1) / BKV, nkb_total - 1);
-    const int n = last + 1;  // key blocks this CTA visits
+    const int G = gridDim.x, c = blockIdx.x;
+    const int C = a.C;
 
     if (threadIdx.x == 0) {
-        mbar_init(qfull, 1);
+        for (int q = 0; q < Q_BUFS; q++) {
+            mbar_init(qfull(q), 1);
+            mbar_init(qempty(q), 1);
+            q_issued[q] = 0;
+        }
         for (int s = 0; s < KV_STAGES; s++) {
             mbar_init(kvfull(s), 1);
             mbar_init(kvempty(s), 1);
+            kv_issued[s] = 0;
         }
         for (int t = 0; t < NQT; t++) {
             mbar_init(sfull(t), 1);
-            mbar_init(pfull(t), 128);
+            mbar_init(sfree(t), 4);  // one arrival per warp of the tile's warpgroup
+            mbar_init(pfull(t), 4);
             mbar_init(pempty(t), 1);
             mbar_init(ofull(t), 1);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
-        *n_issued_smem = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -124,81 +162,121 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- TMA producer
-            int issued = 0;
-            mbar_expect_tx(qfull, NQT * TILE_BYTES);
-            for (int t = 0; t < NQT; t++)
-                tma_load_3d(base + OFF_Q + t * TILE_BYTES, &tm, qfull, h * HSZ, q0 + t * BQ, b);
-            for (int i = 0; i < n; i++) {
-                const int st = i % KV_STAGES;
-                if (!mbar_wait(kvempty(st), (uint32_t)(((i / KV_STAGES) & 1) ^ 1), abort_flag)) break;
-                mbar_expect_tx(kvfull(st), 2 * TILE_BYTES);
-                tma_load_3d(base + OFF_K + st * TILE_BYTES, &tm, kvfull(st), C + h * HSZ, i * BKV, b);
-                tma_load_3d(base + OFF_V + st * TILE_BYTES, &tm, kvfull(st), 2 * C + h * HSZ, i * BKV, b);
-                ++issued;
+            // copies issued per Q buffer and ring slot are counted in shared
+            // memory (read when draining after an abort)
+            int kb = 0;
+            bool ok = true;
+            for (int r = 0, u; ok && (u = item_of(r, c, G, a.nitems)) >= 0; r++) {
+                const Item it = decode_item(a, u);
+                const int b = it.bh / a.NH, h = it.bh % a.NH;
+                const int qb = r & 1;
+                if (!mbar_wait(qempty(qb), (uint32_t)(((r >> 1) & 1) ^ 1), abort_flag)) break;
+                mbar_expect_tx(qfull(qb), NQT * TILE_BYTES);
+                for (int t = 0; t < NQT; t++)
+                    tma_load_3d(base + OFF_Q + (qb * NQT + t) * TILE_BYTES, &tm, qfull(qb), h * HSZ,
+                                it.q0 + t * BQ, b);
+                ++q_issued[qb];
+                for (int i = 0; i < it.nmax; i++, kb++) {
+                    const int st = kb % KV_STAGES;
+                    if (!mbar_wait(kvempty(st), (uint32_t)(((kb / KV_STAGES) & 1) ^ 1), abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t kv = base + OFF_KV + st * 2 * TILE_BYTES;
+                    mbar_expect_tx(kvfull(st), 2 * TILE_BYTES);
+                    tma_load_3d(kv, &tm, kvfull(st), C + h * HSZ, i * BKV, b);
+                    tma_load_3d(kv + TILE_BYTES, &tm, kvfull(st), 2 * C + h * HSZ, i * BKV, b);
+                    ++kv_issued[st];
+                }
             }
-            *n_issued_smem = issued;
         }
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer
             const uint32_t idS = idesc<0>(0, 0, BQ, BKV);
             const uint32_t idPV = idesc<0>(0, 1, BQ, HSZ);
-            auto issue_s = [&](int t, int st) {
-                const uint32_t d = tmem_base + (uint32_t)(t * 192);
-#pragma unroll
-                for (int k = 0; k < HSZ / 16; k++)
-                    umma<0, 1>(d, sdesc(base + OFF_Q + t * TILE_BYTES + k * 32, 16, 1024),
-                               sdesc(base + OFF_K + st * TILE_BYTES + k * 32, 16, 1024), idS,
-                               k ? 1u : 0u);
-                umma_commit<1>(sfull(t));
-            };
-            bool ok = mbar_wait(qfull, 0, abort_flag) && mbar_wait(kvfull(0), 0, abort_flag);
-            if (ok) {
+            int ns[NQT] = {0, 0}, npv[NQT] = {0, 0};
+            bool ok = true;
+            // S_t = Q_t K^T for the CTA's r-th item (Q buffer r & 1) against
+            // the key block in ring position kb
+            auto issue_s = [&](int t, int r, int kb) -> bool {
+                if (ns[t] > 0 && !mbar_wait(sfree(t), (uint32_t)((ns[t] - 1) & 1), abort_flag)) return false;
+                if (!mbar_wait(qfull(r & 1), (uint32_t)((r >> 1) & 1), abort_flag)) return false;
+                const int st = kb % KV_STAGES;
+                if (!mbar_wait(kvfull(st), (uint32_t)((kb / KV_STAGES) & 1), abort_flag)) return false;
                 tc_fence_after();
-                for (int t = 0; t < NQT; t++) issue_s(t, 0);
-            }
-            for (int i = 0; ok && i < n; i++) {
-                const int st = i % KV_STAGES;
-                for (int t = 0; t < NQT && ok; t++) {
-                    if (!mbar_wait(pfull(t), (uint32_t)(i & 1), abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t d = tmem_base + (uint32_t)(t * 192 + 128);
-                    const uint32_t pb = base + OFF_P + t * P_BYTES;
+                const uint32_t d = tmem_base + (uint32_t)(t * TM_TILE);
+                const uint32_t q = base + OFF_Q + ((r & 1) * NQT + t) * TILE_BYTES;
+                const uint32_t k = base + OFF_KV + st * 2 * TILE_BYTES;
 #pragma unroll
-                    for (int k = 0; k < BKV / 16; k++)
-                        umma<0, 1>(d, sdesc(pb + (k >> 2) * TILE_BYTES + (k & 3) * 32, 16, 1024),
-                                   sdesc(base + OFF_V + st * TILE_BYTES + k * 2048, 8192, 1024), idPV,
-                                   (i | k) ? 1u : 0u);
-                    umma_commit<1>(pempty(t));
-                    if (i == n - 1) umma_commit<1>(ofull(t));  // O_t is complete
-                    if (i + 1 < n) {
-                        const int st1 = (i + 1) % KV_STAGES;
-                        if (t == 0) {
-                            if (!mbar_wait(kvfull(st1), (uint32_t)(((i + 1) / KV_STAGES) & 1), abort_flag)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
+                for (int kk = 0; kk < HSZ / 16; kk++)
+                    umma<0, 1>(d, sdesc(q + kk * 32, 16, 1024), sdesc(k + kk * 32, 16, 1024), idS,
+                               kk ? 1u : 0u);
+                umma_commit<1>(sfull(t));
+                ++ns[t];
+                return true;
+            };
+            int kb0 = 0;  // ring position of the current item's key block 0
+            int u = item_of(0, c, G, a.nitems);
+            Item it = decode_item(a, u >= 0 ? u : 0);
+            if (u >= 0) {
+#pragma unroll
+                for (int t = 0; t < NQT; t++)
+                    if (ok && it.n[t] > 0) ok = issue_s(t, 0, 0);
+            }
+            for (int r = 0; ok && u >= 0; r++) {
+                const int un = item_of(r + 1, c, G, a.nitems);
+                const Item nx = decode_item(a, un >= 0 ? un : 0);
+                for (int i = 0; ok && i < it.nmax; i++) {
+#pragma unroll
+                    for (int t = 0; t < NQT; t++) {
+                        if (!ok) continue;
+                        if (i + 1 < it.n[t]) {
+                            ok = issue_s(t, r, kb0 + i + 1);
+                        } else if (un >= 0 && nx.n[t] > 0 &&
+                                   i == (it.n[t] > 0 ? it.n[t] - 1 : it.nmax - 1)) {
+                            ok = issue_s(t, r + 1, kb0 + it.nmax);  // block 0 of the next item
                         }
-                        issue_s(t, st1);
                     }
+                    const int st = (kb0 + i) % KV_STAGES;
+                    const uint32_t v = base + OFF_KV + st * 2 * TILE_BYTES + TILE_BYTES;
+#pragma unroll
+                    for (int t = 0; t < NQT; t++) {
+                        if (!ok || i >= it.n[t]) continue;
+                        if (!mbar_wait(pfull(t), (uint32_t)(npv[t] & 1), abort_flag)) {
+                            ok = false;
+                            continue;
+                        }
+                        tc_fence_after();
+                        const uint32_t d = tmem_base + (uint32_t)(t * TM_TILE + TM_O);
+                        const uint32_t p = tmem_base + (uint32_t)(t * TM_TILE + TM_P);
+#pragma unroll
+                        for (int kk = 0; kk < BKV / 16; kk++)
+                            umma_ts(d, p + (uint32_t)(kk * 8), sdesc(v + kk * 2048, 8192, 1024), idPV,
+                                    (i | kk) ? 1u : 0u);
+                        umma_commit<1>(pempty(t));
+                        if (i == it.n[t] - 1) umma_commit<1>(ofull(t));  // O_t of this item is complete
+                        ++npv[t];
+                    }
+                    if (ok) umma_commit<1>(kvempty(st));  // K/V of this slot are no longer read
                 }
-                umma_commit<1>(kvempty(st));  // K/V of this stage are no longer read
+                if (ok) umma_commit<1>(qempty(r & 1));  // every S of this item is issued
+                kb0 += it.nmax;
+                u = un;
+                it = nx;
             }
         }
     } else {
         // ---------------- softmax warpgroups
         const int t = (warp - 2) >> 2;
         const int qq = warp & 3;  // TMEM lane quarter
-        const int r = qq * 32 + lane;
-        const int query = q0 + t * BQ + r;
-        const uint32_t tS = tmem_base + (uint32_t)(t * 192) + ((uint32_t)(qq * 32) << 16);
-        const uint32_t tO = tS + 128;
-        uint8_t* pbuf = base_ptr + OFF_P + t * P_BYTES;
-        float m = -INFINITY, l = 0.f;
+        const int row = qq * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
+        const uint32_t tS = tmem_base + (uint32_t)(t * TM_TILE) + lane_off;
+        const uint32_t tO = tS + TM_O;
+        const uint32_t tP = tS + TM_P;
+        const float sl = a.scale_log2;
+        int g = 0, nout = 0;
         bool ok = true;
         auto wait_warp = [&](uint32_t bar, uint32_t parity) {
             int w = 1;
@@ -206,89 +284,96 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             w = __shfl_sync(0xffffffffu, w, 0);
             return w != 0;
         };
-        for (int i = 0; i < n; i++) {
-            if (!wait_warp(sfull(t), (uint32_t)(i & 1))) { ok = false; break; }
-            tc_fence_after();
-            const int k0 = i * BKV;
-            const bool diag = k0 + BKV - 1 > q0 + t * BQ;  // some key may follow some query
-            float va[64], vb[64];
-            tmem_ld64(tS, va);
-            tmem_ld64(tS + 64, vb);
-            // row maximum of the raw scores (the scale is positive)
-            float mx = -INFINITY;
-            if (!diag) {
+        for (int r = 0, u; ok && (u = item_of(r, c, G, a.nitems)) >= 0; r++) {
+            const Item it = decode_item(a, u);
+            const int n = t == 0 ? it.n[0] : it.n[1];
+            if (n == 0) continue;
+            const int query = it.q0 + t * BQ + row;
+            float m = -INFINITY, l = 0.f;
+            for (int i = 0; i < n; i++, g++) {
+                if (!wait_warp(sfull(t), (uint32_t)(g & 1))) { ok = false; break; }
+                tc_fence_after();
+                float s[128];
+                tmem_ld64(tS, *reinterpret_cast<float(*)[64]>(&s[0]));
+                tmem_ld64(tS + 64, *reinterpret_cast<float(*)[64]>(&s[64]));
+                // S_t may now be overwritten by the next Q K^T
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sfree(t));
+                const int k0 = i * BKV;
+                if (k0 + BKV - 1 > it.q0 + t * BQ) {  // diagonal block: keys after the query are masked
+                    const int lim = query - k0;
 #pragma unroll
-                for (int j = 0; j < 64; j += 2) mx = fmaxf(mx, fmaxf(va[j], va[j + 1]));
-#pragma unroll
-                for (int j = 0; j < 64; j += 2) mx = fmaxf(mx, fmaxf(vb[j], vb[j + 1]));
-            } else {
-                const int lim = query - k0;  // keys k0 + j with j <= lim are visible
-#pragma unroll
-                for (int j = 0; j < 64; j++) mx = fmaxf(mx, j <= lim ? va[j] : -INFINITY);
-#pragma unroll
-                for (int j = 0; j < 64; j++) mx = fmaxf(mx, j + 64 <= lim ? vb[j] : -INFINITY);
-            }
-            mx *= a.scale_log2;
-            // P may be overwritten (and O rescaled) once the previous P.V is done
-            if (!wait_warp(pempty(t), (uint32_t)((i & 1) ^ 1))) { ok = false; break; }
-            if (i == 0) {
-                m = mx;
-            } else if (__any_sync(0xffffffffu, mx > m + RESCALE_LOG2)) {
-                // lazy rescale of this warp's 32 O rows (and row sums)
-                const float m_new = fmaxf(m, mx);
-                const float f = ex2_approx(m - m_new);
-#pragma unroll 1
-                for (int hh = 0; hh < HSZ; hh += 16) {
-                    float ov[16];
-                    tmem_ld16(tO + hh, ov);
-#pragma unroll
-                    for (int j = 0; j < 16; j++) ov[j] *= f;
-                    tmem_st16(tO + hh, ov);
+                    for (int j = 0; j < 128; j++) s[j] = j <= lim ? s[j] : -INFINITY;
                 }
-                l *= f;
-                m = m_new;
-            }
-            const float neg = -m;
-            float lsum = 0.f;
-            auto emit = [&](const float (&vv)[64], int half) {
-                const int lim = diag ? query - (k0 + half * 64) : 64;
-                // 64 keys = one 128-byte row of atom `half`, eight 16-byte chunks
-                uint8_t* atom = pbuf + half * TILE_BYTES + r * 128;
+                float m4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-                for (int u = 0; u < 8; u++) {
-                    uint32_t pk[4];
+                for (int j = 4; j < 124; j += 8) {
+                    m4[0] = fmax3(m4[0], s[j], s[j + 1]);
+                    m4[1] = fmax3(m4[1], s[j + 2], s[j + 3]);
+                    m4[2] = fmax3(m4[2], s[j + 4], s[j + 5]);
+                    m4[3] = fmax3(m4[3], s[j + 6], s[j + 7]);
+                }
+                m4[0] = fmax3(m4[0], s[124], s[125]);
+                m4[1] = fmax3(m4[1], s[126], s[127]);
+                const float mx = fmax3(fmaxf(m4[0], m4[1]), m4[2], m4[3]) * sl;
+                // P_t (and O_t) may be written once the previous P.V is done
+                if (!wait_warp(pempty(t), (uint32_t)((g & 1) ^ 1))) { ok = false; break; }
+                tc_fence_after();
+                if (i == 0) {
+                    m = mx;
+                } else if (__any_sync(0xffffffffu, mx > m + RESCALE_LOG2)) {
+                    // lazy rescale of this warp's 32 O rows (and row sums)
+                    const float m_new = fmaxf(m, mx);
+                    const float f = ex2_approx(m - m_new);
+#pragma unroll 1
+                    for (int hh = 0; hh < HSZ; hh += 16) {
+                        float ov[16];
+                        tmem_ld16(tO + hh, ov);
 #pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        const int j = 8 * u + 2 * e;
-                        float p0 = ex2_approx(fmaf(vv[j], a.scale_log2, neg));
-                        float p1 = ex2_approx(fmaf(vv[j + 1], a.scale_log2, neg));
-                        if (diag) {
-                            p0 = j <= lim ? p0 : 0.f;
-                            p1 = j + 1 <= lim ? p1 : 0.f;
-                        }
-                        lsum += p0 + p1;
-                        __nv_bfloat162 pr = __floats2bfloat162_rn(p0, p1);
+                        for (int j = 0; j < 16; j++) ov[j] *= f;
+                        tmem_st16(tO + hh, ov);
+                    }
+                    l *= f;
+                    m = m_new;
+                }
+                const float2 sc2 = make_float2(sl, sl), nm2 = make_float2(-m, -m);
+                float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+                for (int ch = 0; ch < 4; ch++) {  // 32 keys = 16 columns of bf16 pairs
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; e++) {
+                        const int j = ch * 32 + 2 * e;
+                        float2 x = ffma2(make_float2(s[j], s[j + 1]), sc2, nm2);
+                        x.x = ex2_approx(x.x);
+                        x.y = ex2_approx(x.y);
+                        acc[e & 1] = fadd2(acc[e & 1], x);
+                        __nv_bfloat162 pr = __floats2bfloat162_rn(x.x, x.y);
                         pk[e] = *reinterpret_cast<uint32_t*>(&pr);
                     }
-                    *reinterpret_cast<uint4*>(atom + ((u ^ (r & 7)) << 4)) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    tmem_st16_nowait(tP + ch * 16, pk);
                 }
-            };
-            emit(va, 0);
-            emit(vb, 1);
-            l += lsum;
-            fence_async_smem();
-            tc_fence_before();
-            mbar_arrive(pfull(t));
-        }
-        // the last P.V completes O
-        if (ok && wait_warp(ofull(t), 0u)) {
+                tmem_wait_st();
+                l += (acc[0].x + acc[1].x) + (acc[0].y + acc[1].y);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(pfull(t));
+            }
+            if (!ok) break;
+            // the item's last P.V completes O_t
+            if (!wait_warp(ofull(t), (uint32_t)(nout & 1))) { ok = false; break; }
+            ++nout;
             tc_fence_after();
             float ov[64];
             tmem_ld64(tO, ov);
-            if (query < T) {
+            // O_t is read: the next item's first P.V may overwrite it (it is
+            // issued after this warpgroup's next pfull arrival)
+            tc_fence_before();
+            if (query < a.T) {
+                const int b = it.bh / a.NH, h = it.bh % a.NH;
                 const float inv = 1.f / l;
-                bf16* dst = a.out + ((size_t)b * T + query) * C + (size_t)h * HSZ;
+                bf16* dst = a.out + ((size_t)b * a.T + query) * C + (size_t)h * HSZ;
 #pragma unroll
                 for (int d = 0; d < HSZ; d += 8) {
                     __nv_bfloat162 p0 = __floats2bfloat162_rn(ov[d] * inv, ov[d + 1] * inv);
@@ -299,7 +384,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         make_uint4(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1),
                                    *reinterpret_cast<uint32_t*>(&p2), *reinterpret_cast<uint32_t*>(&p3));
                 }
-                a.lse[(size_t)blockIdx.y * T + query] = (m + log2f(l)) * LN2_F;
+                a.lse[(size_t)it.bh * a.T + query] = (m + log2f(l)) * LN2_F;
             }
         }
     }
@@ -307,14 +392,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     if (*abort_flag) {
         if (threadIdx.x == 0) {
-            mbar_wait_drain(qfull, 0);
-            const int issued = *n_issued_smem;
-            for (int s = 0; s < KV_STAGES; s++) {
-                if (issued > s) {
-                    const int lst = s + ((issued - 1 - s) / KV_STAGES) * KV_STAGES;
-                    mbar_wait_drain(kvfull(s), (uint32_t)((lst / KV_STAGES) & 1));
-                }
-            }
+            // wait for every copy this CTA issued: the last phase of each barrier
+            for (int q = 0; q < Q_BUFS; q++)
+                if (q_issued[q] > 0) mbar_wait_drain(qfull(q), (uint32_t)((q_issued[q] - 1) & 1));
+            for (int s = 0; s < KV_STAGES; s++)
+                if (kv_issued[s] > 0) mbar_wait_drain(kvfull(s), (uint32_t)((kv_issued[s] - 1) & 1));
             atomicOr(a.err, DEVERR_TIMEOUT);
         }
         if (threadIdx.x == 32) {
@@ -377,9 +459,13 @@ int launch_flash_forward_tc(void* out, float* lse, const void* qkv, int B, int T
     a.T = T;
     a.C = C;
     a.NH = NH;
+    a.BH = B * NH;
+    a.nqb = (T + NQT * BQ - 1) / (NQT * BQ);
+    a.nitems = a.nqb * a.BH;
     a.scale_log2 = 1.4426950408889634f / sqrtf((float)HSZ);
     a.err = err;
-    dim3 grid((T + NQT * BQ - 1) / (NQT * BQ), B * NH);
+    if (a.nitems == 0) return GPT2_OK;
+    dim3 grid(std::min(a.nitems, num_sms()));
     note_launch(1);
     launch_pdl(flash_fwd_tc_k, grid, dim3(NUM_THREADS), SMEM_BYTES, s, tm, a);
     return GPT2_OK;

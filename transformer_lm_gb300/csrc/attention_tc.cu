@@ -196,22 +196,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t idS = idesc<0>(0, 0, BQ, BKV);
             const uint32_t idPV = idesc<0>(0, 1, BQ, HSZ);
             int ns[NQT] = {0, 0}, npv[NQT] = {0, 0};
+            // bit s: the current fill of ring slot s (bit 4 + b: of Q buffer b)
+            // has been waited for; cleared when the slot is handed back
+            uint32_t seen = 0;
             bool ok = true;
+            auto wait_once = [&](uint32_t bit, uint32_t bar, uint32_t parity) -> bool {
+                if (seen & bit) return true;
+                if (!mbar_wait(bar, parity, abort_flag)) return false;
+                seen |= bit;
+                return true;
+            };
             // S_t = Q_t K^T for the CTA's r-th item (Q buffer r & 1) against
             // the key block in ring position kb
             auto issue_s = [&](int t, int r, int kb) -> bool {
                 if (ns[t] > 0 && !mbar_wait(sfree(t), (uint32_t)((ns[t] - 1) & 1), abort_flag)) return false;
-                if (!mbar_wait(qfull(r & 1), (uint32_t)((r >> 1) & 1), abort_flag)) return false;
                 const int st = kb % KV_STAGES;
-                if (!mbar_wait(kvfull(st), (uint32_t)((kb / KV_STAGES) & 1), abort_flag)) return false;
+                if (!wait_once(16u << (r & 1), qfull(r & 1), (uint32_t)((r >> 1) & 1))) return false;
+                if (!wait_once(1u << st, kvfull(st), (uint32_t)((kb / KV_STAGES) & 1))) return false;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(t * TM_TILE);
-                const uint32_t q = base + OFF_Q + ((r & 1) * NQT + t) * TILE_BYTES;
-                const uint32_t k = base + OFF_KV + st * 2 * TILE_BYTES;
+                const uint64_t dq = sdesc(base + OFF_Q + ((r & 1) * NQT + t) * TILE_BYTES, 16, 1024);
+                const uint64_t dk = sdesc(base + OFF_KV + st * 2 * TILE_BYTES, 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < HSZ / 16; kk++)
-                    umma<0, 1>(d, sdesc(q + kk * 32, 16, 1024), sdesc(k + kk * 32, 16, 1024), idS,
-                               kk ? 1u : 0u);
+                for (int kk = 0; kk < HSZ / 16; kk++)  // +32 bytes along K per step
+                    umma<0, 1>(d, dq + 2 * kk, dk + 2 * kk, idS, kk ? 1u : 0u);
                 umma_commit<1>(sfull(t));
                 ++ns[t];
                 return true;
@@ -239,7 +247,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                     }
                     const int st = (kb0 + i) % KV_STAGES;
-                    const uint32_t v = base + OFF_KV + st * 2 * TILE_BYTES + TILE_BYTES;
+                    const uint64_t dv = sdesc(base + OFF_KV + st * 2 * TILE_BYTES + TILE_BYTES, 8192, 1024);
 #pragma unroll
                     for (int t = 0; t < NQT; t++) {
                         if (!ok || i >= it.n[t]) continue;
@@ -251,16 +259,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint32_t d = tmem_base + (uint32_t)(t * TM_TILE + TM_O);
                         const uint32_t p = tmem_base + (uint32_t)(t * TM_TILE + TM_P);
 #pragma unroll
-                        for (int kk = 0; kk < BKV / 16; kk++)
-                            umma_ts(d, p + (uint32_t)(kk * 8), sdesc(v + kk * 2048, 8192, 1024), idPV,
-                                    (i | kk) ? 1u : 0u);
+                        for (int kk = 0; kk < BKV / 16; kk++)  // 16 keys = 8 P columns, 2048 bytes of V
+                            umma_ts(d, p + (uint32_t)(kk * 8), dv + 128 * kk, idPV, (i | kk) ? 1u : 0u);
                         umma_commit<1>(pempty(t));
                         if (i == it.n[t] - 1) umma_commit<1>(ofull(t));  // O_t of this item is complete
                         ++npv[t];
                     }
-                    if (ok) umma_commit<1>(kvempty(st));  // K/V of this slot are no longer read
+                    if (ok) {
+                        umma_commit<1>(kvempty(st));  // K/V of this slot are no longer read
+                        seen &= ~(1u << st);
+                    }
                 }
-                if (ok) umma_commit<1>(qempty(r & 1));  // every S of this item is issued
+                if (ok) {
+                    umma_commit<1>(qempty(r & 1));  // every S of this item is issued
+                    seen &= ~(16u << (r & 1));
+                }
                 kb0 += it.nmax;
                 u = un;
                 it = nx;

@@ -38,6 +38,18 @@ DEVI bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// non-blocking test of the phase with the given parity
+DEVI bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // the same test, but the thread may sleep (up to `ns`) until the phase
 // completes instead of returning at once: waiting warps stop taking issue slots
 DEVI bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {

@@ -18,7 +18,7 @@
 //        before its queries with S = Q K^T, dP = dO V^T and dQ += dS K.
 // Roles (576 threads): warp 0 loads the streamed Q/dO (or K/V) blocks into a
 // 3-stage ring by TMA (and, for DKV, the blocks' LSE and D into shared
-// memory); one thread of warp 1 issues the MMAs; warps 2..17 form P and dS,
+// memory); warp 1 issues the MMAs (converged, one elected lane); warps 2..17 form P and dS,
 // four warps per TMEM lane quarter, each on 32 of the 128 columns. S is
 // double-buffered in TMEM, so the next block's S = ... MMA overlaps the
 // current block's softmax. All waits are bounded; on expiry the CTA records
@@ -223,78 +223,79 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             *x_issued_smem = nx;
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer
+        {
+            // ---------------- MMA issuer (the whole warp runs it, one elected lane issues)
             const uint32_t idSq = idesc<0>(0, 0, BLK, BLK);  // S, dP: both operands K-major
             const uint32_t idAcc = idesc<0>(0, 1, BLK, HSZ); // acc += (P|dS) Y: Y is MN-major
             const uint32_t tS0 = tmem_base, tdP = tmem_base + 256;
             const uint32_t tA0 = tmem_base + 384, tA1 = tmem_base + 448;
             auto ybuf = [&](int g, int which) { return base + OFF_Y + (g % STAGES) * 2 * TILE + which * TILE; };
             auto issue_qk = [&](uint32_t d, uint32_t x, uint32_t y) {
+                const uint64_t dx = sdesc(x, 16, 1024), dy = sdesc(y, 16, 1024);
 #pragma unroll
-                for (int k = 0; k < HSZ / 16; k++)
-                    umma<0, 1>(d, sdesc(x + k * 32, 16, 1024), sdesc(y + k * 32, 16, 1024), idSq,
-                               k ? 1u : 0u);
+                for (int k = 0; k < HSZ / 16; k++)  // +32 bytes along K per step
+                    umma_warp<0, 1>(d, dx + 2 * k, dy + 2 * k, idSq, k ? 1u : 0u);
             };
             auto issue_acc = [&](uint32_t d, uint32_t pa, uint32_t y, bool accumulate) {
+                const uint64_t dp = sdesc(pa, 16, 1024), dy = sdesc(y, 8192, 1024);
 #pragma unroll
-                for (int k = 0; k < BLK / 16; k++)
-                    umma<0, 1>(d, sdesc(pa + (k >> 2) * TILE + (k & 3) * 32, 16, 1024),
-                               sdesc(y + k * 2048, 8192, 1024), idAcc, (accumulate || k) ? 1u : 0u);
+                for (int k = 0; k < BLK / 16; k++)  // 16 rows of K: next atom every 4 steps, 2048 bytes of Y
+                    umma_warp<0, 1>(d, dp + (k >> 2) * (TILE >> 4) + (k & 3) * 2, dy + 128 * k, idAcc,
+                                    (accumulate || k) ? 1u : 0u);
             };
             // S of global block g once its ring stage landed and its S buffer was read
             auto issue_s = [&](int g) {
-                if (!mbar_wait(st_full(g % STAGES), (uint32_t)((g / STAGES) & 1), abort_flag) ||
-                    !mbar_wait(s_empty(g & 1), (uint32_t)(((g >> 1) & 1) ^ 1), abort_flag))
+                if (!mbar_wait_warp(st_full(g % STAGES), (uint32_t)((g / STAGES) & 1), abort_flag) ||
+                    !mbar_wait_warp(s_empty(g & 1), (uint32_t)(((g >> 1) & 1) ^ 1), abort_flag))
                     return false;
                 tc_fence_after();
                 issue_qk(tS0 + (uint32_t)((g & 1) * 128), base + OFF_X0, ybuf(g, 0));
-                umma_commit<1>(s_full(g & 1));
+                umma_commit_warp<1>(s_full(g & 1));
                 return true;
             };
             // dP of global block g once the previous dP was read
             auto issue_dp = [&](int g) {
-                if (!mbar_wait(dp_empty, (uint32_t)((g & 1) ^ 1), abort_flag)) return false;
+                if (!mbar_wait_warp(dp_empty, (uint32_t)((g & 1) ^ 1), abort_flag)) return false;
                 tc_fence_after();
                 issue_qk(tdP, base + OFF_X1, ybuf(g, 1));
-                umma_commit<1>(dp_full);
+                umma_commit_warp<1>(dp_full);
                 return true;
             };
             int g0 = 0;
             bool ok = true;
             for (int t = 0, idx = item_of(0); ok && idx < a.items; idx = item_of(++t)) {
                 const int n = decode_item<DKV>(a, idx).n;
-                if (!mbar_wait(x_full, (uint32_t)(t & 1), abort_flag)) break;
+                if (!mbar_wait_warp(x_full, (uint32_t)(t & 1), abort_flag)) break;
                 tc_fence_after();
                 ok = issue_s(g0) && issue_dp(g0);
-                if (ok && n == 1) umma_commit<1>(x_empty);  // the item's last reads of K/V (Q/dO)
+                if (ok && n == 1) umma_commit_warp<1>(x_empty);  // the item's last reads of K/V (Q/dO)
                 if (ok && n > 1) ok = issue_s(g0 + 1);
                 // the previous item's accumulators have been read out
-                if (ok && !mbar_wait(acc_empty, (uint32_t)((t & 1) ^ 1), abort_flag)) ok = false;
+                if (ok && !mbar_wait_warp(acc_empty, (uint32_t)((t & 1) ^ 1), abort_flag)) ok = false;
                 if (ok) tc_fence_after();
                 for (int u = 0; ok && u < n; u++) {
                     const int g = g0 + u;
                     const uint32_t par = (uint32_t)(g & 1);
                     if (DKV) {
-                        if (!mbar_wait(p_full, par, abort_flag)) { ok = false; break; }
+                        if (!mbar_wait_warp(p_full, par, abort_flag)) { ok = false; break; }
                         tc_fence_after();
                         issue_acc(tA0, base + OFF_P, ybuf(g, 1), u > 0);  // dV += P^T dO
-                        umma_commit<1>(p_empty);
+                        umma_commit_warp<1>(p_empty);
                     }
                     if (u + 1 < n) {
                         if (!issue_dp(g + 1)) { ok = false; break; }
-                        if (u + 2 == n) umma_commit<1>(x_empty);  // the item's last reads of X
+                        if (u + 2 == n) umma_commit_warp<1>(x_empty);  // the item's last reads of X
                     }
-                    if (!mbar_wait(ds_full, par, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait_warp(ds_full, par, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     // DKV: dK += dS^T Q; DQ: dQ += dS K
                     issue_acc(DKV ? tA1 : tA0, base + OFF_DS, ybuf(g, 0), u > 0);
-                    umma_commit<1>(ds_empty);
-                    umma_commit<1>(st_empty(g % STAGES));
+                    umma_commit_warp<1>(ds_empty);
+                    umma_commit_warp<1>(st_empty(g % STAGES));
                     if (u + 2 < n && !issue_s(g + 2)) { ok = false; break; }
                 }
                 if (!ok) break;
-                umma_commit<1>(acc_full);
+                umma_commit_warp<1>(acc_full);
                 g0 += n;
             }
         }
@@ -457,9 +458,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             atomicOr(a.err, DEVERR_TIMEOUT);
         }
-        if (threadIdx.x == 32) {
-            umma_commit_local<1>(drain);
-            mbar_wait_drain(drain, 0);
+        if (warp == 1) {  // the issuing lane commits (elected as when issuing)
+            umma_commit_local_warp<1>(drain);
+            if (lane == 0) mbar_wait_drain(drain, 0);
+            __syncwarp();
         }
         __syncthreads();
     }

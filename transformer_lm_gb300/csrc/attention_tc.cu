@@ -12,7 +12,8 @@
 //   warp 0       TMA: the two Q tiles of each item into a 2-deep buffer, the
 //                K and V blocks of 128 keys into a 4-stage ring (3-D tensor map
 //                over (3C, T, B): rows past the end of a sequence read as 0);
-//   warp 1       one thread issues the MMAs: S_t = Q_t K^T (M=128, N=128,
+//   warp 1       issues the MMAs (the whole warp runs the loop, one elected
+//                lane issues): S_t = Q_t K^T (M=128, N=128,
 //                K=64, both operands in shared memory) and O_t += P_t V
 //                (M=128, N=64, K=128) with P_t read from tensor memory and V
 //                the MN-major operand. S_t for the next key block (or the next
@@ -191,8 +192,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer
+        {
+            // ---------------- MMA issuer (the whole warp runs it, one elected lane issues)
             const uint32_t idS = idesc<0>(0, 0, BQ, BKV);
             const uint32_t idPV = idesc<0>(0, 1, BQ, HSZ);
             int ns[NQT] = {0, 0}, npv[NQT] = {0, 0};
@@ -202,14 +203,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             auto wait_once = [&](uint32_t bit, uint32_t bar, uint32_t parity) -> bool {
                 if (seen & bit) return true;
-                if (!mbar_wait(bar, parity, abort_flag)) return false;
+                if (!mbar_wait_warp(bar, parity, abort_flag)) return false;
                 seen |= bit;
                 return true;
             };
             // S_t = Q_t K^T for the CTA's r-th item (Q buffer r & 1) against
             // the key block in ring position kb
             auto issue_s = [&](int t, int r, int kb) -> bool {
-                if (ns[t] > 0 && !mbar_wait(sfree(t), (uint32_t)((ns[t] - 1) & 1), abort_flag)) return false;
+                if (ns[t] > 0 && !mbar_wait_warp(sfree(t), (uint32_t)((ns[t] - 1) & 1), abort_flag)) return false;
                 const int st = kb % KV_STAGES;
                 if (!wait_once(16u << (r & 1), qfull(r & 1), (uint32_t)((r >> 1) & 1))) return false;
                 if (!wait_once(1u << st, kvfull(st), (uint32_t)((kb / KV_STAGES) & 1))) return false;
@@ -219,8 +220,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint64_t dk = sdesc(base + OFF_KV + st * 2 * TILE_BYTES, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < HSZ / 16; kk++)  // +32 bytes along K per step
-                    umma<0, 1>(d, dq + 2 * kk, dk + 2 * kk, idS, kk ? 1u : 0u);
-                umma_commit<1>(sfull(t));
+                    umma_warp<0, 1>(d, dq + 2 * kk, dk + 2 * kk, idS, kk ? 1u : 0u);
+                umma_commit_warp<1>(sfull(t));
                 ++ns[t];
                 return true;
             };
@@ -251,7 +252,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int t = 0; t < NQT; t++) {
                         if (!ok || i >= it.n[t]) continue;
-                        if (!mbar_wait(pfull(t), (uint32_t)(npv[t] & 1), abort_flag)) {
+                        if (!mbar_wait_warp(pfull(t), (uint32_t)(npv[t] & 1), abort_flag)) {
                             ok = false;
                             continue;
                         }
@@ -260,18 +261,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint32_t p = tmem_base + (uint32_t)(t * TM_TILE + TM_P);
 #pragma unroll
                         for (int kk = 0; kk < BKV / 16; kk++)  // 16 keys = 8 P columns, 2048 bytes of V
-                            umma_ts(d, p + (uint32_t)(kk * 8), dv + 128 * kk, idPV, (i | kk) ? 1u : 0u);
-                        umma_commit<1>(pempty(t));
-                        if (i == it.n[t] - 1) umma_commit<1>(ofull(t));  // O_t of this item is complete
+                            umma_ts_warp(d, p + (uint32_t)(kk * 8), dv + 128 * kk, idPV, (i | kk) ? 1u : 0u);
+                        umma_commit_warp<1>(pempty(t));
+                        if (i == it.n[t] - 1) umma_commit_warp<1>(ofull(t));  // O_t of this item is complete
                         ++npv[t];
                     }
                     if (ok) {
-                        umma_commit<1>(kvempty(st));  // K/V of this slot are no longer read
+                        umma_commit_warp<1>(kvempty(st));  // K/V of this slot are no longer read
                         seen &= ~(1u << st);
                     }
                 }
                 if (ok) {
-                    umma_commit<1>(qempty(r & 1));  // every S of this item is issued
+                    umma_commit_warp<1>(qempty(r & 1));  // every S of this item is issued
                     seen &= ~(16u << (r & 1));
                 }
                 kb0 += it.nmax;
@@ -412,9 +413,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (kv_issued[s] > 0) mbar_wait_drain(kvfull(s), (uint32_t)((kv_issued[s] - 1) & 1));
             atomicOr(a.err, DEVERR_TIMEOUT);
         }
-        if (threadIdx.x == 32) {
-            umma_commit_local<1>(drain);
-            mbar_wait_drain(drain, 0);
+        if (warp == 1) {  // the issuing lane commits (elected as when issuing)
+            umma_commit_local_warp<1>(drain);
+            if (lane == 0) mbar_wait_drain(drain, 0);
+            __syncwarp();
         }
         __syncthreads();
     }

@@ -314,20 +314,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             *n_issued_smem = n_issued;
         }
     } else if (warp == 1) {
-        if (lane == 0 && rank == 0) {
-            // ---------------- MMA issuer (the pair leader)
+        if (rank == 0) {
+            // ---------------- MMA issuer (the pair leader): the whole warp runs
+            // the loop, one elected lane issues
             const uint32_t id = idesc<KIND>(args.a_mn, args.b_mn, BM * CG, BN);
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             for (int st = cid; st < num_units; st += ncl) {
-                if (!mbar_wait(tempty(acc), acc_phase ^ 1u, abort_flag)) break;
+                if (!mbar_wait_warp(tempty(acc), acc_phase ^ 1u, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(acc * BN);
                 const int kb0 = (st / num_super) * args.kb_per;
                 const int kb1 = min(args.num_kb, kb0 + args.kb_per);
                 bool ok = true;
                 for (int kb = kb0; kb < kb1; kb++) {
-                    if (!mbar_wait(full(stage), phase, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait_warp(full(stage), phase, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t sa = base + stage * C::STAGE_BYTES;
                     const uint32_t sb = sa + C::A_BYTES;
@@ -339,13 +340,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint64_t db = args.b_mn
                                                 ? sdesc(sb + k * UK * ROWB, KE * ROWB, 1024)
                                                 : sdesc(sb + k * UK * (int)sizeof(T), 16, 1024);
-                        umma<KIND, CG>(d, da, db, id, (kb > kb0 || k) ? 1u : 0u);
+                        umma_warp<KIND, CG>(d, da, db, id, (kb > kb0 || k) ? 1u : 0u);
                     }
-                    umma_commit<CG>(empty(stage));  // frees the stage in every CTA of the pair
+                    umma_commit_warp<CG>(empty(stage));  // frees the stage in every CTA of the pair
                     if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                umma_commit<CG>(tfull(acc));
+                umma_commit_warp<CG>(tfull(acc));
                 if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             }
         }
@@ -461,9 +462,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             atomicOr(args.err, DEVERR_TIMEOUT);
         }
-        if (threadIdx.x == 32 && rank == 0) {
-            umma_commit_local<CG>(drain);
-            mbar_wait_drain(drain, 0);
+        if (warp == 1 && rank == 0) {  // the issuing lane commits (elected as when issuing)
+            umma_commit_local_warp<CG>(drain);
+            if (lane == 0) mbar_wait_drain(drain, 0);
+            __syncwarp();
         }
         __syncthreads();
     }

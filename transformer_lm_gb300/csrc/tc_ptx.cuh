@@ -221,6 +221,68 @@ DEVI void umma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, 
 }
 #undef UMMA_ASM
 
+// Warp-wide forms: the whole (converged) warp executes them and one lane,
+// chosen by elect.sync, issues the instruction. Issuing from a converged warp
+// keeps the operands in uniform registers; a lone lane of a diverged warp
+// issues markedly slower while the other warps of its SMSP are busy. The
+// elected lane is the same on every call, so its commits track the MMAs it
+// issued.
+#define UMMA_WARP_ASM(GROUP, KINDS)                                                        \
+    asm volatile("{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\t"                    \
+                 "elect.sync _|e, 0xffffffff;\n\t"                                        \
+                 "@e tcgen05.mma.cta_group::" GROUP ".kind::" KINDS " [%0], %1, %2, %3, p;\n\t}\n" ::"r"( \
+                     d_tmem),                                                             \
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)                             \
+                 : "memory")
+template <int KIND, int CG>
+DEVI void umma_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+    if constexpr (KIND == 0 && CG == 1) UMMA_WARP_ASM("1", "f16");
+    else if constexpr (KIND == 0) UMMA_WARP_ASM("2", "f16");
+    else if constexpr (CG == 1) UMMA_WARP_ASM("1", "tf32");
+    else UMMA_WARP_ASM("2", "tf32");
+}
+#undef UMMA_WARP_ASM
+DEVI void umma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+    asm volatile("{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(acc)
+                 : "memory");
+}
+template <int CG> DEVI void umma_commit_warp(uint32_t bar) {
+    if constexpr (CG == 1)
+        asm volatile(
+            "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+            "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(bar)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+            "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+            " [%0], %1;\n\t}\n" ::"r"(bar),
+            "h"((uint16_t)3)
+            : "memory");
+}
+template <int CG> DEVI void umma_commit_local_warp(uint32_t bar) {
+    if constexpr (CG == 1)
+        asm volatile(
+            "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+            "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(bar)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+            "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(bar)
+            : "memory");
+}
+// bounded wait taken by every lane of a converged warp (each lane reads the
+// same phase and the same clock, so the lanes leave the loop together; the
+// vote makes the result warp-uniform regardless)
+DEVI bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    const bool w = mbar_wait(bar, parity, abort_flag);
+    return __all_sync(0xffffffffu, w);
+}
+
 // kind::f16 (bf16) MMA with the A operand in tensor memory: M rows in lanes,
 // K packed two elements per 32-bit column starting at a_tmem; B from shared
 // memory through its descriptor

@@ -11,18 +11,23 @@
 // written with "=" into dqkv (B, T, 3C).
 //
 // Two kernels, neither with float atomics, so every run is bit-identical:
-//   DKV  one CTA per (128-key tile, b, h); it walks the query blocks at and
-//        after its keys, with S^T = K Q^T and dP^T = V dO^T in TMEM and
+//   DKV  one work item per (128-key tile, b, h); it walks the query blocks at
+//        and after its keys, with S^T = K Q^T and dP^T = V dO^T in TMEM and
 //        dV += P^T dO, dK += dS^T Q accumulating in TMEM;
-//   DQ   one CTA per (128-query tile, b, h); it walks the key blocks at and
-//        before its queries with S = Q K^T, dP = dO V^T and dQ += dS K.
-// Roles (576 threads): warp 0 loads the streamed Q/dO (or K/V) blocks into a
-// 3-stage ring by TMA (and, for DKV, the blocks' LSE and D into shared
-// memory); warp 1 issues the MMAs (converged, one elected lane); warps 2..17 form P and dS,
-// four warps per TMEM lane quarter, each on 32 of the 128 columns. S is
-// double-buffered in TMEM, so the next block's S = ... MMA overlaps the
-// current block's softmax. All waits are bounded; on expiry the CTA records
-// DEVERR_TIMEOUT, drains its copies and MMAs and frees TMEM.
+//   DQ   one work item per (128-query tile, b, h); it walks the key blocks at
+//        and before its queries with S = Q K^T, dP = dO V^T and dQ += dS K.
+// Roles (608 threads): warp 0 loads by TMA the item's fixed tiles (K, V or Q,
+// dO; double-buffered, so the next item's arrive during this one) and the
+// streamed Q/dO (or K/V) blocks into a 4-stage ring (and, for DKV, the blocks'
+// LSE and D into shared memory); warp 18 issues the S and dP MMAs and warp 1
+// the accumulating ones (each loop runs as a whole warp, one elected lane
+// issues), so neither chain waits behind the other; warps 2..17 form P and
+// dS, four warps per TMEM lane quarter, each on 32 of the 128 columns, and
+// write them as bf16 pairs into TMEM, where the accumulating MMAs read them as
+// their A operand. The next block's S (and dP) MMA is issued as soon as the
+// current one has been read, so it overlaps the current block's softmax. All
+// waits are bounded; on expiry the CTA records DEVERR_TIMEOUT, drains its
+// copies and MMAs and frees TMEM.
 #include "common.cuh"
 #include "internal.h"
 #include "tc_ptx.cuh"
@@ -39,21 +44,22 @@ using namespace tc;
 
 constexpr int HSZ = 64;
 constexpr int BLK = 128;                   // rows per work item and columns per block
-constexpr int STAGES = 3;
+constexpr int STAGES = 4;
 constexpr int TILE = 128 * 128;            // 128 rows x 64 bf16, 128B-swizzled
-constexpr int OFF_X0 = 0;                  // fixed tiles of the current item: K, V (DKV) or Q, dO (DQ)
-constexpr int OFF_X1 = TILE;
-constexpr int OFF_Y = 2 * TILE;            // ring: stage s holds Y0 at +2s*TILE, Y1 at +(2s+1)*TILE
-constexpr int OFF_P = OFF_Y + STAGES * 2 * TILE;  // P^T (DKV), two 64-column atoms
-constexpr int OFF_DS = OFF_P + 2 * TILE;          // dS^T (DKV) or dS (DQ)
-constexpr int OFF_VEC = OFF_DS + 2 * TILE;        // per stage: -LSE*log2(e) [128], D [128]
+constexpr int OFF_X = 0;                   // [buffer][2]: K, V (DKV) or Q, dO (DQ) of an item
+constexpr int OFF_Y = 4 * TILE;            // ring: stage s holds Y0 at +2s*TILE, Y1 at +(2s+1)*TILE
+constexpr int OFF_VEC = OFF_Y + STAGES * 2 * TILE;  // per stage: -LSE*log2(e) [128], D [128]
 constexpr int OFF_BAR = OFF_VEC + STAGES * 1024;
-constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;
+constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
 constexpr int CW = 16;                     // compute warps (P and dS)
 constexpr int CQ = CW / 4;                 // compute warps per TMEM lane quarter
 constexpr int COLS = 128 / CQ;             // columns per compute thread
-constexpr int NUM_THREADS = 64 + 32 * CW;
-constexpr int TMEM_COLS = 512;  // S0 0, S1 128, dP 256, acc0 384 (dV / dQ), acc1 448 (dK)
+constexpr int QKW = 2 + CW;                // the warp that issues S and dP
+constexpr int NUM_THREADS = 64 + 32 * CW + 32;
+// TMEM columns: S, P (bf16 pairs, DKV), dS (bf16 pairs), dP, and the
+// accumulators (dV | dK for DKV, dQ for DQ)
+constexpr int TMEM_COLS = 512;
+constexpr uint32_t TM_S = 0, TM_P = 128, TM_DS = 192, TM_DP = 256, TM_A0 = 384, TM_A1 = 448;
 constexpr float LOG2E = 1.4426950408889634f;
 
 struct BwdArgs {
@@ -83,9 +89,9 @@ template <bool DKV> DEVI Item decode_item(const BwdArgs& a, int idx) {
 }
 
 // Persistent: each CTA takes one item per round (a snake over the CTAs);
-// the ring, the S/dP buffers and every barrier phase run on counters global
-// to the CTA, so the next item's loads and first MMAs overlap this item's
-// last blocks and its epilogue.
+// the ring and every barrier phase run on counters global to the CTA, so the
+// next item's loads and first MMAs overlap this item's last blocks and its
+// epilogue.
 template <bool DKV>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     flash_bwd_tc_k(const __grid_constant__ CUtensorMap tqkv, const __grid_constant__ CUtensorMap tdo,
@@ -96,35 +102,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t* base_ptr = smem_raw + (base - raw);
     const uint32_t bars = base + OFF_BAR;
     uint8_t* bars_ptr = base_ptr + OFF_BAR;
-    const uint32_t x_full = bars, x_empty = bars + 8u;
-    auto st_full = [&](int s) { return bars + 8u * (2 + s); };
-    auto st_empty = [&](int s) { return bars + 8u * (5 + s); };
-    auto s_full = [&](int b) { return bars + 8u * (8 + b); };
-    auto s_empty = [&](int b) { return bars + 8u * (10 + b); };
-    const uint32_t dp_full = bars + 8u * 12, dp_empty = bars + 8u * 13;
-    const uint32_t p_full = bars + 8u * 14, p_empty = bars + 8u * 15;
-    const uint32_t ds_full = bars + 8u * 16, ds_empty = bars + 8u * 17;
-    const uint32_t acc_full = bars + 8u * 18, acc_empty = bars + 8u * 19, drain = bars + 8u * 20;
-    constexpr int NBARS = 21;
+    auto x_full = [&](int b) { return bars + 8u * b; };
+    auto x_empty = [&](int b) { return bars + 8u * (2 + b); };
+    auto st_full = [&](int s) { return bars + 8u * (4 + s); };
+    auto st_empty = [&](int s) { return bars + 8u * (4 + STAGES + s); };
+    constexpr int B0 = 4 + 2 * STAGES;
+    const uint32_t s_full = bars + 8u * B0, s_empty = bars + 8u * (B0 + 1);
+    const uint32_t dp_full = bars + 8u * (B0 + 2), dp_empty = bars + 8u * (B0 + 3);
+    const uint32_t p_full = bars + 8u * (B0 + 4), p_empty = bars + 8u * (B0 + 5);
+    const uint32_t ds_full = bars + 8u * (B0 + 6), ds_empty = bars + 8u * (B0 + 7);
+    const uint32_t acc_full = bars + 8u * (B0 + 8), acc_empty = bars + 8u * (B0 + 9);
+    const uint32_t drain = bars + 8u * (B0 + 10);
+    constexpr int NBARS = B0 + 11;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars_ptr + 8 * NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars_ptr + 8 * NBARS + 4);
     int* n_issued_smem = reinterpret_cast<int*>(bars_ptr + 8 * NBARS + 8);   // ring loads issued
-    int* x_issued_smem = reinterpret_cast<int*>(bars_ptr + 8 * NBARS + 12);  // fixed-tile loads issued
+    int* x_issued_smem = reinterpret_cast<int*>(bars_ptr + 8 * NBARS + 12);  // fixed-tile loads issued [2]
+    static_assert(8 * NBARS + 20 <= 256, "barrier area");
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const int T = a.T, C = a.C;
 
     if (threadIdx.x == 0) {
-        mbar_init(x_full, 1);
-        mbar_init(x_empty, 1);
+        for (int b = 0; b < 2; b++) {
+            mbar_init(x_full(b), 1);
+            mbar_init(x_empty(b), 1);
+        }
         for (int s = 0; s < STAGES; s++) {
             mbar_init(st_full(s), 1);
-            mbar_init(st_empty(s), 1);
+            mbar_init(st_empty(s), 2);  // released by both MMA-issuing warps
         }
-        for (int q = 0; q < 2; q++) {
-            mbar_init(s_full(q), 1);
-            mbar_init(s_empty(q), CW);
-        }
+        mbar_init(s_full, 1);
+        mbar_init(s_empty, CW);
         mbar_init(dp_full, 1);
         mbar_init(dp_empty, CW);
         mbar_init(p_full, CW);
@@ -133,10 +142,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_init(ds_empty, 1);
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, CW);
-        mbar_init(drain, 1);
+        mbar_init(drain, 2);
         *abort_flag = 0;
         *n_issued_smem = 0;
-        *x_issued_smem = 0;
+        x_issued_smem[0] = 0;
+        x_issued_smem[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -166,23 +176,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (warp == 0) {
         // ---------------- loads
-        int g = 0, nx = 0;
+        int g = 0;
         bool ok = true;
+        // the fixed tiles of the CTA's t-th item into buffer t & 1, once the
+        // item two back has released it
+        auto load_x = [&](int t, int idx) -> bool {
+            const Item it = decode_item<DKV>(a, idx);
+            const int xb = t & 1;
+            if (!wait_warp(x_empty(xb), (uint32_t)(((t >> 1) & 1) ^ 1))) return false;
+            if (lane == 0) {
+                const uint32_t x = base + OFF_X + xb * 2 * TILE;
+                mbar_expect_tx(x_full(xb), 2 * TILE);
+                if (DKV) {
+                    tma_load_3d(x, &tqkv, x_full(xb), C + it.h * HSZ, it.r0, it.b);
+                    tma_load_3d(x + TILE, &tqkv, x_full(xb), 2 * C + it.h * HSZ, it.r0, it.b);
+                } else {
+                    tma_load_3d(x, &tqkv, x_full(xb), it.h * HSZ, it.r0, it.b);
+                    tma_load_3d(x + TILE, &tdo, x_full(xb), it.h * HSZ, it.r0, it.b);
+                }
+                ++x_issued_smem[xb];
+            }
+            return true;
+        };
+        if (item_of(0) < a.items) ok = load_x(0, item_of(0));
         for (int t = 0, idx = item_of(0); ok && idx < a.items; idx = item_of(++t)) {
             const Item it = decode_item<DKV>(a, idx);
             const int xq = it.h * HSZ, xk = C + it.h * HSZ, xv = 2 * C + it.h * HSZ;
-            if (!wait_warp(x_empty, (uint32_t)((t & 1) ^ 1))) break;
-            if (lane == 0) {
-                mbar_expect_tx(x_full, 2 * TILE);
-                if (DKV) {
-                    tma_load_3d(base + OFF_X0, &tqkv, x_full, xk, it.r0, it.b);
-                    tma_load_3d(base + OFF_X1, &tqkv, x_full, xv, it.r0, it.b);
-                } else {
-                    tma_load_3d(base + OFF_X0, &tqkv, x_full, xq, it.r0, it.b);
-                    tma_load_3d(base + OFF_X1, &tdo, x_full, it.h * HSZ, it.r0, it.b);
-                }
-            }
-            ++nx;
             for (int u = 0; u < it.n; u++, g++) {
                 const int st = g % STAGES;
                 if (!wait_warp(st_empty(st), (uint32_t)(((g / STAGES) & 1) ^ 1))) { ok = false; break; }
@@ -215,91 +234,88 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         tma_load_3d(y, &tqkv, st_full(st), xk, c0, it.b);
                         tma_load_3d(y + TILE, &tqkv, st_full(st), xv, c0, it.b);
                     }
+                    *n_issued_smem = g + 1;
+                }
+                // the next item's fixed tiles, right after this item's first block
+                if (u == 0 && item_of(t + 1) < a.items && !load_x(t + 1, item_of(t + 1))) {
+                    ok = false;
+                    break;
                 }
             }
         }
-        if (lane == 0) {
-            *n_issued_smem = g;
-            *x_issued_smem = nx;
-        }
-    } else if (warp == 1) {
-        {
-            // ---------------- MMA issuer (the whole warp runs it, one elected lane issues)
-            const uint32_t idSq = idesc<0>(0, 0, BLK, BLK);  // S, dP: both operands K-major
-            const uint32_t idAcc = idesc<0>(0, 1, BLK, HSZ); // acc += (P|dS) Y: Y is MN-major
-            const uint32_t tS0 = tmem_base, tdP = tmem_base + 256;
-            const uint32_t tA0 = tmem_base + 384, tA1 = tmem_base + 448;
-            auto ybuf = [&](int g, int which) { return base + OFF_Y + (g % STAGES) * 2 * TILE + which * TILE; };
-            auto issue_qk = [&](uint32_t d, uint32_t x, uint32_t y) {
-                const uint64_t dx = sdesc(x, 16, 1024), dy = sdesc(y, 16, 1024);
+    } else if (warp == 1 || warp == QKW) {
+        // ---------------- MMA issuers: warp QKW issues S and dP, warp 1 the
+        // accumulating MMAs, so neither chain waits behind the other. Each
+        // runs its loop as a whole warp; one elected lane issues.
+        const uint32_t idSq = idesc<0>(0, 0, BLK, BLK);  // S, dP: both operands K-major
+        const uint32_t idAcc = idesc<0>(0, 1, BLK, HSZ); // acc += (P|dS) Y: Y is MN-major
+        auto ybuf = [&](int g, int which) { return base + OFF_Y + (g % STAGES) * 2 * TILE + which * TILE; };
+        auto issue_qk = [&](uint32_t d, uint32_t x, uint32_t y) {
+            const uint64_t dx = sdesc(x, 16, 1024), dy = sdesc(y, 16, 1024);
 #pragma unroll
-                for (int k = 0; k < HSZ / 16; k++)  // +32 bytes along K per step
-                    umma_warp<0, 1>(d, dx + 2 * k, dy + 2 * k, idSq, k ? 1u : 0u);
-            };
-            auto issue_acc = [&](uint32_t d, uint32_t pa, uint32_t y, bool accumulate) {
-                const uint64_t dp = sdesc(pa, 16, 1024), dy = sdesc(y, 8192, 1024);
+            for (int k = 0; k < HSZ / 16; k++)  // +32 bytes along K per step
+                umma_warp<0, 1>(d, dx + 2 * k, dy + 2 * k, idSq, k ? 1u : 0u);
+        };
+        // acc += A Y, A = bf16 pairs in TMEM from column ta (16 rows of K = 8
+        // columns per step), Y = 2048 bytes per step
+        auto issue_acc = [&](uint32_t d, uint32_t ta, uint32_t y, bool accumulate) {
+            const uint64_t dy = sdesc(y, 8192, 1024);
 #pragma unroll
-                for (int k = 0; k < BLK / 16; k++)  // 16 rows of K: next atom every 4 steps, 2048 bytes of Y
-                    umma_warp<0, 1>(d, dp + (k >> 2) * (TILE >> 4) + (k & 3) * 2, dy + 128 * k, idAcc,
-                                    (accumulate || k) ? 1u : 0u);
-            };
-            // S of global block g once its ring stage landed and its S buffer was read
-            auto issue_s = [&](int g) {
-                if (!mbar_wait_warp(st_full(g % STAGES), (uint32_t)((g / STAGES) & 1), abort_flag) ||
-                    !mbar_wait_warp(s_empty(g & 1), (uint32_t)(((g >> 1) & 1) ^ 1), abort_flag))
-                    return false;
-                tc_fence_after();
-                issue_qk(tS0 + (uint32_t)((g & 1) * 128), base + OFF_X0, ybuf(g, 0));
-                umma_commit_warp<1>(s_full(g & 1));
-                return true;
-            };
-            // dP of global block g once the previous dP was read
-            auto issue_dp = [&](int g) {
-                if (!mbar_wait_warp(dp_empty, (uint32_t)((g & 1) ^ 1), abort_flag)) return false;
-                tc_fence_after();
-                issue_qk(tdP, base + OFF_X1, ybuf(g, 1));
-                umma_commit_warp<1>(dp_full);
-                return true;
-            };
-            int g0 = 0;
-            bool ok = true;
-            for (int t = 0, idx = item_of(0); ok && idx < a.items; idx = item_of(++t)) {
-                const int n = decode_item<DKV>(a, idx).n;
-                if (!mbar_wait_warp(x_full, (uint32_t)(t & 1), abort_flag)) break;
-                tc_fence_after();
-                ok = issue_s(g0) && issue_dp(g0);
-                if (ok && n == 1) umma_commit_warp<1>(x_empty);  // the item's last reads of K/V (Q/dO)
-                if (ok && n > 1) ok = issue_s(g0 + 1);
+            for (int k = 0; k < BLK / 16; k++)
+                umma_ts_warp(d, ta + (uint32_t)(k * 8), dy + 128 * k, idAcc, (accumulate || k) ? 1u : 0u);
+        };
+        int g = 0;
+        bool ok = true;
+        for (int t = 0, idx = item_of(0); ok && idx < a.items; idx = item_of(++t)) {
+            const int n = decode_item<DKV>(a, idx).n;
+            if (warp == QKW) {
+                const int xb = t & 1;
+                const uint32_t x0 = base + OFF_X + xb * 2 * TILE, x1 = x0 + TILE;
+                if (!mbar_wait_warp(x_full(xb), (uint32_t)((t >> 1) & 1), abort_flag)) break;
+                for (int u = 0; u < n; u++, g++) {
+                    // S of block g once its ring stage landed and the previous S was read
+                    if (!mbar_wait_warp(st_full(g % STAGES), (uint32_t)((g / STAGES) & 1), abort_flag) ||
+                        !mbar_wait_warp(s_empty, (uint32_t)((g & 1) ^ 1), abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_qk(tmem_base + TM_S, x0, ybuf(g, 0));
+                    umma_commit_warp<1>(s_full);
+                    // dP of block g once the previous dP was read
+                    if (!mbar_wait_warp(dp_empty, (uint32_t)((g & 1) ^ 1), abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_qk(tmem_base + TM_DP, x1, ybuf(g, 1));
+                    umma_commit_warp<1>(dp_full);
+                    umma_commit_warp<1>(st_empty(g % STAGES));  // this warp's reads of the stage
+                }
+                if (ok) umma_commit_warp<1>(x_empty(xb));  // the item's last reads of its fixed tiles
+            } else {
                 // the previous item's accumulators have been read out
-                if (ok && !mbar_wait_warp(acc_empty, (uint32_t)((t & 1) ^ 1), abort_flag)) ok = false;
-                if (ok) tc_fence_after();
-                for (int u = 0; ok && u < n; u++) {
-                    const int g = g0 + u;
+                if (!mbar_wait_warp(acc_empty, (uint32_t)((t & 1) ^ 1), abort_flag)) break;
+                tc_fence_after();
+                for (int u = 0; u < n; u++, g++) {
                     const uint32_t par = (uint32_t)(g & 1);
                     if (DKV) {
                         if (!mbar_wait_warp(p_full, par, abort_flag)) { ok = false; break; }
                         tc_fence_after();
-                        issue_acc(tA0, base + OFF_P, ybuf(g, 1), u > 0);  // dV += P^T dO
+                        issue_acc(tmem_base + TM_A0, tmem_base + TM_P, ybuf(g, 1), u > 0);  // dV += P^T dO
                         umma_commit_warp<1>(p_empty);
-                    }
-                    if (u + 1 < n) {
-                        if (!issue_dp(g + 1)) { ok = false; break; }
-                        if (u + 2 == n) umma_commit_warp<1>(x_empty);  // the item's last reads of X
                     }
                     if (!mbar_wait_warp(ds_full, par, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     // DKV: dK += dS^T Q; DQ: dQ += dS K
-                    issue_acc(DKV ? tA1 : tA0, base + OFF_DS, ybuf(g, 0), u > 0);
+                    issue_acc(tmem_base + (DKV ? TM_A1 : TM_A0), tmem_base + TM_DS, ybuf(g, 0), u > 0);
                     umma_commit_warp<1>(ds_empty);
-                    umma_commit_warp<1>(st_empty(g % STAGES));
-                    if (u + 2 < n && !issue_s(g + 2)) { ok = false; break; }
+                    umma_commit_warp<1>(st_empty(g % STAGES));  // this warp's reads of the stage
                 }
-                if (!ok) break;
-                umma_commit_warp<1>(acc_full);
-                g0 += n;
+                if (ok) umma_commit_warp<1>(acc_full);
             }
         }
-    } else {
+    } else if (warp >= 2 && warp < 2 + CW) {
         // ---------------- P and dS: CW warps, CQ per TMEM lane quarter, each
         // on COLS consecutive columns of its row
         const int qq = warp & 3;             // TMEM lane quarter
@@ -307,12 +323,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int r = qq * 32 + lane;        // row within the tile
         const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
         const int c_base = cq * COLS;
-        const uint32_t tdP = tmem_base + lane_off + 256 + c_base;
-        // this thread's COLS columns of row r: atom c_base / 64, 16-byte chunks from k8_0
-        const int k8_0 = (c_base % 64) / 8;
-        uint8_t* pbuf = base_ptr + OFF_P + (c_base / 64) * TILE + r * 128;
-        uint8_t* dsbuf = base_ptr + OFF_DS + (c_base / 64) * TILE + r * 128;
-        const int swz = r & 7;
+        const uint32_t tS = tmem_base + lane_off + TM_S + c_base;
+        const uint32_t tdP = tmem_base + lane_off + TM_DP + c_base;
+        const uint32_t tP = tmem_base + lane_off + TM_P + c_base / 2;   // bf16 pairs
+        const uint32_t tDS = tmem_base + lane_off + TM_DS + c_base / 2;
+        static_assert(COLS == 32, "one 32-column TMEM load per operand");
         int g = 0;
         bool ok = true;
         for (int t = 0, idx = item_of(0); ok && idx < a.items; idx = item_of(++t)) {
@@ -325,21 +340,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 d_row = a.D[(size_t)it.bh * T + row];
             }
             for (int u = 0; u < it.n; u++, g++) {
-                const int sb = g & 1, st = g % STAGES;
+                const int st = g % STAGES;
                 const uint32_t par = (uint32_t)(g & 1);
-                if (!wait_warp(s_full(sb), (uint32_t)((g >> 1) & 1))) { ok = false; break; }
+                if (!wait_warp(s_full, par)) { ok = false; break; }
                 tc_fence_after();
                 const float* vec = reinterpret_cast<const float*>(base_ptr + OFF_VEC + st * 1024);
                 // the diagonal block: DKV sees it first, DQ last
                 const bool diag = DKV ? u == 0 : u == it.n - 1;
                 float P[COLS];
-#pragma unroll
-                for (int ch = 0; ch < COLS / 32; ch++) {
+                {
                     float v[32];
-                    tmem_ld32(tmem_base + lane_off + (uint32_t)(sb * 128 + c_base + ch * 32), v);
+                    tmem_ld32(tS, v);
+                    // S may be overwritten by the next block's MMA
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(s_empty);
 #pragma unroll
                     for (int e = 0; e < 32; e += 4) {
-                        const int c = c_base + ch * 32 + e;
+                        const int c = c_base + e;
                         float4 nl4;
                         if (DKV) nl4 = *reinterpret_cast<const float4*>(vec + c);
                         else nl4 = make_float4(nl_row, nl_row, nl_row, nl_row);
@@ -349,68 +367,60 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             float p = ex2_approx(fmaf(v[e + f], a.scale_log2, nl[f]));
                             // causal: query >= key
                             if (diag) p = (DKV ? c + f >= r : c + f <= r) ? p : 0.f;
-                            P[ch * 32 + e + f] = p;
+                            P[e + f] = p;
                         }
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(s_empty(sb));
                 if (DKV) {
-                    // P^T, bf16
-                    if (!wait_warp(p_empty, par ^ 1u)) { ok = false; break; }
+                    // P^T as bf16 pairs into TMEM, once the previous dV MMA read it
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int k = 0; k < COLS / 8; k++) {
-                        uint32_t pk[4];
-#pragma unroll
-                        for (int e = 0; e < 4; e++) {
-                            __nv_bfloat162 pr = __floats2bfloat162_rn(P[8 * k + 2 * e], P[8 * k + 2 * e + 1]);
-                            pk[e] = *reinterpret_cast<uint32_t*>(&pr);
-                        }
-                        *reinterpret_cast<uint4*>(pbuf + (((k8_0 + k) ^ swz) << 4)) =
-                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    for (int e = 0; e < 16; e++) {
+                        __nv_bfloat162 pr = __floats2bfloat162_rn(P[2 * e], P[2 * e + 1]);
+                        pk[e] = *reinterpret_cast<uint32_t*>(&pr);
                     }
-                    fence_async_smem();
+                    if (!wait_warp(p_empty, par ^ 1u)) { ok = false; break; }
+                    tc_fence_after();
+                    tmem_st16_nowait(tP, pk);
+                    tmem_wait_st();
+                    tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(p_full);
                 }
                 if (!wait_warp(dp_full, par)) { ok = false; break; }
                 tc_fence_after();
-                uint32_t dsk[COLS / 2];
-#pragma unroll
-                for (int ch = 0; ch < COLS / 32; ch++) {
+                uint32_t dsk[16];
+                {
                     float v[32];
-                    tmem_ld32(tdP + (uint32_t)(ch * 32), v);
+                    tmem_ld32(tdP, v);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(dp_empty);
 #pragma unroll
                     for (int e = 0; e < 32; e += 4) {
-                        const int c = c_base + ch * 32 + e;
+                        const int c = c_base + e;
                         float4 d4;
                         if (DKV) d4 = *reinterpret_cast<const float4*>(vec + 128 + c);
                         else d4 = make_float4(d_row, d_row, d_row, d_row);
-                        const int j = ch * 32 + e;
                         __nv_bfloat162 lo =
-                            __floats2bfloat162_rn(P[j] * (v[e] - d4.x), P[j + 1] * (v[e + 1] - d4.y));
+                            __floats2bfloat162_rn(P[e] * (v[e] - d4.x), P[e + 1] * (v[e + 1] - d4.y));
                         __nv_bfloat162 hi =
-                            __floats2bfloat162_rn(P[j + 2] * (v[e + 2] - d4.z), P[j + 3] * (v[e + 3] - d4.w));
-                        dsk[j >> 1] = *reinterpret_cast<uint32_t*>(&lo);
-                        dsk[(j >> 1) + 1] = *reinterpret_cast<uint32_t*>(&hi);
+                            __floats2bfloat162_rn(P[e + 2] * (v[e + 2] - d4.z), P[e + 3] * (v[e + 3] - d4.w));
+                        dsk[e >> 1] = *reinterpret_cast<uint32_t*>(&lo);
+                        dsk[(e >> 1) + 1] = *reinterpret_cast<uint32_t*>(&hi);
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(dp_empty);
                 if (!wait_warp(ds_empty, par ^ 1u)) { ok = false; break; }
-#pragma unroll
-                for (int k = 0; k < COLS / 8; k++)
-                    *reinterpret_cast<uint4*>(dsbuf + (((k8_0 + k) ^ swz) << 4)) =
-                        make_uint4(dsk[4 * k], dsk[4 * k + 1], dsk[4 * k + 2], dsk[4 * k + 3]);
-                fence_async_smem();
+                tc_fence_after();
+                tmem_st16_nowait(tDS, dsk);
+                tmem_wait_st();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ds_full);
             }
             if (!ok) break;
             // epilogue: the accumulator columns split over the column groups.
-            // DKV: [dV 64 | dK 64] at TMEM 384; DQ: dQ 64 at TMEM 384
+            // DKV: [dV 64 | dK 64] at TM_A0; DQ: dQ 64 at TM_A0
             if (!wait_warp(acc_full, (uint32_t)(t & 1))) { ok = false; break; }
             tc_fence_after();
             constexpr int W = (DKV ? 128 : 64) / CQ;  // columns per thread
@@ -418,7 +428,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             float v[W];
 #pragma unroll
             for (int ch = 0; ch < W; ch += 16)
-                tmem_ld16(tmem_base + lane_off + 384u + (uint32_t)(a0 + ch),
+                tmem_ld16(tmem_base + lane_off + TM_A0 + (uint32_t)(a0 + ch),
                           *reinterpret_cast<float(*)[16]>(v + ch));
             tc_fence_before();
             __syncwarp();
@@ -447,8 +457,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (*abort_flag) {
         if (threadIdx.x == 0) {
             // let every issued copy land before the shared memory is released
-            const int nx = *x_issued_smem;
-            if (nx > 0) mbar_wait_drain(x_full, (uint32_t)((nx - 1) & 1));
+            for (int b = 0; b < 2; b++) {
+                const int nx = x_issued_smem[b];
+                if (nx > 0) mbar_wait_drain(x_full(b), (uint32_t)((nx - 1) & 1));
+            }
             const int issued = *n_issued_smem;
             for (int s = 0; s < STAGES; s++) {
                 if (issued > s) {
@@ -458,7 +470,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             atomicOr(a.err, DEVERR_TIMEOUT);
         }
-        if (warp == 1) {  // the issuing lane commits (elected as when issuing)
+        if (warp == 1 || warp == QKW) {  // each issuing lane commits (elected as when issuing)
             umma_commit_local_warp<1>(drain);
             if (lane == 0) mbar_wait_drain(drain, 0);
             __syncwarp();

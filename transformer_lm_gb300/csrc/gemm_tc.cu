@@ -318,8 +318,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // ---------------- MMA issuer (the pair leader): the whole warp runs
             // the loop, one elected lane issues
             const uint32_t id = idesc<KIND>(args.a_mn, args.b_mn, BM * CG, BN);
+            // descriptor advance per K step, in 16-byte units: MN-major operands
+            // move by UK rows of 128 bytes, K-major ones by UK elements
+            const uint32_t lbo_a = args.a_mn ? KE * ROWB : 16, lbo_b = args.b_mn ? KE * ROWB : 16;
+            const uint64_t step_a = (uint64_t)((args.a_mn ? UK * ROWB : UK * (int)sizeof(T)) >> 4);
+            const uint64_t step_b = (uint64_t)((args.b_mn ? UK * ROWB : UK * (int)sizeof(T)) >> 4);
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
+            bool ready = false;  // the current stage is known to have landed
             for (int st = cid; st < num_units; st += ncl) {
                 if (!mbar_wait_warp(tempty(acc), acc_phase ^ 1u, abort_flag)) break;
                 tc_fence_after();
@@ -328,22 +334,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int kb1 = min(args.num_kb, kb0 + args.kb_per);
                 bool ok = true;
                 for (int kb = kb0; kb < kb1; kb++) {
-                    if (!mbar_wait_warp(full(stage), phase, abort_flag)) { ok = false; break; }
+                    if (!ready && !mbar_wait_warp(full(stage), phase, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t sa = base + stage * C::STAGE_BYTES;
-                    const uint32_t sb = sa + C::A_BYTES;
+                    const uint64_t da = sdesc(sa, lbo_a, 1024), db = sdesc(sa + C::A_BYTES, lbo_b, 1024);
+                    const int nst = stage + 1 == C::STAGES ? 0 : stage + 1;
+                    const uint32_t nph = stage + 1 == C::STAGES ? phase ^ 1u : phase;
 #pragma unroll
                     for (int k = 0; k < KSTEPS; k++) {
-                        const uint64_t da = args.a_mn
-                                                ? sdesc(sa + k * UK * ROWB, KE * ROWB, 1024)
-                                                : sdesc(sa + k * UK * (int)sizeof(T), 16, 1024);
-                        const uint64_t db = args.b_mn
-                                                ? sdesc(sb + k * UK * ROWB, KE * ROWB, 1024)
-                                                : sdesc(sb + k * UK * (int)sizeof(T), 16, 1024);
-                        umma_warp<KIND, CG>(d, da, db, id, (kb > kb0 || k) ? 1u : 0u);
+                        // test the next stage while this stage's MMAs are queued,
+                        // so a landed stage costs no wait between the groups
+                        if (k == KSTEPS - 1) ready = __all_sync(0xffffffffu, mbar_test(full(nst), nph));
+                        umma_warp<KIND, CG>(d, da + k * step_a, db + k * step_b, id, (kb > kb0 || k) ? 1u : 0u);
                     }
                     umma_commit_warp<CG>(empty(stage));  // frees the stage in every CTA of the pair
-                    if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+                    stage = nst;
+                    phase = nph;
                 }
                 if (!ok) break;
                 umma_commit_warp<CG>(tfull(acc));

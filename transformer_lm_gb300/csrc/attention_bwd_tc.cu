@@ -355,19 +355,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(s_empty);
+                    const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
 #pragma unroll
                     for (int e = 0; e < 32; e += 4) {
                         const int c = c_base + e;
                         float4 nl4;
                         if (DKV) nl4 = *reinterpret_cast<const float4*>(vec + c);
                         else nl4 = make_float4(nl_row, nl_row, nl_row, nl_row);
-                        const float* nl = &nl4.x;
+                        // exponent arguments two at a time (packed fp32 FMA)
+                        const float2 x01 = ffma2(make_float2(v[e], v[e + 1]), sc2, make_float2(nl4.x, nl4.y));
+                        const float2 x23 = ffma2(make_float2(v[e + 2], v[e + 3]), sc2, make_float2(nl4.z, nl4.w));
+                        float p4[4] = {ex2_approx(x01.x), ex2_approx(x01.y), ex2_approx(x23.x), ex2_approx(x23.y)};
 #pragma unroll
                         for (int f = 0; f < 4; f++) {
-                            float p = ex2_approx(fmaf(v[e + f], a.scale_log2, nl[f]));
                             // causal: query >= key
-                            if (diag) p = (DKV ? c + f >= r : c + f <= r) ? p : 0.f;
-                            P[e + f] = p;
+                            if (diag) p4[f] = (DKV ? c + f >= r : c + f <= r) ? p4[f] : 0.f;
+                            P[e + f] = p4[f];
                         }
                     }
                 }
@@ -402,10 +405,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         float4 d4;
                         if (DKV) d4 = *reinterpret_cast<const float4*>(vec + 128 + c);
                         else d4 = make_float4(d_row, d_row, d_row, d_row);
-                        __nv_bfloat162 lo =
-                            __floats2bfloat162_rn(P[e] * (v[e] - d4.x), P[e + 1] * (v[e + 1] - d4.y));
-                        __nv_bfloat162 hi =
-                            __floats2bfloat162_rn(P[e + 2] * (v[e + 2] - d4.z), P[e + 3] * (v[e + 3] - d4.w));
+                        // P (dP - D), two at a time (packed fp32 add and multiply)
+                        const float2 s01 = fmul2(make_float2(P[e], P[e + 1]),
+                                                 fadd2(make_float2(v[e], v[e + 1]), make_float2(-d4.x, -d4.y)));
+                        const float2 s23 = fmul2(make_float2(P[e + 2], P[e + 3]),
+                                                 fadd2(make_float2(v[e + 2], v[e + 3]), make_float2(-d4.z, -d4.w)));
+                        __nv_bfloat162 lo = __floats2bfloat162_rn(s01.x, s01.y);
+                        __nv_bfloat162 hi = __floats2bfloat162_rn(s23.x, s23.y);
                         dsk[e >> 1] = *reinterpret_cast<uint32_t*>(&lo);
                         dsk[(e >> 1) + 1] = *reinterpret_cast<uint32_t*>(&hi);
                     }

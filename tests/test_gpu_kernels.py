@@ -235,7 +235,8 @@ def test_fused_op_small_shapes_match_oracle():
 
 
 @pytest.mark.parametrize("N,C,dt", [(1000, 768, "bf16"), (37, 64, "f32"), (8192, 768, "bf16"),
-                                    (300, 1024, "bf16"), (129, 1024, "f32")])
+                                    (300, 1024, "bf16"), (129, 1024, "f32"), (515, 640, "bf16"),
+                                    (700, 512, "bf16"), (9, 256, "bf16")])
 def test_layernorm_forward_backward_match_oracle(N, C, dt):
     import torch
     bf16 = dt == "bf16"
@@ -269,5 +270,11 @@ def test_layernorm_forward_backward_match_oracle(N, C, dt):
                               C, 1, scratch)
     G.gpt2_device_status()
     assert rel_to_max(host(g_dinp), dinp) < (2e-2 if bf16 else 1e-5)
-    assert rel_to_max(host(g_dw) - 1.0, dw - 1.0) < (2e-2 if bf16 else 1e-5)
-    assert rel_to_max(host(g_db) - 1.0, db - 1.0) < (2e-2 if bf16 else 1e-5)
+    # dw, db = 1 + sums over rows: the bf16 result is rounded once near 1 (a
+    # half ulp is 2^-8), on top of the sums' own relative error
+    for got, want in ((host(g_dw), dw), (host(g_db), db)):
+        err = np.max(np.abs(got - want))
+        if bf16:
+            assert err <= 2.0 ** -8 * np.max(np.abs(want)) + 2e-2 * np.max(np.abs(want - 1.0))
+        else:
+            assert rel_to_max(got - 1.0, want - 1.0) < 1e-5

@@ -666,6 +666,136 @@ __global__ void __launch_bounds__(LNQ_THREADS, 1) layernorm_backward_bulk_k(
     }
 }
 
+// The same operation (bf16, C = 256 NV) with one warp per row: lane l holds
+// the row's 16-byte vectors l, l + 32, ... (8 columns each), so every access
+// of a warp covers 512 contiguous bytes, and the row sums are warp shuffles.
+// Each warp streams its rows (x, dy and, for +=, the current dx) through its
+// own ring of LNW_BUF row slots in shared memory with cp.async, so LNW_BUF - 1
+// rows per warp are in flight while one is computed without holding them in
+// registers. The dw / db / colsum partials of the lane's columns stay in
+// registers across the warp's rows. The CTA's rows are a contiguous range,
+// taken by its warps in turn; the warps' partials are folded in warp order
+// into part[blockIdx.x] = [dw | db (| colsum)] (G*C floats).
+constexpr int LNW_WARPS = 8;
+constexpr int LNW_BUF = 4;
+
+DEVI void lnw_cp16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+template <int NV>
+__global__ void __launch_bounds__(32 * LNW_WARPS, 1) layernorm_backward_warp_k(
+    bf16* __restrict__ dinp, float* __restrict__ part, const bf16* __restrict__ dout,
+    const bf16* __restrict__ inp, const bf16* __restrict__ w, const float* __restrict__ mean,
+    const float* __restrict__ rstd, int N, int C, int accumulate, int with_colsum) {
+    constexpr int VEC = 8;
+    constexpr int ROWB = 256 * NV * 2;  // bytes of one row of one array
+    // [warp][slot][x | dy | dx] rows; reused at the end for the fold [warp][G][C]
+    extern __shared__ __align__(16) uint8_t lnw_sm[];
+    pdl_enter();
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    const int per = (N + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int r_begin = min(N, (int)blockIdx.x * per), r_end = min(N, r_begin + per);
+    const int G = with_colsum ? 3 : 2;
+    uint8_t* ring = lnw_sm + (size_t)warp * LNW_BUF * 3 * ROWB;
+    const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
+    Vec16<bf16> wv[NV];
+#pragma unroll
+    for (int j = 0; j < NV; j++) wv[j] = ld16(w + (lane + 32 * j) * VEC);
+    float adw[NV][VEC], adb[NV][VEC], acs[NV][VEC];
+#pragma unroll
+    for (int j = 0; j < NV; j++)
+#pragma unroll
+        for (int e = 0; e < VEC; e++) adw[j][e] = adb[j][e] = acs[j][e] = 0.f;
+    // the warp's k-th row is r_begin + warp + k * LNW_WARPS, in slot k % LNW_BUF;
+    // one commit group per row (empty groups past the end keep the count)
+    auto issue = [&](int k) {
+        const int r = r_begin + warp + k * LNW_WARPS;
+        if (r < r_end) {
+            const uint32_t slot = ring_s + (uint32_t)((k % LNW_BUF) * 3 * ROWB);
+            const size_t off = (size_t)r * C + lane * VEC;
+#pragma unroll
+            for (int j = 0; j < NV; j++) {
+                const uint32_t o = (uint32_t)((lane + 32 * j) * 16);
+                lnw_cp16(slot + o, inp + off + 32 * j * VEC);
+                lnw_cp16(slot + ROWB + o, dout + off + 32 * j * VEC);
+                if (accumulate) lnw_cp16(slot + 2 * ROWB + o, dinp + off + 32 * j * VEC);
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+#pragma unroll
+    for (int k = 0; k < LNW_BUF - 1; k++) issue(k);
+    for (int k = 0;; k++) {
+        const int r = r_begin + warp + k * LNW_WARPS;
+        if (r >= r_end) break;
+        issue(k + LNW_BUF - 1);
+        asm volatile("cp.async.wait_group %0;" ::"n"(LNW_BUF - 1) : "memory");
+        __syncwarp();
+        const uint8_t* slot = ring + (size_t)(k % LNW_BUF) * 3 * ROWB;
+        const float mu = mean[r], rs = rstd[r];
+        Vec16<bf16> xv[NV], dv[NV];
+        float gs = 0.f, gns = 0.f;
+#pragma unroll
+        for (int j = 0; j < NV; j++) {
+            xv[j] = *reinterpret_cast<const Vec16<bf16>*>(slot + (lane + 32 * j) * 16);
+            dv[j] = *reinterpret_cast<const Vec16<bf16>*>(slot + ROWB + (lane + 32 * j) * 16);
+#pragma unroll
+            for (int e = 0; e < VEC; e++) {
+                const float g = to_f(wv[j].v[e]) * to_f(dv[j].v[e]);
+                gs += g;
+                gns += g * ((to_f(xv[j].v[e]) - mu) * rs);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            gs += __shfl_xor_sync(0xffffffffu, gs, o);
+            gns += __shfl_xor_sync(0xffffffffu, gns, o);
+        }
+        const float gm = gs / C, gnm = gns / C;
+        bf16* dx = dinp + (size_t)r * C + lane * VEC;
+#pragma unroll
+        for (int j = 0; j < NV; j++) {
+            Vec16<bf16> o, ov;
+            if (accumulate) ov = *reinterpret_cast<const Vec16<bf16>*>(slot + 2 * ROWB + (lane + 32 * j) * 16);
+#pragma unroll
+            for (int e = 0; e < VEC; e++) {
+                const float d = to_f(dv[j].v[e]);
+                const float nh = (to_f(xv[j].v[e]) - mu) * rs;
+                const float val = rs * (to_f(wv[j].v[e]) * d - gm - nh * gnm);
+                o.v[e] = from_f<bf16>(accumulate ? to_f(ov.v[e]) + val : val);
+                adw[j][e] += nh * d;
+                adb[j][e] += d;
+                acs[j][e] += to_f(o.v[e]);
+            }
+            st16(dx + 32 * j * VEC, o);
+        }
+        __syncwarp();  // every lane has read the slot before it is refilled
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    // fold the warps in order through the (now idle) rings: [warp][G][C]
+    float* fold = reinterpret_cast<float*>(lnw_sm);
+    float* mine = fold + (size_t)warp * G * C;
+#pragma unroll
+    for (int j = 0; j < NV; j++)
+#pragma unroll
+        for (int e = 0; e < VEC; e++) {
+            const int c = (lane + 32 * j) * VEC + e;
+            mine[c] = adw[j][e];
+            mine[C + c] = adb[j][e];
+            if (with_colsum) mine[2 * C + c] = acs[j][e];
+        }
+    __syncthreads();
+    float* dst = part + (size_t)blockIdx.x * G * C;
+    for (int c = threadIdx.x; c < G * C; c += blockDim.x) {
+        float t = 0.f;
+#pragma unroll
+        for (int wi = 0; wi < LNW_WARPS; wi++) t += fold[(size_t)wi * G * C + c];
+        dst[c] = t;
+    }
+}
+
 // dst[c] (+)= sum over p of part[p * pstride + c] for every descriptor, summed in
 // increasing p (one launch for many parameter tensors)
 template <typename T>
@@ -786,6 +916,30 @@ int launch_layernorm_backward_part(DType dt, void* dinp, float* part, const void
                                    const float* rstd, int N, int C, int accumulate, int with_colsum,
                                    unsigned int* err, cudaStream_t s) {
     const int P = layernorm_backward_part_rows(dt, N, C);
+    if (layernorm_backward_fuses_colsum(dt, C) && C % 256 == 0) {
+        const int nv = C / 256;
+        // the warps' row rings, later reused by the fold [warp][3][C] fp32
+        const size_t ring = (size_t)LNW_WARPS * LNW_BUF * 3 * C * 2, fold = sizeof(float) * LNW_WARPS * 3 * C;
+        const size_t smem = ring > fold ? ring : fold;
+        note_launch(1);
+#define LNW(NVV)                                                                                       \
+    do {                                                                                               \
+        static size_t done = 0;                                                                        \
+        if (smem > done) {                                                                             \
+            cudaFuncSetAttribute(layernorm_backward_warp_k<NVV>,                                       \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);              \
+            done = smem;                                                                               \
+        }                                                                                              \
+        launch_pdl(layernorm_backward_warp_k<NVV>, dim3(P), dim3(32 * LNW_WARPS), smem, s,             \
+                   (bf16*)dinp, part, (const bf16*)dout, (const bf16*)inp, (const bf16*)w, mean, rstd, \
+                   N, C, accumulate, with_colsum);                                                     \
+    } while (0)
+        if (nv == 1) LNW(1);
+        else if (nv == 2) LNW(2);
+        else LNW(3);
+#undef LNW
+        return P;
+    }
     if (layernorm_backward_fuses_colsum(dt, C)) {
         const int nv = (C / 8 + 31) / 32;
         note_launch(1);

@@ -58,7 +58,7 @@ template <int BN, int CG> struct Cfg {
     static constexpr int EPI_BYTES = EPI_WARPS * STG_BYTES;
     static constexpr int BAR_BYTES = 256 + 1024;  // barriers, flags, per-row softmax partials
     static constexpr int STAGES = (227 * 1024 - EPI_BYTES - BAR_BYTES - 1024) / STAGE_BYTES;
-    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;  // two accumulators, power of two
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES + 1024;
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
@@ -690,13 +690,26 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
     // tile width: 256 (a 256 x 256 pair tile halves the operand traffic per
     // flop of a 256 x 128 one); 128 only for narrow outputs
     int BN = p.N <= 128 ? 128 : 256;
+    // 192-wide tiles (B K-major only: a CTA's 96 rows of B are one TMA box) when
+    // they fill the last wave of CTA pairs markedly better than 256-wide ones
+    if (BN == 256 && p.b_kmajor && dt == DT_BF16 &&
+        (p.epi == EPI_STORE || p.epi == EPI_GELU || p.epi == EPI_RESID || p.epi == EPI_GELU_BWD)) {
+        const long long units = cg == 2 ? sms / 2 : sms, mg = (nm + cg - 1) / cg;
+        // time ~ waves x tile width
+        auto cost = [&](int bn) {
+            const long long tiles = mg * ((p.N + bn - 1) / bn);
+            return (double)((tiles + units - 1) / units) * bn;
+        };
+        if (cost(192) < 0.92 * cost(256)) BN = 192;
+    }
     if (p.epi != EPI_GELU_PART) {
-        // GPT2_GEMM_BN=128|256 overrides the choice (tuning)
+        // GPT2_GEMM_BN=128|192|256 overrides the choice (tuning; 192 with K-major B only)
         static const int force_bn = [] {
             const char* e = getenv("GPT2_GEMM_BN");
             return e ? atoi(e) : 0;
         }();
-        if (force_bn == 128 || force_bn == 256) BN = force_bn;
+        if (force_bn == 128 || force_bn == 256 || (force_bn == 192 && p.b_kmajor && p.epi != EPI_ACCUM))
+            BN = force_bn;
     } else {
         BN = 256;
     }
@@ -763,6 +776,8 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
     ok = ok && make_map(&mp.d2, p.epi == EPI_GELU ? p.D2 : p.D, out_dt, p.N, p.M, p.ldd, OCO, 32);
     if (!ok) return GPT2_ERR_CUDA;
     if (dt == DT_BF16) {
+        if (BN == 192)
+            return cg == 2 ? dispatch_epi<192, 0, 2>(p.epi, mp, a, s) : dispatch_epi<192, 0, 1>(p.epi, mp, a, s);
         if (cg == 2)
             return BN == 256 ? dispatch_epi<256, 0, 2>(p.epi, mp, a, s) : dispatch_epi<128, 0, 2>(p.epi, mp, a, s);
         return BN == 256 ? dispatch_epi<256, 0, 1>(p.epi, mp, a, s) : dispatch_epi<128, 0, 1>(p.epi, mp, a, s);

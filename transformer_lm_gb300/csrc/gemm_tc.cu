@@ -51,11 +51,12 @@ constexpr int STG_BYTES = 32 * ROWB;  // an epilogue warp's staging: 32 rows x 1
 // CG = CTAs per MMA: 1 (tcgen05 cta_group::1, 128 x BN tiles) or 2 (a CTA
 // pair runs cta_group::2 MMAs on 256 x BN tiles; each CTA holds 128 rows of A
 // and BN/2 rows of B in its shared memory and its 128 accumulator rows in TMEM)
-template <int BN, int CG> struct Cfg {
+// NSTG staging buffers per epilogue warp (two for the two-output GELU epilogue)
+template <int BN, int CG, int NSTG = 1> struct Cfg {
     static constexpr int A_BYTES = BM * ROWB;
     static constexpr int B_BYTES = (BN / CG) * ROWB;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int EPI_BYTES = EPI_WARPS * STG_BYTES;
+    static constexpr int EPI_BYTES = EPI_WARPS * NSTG * STG_BYTES;
     static constexpr int BAR_BYTES = 256 + 1024;  // barriers, flags, per-row softmax partials
     static constexpr int STAGES = (227 * 1024 - EPI_BYTES - BAR_BYTES - 1024) / STAGE_BYTES;
     static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;  // two accumulators, power of two
@@ -196,7 +197,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_k(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
               const __grid_constant__ Args args) {
-    using C = Cfg<BN, CG>;
+    using C = Cfg<BN, CG, EPI == EPI_GELU ? 2 : 1>;
     using T = typename std::conditional<KIND == 0, bf16, float>::type;
     constexpr int KE = ROWB / (int)sizeof(T);  // K elements per stage
     constexpr int UK = KIND == 0 ? 16 : 8;     // K elements per MMA
@@ -365,8 +366,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int q = warp & 3;          // TMEM lane quarter this warp may access
         const int hh = (warp - 2) >> 2;  // chunk parity
         const int rl = q * 32 + lane;    // row within the tile
-        uint8_t* stg = ebuf_ptr + (warp - 2) * STG_BYTES;
-        const uint32_t stg_s = ebuf + (uint32_t)((warp - 2) * STG_BYTES);
+        constexpr int NSTG = EPI == EPI_GELU ? 2 : 1;
+        uint8_t* stg = ebuf_ptr + (warp - 2) * NSTG * STG_BYTES;
+        const uint32_t stg_s = ebuf + (uint32_t)((warp - 2) * NSTG * STG_BYTES);
         int acc = 0;
         uint32_t acc_phase = 0;
         bool aborted = false;
@@ -403,27 +405,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 epilogue_chunk<T, TO, EPI, OC>(args, v, r, row, nc, o, o2, pmax, psum);
 #pragma unroll
                 for (int k = 0; k < NV; k++) r[k] = rn[k];
-                // this warp's previous store has read the staging buffer
+                // this warp's previous stores have read the staging buffer(s)
                 if (lane == 0) bulk_wait_read<0>();
                 __syncwarp();
                 stage_row(stg, lane, o);
+                if constexpr (EPI == EPI_GELU) stage_row(stg + STG_BYTES, lane, o2);  // its own buffer
                 fence_async_smem();
                 __syncwarp();
                 if (lane == 0) {
                     if constexpr (EPI == EPI_SPLITK) tma_store_3d(&tmD, stg_s, nc, m0 + q * 32, split);
                     else tma_store_2d(&tmD, stg_s, nc, m0 + q * 32);
+                    if constexpr (EPI == EPI_GELU) tma_store_2d(&tmD2, stg_s + STG_BYTES, nc, m0 + q * 32);
                     bulk_commit();
-                }
-                if constexpr (EPI == EPI_GELU) {
-                    if (lane == 0) bulk_wait_read<0>();
-                    __syncwarp();
-                    stage_row(stg, lane, o2);
-                    fence_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&tmD2, stg_s, nc, m0 + q * 32);
-                        bulk_commit();
-                    }
                 }
             }
             // this warp's accumulator rows are read: release them to the leader's MMA
@@ -584,7 +577,7 @@ struct Maps {
 // clusters as can be co-resident (cudaOccupancyMaxActiveClusters).
 template <int BN, int KIND, int EPI, int CG>
 static int launch_tc(const Maps& mp, const tc::Args& a, cudaStream_t s) {
-    using C = tc::Cfg<BN, CG>;
+    using C = tc::Cfg<BN, CG, EPI == EPI_GELU ? 2 : 1>;
     auto kern = tc::gemm_tc_k<BN, KIND, EPI, CG>;
     static bool attr_done = false;
     static int max_clusters = 0;

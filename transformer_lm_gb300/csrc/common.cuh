@@ -77,15 +77,6 @@ DEVI float tanh_fast(float x) {
     asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-DEVI float gelu_fwd_fast(float x) {
-    float u = GELU_K0 * (x + GELU_K1 * x * x * x);
-    return 0.5f * x * (1.0f + tanh_fast(u));
-}
-DEVI float gelu_grad_fast(float x) {
-    float u = GELU_K0 * (x + GELU_K1 * x * x * x);
-    float t = tanh_fast(u);
-    return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * GELU_K0 * (1.0f + 3.0f * GELU_K1 * x * x);
-}
 // d gelu / dx = 0.5 (1 + tanh u) + 0.5 x (1 - tanh^2 u) sqrt(2/pi) (1 + 3 * 0.044715 x^2)
 DEVI float gelu_grad(float x) {
     float u = GELU_K0 * (x + GELU_K1 * x * x * x);

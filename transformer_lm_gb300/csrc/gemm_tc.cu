@@ -95,6 +95,29 @@ DEVI void tile_coords(int st, int num_mg, int num_n, int group, int& mg, int& nb
 // barrier 1 among the epilogue threads
 DEVI void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(EPI_THREADS) : "memory"); }
 
+// gelu(x) = 0.5 x (1 + tanh(x (K0 + K0 K1 x^2))) for two values, packed fp32
+// arithmetic and the hardware tanh (used where the result is rounded to bf16)
+DEVI float2 gelu_fwd_fast2(float2 x) {
+    const float2 u = fmul2(x, ffma2(fmul2(x, x), make_float2(GELU_K0 * GELU_K1, GELU_K0 * GELU_K1),
+                                    make_float2(GELU_K0, GELU_K0)));
+    const float2 h = fmul2(x, make_float2(0.5f, 0.5f));
+    return ffma2(h, make_float2(tanh_fast(u.x), tanh_fast(u.y)), h);
+}
+// gelu'(x) for two values with packed fp32 arithmetic and the hardware tanh
+// (used where the result is rounded to bf16): with t = tanh(x (K0 + K0 K1 x^2)),
+// gelu'(x) = (0.5 + 0.5 t) + x (0.5 K0 + 1.5 K0 K1 x^2) (1 - t^2)
+DEVI float2 gelu_grad_fast2(float2 x) {
+    const float2 x2 = fmul2(x, x);
+    const float2 u = fmul2(x, ffma2(x2, make_float2(GELU_K0 * GELU_K1, GELU_K0 * GELU_K1),
+                                    make_float2(GELU_K0, GELU_K0)));
+    const float2 t = make_float2(tanh_fast(u.x), tanh_fast(u.y));
+    const float2 a = ffma2(t, make_float2(0.5f, 0.5f), make_float2(0.5f, 0.5f));
+    const float2 b = fmul2(x, ffma2(x2, make_float2(1.5f * GELU_K0 * GELU_K1, 1.5f * GELU_K0 * GELU_K1),
+                                    make_float2(0.5f * GELU_K0, 0.5f * GELU_K0)));
+    const float2 omt = ffma2(t, make_float2(-t.x, -t.y), make_float2(1.f, 1.f));
+    return ffma2(b, omt, a);
+}
+
 // ------------------------------------------------------------------ epilogue
 // One 128-byte output chunk of one row: the accumulator values v[OC], the
 // chunk's first column nc, the row; the result leaves packed in o (and the
@@ -138,7 +161,17 @@ DEVI void epilogue_chunk(const Args& a, float (&v)[OC], const Vec16<T> (&r)[OC *
             }
         }
     }
-    if constexpr (EPI == EPI_RESID || EPI == EPI_GELU_BWD || EPI == EPI_ACCUM) {
+    if constexpr (EPI == EPI_GELU_BWD && sizeof(T) == 2) {
+#pragma unroll
+        for (int k = 0; k < OC / VEC; k++)
+#pragma unroll
+            for (int e = 0; e < VEC; e += 2) {
+                const float2 g = gelu_grad_fast2(make_float2(to_f(r[k].v[e]), to_f(r[k].v[e + 1])));
+                const float2 y = fmul2(make_float2(v[k * VEC + e], v[k * VEC + e + 1]), g);
+                v[k * VEC + e] = y.x;
+                v[k * VEC + e + 1] = y.y;
+            }
+    } else if constexpr (EPI == EPI_RESID || EPI == EPI_GELU_BWD || EPI == EPI_ACCUM) {
 #pragma unroll
         for (int k = 0; k < OC / VEC; k++)
 #pragma unroll
@@ -146,7 +179,7 @@ DEVI void epilogue_chunk(const Args& a, float (&v)[OC], const Vec16<T> (&r)[OC *
                 const float rv = to_f(r[k].v[e]);
                 float& x = v[k * VEC + e];
                 if constexpr (EPI == EPI_RESID) x += rv;
-                else if constexpr (EPI == EPI_GELU_BWD) x *= sizeof(T) == 2 ? gelu_grad_fast(rv) : gelu_grad(rv);
+                else if constexpr (EPI == EPI_GELU_BWD) x *= gelu_grad(rv);
                 else x = rv + x;
             }
     }
@@ -175,8 +208,8 @@ DEVI void epilogue_chunk(const Args& a, float (&v)[OC], const Vec16<T> (&r)[OC *
             o[e] = *reinterpret_cast<uint32_t*>(&pr);
             if constexpr (EPI == EPI_GELU) {
                 // GELU of the rounded pre-activation (what the backward sees)
-                const float2 f = __bfloat1622float2(pr);
-                __nv_bfloat162 gr = __floats2bfloat162_rn(gelu_fwd_fast(f.x), gelu_fwd_fast(f.y));
+                const float2 g = gelu_fwd_fast2(__bfloat1622float2(pr));
+                __nv_bfloat162 gr = __floats2bfloat162_rn(g.x, g.y);
                 o2[e] = *reinterpret_cast<uint32_t*>(&gr);
             }
         }

@@ -279,6 +279,22 @@ void launch_encoder_backward(DType dt, void* dwte, void* dwpe, const void* dout,
 }
 
 // ------------------------------------------------------------------ LayerNorm
+using tc::fadd2;
+using tc::ffma2;
+using tc::fmul2;
+// two bf16 (one 32-bit word, low half first) widened to fp32, and back (rounded)
+DEVI float2 bf2_f2(uint32_t u) { return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u)); }
+// the same widening, opaque to the compiler: recomputed at every use rather
+// than kept live in registers between a kernel's passes over a row
+DEVI float2 bf2_f2_v(uint32_t u) {
+    uint32_t lo, hi;
+    asm volatile("shl.b32 %0, %2, 16;\n\tand.b32 %1, %2, 0xffff0000;" : "=r"(lo), "=r"(hi) : "r"(u));
+    return make_float2(__uint_as_float(lo), __uint_as_float(hi));
+}
+DEVI uint32_t f2_bf2(float2 v) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
+    return *reinterpret_cast<const uint32_t*>(&b);
+}
 // layernorm_forward_kernel3: one warp per row, the row held in registers;
 // mean, biased variance, rstd = 1/sqrt(var + 1e-5), y = (x - mean) rstd w + b.
 // mean/rstd are kept in fp32.
@@ -342,6 +358,64 @@ __global__ void layernorm_forward_k(T* __restrict__ out, float* __restrict__ mea
     }
 }
 
+// bf16 rows with C = 256 NV (NV <= 3): lane l keeps the row's 16-byte vectors
+// l, l + 32, ... as packed bf16 words (4 NV registers) and widens them anew in
+// each pass, so the kernel fits in 40 registers and 48 one-row warps are
+// resident per SM; the statistics and the affine map use packed fp32 arithmetic.
+template <int NV>
+__global__ void __launch_bounds__(256, 6) layernorm_forward_bf16_k(bf16* __restrict__ out, float* __restrict__ mean,
+                                                                   float* __restrict__ rstd,
+                                                                   const bf16* __restrict__ inp,
+                                                                   const bf16* __restrict__ w,
+                                                                   const bf16* __restrict__ b, int N) {
+    constexpr int C = 256 * NV;
+    pdl_enter();
+    const int row = blockIdx.x * 8 + threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    if (row >= N) return;
+    const uint4* x = reinterpret_cast<const uint4*>(inp + (size_t)row * C) + lane;
+    uint4 xv[NV];
+#pragma unroll
+    for (int j = 0; j < NV; j++) xv[j] = x[32 * j];
+    float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < NV; j++) {
+        s2 = fadd2(s2, fadd2(bf2_f2_v(xv[j].x), bf2_f2_v(xv[j].y)));
+        s2 = fadd2(s2, fadd2(bf2_f2_v(xv[j].z), bf2_f2_v(xv[j].w)));
+    }
+    const float m = warp_sum(s2.x + s2.y) / C;
+    const float2 nm = make_float2(-m, -m);
+    float2 v2 = make_float2(0.f, 0.f);
+    auto sq = [&](uint32_t u) {
+        const float2 d = fadd2(bf2_f2_v(u), nm);
+        v2 = ffma2(d, d, v2);
+    };
+#pragma unroll
+    for (int j = 0; j < NV; j++) {
+        sq(xv[j].x); sq(xv[j].y); sq(xv[j].z); sq(xv[j].w);
+    }
+    const float var = warp_sum(v2.x + v2.y) / C;
+    const float r = rsqrtf(var + 1e-5f);
+    // y = (x r - m r) w + b
+    const float2 r2 = make_float2(r, r), nmr = make_float2(-m * r, -m * r);
+    uint4* y = reinterpret_cast<uint4*>(out + (size_t)row * C) + lane;
+    const uint4* wp = reinterpret_cast<const uint4*>(w) + lane;
+    const uint4* bp = reinterpret_cast<const uint4*>(b) + lane;
+    auto aff = [&](uint32_t xu, uint32_t wu, uint32_t bu) {
+        return f2_bf2(ffma2(ffma2(bf2_f2_v(xu), r2, nmr), bf2_f2_v(wu), bf2_f2_v(bu)));
+    };
+#pragma unroll
+    for (int j = 0; j < NV; j++) {
+        const uint4 wu = __ldg(wp + 32 * j), bu = __ldg(bp + 32 * j);
+        y[32 * j] = make_uint4(aff(xv[j].x, wu.x, bu.x), aff(xv[j].y, wu.y, bu.y), aff(xv[j].z, wu.z, bu.z),
+                               aff(xv[j].w, wu.w, bu.w));
+    }
+    if (lane == 0) {
+        mean[row] = m;
+        rstd[row] = r;
+    }
+}
+
 static int maxv_for(int cv) {
     int per = (cv + 31) / 32;
     return per <= 1 ? 1 : per <= 2 ? 2 : per <= 4 ? 4 : 8;
@@ -354,6 +428,15 @@ void launch_layernorm_forward(DType dt, void* out, float* mean, float* rstd, con
     const int mv = maxv_for(C / VEC);
     const int block = 256, rows = block / 32;
     unsigned g = (unsigned)((N + rows - 1) / rows);
+    if (dt == DT_BF16 && C % 256 == 0 && C <= 768) {
+        const int nv = C / 256;
+#define LNF2(NVV)                                                                                          \
+    launch_pdl(layernorm_forward_bf16_k<NVV>, g, block, 0, s, (bf16*)out, mean, rstd, (const bf16*)inp, \
+               (const bf16*)w, (const bf16*)b, N)
+        if (nv == 1) LNF2(1); else if (nv == 2) LNF2(2); else LNF2(3);
+#undef LNF2
+        return;
+    }
 #define LNF(TT, MV)                                                                            \
     launch_pdl(layernorm_forward_k<TT, MV>, g, block, 0, s, (TT*)out, mean, rstd, (const TT*)inp,        \
                                                     (const TT*)w, (const TT*)b, N, C)
@@ -699,14 +782,19 @@ __global__ void __launch_bounds__(32 * LNW_WARPS, 1) layernorm_backward_warp_k(
     const int G = with_colsum ? 3 : 2;
     uint8_t* ring = lnw_sm + (size_t)warp * LNW_BUF * 3 * ROWB;
     const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
-    Vec16<bf16> wv[NV];
+    // packed fp32 arithmetic on column pairs: lane l's vector j holds columns
+    // (l + 32 j) * 8 + 2 e, + 1 in pair e
+    float2 wf[NV][VEC / 2];
 #pragma unroll
-    for (int j = 0; j < NV; j++) wv[j] = ld16(w + (lane + 32 * j) * VEC);
-    float adw[NV][VEC], adb[NV][VEC], acs[NV][VEC];
+    for (int j = 0; j < NV; j++) {
+        const uint4 u = *reinterpret_cast<const uint4*>(w + (lane + 32 * j) * VEC);
+        wf[j][0] = bf2_f2(u.x); wf[j][1] = bf2_f2(u.y); wf[j][2] = bf2_f2(u.z); wf[j][3] = bf2_f2(u.w);
+    }
+    float2 adw[NV][VEC / 2], adb[NV][VEC / 2], acs[NV][VEC / 2];
 #pragma unroll
     for (int j = 0; j < NV; j++)
 #pragma unroll
-        for (int e = 0; e < VEC; e++) adw[j][e] = adb[j][e] = acs[j][e] = 0.f;
+        for (int e = 0; e < VEC / 2; e++) adw[j][e] = adb[j][e] = acs[j][e] = make_float2(0.f, 0.f);
     // the warp's k-th row is r_begin + warp + k * LNW_WARPS, in slot k % LNW_BUF;
     // one commit group per row (empty groups past the end keep the count)
     auto issue = [&](int k) {
@@ -734,41 +822,53 @@ __global__ void __launch_bounds__(32 * LNW_WARPS, 1) layernorm_backward_warp_k(
         __syncwarp();
         const uint8_t* slot = ring + (size_t)(k % LNW_BUF) * 3 * ROWB;
         const float mu = mean[r], rs = rstd[r];
-        Vec16<bf16> xv[NV], dv[NV];
-        float gs = 0.f, gns = 0.f;
+        const float2 rs2 = make_float2(rs, rs), nmr = make_float2(-mu * rs, -mu * rs);
+        // g = w dy and nhat = (x - mean) rstd per column; the row sums of g and
+        // g nhat; the dw, db column partials
+        float2 g[NV][VEC / 2], nh[NV][VEC / 2];
+        float2 gs2 = make_float2(0.f, 0.f), gns2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < NV; j++) {
-            xv[j] = *reinterpret_cast<const Vec16<bf16>*>(slot + (lane + 32 * j) * 16);
-            dv[j] = *reinterpret_cast<const Vec16<bf16>*>(slot + ROWB + (lane + 32 * j) * 16);
+            const uint4 xu = *reinterpret_cast<const uint4*>(slot + (lane + 32 * j) * 16);
+            const uint4 du = *reinterpret_cast<const uint4*>(slot + ROWB + (lane + 32 * j) * 16);
+            const uint32_t xw[4] = {xu.x, xu.y, xu.z, xu.w}, dw[4] = {du.x, du.y, du.z, du.w};
 #pragma unroll
-            for (int e = 0; e < VEC; e++) {
-                const float g = to_f(wv[j].v[e]) * to_f(dv[j].v[e]);
-                gs += g;
-                gns += g * ((to_f(xv[j].v[e]) - mu) * rs);
+            for (int e = 0; e < VEC / 2; e++) {
+                const float2 d = bf2_f2(dw[e]);
+                g[j][e] = fmul2(wf[j][e], d);
+                nh[j][e] = ffma2(bf2_f2(xw[e]), rs2, nmr);
+                gs2 = fadd2(gs2, g[j][e]);
+                gns2 = ffma2(g[j][e], nh[j][e], gns2);
+                adw[j][e] = ffma2(nh[j][e], d, adw[j][e]);
+                adb[j][e] = fadd2(adb[j][e], d);
             }
         }
+        float gs = gs2.x + gs2.y, gns = gns2.x + gns2.y;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             gs += __shfl_xor_sync(0xffffffffu, gs, o);
             gns += __shfl_xor_sync(0xffffffffu, gns, o);
         }
-        const float gm = gs / C, gnm = gns / C;
+        // dx = rstd (g - mean(g) - nhat mean(g nhat)) = rstd g + c0 + c1 nhat
+        const float c0 = -rs * (gs / C), c1 = -rs * (gns / C);
+        const float2 c02 = make_float2(c0, c0), c12 = make_float2(c1, c1);
         bf16* dx = dinp + (size_t)r * C + lane * VEC;
 #pragma unroll
         for (int j = 0; j < NV; j++) {
-            Vec16<bf16> o, ov;
-            if (accumulate) ov = *reinterpret_cast<const Vec16<bf16>*>(slot + 2 * ROWB + (lane + 32 * j) * 16);
-#pragma unroll
-            for (int e = 0; e < VEC; e++) {
-                const float d = to_f(dv[j].v[e]);
-                const float nh = (to_f(xv[j].v[e]) - mu) * rs;
-                const float val = rs * (to_f(wv[j].v[e]) * d - gm - nh * gnm);
-                o.v[e] = from_f<bf16>(accumulate ? to_f(ov.v[e]) + val : val);
-                adw[j][e] += nh * d;
-                adb[j][e] += d;
-                acs[j][e] += to_f(o.v[e]);
+            uint32_t ow[4] = {0u, 0u, 0u, 0u};
+            if (accumulate) {
+                const uint4 ou = *reinterpret_cast<const uint4*>(slot + 2 * ROWB + (lane + 32 * j) * 16);
+                ow[0] = ou.x; ow[1] = ou.y; ow[2] = ou.z; ow[3] = ou.w;
             }
-            st16(dx + 32 * j * VEC, o);
+            uint32_t res[4];
+#pragma unroll
+            for (int e = 0; e < VEC / 2; e++) {
+                float2 v = ffma2(nh[j][e], c12, ffma2(g[j][e], rs2, c02));
+                if (accumulate) v = fadd2(bf2_f2(ow[e]), v);
+                res[e] = f2_bf2(v);
+                acs[j][e] = fadd2(acs[j][e], bf2_f2(res[e]));
+            }
+            *reinterpret_cast<uint4*>(dx + 32 * j * VEC) = make_uint4(res[0], res[1], res[2], res[3]);
         }
         __syncwarp();  // every lane has read the slot before it is refilled
     }
@@ -780,11 +880,11 @@ __global__ void __launch_bounds__(32 * LNW_WARPS, 1) layernorm_backward_warp_k(
 #pragma unroll
     for (int j = 0; j < NV; j++)
 #pragma unroll
-        for (int e = 0; e < VEC; e++) {
-            const int c = (lane + 32 * j) * VEC + e;
-            mine[c] = adw[j][e];
-            mine[C + c] = adb[j][e];
-            if (with_colsum) mine[2 * C + c] = acs[j][e];
+        for (int e = 0; e < VEC / 2; e++) {
+            const int c = (lane + 32 * j) * VEC + 2 * e;
+            *reinterpret_cast<float2*>(mine + c) = adw[j][e];
+            *reinterpret_cast<float2*>(mine + C + c) = adb[j][e];
+            if (with_colsum) *reinterpret_cast<float2*>(mine + 2 * C + c) = acs[j][e];
         }
     __syncthreads();
     float* dst = part + (size_t)blockIdx.x * G * C;

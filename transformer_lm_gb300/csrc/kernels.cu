@@ -181,6 +181,56 @@ __global__ void __launch_bounds__(1024) token_scan_k(const int* __restrict__ cou
     if (tid == nt - 1) offsets[Vp] = base;
 }
 
+// the same scan with the counts staged in shared memory: the global reads and
+// writes are coalesced, and each thread scans a contiguous run from shared memory
+// (Vp ints of dynamic shared memory)
+__global__ void __launch_bounds__(1024) token_scan_smem_k(const int* __restrict__ counts, int Vp,
+                                                          int* __restrict__ offsets,
+                                                          int* __restrict__ cursor) {
+    pdl_enter();
+    extern __shared__ int tsm[];
+    __shared__ int warp_tot[32];
+    const int tid = threadIdx.x, nt = blockDim.x;
+    for (int v = tid; v < Vp; v += nt) tsm[v] = counts[v];
+    __syncthreads();
+    const int per = (Vp + nt - 1) / nt;
+    const int lo = min(Vp, tid * per), hi = min(Vp, lo + per);
+    int local = 0;
+    for (int v = lo; v < hi; v++) local += tsm[v];
+    const int lane = tid & 31, warp = tid >> 5;
+    int x = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = (lane < nt / 32) ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        warp_tot[lane] = w;
+    }
+    __syncthreads();
+    int base = (warp > 0 ? warp_tot[warp - 1] : 0) + x - local;
+    for (int v = lo; v < hi; v++) {
+        const int c = tsm[v];
+        tsm[v] = base;
+        base += c;
+    }
+    if (tid == nt - 1) offsets[Vp] = base;
+    __syncthreads();
+    for (int v = tid; v < Vp; v += nt) {
+        const int o = tsm[v];
+        offsets[v] = o;
+        cursor[v] = o;
+    }
+}
+
 __global__ void token_scatter_k(const int* __restrict__ tok, int n, int* cursor,
                                 int* __restrict__ order) {
     pdl_enter();
@@ -266,7 +316,17 @@ void launch_encoder_backward(DType dt, void* dwte, void* dwpe, const void* dout,
         launch_pdl(encoder_backward_wpe_k<float>, g, 256, 0, s, (float*)dwpe, (const float*)dout, B, T, C);
     launch_zero(ws_counts, sizeof(int) * (size_t)Vp, s);
     launch_pdl(token_count_k, grid_for(n, 256), 256, 0, s, tok, n, ws_counts);
-    launch_pdl(token_scan_k, 1, 1024, 0, s, ws_counts, Vp, ws_offsets, ws_cursor);
+    const size_t scan_smem = sizeof(int) * (size_t)Vp;
+    if (scan_smem <= 200 * 1024) {
+        static size_t done = 0;
+        if (scan_smem > done) {
+            cudaFuncSetAttribute(token_scan_smem_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)scan_smem);
+            done = scan_smem;
+        }
+        launch_pdl(token_scan_smem_k, 1, 1024, scan_smem, s, ws_counts, Vp, ws_offsets, ws_cursor);
+    } else {
+        launch_pdl(token_scan_k, 1, 1024, 0, s, ws_counts, Vp, ws_offsets, ws_cursor);
+    }
     launch_pdl(token_scatter_k, grid_for(n, 256), 256, 0, s, tok, n, ws_cursor, ws_order);
     launch_pdl(token_rank_k, grid_for(n, 256), 256, 0, s, tok, ws_offsets, ws_order, n, ws_sorted);
     unsigned gw = (unsigned)((Vp + 7) / 8);
@@ -1178,10 +1238,13 @@ void launch_colsum_accum(DType dt, void* dbias, const void* dout, int M, int N, 
 // loss = log(sum exp(l - max)) + max - l[target], and the logits are replaced
 // by dlogits = (p - 1[i == target]) * dloss; the padded columns [V, Vp) get 0.
 // Pass 1 reads the row once (online max/sum per 16-byte vector); pass 2
-// re-reads it (an L2 hit: each block's row is only ~100 KB) and writes.
+// re-reads it (an L2 hit: each block's row is only ~100 KB) and writes. Both
+// passes issue CLS_UNROLL independent 16-byte loads per thread before using
+// them, so enough bytes are in flight to cover the memory latency.
 // exp(x - m) is taken as 2^(x log2(e) - m log2(e)): one FMA and the hardware
 // ex2 per element (relative error ~2^-22).
 constexpr int CLS_BLOCK = 512;
+constexpr int CLS_UNROLL = 4;
 constexpr float CLS_LOG2E = 1.4426950408889634f;
 
 DEVI float cls_exp2(float x) {
@@ -1191,7 +1254,7 @@ DEVI float cls_exp2(float x) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(CLS_BLOCK) classifier_k(T* __restrict__ logits,
+__global__ void __launch_bounds__(CLS_BLOCK, 3) classifier_k(T* __restrict__ logits,
                                                           float* __restrict__ losses,
                                                           const int* __restrict__ targets, int V,
                                                           int Vp, float dloss) {
@@ -1205,8 +1268,7 @@ __global__ void __launch_bounds__(CLS_BLOCK) classifier_k(T* __restrict__ logits
     if (threadIdx.x == 0) s_tlogit = to_f(x[tgt]);
     const int nvec = Vp / VEC;
     float m = -INFINITY, sum = 0.f;
-    for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
-        Vec16<T> a = ld16(x + (size_t)vi * VEC);
+    auto update = [&](const Vec16<T>& a, int vi) {
         float f[VEC];
         float lm = -INFINITY;
 #pragma unroll
@@ -1214,14 +1276,23 @@ __global__ void __launch_bounds__(CLS_BLOCK) classifier_k(T* __restrict__ logits
             f[k] = (vi * VEC + k < V) ? to_f(a.v[k]) : -INFINITY;
             lm = fmaxf(lm, f[k]);
         }
-        if (lm == -INFINITY) continue;
+        if (lm == -INFINITY) return;
         const float nm = fmaxf(m, lm), nl = -nm * CLS_LOG2E;
         float acc = 0.f;
 #pragma unroll
         for (int k = 0; k < VEC; k++) acc += cls_exp2(fmaf(f[k], CLS_LOG2E, nl));
         sum = sum * cls_exp2((m - nm) * CLS_LOG2E) + acc;
         m = nm;
+    };
+    int vi = threadIdx.x;
+    for (; vi + (CLS_UNROLL - 1) * CLS_BLOCK < nvec; vi += CLS_UNROLL * CLS_BLOCK) {
+        Vec16<T> a[CLS_UNROLL];
+#pragma unroll
+        for (int u = 0; u < CLS_UNROLL; u++) a[u] = ld16(x + (size_t)(vi + u * CLS_BLOCK) * VEC);
+#pragma unroll
+        for (int u = 0; u < CLS_UNROLL; u++) update(a[u], vi + u * CLS_BLOCK);
     }
+    for (; vi < nvec; vi += CLS_BLOCK) update(ld16(x + (size_t)vi * VEC), vi);
     const int lane = threadIdx.x & 31, warp = threadIdx.x / 32, nw = blockDim.x / 32;
     float wm = warp_max(m);
     if (lane == 0) s_max[warp] = wm;
@@ -1233,20 +1304,29 @@ __global__ void __launch_bounds__(CLS_BLOCK) classifier_k(T* __restrict__ logits
     const float bs = warp_sum(lane < nw ? s_sum[lane] : 0.f);
     if (threadIdx.x == 0) losses[row] = logf(bs) + bm - s_tlogit;
     const float inv = 1.f / bs, bl = -bm * CLS_LOG2E;
-    for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
-        Vec16<T> a = ld16(x + (size_t)vi * VEC), o;
+    auto grad = [&](const Vec16<T>& a, int vi) {
+        Vec16<T> o;
 #pragma unroll
         for (int k = 0; k < VEC; k++) {
-            int i = vi * VEC + k;
+            const int i = vi * VEC + k;
             float d = 0.f;
             if (i < V) {
-                float p = cls_exp2(fmaf(to_f(a.v[k]), CLS_LOG2E, bl)) * inv;
+                const float p = cls_exp2(fmaf(to_f(a.v[k]), CLS_LOG2E, bl)) * inv;
                 d = (p - (i == tgt ? 1.f : 0.f)) * dloss;
             }
             o.v[k] = from_f<T>(d);
         }
         st16_cs(x + (size_t)vi * VEC, o);
+    };
+    vi = threadIdx.x;
+    for (; vi + (CLS_UNROLL - 1) * CLS_BLOCK < nvec; vi += CLS_UNROLL * CLS_BLOCK) {
+        Vec16<T> a[CLS_UNROLL];
+#pragma unroll
+        for (int u = 0; u < CLS_UNROLL; u++) a[u] = ld16(x + (size_t)(vi + u * CLS_BLOCK) * VEC);
+#pragma unroll
+        for (int u = 0; u < CLS_UNROLL; u++) grad(a[u], vi + u * CLS_BLOCK);
     }
+    for (; vi < nvec; vi += CLS_BLOCK) grad(ld16(x + (size_t)vi * VEC), vi);
 }
 
 void launch_classifier(DType dt, void* logits, float* losses, const int* targets, int BT, int V,

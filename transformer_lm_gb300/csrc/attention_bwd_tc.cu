@@ -111,9 +111,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t dp_full = bars + 8u * (B0 + 2), dp_empty = bars + 8u * (B0 + 3);
     const uint32_t p_full = bars + 8u * (B0 + 4), p_empty = bars + 8u * (B0 + 5);
     const uint32_t ds_full = bars + 8u * (B0 + 6), ds_empty = bars + 8u * (B0 + 7);
-    const uint32_t acc_full = bars + 8u * (B0 + 8), acc_empty = bars + 8u * (B0 + 9);
-    const uint32_t drain = bars + 8u * (B0 + 10);
-    constexpr int NBARS = B0 + 11;
+    // per accumulator buffer (DQ alternates two; DKV's dV | dK fill the rest of TMEM)
+    auto acc_full = [&](int b) { return bars + 8u * (B0 + 8 + b); };
+    auto acc_empty = [&](int b) { return bars + 8u * (B0 + 10 + b); };
+    const uint32_t drain = bars + 8u * (B0 + 12);
+    constexpr int NBARS = B0 + 13;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars_ptr + 8 * NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars_ptr + 8 * NBARS + 4);
     int* n_issued_smem = reinterpret_cast<int*>(bars_ptr + 8 * NBARS + 8);   // ring loads issued
@@ -140,8 +142,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_init(p_empty, 1);
         mbar_init(ds_full, CW);
         mbar_init(ds_empty, 1);
-        mbar_init(acc_full, 1);
-        mbar_init(acc_empty, CW);
+        for (int b = 0; b < 2; b++) {
+            mbar_init(acc_full(b), 1);
+            mbar_init(acc_empty(b), CW);
+        }
         mbar_init(drain, 2);
         *abort_flag = 0;
         *n_issued_smem = 0;
@@ -294,8 +298,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (ok) umma_commit_warp<1>(x_empty(xb));  // the item's last reads of its fixed tiles
             } else {
-                // the previous item's accumulators have been read out
-                if (!mbar_wait_warp(acc_empty, (uint32_t)((t & 1) ^ 1), abort_flag)) break;
+                // DQ alternates two accumulator buffers over the items; the buffer's
+                // previous item has been read out
+                const int ab = DKV ? 0 : (t & 1);
+                const uint32_t acc_par = DKV ? (uint32_t)(t & 1) : (uint32_t)((t >> 1) & 1);
+                if (!mbar_wait_warp(acc_empty(ab), acc_par ^ 1u, abort_flag)) break;
                 tc_fence_after();
                 for (int u = 0; u < n; u++, g++) {
                     const uint32_t par = (uint32_t)(g & 1);
@@ -308,11 +315,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (!mbar_wait_warp(ds_full, par, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     // DKV: dK += dS^T Q; DQ: dQ += dS K
-                    issue_acc(tmem_base + (DKV ? TM_A1 : TM_A0), tmem_base + TM_DS, ybuf(g, 0), u > 0);
+                    issue_acc(tmem_base + (DKV || ab ? TM_A1 : TM_A0), tmem_base + TM_DS, ybuf(g, 0), u > 0);
                     umma_commit_warp<1>(ds_empty);
                     umma_commit_warp<1>(st_empty(g % STAGES));  // this warp's reads of the stage
                 }
-                if (ok) umma_commit_warp<1>(acc_full);
+                if (ok) umma_commit_warp<1>(acc_full(ab));
             }
         }
     } else if (warp >= 2 && warp < 2 + CW) {
@@ -330,6 +337,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         static_assert(COLS == 32, "one 32-column TMEM load per operand");
         int g = 0;
         bool ok = true;
+        // Item t's accumulators are read out after the first block of item t + 1
+        // (whose S and dP were computed under item t's last block), so the
+        // wait for item t's last MMAs and the read-out overlap the tensor work
+        // of item t + 1. The columns split over the column groups: DKV
+        // [dV 64 | dK 64] at TM_A0; DQ dQ 64 at TM_A0 or TM_A1 (item parity).
+        int pend_t = -1;
+        Item pend_it{};
+        auto epilogue = [&](int t, const Item& it) -> bool {
+            const int ab = DKV ? 0 : (t & 1);
+            const uint32_t acc_par = DKV ? (uint32_t)(t & 1) : (uint32_t)((t >> 1) & 1);
+            if (!wait_warp(acc_full(ab), acc_par)) return false;
+            tc_fence_after();
+            constexpr int W = (DKV ? 128 : 64) / CQ;  // columns per thread
+            const int a0 = cq * W;                    // first accumulator column
+            const uint32_t tacc = tmem_base + lane_off + (ab ? TM_A1 : TM_A0) + (uint32_t)a0;
+            float v[W];
+#pragma unroll
+            for (int ch = 0; ch < W; ch += 16)
+                tmem_ld16(tacc + (uint32_t)ch, *reinterpret_cast<float(*)[16]>(v + ch));
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty(ab));  // the buffer's next item may overwrite them
+            const int row = it.r0 + r;
+            if (row < T) {
+                const bool is_k = DKV && a0 >= 64;
+                const float sc = (!DKV || is_k) ? a.scale : 1.f;
+                const int col = DKV ? (is_k ? C + it.h * HSZ : 2 * C + it.h * HSZ) + (a0 % 64)
+                                    : it.h * HSZ + a0;
+                bf16* dst = a.dqkv + ((size_t)it.b * T + row) * 3 * C + col;
+#pragma unroll
+                for (int d = 0; d < W; d += 8) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        __nv_bfloat162 pr = __floats2bfloat162_rn(v[d + 2 * e] * sc, v[d + 2 * e + 1] * sc);
+                        pk[e] = *reinterpret_cast<uint32_t*>(&pr);
+                    }
+                    *reinterpret_cast<uint4*>(dst + d) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+            }
+            return true;
+        };
         for (int t = 0, idx = item_of(0); ok && idx < a.items; idx = item_of(++t)) {
             const Item it = decode_item<DKV>(a, idx);
             const int row = it.r0 + r;  // key (DKV) or query (DQ)
@@ -423,40 +472,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ds_full);
-            }
-            if (!ok) break;
-            // epilogue: the accumulator columns split over the column groups.
-            // DKV: [dV 64 | dK 64] at TM_A0; DQ: dQ 64 at TM_A0
-            if (!wait_warp(acc_full, (uint32_t)(t & 1))) { ok = false; break; }
-            tc_fence_after();
-            constexpr int W = (DKV ? 128 : 64) / CQ;  // columns per thread
-            const int a0 = cq * W;                    // first accumulator column
-            float v[W];
-#pragma unroll
-            for (int ch = 0; ch < W; ch += 16)
-                tmem_ld16(tmem_base + lane_off + TM_A0 + (uint32_t)(a0 + ch),
-                          *reinterpret_cast<float(*)[16]>(v + ch));
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty);  // the next item may overwrite them
-            if (row < T) {
-                const bool is_k = DKV && a0 >= 64;
-                const float sc = (!DKV || is_k) ? a.scale : 1.f;
-                const int col = DKV ? (is_k ? C + it.h * HSZ : 2 * C + it.h * HSZ) + (a0 % 64)
-                                    : it.h * HSZ + a0;
-                bf16* dst = a.dqkv + ((size_t)it.b * T + row) * 3 * C + col;
-#pragma unroll
-                for (int d = 0; d < W; d += 8) {
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        __nv_bfloat162 pr = __floats2bfloat162_rn(v[d + 2 * e] * sc, v[d + 2 * e + 1] * sc);
-                        pk[e] = *reinterpret_cast<uint32_t*>(&pr);
-                    }
-                    *reinterpret_cast<uint4*>(dst + d) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                if (u == 0 && pend_t >= 0) {
+                    if (!epilogue(pend_t, pend_it)) { ok = false; break; }
+                    pend_t = -1;
                 }
             }
+            if (!ok) break;
+            pend_t = t;
+            pend_it = it;
         }
+        // the last item's read-out
+        if (ok && pend_t >= 0) epilogue(pend_t, pend_it);
     }
 
     __syncthreads();

@@ -515,44 +515,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-// D_i = dO_i . O_i for every (b, h, i), eight threads per row (16-byte
-// loads); a thread group takes ROWDOT_R rows, nrows / ROWDOT_R apart, and
-// issues all their loads before the first product
-constexpr int ROWDOT_R = 4;
-
+// D_i = dO_i . O_i for every (b, h, i), eight threads per row (16-byte loads)
 __global__ void rowdot64_k(float* __restrict__ D, const bf16* __restrict__ dout,
                            const bf16* __restrict__ out, int T, int C, int NH, int nrows) {
     pdl_enter();
     const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-    const int part = idx & 7;
-    const int span = (nrows + ROWDOT_R - 1) / ROWDOT_R;  // rows between a group's rows
-    Vec16<bf16> g[ROWDOT_R], o[ROWDOT_R];
+    const int row = idx >> 3, part = idx & 7;
+    float s = 0.f;
+    if (row < nrows) {
+        const int bh = row / T, t = row % T;
+        const int b = bh / NH, h = bh % NH;
+        const size_t off = ((size_t)b * T + t) * C + (size_t)h * HSZ + part * 8;
+        const Vec16<bf16> g = ld16(dout + off), o = ld16(out + off);
 #pragma unroll
-    for (int j = 0; j < ROWDOT_R; j++) {
-        const int row = (idx >> 3) + j * span;
-        if ((idx >> 3) < span && row < nrows) {
-            const int bh = row / T, t = row % T;
-            const int b = bh / NH, h = bh % NH;
-            const size_t off = ((size_t)b * T + t) * C + (size_t)h * HSZ + part * 8;
-            g[j] = ld16(dout + off);
-            o[j] = ld16(out + off);
-        }
+        for (int e = 0; e < 8; e++) s = fmaf(to_f(g.v[e]), to_f(o.v[e]), s);
     }
-#pragma unroll
-    for (int j = 0; j < ROWDOT_R; j++) {
-        const int row = (idx >> 3) + j * span;
-        float s = 0.f;
-        if ((idx >> 3) < span && row < nrows) {
-            const bf16* gp = reinterpret_cast<const bf16*>(&g[j]);
-            const bf16* op = reinterpret_cast<const bf16*>(&o[j]);
-#pragma unroll
-            for (int e = 0; e < 8; e++) s = fmaf(to_f(gp[e]), to_f(op[e]), s);
-        }
-        s += __shfl_xor_sync(0xffffffffu, s, 4);
-        s += __shfl_xor_sync(0xffffffffu, s, 2);
-        s += __shfl_xor_sync(0xffffffffu, s, 1);
-        if ((idx >> 3) < span && row < nrows && part == 0) D[row] = s;
-    }
+    s += __shfl_xor_sync(0xffffffffu, s, 4);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    if (row < nrows && part == 0) D[row] = s;
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -612,8 +593,7 @@ int launch_flash_backward_tc(void* dqkv, const void* dout, const void* qkv, cons
     if (rc != GPT2_OK) return rc;
     const int nrows = B * NH * T;
     note_launch(3);
-    const int span = (nrows + ROWDOT_R - 1) / ROWDOT_R;
-    launch_pdl(rowdot64_k, dim3((span * 8 + 255) / 256), dim3(256), 0, s, D, (const bf16*)dout,
+    launch_pdl(rowdot64_k, dim3((nrows * 8 + 255) / 256), dim3(256), 0, s, D, (const bf16*)dout,
                (const bf16*)out, T, C, NH, nrows);
     BwdArgs a;
     a.dqkv = (bf16*)dqkv;

@@ -191,7 +191,16 @@ __global__ void __launch_bounds__(1024) token_scan_smem_k(const int* __restrict_
     extern __shared__ int tsm[];
     __shared__ int warp_tot[32];
     const int tid = threadIdx.x, nt = blockDim.x;
-    for (int v = tid; v < Vp; v += nt) tsm[v] = counts[v];
+    // eight loads in flight per thread
+    int v0 = tid;
+    for (; v0 + 7 * nt < Vp; v0 += 8 * nt) {
+        int c[8];
+#pragma unroll
+        for (int u = 0; u < 8; u++) c[u] = counts[v0 + u * nt];
+#pragma unroll
+        for (int u = 0; u < 8; u++) tsm[v0 + u * nt] = c[u];
+    }
+    for (; v0 < Vp; v0 += nt) tsm[v0] = counts[v0];
     __syncthreads();
     const int per = (Vp + nt - 1) / nt;
     const int lo = min(Vp, tid * per), hi = min(Vp, lo + per);

@@ -883,14 +883,22 @@ __global__ void __launch_bounds__(32 * LNW_WARPS, 1) layernorm_backward_warp_k(
     };
 #pragma unroll
     for (int k = 0; k < LNW_BUF - 1; k++) issue(k);
+    // lane l holds the mean and rstd of the warp's row k0 + l (k0 = k rounded
+    // down to a multiple of 32), read a batch at a time ahead of their rows
+    float mu_l = 0.f, rs_l = 0.f;
     for (int k = 0;; k++) {
         const int r = r_begin + warp + k * LNW_WARPS;
         if (r >= r_end) break;
+        if ((k & 31) == 0) {
+            const int rr = r + lane * LNW_WARPS;
+            mu_l = rr < r_end ? mean[rr] : 0.f;
+            rs_l = rr < r_end ? rstd[rr] : 0.f;
+        }
         issue(k + LNW_BUF - 1);
         asm volatile("cp.async.wait_group %0;" ::"n"(LNW_BUF - 1) : "memory");
         __syncwarp();
         const uint8_t* slot = ring + (size_t)(k % LNW_BUF) * 3 * ROWB;
-        const float mu = mean[r], rs = rstd[r];
+        const float mu = __shfl_sync(0xffffffffu, mu_l, k & 31), rs = __shfl_sync(0xffffffffu, rs_l, k & 31);
         const float2 rs2 = make_float2(rs, rs), nmr = make_float2(-mu * rs, -mu * rs);
         // g = w dy and nhat = (x - mean) rstd per column; the row sums of g and
         // g nhat; the dw, db column partials

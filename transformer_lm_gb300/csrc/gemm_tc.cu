@@ -558,10 +558,10 @@ static bool make_map_3d_f32(CUtensorMap* m, void* ptr, int N, int M, int S, uint
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// D[m, n] += sum over s = 0..S-1 (in order) of ws[s][m][n]; 8 columns per thread
+// D[m, n] (+)= sum over s = 0..S-1 (in order) of ws[s][m][n]; 8 columns per thread
 __global__ void __launch_bounds__(256) splitk_reduce_k(bf16* __restrict__ D, long long ldd,
                                                        const float* __restrict__ ws, int M, int N,
-                                                       int S) {
+                                                       int S, int accumulate) {
     pdl_enter();
     const int n8 = N / 8;
     const long long total = (long long)M * n8;
@@ -584,21 +584,27 @@ __global__ void __launch_bounds__(256) splitk_reduce_k(bf16* __restrict__ D, lon
             acc[4] += x1.x; acc[5] += x1.y; acc[6] += x1.z; acc[7] += x1.w;
         }
         bf16* d = D + (size_t)m * ldd + c;
-        Vec16<bf16> o = ld16(d);
+        Vec16<bf16> o;
+        if (accumulate) {
+            o = ld16(d);
 #pragma unroll
-        for (int e = 0; e < 8; e++) o.v[e] = from_f<bf16>(to_f(o.v[e]) + acc[e]);
+            for (int e = 0; e < 8; e++) o.v[e] = from_f<bf16>(to_f(o.v[e]) + acc[e]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; e++) o.v[e] = from_f<bf16>(acc[e]);
+        }
         st16(d, o);
     }
 }
 
 static int launch_splitk_reduce(bf16* D, long long ldd, const float* ws, int M, int N, int S,
-                                cudaStream_t s) {
+                                int accumulate, cudaStream_t s) {
     const long long total = (long long)M * (N / 8);
     long long blocks = (total + 255) / 256;
     const long long cap = (long long)num_sms() * 8;
     if (blocks > cap) blocks = cap;
     note_launch(1);
-    launch_pdl(splitk_reduce_k, dim3((unsigned)blocks), dim3(256), 0, s, D, ldd, ws, M, N, S);
+    launch_pdl(splitk_reduce_k, dim3((unsigned)blocks), dim3(256), 0, s, D, ldd, ws, M, N, S, accumulate);
     return GPT2_OK;
 }
 
@@ -752,11 +758,14 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
     a.splits = 1;
     a.kb_per = a.num_kb;
     // Split-K for "+=" products with fewer tiles than CTA slots (the weight
-    // grads): each K range writes fp32 partials to the scratch and a second
-    // kernel adds them to D in range order (deterministic). The range count
-    // minimises a cost model: waves x (k-blocks per range + 6) x 0.25 us per
-    // 256-wide k-block, plus the partials' traffic at 5 TB/s.
-    if (p.epi == EPI_ACCUM && dt == DT_BF16 && p.ws && p.ws_floats > 0) {
+    // grads) and for long-K plain stores without bias whose tiles fill the last
+    // wave of CTA pairs poorly: each K range writes fp32 partials to the
+    // scratch and a second kernel adds them (to D, or into D) in range order
+    // (deterministic). The range count minimises a cost model: waves x
+    // (k-blocks per range + 6) x 0.25 us per 256-wide k-block, plus the
+    // partials' traffic at 5 TB/s.
+    const bool split_ok = p.epi == EPI_ACCUM || (p.epi == EPI_STORE && !p.bias && BN == 256);
+    if (split_ok && dt == DT_BF16 && p.ws && p.ws_floats > 0) {
         const long long units = cg == 2 ? sms / 2 : sms;
         const long long tiles = ((nm + cg - 1) / cg) * a.num_n;
         const double t_kb = 0.25 * BN / 256.0, mn = (double)p.M * p.N;
@@ -794,7 +803,7 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
         const int rc = cg == 2 ? dispatch_epi<256, 0, 2>(EPI_SPLITK, mp, a, s)
                                : dispatch_epi<256, 0, 1>(EPI_SPLITK, mp, a, s);
         if (rc != GPT2_OK) return rc;
-        return launch_splitk_reduce((bf16*)p.D, p.ldd, p.ws, p.M, p.N, a.splits, s);
+        return launch_splitk_reduce((bf16*)p.D, p.ldd, p.ws, p.M, p.N, a.splits, p.epi == EPI_ACCUM ? 1 : 0, s);
     }
     // output boxes: one 128-byte chunk x 32 rows (an epilogue warp's store)
     const int OCO = tc::ROWB / osz;

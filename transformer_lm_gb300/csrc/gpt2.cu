@@ -92,7 +92,9 @@ struct Model {
     float *ln1_mean, *ln1_rstd, *ln2_mean, *ln2_rstd, *lnf_mean, *lnf_rstd, *lse, *losses, *mean_loss;
     void *dresidual, *dbtc, *dbt4c;
     float *attn_D, *ws;
-    float* gemm_ws = nullptr;  // split-K partials of the weight-gradient GEMMs
+    float* gemm_ws = nullptr;  // split-K partials of the weight-gradient GEMMs (side stream)
+    float* gemm_ws_main = nullptr;  // split-K partials of the main stream's products
+    bool in_side = false;           // launches are being issued for the side stream
     // LayerNorm and bias gradients as partial rows, reduced by one launch at
     // the end of the backward (areas: 2L+1 LayerNorms [ln1 of l = 2l, ln2 of
     // l = 2l+1, lnf = 2L], their column sums when not fused, fc and qkv biases)
@@ -153,9 +155,15 @@ int gemm(Model* m, int epi, const void* A, long long lda, int a_km, const void* 
     p.B = B; p.ldb = ldb; p.b_kmajor = b_km;
     p.D = D; p.ldd = ldd; p.bias = bias; p.aux = aux; p.ldaux = ldaux; p.D2 = D2;
     p.M = M; p.N = N; p.K = K; p.epi = epi;
-    if (m->gemm_ws) {
-        p.ws = m->gemm_ws;
-        p.ws_floats = gemm_ws_floats(m->C);
+    // each stream has its own split-K scratch, so concurrent products never share one
+    if (m->in_side) {
+        if (m->gemm_ws) {
+            p.ws = m->gemm_ws;
+            p.ws_floats = gemm_ws_floats(m->C);
+        }
+    } else if (m->gemm_ws_main) {
+        p.ws = m->gemm_ws_main;
+        p.ws_floats = gemm_ws_main_floats((size_t)m->B * m->T, m->C);
     }
     int rc;
     int ti = tbegin(m, FAM_GEMM, 2.0 * M * N * K);
@@ -269,6 +277,7 @@ int alloc_acts(Model* m, int B, int T) {
         {&m->dbt4c, BT * 4 * C * es}, {(void**)&m->attn_D, (size_t)B * NH * T * 4},
         {(void**)&m->ws, 4 * std::max(layernorm_backward_ws_floats(m->C), colsum_ws_floats(4 * m->C))},
         {(void**)&m->gemm_ws, 4 * gemm_ws_floats(m->C)},
+        {(void**)&m->gemm_ws_main, 4 * std::max(gemm_ws_floats(m->C), gemm_ws_main_floats(BT, m->C))},
         {(void**)&m->enc_counts, (size_t)m->Vp * 4}, {(void**)&m->enc_offsets, ((size_t)m->Vp + 1) * 4},
         {(void**)&m->enc_cursor, (size_t)m->Vp * 4}, {(void**)&m->enc_order, BT * 4},
         {(void**)&m->enc_sorted, BT * 4},
@@ -434,7 +443,9 @@ int run_backward(Model* m) {
     auto on_side = [&](auto&& f) -> int {
         cudaStream_t keep = m->stream;
         m->stream = side;
+        m->in_side = true;
         const int rc = f();
+        m->in_side = false;
         m->stream = keep;
         return rc;
     };

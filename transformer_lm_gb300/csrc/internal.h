@@ -45,6 +45,8 @@ struct GemmParams {
 
 // fp32 split-K scratch the model gives its GEMMs: four (4C x C) slices
 inline size_t gemm_ws_floats(int C) { return (size_t)16 * C * C; }
+// the main stream's split-K scratch: three K ranges of a (B*T) x C product
+inline size_t gemm_ws_main_floats(size_t BT, int C) { return (size_t)3 * BT * C; }
 
 // SIMT (FP32 FMA) GEMM, dtype = element type of A, B, D, bias, aux.
 int gemm_simt(const GemmParams& p, DType dt, cudaStream_t s);

@@ -102,6 +102,33 @@ def test_gemm_split_k_accumulate_matches_oracle(shape, a_km, b_km):
     assert np.array_equal(outs[0], outs[1])
 
 
+@pytest.mark.parametrize("shape,a_km,b_km", [((2048, 768, 12288), 1, 0), ((1024, 264, 16384), 1, 1),
+                                              ((2048, 520, 16384), 0, 0), ((8192, 768, 6400), 1, 0)],
+                         ids=lambda x: "x".join(map(str, x)) if isinstance(x, tuple) else str(x))
+def test_gemm_split_k_store_matches_oracle(shape, a_km, b_km):
+    """D = A B^T without bias over a long K with a scratch (the classifier's
+    dlnf shape family): K may be split into ranges whose fp32 partials are
+    summed in order and stored, so D's previous contents must not leak in; the
+    result must match the oracle and repeat bit for bit."""
+    import torch
+    M, N, K = shape
+    A, B, bias, aux, D0 = _operands(M, N, K, 31 + M + K, True)
+    ref = oracle.matmul_forward(A, B, None)
+    sA, lda = _stored(A, a_km)
+    sB, ldb = _stored(B, b_km)
+    dA, dB = dev(sA, "bf16"), dev(sB, "bf16")
+    ws = torch.empty(3 * M * N + 64, dtype=torch.float32, device="cuda")
+    outs = []
+    for _ in range(2):
+        D = dev(D0 * 1e3, "bf16")  # stale contents a += would keep
+        G.gpt2_gemm(G.GPT2_BF16, 1, "store", dA, lda, a_km, dB, ldb, b_km, D, N, M=M, N=N, K=K,
+                    ws=ws, ws_floats=ws.numel())
+        G.gpt2_device_status()
+        outs.append(host(D))
+    assert rel_to_max(outs[0], ref) < 1e-2
+    assert np.array_equal(outs[0], outs[1])
+
+
 @pytest.mark.parametrize("mode", MODES, ids=lambda m: f"{m[0]}-tc{m[1]}")
 @pytest.mark.parametrize("epi", ["gelu", "resid", "gelu_bwd", "accum"])
 @pytest.mark.parametrize("shape", [(300, 392, 200), (1024, 392, 200), (2048, 264, 520)],

@@ -627,7 +627,7 @@ static int launch_tc(const Maps& mp, const tc::Args& a, cudaStream_t s) {
         attr_done = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[3];
     cfg.blockDim = dim3(tc::NUM_THREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = s;
@@ -654,11 +654,7 @@ static int launch_tc(const Maps& mp, const tc::Args& a, cudaStream_t s) {
         const long long ncl = supers < max_clusters ? supers : max_clusters;
         cfg.gridDim = dim3((unsigned)(ncl * 2));
     }
-    if (pdl_enabled()) {
-        attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
-        cfg.numAttrs++;
-    }
+    cfg.numAttrs += launch_attrs(attr + cfg.numAttrs);
     note_launch(1);
     if (cudaLaunchKernelEx(&cfg, kern, mp.a, mp.b, mp.d, mp.d2, a) != cudaSuccess)
         return GPT2_ERR_CUDA;

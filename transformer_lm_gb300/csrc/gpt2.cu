@@ -431,6 +431,15 @@ int run_backward(Model* m) {
     const bool par = m->side != nullptr && !m->timing.on;
     cudaStream_t side = par ? m->side : s;
     int evi = 0;
+    // the main-stream chain launches at the device's greatest priority, the
+    // side stream's at the default one (restored on every return)
+    struct PriorityScope {
+        explicit PriorityScope(int p) { set_launch_priority(p); }
+        ~PriorityScope() { set_launch_priority(0); }
+    };
+    int prio_least = 0, prio_greatest = 0;
+    if (par && cudaDeviceGetStreamPriorityRange(&prio_least, &prio_greatest) != cudaSuccess) prio_greatest = 0;
+    PriorityScope prio_scope(par ? prio_greatest : 0);
     // a point on one stream that the other must pass before going on
     auto edge = [&](cudaStream_t from, cudaStream_t to) -> int {
         if (!par) return GPT2_OK;
@@ -444,7 +453,10 @@ int run_backward(Model* m) {
         cudaStream_t keep = m->stream;
         m->stream = side;
         m->in_side = true;
+        const int keep_prio = launch_priority();
+        set_launch_priority(0);
         const int rc = f();
+        set_launch_priority(keep_prio);
         m->in_side = false;
         m->stream = keep;
         return rc;

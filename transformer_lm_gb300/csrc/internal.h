@@ -161,6 +161,27 @@ int num_sms();
 // off): the kernel may be scheduled while the previous one drains, and waits
 // for it in pdl_enter().
 bool pdl_enabled();
+// Scheduling priority of the launches issued from now on by this thread (0:
+// the stream's own). The backward raises it for its main-stream chain, so
+// that SMs freed by a finishing kernel go to the critical path first.
+int launch_priority();
+void set_launch_priority(int priority);
+// the attributes every launch of the library carries: programmatic stream
+// serialization (unless turned off) and the current priority; returns the count
+inline unsigned launch_attrs(cudaLaunchAttribute* attr) {
+    unsigned n = 0;
+    if (pdl_enabled()) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        n++;
+    }
+    if (const int pr = launch_priority()) {
+        attr[n].id = cudaLaunchAttributePriority;
+        attr[n].val.priority = pr;
+        n++;
+    }
+    return n;
+}
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                               cudaStream_t s, Args&&... args) {
@@ -169,11 +190,9 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
     cfg.attrs = attr;
-    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    cfg.numAttrs = launch_attrs(attr);
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 // records the library's last error (text and GPT2_ERR_* code); returns code

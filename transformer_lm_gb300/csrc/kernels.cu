@@ -25,6 +25,12 @@ bool pdl_enabled() {
     return on;
 }
 
+namespace {
+thread_local int t_launch_priority = 0;
+}
+int launch_priority() { return t_launch_priority; }
+void set_launch_priority(int priority) { t_launch_priority = priority; }
+
 int num_sms() {
     static int n = 0;
     if (n == 0) {

@@ -187,8 +187,8 @@ long long gpt2_launch_count(void);
 int fused_linear_bias_gelu_softmax(const float* x, const float* W, const float* b, float* out,
                                    int M, int K, int N, void* stream);
 
-/* Allocation-free variant of fused_linear_bias_gelu_softmax (no counterpart in
- * the paper: it exists for callers that cannot let a library allocate device
+/* Allocation-free variant of fused_linear_bias_gelu_softmax (an addition to the
+ * operator's problem statement: it exists for callers that cannot let a library allocate device
  * memory -- processes whose own pool allocator owns all device memory, where a
  * cudaMalloc behind its back can fail or fragment the pool, and loops that
  * cannot take the device-wide synchronisation a cudaMalloc may imply).

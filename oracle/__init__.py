@@ -38,7 +38,8 @@ def build(force: bool = False) -> str:
         if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= newest:
             return _LIB
         tmp = _LIB + f".tmp{os.getpid()}"
-        cmd = ["gcc", "-O2", "-std=c99", "-D_GNU_SOURCE", "-fPIC", "-shared", "-fopenmp",
+        cmd = ["gcc", "-O2", "-std=c99", "-D_GNU_SOURCE", "-ffp-contract=off", "-fPIC", "-shared",
+               "-fopenmp",
                "-o", tmp, _SRC, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB)
@@ -92,6 +93,26 @@ def lib():
         L.oracle_attention_backward.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int,
                                                 ctypes.c_int, ctypes.c_int]
         L.oracle_num_threads.restype = ctypes.c_int
+        _u64p = ctypes.POINTER(ctypes.c_ulonglong)
+        L.oracle_random_u32.restype = ctypes.c_uint
+        L.oracle_random_u32.argtypes = [_u64p]
+        L.oracle_random_f32.restype = ctypes.c_float
+        L.oracle_random_f32.argtypes = [_u64p]
+        L.oracle_squirrel_noise5.restype = ctypes.c_uint
+        L.oracle_squirrel_noise5.argtypes = [ctypes.c_uint, ctypes.c_uint]
+        L.oracle_noise_2d.restype = ctypes.c_uint
+        L.oracle_noise_2d.argtypes = [ctypes.c_uint, ctypes.c_uint, ctypes.c_uint]
+        L.oracle_bf16_rne.restype = ctypes.c_ushort
+        L.oracle_bf16_rne.argtypes = [ctypes.c_float]
+        L.oracle_stochastic_round_bf16.restype = ctypes.c_ushort
+        L.oracle_stochastic_round_bf16.argtypes = [ctypes.c_float, ctypes.c_uint]
+        _usp = ctypes.POINTER(ctypes.c_ushort)
+        _fp = ctypes.POINTER(ctypes.c_float)
+        L.oracle_adamw_bf16_sr.argtypes = [_usp, _usp, _fp, _fp, ctypes.c_size_t, ctypes.c_float,
+                                           ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                           ctypes.c_float, ctypes.c_int, ctypes.c_uint]
+        L.oracle_sample_softmax.restype = ctypes.c_int
+        L.oracle_sample_softmax.argtypes = [_dp, ctypes.c_int, ctypes.c_double]
         _lib = L
     return _lib
 
@@ -180,6 +201,52 @@ def adamw(params, grads, m, v, lr, beta1, beta2, eps, wd, t):
     n = params.size
     lib().oracle_adamw(_d(params), _d(_f64(grads)), _d(m), _d(v), n, lr, beta1, beta2, eps, wd,
                        int(t))
+
+
+class Rng:
+    """The page's xorshift* generator on a 64-bit state."""
+
+    def __init__(self, state: int):
+        self.state = ctypes.c_ulonglong(state)
+
+    def u32(self) -> int:
+        return int(lib().oracle_random_u32(ctypes.byref(self.state)))
+
+    def f32(self) -> float:
+        return float(lib().oracle_random_f32(ctypes.byref(self.state)))
+
+
+def squirrel_noise5(position: int, seed: int) -> int:
+    return int(lib().oracle_squirrel_noise5(position & 0xFFFFFFFF, seed & 0xFFFFFFFF))
+
+
+def noise_2d(x: int, y: int, seed: int) -> int:
+    return int(lib().oracle_noise_2d(x & 0xFFFFFFFF, y & 0xFFFFFFFF, seed & 0xFFFFFFFF))
+
+
+def bf16_rne(x: float) -> int:
+    return int(lib().oracle_bf16_rne(x))
+
+
+def stochastic_round_bf16(x: float, random: int) -> int:
+    return int(lib().oracle_stochastic_round_bf16(x, random & 0xFFFFFFFF))
+
+
+def adamw_bf16_sr(params_bits, grads_bits, m, v, lr, beta1, beta2, eps, wd, t, seed):
+    """In place: uint16 bf16 bit patterns of params, float32 m and v."""
+    assert params_bits.dtype == np.uint16 and params_bits.flags.c_contiguous
+    g = np.ascontiguousarray(grads_bits, dtype=np.uint16)
+    assert m.dtype == np.float32 and v.dtype == np.float32
+    _usp = ctypes.POINTER(ctypes.c_ushort)
+    _fp = ctypes.POINTER(ctypes.c_float)
+    lib().oracle_adamw_bf16_sr(params_bits.ctypes.data_as(_usp), g.ctypes.data_as(_usp),
+                               m.ctypes.data_as(_fp), v.ctypes.data_as(_fp), params_bits.size,
+                               lr, beta1, beta2, eps, wd, int(t), seed & 0xFFFFFFFF)
+
+
+def sample_softmax(logits, coin: float) -> int:
+    lg = _f64(logits).reshape(-1)
+    return int(lib().oracle_sample_softmax(_d(lg), lg.size, float(coin)))
 
 
 def layernorm_forward(x, w, b):

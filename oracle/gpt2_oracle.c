@@ -657,3 +657,140 @@ void oracle_fused_linear_bias_gelu_softmax(const double* x, const double* W, con
         for (int j = 0; j < N; j++) row[j] /= sum;
     }
 }
+
+/* ------------------------------------------------------------------------
+ * Random numbers, stochastic rounding and sampling ([P1]).
+ * These follow the page's fixed-width integer and float arithmetic: the
+ * stochastic-rounding decision depends on the float bits of the update, so
+ * the AdamW update below is computed in float (the page's precision), with
+ * each operation written out (no contraction: the oracle is built with
+ * -ffp-contract=off) and the page's two-FMA lerp.
+ * ------------------------------------------------------------------------ */
+
+/* [P1] random_u32: xorshift* (Vigna) -- three xorshifts of the 64-bit state,
+ * then the top 32 bits of the state times 0x2545F4914F6CDD1D. */
+unsigned int oracle_random_u32(unsigned long long* state) {
+    unsigned long long x = *state;
+    x ^= x >> 12;
+    x ^= x << 25;
+    x ^= x >> 27;
+    *state = x;
+    return (unsigned int)((x * 0x2545F4914F6CDD1DULL) >> 32);
+}
+
+/* [P1] random_f32: the top 24 of those 32 bits as a float in [0, 1). */
+float oracle_random_f32(unsigned long long* state) {
+    return (float)(oracle_random_u32(state) >> 8) / 16777216.0f;
+}
+
+/* [P1] SquirrelNoise5 (Squirrel Eiserloh's position hash, version 5): the
+ * position times a constant, plus the seed, then four rounds of
+ * xorshift-right / add-or-multiply by a constant, and a last xorshift.
+ * All arithmetic is modulo 2^32. */
+unsigned int oracle_squirrel_noise5(unsigned int position, unsigned int seed) {
+    unsigned int b = position;
+    b *= 0xd2a80a3fu;
+    b += seed;
+    b ^= b >> 9;
+    b += 0xa884f197u;
+    b ^= b >> 11;
+    b *= 0x6C736F4Bu;
+    b ^= b >> 13;
+    b += 0xB79F3ABBu;
+    b ^= b >> 15;
+    b *= 0x1b56c4f5u;
+    b ^= b >> 17;
+    return b;
+}
+
+/* [P1] Get2dNoiseUint: the 2-D position (x, y) hashed as x + 198491317 y
+ * (modulo 2^32). */
+unsigned int oracle_noise_2d(unsigned int x, unsigned int y, unsigned int seed) {
+    return oracle_squirrel_noise5(x + 198491317u * y, seed);
+}
+
+static unsigned int f32_bits(float f) {
+    unsigned int u;
+    memcpy(&u, &f, 4);
+    return u;
+}
+static float bits_f32(unsigned int u) {
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* IEEE round-to-nearest-even of a float to bfloat16 (the upper 16 bits of
+ * the float format); a NaN stays a (quiet) NaN. */
+unsigned short oracle_bf16_rne(float x) {
+    unsigned int u = f32_bits(x);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu))
+        return (unsigned short)((u >> 16) | 0x0040u);
+    unsigned int lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb;
+    return (unsigned short)(u >> 16);
+}
+
+/* [P1] stochastic_rounding, bf16 form: the low 16 bits of the float are
+ * compared with the low 16 bits of `random`; above them the float is pushed
+ * to the top of its bf16 interval (low bits all ones), else to the bottom
+ * (low bits cleared), and the result is converted with round-to-nearest. */
+unsigned short oracle_stochastic_round_bf16(float x, unsigned int random) {
+    unsigned int threshold = random & 0xFFFFu;
+    unsigned int u = f32_bits(x);
+    unsigned int low = u & 0xFFFFu;
+    u = low > threshold ? (u | 0xFFFFu) : (u & ~0xFFFFu);
+    return oracle_bf16_rne(bits_f32(u));
+}
+
+/* [P1] adamw_kernel3 without master weights: bf16 parameters and gradients,
+ * float moments. With g = grad, lerp(a, b, w) = fma(w, b, fma(-w, a, a)):
+ *   m = lerp(g, m, b1); v = lerp(g*g, v, b2);
+ *   mhat = m / (1 - b1^t); vhat = v / (1 - b2^t);
+ *   p = p - lr * (mhat / (sqrt(vhat) + eps) + wd * p)     (all in float)
+ * and the new bf16 parameter is p stochastically rounded. Element i of the
+ * flat buffer is the page's thread (i mod 512) of block (i / 512); its random
+ * word is Get2dNoiseUint of that position under the step's seed, and the
+ * page's bf16 rounding routine hashes the same position again with that word
+ * as the seed. Parameters and gradients are passed as bf16 bit patterns. */
+void oracle_adamw_bf16_sr(unsigned short* params, const unsigned short* grads, float* mstate,
+                          float* vstate, size_t n, float lr, float beta1, float beta2, float eps,
+                          float wd, int t, unsigned int seed) {
+    const float c1 = 1.0f - powf(beta1, (float)t);
+    const float c2 = 1.0f - powf(beta2, (float)t);
+    for (size_t i = 0; i < n; i++) {
+        float g = bits_f32((unsigned int)grads[i] << 16);
+        float m = fmaf(beta1, mstate[i], fmaf(-beta1, g, g));
+        float gg = g * g;
+        float v = fmaf(beta2, vstate[i], fmaf(-beta2, gg, gg));
+        mstate[i] = m;
+        vstate[i] = v;
+        float mhat = m / c1;
+        float vhat = v / c2;
+        float old = bits_f32((unsigned int)params[i] << 16);
+        float den = sqrtf(vhat) + eps;
+        float upd = mhat / den + wd * old;
+        float p = old - lr * upd;
+        unsigned int x = (unsigned int)(i % 512), y = (unsigned int)(i / 512);
+        unsigned int random = oracle_noise_2d(x, y, seed);
+        params[i] = oracle_stochastic_round_bf16(p, oracle_noise_2d(x, y, random));
+    }
+}
+
+/* [P1] sample_softmax: the index drawn from softmax(logits[0..n)) with a
+ * coin in [0, 1): the first i whose cumulative probability exceeds the coin
+ * (n - 1 when rounding leaves none). In double precision, with the row max
+ * subtracted before exponentiating (the probabilities are unchanged). */
+int oracle_sample_softmax(const double* logits, int n, double coin) {
+    double mx = -INFINITY;
+    for (int i = 0; i < n; i++) if (logits[i] > mx) mx = logits[i];
+    double norm = 0.0;
+    for (int i = 0; i < n; i++) norm += exp(logits[i] - mx);
+    double target = coin * norm;
+    double cdf = 0.0;
+    for (int i = 0; i < n; i++) {
+        cdf += exp(logits[i] - mx);
+        if (target < cdf) return i;
+    }
+    return n - 1;
+}

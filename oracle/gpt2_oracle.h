@@ -113,6 +113,26 @@ void oracle_adamw(double* params, const double* grads, double* mstate, double* v
 void oracle_fused_linear_bias_gelu_softmax(const double* x, const double* W, const double* b,
                                            double* y, int M, int K, int N);
 
+/* ---- random numbers, stochastic rounding, sampling ---- */
+/* xorshift* step of the 64-bit state; a float in [0, 1) from its top 24 bits. */
+unsigned int oracle_random_u32(unsigned long long* state);
+float oracle_random_f32(unsigned long long* state);
+/* SquirrelNoise5 position hash, and its 2-D form (x + 198491317 y). */
+unsigned int oracle_squirrel_noise5(unsigned int position, unsigned int seed);
+unsigned int oracle_noise_2d(unsigned int x, unsigned int y, unsigned int seed);
+/* float -> bf16 bits, round to nearest even. */
+unsigned short oracle_bf16_rne(float x);
+/* float -> bf16 bits, stochastic rounding with the low 16 bits of random. */
+unsigned short oracle_stochastic_round_bf16(float x, unsigned int random);
+/* AdamW without master weights: bf16 params (bit patterns, updated in place)
+ * and grads, float moments; the update in float, the result stochastically
+ * rounded with the step's seed. */
+void oracle_adamw_bf16_sr(unsigned short* params, const unsigned short* grads, float* mstate,
+                          float* vstate, size_t n, float lr, float beta1, float beta2, float eps,
+                          float wd, int t, unsigned int seed);
+/* Index sampled from softmax(logits[0..n)) with coin in [0, 1). */
+int oracle_sample_softmax(const double* logits, int n, double coin);
+
 /* Number of OpenMP threads the oracle uses (1 when built without OpenMP). */
 int oracle_num_threads(void);
 

@@ -48,27 +48,10 @@ def select_model(name: str) -> None:
                     "wd 0.1)")
 
 
-def model_flops_per_token() -> float:
+def model_flops_per_token() -> float:  # noqa: D401
     """6 * (matmul weights, unpadded vocab) + causal attention fwd+bwd: 6 L C T."""
     n_mm = 12 * L * C * C + C * V
     return 6.0 * n_mm + 6.0 * L * C * T
-
-
-def gemm_traffic():
-    """DRAM bytes per GEMM launch from the committed ncu summary, or None when
-    the GEMM source has changed since those counters were taken."""
-    import hashlib
-    root = os.path.dirname(os.path.abspath(__file__))
-    try:
-        text = open(os.path.join(root, "profiles", "roofline_gemm_step.md")).read()
-        src = open(os.path.join(root, "transformer_lm_gb300", "csrc", "gemm_tc.cu"), "rb").read()
-    except OSError:
-        return None
-    vals = dict(line.split(":", 1) for line in text.splitlines()
-                if line.startswith(("traffic_bytes_per_launch:", "source_sha256_16:")))
-    if vals.get("source_sha256_16", "").strip() != hashlib.sha256(src).hexdigest()[:16]:
-        return None
-    return float(vals["traffic_bytes_per_launch"])
 
 
 def load_peaks() -> dict:
@@ -178,16 +161,22 @@ def job_throughput(tokens_per_rank: int, world: int, seconds: float) -> float:
 
 # --------------------------------------------------------------------------- CPU oracle arm
 ORACLE_SAMPLE_T = 256
+FUSED_SHAPE = (1024, 8192, 8192)  # M, K, N of the fused operator workload
+FUSED_FLOPS = 2.0 * FUSED_SHAPE[0] * FUSED_SHAPE[1] * FUSED_SHAPE[2]
+# algorithmic bytes: read x (M,K), W (N,K), b (N), write y (M,N), all fp32
+FUSED_BYTES = 4.0 * (FUSED_SHAPE[0] * FUSED_SHAPE[1] + FUSED_SHAPE[2] * FUSED_SHAPE[1]
+                     + FUSED_SHAPE[2] + FUSED_SHAPE[0] * FUSED_SHAPE[2])
+FUSED_ORACLE_ROWS = 32
 
 
-def oracle_sample_setup(seed: int = 1337):
-    """The oracle on a bounded sample of the workload: the full 124M model and
-    AdamW over all its parameters, on a batch of B=1, T=ORACLE_SAMPLE_T tokens."""
+def oracle_sample_setup(dims_name: str, seed: int = 1337):
+    """The oracle on a bounded sample of a training workload: the full model
+    and AdamW over all its parameters, on a batch of B=1, T=ORACLE_SAMPLE_T."""
     import numpy as np
 
     import oracle
     from transformer_lm_gb300 import inputs
-    d = getattr(inputs, DIMS)
+    d = getattr(inputs, dims_name)
     params = inputs.round_to_bf16(inputs.gpt2_params(d, seed)).astype(np.float64)
     tok = inputs.tokens(42, 1, 1, ORACLE_SAMPLE_T, d.V)
     tgt = inputs.tokens(42, 2, 1, ORACLE_SAMPLE_T, d.V)
@@ -206,17 +195,34 @@ def oracle_sample_step(st) -> None:
     oracle.adamw(st["params"], st["grads"], st["m"], st["v"], LR, B1, B2, EPS, WD, st["step"])
 
 
-def cpu_baseline(steps: int = 1) -> dict:
+def cpu_baseline_train(dims_name: str, steps: int) -> dict:
     import oracle
-    st = oracle_sample_setup()
+    st = oracle_sample_setup(dims_name)
     t0 = time.perf_counter()
     for _ in range(steps):
         oracle_sample_step(st)
     dt = time.perf_counter() - t0
     return {"value": steps * ORACLE_SAMPLE_T / dt, "unit": "tokens/s", "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": (f"full {DIMS[5:]} model fwd+bwd on B=1 T={ORACLE_SAMPLE_T} plus AdamW over "
+            "sample": (f"full {dims_name[5:]} model fwd+bwd on B=1 T={ORACLE_SAMPLE_T} plus AdamW over "
                        f"all params, {steps} step(s), fp64, {dt:.1f} s")}
+
+
+def cpu_baseline_fused() -> dict:
+    """The oracle's fused operator on FUSED_ORACLE_ROWS rows of x with the full
+    W (rows are independent), scaled to the whole (M, K, N) operator."""
+    import oracle
+    from transformer_lm_gb300 import inputs
+    M, K, N = FUSED_SHAPE
+    x, W, b = inputs.fused_op_inputs(M, K, N, seed=5)
+    xs = x[:FUSED_ORACLE_ROWS].copy()
+    t0 = time.perf_counter()
+    oracle.fused_linear_bias_gelu_softmax(xs, W, b)
+    dt = time.perf_counter() - t0
+    return {"value": 1000.0 * dt * M / FUSED_ORACLE_ROWS, "unit": "ms per operator call",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": (f"{FUSED_ORACLE_ROWS} of the {M} rows (full K={K}, N={N}) in fp64, "
+                       f"{dt:.2f} s, scaled by {M // FUSED_ORACLE_ROWS}")}
 
 
 def run_reference(args):
@@ -224,7 +230,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     import oracle
-    st = oracle_sample_setup()
+    st = oracle_sample_setup(DIMS)
     for _ in range(args.warmup):
         oracle_sample_step(st)
     t0 = time.perf_counter()
@@ -249,59 +255,60 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------------------- GPU arm
-def run_ours(args):
-    world, rank, local = dist_setup()
-    import numpy as np
+def profile_value(fname: str, key: str, sources: list[str]):
+    """A number recorded in a committed ncu summary under profiles/, or None
+    when any of the listed sources has changed since it was taken."""
+    import hashlib
+    try:
+        text = open(os.path.join(ROOT, "profiles", fname)).read()
+        h = hashlib.sha256()
+        for src in sources:
+            h.update(open(os.path.join(ROOT, "transformer_lm_gb300", "csrc", src), "rb").read())
+    except OSError:
+        return None
+    vals = dict(line.split(":", 1) for line in text.splitlines() if ":" in line)
+    if vals.get("source_sha256_16", "").strip() != h.hexdigest()[:16] or key not in vals:
+        return None
+    return float(vals[key])
+
+
+def train_workload(world, rank, steps, warmup, peaks, stream, with_breakdown=True):
+    """Time the current model selection (select_model): device-resident steps
+    (graph replays), an instrumented per-kernel pass, and the host-buffer step."""
     import torch
 
     from transformer_lm_gb300 import gpt2 as G
     from transformer_lm_gb300 import inputs
 
-    torch.cuda.set_device(local)
-    peaks = load_peaks()
-    # baseline first, on rank 0 only, at N=1 only, before any GPU work
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(2)
-
     G.gpt2_init(L, C, NH, V, Vp, MAXT, 1337 + rank)
-    # a created stream (the legacy default stream has handle 0, which the
-    # library reads as "use your own stream"); torch events are recorded on it
-    stream = torch.cuda.Stream()
-    torch.cuda.set_stream(stream)
     G.gpt2_set_stream(stream.cuda_stream)
     G.gpt2_set_grad_accum(ACCUM)
     # ACCUM micro-batches of B x T ids, one after another
-    tok = inputs.tokens(42 + rank, 1, ACCUM * B, T, V)
-    tgt = inputs.tokens(42 + rank, 2, ACCUM * B, T, V)
-    d_tok = torch.from_numpy(tok.reshape(-1)).cuda()
-    d_tgt = torch.from_numpy(tgt.reshape(-1)).cuda()
+    tok = inputs.tokens(42 + rank, 1, ACCUM * B, T, V).reshape(-1)
+    tgt = inputs.tokens(42 + rank, 2, ACCUM * B, T, V).reshape(-1)
+    d_tok = torch.from_numpy(tok).cuda()
+    d_tgt = torch.from_numpy(tgt).cuda()
     d_loss = torch.zeros(ACCUM, device="cuda")
     step_no = [0]
 
-    # pinned host copies of the batch for the end-to-end leg
-    h_tok = torch.from_numpy(tok.reshape(-1)).pin_memory()
-    h_tgt = torch.from_numpy(tgt.reshape(-1)).pin_memory()
-
     def device_step():
-        # forward + zero_grad + backward + AdamW; replayed from a CUDA graph
-        # once the first call has recorded it
+        # zero_grad + ACCUM x (forward + backward) + AdamW; replayed from a
+        # CUDA graph once the first call has recorded it
         step_no[0] += 1
         G.gpt2_train_step(d_tok, d_tgt, B, T, LR, B1, B2, EPS, WD, step_no[0], d_loss)
 
     def host_step():
-        # the batch goes up from pinned host memory and the loss comes back
-        d_tok.copy_(h_tok, non_blocking=True)
-        d_tgt.copy_(h_tgt, non_blocking=True)
-        device_step()
-        return float(d_loss.cpu().mean())
+        # the public host-buffer call: ids checked and copied up, the step, the
+        # micro-step losses copied back (the call synchronises)
+        step_no[0] += 1
+        return G.gpt2_train_step_host(tok, tgt, B, T, LR, B1, B2, EPS, WD, step_no[0])
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         device_step()
     G.gpt2_sync()
 
     # ---- device-resident timed region
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(torch.cuda.current_device())
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()
@@ -310,88 +317,201 @@ def run_ours(args):
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         device_step()
     ev1.record(stream)
     torch.cuda.synchronize()
     launches = G.gpt2_launch_count() - launches0
     clk = clocks.stop()
     barrier(world)
-    ms = ev0.elapsed_time(ev1)
-    ms = max_over_ranks(ms, world)
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world)
     G.gpt2_sync()
     loss_dev = float(d_loss.cpu().mean())
 
     # ---- per-kernel durations: CUDA events around every launch, on the
     # library's stream, over a second pass of the same steps (kept out of
     # the timed region above because the extra event records slow the step)
-    G.gpt2_timing_begin(args.steps * 500 * ACCUM * L // 12)
-    for _ in range(args.steps):
-        device_step()
-    G.gpt2_timing_end()
+    fam = None
+    if with_breakdown:
+        G.gpt2_timing_begin(steps * 500 * ACCUM * max(L, 12) // 12)
+        for _ in range(steps):
+            device_step()
+        G.gpt2_timing_end()
+        fam = {}
+        for f in G.FAMILIES:
+            t_ms, n, work = G.gpt2_timing_get(f)
+            fam[f] = dict(ms=t_ms, launches=n, work=work)
 
-    # ---- end-to-end: host tokens in, loss read back, every step
+    # ---- end-to-end through the host-buffer C-ABI call
     for _ in range(2):
         host_step()
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(args.steps):
+    for _ in range(steps):
         loss_host = host_step()
-    torch.cuda.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     G.gpt2_sync()
+    G.gpt2_free()
 
-    tokens_all = world * ACCUM * B * T * args.steps
-    value = job_throughput(ACCUM * B * T * args.steps, world, ms / 1000.0)
-    e2e_value = job_throughput(ACCUM * B * T * args.steps, world, e2e_s)
+    tokens_per_rank = ACCUM * B * T * steps
     step_flops = model_flops_per_token() * ACCUM * B * T
+    step_s = ms / 1000.0 / steps
+    out = {
+        "value": job_throughput(tokens_per_rank, world, ms / 1000.0), "unit": "tokens/s",
+        "ms_per_step": ms / steps, "steps": steps, "warmup": warmup,
+        "mfu": step_flops / step_s / (peaks["bf16_tflops"] * 1e12),
+        "mfu_vs_sustained_peak": step_flops / step_s / (peaks["bf16_tflops_sustained"] * 1e12),
+        "model_tflop_per_step": step_flops / 1e12,
+        "e2e": {"value": job_throughput(tokens_per_rank, world, e2e_s), "unit": "tokens/s",
+                "h2d_bytes_per_step": 2 * ACCUM * B * T * 4, "d2h_bytes_per_step": 4 * ACCUM,
+                "call": "gpt2_train_step_host (host int32 ids in, host losses out)"},
+        "gpu_launches": launches, "clocks": clk,
+        "loss": {"device_path": loss_dev, "host_path": float(loss_host.mean())},
+    }
+    if fam is not None:
+        g = fam["gemm"]
+        gemm_tflops = g["work"] / (g["ms"] / 1000.0) / 1e12 if g["ms"] > 0 else None
+        # the timed region is well under a second at held maximum clocks: the
+        # burst peak is the one that matches it (the sustained figure is given too)
+        peak_t = peaks["bf16_tflops"]
+        out["roofline"] = {
+            "bound": "tensor", "kernel": "gemm_tc_k (tcgen05 bf16 GEMM, all launches)",
+            "achieved": gemm_tflops, "peak": peak_t, "unit": "TFLOP/s",
+            "frac": (gemm_tflops / peak_t) if gemm_tflops else None,
+            "peak_source": f"{peaks['source']} bf16_tflops (burst)",
+            "frac_vs_sustained": (gemm_tflops / peaks["bf16_tflops_sustained"]) if gemm_tflops else None,
+            "traffic": (profile_value("roofline_gemm_step.md", "traffic_bytes_per_launch", ["gemm_tc.cu"])
+                        if DIMS == "GPT2_124M" else None),
+            "per_launch_gflop": g["work"] / max(g["launches"], 1) / 1e9,
+            "avg_launch_ms": g["ms"] / max(g["launches"], 1)}
+        breakdown = {f: {"ms_per_step": v["ms"] / steps, "launches_per_step": v["launches"] / steps}
+                     for f, v in fam.items() if v["launches"]}
+        for f in ("ln_fwd", "ln_bwd", "classifier", "adamw", "encoder"):
+            if fam[f]["ms"] > 0:
+                breakdown[f]["gb_per_s"] = fam[f]["work"] / (fam[f]["ms"] / 1000.0) / 1e9
+                breakdown[f]["frac_of_hbm"] = breakdown[f]["gb_per_s"] / peaks["hbm_gbs"]
+        for f in ("attn_fwd", "attn_bwd"):
+            if fam[f]["ms"] > 0:
+                breakdown[f]["tflop_per_s"] = fam[f]["work"] / (fam[f]["ms"] / 1000.0) / 1e12
+                breakdown[f]["frac_of_peak"] = breakdown[f]["tflop_per_s"] / peaks["bf16_tflops"]
+        out["breakdown"] = breakdown
+    return out
 
-    fam = {}
-    for f in G.FAMILIES:
-        t_ms, n, work = G.gpt2_timing_get(f)
-        fam[f] = dict(ms=t_ms, launches=n, work=work)
-    g = fam["gemm"]
-    gemm_tflops = g["work"] / (g["ms"] / 1000.0) / 1e12 if g["ms"] > 0 else None
-    peak_t = peaks["bf16_tflops_sustained"]
-    roofline = {"bound": "tensor", "kernel": "gemm_tc_k (tcgen05 bf16 GEMM, all launches)",
-                "achieved": gemm_tflops, "peak": peak_t, "unit": "TFLOP/s",
-                "frac": (gemm_tflops / peak_t) if gemm_tflops else None,
-                "peak_source": f"{peaks['source']} bf16_tflops_sustained",
-                "traffic": gemm_traffic(),
-                "per_launch_gflop": g["work"] / max(g["launches"], 1) / 1e9,
-                "avg_launch_ms": g["ms"] / max(g["launches"], 1)}
-    breakdown = {f: {"ms_per_step": v["ms"] / args.steps, "launches_per_step": v["launches"] / args.steps}
-                 for f, v in fam.items() if v["launches"]}
-    for f in ("ln_fwd", "ln_bwd", "classifier", "adamw", "encoder"):
-        if fam[f]["ms"] > 0:
-            breakdown[f]["gb_per_s"] = fam[f]["work"] / (fam[f]["ms"] / 1000.0) / 1e9
-    for f in ("attn_fwd", "attn_bwd"):
-        if fam[f]["ms"] > 0:
-            breakdown[f]["tflop_per_s"] = fam[f]["work"] / (fam[f]["ms"] / 1000.0) / 1e12
+
+def fused_workload(reps, warmup, peaks):
+    """The stand-alone fused Linear+bias+GELU+softmax at (M, K, N) = FUSED_SHAPE,
+    fp32 in and out, CUDA events over `reps` calls on one stream. The operands
+    (320 MiB) exceed L2, so no flush is needed between calls."""
+    import torch
+
+    from transformer_lm_gb300 import gpt2 as G
+    from transformer_lm_gb300 import inputs
+    M, K, N = FUSED_SHAPE
+    x, W, b = inputs.fused_op_inputs(M, K, N, seed=5)
+    dx, dW, db = (torch.from_numpy(a).cuda() for a in (x, W, b))
+    out = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    res = {}
+    for name, fn in (("fused_linear_bias_gelu_softmax", G.fused_linear_bias_gelu_softmax),
+                     ("fused_linear_bias_gelu_softmax_noalloc", G.fused_linear_bias_gelu_softmax_noalloc)):
+        for _ in range(warmup):
+            fn(dx, dW, db, out, M, K, N, s.cuda_stream)
+        torch.cuda.synchronize()
+        clocks = ClockSampler(torch.cuda.current_device())
+        clocks.start()
+        time.sleep(0.3)
+        l0 = G.gpt2_launch_count()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(reps):
+            fn(dx, dW, db, out, M, K, N, s.cuda_stream)
+        e1.record(s)
+        torch.cuda.synchronize()
+        clk = clocks.stop()
+        G.gpt2_device_status()
+        ms = e0.elapsed_time(e1) / reps
+        res[name] = dict(ms=ms, launches=(G.gpt2_launch_count() - l0) / reps, clocks=clk)
+    main = res["fused_linear_bias_gelu_softmax"]
+    ms = main["ms"]
+    # the operator is fp32 with TF32 allowed: its own peak is the TF32 rate,
+    # the measured bf16 burst peak times the nominal TF32 : bf16 ratio (1.1 : 2.25)
+    peak_tf32 = peaks["bf16_tflops"] * 1.1 / 2.25
+    achieved = FUSED_FLOPS / (ms / 1000.0) / 1e12
+    traffic = profile_value("fused_op_1024x8192x8192.md", "traffic_bytes_per_call",
+                            ["ops.cu", "gemm_tc.cu", "kernels.cu"])
+    return {
+        "workload": (f"fused Linear+bias+GELU(tanh)+row softmax, fp32, x [{M},{K}], W [{N},{K}], "
+                     f"b [{N}] (synthetic: x~N(0,1), W~N(0,1/sqrt(K)), b~U(-0.1,0.1))"),
+        "metric": "time per operator call", "value": ms, "unit": "ms", "higher_is_better": False,
+        "dtype": "f32 (bf16x3 split products on the tensor cores)",
+        "tflop_per_s": achieved, "gpu_launches_per_call": main["launches"], "clocks": main["clocks"],
+        "l2": "no flush: operands (320 MiB) exceed L2",
+        "roofline": {"bound": "tensor", "kernel": "gemm_tc_k EPI_GELU_PART (with its split and finish passes)",
+                     "achieved": achieved, "peak": peak_tf32, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf32,
+                     "peak_source": f"{peaks['source']} bf16_tflops x 1.1/2.25 (nominal TF32:bf16)",
+                     "executed_bf16_tflop_per_s": 3.0 * achieved,
+                     "executed_frac_of_bf16_peak": 3.0 * achieved / peaks["bf16_tflops"],
+                     "algorithmic_bytes": FUSED_BYTES, "traffic": traffic},
+        "noalloc_variant_ms": res["fused_linear_bias_gelu_softmax_noalloc"]["ms"],
+    }
+
+
+def run_ours(args):
+    world, rank, local = dist_setup()
+    import torch
+
+    torch.cuda.set_device(local)
+    peaks = load_peaks()
+    extra = world == 1 and not args.no_extra
+    # CPU baselines first, on rank 0 only, at N=1 only, before any GPU work
+    cpu, cpu_350, cpu_fused = None, None, None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_train(DIMS, 2)
+        if extra and DIMS == "GPT2_124M":
+            cpu_350 = cpu_baseline_train("GPT2_350M", 1)
+            cpu_fused = cpu_baseline_fused()
+
+    from transformer_lm_gb300 import gpt2 as G
+    # a created stream (the legacy default stream has handle 0, which the
+    # library reads as "use your own stream"); torch events are recorded on it
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    head = train_workload(world, rank, args.steps, args.warmup, peaks, stream)
+
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
         "config": {"workload": WORKLOAD, "global_batch": ACCUM * B * world, "seq_len": T,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "no flush: per-step working set (~6 GB) is larger than L2"},
-        "mfu": step_flops / (ms / 1000.0 / args.steps) / (peaks["bf16_tflops_sustained"] * 1e12),
-        "mfu_vs_burst_peak": step_flops / (ms / 1000.0 / args.steps) / (peaks["bf16_tflops"] * 1e12),
-        "model_tflop_per_step": step_flops / 1e12,
-        "roofline": roofline,
-        "breakdown": breakdown,
-        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": 2 * ACCUM * B * T * 4,
-                "d2h_bytes_per_step": 4 * ACCUM},
-        "gpu_launches": launches,
-        "clocks": clk,
-        "loss": {"device_path": loss_dev, "host_path": loss_host},
     }
+    for k in ("mfu", "mfu_vs_sustained_peak", "model_tflop_per_step", "roofline", "breakdown",
+              "e2e", "gpu_launches", "clocks", "loss"):
+        if k in head:
+            line[k] = head[k]
     if cpu is not None:
         line["cpu_baseline"] = cpu
+    if extra and DIMS == "GPT2_124M":
+        # the other workloads, each with its own roofline and CPU baseline
+        select_model("350m")
+        w350 = train_workload(world, rank, min(args.steps, 5), 3, peaks, stream)
+        w350["workload"] = WORKLOAD
+        w350["dtype"] = "bf16"
+        if cpu_350 is not None:
+            w350["cpu_baseline"] = cpu_350
+        fused = fused_workload(20, 3, peaks)
+        if cpu_fused is not None:
+            fused["cpu_baseline"] = cpu_fused
+        line["workloads"] = {"gpt2_350m_bf16_b16_t1024_accum4": w350,
+                             "fused_linear_gelu_softmax_1024x8192x8192_f32": fused}
+        line["gpu_launches_all_workloads"] = (line.get("gpu_launches", 0) + w350["gpu_launches"])
     if rank == 0:
         print(json.dumps(line), flush=True)
-    G.gpt2_free()
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -405,6 +525,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time only the headline workload (no 350M / fused-operator sub-records)")
     ap.add_argument("--model", default="124m", choices=["124m", "350m"],
                     help="124m: the headline workload (B=8, T=1024); 350m: B=16, T=1024, "
                          "4 accumulation micro-steps per update")

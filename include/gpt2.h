@@ -89,6 +89,9 @@ int gpt2_zero_grad(void);
  * backward with dloss = 1/(k*B*T) instead of the page's 1/(B*T). */
 int gpt2_set_grad_accum(int k);
 
+/* The current accumulation count k (>= 1), or GPT2_ERR_STATE without a model. */
+int gpt2_get_grad_accum(void);
+
 /* Backward pass of the last forward (llm.c gpt2_backward). Parameter
  * gradients ACCUMULATE (+=); activation gradients are overwritten, except the
  * residual-stream gradient to which each LayerNorm backward adds.
@@ -98,8 +101,26 @@ int gpt2_backward(void);
 /* AdamW update of every parameter (llm.c gpt2_update / adamw_kernel3):
  * m = b1 m + (1-b1) g; v = b2 v + (1-b2) g^2; mhat = m/(1-b1^step); vhat = v/(1-b2^step);
  * theta -= lr (mhat/(sqrt(vhat)+eps) + wd theta). step >= 1. In GPT2_BF16 the fp32
- * master copy is updated and rounded (nearest-even) into the bf16 parameters. */
+ * master copy is updated and rounded (nearest-even) into the bf16 parameters;
+ * without master weights (gpt2_set_master_weights(0)) the bf16 parameters are
+ * updated in place: the update is computed in fp32 as the page writes it and
+ * rounded to bf16 stochastically (adamw_kernel3's stochastic_rounding branch). */
 int gpt2_adamw(float lr, float beta1, float beta2, float eps, float weight_decay, int step);
+
+/* Keep (1, the default) or drop (0) the fp32 master copy of the bf16
+ * parameters (llm.c "train_gpt2.cu", use_master_weights / the -w flag).
+ * Without it AdamW reads and writes the bf16 parameters directly and rounds
+ * each new value stochastically: with the low 16 bits of the fp32 value
+ * compared against 16 random bits, it goes to the upper bf16 neighbour with
+ * probability (low bits) / 65536, so the rounding is unbiased. The random
+ * bits of element i come from the page's SquirrelNoise5 hash of the position
+ * (i mod 512, i / 512) under a per-update seed drawn from the model's
+ * xorshift* stream (state 13371337 at gpt2_init, as on the page). This saves
+ * 4 bytes per parameter of memory and of AdamW traffic. Turning it back on
+ * copies the current bf16 parameters into a new master copy. bf16 models
+ * only (GPT2_ERR_CONFIG otherwise, except enabled = 1, which is a no-op);
+ * discards a recorded gpt2_train_step graph. */
+int gpt2_set_master_weights(int enabled);
 
 /* One whole training step on DEVICE-resident int32 tokens and targets:
  * gpt2_zero_grad, then for each of the k = gpt2_set_grad_accum micro-steps
@@ -115,6 +136,20 @@ int gpt2_adamw(float lr, float beta1, float beta2, float eps, float weight_decay
  * runs eagerly. */
 int gpt2_train_step(const int* d_tokens, const int* d_targets, int B, int T, float lr, float beta1,
                     float beta2, float eps, float weight_decay, int step, float* d_mean_loss);
+
+/* The same whole step on HOST int32 tokens and targets (k*B*T ids each, k =
+ * gpt2_set_grad_accum), the training loop of llm.c "train_gpt2.cu" (main:
+ * a batch from the loader, gpt2_forward, gpt2_zero_grad, gpt2_backward,
+ * gpt2_update, the loss printed). The ids are checked on the host (any id
+ * outside [0, V) returns GPT2_ERR_TOKEN before any work is enqueued), staged
+ * in a pinned buffer the library keeps, copied to the device in one transfer,
+ * the step runs as gpt2_train_step does (a CUDA-graph replay after the first
+ * call), and the k micro-step mean losses are copied back to the HOST array
+ * mean_loss (k floats; may be NULL). The call synchronises the model's stream
+ * and reports device errors (GPT2_ERR_DEVICE_TIMEOUT, GPT2_ERR_TOKEN) like
+ * gpt2_sync. The caller keeps ownership of all three host arrays. */
+int gpt2_train_step_host(const int* tokens, const int* targets, int B, int T, float lr, float beta1,
+                         float beta2, float eps, float weight_decay, int step, float* mean_loss);
 
 /* Wait for the stream; report GPT2_ERR_DEVICE_TIMEOUT / GPT2_ERR_TOKEN raised by kernels. */
 int gpt2_sync(void);
@@ -144,7 +179,33 @@ int gpt2_get_losses(float* host);       /* per-position losses of the last forwa
 #define GPT2_ACT_LNF 10      /* (B,T,C) */
 #define GPT2_ACT_LOGITS 11   /* (B,T,Vp): logits after forward without targets, dlogits after one with targets */
 #define GPT2_ACT_LSE 18      /* (L,B,NH,T) fp32 attention log-sum-exp */
+#define GPT2_ACT_PROBS 12    /* (B,T,Vp) fp32 softmax over the first V logits, 0 on the padding,
+                                after a forward without targets (the probs output of llm.c
+                                fused_classifier_kernel3); computed on the device at the call */
 int gpt2_get_activation(int which, int layer, float* host, size_t* n);
+
+/* ---- inference (llm.c "train_gpt2.cu": sample_softmax and the generation
+ * block of main) ----
+ * gpt2_sample: after a forward without targets, draw one token per sequence
+ * b in [0, B) from the model's distribution at position t (softmax over the
+ * first V logits of row (b, t)), following sample_softmax: the first index
+ * whose cumulative probability exceeds coins[b]. coins: HOST, B floats in
+ * [0, 1) (e.g. from the page's random_f32); out: HOST, B ints. Runs on the
+ * device (one block per sequence) and synchronises. GPT2_ERR_STATE without
+ * a preceding target-less forward; GPT2_ERR_ARG for t outside [0, T) or a
+ * coin outside [0, 1). */
+int gpt2_sample(int t, const float* coins, int* out);
+
+/* gpt2_generate: autoregressive sampling on the device. tokens: HOST int32
+ * (B, T), read and written; positions [t_begin, t_end) are generated, each
+ * from a forward over the whole (B, T) window (the page's generation loop,
+ * which also recomputes the full forward per token) and gpt2_sample at
+ * position t - 1 with one coin per sequence drawn from *rng_state by the
+ * page's xorshift* random_f32 (for t, then for b). Tokens stay on the device
+ * between positions (one upload, one download, no synchronisation per
+ * token). *rng_state is advanced as the draws did. 1 <= t_begin <= t_end <= T;
+ * B, T as for gpt2_forward. */
+int gpt2_generate(int* tokens, int B, int T, int t_begin, int t_end, unsigned long long* rng_state);
 
 /* Release all device memory held by the model. */
 int gpt2_free(void);

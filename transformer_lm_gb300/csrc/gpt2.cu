@@ -73,6 +73,9 @@ struct Model {
     void* params = nullptr;
     void* grads = nullptr;
     float* master = nullptr;
+    bool sr = false;  // bf16 without a master copy: AdamW rounds stochastically
+    // the seed stream of the stochastic rounding (xorshift*, one draw per update)
+    unsigned long long rng_state = 13371337ULL;
     float* mom_m = nullptr;
     float* mom_v = nullptr;
     unsigned int* d_err = nullptr;
@@ -92,6 +95,8 @@ struct Model {
     float *ln1_mean, *ln1_rstd, *ln2_mean, *ln2_rstd, *lnf_mean, *lnf_rstd, *lse, *losses, *mean_loss;
     void *dresidual, *dbtc, *dbt4c;
     float *attn_D, *ws;
+    float* coins = nullptr;    // (T, B) sampling coins of gpt2_sample / gpt2_generate
+    int* sampled = nullptr;    // (B) indices drawn by gpt2_sample
     float* gemm_ws = nullptr;  // split-K partials of the weight-gradient GEMMs (side stream)
     float* gemm_ws_main = nullptr;  // split-K partials of the main stream's products
     bool in_side = false;           // launches are being issued for the side stream
@@ -113,6 +118,12 @@ struct Model {
     int g_B = 0, g_T = 0, g_accum = 0;
     long long g_launches = 0;  // kernel launches one replay makes
     int *enc_counts, *enc_offsets, *enc_cursor, *enc_order, *enc_sorted;
+    // gpt2_train_step_host: device ids and losses of the host-buffer step, and
+    // their pinned staging (2*n ids, then k losses); n = k*B*T ids per side
+    int* hs_dev = nullptr;
+    int* hs_pinned = nullptr;
+    size_t hs_n = 0;
+    int hs_k = 0;
     Timing timing;
 };
 
@@ -198,6 +209,8 @@ void free_model(Model* m) {
     cudaFree(m->mom_v);
     cudaFree(m->d_err);
     cudaFree(m->d_hyper);
+    cudaFree(m->hs_dev);
+    if (m->hs_pinned) cudaFreeHost(m->hs_pinned);
     if (m->graph_exec) cudaGraphExecDestroy(m->graph_exec);
     if (m->graph) cudaGraphDestroy(m->graph);
     for (cudaEvent_t e : m->timing.ev) cudaEventDestroy(e);
@@ -281,6 +294,7 @@ int alloc_acts(Model* m, int B, int T) {
         {(void**)&m->enc_counts, (size_t)m->Vp * 4}, {(void**)&m->enc_offsets, ((size_t)m->Vp + 1) * 4},
         {(void**)&m->enc_cursor, (size_t)m->Vp * 4}, {(void**)&m->enc_order, BT * 4},
         {(void**)&m->enc_sorted, BT * 4},
+        {(void**)&m->coins, BT * 4}, {(void**)&m->sampled, (size_t)B * 4},
     };
     size_t total = 0;
     for (auto& it : items) total += align256(it.bytes);
@@ -619,14 +633,28 @@ int to_host_f32(Model* m, float* host, const void* src, size_t n, DType dt) {
 }  // namespace
 
 namespace {
+// llm.c "train_gpt2.cu", random_u32: xorshift* on the 64-bit state
+uint32_t random_u32(unsigned long long* state) {
+    unsigned long long x = *state;
+    x ^= x >> 12;
+    x ^= x << 25;
+    x ^= x >> 27;
+    *state = x;
+    return (uint32_t)((x * 0x2545F4914F6CDD1DULL) >> 32);
+}
+
+// hyper != NULL: the launch is being recorded and reads its hyperparameters
+// (and the rounding seed) from device memory at replay time
 int run_adamw(Model* m, float lr, float beta1, float beta2, float eps, float weight_decay, int step,
               const float* hyper) {
     const float c1 = 1.0f - powf(beta1, (float)step);
     const float c2 = 1.0f - powf(beta2, (float)step);
-    const double bytes = (double)m->nparams * (m->master ? (2 * m->esz + 24) : (4.0 * 7));
+    const double bytes = (double)m->nparams *
+                         (m->master ? (2 * m->esz + 24) : m->sr ? (3.0 * m->esz + 16) : (4.0 * 7));
+    const uint32_t seed = m->sr && !hyper ? random_u32(&m->rng_state) : 0u;
     TIMED(FAM_ADAMW, bytes,
           launch_adamw(m->dt, m->params, m->master, m->grads, m->mom_m, m->mom_v, m->nparams, lr,
-                       beta1, beta2, c1, c2, eps, weight_decay, hyper, m->stream));
+                       beta1, beta2, c1, c2, eps, weight_decay, hyper, m->stream, m->sr, seed));
     CUDA_TRY(cudaGetLastError());
     return GPT2_OK;
 }
@@ -810,6 +838,11 @@ int gpt2_set_grad_accum(int k) {
     return GPT2_OK;
 }
 
+int gpt2_get_grad_accum(void) {
+    TRY(check_model());
+    return g->grad_accum;
+}
+
 int gpt2_backward(void) {
     TRY(check_model());
     if (!g->fwd_done || !g->fwd_targets)
@@ -842,7 +875,8 @@ int gpt2_train_step(const int* d_tokens, const int* d_targets, int B, int T, flo
                       m->g_accum == m->grad_accum;
     if (same && !m->timing.on) {
         const float c1 = 1.0f - powf(beta1, (float)step), c2 = 1.0f - powf(beta2, (float)step);
-        launch_set_hyper(m->d_hyper, lr, beta1, beta2, c1, c2, eps, weight_decay, m->stream);
+        const uint32_t seed = m->sr ? random_u32(&m->rng_state) : 0u;
+        launch_set_hyper(m->d_hyper, lr, beta1, beta2, c1, c2, eps, weight_decay, seed, m->stream);
         CUDA_TRY(cudaGraphLaunch(m->graph_exec, m->stream));
         note_launch((int)m->g_launches);
         m->fwd_done = 1;
@@ -902,6 +936,46 @@ int gpt2_train_step(const int* d_tokens, const int* d_targets, int B, int T, flo
     return GPT2_OK;
 }
 
+int gpt2_train_step_host(const int* tokens, const int* targets, int B, int T, float lr, float beta1,
+                         float beta2, float eps, float weight_decay, int step, float* mean_loss) {
+    TRY(check_model());
+    Model* m = g;
+    if (!tokens || !targets) return fail(GPT2_ERR_ARG, "tokens and targets are required");
+    if (B <= 0 || T <= 0) return fail(GPT2_ERR_ARG, "B=%d T=%d must be positive", B, T);
+    const int k = m->grad_accum;
+    const size_t n = (size_t)k * B * T;
+    for (size_t i = 0; i < n; i++)
+        if (tokens[i] < 0 || tokens[i] >= m->V || targets[i] < 0 || targets[i] >= m->V)
+            return fail(GPT2_ERR_TOKEN, "id at position %zu outside [0, %d)", i, m->V);
+    // device ids and pinned staging, kept for the next calls of the same size
+    if (m->hs_n != n || m->hs_k != k) {
+        CUDA_TRY(cudaStreamSynchronize(m->stream));
+        cudaFree(m->hs_dev);
+        if (m->hs_pinned) cudaFreeHost(m->hs_pinned);
+        m->hs_dev = nullptr;
+        m->hs_pinned = nullptr;
+        m->hs_n = 0;
+        const size_t bytes = (2 * n + (size_t)k) * 4;
+        CUDA_TRY(cudaMalloc((void**)&m->hs_dev, bytes + 256));
+        CUDA_TRY(cudaMallocHost((void**)&m->hs_pinned, bytes + 256));
+        m->hs_n = n;
+        m->hs_k = k;
+    }
+    // the previous call synchronised, so its copies out of the staging are done
+    memcpy(m->hs_pinned, tokens, n * 4);
+    memcpy(m->hs_pinned + n, targets, n * 4);
+    CUDA_TRY(cudaMemcpyAsync(m->hs_dev, m->hs_pinned, 2 * n * 4, cudaMemcpyHostToDevice, m->stream));
+    float* d_loss = (float*)(m->hs_dev + 2 * n);
+    TRY(gpt2_train_step(m->hs_dev, m->hs_dev + n, B, T, lr, beta1, beta2, eps, weight_decay, step,
+                        d_loss));
+    float* h_loss = (float*)(m->hs_pinned + 2 * n);
+    CUDA_TRY(cudaMemcpyAsync(h_loss, d_loss, (size_t)k * 4, cudaMemcpyDeviceToHost, m->stream));
+    CUDA_TRY(cudaStreamSynchronize(m->stream));
+    TRY(read_err(m));
+    if (mean_loss) memcpy(mean_loss, h_loss, (size_t)k * 4);
+    return GPT2_OK;
+}
+
 int gpt2_sync(void) {
     TRY(check_model());
     CUDA_TRY(cudaStreamSynchronize(g->stream));
@@ -929,10 +1003,35 @@ int gpt2_get_grads(float* host) {
     return to_host_f32(g, host, g->grads, g->nparams, g->dt);
 }
 
+int gpt2_set_master_weights(int enabled) {
+    TRY(check_model());
+    Model* m = g;
+    if (m->prec != GPT2_BF16)
+        return enabled ? GPT2_OK : fail(GPT2_ERR_CONFIG, "only bf16 training runs without master weights");
+    if (enabled && !m->master) {
+        CUDA_TRY(cudaStreamSynchronize(m->stream));
+        CUDA_TRY(cudaMalloc((void**)&m->master, m->nparams * 4 + 256));
+        launch_to_f32(m->dt, m->master, m->params, m->nparams, m->stream);
+        m->sr = false;
+    } else if (!enabled && m->master) {
+        CUDA_TRY(cudaStreamSynchronize(m->stream));
+        cudaFree(m->master);
+        m->master = nullptr;
+        m->sr = true;
+    }
+    // a recorded step holds the old update kernel
+    if (m->graph_exec) cudaGraphExecDestroy(m->graph_exec);
+    if (m->graph) cudaGraphDestroy(m->graph);
+    m->graph_exec = nullptr;
+    m->graph = nullptr;
+    CUDA_TRY(cudaGetLastError());
+    return GPT2_OK;
+}
+
 int gpt2_get_master(float* host) {
     TRY(check_model());
     if (!host) return fail(GPT2_ERR_ARG, "host is NULL");
-    if (!g->master) return fail(GPT2_ERR_STATE, "no master weights in fp32 mode");
+    if (!g->master) return fail(GPT2_ERR_STATE, "no master weights (fp32 mode, or turned off)");
     return to_host_f32(g, host, g->master, g->nparams, DT_F32);
 }
 
@@ -1000,13 +1099,78 @@ int gpt2_get_activation(int which, int layer, float* host, size_t* n_out) {
         case GPT2_ACT_LNF: src = m->lnf; n = BT * C; break;
         case GPT2_ACT_LOGITS: src = m->logits; n = BT * m->Vp; break;
         case GPT2_ACT_LSE: n = (size_t)m->B * m->NH * m->T; src = m->lse + layer * n; dt = DT_F32; break;
+        case GPT2_ACT_PROBS: n = BT * m->Vp; break;
         default: return fail(GPT2_ERR_ARG, "unknown activation %d", which);
     }
     if (n_out) *n_out = n;
     if (!host) return GPT2_OK;
+    if (which == GPT2_ACT_PROBS) {
+        if (m->fwd_targets || !m->fwd_done)
+            return fail(GPT2_ERR_STATE, "probabilities need a preceding forward without targets");
+        float* tmp = nullptr;
+        CUDA_TRY(cudaMalloc(&tmp, n * 4 + 16));
+        launch_probs(m->dt, tmp, m->logits, (int)BT, m->V, m->Vp, m->stream);
+        cudaError_t e = cudaMemcpyAsync(host, tmp, n * 4, cudaMemcpyDeviceToHost, m->stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(m->stream);
+        cudaFree(tmp);
+        if (e != cudaSuccess) return fail(GPT2_ERR_CUDA, "probs: %s", cudaGetErrorString(e));
+        return GPT2_OK;
+    }
     if (m->L == 0 && (which >= GPT2_ACT_LN1 && which <= GPT2_ACT_RESIDUAL3))
         return fail(GPT2_ERR_ARG, "no layers");
     return to_host_f32(m, host, src, n, dt);
+}
+
+int gpt2_sample(int t, const float* coins, int* out) {
+    TRY(check_model());
+    Model* m = g;
+    if (!coins || !out) return fail(GPT2_ERR_ARG, "coins and out are required");
+    if (!m->acts || !m->fwd_done || m->fwd_targets)
+        return fail(GPT2_ERR_STATE, "sampling needs a preceding forward without targets");
+    if (t < 0 || t >= m->T) return fail(GPT2_ERR_ARG, "position t=%d outside [0, %d)", t, m->T);
+    const int B = m->B;
+    for (int b = 0; b < B; b++)
+        if (!(coins[b] >= 0.f && coins[b] < 1.f)) return fail(GPT2_ERR_ARG, "coin %d outside [0, 1)", b);
+    CUDA_TRY(cudaMemcpyAsync(m->coins, coins, (size_t)B * 4, cudaMemcpyHostToDevice, m->stream));
+    launch_sample(m->dt, (const char*)m->logits + (size_t)t * m->Vp * m->esz, (long long)m->T * m->Vp, B,
+                  m->V, m->coins, m->sampled, 1, m->stream);
+    CUDA_TRY(cudaMemcpyAsync(out, m->sampled, (size_t)B * 4, cudaMemcpyDeviceToHost, m->stream));
+    CUDA_TRY(cudaStreamSynchronize(m->stream));
+    return GPT2_OK;
+}
+
+int gpt2_generate(int* tokens, int B, int T, int t_begin, int t_end, unsigned long long* rng_state) {
+    TRY(check_model());
+    Model* m = g;
+    if (!tokens || !rng_state) return fail(GPT2_ERR_ARG, "tokens and rng_state are required");
+    TRY(check_shape(m, B, T));
+    if (t_begin < 1 || t_end > T || t_begin > t_end)
+        return fail(GPT2_ERR_ARG, "positions [%d, %d) must lie in [1, T=%d]", t_begin, t_end, T);
+    const size_t n = (size_t)B * T;
+    for (size_t i = 0; i < n; i++)
+        if (tokens[i] < 0 || tokens[i] >= m->V)
+            return fail(GPT2_ERR_TOKEN, "id at position %zu outside [0, %d)", i, m->V);
+    // every coin up front, in the order the loop draws them (t, then b)
+    std::vector<float> coins((size_t)(t_end - t_begin) * B);
+    unsigned long long st = *rng_state;
+    for (float& c : coins) c = (float)(random_u32(&st) >> 8) / 16777216.0f;
+    CUDA_TRY(cudaMemcpyAsync(m->tokens, tokens, n * 4, cudaMemcpyHostToDevice, m->stream));
+    if (!coins.empty())
+        CUDA_TRY(cudaMemcpyAsync(m->coins, coins.data(), coins.size() * 4, cudaMemcpyHostToDevice, m->stream));
+    for (int t = t_begin; t < t_end; t++) {
+        TRY(run_forward(m, false));
+        // the distribution at position t-1 gives the token at position t
+        launch_sample(m->dt, (const char*)m->logits + (size_t)(t - 1) * m->Vp * m->esz,
+                      (long long)T * m->Vp, B, m->V, m->coins + (size_t)(t - t_begin) * B, m->tokens + t,
+                      T, m->stream);
+    }
+    CUDA_TRY(cudaMemcpyAsync(tokens, m->tokens, n * 4, cudaMemcpyDeviceToHost, m->stream));
+    CUDA_TRY(cudaStreamSynchronize(m->stream));
+    TRY(read_err(m));
+    *rng_state = st;
+    m->fwd_done = 1;
+    m->fwd_targets = 0;
+    return GPT2_OK;
 }
 
 int gpt2_free(void) {

@@ -110,6 +110,12 @@ void launch_reduce_partials_multi(DType dt, const PartialDesc* d_desc, int ndesc
 void launch_classifier(DType dt, void* logits, float* losses, const int* targets, int BT, int V,
                        int Vp, float dloss, cudaStream_t s);
 void launch_mean(const float* x, int n, float* out, cudaStream_t s);
+// probs (rows, Vp) fp32 = softmax over the first V columns of logits (rows, Vp); 0 on the padding
+void launch_probs(DType dt, float* probs, const void* logits, int rows, int V, int Vp, cudaStream_t s);
+// per row r: the index sampled from softmax(logits[r*row_stride + 0 .. V)) with coins[r]
+// (llm.c sample_softmax), written to out[r * out_stride]
+void launch_sample(DType dt, const void* logits, long long row_stride, int rows, int V, const float* coins,
+                   int* out, long long out_stride, cudaStream_t s);
 // ranges of the flat parameter buffers one AdamW launch updates (offsets and
 // counts are multiples of 4)
 struct AdamRanges {
@@ -117,15 +123,18 @@ struct AdamRanges {
 };
 void launch_adamw_ranges(DType dt, void* params, float* master, const void* grads, float* m,
                          float* v, const AdamRanges& r, int nranges, float lr, float b1, float b2,
-                         float c1, float c2, float eps, float wd, const float* hyper, cudaStream_t s);
-// hyper: NULL, or device floats {lr, b1, b2, c1, c2, eps, wd} that replace the
-// by-value ones (a CUDA graph replays the launch with new values there)
+                         float c1, float c2, float eps, float wd, const float* hyper, cudaStream_t s,
+                         bool stochastic = false, uint32_t seed = 0);
+// hyper: NULL, or device floats {lr, b1, b2, c1, c2, eps, wd, seed bits} that
+// replace the by-value ones (a CUDA graph replays the launch with new values
+// there). stochastic (bf16 only): no master copy; the fp32 update is rounded
+// to the bf16 parameter stochastically with this step's seed.
 void launch_adamw(DType dt, void* params, float* master, const void* grads, float* m, float* v,
                   size_t n, float lr, float b1, float b2, float c1, float c2, float eps, float wd,
-                  const float* hyper, cudaStream_t s);
-// writes {lr, b1, b2, c1, c2, eps, wd} to h with a one-thread kernel
+                  const float* hyper, cudaStream_t s, bool stochastic = false, uint32_t seed = 0);
+// writes {lr, b1, b2, c1, c2, eps, wd, seed bits} to h with a one-thread kernel
 void launch_set_hyper(float* h, float lr, float b1, float b2, float c1, float c2, float eps, float wd,
-                      cudaStream_t s);
+                      uint32_t seed, cudaStream_t s);
 void launch_zero(void* p, size_t bytes, cudaStream_t s);
 void launch_init_normal(DType dt, void* p, size_t n, float stddev, unsigned long long seed,
                         unsigned long long stream_id, cudaStream_t s);

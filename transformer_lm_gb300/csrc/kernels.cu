@@ -1361,6 +1361,124 @@ void launch_classifier(DType dt, void* logits, float* losses, const int* targets
         launch_pdl(classifier_k<float>, BT, CLS_BLOCK, 0, s, (float*)logits, losses, targets, V, Vp, dloss);
 }
 
+// ------------------------------------------------------------------ inference
+// Probabilities of the tied classifier (fused_classifier_kernel3's probs
+// output, for a forward without targets): probs[r][i] = softmax over i < V of
+// logits[r][:], 0 on the padding [V, Vp). One block per row.
+template <typename T>
+__global__ void __launch_bounds__(512) probs_k(float* __restrict__ probs, const T* __restrict__ logits,
+                                               int V, int Vp) {
+    pdl_enter();
+    __shared__ float s_red[32];
+    const T* x = logits + (size_t)blockIdx.x * Vp;
+    float* y = probs + (size_t)blockIdx.x * Vp;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x / 32, nw = blockDim.x / 32;
+    float m = -INFINITY;
+    for (int i = threadIdx.x; i < V; i += blockDim.x) m = fmaxf(m, to_f(x[i]));
+    m = warp_max(m);
+    if (lane == 0) s_red[warp] = m;
+    __syncthreads();
+    m = warp_max(lane < nw ? s_red[lane] : -INFINITY);
+    __syncthreads();
+    float sum = 0.f;
+    for (int i = threadIdx.x; i < V; i += blockDim.x) sum += expf(to_f(x[i]) - m);
+    sum = warp_sum(sum);
+    if (lane == 0) s_red[warp] = sum;
+    __syncthreads();
+    sum = warp_sum(lane < nw ? s_red[lane] : 0.f);
+    const float inv = 1.f / sum;
+    for (int i = threadIdx.x; i < Vp; i += blockDim.x) y[i] = i < V ? expf(to_f(x[i]) - m) * inv : 0.f;
+}
+
+void launch_probs(DType dt, float* probs, const void* logits, int rows, int V, int Vp, cudaStream_t s) {
+    note_launch(1);
+    if (dt == DT_BF16) launch_pdl(probs_k<bf16>, rows, 512, 0, s, probs, (const bf16*)logits, V, Vp);
+    else launch_pdl(probs_k<float>, rows, 512, 0, s, probs, (const float*)logits, V, Vp);
+}
+
+// sample_softmax on the device: one block per row r, logits row at
+// logits + r * row_stride; with p = softmax over i < V and the coin c in
+// [0, 1), the sample is the first i whose cumulative probability exceeds c
+// (V - 1 if rounding leaves none). The row max is subtracted before
+// exponentiating (same probabilities, no overflow). Thread j owns the
+// contiguous index range [j*chunk, (j+1)*chunk); the block scans the range
+// sums, and the thread whose range holds c * sum walks it in index order.
+// The index goes to out[r * out_stride].
+constexpr int SAMPLE_BLOCK = 1024;
+
+template <typename T>
+__global__ void __launch_bounds__(SAMPLE_BLOCK) sample_k(const T* __restrict__ logits, long long row_stride,
+                                                         int V, const float* __restrict__ coins,
+                                                         int* __restrict__ out, long long out_stride) {
+    pdl_enter();
+    __shared__ float s_red[32];
+    __shared__ int s_idx;
+    const T* x = logits + (size_t)blockIdx.x * row_stride;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x / 32;
+    constexpr int NW = SAMPLE_BLOCK / 32;
+    float m = -INFINITY;
+    for (int i = threadIdx.x; i < V; i += SAMPLE_BLOCK) m = fmaxf(m, to_f(x[i]));
+    m = warp_max(m);
+    if (lane == 0) s_red[warp] = m;
+    if (threadIdx.x == 0) s_idx = V - 1;
+    __syncthreads();
+    m = warp_max(s_red[lane]);
+    __syncthreads();
+    const int chunk = (V + SAMPLE_BLOCK - 1) / SAMPLE_BLOCK;
+    const int i0 = min(V, (int)threadIdx.x * chunk), i1 = min(V, i0 + chunk);
+    float own = 0.f;
+    for (int i = i0; i < i1; i++) own += expf(to_f(x[i]) - m);
+    // inclusive scan of the range sums: within the warp, then over warps
+    float inc = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
+    }
+    if (lane == 31) s_red[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        float w = s_red[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float t = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += t;
+        }
+        s_red[lane] = w;
+    }
+    __syncthreads();
+    const float before = warp > 0 ? s_red[warp - 1] : 0.f;
+    inc += before;
+    const float excl = inc - own;
+    const float target = coins[blockIdx.x] * s_red[NW - 1];
+    if (target < inc && i1 > i0) {
+        // this range or an earlier one holds the sample: the first such range wins
+        float cdf = excl;
+        int idx = i1 - 1;
+        for (int i = i0; i < i1; i++) {
+            cdf += expf(to_f(x[i]) - m);
+            if (target < cdf) {
+                idx = i;
+                break;
+            }
+        }
+        atomicMin(&s_idx, idx);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) out[(size_t)blockIdx.x * out_stride] = s_idx;
+}
+
+void launch_sample(DType dt, const void* logits, long long row_stride, int rows, int V, const float* coins,
+                   int* out, long long out_stride, cudaStream_t s) {
+    note_launch(1);
+    if (dt == DT_BF16)
+        launch_pdl(sample_k<bf16>, rows, SAMPLE_BLOCK, 0, s, (const bf16*)logits, row_stride, V, coins, out,
+                   out_stride);
+    else
+        launch_pdl(sample_k<float>, rows, SAMPLE_BLOCK, 0, s, (const float*)logits, row_stride, V, coins, out,
+                   out_stride);
+}
+
 // mean of n floats in a fixed order (single block)
 __global__ void __launch_bounds__(1024) mean_k(const float* __restrict__ x, int n,
                                                float* __restrict__ out) {
@@ -1396,15 +1514,61 @@ DEVI float adamw_one(float g, float& m, float& v, float theta, float lr, float b
     return theta - lr * (mh / (sqrtf(vh) + eps) + wd * theta);
 }
 
-template <typename T>
+// adamw_kernel3 without master weights: the update in fp32, operation by
+// operation as the page writes it (lerp as two FMAs; the rn intrinsics keep
+// the compiler from contracting or reordering), then stochastic rounding of
+// the result to bf16. Element `idx` of the flat buffer is the page's thread
+// idx % 512 of block idx / 512; its random word is the SquirrelNoise5 hash of
+// that position under the step's seed, hashed once more with the same
+// position by the page's bf16 rounding routine.
+DEVI uint32_t squirrel_noise5(uint32_t pos, uint32_t seed) {
+    uint32_t b = pos * 0xd2a80a3fu;
+    b += seed;
+    b ^= b >> 9;
+    b += 0xa884f197u;
+    b ^= b >> 11;
+    b *= 0x6C736F4Bu;
+    b ^= b >> 13;
+    b += 0xB79F3ABBu;
+    b ^= b >> 15;
+    b *= 0x1b56c4f5u;
+    b ^= b >> 17;
+    return b;
+}
+DEVI uint32_t noise_2d(uint32_t x, uint32_t y, uint32_t seed) {
+    return squirrel_noise5(x + 198491317u * y, seed);
+}
+DEVI bf16 round_bf16_stochastic(float p, size_t idx, uint32_t seed) {
+    const uint32_t x = (uint32_t)(idx & 511), y = (uint32_t)(idx >> 9);
+    const uint32_t rnd = noise_2d(x, y, noise_2d(x, y, seed));
+    uint32_t bits = __float_as_uint(p);
+    bits = (bits & 0xFFFFu) > (rnd & 0xFFFFu) ? (bits | 0xFFFFu) : (bits & ~0xFFFFu);
+    return __float2bfloat16_rn(__uint_as_float(bits));
+}
+DEVI float adamw_one_sr(float g, float& m, float& v, float old, float lr, float b1, float b2,
+                        float c1, float c2, float eps, float wd) {
+    m = __fmaf_rn(b1, m, __fmaf_rn(-b1, g, g));
+    const float gg = __fmul_rn(g, g);
+    v = __fmaf_rn(b2, v, __fmaf_rn(-b2, gg, gg));
+    const float mh = __fdiv_rn(m, c1), vh = __fdiv_rn(v, c2);
+    const float den = __fadd_rn(__fsqrt_rn(vh), eps);
+    const float upd = __fadd_rn(__fdiv_rn(mh, den), __fmul_rn(wd, old));
+    return __fsub_rn(old, __fmul_rn(lr, upd));
+}
+
+// SR: bf16 parameters without a master copy, updated in place with
+// stochastic rounding (seed: this step's, or hyper[7] in graph replays)
+template <typename T, bool SR>
 __global__ void adamw_k(T* __restrict__ params, float* __restrict__ master,
                         const T* __restrict__ grads, float* __restrict__ mst,
                         float* __restrict__ vst, const AdamRanges r, float lr, float b1, float b2,
-                        float c1, float c2, float eps, float wd, const float* __restrict__ hyper) {
+                        float c1, float c2, float eps, float wd, uint32_t seed,
+                        const float* __restrict__ hyper) {
     pdl_enter();
     if (hyper) {  // hyperparameters from device memory (graph replays)
         lr = hyper[0]; b1 = hyper[1]; b2 = hyper[2]; c1 = hyper[3]; c2 = hyper[4];
         eps = hyper[5]; wd = hyper[6];
+        seed = __float_as_uint(hyper[7]);
     }
     // this block row's range of the flat parameter buffers
     const size_t off = r.off[blockIdx.y], n = r.n[blockIdx.y];
@@ -1428,7 +1592,7 @@ __global__ void adamw_k(T* __restrict__ params, float* __restrict__ master,
                 float4 g4 = __ldcs(reinterpret_cast<const float4*>(grads + i));
                 g[0] = g4.x; g[1] = g4.y; g[2] = g4.z; g[3] = g4.w;
             }
-            if (master) {
+            if (!SR && master) {
                 float4 t4 = __ldcs(reinterpret_cast<const float4*>(master + i));
                 th[0] = t4.x; th[1] = t4.y; th[2] = t4.z; th[3] = t4.w;
             } else {
@@ -1437,17 +1601,22 @@ __global__ void adamw_k(T* __restrict__ params, float* __restrict__ master,
             }
             float mm[4] = {m4.x, m4.y, m4.z, m4.w}, vv[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
-            for (int k = 0; k < 4; k++)
-                th[k] = adamw_one<T>(g[k], mm[k], vv[k], th[k], lr, b1, b2, c1, c2, eps, wd);
+            for (int k = 0; k < 4; k++) {
+                if constexpr (SR) th[k] = adamw_one_sr(g[k], mm[k], vv[k], th[k], lr, b1, b2, c1, c2, eps, wd);
+                else th[k] = adamw_one<T>(g[k], mm[k], vv[k], th[k], lr, b1, b2, c1, c2, eps, wd);
+            }
             __stcs(reinterpret_cast<float4*>(mst + i), make_float4(mm[0], mm[1], mm[2], mm[3]));
             __stcs(reinterpret_cast<float4*>(vst + i), make_float4(vv[0], vv[1], vv[2], vv[3]));
-            if (master)
+            if (!SR && master)
                 __stcs(reinterpret_cast<float4*>(master + i), make_float4(th[0], th[1], th[2], th[3]));
             if constexpr (sizeof(T) == 2) {
                 uint2 praw;
                 bf16* pb = reinterpret_cast<bf16*>(&praw);
 #pragma unroll
-                for (int k = 0; k < 4; k++) pb[k] = from_f<bf16>(th[k]);
+                for (int k = 0; k < 4; k++) {
+                    if constexpr (SR) pb[k] = round_bf16_stochastic(th[k], off + i + k, seed);
+                    else pb[k] = from_f<bf16>(th[k]);
+                }
                 __stcs(reinterpret_cast<uint2*>(params + i), praw);
             } else {
                 __stcs(reinterpret_cast<float4*>(params + i), make_float4(th[0], th[1], th[2], th[3]));
@@ -1455,12 +1624,18 @@ __global__ void adamw_k(T* __restrict__ params, float* __restrict__ master,
         } else {
             for (size_t j = i; j < n; j++) {
                 float mm = mst[j], vv = vst[j];
-                float th = master ? master[j] : to_f(params[j]);
-                th = adamw_one<T>(to_f(grads[j]), mm, vv, th, lr, b1, b2, c1, c2, eps, wd);
+                if constexpr (SR) {
+                    const float th = adamw_one_sr(to_f(grads[j]), mm, vv, to_f(params[j]), lr, b1, b2, c1,
+                                                  c2, eps, wd);
+                    if constexpr (sizeof(T) == 2) params[j] = round_bf16_stochastic(th, off + j, seed);
+                } else {
+                    float th = master ? master[j] : to_f(params[j]);
+                    th = adamw_one<T>(to_f(grads[j]), mm, vv, th, lr, b1, b2, c1, c2, eps, wd);
+                    if (master) master[j] = th;
+                    params[j] = from_f<T>(th);
+                }
                 mst[j] = mm;
                 vst[j] = vv;
-                if (master) master[j] = th;
-                params[j] = from_f<T>(th);
             }
         }
     }
@@ -1468,39 +1643,45 @@ __global__ void adamw_k(T* __restrict__ params, float* __restrict__ master,
 
 void launch_adamw(DType dt, void* params, float* master, const void* grads, float* m, float* v,
                   size_t n, float lr, float b1, float b2, float c1, float c2, float eps, float wd,
-                  const float* hyper, cudaStream_t s) {
+                  const float* hyper, cudaStream_t s, bool stochastic, uint32_t seed) {
     AdamRanges r = {};
     r.off[0] = 0;
     r.n[0] = n;
-    launch_adamw_ranges(dt, params, master, grads, m, v, r, 1, lr, b1, b2, c1, c2, eps, wd, hyper, s);
+    launch_adamw_ranges(dt, params, master, grads, m, v, r, 1, lr, b1, b2, c1, c2, eps, wd, hyper, s,
+                        stochastic, seed);
 }
 
 void launch_adamw_ranges(DType dt, void* params, float* master, const void* grads, float* m,
                          float* v, const AdamRanges& r, int nranges, float lr, float b1, float b2,
-                         float c1, float c2, float eps, float wd, const float* hyper, cudaStream_t s) {
+                         float c1, float c2, float eps, float wd, const float* hyper, cudaStream_t s,
+                         bool stochastic, uint32_t seed) {
     if (nranges <= 0) return;
     size_t nmax = 0;
     for (int i = 0; i < nranges; i++) nmax = r.n[i] > nmax ? r.n[i] : nmax;
     note_launch(1);
     const dim3 grid(grid_for((nmax + 3) / 4, 256, 8), (unsigned)nranges);
-    if (dt == DT_BF16)
-        launch_pdl(adamw_k<bf16>, grid, dim3(256), 0, s, (bf16*)params, master, (const bf16*)grads, m, v, r,
-                   lr, b1, b2, c1, c2, eps, wd, hyper);
+    if (dt == DT_BF16 && stochastic)
+        launch_pdl(adamw_k<bf16, true>, grid, dim3(256), 0, s, (bf16*)params, (float*)nullptr,
+                   (const bf16*)grads, m, v, r, lr, b1, b2, c1, c2, eps, wd, seed, hyper);
+    else if (dt == DT_BF16)
+        launch_pdl(adamw_k<bf16, false>, grid, dim3(256), 0, s, (bf16*)params, master, (const bf16*)grads, m,
+                   v, r, lr, b1, b2, c1, c2, eps, wd, seed, hyper);
     else
-        launch_pdl(adamw_k<float>, grid, dim3(256), 0, s, (float*)params, master, (const float*)grads, m, v,
-                   r, lr, b1, b2, c1, c2, eps, wd, hyper);
+        launch_pdl(adamw_k<float, false>, grid, dim3(256), 0, s, (float*)params, master, (const float*)grads,
+                   m, v, r, lr, b1, b2, c1, c2, eps, wd, seed, hyper);
 }
 
 __global__ void set_hyper_k(float* h, float lr, float b1, float b2, float c1, float c2, float eps,
-                            float wd) {
+                            float wd, uint32_t seed) {
     pdl_enter();
     h[0] = lr; h[1] = b1; h[2] = b2; h[3] = c1; h[4] = c2; h[5] = eps; h[6] = wd;
+    h[7] = __uint_as_float(seed);
 }
 
 void launch_set_hyper(float* h, float lr, float b1, float b2, float c1, float c2, float eps, float wd,
-                      cudaStream_t s) {
+                      uint32_t seed, cudaStream_t s) {
     note_launch(1);
-    launch_pdl(set_hyper_k, 1, 1, 0, s, h, lr, b1, b2, c1, c2, eps, wd);
+    launch_pdl(set_hyper_k, 1, 1, 0, s, h, lr, b1, b2, c1, c2, eps, wd, seed);
 }
 
 // ------------------------------------------------------------------ split-precision operands

@@ -69,8 +69,11 @@ int fused_linear_bias_gelu_softmax(const float* x, const float* W, const float* 
     if (current_device(&dev) != GPT2_OK) return GPT2_ERR_CUDA;
     unsigned int* err = err_word(dev);
     if (!err) return GPT2_ERR_NOMEM;
+    // the split operands are 3 * Kp columns wide and the GEMM's K is an int
+    if (K > (0x7fffffff / 3) - 8)
+        return set_error(GPT2_ERR_ARG, "fused op: K=%d too large for the split product", K);
     const int tile_n = gemm_tc_part_tile_n();
-    const int tiles = (N + tile_n - 1) / tile_n;
+    const int tiles = (int)(((long long)N + tile_n - 1) / tile_n);
     // scratch: the row-tile softmax partials, then the split operands
     // x' (M, 3Kp) and W' (N, 3Kp) in bf16
     const int Kp = (K + 7) / 8 * 8;
@@ -311,7 +314,7 @@ extern "C" int fused_linear_bias_gelu_softmax_noalloc(const float* x, const floa
         return gk::set_error(GPT2_ERR_ALIGN,
                              "fused op (no-alloc): pointers must be 16-byte aligned, K and N multiples of 4");
     const int tile_n = gemm_tc_part_tile_n();
-    const long long tiles = (N + tile_n - 1) / tile_n;
+    const long long tiles = ((long long)N + tile_n - 1) / tile_n;
     if ((long long)M * tiles > NOALLOC_MAX_PARTIALS)
         return gk::set_error(GPT2_ERR_ARG,
                              "fused op (no-alloc): M * ceil(N/256) = %lld exceeds the static scratch "

@@ -22,7 +22,7 @@ ERRORS = {0: "OK", -1: "CONFIG", -2: "STATE", -3: "SHAPE", -4: "TOKEN", -5: "ALI
           -7: "NOMEM", -8: "ARG", -9: "DEVICE_TIMEOUT"}
 
 ACT = dict(encoded=0, ln1=1, qkv=2, atty=4, residual2=5, ln2=6, fch=7, fch_gelu=8, residual3=9,
-           lnf=10, logits=11, lse=18)
+           lnf=10, logits=11, probs=12, lse=18)
 
 EPI = dict(store=0, gelu=1, resid=2, gelu_bwd=3, accum=4)
 
@@ -54,8 +54,10 @@ _SIGS = {
     "gpt2_forward_device": (_i, [_vp, _vp, _i, _i, _vp]),
     "gpt2_zero_grad": (_i, []),
     "gpt2_set_grad_accum": (_i, [_i]),
+    "gpt2_get_grad_accum": (_i, []),
     "gpt2_backward": (_i, []),
     "gpt2_adamw": (_i, [_f, _f, _f, _f, _f, _i]),
+    "gpt2_set_master_weights": (_i, [_i]),
     "gpt2_sync": (_i, []),
     "gpt2_num_params": (_sz, []),
     "gpt2_param_sizes": (_i, [ctypes.POINTER(_sz)]),
@@ -67,6 +69,8 @@ _SIGS = {
     "gpt2_get_losses": (_i, [_fp]),
     "gpt2_get_activation": (_i, [_i, _i, _fp, ctypes.POINTER(_sz)]),
     "gpt2_free": (_i, []),
+    "gpt2_sample": (_i, [_i, _fp, _ip]),
+    "gpt2_generate": (_i, [_ip, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_ulonglong)]),
     "gpt2_last_error": (ctypes.c_char_p, []),
     "gpt2_last_status": (_i, []),
     "gpt2_timing_begin": (_i, [_i]),
@@ -81,6 +85,7 @@ _SIGS = {
     "gpt2_attention_backward": (_i, [_i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "gpt2_device_status": (_i, []),
     "gpt2_train_step": (_i, [_vp, _vp, _i, _i, _f, _f, _f, _f, _f, _i, _vp]),
+    "gpt2_train_step_host": (_i, [_ip, _ip, _i, _i, _f, _f, _f, _f, _f, _i, _fp]),
     "gpt2_layernorm_forward": (_i, [_i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp]),
     "gpt2_layernorm_backward_scratch_floats": (_sz, [_i]),
     "gpt2_layernorm_backward": (_i, [_i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _vp,
@@ -165,6 +170,13 @@ def gpt2_set_grad_accum(k) -> None:
     _check("gpt2_set_grad_accum", lib().gpt2_set_grad_accum(k))
 
 
+def gpt2_get_grad_accum() -> int:
+    k = int(lib().gpt2_get_grad_accum())
+    if k < 1:
+        raise GPT2Error("gpt2_get_grad_accum", k, gpt2_last_error())
+    return k
+
+
 def gpt2_backward() -> None:
     _check("gpt2_backward", lib().gpt2_backward())
 
@@ -173,12 +185,31 @@ def gpt2_adamw(lr, beta1, beta2, eps, weight_decay, step) -> None:
     _check("gpt2_adamw", lib().gpt2_adamw(lr, beta1, beta2, eps, weight_decay, step))
 
 
+def gpt2_set_master_weights(enabled: bool) -> None:
+    _check("gpt2_set_master_weights", lib().gpt2_set_master_weights(int(bool(enabled))))
+
+
 def gpt2_train_step(d_tokens, d_targets, B, T, lr, beta1, beta2, eps, weight_decay, step,
                     d_mean_loss=None) -> None:
     """Forward, zero_grad, backward and AdamW on device buffers (CUDA-graph replays)."""
     _check("gpt2_train_step", lib().gpt2_train_step(ptr(d_tokens), ptr(d_targets), B, T, lr, beta1,
                                                     beta2, eps, weight_decay, step,
                                                     ptr(d_mean_loss)))
+
+
+def gpt2_train_step_host(tokens, targets, B, T, lr, beta1, beta2, eps, weight_decay,
+                         step) -> np.ndarray:
+    """The whole step on host ids (k*B*T each, k = the accumulation count);
+    returns the k micro-step mean losses."""
+    tok, tgt = _ints(tokens), _ints(targets)
+    k = gpt2_get_grad_accum()
+    if tok.size != k * B * T or tgt.size != k * B * T:
+        raise ValueError(f"expected {k}*{B}*{T} token and target ids, got {tok.size}, {tgt.size}")
+    out = np.empty(k, dtype=np.float32)
+    _check("gpt2_train_step_host",
+           lib().gpt2_train_step_host(_as_ip(tok), _as_ip(tgt), B, T, lr, beta1, beta2, eps,
+                                      weight_decay, step, out.ctypes.data_as(_fp)))
+    return out
 
 
 def gpt2_sync() -> None:
@@ -245,6 +276,22 @@ def gpt2_get_activation(name: str, layer: int = 0) -> np.ndarray:
     _check("gpt2_get_activation",
            lib().gpt2_get_activation(which, layer, out.ctypes.data_as(_fp), None))
     return out
+
+
+def gpt2_sample(t: int, coins) -> np.ndarray:
+    c = np.ascontiguousarray(coins, dtype=np.float32).reshape(-1)
+    out = np.empty(c.size, dtype=np.int32)
+    _check("gpt2_sample", lib().gpt2_sample(t, c.ctypes.data_as(_fp), out.ctypes.data_as(_ip)))
+    return out
+
+
+def gpt2_generate(tokens, B, T, t_begin, t_end, rng_state: int):
+    """Returns (tokens (B, T) int32, advanced rng_state)."""
+    tok = np.array(tokens, dtype=np.int32).reshape(-1).copy()
+    st = ctypes.c_ulonglong(rng_state)
+    _check("gpt2_generate", lib().gpt2_generate(tok.ctypes.data_as(_ip), B, T, t_begin, t_end,
+                                                ctypes.byref(st)))
+    return tok.reshape(B, T), int(st.value)
 
 
 def gpt2_free() -> None:

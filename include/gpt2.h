@@ -46,6 +46,9 @@ extern "C" {
 #define GPT2_FP32 0 /* fp32 parameters, gradients and activations (llm.c train_gpt2_fp32.cu) */
 #define GPT2_BF16 1 /* bf16 parameters, gradients and activations; fp32 master weights and AdamW
                        moments (llm.c train_gpt2.cu, default floatX and use_master_weights) */
+#define GPT2_FP16 2 /* fp16 parameters, gradients and activations, fp32 master weights and AdamW
+                       moments (llm.c train_gpt2.cu, the ENABLE_FP16 build: floatX = half), with
+                       dynamic loss scaling (gpt2_set_loss_scaling), which that page lacks */
 
 /* Create the model with seeded random initial weights in bf16 mixed precision on
  * the tensor cores (the llm.c page's default build). Equivalent to
@@ -57,9 +60,10 @@ extern "C" {
  * previous model. Errors: GPT2_ERR_CONFIG, GPT2_ERR_NOMEM, GPT2_ERR_CUDA. */
 int gpt2_init(int L, int C, int NH, int V, int Vp, int maxT, unsigned long long seed);
 
-/* As gpt2_init with an explicit precision (GPT2_FP32 / GPT2_BF16) and
- * tensor_cores: 1 = tcgen05 tensor-core GEMMs and attention (bf16 only),
- * 0 = SIMT FP32-FMA kernels ("-f 0", TF32 off, in llm.c train_gpt2.cu main). */
+/* As gpt2_init with an explicit precision (GPT2_FP32 / GPT2_BF16 / GPT2_FP16)
+ * and tensor_cores: 1 = tcgen05 tensor-core GEMMs and attention (bf16 or fp16
+ * operands), 0 = SIMT FP32-FMA kernels ("-f 0", TF32 off, in llm.c
+ * train_gpt2.cu main). */
 int gpt2_init_ex(int L, int C, int NH, int V, int Vp, int maxT, unsigned long long seed,
                  int precision, int tensor_cores);
 
@@ -207,6 +211,24 @@ int gpt2_sample(int t, const float* coins, int* out);
  * B, T as for gpt2_forward. */
 int gpt2_generate(int* tokens, int B, int T, int t_begin, int t_end, unsigned long long* rng_state);
 
+/* ---- loss scaling (GPT2_FP16 only) ----
+ * fp16 keeps 5 exponent bits, so small gradients underflow and large ones
+ * overflow. The backward is seeded with dloss = scale / (k B T) (the loss
+ * itself and its value are unscaled); gradients are stored scaled. Before
+ * each AdamW update a kernel checks every gradient: if any is inf or NaN the
+ * update is skipped (parameters and moments unchanged) and the scale halves;
+ * otherwise AdamW uses gradient / scale and, after growth_interval updates in
+ * a row without overflow, the scale doubles. The state lives in device memory,
+ * so CUDA-graph replays of gpt2_train_step keep it current. Defaults: scale
+ * 65536 (2^16), growth_interval 2000. gpt2_get_grads / gpt2_set_grads work in
+ * unscaled values.
+ * gpt2_set_loss_scaling: restart with init_scale (a power of two) and
+ * growth_interval >= 1; GPT2_ERR_CONFIG outside GPT2_FP16.
+ * gpt2_get_loss_scale: the current scale (1 outside GPT2_FP16) and the number
+ * of updates skipped so far (either pointer may be NULL); synchronises. */
+int gpt2_set_loss_scaling(float init_scale, int growth_interval);
+int gpt2_get_loss_scale(float* scale, long long* skipped);
+
 /* Release all device memory held by the model. */
 int gpt2_free(void);
 
@@ -237,14 +259,16 @@ long long gpt2_launch_count(void);
  * GELU + Softmax" problem statement: nn.Linear then GELU then softmax over dim 1).
  * x: DEVICE fp32 (M,K) row-major; W: DEVICE fp32 (N,K) row-major (nn.Linear
  * layout); b: DEVICE fp32 (N); out: DEVICE fp32 (M,N) row-major, caller-owned.
- * The GEMM splits each fp32 operand into bf16 halves (hi, lo) and runs
- * hi.hi + hi.lo + lo.hi on the bf16 tensor cores with fp32 accumulation
- * (about 2^-16 relative per product; outputs within 1e-3 relative of fp64).
- * x, W and out must be 16-byte aligned with K % 4 == 0 and N % 4 == 0 (else
- * GPT2_ERR_ALIGN); M, K, N >= 1 (else GPT2_ERR_ARG). Asynchronous on `stream`
- * (a cudaStream_t, NULL = legacy default stream). The first call on a device
- * allocates its scratch (per-row softmax partials and the split operands,
- * 6*(M+N)*K bytes; grown as needed and kept until exit). */
+ * The product kernel splits each fp32 operand into bf16 halves (hi, lo) in
+ * shared memory as its tiles arrive and runs hi.hi + hi.lo + lo.hi on the bf16
+ * tensor cores with fp32 accumulation (about 2^-16 relative per product;
+ * outputs within 1e-3 relative of fp64). x, W, b and out must be 16-byte
+ * aligned with K % 4 == 0 and N % 4 == 0 (else GPT2_ERR_ALIGN); M, K, N >= 1
+ * (else GPT2_ERR_ARG). Asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ * default stream). The first call on a device allocates its scratch (the
+ * per-row softmax partials, 8 * M * ceil(N/256) bytes; grown as needed and
+ * kept until exit). The output is undefined when gpt2_device_status() then
+ * reports GPT2_ERR_DEVICE_TIMEOUT. */
 int fused_linear_bias_gelu_softmax(const float* x, const float* W, const float* b, float* out,
                                    int M, int K, int N, void* stream);
 
@@ -253,27 +277,27 @@ int fused_linear_bias_gelu_softmax(const float* x, const float* W, const float* 
  * memory -- processes whose own pool allocator owns all device memory, where a
  * cudaMalloc behind its back can fail or fragment the pool, and loops that
  * cannot take the device-wide synchronisation a cudaMalloc may imply).
- * Same arguments and errors as fused_linear_bias_gelu_softmax; it calls no
- * cudaMalloc/cudaFree or other allocating routine. Its GEMM is single-pass TF32
- * (operands truncated to a 10-bit mantissa): elementwise error up to a few
- * 1e-3 relative at K = 8192. Its per-row softmax
- * partials live in a static device array of 1 MiB that every GPU loading the
- * library holds until exit, which limits M * ceil(N/256) to 131072 (e.g.
- * M = 1024 rows with N up to 32768); larger sizes return GPT2_ERR_ARG with a
- * message in gpt2_last_error(). Every call shares that array and leaves its
- * contents behind (nothing needs clearing: each call writes every partial it
- * reads); calls whose GPU work overlaps race on it. The first call on a device
- * (with that device current) looks up the array's device address; make that
- * first call before any stream capture. An expired in-kernel wait is reported
- * by gpt2_device_status(). */
+ * Same arguments, errors and arithmetic as fused_linear_bias_gelu_softmax (the
+ * same kernels, so the same output bit for bit, within 1e-3 relative of fp64);
+ * it calls no cudaMalloc/cudaFree or other allocating routine. Its per-row
+ * softmax partials live in a static device array of 1 MiB that every GPU
+ * loading the library holds until exit, which limits M * ceil(N/256) to
+ * 131072 (e.g. M = 1024 rows with N up to 32768); larger sizes return
+ * GPT2_ERR_ARG with a message in gpt2_last_error(). Every call shares that
+ * array and leaves its contents behind (nothing needs clearing: each call
+ * writes every partial it reads); calls whose GPU work overlaps race on it.
+ * The first call on a device (with that device current) looks up the array's
+ * device address; make that first call before any stream capture. An expired
+ * in-kernel wait is reported by gpt2_device_status(), and the output of that
+ * call is then undefined. */
 int fused_linear_bias_gelu_softmax_noalloc(const float* x, const float* W, const float* b,
                                            float* out, int M, int K, int N, void* stream);
 
 /* ---- kernel-level entry points (DEVICE pointers, asynchronous on `stream`) ----
  * gpt2_gemm: D[M,N] = A[M,K] . B[N,K]^T with the step's fused epilogues.
- *  dtype GPT2_FP32 / GPT2_BF16 is the element type of A, B, D, bias, aux, D2;
- *  tensor_cores = 1 selects the tcgen05 kernel (bf16: kind::f16; fp32: kind::tf32,
- *  K-major operands only), 0 the SIMT FP32-FMA kernel.
+ *  dtype GPT2_FP32 / GPT2_BF16 / GPT2_FP16 is the element type of A, B, D, bias,
+ *  aux, D2; tensor_cores = 1 selects the tcgen05 kernel (bf16 and fp16:
+ *  kind::f16; fp32: kind::tf32, K-major operands only), 0 the SIMT FP32-FMA kernel.
  *  Storage: a_kmajor ? A(m,k) = A[m*lda + k] : A[k*lda + m];
  *           b_kmajor ? B(n,k) = B[n*ldb + k] : B[k*ldb + n];  D(m,n) = D[m*ldd + n].
  *  epilogue: 0 D = acc (+ bias[n]); 1 D = acc + bias[n], D2 = gelu(D) (same ldd);
@@ -297,7 +321,7 @@ int gpt2_gemm(int dtype, int tensor_cores, int epilogue, const void* A, long lon
 /* Causal attention forward over a fused (B,T,3,NH,HS) qkv: out (B,T,NH*HS) and
  * lse (B,NH,T) fp32 natural-log sum of exp of the scaled scores (llm.c
  * attention_forward with softmax_forward_kernel5, scale 1/sqrt(HS)).
- * HS = C/NH in {16,32,64,128}; bf16 with tensor_cores and HS == 64 uses the
+ * HS = C/NH in {16,32,64,128}; bf16 or fp16 with tensor_cores and HS == 64 uses the
  * tensor-core flash kernel, everything else the SIMT kernel. */
 int gpt2_attention_forward(int dtype, int tensor_cores, const void* qkv, void* out, float* lse,
                            int B, int T, int C, int NH, void* stream);

@@ -3,11 +3,14 @@ the comparison metrics the tolerances are stated in."""
 import numpy as np
 
 
-def dev(a, dtype="f32"):
+def _torch_dtype(dtype):
     import torch
-    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
-    t = t.to(torch.bfloat16) if dtype == "bf16" else t
-    return t.cuda()
+    return {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[dtype]
+
+
+def dev(a, dtype="f32"):
+    t = __import__("torch").from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+    return t.to(_torch_dtype(dtype)).cuda()
 
 
 def host(t):
@@ -18,8 +21,7 @@ def host(t):
 
 def empty(shape, dtype="f32"):
     import torch
-    return torch.zeros(shape, dtype=torch.bfloat16 if dtype == "bf16" else torch.float32,
-                       device="cuda")
+    return torch.zeros(shape, dtype=_torch_dtype(dtype), device="cuda")
 
 
 def max_rel_floor(got, ref, floor):

@@ -2,10 +2,10 @@
 
 It is for callers that cannot let the library allocate device memory: its
 scratch is a static device array. It must give the operator's result within
-the operator's bound (checked against the CPU oracle), agree with the
-allocating entry point call after call (the shared array keeps the previous
-call's contents), allocate nothing on the device, and refuse sizes beyond
-that array with a clear error.
+the operator's bound (checked against the CPU oracle), equal the allocating
+entry point's output bit for bit call after call (the shared array keeps the
+previous call's contents), allocate nothing on the device, and refuse sizes
+beyond that array with a clear error.
 This file is collected last so that a run stopping at the first failure has
 already run every other test; it also passes on its own in a fresh process.
 """
@@ -18,11 +18,9 @@ from transformer_lm_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
 
-# the bound include/gpt2.h states for this entry point (max elementwise
-# relative error against the exact operator)
-BOUND = 5e-3
-# the two entry points against each other
-TOL = 2e-2
+# the operator's bound (max elementwise relative error against the exact
+# operator), which include/gpt2.h states for this entry point
+BOUND = 1e-3
 
 
 def _dev(M, K, N, seed):
@@ -48,11 +46,10 @@ def test_noalloc_matches_oracle_and_allocating_entry_point_on_two_calls_in_a_row
         alloc = _run(G.fused_linear_bias_gelu_softmax, dev, M, K, N)
         got = _run(G.fused_linear_bias_gelu_softmax_noalloc, dev, M, K, N)
         rel_oracle = np.max(np.abs(got - ref) / np.abs(ref))
-        rel_alloc = np.max(np.abs(got - alloc) / np.abs(alloc))
-        print(f"noalloc {M}x{K}x{N}: max rel err vs oracle {rel_oracle:.2e}, "
-              f"vs allocating entry {rel_alloc:.2e}")
+        print(f"noalloc {M}x{K}x{N}: max rel err vs oracle {rel_oracle:.2e}")
         assert rel_oracle <= BOUND, (M, K, N, rel_oracle)
-        assert rel_alloc <= TOL, (M, K, N, rel_alloc)
+        # the same kernels as the allocating entry point: the same bits
+        assert np.array_equal(got, alloc), (M, K, N)
         np.testing.assert_allclose(got.sum(1), 1.0, atol=1e-5)
 
 

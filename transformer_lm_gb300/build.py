@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgpt2.so")
 
-SOURCES = ["gpt2.cu", "kernels.cu", "gemm_simt.cu", "gemm_tc.cu", "attention.cu", "attention_tc.cu", "attention_bwd_tc.cu", "ops.cu"]
+SOURCES = ["gpt2.cu", "kernels.cu", "gemm_simt.cu", "gemm_tc.cu", "attention.cu", "attention_tc.cu", "attention_bwd_tc.cu", "ops.cu", "fused_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

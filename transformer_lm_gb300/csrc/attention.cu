@@ -601,9 +601,14 @@ static void simt_backward(void* dqkv, const void* dout, const void* qkv, const f
 int launch_attention_forward(DType dt, int tensor_cores, void* out, float* lse, const void* qkv,
                              int B, int T, int C, int NH, cudaStream_t s, unsigned int* err) {
     const int HS = C / NH;
+    if (dt == DT_F16 && tensor_cores && HS == 64) {
+        // tcgen05 kernel (fp16 operands); the SIMT kernel for operands TMA cannot address
+        const int rc = launch_flash_forward_tc(dt, out, lse, qkv, B, T, C, NH, s, err);
+        if (rc != GPT2_ERR_ALIGN) return rc;
+    }
     if (dt == DT_BF16 && tensor_cores && HS == 64) {
         // tcgen05 kernel; the m16n8k16 kernel remains for operands TMA cannot address
-        const int rc = launch_flash_forward_tc(out, lse, qkv, B, T, C, NH, s, err);
+        const int rc = launch_flash_forward_tc(dt, out, lse, qkv, B, T, C, NH, s, err);
         if (rc != GPT2_ERR_ALIGN) return rc;
         note_launch(1);
         dim3 grid((T + fa::BLK - 1) / fa::BLK, B * NH);
@@ -613,6 +618,7 @@ int launch_attention_forward(DType dt, int tensor_cores, void* out, float* lse, 
     }
     note_launch(1);
     if (dt == DT_BF16) simt_forward<bf16>(out, lse, qkv, B, T, C, NH, s);
+    else if (dt == DT_F16) simt_forward<f16>(out, lse, qkv, B, T, C, NH, s);
     else simt_forward<float>(out, lse, qkv, B, T, C, NH, s);
     return GPT2_OK;
 }
@@ -622,9 +628,14 @@ int launch_attention_backward(DType dt, int tensor_cores, void* dqkv, const void
                               int T, int C, int NH, cudaStream_t s, unsigned int* err) {
     const int HS = C / NH;
     const int n = B * NH * T;
+    if (dt == DT_F16 && tensor_cores && HS == 64) {
+        // tcgen05 kernels (fp16 operands); the SIMT kernels for operands TMA cannot address
+        const int rc = launch_flash_backward_tc(dt, dqkv, dout, qkv, out, lse, D, B, T, C, NH, s, err);
+        if (rc != GPT2_ERR_ALIGN) return rc;
+    }
     if (dt == DT_BF16 && tensor_cores && HS == 64) {
         // tcgen05 kernels; the m16n8k16 kernels remain for operands TMA cannot address
-        const int rc = launch_flash_backward_tc(dqkv, dout, qkv, out, lse, D, B, T, C, NH, s, err);
+        const int rc = launch_flash_backward_tc(dt, dqkv, dout, qkv, out, lse, D, B, T, C, NH, s, err);
         if (rc != GPT2_ERR_ALIGN) return rc;
         note_launch(2);
         dim3 grid((T + fa::BLK - 1) / fa::BLK, B * NH);
@@ -640,10 +651,14 @@ int launch_attention_backward(DType dt, int tensor_cores, void* dqkv, const void
     if (dt == DT_BF16)
         attn_rowdot_k<bf16><<<(n + 255) / 256, 256, 0, s>>>(D, (const bf16*)dout, (const bf16*)out,
                                                             B, T, C, NH, HS);
+    else if (dt == DT_F16)
+        attn_rowdot_k<f16><<<(n + 255) / 256, 256, 0, s>>>(D, (const f16*)dout, (const f16*)out,
+                                                           B, T, C, NH, HS);
     else
         attn_rowdot_k<float><<<(n + 255) / 256, 256, 0, s>>>(D, (const float*)dout,
                                                              (const float*)out, B, T, C, NH, HS);
     if (dt == DT_BF16) simt_backward<bf16>(dqkv, dout, qkv, lse, D, B, T, C, NH, s);
+    else if (dt == DT_F16) simt_backward<f16>(dqkv, dout, qkv, lse, D, B, T, C, NH, s);
     else simt_backward<float>(dqkv, dout, qkv, lse, D, B, T, C, NH, s);
     return GPT2_OK;
 }

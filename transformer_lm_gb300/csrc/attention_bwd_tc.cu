@@ -37,6 +37,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <type_traits>
 
 namespace gk {
 namespace fabw {
@@ -63,7 +64,7 @@ constexpr uint32_t TM_S = 0, TM_P = 128, TM_DS = 192, TM_DP = 256, TM_A0 = 384, 
 constexpr float LOG2E = 1.4426950408889634f;
 
 struct BwdArgs {
-    bf16* dqkv;
+    void* dqkv;  // bf16 or fp16, as the operands
     const float* lse;
     const float* D;
     int T, C, NH, BH, nblk, items;
@@ -92,10 +93,12 @@ template <bool DKV> DEVI Item decode_item(const BwdArgs& a, int idx) {
 // the ring and every barrier phase run on counters global to the CTA, so the
 // next item's loads and first MMAs overlap this item's last blocks and its
 // epilogue.
-template <bool DKV>
+// KIND 0: bf16 operands, 2: fp16 (the tcgen05 kind::f16 operand type)
+template <bool DKV, int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     flash_bwd_tc_k(const __grid_constant__ CUtensorMap tqkv, const __grid_constant__ CUtensorMap tdo,
                    const __grid_constant__ BwdArgs a) {
+    using H = typename std::conditional<KIND == 2, f16, bf16>::type;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -251,14 +254,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ---------------- MMA issuers: warp QKW issues S and dP, warp 1 the
         // accumulating MMAs, so neither chain waits behind the other. Each
         // runs its loop as a whole warp; one elected lane issues.
-        const uint32_t idSq = idesc<0>(0, 0, BLK, BLK);  // S, dP: both operands K-major
-        const uint32_t idAcc = idesc<0>(0, 1, BLK, HSZ); // acc += (P|dS) Y: Y is MN-major
+        const uint32_t idSq = idesc<KIND>(0, 0, BLK, BLK);  // S, dP: both operands K-major
+        const uint32_t idAcc = idesc<KIND>(0, 1, BLK, HSZ); // acc += (P|dS) Y: Y is MN-major
         auto ybuf = [&](int g, int which) { return base + OFF_Y + (g % STAGES) * 2 * TILE + which * TILE; };
         auto issue_qk = [&](uint32_t d, uint32_t x, uint32_t y) {
             const uint64_t dx = sdesc(x, 16, 1024), dy = sdesc(y, 16, 1024);
 #pragma unroll
             for (int k = 0; k < HSZ / 16; k++)  // +32 bytes along K per step
-                umma_warp<0, 1>(d, dx + 2 * k, dy + 2 * k, idSq, k ? 1u : 0u);
+                umma_warp<KIND, 1>(d, dx + 2 * k, dy + 2 * k, idSq, k ? 1u : 0u);
         };
         // acc += A Y, A = bf16 pairs in TMEM from column ta (16 rows of K = 8
         // columns per step), Y = 2048 bytes per step
@@ -365,15 +368,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const float sc = (!DKV || is_k) ? a.scale : 1.f;
                 const int col = DKV ? (is_k ? C + it.h * HSZ : 2 * C + it.h * HSZ) + (a0 % 64)
                                     : it.h * HSZ + a0;
-                bf16* dst = a.dqkv + ((size_t)it.b * T + row) * 3 * C + col;
+                H* dst = (H*)a.dqkv + ((size_t)it.b * T + row) * 3 * C + col;
 #pragma unroll
                 for (int d = 0; d < W; d += 8) {
                     uint32_t pk[4];
 #pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        __nv_bfloat162 pr = __floats2bfloat162_rn(v[d + 2 * e] * sc, v[d + 2 * e + 1] * sc);
-                        pk[e] = *reinterpret_cast<uint32_t*>(&pr);
-                    }
+                    for (int e = 0; e < 4; e++) pk[e] = f2_h2<H>(v[d + 2 * e] * sc, v[d + 2 * e + 1] * sc);
                     *reinterpret_cast<uint4*>(dst + d) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
             }
@@ -427,10 +427,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // P^T as bf16 pairs into TMEM, once the previous dV MMA read it
                     uint32_t pk[16];
 #pragma unroll
-                    for (int e = 0; e < 16; e++) {
-                        __nv_bfloat162 pr = __floats2bfloat162_rn(P[2 * e], P[2 * e + 1]);
-                        pk[e] = *reinterpret_cast<uint32_t*>(&pr);
-                    }
+                    for (int e = 0; e < 16; e++) pk[e] = f2_h2<H>(P[2 * e], P[2 * e + 1]);
                     if (!wait_warp(p_empty, par ^ 1u)) { ok = false; break; }
                     tc_fence_after();
                     tmem_st16_nowait(tP, pk);
@@ -459,10 +456,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                                  fadd2(make_float2(v[e], v[e + 1]), make_float2(-d4.x, -d4.y)));
                         const float2 s23 = fmul2(make_float2(P[e + 2], P[e + 3]),
                                                  fadd2(make_float2(v[e + 2], v[e + 3]), make_float2(-d4.z, -d4.w)));
-                        __nv_bfloat162 lo = __floats2bfloat162_rn(s01.x, s01.y);
-                        __nv_bfloat162 hi = __floats2bfloat162_rn(s23.x, s23.y);
-                        dsk[e >> 1] = *reinterpret_cast<uint32_t*>(&lo);
-                        dsk[(e >> 1) + 1] = *reinterpret_cast<uint32_t*>(&hi);
+                        dsk[e >> 1] = f2_h2<H>(s01.x, s01.y);
+                        dsk[(e >> 1) + 1] = f2_h2<H>(s23.x, s23.y);
                     }
                 }
                 if (!wait_warp(ds_empty, par ^ 1u)) { ok = false; break; }
@@ -516,8 +511,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // D_i = dO_i . O_i for every (b, h, i), eight threads per row (16-byte loads)
-__global__ void rowdot64_k(float* __restrict__ D, const bf16* __restrict__ dout,
-                           const bf16* __restrict__ out, int T, int C, int NH, int nrows) {
+template <typename H>
+__global__ void rowdot64_k(float* __restrict__ D, const H* __restrict__ dout,
+                           const H* __restrict__ out, int T, int C, int NH, int nrows) {
     pdl_enter();
     const int idx = blockIdx.x * blockDim.x + threadIdx.x;
     const int row = idx >> 3, part = idx & 7;
@@ -526,7 +522,7 @@ __global__ void rowdot64_k(float* __restrict__ D, const bf16* __restrict__ dout,
         const int bh = row / T, t = row % T;
         const int b = bh / NH, h = bh % NH;
         const size_t off = ((size_t)b * T + t) * C + (size_t)h * HSZ + part * 8;
-        const Vec16<bf16> g = ld16(dout + off), o = ld16(out + off);
+        const Vec16<H> g = ld16(dout + off), o = ld16(out + off);
 #pragma unroll
         for (int e = 0; e < 8; e++) s = fmaf(to_f(g.v[e]), to_f(o.v[e]), s);
     }
@@ -550,26 +546,27 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// (B, T, width) bf16 as a 3-D tensor (width, T, B) with 64 x 128 x 1 boxes
-static int make_map(CUtensorMap* tm, const void* p, int width, int T, int B) {
+// (B, T, width) bf16 or fp16 as a 3-D tensor (width, T, B) with 64 x 128 x 1 boxes
+static int make_map(CUtensorMap* tm, DType dt, const void* p, int width, int T, int B) {
     auto fn = encode_fn();
     if (!fn) return set_error(GPT2_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
     cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)T, (cuuint64_t)B};
     cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)T * width * 2};
     cuuint32_t box[3] = {HSZ, BLK, 1};
     cuuint32_t es[3] = {1, 1, 1};
-    if (fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p), dims, strides, box, es,
+    if (fn(tm, dt == DT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+           const_cast<void*>(p), dims, strides, box, es,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return set_error(GPT2_ERR_CUDA, "flash backward: tensor map encoding failed");
     return GPT2_OK;
 }
 
-template <bool DKV> static int opt_in() {
+template <bool DKV, int KIND> static int opt_in() {
     static bool done = false;
     if (done) return GPT2_OK;
-    const cudaError_t e =
-        cudaFuncSetAttribute(flash_bwd_tc_k<DKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    const cudaError_t e = cudaFuncSetAttribute(flash_bwd_tc_k<DKV, KIND>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess)
         return set_error(GPT2_ERR_CUDA, "flash backward: shared-memory opt-in failed: %s", cudaGetErrorString(e));
     done = true;
@@ -579,24 +576,30 @@ template <bool DKV> static int opt_in() {
 }  // namespace fabw
 
 // D = rowsum(dO * O), then dQ (query tiles) and dK, dV (key tiles)
-int launch_flash_backward_tc(void* dqkv, const void* dout, const void* qkv, const void* out,
+int launch_flash_backward_tc(DType dt, void* dqkv, const void* dout, const void* qkv, const void* out,
                              const float* lse, float* D, int B, int T, int C, int NH, cudaStream_t s,
                              unsigned int* err) {
     using namespace fabw;
+    if (dt != DT_BF16 && dt != DT_F16) return set_error(GPT2_ERR_CONFIG, "flash backward: 16-bit operands only");
+    const bool h16 = dt == DT_F16;
     if ((uintptr_t)qkv % 16 || (uintptr_t)dout % 16 || (uintptr_t)out % 16 || C % 64 || C / NH != HSZ)
         return set_error(GPT2_ERR_ALIGN, "flash backward: 16-byte aligned operands and head size 64 needed");
     CUtensorMap tqkv, tdo;
-    int rc = make_map(&tqkv, qkv, 3 * C, T, B);
-    if (rc == GPT2_OK) rc = make_map(&tdo, dout, C, T, B);
-    if (rc == GPT2_OK) rc = opt_in<true>();
-    if (rc == GPT2_OK) rc = opt_in<false>();
+    int rc = make_map(&tqkv, dt, qkv, 3 * C, T, B);
+    if (rc == GPT2_OK) rc = make_map(&tdo, dt, dout, C, T, B);
+    if (rc == GPT2_OK) rc = h16 ? opt_in<true, 2>() : opt_in<true, 0>();
+    if (rc == GPT2_OK) rc = h16 ? opt_in<false, 2>() : opt_in<false, 0>();
     if (rc != GPT2_OK) return rc;
     const int nrows = B * NH * T;
     note_launch(3);
-    launch_pdl(rowdot64_k, dim3((nrows * 8 + 255) / 256), dim3(256), 0, s, D, (const bf16*)dout,
-               (const bf16*)out, T, C, NH, nrows);
+    if (h16)
+        launch_pdl(rowdot64_k<f16>, dim3((nrows * 8 + 255) / 256), dim3(256), 0, s, D, (const f16*)dout,
+                   (const f16*)out, T, C, NH, nrows);
+    else
+        launch_pdl(rowdot64_k<bf16>, dim3((nrows * 8 + 255) / 256), dim3(256), 0, s, D, (const bf16*)dout,
+                   (const bf16*)out, T, C, NH, nrows);
     BwdArgs a;
-    a.dqkv = (bf16*)dqkv;
+    a.dqkv = dqkv;
     a.lse = lse;
     a.D = D;
     a.T = T;
@@ -609,8 +612,13 @@ int launch_flash_backward_tc(void* dqkv, const void* dout, const void* qkv, cons
     a.scale_log2 = LOG2E * a.scale;
     a.err = err;
     const int grid = a.items < num_sms() ? a.items : num_sms();  // persistent
-    launch_pdl(flash_bwd_tc_k<false>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, s, tqkv, tdo, a);
-    launch_pdl(flash_bwd_tc_k<true>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, s, tqkv, tdo, a);
+    if (h16) {
+        launch_pdl(flash_bwd_tc_k<false, 2>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, s, tqkv, tdo, a);
+        launch_pdl(flash_bwd_tc_k<true, 2>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, s, tqkv, tdo, a);
+    } else {
+        launch_pdl(flash_bwd_tc_k<false, 0>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, s, tqkv, tdo, a);
+        launch_pdl(flash_bwd_tc_k<true, 0>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, s, tqkv, tdo, a);
+    }
     return GPT2_OK;
 }
 

@@ -40,6 +40,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 namespace gk {
 namespace fatc {
@@ -65,7 +66,7 @@ constexpr float LN2_F = 0.6931471805599453f;
 constexpr float RESCALE_LOG2 = 8.f;  // lazy-rescale threshold (log2 units)
 
 struct FwdArgs {
-    bf16* out;
+    void* out;  // bf16 or fp16, as the operands
     float* lse;
     int T, C, NH, BH;
     int nqb, nitems;
@@ -98,8 +99,11 @@ DEVI int item_of(int r, int c, int G, int nitems) {
     return u < nitems ? u : -1;
 }
 
+// KIND 0: bf16 operands and output, 2: fp16 (the tcgen05 kind::f16 operand type)
+template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     flash_fwd_tc_k(const __grid_constant__ CUtensorMap tm, const __grid_constant__ FwdArgs a) {
+    using H = typename std::conditional<KIND == 2, f16, bf16>::type;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -194,8 +198,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == 1) {
         {
             // ---------------- MMA issuer (the whole warp runs it, one elected lane issues)
-            const uint32_t idS = idesc<0>(0, 0, BQ, BKV);
-            const uint32_t idPV = idesc<0>(0, 1, BQ, HSZ);
+            const uint32_t idS = idesc<KIND>(0, 0, BQ, BKV);
+            const uint32_t idPV = idesc<KIND>(0, 1, BQ, HSZ);
             int ns[NQT] = {0, 0}, npv[NQT] = {0, 0};
             // bit s: the current fill of ring slot s (bit 4 + b: of Q buffer b)
             // has been waited for; cleared when the slot is handed back
@@ -220,7 +224,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint64_t dk = sdesc(base + OFF_KV + st * 2 * TILE_BYTES, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < HSZ / 16; kk++)  // +32 bytes along K per step
-                    umma_warp<0, 1>(d, dq + 2 * kk, dk + 2 * kk, idS, kk ? 1u : 0u);
+                    umma_warp<KIND, 1>(d, dq + 2 * kk, dk + 2 * kk, idS, kk ? 1u : 0u);
                 umma_commit_warp<1>(sfull(t));
                 ++ns[t];
                 return true;
@@ -363,8 +367,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         x.x = ex2_approx(x.x);
                         x.y = ex2_approx(x.y);
                         acc[e & 1] = fadd2(acc[e & 1], x);
-                        __nv_bfloat162 pr = __floats2bfloat162_rn(x.x, x.y);
-                        pk[e] = *reinterpret_cast<uint32_t*>(&pr);
+                        pk[e] = f2_h2<H>(x.x, x.y);
                     }
                     tmem_st16_nowait(tP + ch * 16, pk);
                 }
@@ -387,16 +390,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (query < a.T) {
                 const int b = it.bh / a.NH, h = it.bh % a.NH;
                 const float inv = 1.f / l;
-                bf16* dst = a.out + ((size_t)b * a.T + query) * C + (size_t)h * HSZ;
+                H* dst = (H*)a.out + ((size_t)b * a.T + query) * C + (size_t)h * HSZ;
 #pragma unroll
                 for (int d = 0; d < HSZ; d += 8) {
-                    __nv_bfloat162 p0 = __floats2bfloat162_rn(ov[d] * inv, ov[d + 1] * inv);
-                    __nv_bfloat162 p1 = __floats2bfloat162_rn(ov[d + 2] * inv, ov[d + 3] * inv);
-                    __nv_bfloat162 p2 = __floats2bfloat162_rn(ov[d + 4] * inv, ov[d + 5] * inv);
-                    __nv_bfloat162 p3 = __floats2bfloat162_rn(ov[d + 6] * inv, ov[d + 7] * inv);
                     *reinterpret_cast<uint4*>(dst + d) =
-                        make_uint4(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1),
-                                   *reinterpret_cast<uint32_t*>(&p2), *reinterpret_cast<uint32_t*>(&p3));
+                        make_uint4(f2_h2<H>(ov[d] * inv, ov[d + 1] * inv), f2_h2<H>(ov[d + 2] * inv, ov[d + 3] * inv),
+                                   f2_h2<H>(ov[d + 4] * inv, ov[d + 5] * inv),
+                                   f2_h2<H>(ov[d + 6] * inv, ov[d + 7] * inv));
                 }
                 a.lse[(size_t)it.bh * a.T + query] = (m + log2f(l)) * LN2_F;
             }
@@ -442,8 +442,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace fatc
 
-// qkv (B, T, 3C) bf16 viewed as a 3-D tensor (3C, T, B); 64 x 128 x 1 boxes
-int launch_flash_forward_tc(void* out, float* lse, const void* qkv, int B, int T, int C, int NH,
+// qkv (B, T, 3C) bf16 or fp16 viewed as a 3-D tensor (3C, T, B); 64 x 128 x 1 boxes
+int launch_flash_forward_tc(DType dt, void* out, float* lse, const void* qkv, int B, int T, int C, int NH,
                             cudaStream_t s, unsigned int* err) {
     using namespace fatc;
     auto fn = encode_fn();
@@ -455,21 +455,23 @@ int launch_flash_forward_tc(void* out, float* lse, const void* qkv, int B, int T
     cuuint64_t strides[2] = {(cuuint64_t)3 * C * 2, (cuuint64_t)T * 3 * C * 2};
     cuuint32_t box[3] = {HSZ, BQ, 1};
     cuuint32_t es[3] = {1, 1, 1};
-    if (fn(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(qkv), dims, strides, box, es,
+    if (dt != DT_BF16 && dt != DT_F16) return set_error(GPT2_ERR_CONFIG, "flash forward: 16-bit operands only");
+    if (fn(&tm, dt == DT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+           const_cast<void*>(qkv), dims, strides, box, es,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return set_error(GPT2_ERR_CUDA, "flash forward: tensor map encoding failed");
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(flash_fwd_tc_k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             SMEM_BYTES);
+    auto kern = dt == DT_F16 ? flash_fwd_tc_k<2> : flash_fwd_tc_k<0>;
+    static bool attr[2] = {false, false};
+    if (!attr[dt == DT_F16]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess)
             return set_error(GPT2_ERR_CUDA, "flash forward: shared-memory opt-in failed: %s",
                              cudaGetErrorString(e));
-        attr = true;
+        attr[dt == DT_F16] = true;
     }
     FwdArgs a;
-    a.out = (bf16*)out;
+    a.out = out;
     a.lse = lse;
     a.T = T;
     a.C = C;
@@ -482,7 +484,7 @@ int launch_flash_forward_tc(void* out, float* lse, const void* qkv, int B, int T
     if (a.nitems == 0) return GPT2_OK;
     dim3 grid(std::min(a.nitems, num_sms()));
     note_launch(1);
-    launch_pdl(flash_fwd_tc_k, grid, dim3(NUM_THREADS), SMEM_BYTES, s, tm, a);
+    launch_pdl(kern, grid, dim3(NUM_THREADS), SMEM_BYTES, s, tm, a);
     return GPT2_OK;
 }
 

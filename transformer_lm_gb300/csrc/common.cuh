@@ -2,19 +2,40 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #define DEVI __device__ __forceinline__
 
 typedef __nv_bfloat16 bf16;
+typedef __half f16;
 
 // ---------------------------------------------------------------- conversions
 DEVI float to_f(float x) { return x; }
 DEVI float to_f(bf16 x) { return __bfloat162float(x); }
+DEVI float to_f(f16 x) { return __half2float(x); }
 template <typename T> DEVI T from_f(float x);
 template <> DEVI float from_f<float>(float x) { return x; }
 template <> DEVI bf16 from_f<bf16>(float x) { return __float2bfloat16_rn(x); }
+template <> DEVI f16 from_f<f16>(float x) { return __float2half_rn(x); }
+
+// two 16-bit values in one 32-bit word (low half first) widened to fp32, and
+// two fp32 values rounded (nearest even) into one such word
+template <typename H> DEVI float2 h2_f2(uint32_t u);
+template <> DEVI float2 h2_f2<bf16>(uint32_t u) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+}
+template <> DEVI float2 h2_f2<f16>(uint32_t u) { return __half22float2(*reinterpret_cast<const __half2*>(&u)); }
+template <typename H> DEVI uint32_t f2_h2(float a, float b);
+template <> DEVI uint32_t f2_h2<bf16>(float a, float b) {
+    __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+template <> DEVI uint32_t f2_h2<f16>(float a, float b) {
+    __half2 r = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&r);
+}
 
 // 16-byte vector of T (4 floats or 8 bf16)
 template <typename T> struct alignas(16) Vec16 {

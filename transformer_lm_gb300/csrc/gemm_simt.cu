@@ -112,6 +112,7 @@ int gemm_simt(const GemmParams& p, DType dt, cudaStream_t s) {
     if (grid.y > 65535) return GPT2_ERR_CONFIG;
     note_launch(1);
     if (dt == DT_BF16) gemm_simt_k<bf16><<<grid, 256, 0, s>>>(p);
+    else if (dt == DT_F16) gemm_simt_k<f16><<<grid, 256, 0, s>>>(p);
     else gemm_simt_k<float><<<grid, 256, 0, s>>>(p);
     return GPT2_OK;
 }

@@ -204,13 +204,11 @@ DEVI void epilogue_chunk(const Args& a, float (&v)[OC], const Vec16<T> (&r)[OC *
     } else {
 #pragma unroll
         for (int e = 0; e < 32; e++) {
-            __nv_bfloat162 pr = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
-            o[e] = *reinterpret_cast<uint32_t*>(&pr);
+            o[e] = f2_h2<TO>(v[2 * e], v[2 * e + 1]);
             if constexpr (EPI == EPI_GELU) {
                 // GELU of the rounded pre-activation (what the backward sees)
-                const float2 g = gelu_fwd_fast2(__bfloat1622float2(pr));
-                __nv_bfloat162 gr = __floats2bfloat162_rn(g.x, g.y);
-                o2[e] = *reinterpret_cast<uint32_t*>(&gr);
+                const float2 g = gelu_fwd_fast2(h2_f2<TO>(o[e]));
+                o2[e] = f2_h2<TO>(g.x, g.y);
             }
         }
     }
@@ -231,19 +229,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
               const __grid_constant__ Args args) {
     using C = Cfg<BN, CG, EPI == EPI_GELU ? 2 : 1>;
-    using T = typename std::conditional<KIND == 0, bf16, float>::type;
+    // KIND 0: bf16 operands, 1: fp32 (tf32 MMAs), 2: fp16 operands
+    using T = typename std::conditional<KIND == 1, float,
+                                        typename std::conditional<KIND == 2, f16, bf16>::type>::type;
     constexpr int KE = ROWB / (int)sizeof(T);  // K elements per stage
-    constexpr int UK = KIND == 0 ? 16 : 8;     // K elements per MMA
+    constexpr int UK = KIND == 1 ? 8 : 16;     // K elements per MMA
     constexpr int KSTEPS = KE / UK;            // MMAs per stage (4)
     constexpr int BNC = BN / CG;               // rows of B this CTA holds
     // epilogue output: fp32 for kind::tf32, split-K partials and the fused
-    // operator's GELU tiles, else bf16;
+    // operator's GELU tiles, else the operands' 16-bit type;
     // a 128-byte chunk holds OC output columns
     constexpr bool OUT_F32 = KIND == 1 || EPI == EPI_SPLITK || EPI == EPI_GELU_PART;
-    using TO = typename std::conditional<OUT_F32, float, bf16>::type;
+    using TO = typename std::conditional<OUT_F32, float, T>::type;
     constexpr int OC = OUT_F32 ? 32 : 64;
     constexpr int NCH = BN / OC;
-    static_assert(EPI != EPI_SPLITK || KIND == 0, "split-K partials: bf16 operands only");
+    static_assert(EPI != EPI_SPLITK || KIND != 1, "split-K partials: 16-bit operands only");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -531,12 +531,15 @@ static bool make_map(CUtensorMap* m, const void* ptr, DType dt, uint64_t inner, 
                      long long ld, uint32_t box_inner, uint32_t box_outer) {
     auto fn = encode_fn();
     if (!fn) return false;
-    const size_t esz = dt == DT_BF16 ? 2 : 4;
+    const size_t esz = dtype_size(dt);
     cuuint64_t dims[2] = {inner, rows};
     cuuint64_t strides[1] = {(cuuint64_t)ld * esz};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t es[2] = {1, 1};
-    CUresult r = fn(m, dt == DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+    const CUtensorMapDataType ty = dt == DT_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                   : dt == DT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    CUresult r = fn(m, ty,
                     2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -559,7 +562,8 @@ static bool make_map_3d_f32(CUtensorMap* m, void* ptr, int N, int M, int S, uint
 }
 
 // D[m, n] (+)= sum over s = 0..S-1 (in order) of ws[s][m][n]; 8 columns per thread
-__global__ void __launch_bounds__(256) splitk_reduce_k(bf16* __restrict__ D, long long ldd,
+template <typename H>
+__global__ void __launch_bounds__(256) splitk_reduce_k(H* __restrict__ D, long long ldd,
                                                        const float* __restrict__ ws, int M, int N,
                                                        int S, int accumulate) {
     pdl_enter();
@@ -583,28 +587,33 @@ __global__ void __launch_bounds__(256) splitk_reduce_k(bf16* __restrict__ D, lon
             acc[0] += x0.x; acc[1] += x0.y; acc[2] += x0.z; acc[3] += x0.w;
             acc[4] += x1.x; acc[5] += x1.y; acc[6] += x1.z; acc[7] += x1.w;
         }
-        bf16* d = D + (size_t)m * ldd + c;
-        Vec16<bf16> o;
+        H* d = D + (size_t)m * ldd + c;
+        Vec16<H> o;
         if (accumulate) {
             o = ld16(d);
 #pragma unroll
-            for (int e = 0; e < 8; e++) o.v[e] = from_f<bf16>(to_f(o.v[e]) + acc[e]);
+            for (int e = 0; e < 8; e++) o.v[e] = from_f<H>(to_f(o.v[e]) + acc[e]);
         } else {
 #pragma unroll
-            for (int e = 0; e < 8; e++) o.v[e] = from_f<bf16>(acc[e]);
+            for (int e = 0; e < 8; e++) o.v[e] = from_f<H>(acc[e]);
         }
         st16(d, o);
     }
 }
 
-static int launch_splitk_reduce(bf16* D, long long ldd, const float* ws, int M, int N, int S,
+static int launch_splitk_reduce(DType dt, void* D, long long ldd, const float* ws, int M, int N, int S,
                                 int accumulate, cudaStream_t s) {
     const long long total = (long long)M * (N / 8);
     long long blocks = (total + 255) / 256;
     const long long cap = (long long)num_sms() * 8;
     if (blocks > cap) blocks = cap;
     note_launch(1);
-    launch_pdl(splitk_reduce_k, dim3((unsigned)blocks), dim3(256), 0, s, D, ldd, ws, M, N, S, accumulate);
+    if (dt == DT_F16)
+        launch_pdl(splitk_reduce_k<f16>, dim3((unsigned)blocks), dim3(256), 0, s, (f16*)D, ldd, ws, M, N, S,
+                   accumulate);
+    else
+        launch_pdl(splitk_reduce_k<bf16>, dim3((unsigned)blocks), dim3(256), 0, s, (bf16*)D, ldd, ws, M, N, S,
+                   accumulate);
     return GPT2_OK;
 }
 
@@ -663,7 +672,7 @@ static int launch_tc(const Maps& mp, const tc::Args& a, cudaStream_t s) {
 
 template <int BN, int KIND, int CG>
 static int dispatch_epi(int epi, const Maps& mp, const tc::Args& a, cudaStream_t s) {
-    if constexpr (KIND == 0) {
+    if constexpr (KIND != 1) {
         switch (epi) {
             case EPI_STORE: return launch_tc<BN, KIND, EPI_STORE, CG>(mp, a, s);
             case EPI_GELU: return launch_tc<BN, KIND, EPI_GELU, CG>(mp, a, s);
@@ -689,16 +698,16 @@ static bool al16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
     if (p.M <= 0 || p.N <= 0 || p.K <= 0) return GPT2_ERR_ARG;
-    const int esz = dt == DT_BF16 ? 2 : 4;
+    const int esz = (int)dtype_size(dt);
     const int vec = 16 / esz;
     const int KE = tc::ROWB / esz;
     // tf32 operands only in K-major form
     if (dt == DT_F32 && (!p.a_kmajor || !p.b_kmajor)) return GPT2_ERR_CONFIG;
     // the fused operator's GELU tiles (and bias) are fp32 whatever the operands
     const DType out_dt = p.epi == EPI_GELU_PART ? DT_F32 : dt;
-    const int osz = out_dt == DT_BF16 ? 2 : 4;
+    const int osz = (int)dtype_size(out_dt);
     if (!al16(p.A) || !al16(p.B) || !al16(p.D) || (p.lda * esz) % 16 || (p.ldb * esz) % 16 ||
-        (p.ldd * osz) % 16 || p.N % (16 / osz) || (dt == DT_BF16 && p.N % vec && p.epi != EPI_GELU_PART))
+        (p.ldd * osz) % 16 || p.N % (16 / osz) || (dt != DT_F32 && p.N % vec && p.epi != EPI_GELU_PART))
         return GPT2_ERR_ALIGN;
     const bool has_aux = p.epi == EPI_RESID || p.epi == EPI_GELU_BWD;
     if (has_aux && (!p.aux || !al16(p.aux) || (p.ldaux * esz) % 16)) return GPT2_ERR_ALIGN;
@@ -720,7 +729,7 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
     int BN = p.N <= 128 ? 128 : 256;
     // 192-wide tiles (B K-major only: a CTA's 96 rows of B are one TMA box) when
     // they fill the last wave of CTA pairs markedly better than 256-wide ones
-    if (BN == 256 && p.b_kmajor && dt == DT_BF16 &&
+    if (BN == 256 && p.b_kmajor && dt != DT_F32 &&
         (p.epi == EPI_STORE || p.epi == EPI_GELU || p.epi == EPI_RESID || p.epi == EPI_GELU_BWD)) {
         const long long units = cg == 2 ? sms / 2 : sms, mg = (nm + cg - 1) / cg;
         // time ~ waves x tile width
@@ -761,7 +770,7 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
     // (k-blocks per range + 6) x 0.25 us per 256-wide k-block, plus the
     // partials' traffic at 5 TB/s.
     const bool split_ok = p.epi == EPI_ACCUM || (p.epi == EPI_STORE && !p.bias && BN == 256);
-    if (split_ok && dt == DT_BF16 && p.ws && p.ws_floats > 0) {
+    if (split_ok && dt != DT_F32 && p.ws && p.ws_floats > 0) {
         const long long units = cg == 2 ? sms / 2 : sms;
         const long long tiles = ((nm + cg - 1) / cg) * a.num_n;
         const double t_kb = 0.25 * BN / 256.0, mn = (double)p.M * p.N;
@@ -796,10 +805,12 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
         ok = ok && make_map_3d_f32(&mp.d, p.ws, p.N, p.M, a.splits, 32, 32);
         mp.d2 = mp.d;
         if (!ok) return GPT2_ERR_CUDA;
-        const int rc = cg == 2 ? dispatch_epi<256, 0, 2>(EPI_SPLITK, mp, a, s)
-                               : dispatch_epi<256, 0, 1>(EPI_SPLITK, mp, a, s);
+        const int rc = dt == DT_F16 ? (cg == 2 ? dispatch_epi<256, 2, 2>(EPI_SPLITK, mp, a, s)
+                                               : dispatch_epi<256, 2, 1>(EPI_SPLITK, mp, a, s))
+                                    : (cg == 2 ? dispatch_epi<256, 0, 2>(EPI_SPLITK, mp, a, s)
+                                               : dispatch_epi<256, 0, 1>(EPI_SPLITK, mp, a, s));
         if (rc != GPT2_OK) return rc;
-        return launch_splitk_reduce((bf16*)p.D, p.ldd, p.ws, p.M, p.N, a.splits, p.epi == EPI_ACCUM ? 1 : 0, s);
+        return launch_splitk_reduce(dt, p.D, p.ldd, p.ws, p.M, p.N, a.splits, p.epi == EPI_ACCUM ? 1 : 0, s);
     }
     // output boxes: one 128-byte chunk x 32 rows (an epilogue warp's store)
     const int OCO = tc::ROWB / osz;
@@ -812,6 +823,13 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
         if (cg == 2)
             return BN == 256 ? dispatch_epi<256, 0, 2>(p.epi, mp, a, s) : dispatch_epi<128, 0, 2>(p.epi, mp, a, s);
         return BN == 256 ? dispatch_epi<256, 0, 1>(p.epi, mp, a, s) : dispatch_epi<128, 0, 1>(p.epi, mp, a, s);
+    }
+    if (dt == DT_F16) {
+        if (BN == 192)
+            return cg == 2 ? dispatch_epi<192, 2, 2>(p.epi, mp, a, s) : dispatch_epi<192, 2, 1>(p.epi, mp, a, s);
+        if (cg == 2)
+            return BN == 256 ? dispatch_epi<256, 2, 2>(p.epi, mp, a, s) : dispatch_epi<128, 2, 2>(p.epi, mp, a, s);
+        return BN == 256 ? dispatch_epi<256, 2, 1>(p.epi, mp, a, s) : dispatch_epi<128, 2, 1>(p.epi, mp, a, s);
     }
     if (cg == 2)
         return BN == 256 ? dispatch_epi<256, 1, 2>(p.epi, mp, a, s) : dispatch_epi<128, 1, 2>(p.epi, mp, a, s);

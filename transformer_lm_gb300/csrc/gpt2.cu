@@ -65,7 +65,7 @@ constexpr int kEvents = 16;  // fork / join events of the two-stream backward
 
 struct Model {
     int L, C, NH, V, Vp, maxT, HS;
-    int prec;  // GPT2_FP32 / GPT2_BF16
+    int prec;  // GPT2_FP32 / GPT2_BF16 / GPT2_FP16
     int tc;
     DType dt;
     size_t esz;
@@ -73,6 +73,7 @@ struct Model {
     void* params = nullptr;
     void* grads = nullptr;
     float* master = nullptr;
+    LossScaler* scaler = nullptr;  // fp16 training: dynamic loss scaling (device state)
     bool sr = false;  // bf16 without a master copy: AdamW rounds stochastically
     // the seed stream of the stochastic rounding (xorshift*, one draw per update)
     unsigned long long rng_state = 13371337ULL;
@@ -209,6 +210,7 @@ void free_model(Model* m) {
     cudaFree(m->mom_v);
     cudaFree(m->d_err);
     cudaFree(m->d_hyper);
+    cudaFree(m->scaler);
     cudaFree(m->hs_dev);
     if (m->hs_pinned) cudaFreeHost(m->hs_pinned);
     if (m->graph_exec) cudaGraphExecDestroy(m->graph_exec);
@@ -421,7 +423,8 @@ int run_forward(Model* m, bool has_targets) {
     if (has_targets) {
         const float dloss = 1.0f / ((float)m->grad_accum * (float)BT);
         TIMED(FAM_CLASSIFIER, 2.0 * BT * m->Vp * es,
-              launch_classifier(dt, m->logits, m->losses, m->targets, (int)BT, m->V, m->Vp, dloss, s));
+              launch_classifier(dt, m->logits, m->losses, m->targets, (int)BT, m->V, m->Vp, dloss, s,
+                                m->scaler ? &m->scaler->scale : nullptr));
     }
     CUDA_TRY(cudaGetLastError());
     m->fwd_done = 1;
@@ -652,9 +655,14 @@ int run_adamw(Model* m, float lr, float beta1, float beta2, float eps, float wei
     const double bytes = (double)m->nparams *
                          (m->master ? (2 * m->esz + 24) : m->sr ? (3.0 * m->esz + 16) : (4.0 * 7));
     const uint32_t seed = m->sr && !hyper ? random_u32(&m->rng_state) : 0u;
+    // fp16: an update whose gradients overflowed is skipped and the scale adapts
+    if (m->scaler)
+        TIMED(FAM_OTHER, (double)m->nparams * m->esz,
+              launch_nonfinite(m->dt, m->grads, m->nparams, m->scaler, m->stream));
     TIMED(FAM_ADAMW, bytes,
           launch_adamw(m->dt, m->params, m->master, m->grads, m->mom_m, m->mom_v, m->nparams, lr,
-                       beta1, beta2, c1, c2, eps, weight_decay, hyper, m->stream, m->sr, seed));
+                       beta1, beta2, c1, c2, eps, weight_decay, hyper, m->stream, m->sr, seed, m->scaler));
+    if (m->scaler) TIMED(FAM_OTHER, 0.0, launch_scaler_update(m->scaler, m->stream));
     CUDA_TRY(cudaGetLastError());
     return GPT2_OK;
 }
@@ -688,11 +696,11 @@ int gpt2_init_ex(int L, int C, int NH, int V, int Vp, int maxT, unsigned long lo
     if (HS != 16 && HS != 32 && HS != 64 && HS != 128)
         return fail(GPT2_ERR_CONFIG, "head size %d not in {16,32,64,128}", HS);
     if (C % 8 || Vp % 8) return fail(GPT2_ERR_CONFIG, "C and Vp must be multiples of 8");
-    if (precision != GPT2_FP32 && precision != GPT2_BF16)
+    if (precision != GPT2_FP32 && precision != GPT2_BF16 && precision != GPT2_FP16)
         return fail(GPT2_ERR_CONFIG, "precision %d unknown", precision);
     if (precision == GPT2_FP32 && tensor_cores)
         return fail(GPT2_ERR_CONFIG, "fp32 training runs on the SIMT path (tensor_cores=0)");
-    if (C > (precision == GPT2_BF16 ? 2048 : 1024))
+    if (C > (precision == GPT2_FP32 ? 1024 : 2048))
         return fail(GPT2_ERR_CONFIG, "C=%d too large for the row-in-registers LayerNorm", C);
     if (g) {
         free_model(g);
@@ -702,8 +710,8 @@ int gpt2_init_ex(int L, int C, int NH, int V, int Vp, int maxT, unsigned long lo
     m->L = L; m->C = C; m->NH = NH; m->V = V; m->Vp = Vp; m->maxT = maxT; m->HS = HS;
     m->prec = precision;
     m->tc = tensor_cores ? 1 : 0;
-    m->dt = precision == GPT2_BF16 ? DT_BF16 : DT_F32;
-    m->esz = precision == GPT2_BF16 ? 2 : 4;
+    m->dt = precision == GPT2_BF16 ? DT_BF16 : precision == GPT2_FP16 ? DT_F16 : DT_F32;
+    m->esz = dtype_size(m->dt);
     const size_t Cs = C, Ls = L;
     size_t sz[16] = {(size_t)Vp * Cs, (size_t)maxT * Cs, Ls * Cs, Ls * Cs, Ls * 3 * Cs * Cs,
                      Ls * 3 * Cs, Ls * Cs * Cs, Ls * Cs, Ls * Cs, Ls * Cs, Ls * 4 * Cs * Cs,
@@ -733,12 +741,22 @@ int gpt2_init_ex(int L, int C, int NH, int V, int Vp, int maxT, unsigned long lo
               cudaMalloc((void**)&m->mom_v, off * 4 + 256) == cudaSuccess &&
               cudaMalloc((void**)&m->d_err, 256) == cudaSuccess &&
               cudaMalloc((void**)&m->d_hyper, 256) == cudaSuccess &&
-              (precision == GPT2_FP32 || cudaMalloc((void**)&m->master, off * 4 + 256) == cudaSuccess);
+              (precision == GPT2_FP32 || cudaMalloc((void**)&m->master, off * 4 + 256) == cudaSuccess) &&
+              (precision != GPT2_FP16 || cudaMalloc((void**)&m->scaler, 256) == cudaSuccess);
     if (!ok) {
         free_model(m);
         return fail(GPT2_ERR_NOMEM, "parameter/optimizer allocation (%zu params) failed", off);
     }
     launch_zero(m->d_err, 4, m->stream);
+    if (m->scaler) {
+        // loss scale 2^16, doubled after 2000 good steps in a row
+        const LossScaler sc = {65536.f, 0, 0, 2000, 0};
+        e = cudaMemcpyAsync(m->scaler, &sc, sizeof(sc), cudaMemcpyHostToDevice, m->stream);
+        if (e != cudaSuccess) {
+            free_model(m);
+            return fail(GPT2_ERR_CUDA, "loss scaler: %s", cudaGetErrorString(e));
+        }
+    }
     init_params(m, seed);
     launch_zero(m->grads, off * m->esz, m->stream);
     reset_optimizer(m);
@@ -997,10 +1015,52 @@ int gpt2_get_params(float* host) {
     return to_host_f32(g, host, g->params, g->nparams, g->dt);
 }
 
+// fp16: the current loss scale (1 otherwise); synchronises
+static int current_scale(Model* m, float* scale) {
+    *scale = 1.f;
+    if (!m->scaler) return GPT2_OK;
+    CUDA_TRY(cudaMemcpyAsync(scale, &m->scaler->scale, 4, cudaMemcpyDeviceToHost, m->stream));
+    CUDA_TRY(cudaStreamSynchronize(m->stream));
+    return GPT2_OK;
+}
+
 int gpt2_get_grads(float* host) {
     TRY(check_model());
     if (!host) return fail(GPT2_ERR_ARG, "host is NULL");
-    return to_host_f32(g, host, g->grads, g->nparams, g->dt);
+    TRY(to_host_f32(g, host, g->grads, g->nparams, g->dt));
+    float sc;
+    TRY(current_scale(g, &sc));
+    if (sc != 1.f) {  // the stored gradients are loss-scaled
+        const float inv = 1.f / sc;
+        for (size_t i = 0; i < g->nparams; i++) host[i] *= inv;
+    }
+    return GPT2_OK;
+}
+
+int gpt2_set_loss_scaling(float init_scale, int growth_interval) {
+    TRY(check_model());
+    Model* m = g;
+    if (!m->scaler) return fail(GPT2_ERR_CONFIG, "loss scaling exists in GPT2_FP16 mode only");
+    int ex = 0;
+    if (!(init_scale > 0.f) || frexpf(init_scale, &ex) != 0.5f || growth_interval < 1)
+        return fail(GPT2_ERR_ARG, "loss scale must be a power of two and growth_interval >= 1");
+    const LossScaler sc = {init_scale, 0, 0, growth_interval, 0};
+    CUDA_TRY(cudaMemcpyAsync(m->scaler, &sc, sizeof(sc), cudaMemcpyHostToDevice, m->stream));
+    CUDA_TRY(cudaStreamSynchronize(m->stream));
+    return GPT2_OK;
+}
+
+int gpt2_get_loss_scale(float* scale, long long* skipped) {
+    TRY(check_model());
+    Model* m = g;
+    LossScaler sc = {1.f, 0, 0, 0, 0};
+    if (m->scaler) {
+        CUDA_TRY(cudaMemcpyAsync(&sc, m->scaler, sizeof(sc), cudaMemcpyDeviceToHost, m->stream));
+        CUDA_TRY(cudaStreamSynchronize(m->stream));
+    }
+    if (scale) *scale = sc.scale;
+    if (skipped) *skipped = sc.skipped;
+    return GPT2_OK;
 }
 
 int gpt2_set_master_weights(int enabled) {
@@ -1056,6 +1116,14 @@ int gpt2_set_grads(const float* host) {
     TRY(check_model());
     if (!host) return fail(GPT2_ERR_ARG, "host is NULL");
     Model* m = g;
+    float sc;
+    TRY(current_scale(m, &sc));
+    std::vector<float> scaled;
+    if (sc != 1.f) {  // stored loss-scaled, as the backward leaves them
+        scaled.assign(host, host + m->nparams);
+        for (float& x : scaled) x *= sc;
+        host = scaled.data();
+    }
     float* tmp = nullptr;
     CUDA_TRY(cudaMalloc(&tmp, m->nparams * 4 + 16));
     cudaError_t e = cudaMemcpyAsync(tmp, host, m->nparams * 4, cudaMemcpyHostToDevice, m->stream);

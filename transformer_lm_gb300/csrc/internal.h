@@ -13,7 +13,10 @@
 namespace gk {
 
 // element type of parameters/activations
-enum DType { DT_F32 = 0, DT_BF16 = 1 };
+enum DType { DT_F32 = 0, DT_BF16 = 1, DT_F16 = 2 };
+inline size_t dtype_size(DType dt) { return dt == DT_F32 ? 4 : 2; }
+// elements in a 16-byte vector
+inline int dtype_vec(DType dt) { return dt == DT_F32 ? 4 : 8; }
 
 // GEMM epilogues, applied to the fp32 accumulator acc[m][n]:
 //  EPI_STORE     D = acc (+ bias[n])
@@ -106,9 +109,10 @@ int launch_colsum_part(DType dt, float* part, const void* dout, int M, int N, cu
 // one launch over a device table of descriptors
 void launch_reduce_partials_multi(DType dt, const PartialDesc* d_desc, int ndesc, int maxwidth,
                                   cudaStream_t s);
-// logits (BT, Vp) -> dlogits in place; losses[BT] fp32
+// logits (BT, Vp) -> dlogits in place; losses[BT] fp32. dloss_scale: NULL, or
+// a device float the seed dloss is multiplied by (the loss scale of fp16 training)
 void launch_classifier(DType dt, void* logits, float* losses, const int* targets, int BT, int V,
-                       int Vp, float dloss, cudaStream_t s);
+                       int Vp, float dloss, cudaStream_t s, const float* dloss_scale = nullptr);
 void launch_mean(const float* x, int n, float* out, cudaStream_t s);
 // probs (rows, Vp) fp32 = softmax over the first V columns of logits (rows, Vp); 0 on the padding
 void launch_probs(DType dt, float* probs, const void* logits, int rows, int V, int Vp, cudaStream_t s);
@@ -121,17 +125,33 @@ void launch_sample(DType dt, const void* logits, long long row_stride, int rows,
 struct AdamRanges {
     size_t off[8], n[8];
 };
+// dynamic loss scaling of fp16 training, in device memory (graph replays keep
+// it current): the backward is seeded with scale / (k B T); a step whose
+// gradients hold an inf or NaN is skipped and halves the scale; growth_interval
+// good steps in a row double it
+struct LossScaler {
+    float scale;
+    int good_steps;
+    int found_inf;
+    int growth_interval;
+    long long skipped;
+};
+// found_inf |= any gradient is inf or NaN
+void launch_nonfinite(DType dt, const void* grads, size_t n, LossScaler* sc, cudaStream_t s);
+// the scale's update after an AdamW launch (which skipped the step on found_inf)
+void launch_scaler_update(LossScaler* sc, cudaStream_t s);
 void launch_adamw_ranges(DType dt, void* params, float* master, const void* grads, float* m,
                          float* v, const AdamRanges& r, int nranges, float lr, float b1, float b2,
                          float c1, float c2, float eps, float wd, const float* hyper, cudaStream_t s,
-                         bool stochastic = false, uint32_t seed = 0);
+                         bool stochastic = false, uint32_t seed = 0, const LossScaler* scaler = nullptr);
 // hyper: NULL, or device floats {lr, b1, b2, c1, c2, eps, wd, seed bits} that
 // replace the by-value ones (a CUDA graph replays the launch with new values
 // there). stochastic (bf16 only): no master copy; the fp32 update is rounded
 // to the bf16 parameter stochastically with this step's seed.
 void launch_adamw(DType dt, void* params, float* master, const void* grads, float* m, float* v,
                   size_t n, float lr, float b1, float b2, float c1, float c2, float eps, float wd,
-                  const float* hyper, cudaStream_t s, bool stochastic = false, uint32_t seed = 0);
+                  const float* hyper, cudaStream_t s, bool stochastic = false, uint32_t seed = 0,
+                  const LossScaler* scaler = nullptr);
 // writes {lr, b1, b2, c1, c2, eps, wd, seed bits} to h with a one-thread kernel
 void launch_set_hyper(float* h, float lr, float b1, float b2, float c1, float c2, float eps, float wd,
                       uint32_t seed, cudaStream_t s);
@@ -147,20 +167,29 @@ void launch_split_bf16x3(void* dst, const float* src, int rows, int K, int Kp, i
 // out = softmax over each row of a (M,N) fp32 tile-partial GELU output (fused operator pass 2)
 void launch_softmax_finish(float* y, const float* part, int M, int N, int tiles, cudaStream_t s);
 
+// ---- fused operator (fused_tc.cu) ----
+// y = gelu(x W^T + b) (fp32 x (M,K), W (N,K), b (N), y (M,N), all 16-byte
+// aligned, K % 4 == 0 == N % 4) with the bf16 hi/lo split of x and W done in
+// the kernel; part[row * part_ld + t] = (max, sum exp(y - max)) over the row's
+// 256-column tile t (float2). err: device error word of the bounded waits.
+int launch_fused_split_gemm(const float* x, const float* W, const float* b, float* y, float* part,
+                            int part_ld, int M, int K, int N, cudaStream_t s, unsigned int* err);
+int fused_split_tile_n();
+
 // ---- attention (attention.cu) ----
 // qkv (B,T,3C) -> out (B,T,C), lse (B,NH,T) fp32 natural-log sum of exp of the scaled scores
 // returns 0 or a GPT2_ERR_* code; err: device error word of the bounded waits
 int launch_attention_forward(DType dt, int tensor_cores, void* out, float* lse, const void* qkv,
                              int B, int T, int C, int NH, cudaStream_t s, unsigned int* err);
-// tcgen05 flash forward (bf16, head size 64)
-int launch_flash_forward_tc(void* out, float* lse, const void* qkv, int B, int T, int C, int NH,
+// tcgen05 flash forward (bf16 or fp16, head size 64)
+int launch_flash_forward_tc(DType dt, void* out, float* lse, const void* qkv, int B, int T, int C, int NH,
                             cudaStream_t s, unsigned int* err);
 // dqkv (B,T,3C) written; D scratch (B,NH,T) fp32; returns 0 or a GPT2_ERR_* code
 int launch_attention_backward(DType dt, int tensor_cores, void* dqkv, const void* dout,
                               const void* qkv, const void* out, const float* lse, float* D,
                               int B, int T, int C, int NH, cudaStream_t s, unsigned int* err);
-// tcgen05 flash backward (bf16, head size 64): D = rowsum(dO * O), then dQ, dK, dV
-int launch_flash_backward_tc(void* dqkv, const void* dout, const void* qkv, const void* out,
+// tcgen05 flash backward (bf16 or fp16, head size 64): D = rowsum(dO * O), then dQ, dK, dV
+int launch_flash_backward_tc(DType dt, void* dqkv, const void* dout, const void* qkv, const void* out,
                              const float* lse, float* D, int B, int T, int C, int NH, cudaStream_t s,
                              unsigned int* err);
 

@@ -14,6 +14,7 @@
 #include <stdlib.h>
 
 #include <atomic>
+#include <type_traits>
 
 namespace gk {
 
@@ -45,6 +46,21 @@ int num_sms() {
 static std::atomic<long long> g_launches{0};
 void note_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 long long launch_count() { return g_launches.load(std::memory_order_relaxed); }
+
+// runs the statement with E = the element type of dt (bf16, fp16 or fp32)
+#define DISPATCH_E(dt, ...)                \
+    do {                                   \
+        if ((dt) == DT_BF16) {             \
+            using E = bf16;                \
+            __VA_ARGS__;                   \
+        } else if ((dt) == DT_F16) {       \
+            using E = f16;                 \
+            __VA_ARGS__;                   \
+        } else {                           \
+            using E = float;               \
+            __VA_ARGS__;                   \
+        }                                  \
+    } while (0)
 
 static inline unsigned int grid_for(size_t work, int block, int per_sm = 8) {
     size_t g = (work + block - 1) / block;
@@ -102,14 +118,10 @@ __global__ void encoder_forward_k(T* __restrict__ out, const int* __restrict__ t
 void launch_encoder_forward(DType dt, void* out, const int* tok, const void* wte, const void* wpe,
                             int B, int T, int C, cudaStream_t s) {
     note_launch(1);
-    size_t work = (size_t)B * T * C / (dt == DT_BF16 ? 8 : 4);
+    size_t work = (size_t)B * T * C / dtype_vec(dt);
     unsigned g = grid_for(work, 256);
-    if (dt == DT_BF16)
-        launch_pdl(encoder_forward_k<bf16>, g, 256, 0, s, (bf16*)out, tok, (const bf16*)wte,
-                                                  (const bf16*)wpe, B * T, T, C);
-    else
-        launch_pdl(encoder_forward_k<float>, g, 256, 0, s, (float*)out, tok, (const float*)wte,
-                                                   (const float*)wpe, B * T, T, C);
+    DISPATCH_E(dt, launch_pdl(encoder_forward_k<E>, g, 256, 0, s, (E*)out, tok, (const E*)wte,
+                              (const E*)wpe, B * T, T, C));
 }
 
 // encoder_backward_kernel, made deterministic.
@@ -323,12 +335,9 @@ void launch_encoder_backward(DType dt, void* dwte, void* dwpe, const void* dout,
                              int* ws_cursor, int* ws_order, int* ws_sorted, cudaStream_t s) {
     note_launch(6);
     const int n = B * T;
-    const int VEC = dt == DT_BF16 ? 8 : 4;
+    const int VEC = dtype_vec(dt);
     unsigned g = grid_for((size_t)T * C / VEC, 256);
-    if (dt == DT_BF16)
-        launch_pdl(encoder_backward_wpe_k<bf16>, g, 256, 0, s, (bf16*)dwpe, (const bf16*)dout, B, T, C);
-    else
-        launch_pdl(encoder_backward_wpe_k<float>, g, 256, 0, s, (float*)dwpe, (const float*)dout, B, T, C);
+    DISPATCH_E(dt, launch_pdl(encoder_backward_wpe_k<E>, g, 256, 0, s, (E*)dwpe, (const E*)dout, B, T, C));
     launch_zero(ws_counts, sizeof(int) * (size_t)Vp, s);
     launch_pdl(token_count_k, grid_for(n, 256), 256, 0, s, tok, n, ws_counts);
     const size_t scan_smem = sizeof(int) * (size_t)Vp;
@@ -345,12 +354,8 @@ void launch_encoder_backward(DType dt, void* dwte, void* dwpe, const void* dout,
     launch_pdl(token_scatter_k, grid_for(n, 256), 256, 0, s, tok, n, ws_cursor, ws_order);
     launch_pdl(token_rank_k, grid_for(n, 256), 256, 0, s, tok, ws_offsets, ws_order, n, ws_sorted);
     unsigned gw = (unsigned)((Vp + 7) / 8);
-    if (dt == DT_BF16)
-        launch_pdl(encoder_backward_wte_k<bf16>, gw, 256, 0, s, (bf16*)dwte, (const bf16*)dout, ws_offsets,
-                                                        ws_sorted, Vp, C);
-    else
-        launch_pdl(encoder_backward_wte_k<float>, gw, 256, 0, s, (float*)dwte, (const float*)dout,
-                                                         ws_offsets, ws_sorted, Vp, C);
+    DISPATCH_E(dt, launch_pdl(encoder_backward_wte_k<E>, gw, 256, 0, s, (E*)dwte, (const E*)dout, ws_offsets,
+                              ws_sorted, Vp, C));
 }
 
 // ------------------------------------------------------------------ LayerNorm
@@ -370,6 +375,21 @@ DEVI uint32_t f2_bf2(float2 v) {
     const __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
     return *reinterpret_cast<const uint32_t*>(&b);
 }
+// the same for either 16-bit type (fp16 widens with two conversions)
+template <typename H> DEVI float2 h2_f2_v(uint32_t u);
+template <> DEVI float2 h2_f2_v<bf16>(uint32_t u) { return bf2_f2_v(u); }
+template <> DEVI float2 h2_f2_v<f16>(uint32_t u) {
+    float lo, hi;
+    asm volatile("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+                 : "=f"(lo), "=f"(hi)
+                 : "r"(u));
+    return make_float2(lo, hi);
+}
+template <typename H> DEVI uint32_t f2_h2v(float2 v) { return f2_h2<H>(v.x, v.y); }
+// plain widening (the compiler may keep the result live)
+template <typename H> DEVI float2 h2_f2w(uint32_t u);
+template <> DEVI float2 h2_f2w<bf16>(uint32_t u) { return bf2_f2(u); }
+template <> DEVI float2 h2_f2w<f16>(uint32_t u) { return h2_f2<f16>(u); }
 // layernorm_forward_kernel3: one warp per row, the row held in registers;
 // mean, biased variance, rstd = 1/sqrt(var + 1e-5), y = (x - mean) rstd w + b.
 // mean/rstd are kept in fp32.
@@ -433,16 +453,17 @@ __global__ void layernorm_forward_k(T* __restrict__ out, float* __restrict__ mea
     }
 }
 
-// bf16 rows with C = 256 NV (NV <= 3): lane l keeps the row's 16-byte vectors
-// l, l + 32, ... as packed bf16 words (4 NV registers) and widens them anew in
-// each pass, so the kernel fits in 40 registers and 48 one-row warps are
-// resident per SM; the statistics and the affine map use packed fp32 arithmetic.
-template <int NV>
-__global__ void __launch_bounds__(256, 6) layernorm_forward_bf16_k(bf16* __restrict__ out, float* __restrict__ mean,
+// 16-bit rows (bf16 or fp16, H) with C = 256 NV (NV <= 3): lane l keeps the
+// row's 16-byte vectors l, l + 32, ... as packed 16-bit words (4 NV registers)
+// and widens them anew in each pass, so the kernel fits in 40 registers and 48
+// one-row warps are resident per SM; the statistics and the affine map use
+// packed fp32 arithmetic.
+template <typename H, int NV>
+__global__ void __launch_bounds__(256, 6) layernorm_forward_bf16_k(H* __restrict__ out, float* __restrict__ mean,
                                                                    float* __restrict__ rstd,
-                                                                   const bf16* __restrict__ inp,
-                                                                   const bf16* __restrict__ w,
-                                                                   const bf16* __restrict__ b, int N) {
+                                                                   const H* __restrict__ inp,
+                                                                   const H* __restrict__ w,
+                                                                   const H* __restrict__ b, int N) {
     constexpr int C = 256 * NV;
     pdl_enter();
     const int row = blockIdx.x * 8 + threadIdx.x / 32;
@@ -455,14 +476,14 @@ __global__ void __launch_bounds__(256, 6) layernorm_forward_bf16_k(bf16* __restr
     float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < NV; j++) {
-        s2 = fadd2(s2, fadd2(bf2_f2_v(xv[j].x), bf2_f2_v(xv[j].y)));
-        s2 = fadd2(s2, fadd2(bf2_f2_v(xv[j].z), bf2_f2_v(xv[j].w)));
+        s2 = fadd2(s2, fadd2(h2_f2_v<H>(xv[j].x), h2_f2_v<H>(xv[j].y)));
+        s2 = fadd2(s2, fadd2(h2_f2_v<H>(xv[j].z), h2_f2_v<H>(xv[j].w)));
     }
     const float m = warp_sum(s2.x + s2.y) / C;
     const float2 nm = make_float2(-m, -m);
     float2 v2 = make_float2(0.f, 0.f);
     auto sq = [&](uint32_t u) {
-        const float2 d = fadd2(bf2_f2_v(u), nm);
+        const float2 d = fadd2(h2_f2_v<H>(u), nm);
         v2 = ffma2(d, d, v2);
     };
 #pragma unroll
@@ -477,7 +498,7 @@ __global__ void __launch_bounds__(256, 6) layernorm_forward_bf16_k(bf16* __restr
     const uint4* wp = reinterpret_cast<const uint4*>(w) + lane;
     const uint4* bp = reinterpret_cast<const uint4*>(b) + lane;
     auto aff = [&](uint32_t xu, uint32_t wu, uint32_t bu) {
-        return f2_bf2(ffma2(ffma2(bf2_f2_v(xu), r2, nmr), bf2_f2_v(wu), bf2_f2_v(bu)));
+        return f2_h2v<H>(ffma2(ffma2(h2_f2_v<H>(xu), r2, nmr), h2_f2_v<H>(wu), h2_f2_v<H>(bu)));
     };
 #pragma unroll
     for (int j = 0; j < NV; j++) {
@@ -499,27 +520,28 @@ static int maxv_for(int cv) {
 void launch_layernorm_forward(DType dt, void* out, float* mean, float* rstd, const void* inp,
                               const void* w, const void* b, int N, int C, cudaStream_t s) {
     note_launch(1);
-    const int VEC = dt == DT_BF16 ? 8 : 4;
+    const int VEC = dtype_vec(dt);
     const int mv = maxv_for(C / VEC);
     const int block = 256, rows = block / 32;
     unsigned g = (unsigned)((N + rows - 1) / rows);
-    if (dt == DT_BF16 && C % 256 == 0 && C <= 768) {
+    if (dt != DT_F32 && C % 256 == 0 && C <= 768) {
         const int nv = C / 256;
-#define LNF2(NVV)                                                                                          \
-    launch_pdl(layernorm_forward_bf16_k<NVV>, g, block, 0, s, (bf16*)out, mean, rstd, (const bf16*)inp, \
-               (const bf16*)w, (const bf16*)b, N)
-        if (nv == 1) LNF2(1); else if (nv == 2) LNF2(2); else LNF2(3);
+#define LNF2(H, NVV)                                                                                 \
+    launch_pdl(layernorm_forward_bf16_k<H, NVV>, g, block, 0, s, (H*)out, mean, rstd, (const H*)inp, \
+               (const H*)w, (const H*)b, N)
+        if (dt == DT_BF16) {
+            if (nv == 1) LNF2(bf16, 1); else if (nv == 2) LNF2(bf16, 2); else LNF2(bf16, 3);
+        } else {
+            if (nv == 1) LNF2(f16, 1); else if (nv == 2) LNF2(f16, 2); else LNF2(f16, 3);
+        }
 #undef LNF2
         return;
     }
 #define LNF(TT, MV)                                                                            \
     launch_pdl(layernorm_forward_k<TT, MV>, g, block, 0, s, (TT*)out, mean, rstd, (const TT*)inp,        \
                                                     (const TT*)w, (const TT*)b, N, C)
-    if (dt == DT_BF16) {
-        if (mv == 1) LNF(bf16, 1); else if (mv == 2) LNF(bf16, 2); else if (mv == 4) LNF(bf16, 4); else LNF(bf16, 8);
-    } else {
-        if (mv == 1) LNF(float, 1); else if (mv == 2) LNF(float, 2); else if (mv == 4) LNF(float, 4); else LNF(float, 8);
-    }
+    DISPATCH_E(dt, if (mv == 1) LNF(E, 1); else if (mv == 2) LNF(E, 2); else if (mv == 4) LNF(E, 4);
+                   else LNF(E, 8));
 #undef LNF
 }
 
@@ -627,10 +649,10 @@ __host__ __device__ inline size_t lnq_body_bytes(int C, int groups) {
     return ((ring > fold ? ring : fold) + 15) / 16 * 16;
 }
 
-template <int NV>
+template <typename H, int NV>
 __global__ void __launch_bounds__(LNQ_THREADS, 1) layernorm_backward_bulk_k(
-    bf16* __restrict__ dinp, float* __restrict__ part, const bf16* __restrict__ dout,
-    const bf16* __restrict__ inp, const bf16* __restrict__ w, const float* __restrict__ mean,
+    H* __restrict__ dinp, float* __restrict__ part, const H* __restrict__ dout,
+    const H* __restrict__ inp, const H* __restrict__ w, const float* __restrict__ mean,
     const float* __restrict__ rstd, int N, int C, int accumulate, int with_colsum,
     unsigned int* __restrict__ err) {
     constexpr int VEC = 8;
@@ -695,7 +717,7 @@ __global__ void __launch_bounds__(LNQ_THREADS, 1) layernorm_backward_bulk_k(
             *issued_s = issued;
         }
     } else if (warp < CWARPS) {
-        Vec16<bf16> wv;
+        Vec16<H> wv;
         if (has) wv = ld16(w + vi * VEC);
         int par = 0;
         bool ok_all = true;
@@ -714,7 +736,7 @@ __global__ void __launch_bounds__(LNQ_THREADS, 1) layernorm_backward_bulk_k(
             for (int i = 0; i < nrows; i += 2, par ^= 1) {
                 const int nr = min(2, nrows - i);
                 float mu[2], rs[2], g[2][VEC], nh[2][VEC];
-                Vec16<bf16> dvv[2], ovv[2];
+                Vec16<H> dvv[2], ovv[2];
                 float gs[2] = {0.f, 0.f}, gns[2] = {0.f, 0.f};
                 const bool use = has && ok;
 #pragma unroll
@@ -723,11 +745,11 @@ __global__ void __launch_bounds__(LNQ_THREADS, 1) layernorm_backward_bulk_k(
                     mu[q] = mean[r];
                     rs[q] = rstd[r];
                     const uint8_t* rowp = slot + (size_t)(i + (q < nr ? q : 0)) * rowb;
-                    Vec16<bf16> xv;
+                    Vec16<H> xv;
                     if (use) {
-                        xv = *reinterpret_cast<const Vec16<bf16>*>(rowp + vi * 16);
-                        dvv[q] = *reinterpret_cast<const Vec16<bf16>*>(rowp + arrb + vi * 16);
-                        if (accumulate) ovv[q] = *reinterpret_cast<const Vec16<bf16>*>(rowp + 2 * arrb + vi * 16);
+                        xv = *reinterpret_cast<const Vec16<H>*>(rowp + vi * 16);
+                        dvv[q] = *reinterpret_cast<const Vec16<H>*>(rowp + arrb + vi * 16);
+                        if (accumulate) ovv[q] = *reinterpret_cast<const Vec16<H>*>(rowp + 2 * arrb + vi * 16);
                     }
 #pragma unroll
                     for (int e = 0; e < VEC; e++) {
@@ -772,12 +794,12 @@ __global__ void __launch_bounds__(LNQ_THREADS, 1) layernorm_backward_bulk_k(
                     for (int q = 0; q < 2; q++) {
                         if (q >= nr) break;
                         const float gm = gs[q] / C, gnm = gns[q] / C;
-                        Vec16<bf16> o;
+                        Vec16<H> o;
 #pragma unroll
                         for (int e = 0; e < VEC; e++) {
                             const float val = rs[q] * (g[q][e] - gm - nh[q][e] * gnm);
                             const float d = to_f(dvv[q].v[e]);
-                            o.v[e] = from_f<bf16>(accumulate ? to_f(ovv[q].v[e]) + val : val);
+                            o.v[e] = from_f<H>(accumulate ? to_f(ovv[q].v[e]) + val : val);
                             adw[e] += nh[q][e] * d;
                             adb[e] += d;
                             acs[e] += to_f(o.v[e]);
@@ -841,10 +863,10 @@ DEVI void lnw_cp16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
-template <int NV>
+template <typename H, int NV>
 __global__ void __launch_bounds__(32 * LNW_WARPS, 1) layernorm_backward_warp_k(
-    bf16* __restrict__ dinp, float* __restrict__ part, const bf16* __restrict__ dout,
-    const bf16* __restrict__ inp, const bf16* __restrict__ w, const float* __restrict__ mean,
+    H* __restrict__ dinp, float* __restrict__ part, const H* __restrict__ dout,
+    const H* __restrict__ inp, const H* __restrict__ w, const float* __restrict__ mean,
     const float* __restrict__ rstd, int N, int C, int accumulate, int with_colsum) {
     constexpr int VEC = 8;
     constexpr int ROWB = 256 * NV * 2;  // bytes of one row of one array
@@ -863,7 +885,7 @@ __global__ void __launch_bounds__(32 * LNW_WARPS, 1) layernorm_backward_warp_k(
 #pragma unroll
     for (int j = 0; j < NV; j++) {
         const uint4 u = *reinterpret_cast<const uint4*>(w + (lane + 32 * j) * VEC);
-        wf[j][0] = bf2_f2(u.x); wf[j][1] = bf2_f2(u.y); wf[j][2] = bf2_f2(u.z); wf[j][3] = bf2_f2(u.w);
+        wf[j][0] = h2_f2w<H>(u.x); wf[j][1] = h2_f2w<H>(u.y); wf[j][2] = h2_f2w<H>(u.z); wf[j][3] = h2_f2w<H>(u.w);
     }
     float2 adw[NV][VEC / 2], adb[NV][VEC / 2], acs[NV][VEC / 2];
 #pragma unroll
@@ -917,9 +939,9 @@ __global__ void __launch_bounds__(32 * LNW_WARPS, 1) layernorm_backward_warp_k(
             const uint32_t xw[4] = {xu.x, xu.y, xu.z, xu.w}, dw[4] = {du.x, du.y, du.z, du.w};
 #pragma unroll
             for (int e = 0; e < VEC / 2; e++) {
-                const float2 d = bf2_f2(dw[e]);
+                const float2 d = h2_f2w<H>(dw[e]);
                 g[j][e] = fmul2(wf[j][e], d);
-                nh[j][e] = ffma2(bf2_f2(xw[e]), rs2, nmr);
+                nh[j][e] = ffma2(h2_f2w<H>(xw[e]), rs2, nmr);
                 gs2 = fadd2(gs2, g[j][e]);
                 gns2 = ffma2(g[j][e], nh[j][e], gns2);
                 adw[j][e] = ffma2(nh[j][e], d, adw[j][e]);
@@ -935,7 +957,7 @@ __global__ void __launch_bounds__(32 * LNW_WARPS, 1) layernorm_backward_warp_k(
         // dx = rstd (g - mean(g) - nhat mean(g nhat)) = rstd g + c0 + c1 nhat
         const float c0 = -rs * (gs / C), c1 = -rs * (gns / C);
         const float2 c02 = make_float2(c0, c0), c12 = make_float2(c1, c1);
-        bf16* dx = dinp + (size_t)r * C + lane * VEC;
+        H* dx = dinp + (size_t)r * C + lane * VEC;
 #pragma unroll
         for (int j = 0; j < NV; j++) {
             uint32_t ow[4] = {0u, 0u, 0u, 0u};
@@ -947,9 +969,9 @@ __global__ void __launch_bounds__(32 * LNW_WARPS, 1) layernorm_backward_warp_k(
 #pragma unroll
             for (int e = 0; e < VEC / 2; e++) {
                 float2 v = ffma2(nh[j][e], c12, ffma2(g[j][e], rs2, c02));
-                if (accumulate) v = fadd2(bf2_f2(ow[e]), v);
-                res[e] = f2_bf2(v);
-                acs[j][e] = fadd2(acs[j][e], bf2_f2(res[e]));
+                if (accumulate) v = fadd2(h2_f2w<H>(ow[e]), v);
+                res[e] = f2_h2v<H>(v);
+                acs[j][e] = fadd2(acs[j][e], h2_f2w<H>(res[e]));
             }
             *reinterpret_cast<uint4*>(dx + 32 * j * VEC) = make_uint4(res[0], res[1], res[2], res[3]);
         }
@@ -1053,26 +1075,30 @@ void launch_layernorm_backward(DType dt, void* dinp, void* dw, void* db, const v
                                                  accumulate, 0, err, s);
     note_launch(1);
     const unsigned rg = (unsigned)((2 * C + 31) / 32);
-    if (dt == DT_BF16)
-        launch_pdl(reduce_partials_k<bf16>, rg, 256, 0, s, (bf16*)dw, (bf16*)db, C, ws, P, 2 * C);
-    else
-        launch_pdl(reduce_partials_k<float>, rg, 256, 0, s, (float*)dw, (float*)db, C, ws, P, 2 * C);
+    DISPATCH_E(dt, launch_pdl(reduce_partials_k<E>, rg, 256, 0, s, (E*)dw, (E*)db, C, ws, P, 2 * C));
 }
 
 // ------------------------------------------------------------------ partial-row form
 bool layernorm_backward_fuses_colsum(DType dt, int C) {
-    return dt == DT_BF16 && (C / 8 + 31) / 32 <= 3 && (C * 2) % 16 == 0;
+    return dt != DT_F32 && (C / 8 + 31) / 32 <= 3 && (C * 2) % 16 == 0;
 }
 
 int layernorm_backward_part_rows(DType dt, int N, int C) {
     if (layernorm_backward_fuses_colsum(dt, C)) return N < num_sms() ? N : num_sms();
     const size_t smem = sizeof(float) * 2 * C * (LNB_BLOCK / 32);
-    const int nv = (C / (dt == DT_BF16 ? 8 : 4) + 31) / 32;
+    const int nv = (C / dtype_vec(dt) + 31) / 32;
     if (dt == DT_BF16) {
         switch (nv) {
             case 4: return lnb_blocks<bf16, 4>(N, smem); case 5: return lnb_blocks<bf16, 5>(N, smem);
             case 6: return lnb_blocks<bf16, 6>(N, smem); case 7: return lnb_blocks<bf16, 7>(N, smem);
             default: return lnb_blocks<bf16, 8>(N, smem);
+        }
+    }
+    if (dt == DT_F16) {  // (each instantiation opts in to its shared memory itself)
+        switch (nv) {
+            case 4: return lnb_blocks<f16, 4>(N, smem); case 5: return lnb_blocks<f16, 5>(N, smem);
+            case 6: return lnb_blocks<f16, 6>(N, smem); case 7: return lnb_blocks<f16, 7>(N, smem);
+            default: return lnb_blocks<f16, 8>(N, smem);
         }
     }
     switch (nv) {
@@ -1083,11 +1109,11 @@ int layernorm_backward_part_rows(DType dt, int N, int C) {
     }
 }
 
-template <int NV> static size_t lnq_opt_in(int C) {
+template <typename H, int NV> static size_t lnq_opt_in(int C) {
     const size_t smem = lnq_body_bytes(C, (LNQ_THREADS / 32 - 1) / NV) + 16 * LNQ_RING + 16 + LNQ_XCH * 20;
     static size_t done = 0;
     if (smem > done) {
-        cudaFuncSetAttribute(layernorm_backward_bulk_k<NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(layernorm_backward_bulk_k<H, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
         done = smem;
     }
@@ -1105,40 +1131,44 @@ int launch_layernorm_backward_part(DType dt, void* dinp, float* part, const void
         const size_t ring = (size_t)LNW_WARPS * LNW_BUF * 3 * C * 2, fold = sizeof(float) * LNW_WARPS * 3 * C;
         const size_t smem = ring > fold ? ring : fold;
         note_launch(1);
-#define LNW(NVV)                                                                                       \
+#define LNW(H, NVV)                                                                                    \
     do {                                                                                               \
         static size_t done = 0;                                                                        \
         if (smem > done) {                                                                             \
-            cudaFuncSetAttribute(layernorm_backward_warp_k<NVV>,                                       \
+            cudaFuncSetAttribute(layernorm_backward_warp_k<H, NVV>,                                    \
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);              \
             done = smem;                                                                               \
         }                                                                                              \
-        launch_pdl(layernorm_backward_warp_k<NVV>, dim3(P), dim3(32 * LNW_WARPS), smem, s,             \
-                   (bf16*)dinp, part, (const bf16*)dout, (const bf16*)inp, (const bf16*)w, mean, rstd, \
+        launch_pdl(layernorm_backward_warp_k<H, NVV>, dim3(P), dim3(32 * LNW_WARPS), smem, s,          \
+                   (H*)dinp, part, (const H*)dout, (const H*)inp, (const H*)w, mean, rstd,             \
                    N, C, accumulate, with_colsum);                                                     \
     } while (0)
-        if (nv == 1) LNW(1);
-        else if (nv == 2) LNW(2);
-        else LNW(3);
+        if (dt == DT_BF16) {
+            if (nv == 1) LNW(bf16, 1); else if (nv == 2) LNW(bf16, 2); else LNW(bf16, 3);
+        } else {
+            if (nv == 1) LNW(f16, 1); else if (nv == 2) LNW(f16, 2); else LNW(f16, 3);
+        }
 #undef LNW
         return P;
     }
     if (layernorm_backward_fuses_colsum(dt, C)) {
         const int nv = (C / 8 + 31) / 32;
         note_launch(1);
-#define LNQ(NVV)                                                                                 \
-    launch_pdl(layernorm_backward_bulk_k<NVV>, dim3(P), dim3(LNQ_THREADS),                       \
-               lnq_opt_in<NVV>(C), s, (bf16*)dinp, part, (const bf16*)dout, (const bf16*)inp,     \
-               (const bf16*)w, mean, rstd, N, C, accumulate, with_colsum, err)
-        if (nv == 1) LNQ(1);
-        else if (nv == 2) LNQ(2);
-        else LNQ(3);
+#define LNQ(H, NVV)                                                                              \
+    launch_pdl(layernorm_backward_bulk_k<H, NVV>, dim3(P), dim3(LNQ_THREADS),                    \
+               lnq_opt_in<H, NVV>(C), s, (H*)dinp, part, (const H*)dout, (const H*)inp,          \
+               (const H*)w, mean, rstd, N, C, accumulate, with_colsum, err)
+        if (dt == DT_BF16) {
+            if (nv == 1) LNQ(bf16, 1); else if (nv == 2) LNQ(bf16, 2); else LNQ(bf16, 3);
+        } else {
+            if (nv == 1) LNQ(f16, 1); else if (nv == 2) LNQ(f16, 2); else LNQ(f16, 3);
+        }
 #undef LNQ
         return P;
     }
     note_launch(1);
     const size_t smem = sizeof(float) * 2 * C * (LNB_BLOCK / 32);
-    const int nv = (C / (dt == DT_BF16 ? 8 : 4) + 31) / 32;
+    const int nv = (C / dtype_vec(dt) + 31) / 32;
 #define LNB2(TT, NVV)                                                                            \
     launch_pdl(layernorm_backward_k<TT, NVV>, dim3(P), dim3(LNB_BLOCK), smem, s, (TT*)dinp, part,  \
                (const TT*)dout, (const TT*)inp, (const TT*)w, mean, rstd, N, C, accumulate)
@@ -1146,6 +1176,11 @@ int launch_layernorm_backward_part(DType dt, void* dinp, float* part, const void
         switch (nv) {
             case 4: LNB2(bf16, 4); break; case 5: LNB2(bf16, 5); break; case 6: LNB2(bf16, 6); break;
             case 7: LNB2(bf16, 7); break; default: LNB2(bf16, 8); break;
+        }
+    } else if (dt == DT_F16) {
+        switch (nv) {
+            case 4: LNB2(f16, 4); break; case 5: LNB2(f16, 5); break; case 6: LNB2(f16, 6); break;
+            case 7: LNB2(f16, 7); break; default: LNB2(f16, 8); break;
         }
     } else {
         switch (nv) {
@@ -1163,8 +1198,7 @@ void launch_reduce_partials_multi(DType dt, const PartialDesc* d_desc, int ndesc
     if (ndesc <= 0) return;
     note_launch(1);
     const dim3 grid((unsigned)((maxwidth + 255) / 256), (unsigned)ndesc);
-    if (dt == DT_BF16) launch_pdl(reduce_partials_multi_k<bf16>, grid, dim3(256), 0, s, d_desc);
-    else launch_pdl(reduce_partials_multi_k<float>, grid, dim3(256), 0, s, d_desc);
+    DISPATCH_E(dt, launch_pdl(reduce_partials_multi_k<E>, grid, dim3(256), 0, s, d_desc));
 }
 
 // ------------------------------------------------------------------ bias gradient
@@ -1228,18 +1262,17 @@ int colsum_part_rows(int M) {
 int launch_colsum_part(DType dt, float* part, const void* dout, int M, int N, cudaStream_t s) {
     const int R = colsum_part_rows(M);
     const int rps = (M + R - 1) / R;
-    const int VEC = dt == DT_BF16 ? 8 : 4;
+    const int VEC = dtype_vec(dt);
     const dim3 grid((N + 32 * VEC - 1) / (32 * VEC), R);
     note_launch(1);
-    if (dt == DT_BF16) launch_pdl(colsum_partial_k<bf16>, grid, dim3(256), 0, s, part, (const bf16*)dout, M, N, rps);
-    else launch_pdl(colsum_partial_k<float>, grid, dim3(256), 0, s, part, (const float*)dout, M, N, rps);
+    DISPATCH_E(dt, launch_pdl(colsum_partial_k<E>, grid, dim3(256), 0, s, part, (const E*)dout, M, N, rps));
     return R;
 }
 
 void launch_colsum_accum(DType dt, void* dbias, const void* dout, int M, int N, float* ws,
                          cudaStream_t s) {
     note_launch(2);
-    const int VEC = dt == DT_BF16 ? 8 : 4;
+    const int VEC = dtype_vec(dt);
     int R = (M + 31) / 32;
     if (R > CS_SLABS) R = CS_SLABS;
     if (R < 1) R = 1;
@@ -1247,13 +1280,8 @@ void launch_colsum_accum(DType dt, void* dbias, const void* dout, int M, int N, 
     R = (M + rps - 1) / rps;
     dim3 grid((N + 32 * VEC - 1) / (32 * VEC), R);
     const unsigned rg = (unsigned)((N + 31) / 32);
-    if (dt == DT_BF16) {
-        launch_pdl(colsum_partial_k<bf16>, grid, 256, 0, s, ws, (const bf16*)dout, M, N, rps);
-        launch_pdl(reduce_partials_k<bf16>, rg, 256, 0, s, (bf16*)dbias, (bf16*)dbias, N, ws, R, N);
-    } else {
-        launch_pdl(colsum_partial_k<float>, grid, 256, 0, s, ws, (const float*)dout, M, N, rps);
-        launch_pdl(reduce_partials_k<float>, rg, 256, 0, s, (float*)dbias, (float*)dbias, N, ws, R, N);
-    }
+    DISPATCH_E(dt, launch_pdl(colsum_partial_k<E>, grid, 256, 0, s, ws, (const E*)dout, M, N, rps);
+                   launch_pdl(reduce_partials_k<E>, rg, 256, 0, s, (E*)dbias, (E*)dbias, N, ws, R, N));
 }
 
 // ------------------------------------------------------------------ classifier
@@ -1280,9 +1308,11 @@ template <typename T>
 __global__ void __launch_bounds__(CLS_BLOCK, 3) classifier_k(T* __restrict__ logits,
                                                           float* __restrict__ losses,
                                                           const int* __restrict__ targets, int V,
-                                                          int Vp, float dloss) {
+                                                          int Vp, float dloss,
+                                                          const float* __restrict__ dloss_scale) {
     pdl_enter();
     constexpr int VEC = Vec16<T>::N;
+    if (dloss_scale) dloss *= *dloss_scale;  // loss scaling (fp16 training)
     __shared__ float s_max[32], s_sum[32];
     __shared__ float s_tlogit;
     const int row = blockIdx.x;
@@ -1353,12 +1383,10 @@ __global__ void __launch_bounds__(CLS_BLOCK, 3) classifier_k(T* __restrict__ log
 }
 
 void launch_classifier(DType dt, void* logits, float* losses, const int* targets, int BT, int V,
-                       int Vp, float dloss, cudaStream_t s) {
+                       int Vp, float dloss, cudaStream_t s, const float* dloss_scale) {
     note_launch(1);
-    if (dt == DT_BF16)
-        launch_pdl(classifier_k<bf16>, BT, CLS_BLOCK, 0, s, (bf16*)logits, losses, targets, V, Vp, dloss);
-    else
-        launch_pdl(classifier_k<float>, BT, CLS_BLOCK, 0, s, (float*)logits, losses, targets, V, Vp, dloss);
+    DISPATCH_E(dt, launch_pdl(classifier_k<E>, BT, CLS_BLOCK, 0, s, (E*)logits, losses, targets, V, Vp, dloss,
+                              dloss_scale));
 }
 
 // ------------------------------------------------------------------ inference
@@ -1392,8 +1420,7 @@ __global__ void __launch_bounds__(512) probs_k(float* __restrict__ probs, const 
 
 void launch_probs(DType dt, float* probs, const void* logits, int rows, int V, int Vp, cudaStream_t s) {
     note_launch(1);
-    if (dt == DT_BF16) launch_pdl(probs_k<bf16>, rows, 512, 0, s, probs, (const bf16*)logits, V, Vp);
-    else launch_pdl(probs_k<float>, rows, 512, 0, s, probs, (const float*)logits, V, Vp);
+    DISPATCH_E(dt, launch_pdl(probs_k<E>, rows, 512, 0, s, probs, (const E*)logits, V, Vp));
 }
 
 // sample_softmax on the device: one block per row r, logits row at
@@ -1471,12 +1498,8 @@ __global__ void __launch_bounds__(SAMPLE_BLOCK) sample_k(const T* __restrict__ l
 void launch_sample(DType dt, const void* logits, long long row_stride, int rows, int V, const float* coins,
                    int* out, long long out_stride, cudaStream_t s) {
     note_launch(1);
-    if (dt == DT_BF16)
-        launch_pdl(sample_k<bf16>, rows, SAMPLE_BLOCK, 0, s, (const bf16*)logits, row_stride, V, coins, out,
-                   out_stride);
-    else
-        launch_pdl(sample_k<float>, rows, SAMPLE_BLOCK, 0, s, (const float*)logits, row_stride, V, coins, out,
-                   out_stride);
+    DISPATCH_E(dt, launch_pdl(sample_k<E>, rows, SAMPLE_BLOCK, 0, s, (const E*)logits, row_stride, V, coins,
+                              out, out_stride));
 }
 
 // mean of n floats in a fixed order (single block)
@@ -1557,18 +1580,26 @@ DEVI float adamw_one_sr(float g, float& m, float& v, float old, float lr, float 
 }
 
 // SR: bf16 parameters without a master copy, updated in place with
-// stochastic rounding (seed: this step's, or hyper[7] in graph replays)
+// stochastic rounding (seed: this step's, or hyper[7] in graph replays).
+// scaler (fp16 training): the gradients hold loss-scale times the gradient;
+// a step whose gradients overflowed is skipped, the others are unscaled
+// (multiplied by 1/scale, a power of two: exact).
 template <typename T, bool SR>
 __global__ void adamw_k(T* __restrict__ params, float* __restrict__ master,
                         const T* __restrict__ grads, float* __restrict__ mst,
                         float* __restrict__ vst, const AdamRanges r, float lr, float b1, float b2,
                         float c1, float c2, float eps, float wd, uint32_t seed,
-                        const float* __restrict__ hyper) {
+                        const float* __restrict__ hyper, const LossScaler* __restrict__ scaler) {
     pdl_enter();
     if (hyper) {  // hyperparameters from device memory (graph replays)
         lr = hyper[0]; b1 = hyper[1]; b2 = hyper[2]; c1 = hyper[3]; c2 = hyper[4];
         eps = hyper[5]; wd = hyper[6];
         seed = __float_as_uint(hyper[7]);
+    }
+    float inv_scale = 1.f;
+    if (scaler) {
+        if (scaler->found_inf) return;  // the whole update is skipped
+        inv_scale = 1.f / scaler->scale;
     }
     // this block row's range of the flat parameter buffers
     const size_t off = r.off[blockIdx.y], n = r.n[blockIdx.y];
@@ -1585,9 +1616,9 @@ __global__ void adamw_k(T* __restrict__ params, float* __restrict__ master,
             float g[4], th[4];
             if constexpr (sizeof(T) == 2) {
                 uint2 graw = __ldcs(reinterpret_cast<const uint2*>(grads + i));
-                const bf16* gb = reinterpret_cast<const bf16*>(&graw);
+                const T* gb = reinterpret_cast<const T*>(&graw);
 #pragma unroll
-                for (int k = 0; k < 4; k++) g[k] = to_f(gb[k]);
+                for (int k = 0; k < 4; k++) g[k] = to_f(gb[k]) * inv_scale;
             } else {
                 float4 g4 = __ldcs(reinterpret_cast<const float4*>(grads + i));
                 g[0] = g4.x; g[1] = g4.y; g[2] = g4.z; g[3] = g4.w;
@@ -1611,11 +1642,11 @@ __global__ void adamw_k(T* __restrict__ params, float* __restrict__ master,
                 __stcs(reinterpret_cast<float4*>(master + i), make_float4(th[0], th[1], th[2], th[3]));
             if constexpr (sizeof(T) == 2) {
                 uint2 praw;
-                bf16* pb = reinterpret_cast<bf16*>(&praw);
+                T* pb = reinterpret_cast<T*>(&praw);
 #pragma unroll
                 for (int k = 0; k < 4; k++) {
                     if constexpr (SR) pb[k] = round_bf16_stochastic(th[k], off + i + k, seed);
-                    else pb[k] = from_f<bf16>(th[k]);
+                    else pb[k] = from_f<T>(th[k]);
                 }
                 __stcs(reinterpret_cast<uint2*>(params + i), praw);
             } else {
@@ -1630,7 +1661,7 @@ __global__ void adamw_k(T* __restrict__ params, float* __restrict__ master,
                     if constexpr (sizeof(T) == 2) params[j] = round_bf16_stochastic(th, off + j, seed);
                 } else {
                     float th = master ? master[j] : to_f(params[j]);
-                    th = adamw_one<T>(to_f(grads[j]), mm, vv, th, lr, b1, b2, c1, c2, eps, wd);
+                    th = adamw_one<T>(to_f(grads[j]) * inv_scale, mm, vv, th, lr, b1, b2, c1, c2, eps, wd);
                     if (master) master[j] = th;
                     params[j] = from_f<T>(th);
                 }
@@ -1643,18 +1674,19 @@ __global__ void adamw_k(T* __restrict__ params, float* __restrict__ master,
 
 void launch_adamw(DType dt, void* params, float* master, const void* grads, float* m, float* v,
                   size_t n, float lr, float b1, float b2, float c1, float c2, float eps, float wd,
-                  const float* hyper, cudaStream_t s, bool stochastic, uint32_t seed) {
+                  const float* hyper, cudaStream_t s, bool stochastic, uint32_t seed,
+                  const LossScaler* scaler) {
     AdamRanges r = {};
     r.off[0] = 0;
     r.n[0] = n;
     launch_adamw_ranges(dt, params, master, grads, m, v, r, 1, lr, b1, b2, c1, c2, eps, wd, hyper, s,
-                        stochastic, seed);
+                        stochastic, seed, scaler);
 }
 
 void launch_adamw_ranges(DType dt, void* params, float* master, const void* grads, float* m,
                          float* v, const AdamRanges& r, int nranges, float lr, float b1, float b2,
                          float c1, float c2, float eps, float wd, const float* hyper, cudaStream_t s,
-                         bool stochastic, uint32_t seed) {
+                         bool stochastic, uint32_t seed, const LossScaler* scaler) {
     if (nranges <= 0) return;
     size_t nmax = 0;
     for (int i = 0; i < nranges; i++) nmax = r.n[i] > nmax ? r.n[i] : nmax;
@@ -1662,13 +1694,64 @@ void launch_adamw_ranges(DType dt, void* params, float* master, const void* grad
     const dim3 grid(grid_for((nmax + 3) / 4, 256, 8), (unsigned)nranges);
     if (dt == DT_BF16 && stochastic)
         launch_pdl(adamw_k<bf16, true>, grid, dim3(256), 0, s, (bf16*)params, (float*)nullptr,
-                   (const bf16*)grads, m, v, r, lr, b1, b2, c1, c2, eps, wd, seed, hyper);
-    else if (dt == DT_BF16)
-        launch_pdl(adamw_k<bf16, false>, grid, dim3(256), 0, s, (bf16*)params, master, (const bf16*)grads, m,
-                   v, r, lr, b1, b2, c1, c2, eps, wd, seed, hyper);
+                   (const bf16*)grads, m, v, r, lr, b1, b2, c1, c2, eps, wd, seed, hyper, scaler);
     else
-        launch_pdl(adamw_k<float, false>, grid, dim3(256), 0, s, (float*)params, master, (const float*)grads,
-                   m, v, r, lr, b1, b2, c1, c2, eps, wd, seed, hyper);
+        DISPATCH_E(dt, launch_pdl(adamw_k<E, false>, grid, dim3(256), 0, s, (E*)params, master,
+                                  (const E*)grads, m, v, r, lr, b1, b2, c1, c2, eps, wd, seed, hyper,
+                                  scaler));
+}
+
+// ------------------------------------------------------------------ loss scaling (fp16)
+// found_inf = 1 if any gradient is inf or NaN (its exponent bits all ones)
+template <typename T>
+__global__ void nonfinite_k(const T* __restrict__ g, size_t n, LossScaler* __restrict__ sc) {
+    pdl_enter();
+    constexpr int VEC = Vec16<T>::N;
+    bool bad = false;
+    const size_t nv = n / VEC;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += (size_t)gridDim.x * blockDim.x) {
+        const uint4 u = __ldcs(reinterpret_cast<const uint4*>(g) + i);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            if constexpr (sizeof(T) == 2) {
+                constexpr uint32_t E = std::is_same<T, f16>::value ? 0x7C007C00u : 0x7F807F80u;
+                bad |= (w[k] & 0xFFFFu & E) == (E & 0xFFFFu) || (w[k] & 0xFFFF0000u & E) == (E & 0xFFFF0000u);
+            } else {
+                bad |= (w[k] & 0x7F800000u) == 0x7F800000u;
+            }
+        }
+    }
+    for (size_t j = nv * VEC + (size_t)blockIdx.x * blockDim.x + threadIdx.x; j < n;
+         j += (size_t)gridDim.x * blockDim.x)
+        bad |= !isfinite(to_f(g[j]));
+    if (__syncthreads_or(bad) && threadIdx.x == 0) sc->found_inf = 1;
+}
+
+void launch_nonfinite(DType dt, const void* grads, size_t n, LossScaler* sc, cudaStream_t s) {
+    note_launch(1);
+    const unsigned g = grid_for(n / 8 + 1, 256, 8);
+    DISPATCH_E(dt, launch_pdl(nonfinite_k<E>, g, 256, 0, s, (const E*)grads, n, sc));
+}
+
+// after the update: an overflowed step halves the scale and restarts the count
+// of good steps; growth_interval good steps in a row double it
+__global__ void scaler_update_k(LossScaler* __restrict__ sc) {
+    pdl_enter();
+    if (sc->found_inf) {
+        sc->scale *= 0.5f;
+        sc->good_steps = 0;
+        sc->skipped += 1;
+    } else if (++sc->good_steps >= sc->growth_interval) {
+        sc->scale *= 2.0f;
+        sc->good_steps = 0;
+    }
+    sc->found_inf = 0;
+}
+
+void launch_scaler_update(LossScaler* sc, cudaStream_t s) {
+    note_launch(1);
+    launch_pdl(scaler_update_k, 1, 1, 0, s, sc);
 }
 
 __global__ void set_hyper_k(float* h, float lr, float b1, float b2, float c1, float c2, float eps,
@@ -1772,15 +1855,13 @@ void launch_init_normal(DType dt, void* p, size_t n, float stddev, unsigned long
                         unsigned long long stream_id, cudaStream_t s) {
     note_launch(1);
     unsigned g = grid_for(n, 256, 16);
-    if (dt == DT_BF16) init_normal_k<bf16><<<g, 256, 0, s>>>((bf16*)p, n, stddev, seed, stream_id);
-    else init_normal_k<float><<<g, 256, 0, s>>>((float*)p, n, stddev, seed, stream_id);
+    DISPATCH_E(dt, init_normal_k<E><<<g, 256, 0, s>>>((E*)p, n, stddev, seed, stream_id));
 }
 
 void launch_fill(DType dt, void* p, size_t n, float value, cudaStream_t s) {
     note_launch(1);
     unsigned g = grid_for(n, 256, 16);
-    if (dt == DT_BF16) fill_k<bf16><<<g, 256, 0, s>>>((bf16*)p, n, value);
-    else fill_k<float><<<g, 256, 0, s>>>((float*)p, n, value);
+    DISPATCH_E(dt, fill_k<E><<<g, 256, 0, s>>>((E*)p, n, value));
 }
 
 template <typename T>
@@ -1799,14 +1880,12 @@ __global__ void from_f32_k(T* __restrict__ dst, const float* __restrict__ src, s
 void launch_to_f32(DType dt, float* dst, const void* src, size_t n, cudaStream_t s) {
     note_launch(1);
     unsigned g = grid_for(n, 256, 16);
-    if (dt == DT_BF16) to_f32_k<bf16><<<g, 256, 0, s>>>(dst, (const bf16*)src, n);
-    else to_f32_k<float><<<g, 256, 0, s>>>(dst, (const float*)src, n);
+    DISPATCH_E(dt, to_f32_k<E><<<g, 256, 0, s>>>(dst, (const E*)src, n));
 }
 void launch_from_f32(DType dt, void* dst, const float* src, size_t n, cudaStream_t s) {
     note_launch(1);
     unsigned g = grid_for(n, 256, 16);
-    if (dt == DT_BF16) from_f32_k<bf16><<<g, 256, 0, s>>>((bf16*)dst, src, n);
-    else from_f32_k<float><<<g, 256, 0, s>>>((float*)dst, src, n);
+    DISPATCH_E(dt, from_f32_k<E><<<g, 256, 0, s>>>((E*)dst, src, n));
 }
 
 // ------------------------------------------------------------------ fused operator, pass 2

@@ -2,13 +2,14 @@
 //
 //  * fused_linear_bias_gelu_softmax: y = softmax_row(gelu_tanh(x W^T + b))
 //    (POPCORNBENCH "fused Linear + GELU + Softmax" problem: nn.Linear, GELU,
-//    softmax over dim 1). x and W are split into bf16 halves (hi, lo) and
-//    x W^T runs as hi.hi + hi.lo + lo.hi on the bf16 tensor cores (about
-//    2^-16 relative per product, fp32 accumulation); the GEMM epilogue adds
-//    the bias, applies GELU, stores the row tile and records, per row and
-//    256-column tile, (max, sum exp(v - max)). The last pass merges the tile
-//    partials of each row and rewrites the row as exp(v - max) / sum. The
-//    allocation-free variant keeps the single-pass TF32 GEMM.
+//    softmax over dim 1). The product kernel (fused_tc.cu) splits x and W into
+//    bf16 halves (hi, lo) in shared memory as their fp32 tiles arrive and runs
+//    x W^T as hi.hi + hi.lo + lo.hi on the bf16 tensor cores (about 2^-16
+//    relative per product, fp32 accumulation); its epilogue adds the bias,
+//    applies GELU, stores the row tile and records, per row and 256-column
+//    tile, (max, sum exp(v - max)). The last pass merges the tile partials of
+//    each row and rewrites the row as exp(v - max) / sum. The allocation-free
+//    variant runs the same two kernels with its partials in a static array.
 //  * gpt2_gemm / gpt2_attention_forward / gpt2_attention_backward: the
 //    training step's kernels exposed one at a time.
 #include "gpt2.h"
@@ -54,6 +55,9 @@ unsigned int* err_word(int dev) {
 
 bool al16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+bool known_dtype(int dtype) { return dtype == GPT2_FP32 || dtype == GPT2_BF16 || dtype == GPT2_FP16; }
+DType to_dt(int dtype) { return dtype == GPT2_BF16 ? DT_BF16 : dtype == GPT2_FP16 ? DT_F16 : DT_F32; }
+
 }  // namespace
 
 static int noalloc_err_of(int dev, unsigned int* bits);
@@ -69,17 +73,10 @@ int fused_linear_bias_gelu_softmax(const float* x, const float* W, const float* 
     if (current_device(&dev) != GPT2_OK) return GPT2_ERR_CUDA;
     unsigned int* err = err_word(dev);
     if (!err) return GPT2_ERR_NOMEM;
-    // the split operands are 3 * Kp columns wide and the GEMM's K is an int
-    if (K > (0x7fffffff / 3) - 8)
-        return set_error(GPT2_ERR_ARG, "fused op: K=%d too large for the split product", K);
-    const int tile_n = gemm_tc_part_tile_n();
+    const int tile_n = fused_split_tile_n();
     const int tiles = (int)(((long long)N + tile_n - 1) / tile_n);
-    // scratch: the row-tile softmax partials, then the split operands
-    // x' (M, 3Kp) and W' (N, 3Kp) in bf16
-    const int Kp = (K + 7) / 8 * 8;
-    const size_t part_bytes = ((size_t)M * tiles * 2 * sizeof(float) + 255) / 256 * 256;
-    const size_t xs_bytes = ((size_t)M * 3 * Kp * 2 + 255) / 256 * 256;
-    const size_t need = part_bytes + xs_bytes + (size_t)N * 3 * Kp * 2;
+    // scratch: the row-tile softmax partials
+    const size_t need = ((size_t)M * tiles * 2 * sizeof(float) + 255) / 256 * 256;
     char* scratch;
     {
         std::lock_guard<std::mutex> lk(ops_mu);
@@ -93,20 +90,8 @@ int fused_linear_bias_gelu_softmax(const float* x, const float* W, const float* 
         scratch = (char*)dev_part[dev];
     }
     float* part = (float*)scratch;
-    void* xs = scratch + part_bytes;
-    void* ws = scratch + part_bytes + xs_bytes;
     cudaStream_t s = (cudaStream_t)stream;
-    // x W^T as hi.hi + hi.lo + lo.hi over bf16 halves of each fp32 operand, on
-    // the bf16 tensor cores (fp32 accumulation)
-    launch_split_bf16x3(xs, x, M, K, Kp, 0, s);
-    launch_split_bf16x3(ws, W, N, K, Kp, 1, s);
-    GemmParams p = {};
-    p.A = xs; p.lda = 3LL * Kp; p.a_kmajor = 1;
-    p.B = ws; p.ldb = 3LL * Kp; p.b_kmajor = 1;
-    p.D = out; p.ldd = N; p.bias = b;
-    p.part = part; p.part_ld = tiles;
-    p.M = M; p.N = N; p.K = 3 * Kp; p.epi = EPI_GELU_PART;
-    int rc = gemm_tc(p, DT_BF16, s, err);
+    const int rc = launch_fused_split_gemm(x, W, b, out, part, tiles, M, K, N, s, err);
     if (rc != GPT2_OK) return rc;
     launch_softmax_finish(out, part, M, N, tiles, s);
     return launch_status();
@@ -117,7 +102,7 @@ int gpt2_gemm(int dtype, int tensor_cores, int epilogue, const void* A, long lon
               const void* aux, long long ldaux, void* D2, int M, int N, int K, float* ws,
               size_t ws_floats, void* stream) {
     if (!A || !B || !D) return GPT2_ERR_ARG;
-    if (dtype != GPT2_FP32 && dtype != GPT2_BF16) return GPT2_ERR_CONFIG;
+    if (!known_dtype(dtype)) return GPT2_ERR_CONFIG;
     if (epilogue < EPI_STORE || epilogue > EPI_ACCUM) return GPT2_ERR_ARG;
     if ((epilogue == EPI_RESID || epilogue == EPI_GELU_BWD) && !aux) return GPT2_ERR_ARG;
     if (epilogue == EPI_GELU && !D2) return GPT2_ERR_ARG;
@@ -128,7 +113,7 @@ int gpt2_gemm(int dtype, int tensor_cores, int epilogue, const void* A, long lon
     p.M = M; p.N = N; p.K = K; p.epi = epilogue;
     if (ws && ((uintptr_t)ws & 15u)) return GPT2_ERR_ALIGN;
     p.ws = ws; p.ws_floats = ws ? ws_floats : 0;
-    const DType dt = dtype == GPT2_BF16 ? DT_BF16 : DT_F32;
+    const DType dt = to_dt(dtype);
     int rc;
     if (tensor_cores) {
         int dev;
@@ -149,12 +134,12 @@ int gpt2_attention_forward(int dtype, int tensor_cores, const void* qkv, void* o
     if (B < 1 || T < 1 || NH < 1 || C % NH) return GPT2_ERR_ARG;
     const int HS = C / NH;
     if (HS != 16 && HS != 32 && HS != 64 && HS != 128) return GPT2_ERR_CONFIG;
-    if (dtype != GPT2_FP32 && dtype != GPT2_BF16) return GPT2_ERR_CONFIG;
+    if (!known_dtype(dtype)) return GPT2_ERR_CONFIG;
     int dev;
     if (current_device(&dev) != GPT2_OK) return GPT2_ERR_CUDA;
     unsigned int* err = err_word(dev);
     if (!err) return GPT2_ERR_NOMEM;
-    const int rc = launch_attention_forward(dtype == GPT2_BF16 ? DT_BF16 : DT_F32, tensor_cores, out,
+    const int rc = launch_attention_forward(to_dt(dtype), tensor_cores, out,
                                             lse, qkv, B, T, C, NH, (cudaStream_t)stream, err);
     if (rc != GPT2_OK) return rc;
     return launch_status();
@@ -167,12 +152,12 @@ int gpt2_attention_backward(int dtype, int tensor_cores, const void* dout, const
     if (B < 1 || T < 1 || NH < 1 || C % NH) return GPT2_ERR_ARG;
     const int HS = C / NH;
     if (HS != 16 && HS != 32 && HS != 64 && HS != 128) return GPT2_ERR_CONFIG;
-    if (dtype != GPT2_FP32 && dtype != GPT2_BF16) return GPT2_ERR_CONFIG;
+    if (!known_dtype(dtype)) return GPT2_ERR_CONFIG;
     int dev;
     if (current_device(&dev) != GPT2_OK) return GPT2_ERR_CUDA;
     unsigned int* err = err_word(dev);
     if (!err) return GPT2_ERR_NOMEM;
-    const int rc = launch_attention_backward(dtype == GPT2_BF16 ? DT_BF16 : DT_F32, tensor_cores, dqkv,
+    const int rc = launch_attention_backward(to_dt(dtype), tensor_cores, dqkv,
                                              dout, qkv, out, lse, scratch_D, B, T, C, NH,
                                              (cudaStream_t)stream, err);
     if (rc != GPT2_OK) return rc;
@@ -182,9 +167,9 @@ int gpt2_attention_backward(int dtype, int tensor_cores, const void* dout, const
 int gpt2_layernorm_forward(int dtype, void* out, float* mean, float* rstd, const void* inp,
                            const void* w, const void* b, int N, int C, void* stream) {
     if (!out || !mean || !rstd || !inp || !w || !b) return GPT2_ERR_ARG;
-    if (dtype != GPT2_FP32 && dtype != GPT2_BF16) return GPT2_ERR_CONFIG;
-    if (N < 1 || C < 8 || C % 8 || C > (dtype == GPT2_BF16 ? 2048 : 1024)) return GPT2_ERR_ARG;
-    launch_layernorm_forward(dtype == GPT2_BF16 ? DT_BF16 : DT_F32, out, mean, rstd, inp, w, b, N,
+    if (!known_dtype(dtype)) return GPT2_ERR_CONFIG;
+    if (N < 1 || C < 8 || C % 8 || C > (dtype == GPT2_FP32 ? 1024 : 2048)) return GPT2_ERR_ARG;
+    launch_layernorm_forward(to_dt(dtype), out, mean, rstd, inp, w, b, N,
                              C, (cudaStream_t)stream);
     return launch_status();
 }
@@ -195,13 +180,13 @@ int gpt2_layernorm_backward(int dtype, void* dinp, void* dw, void* db, const voi
                             const void* inp, const void* w, const float* mean, const float* rstd,
                             int N, int C, int accumulate, float* scratch, void* stream) {
     if (!dinp || !dw || !db || !dout || !inp || !w || !mean || !rstd || !scratch) return GPT2_ERR_ARG;
-    if (dtype != GPT2_FP32 && dtype != GPT2_BF16) return GPT2_ERR_CONFIG;
-    if (N < 1 || C < 8 || C % 8 || C > (dtype == GPT2_BF16 ? 2048 : 1024)) return GPT2_ERR_ARG;
+    if (!known_dtype(dtype)) return GPT2_ERR_CONFIG;
+    if (N < 1 || C < 8 || C % 8 || C > (dtype == GPT2_FP32 ? 1024 : 2048)) return GPT2_ERR_ARG;
     int dev;
     if (current_device(&dev) != GPT2_OK) return GPT2_ERR_CUDA;
     unsigned int* err = err_word(dev);
     if (!err) return GPT2_ERR_NOMEM;
-    launch_layernorm_backward(dtype == GPT2_BF16 ? DT_BF16 : DT_F32, dinp, dw, db, dout, inp, w, mean,
+    launch_layernorm_backward(to_dt(dtype), dinp, dw, db, dout, inp, w, mean,
                               rstd, N, C, accumulate, scratch, err, (cudaStream_t)stream);
     return launch_status();
 }
@@ -313,7 +298,7 @@ extern "C" int fused_linear_bias_gelu_softmax_noalloc(const float* x, const floa
     if (!al16(x) || !al16(W) || !al16(b) || !al16(out) || K % 4 || N % 4)
         return gk::set_error(GPT2_ERR_ALIGN,
                              "fused op (no-alloc): pointers must be 16-byte aligned, K and N multiples of 4");
-    const int tile_n = gemm_tc_part_tile_n();
+    const int tile_n = fused_split_tile_n();
     const long long tiles = ((long long)N + tile_n - 1) / tile_n;
     if ((long long)M * tiles > NOALLOC_MAX_PARTIALS)
         return gk::set_error(GPT2_ERR_ARG,
@@ -326,14 +311,8 @@ extern "C" int fused_linear_bias_gelu_softmax_noalloc(const float* x, const floa
     if (noalloc_setup(dev, &d) != GPT2_OK)
         return gk::set_error(GPT2_ERR_CUDA, "fused op (no-alloc): cudaGetSymbolAddress failed");
     cudaStream_t s = (cudaStream_t)stream;
-    GemmParams p = {};
-    p.A = x; p.lda = K; p.a_kmajor = 1;
-    p.B = W; p.ldb = K; p.b_kmajor = 1;
-    p.D = out; p.ldd = N; p.bias = b;
-    p.part = d.part; p.part_ld = (int)tiles;
-    p.M = M; p.N = N; p.K = K; p.epi = EPI_GELU_PART;
-    int rc = gemm_tc(p, DT_F32, s, d.err);
-    if (rc != GPT2_OK) return gk::set_error(rc, "fused op (no-alloc): GEMM launch rejected");
+    const int rc = launch_fused_split_gemm(x, W, b, out, d.part, (int)tiles, M, K, N, s, d.err);
+    if (rc != GPT2_OK) return rc;
     launch_softmax_finish(out, d.part, M, N, (int)tiles, s);
     if (cudaGetLastError() != cudaSuccess)
         return gk::set_error(GPT2_ERR_CUDA, "fused op (no-alloc): launch failed");

@@ -205,7 +205,8 @@ template <int CG> DEVI void umma_commit_local(uint32_t bar) {
             : "memory");
 }
 
-// KIND 0: kind::f16 with bf16 operands; KIND 1: kind::tf32
+// KIND 0: kind::f16 with bf16 operands; KIND 1: kind::tf32; KIND 2: kind::f16
+// with fp16 operands (the operand type is in the instruction descriptor)
 #define UMMA_ASM(GROUP, KINDS)                                                            \
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"                        \
                  "tcgen05.mma.cta_group::" GROUP ".kind::" KINDS " [%0], %1, %2, %3, p;\n\t}\n" ::"r"( \
@@ -214,8 +215,8 @@ template <int CG> DEVI void umma_commit_local(uint32_t bar) {
                  : "memory")
 template <int KIND, int CG>
 DEVI void umma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
-    if constexpr (KIND == 0 && CG == 1) UMMA_ASM("1", "f16");
-    else if constexpr (KIND == 0) UMMA_ASM("2", "f16");
+    if constexpr (KIND != 1 && CG == 1) UMMA_ASM("1", "f16");
+    else if constexpr (KIND != 1) UMMA_ASM("2", "f16");
     else if constexpr (CG == 1) UMMA_ASM("1", "tf32");
     else UMMA_ASM("2", "tf32");
 }
@@ -236,8 +237,8 @@ DEVI void umma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, 
                  : "memory")
 template <int KIND, int CG>
 DEVI void umma_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
-    if constexpr (KIND == 0 && CG == 1) UMMA_WARP_ASM("1", "f16");
-    else if constexpr (KIND == 0) UMMA_WARP_ASM("2", "f16");
+    if constexpr (KIND != 1 && CG == 1) UMMA_WARP_ASM("1", "f16");
+    else if constexpr (KIND != 1) UMMA_WARP_ASM("2", "f16");
     else if constexpr (CG == 1) UMMA_WARP_ASM("1", "tf32");
     else UMMA_WARP_ASM("2", "tf32");
 }
@@ -425,11 +426,12 @@ DEVI uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
 }
 
 // Instruction descriptor: D fp32 (bits 4-5 = 1), A/B format (bits 7-9,
-// 10-12: bf16 = 1 for kind::f16, tf32 = 2 for kind::tf32), A/B major
-// (bits 15/16: 1 = MN-major), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+// 10-12: fp16 = 0 and bf16 = 1 for kind::f16, tf32 = 2 for kind::tf32), A/B
+// major (bits 15/16: 1 = MN-major), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+// KIND as for umma: 0 bf16, 1 tf32, 2 fp16.
 template <int KIND>
 DEVI uint32_t idesc(int a_mn, int b_mn, int M, int N) {
-    uint32_t fmt = KIND == 0 ? 1u : 2u;
+    uint32_t fmt = KIND == 0 ? 1u : KIND == 2 ? 0u : 2u;
     uint32_t d = 0;
     d |= 1u << 4;
     d |= fmt << 7;

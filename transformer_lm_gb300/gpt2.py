@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgpt2.so"
 
 GPT2_FP32 = 0
 GPT2_BF16 = 1
+GPT2_FP16 = 2
 
 ERRORS = {0: "OK", -1: "CONFIG", -2: "STATE", -3: "SHAPE", -4: "TOKEN", -5: "ALIGN", -6: "CUDA",
           -7: "NOMEM", -8: "ARG", -9: "DEVICE_TIMEOUT"}
@@ -70,6 +71,8 @@ _SIGS = {
     "gpt2_get_activation": (_i, [_i, _i, _fp, ctypes.POINTER(_sz)]),
     "gpt2_free": (_i, []),
     "gpt2_sample": (_i, [_i, _fp, _ip]),
+    "gpt2_set_loss_scaling": (_i, [_f, _i]),
+    "gpt2_get_loss_scale": (_i, [_fp, ctypes.POINTER(_ll)]),
     "gpt2_generate": (_i, [_ip, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_ulonglong)]),
     "gpt2_last_error": (ctypes.c_char_p, []),
     "gpt2_last_status": (_i, []),
@@ -292,6 +295,18 @@ def gpt2_generate(tokens, B, T, t_begin, t_end, rng_state: int):
     _check("gpt2_generate", lib().gpt2_generate(tok.ctypes.data_as(_ip), B, T, t_begin, t_end,
                                                 ctypes.byref(st)))
     return tok.reshape(B, T), int(st.value)
+
+
+def gpt2_set_loss_scaling(init_scale: float, growth_interval: int) -> None:
+    _check("gpt2_set_loss_scaling", lib().gpt2_set_loss_scaling(init_scale, growth_interval))
+
+
+def gpt2_get_loss_scale():
+    """(current loss scale, updates skipped so far)."""
+    sc = ctypes.c_float()
+    sk = _ll()
+    _check("gpt2_get_loss_scale", lib().gpt2_get_loss_scale(ctypes.byref(sc), ctypes.byref(sk)))
+    return float(sc.value), int(sk.value)
 
 
 def gpt2_free() -> None:

@@ -123,6 +123,12 @@ def round_to_bf16(a: np.ndarray) -> np.ndarray:
     return u.astype(np.uint32).view(np.float32)
 
 
+def round_to_fp16(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest IEEE half (ties to even, numpy's
+    conversion); returns float32."""
+    return np.ascontiguousarray(a, dtype=np.float32).astype(np.float16).astype(np.float32)
+
+
 def fused_op_inputs(M: int, K: int, N: int, seed: int):
     """x ~ N(0,1) (M,K); W ~ N(0, 1/sqrt(K)) (N,K) in nn.Linear layout; b ~ U(-0.1, 0.1)."""
     x = normal(seed, 100, M * K).astype(np.float32).reshape(M, K)

@@ -19,7 +19,10 @@
 //               and its 128-byte bf16 lo row (over the second), both in the
 //               128-byte-swizzled K-major layout the MMA reads; two lanes share
 //               a row (one per box) and synchronise between reading and writing;
-//               then they signal the pair leader;
+//               then they signal their CTA's conversion barrier (in the second
+//               CTA of the pair, warp 1 forwards each completed phase to the
+//               leader's barrier: one cluster-scope arrival per stage instead
+//               of one per converter warp);
 //   warp 1      (leader) issues the 12 MMAs of a stage (3 products x 4 k-steps
 //               of 16) into one of two TMEM accumulators and commits the stage
 //               back to both CTAs' producers;
@@ -115,7 +118,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; s++) {
             mbar_init(full(s), 1);
-            mbar_init(conv(s), 2 * CONV_WARPS);
+            // leader: its converter warps and the peer's forwarder; peer: its converter warps
+            mbar_init(conv(s), rank == 0 ? CONV_WARPS + 1 : CONV_WARPS);
             mbar_init(empty(s), 1);
         }
         for (int c = 0; c < 2; c++) {
@@ -167,6 +171,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             *n_issued_smem = n_issued;
         }
     } else if (warp == 1) {
+        if (rank == 1) {
+            // ---------------- forwarder (second CTA): each completed local
+            // conversion phase becomes one arrival on the leader's barrier
+            const uint32_t conv_leader = mapa_rank(conv(0), 0);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int st = cid; ok && st < num_tiles; st += ncl) {
+                for (int kb = 0; kb < a.num_kb; kb++) {
+                    if (!mbar_wait_warp(conv(stage), phase, abort_flag)) { ok = false; break; }
+                    if (lane == 0) mbar_arrive_cluster(conv_leader + 8u * (uint32_t)stage);
+                    __syncwarp();
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+        }
         if (rank == 0) {
             // ---------------- MMA issuer (the pair leader, a converged warp)
             const uint32_t id = idesc<0>(0, 0, 2 * BM, BN);
@@ -205,7 +225,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int cw = warp - 2 - EPI_WARPS;
         const int box = (lane >> 3) & 1;
         const int rsub = (lane & 7) + ((lane >> 4) << 3);  // row within the warp's 16
-        const uint32_t conv_leader = mapa_rank(conv(0), 0);
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
@@ -247,7 +266,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // the generic-proxy writes become visible to the MMA's async proxy
                 fence_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(conv_leader + 8u * (uint32_t)stage);
+                if (lane == 0) mbar_arrive(conv(stage));  // this CTA's barrier
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }

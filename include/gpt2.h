@@ -155,6 +155,14 @@ int gpt2_train_step(const int* d_tokens, const int* d_targets, int B, int T, flo
 int gpt2_train_step_host(const int* tokens, const int* targets, int B, int T, float lr, float beta1,
                          float beta2, float eps, float weight_decay, int step, float* mean_loss);
 
+/* Time limit (nanoseconds) of every bounded in-kernel wait of the library's
+ * tensor-core and bulk-copy kernels on the current device (0 restores the
+ * default, 2 s). A kernel whose wait runs out sets GPT2_ERR_DEVICE_TIMEOUT in
+ * its error word, waits (up to 2 s, whatever this limit) for the copies and
+ * MMAs it has in flight, frees its tensor memory and returns; the results of
+ * that launch are undefined. Applies to launches made after the call. */
+int gpt2_set_wait_limit(unsigned long long ns);
+
 /* Wait for the stream; report GPT2_ERR_DEVICE_TIMEOUT / GPT2_ERR_TOKEN raised by kernels. */
 int gpt2_sync(void);
 

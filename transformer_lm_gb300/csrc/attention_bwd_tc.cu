@@ -622,4 +622,9 @@ int launch_flash_backward_tc(DType dt, void* dqkv, const void* dout, const void*
     return GPT2_OK;
 }
 
+// the bounded-wait limit of this translation unit's kernels (0: the default)
+int set_wait_limit_attn_bwd(unsigned long long ns) {
+    return tc::set_tu_wait_limit(ns ? ns : tc::WAIT_LIMIT_NS) == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+}
+
 }  // namespace gk

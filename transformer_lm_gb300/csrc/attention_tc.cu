@@ -488,4 +488,9 @@ int launch_flash_forward_tc(DType dt, void* out, float* lse, const void* qkv, in
     return GPT2_OK;
 }
 
+// the bounded-wait limit of this translation unit's kernels (0: the default)
+int set_wait_limit_attn_fwd(unsigned long long ns) {
+    return tc::set_tu_wait_limit(ns ? ns : tc::WAIT_LIMIT_NS) == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+}
+
 }  // namespace gk

@@ -461,4 +461,9 @@ int launch_fused_split_gemm(const float* x, const float* W, const float* b, floa
     return GPT2_OK;
 }
 
+// the bounded-wait limit of this translation unit's kernels (0: the default)
+int set_wait_limit_fused(unsigned long long ns) {
+    return tc::set_tu_wait_limit(ns ? ns : tc::WAIT_LIMIT_NS) == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+}
+
 }  // namespace gk

@@ -494,6 +494,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             atomicOr(args.err, DEVERR_TIMEOUT);
         }
+        if (CG == 2 && rank == 1 && threadIdx.x == 0) {
+            // this CTA's loads complete on the leader's barriers, which it cannot
+            // wait on: give any still in flight a bounded time (100 us) to land
+            const unsigned long long t0 = globaltimer();
+            while (globaltimer() - t0 < 100000ull) {
+            }
+        }
         if (warp == 1 && rank == 0) {  // the issuing lane commits (elected as when issuing)
             umma_commit_local_warp<CG>(drain);
             if (lane == 0) mbar_wait_drain(drain, 0);
@@ -834,6 +841,11 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
     if (cg == 2)
         return BN == 256 ? dispatch_epi<256, 1, 2>(p.epi, mp, a, s) : dispatch_epi<128, 1, 2>(p.epi, mp, a, s);
     return BN == 256 ? dispatch_epi<256, 1, 1>(p.epi, mp, a, s) : dispatch_epi<128, 1, 1>(p.epi, mp, a, s);
+}
+
+// the bounded-wait limit of this translation unit's kernels (0: the default)
+int set_wait_limit_gemm(unsigned long long ns) {
+    return tc::set_tu_wait_limit(ns ? ns : tc::WAIT_LIMIT_NS) == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
 }  // namespace gk

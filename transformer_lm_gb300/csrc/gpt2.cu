@@ -994,6 +994,14 @@ int gpt2_train_step_host(const int* tokens, const int* targets, int B, int T, fl
     return GPT2_OK;
 }
 
+int gpt2_set_wait_limit(unsigned long long ns) {
+    const int rc[5] = {set_wait_limit_gemm(ns), set_wait_limit_attn_fwd(ns), set_wait_limit_attn_bwd(ns),
+                       set_wait_limit_kernels(ns), set_wait_limit_fused(ns)};
+    for (int r : rc)
+        if (r != GPT2_OK) return fail(GPT2_ERR_CUDA, "setting the wait limit failed on the current device");
+    return GPT2_OK;
+}
+
 int gpt2_sync(void) {
     TRY(check_model());
     CUDA_TRY(cudaStreamSynchronize(g->stream));

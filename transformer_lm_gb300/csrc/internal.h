@@ -195,6 +195,14 @@ int launch_flash_backward_tc(DType dt, void* dqkv, const void* dout, const void*
 
 int num_sms();
 
+// the limit of the bounded in-kernel waits of each translation unit's kernels
+// (ns; 0 restores the default of 2 s); drain waits after an abort keep 2 s
+int set_wait_limit_gemm(unsigned long long ns);
+int set_wait_limit_attn_fwd(unsigned long long ns);
+int set_wait_limit_attn_bwd(unsigned long long ns);
+int set_wait_limit_kernels(unsigned long long ns);
+int set_wait_limit_fused(unsigned long long ns);
+
 // Programmatic dependent launch for the step's kernels (GPT2_PDL=0 turns it
 // off): the kernel may be scheduled while the previous one drains, and waits
 // for it in pdl_enter().

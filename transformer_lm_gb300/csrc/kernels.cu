@@ -10,6 +10,8 @@
 #include "internal.h"
 #include "tc_ptx.cuh"
 
+#include "gpt2.h"
+
 #include <math.h>
 #include <stdlib.h>
 
@@ -1928,6 +1930,11 @@ __global__ void __launch_bounds__(256) softmax_finish_k(float* __restrict__ y,
 void launch_softmax_finish(float* y, const float* part, int M, int N, int tiles, cudaStream_t s) {
     note_launch(1);
     softmax_finish_k<<<M, 256, 0, s>>>(y, (const float2*)part, N, tiles);
+}
+
+// the bounded-wait limit of this translation unit's kernels (0: the default)
+int set_wait_limit_kernels(unsigned long long ns) {
+    return tc::set_tu_wait_limit(ns ? ns : tc::WAIT_LIMIT_NS) == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
 }  // namespace gk

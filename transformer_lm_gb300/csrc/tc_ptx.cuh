@@ -12,7 +12,15 @@
 namespace gk {
 namespace tc {
 
-constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;   // default limit of a wait (2 s)
+constexpr unsigned long long DRAIN_LIMIT_NS = 2000000000ull;  // waits for in-flight work after an abort
+// The limit this translation unit's bounded waits use; host code changes it
+// with set_tu_wait_limit (a copy per translation unit, since device code is
+// not linked across them). The drain waits keep DRAIN_LIMIT_NS.
+static __device__ unsigned long long g_wait_limit_ns = WAIT_LIMIT_NS;
+static inline cudaError_t set_tu_wait_limit(unsigned long long ns) {
+    return cudaMemcpyToSymbol(g_wait_limit_ns, &ns, sizeof(ns));
+}
 
 // ------------------------------------------------------------------ PTX wrappers
 DEVI uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -74,11 +82,12 @@ DEVI unsigned long long globaltimer() {
 DEVI bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
+    const unsigned long long limit = *(volatile unsigned long long*)&g_wait_limit_ns;
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if ((it & 7u) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+            if (globaltimer() - t0 > limit) {
                 *abort_flag = 1;
                 return false;
             }
@@ -89,7 +98,7 @@ DEVI bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
 DEVI bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
     const unsigned long long t0 = globaltimer();
     while (!mbar_try_wait(bar, parity))
-        if (globaltimer() - t0 > WAIT_LIMIT_NS) return false;
+        if (globaltimer() - t0 > DRAIN_LIMIT_NS) return false;
     return true;
 }
 

@@ -60,6 +60,7 @@ _SIGS = {
     "gpt2_adamw": (_i, [_f, _f, _f, _f, _f, _i]),
     "gpt2_set_master_weights": (_i, [_i]),
     "gpt2_sync": (_i, []),
+    "gpt2_set_wait_limit": (_i, [ctypes.c_ulonglong]),
     "gpt2_num_params": (_sz, []),
     "gpt2_param_sizes": (_i, [ctypes.POINTER(_sz)]),
     "gpt2_get_params": (_i, [_fp]),
@@ -213,6 +214,10 @@ def gpt2_train_step_host(tokens, targets, B, T, lr, beta1, beta2, eps, weight_de
            lib().gpt2_train_step_host(_as_ip(tok), _as_ip(tgt), B, T, lr, beta1, beta2, eps,
                                       weight_decay, step, out.ctypes.data_as(_fp)))
     return out
+
+
+def gpt2_set_wait_limit(ns: int) -> None:
+    _check("gpt2_set_wait_limit", lib().gpt2_set_wait_limit(int(ns)))
 
 
 def gpt2_sync() -> None:

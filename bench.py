@@ -255,6 +255,11 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------------------- GPU arm
+def progress(msg: str) -> None:
+    """One line on stderr (the JSON result line is the only stdout output)."""
+    print(f"[bench {time.strftime('%H:%M:%S')}] {msg}", file=sys.stderr, flush=True)
+
+
 def profile_value(fname: str, key: str, sources: list[str]):
     """A number recorded in a committed ncu summary under profiles/, or None
     when any of the listed sources has changed since it was taken."""
@@ -280,6 +285,7 @@ def train_workload(world, rank, steps, warmup, peaks, stream, with_breakdown=Tru
     from transformer_lm_gb300 import gpt2 as G
     from transformer_lm_gb300 import inputs
 
+    progress(f"{DIMS}: init")
     G.gpt2_init(L, C, NH, V, Vp, MAXT, 1337 + rank)
     G.gpt2_set_stream(stream.cuda_stream)
     G.gpt2_set_grad_accum(ACCUM)
@@ -306,6 +312,7 @@ def train_workload(world, rank, steps, warmup, peaks, stream, with_breakdown=Tru
     for _ in range(warmup):
         device_step()
     G.gpt2_sync()
+    progress(f"{DIMS}: {warmup} warm-up steps done")
 
     # ---- device-resident timed region
     clocks = ClockSampler(torch.cuda.current_device())
@@ -331,6 +338,7 @@ def train_workload(world, rank, steps, warmup, peaks, stream, with_breakdown=Tru
     # ---- per-kernel durations: CUDA events around every launch, on the
     # library's stream, over a second pass of the same steps (kept out of
     # the timed region above because the extra event records slow the step)
+    progress(f"{DIMS}: timed region done, {ms / steps:.3f} ms/step")
     fam = None
     if with_breakdown:
         G.gpt2_timing_begin(steps * 500 * ACCUM * max(L, 12) // 12)
@@ -342,9 +350,11 @@ def train_workload(world, rank, steps, warmup, peaks, stream, with_breakdown=Tru
             t_ms, n, work = G.gpt2_timing_get(f)
             fam[f] = dict(ms=t_ms, launches=n, work=work)
 
+    progress(f"{DIMS}: per-kernel pass done")
     # ---- end-to-end through the host-buffer C-ABI call
-    for _ in range(2):
+    for i in range(2):
         host_step()
+        progress(f"{DIMS}: host-buffer warm-up step {i + 1} done")
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -415,6 +425,7 @@ def fused_workload(reps, warmup, peaks):
     res = {}
     for name, fn in (("fused_linear_bias_gelu_softmax", G.fused_linear_bias_gelu_softmax),
                      ("fused_linear_bias_gelu_softmax_noalloc", G.fused_linear_bias_gelu_softmax_noalloc)):
+        progress(f"{name}: timing")
         for _ in range(warmup):
             fn(dx, dW, db, out, M, K, N, s.cuda_stream)
         torch.cuda.synchronize()
@@ -448,7 +459,7 @@ def fused_workload(reps, warmup, peaks):
         "dtype": "f32 (bf16x3 split products on the tensor cores)",
         "tflop_per_s": achieved, "gpu_launches_per_call": main["launches"], "clocks": main["clocks"],
         "l2": "no flush: operands (320 MiB) exceed L2",
-        "roofline": {"bound": "tensor", "kernel": "gemm_tc_k EPI_GELU_PART (with its split and finish passes)",
+        "roofline": {"bound": "tensor", "kernel": "fused_split_gemm_k (with its softmax finish pass)",
                      "achieved": achieved, "peak": peak_tf32, "unit": "TFLOP/s",
                      "frac": achieved / peak_tf32,
                      "peak_source": f"{peaks['source']} bf16_tflops x 1.1/2.25 (nominal TF32:bf16)",

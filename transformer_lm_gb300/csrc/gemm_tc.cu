@@ -57,11 +57,18 @@ template <int BN, int CG, int NSTG = 1> struct Cfg {
     static constexpr int B_BYTES = (BN / CG) * ROWB;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int EPI_BYTES = EPI_WARPS * NSTG * STG_BYTES;
-    static constexpr int BAR_BYTES = 256 + 1024;  // barriers, flags, per-row softmax partials
+    static constexpr int BAR_BYTES = 256;  // barriers and flags
     static constexpr int STAGES = (227 * 1024 - EPI_BYTES - BAR_BYTES - 1024) / STAGE_BYTES;
     static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;  // two accumulators, power of two
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES + 1024;
-    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+    static constexpr int USED_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES + 1024;
+    static_assert(USED_BYTES <= 227 * 1024, "shared memory");
+    // Every CTA requests the per-block maximum, whatever its layout uses: a
+    // CTA then holds its SM alone, and no CTA of another kernel (one launched
+    // early by programmatic dependent launch, or one of the other stream's)
+    // shares the SM with the persistent tile loop. With the layout's size
+    // alone, small kernels could join a GEMM CTA on its SM; the GPT-2 350M
+    // step then stopped making progress now and then (not explained).
+    static constexpr int SMEM_BYTES = 227 * 1024;
 };
 
 struct Args {
@@ -75,8 +82,6 @@ struct Args {
     const void* aux;
     long long ldaux;
     void* D2;
-    float* part;
-    int part_ld;
     int splits, kb_per;  // split-K: K ranges per tile and k-blocks per range
     unsigned int* err;
 };
@@ -143,12 +148,12 @@ DEVI void load_operand(const Args& a, int row, int nc, Vec16<T> (&r)[OC * sizeof
 
 template <typename T, typename TO, int EPI, int OC>
 DEVI void epilogue_chunk(const Args& a, float (&v)[OC], const Vec16<T> (&r)[OC * sizeof(T) / 16], int row,
-                         int nc, uint32_t (&o)[32], uint32_t (&o2)[32], float& pmax, float& psum) {
+                         int nc, uint32_t (&o)[32], uint32_t (&o2)[32]) {
     constexpr int VEC = 16 / (int)sizeof(T);
     // the bias has the output's element type
     constexpr int BV = 16 / (int)sizeof(TO);
     const TO* bias = (const TO*)a.bias;
-    if constexpr (EPI == EPI_STORE || EPI == EPI_GELU || EPI == EPI_RESID || EPI == EPI_GELU_PART) {
+    if constexpr (EPI == EPI_STORE || EPI == EPI_GELU || EPI == EPI_RESID) {
         if (bias) {
 #pragma unroll
             for (int k = 0; k < OC / BV; k++) {
@@ -182,21 +187,6 @@ DEVI void epilogue_chunk(const Args& a, float (&v)[OC], const Vec16<T> (&r)[OC *
                 else if constexpr (EPI == EPI_GELU_BWD) x *= gelu_grad(rv);
                 else x = rv + x;
             }
-    }
-    if constexpr (EPI == EPI_GELU_PART) {
-        float cm = pmax;
-#pragma unroll
-        for (int e = 0; e < OC; e++) {
-            v[e] = gelu_fwd(v[e]);
-            cm = fmaxf(cm, v[e]);
-        }
-        if (row < a.M) {
-            float sum = 0.f;
-#pragma unroll
-            for (int e = 0; e < OC; e++) sum += nc + e < a.N ? expf(v[e] - cm) : 0.f;
-            psum = psum * expf(pmax - cm) + sum;
-            pmax = cm;
-        }
     }
     if constexpr (sizeof(TO) == 4) {
 #pragma unroll
@@ -236,10 +226,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr int UK = KIND == 1 ? 8 : 16;     // K elements per MMA
     constexpr int KSTEPS = KE / UK;            // MMAs per stage (4)
     constexpr int BNC = BN / CG;               // rows of B this CTA holds
-    // epilogue output: fp32 for kind::tf32, split-K partials and the fused
+    // epilogue output: fp32 for kind::tf32 and split-K partials
     // operator's GELU tiles, else the operands' 16-bit type;
     // a 128-byte chunk holds OC output columns
-    constexpr bool OUT_F32 = KIND == 1 || EPI == EPI_SPLITK || EPI == EPI_GELU_PART;
+    constexpr bool OUT_F32 = KIND == 1 || EPI == EPI_SPLITK;
     using TO = typename std::conditional<OUT_F32, float, T>::type;
     constexpr int OC = OUT_F32 ? 32 : 64;
     constexpr int NCH = BN / OC;
@@ -263,7 +253,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars_ptr + 8 * NBARS + 4);
     int* n_issued_smem = reinterpret_cast<int*>(bars_ptr + 8 * NBARS + 8);
     volatile int* epi_abort = reinterpret_cast<volatile int*>(bars_ptr + 8 * NBARS + 12);
-    float2* row_part = reinterpret_cast<float2*>(bars_ptr + 256);  // [BM] softmax partials
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const int rank = CG == 2 ? (int)(cluster_rank() & 1u) : 0;  // 0: pair leader (issues MMAs)
@@ -394,8 +383,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ---------------- epilogue warps 2..9: a warp owns its TMEM lane
         // quarter's 32 rows and the column chunks j = hh, hh + 2, ... of each
         // tile; it stages a chunk in its own buffer and stores it itself.
-        // Every epilogue thread runs every tile (EPI_GELU_PART's named barrier
-        // stays matched); after an expired wait the work is skipped.
+        // After an expired wait the work is skipped.
         const int q = warp & 3;          // TMEM lane quarter this warp may access
         const int hh = (warp - 2) >> 2;  // chunk parity
         const int rl = q * 32 + lane;    // row within the tile
@@ -424,7 +412,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 *epi_abort = 1;
             }
             if (!aborted) tc_fence_after();
-            float pmax = -INFINITY, psum = 0.f;
 #pragma unroll 1
             for (int j = hh; j < NCH && !aborted; j += 2) {
                 const int nc = n0 + j * OC;
@@ -435,7 +422,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 Vec16<T> rn[NV];  // the next chunk's operand, in flight during this one
                 if (j + 2 < NCH) load_operand<T, EPI, OC>(args, row, nc + 2 * OC, rn);
                 uint32_t o[32], o2[32];
-                epilogue_chunk<T, TO, EPI, OC>(args, v, r, row, nc, o, o2, pmax, psum);
+                epilogue_chunk<T, TO, EPI, OC>(args, v, r, row, nc, o, o2);
 #pragma unroll
                 for (int k = 0; k < NV; k++) r[k] = rn[k];
                 // this warp's previous stores have read the staging buffer(s)
@@ -458,21 +445,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (lane == 0 && !aborted) {
                 if constexpr (CG == 1) mbar_arrive(tempty(acc));
                 else mbar_arrive_cluster(tempty_leader + 8u * (uint32_t)acc);
-            }
-            if constexpr (EPI == EPI_GELU_PART) {
-                // merge the two chunk parities of the row, then one partial per (row, tile)
-                if (hh == 1) row_part[rl] = make_float2(pmax, psum);
-                epi_bar();
-                if (hh == 0 && row < args.M && !aborted) {
-                    const float2 o = row_part[rl];
-                    const float m = fmaxf(pmax, o.x);
-                    float sum = 0.f;
-                    if (pmax != -INFINITY) sum += psum * expf(pmax - m);
-                    if (o.x != -INFINITY) sum += o.y * expf(o.x - m);
-                    reinterpret_cast<float2*>(args.part)[(size_t)row * args.part_ld + nb] =
-                        make_float2(m, sum);
-                }
-                epi_bar();  // row_part is free for the next tile
             }
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
@@ -687,19 +659,15 @@ static int dispatch_epi(int epi, const Maps& mp, const tc::Args& a, cudaStream_t
             case EPI_GELU_BWD: return launch_tc<BN, KIND, EPI_GELU_BWD, CG>(mp, a, s);
             case EPI_ACCUM: return launch_tc<BN, KIND, EPI_ACCUM, CG>(mp, a, s);
             case EPI_SPLITK: return launch_tc<BN, KIND, EPI_SPLITK, CG>(mp, a, s);
-            case EPI_GELU_PART: return launch_tc<BN, KIND, EPI_GELU_PART, CG>(mp, a, s);
             default: return GPT2_ERR_CONFIG;
         }
     } else {
         switch (epi) {
             case EPI_STORE: return launch_tc<BN, KIND, EPI_STORE, CG>(mp, a, s);
-            case EPI_GELU_PART: return launch_tc<BN, KIND, EPI_GELU_PART, CG>(mp, a, s);
             default: return GPT2_ERR_CONFIG;
         }
     }
 }
-
-int gemm_tc_part_tile_n() { return 256; }
 
 static bool al16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -711,10 +679,10 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
     // tf32 operands only in K-major form
     if (dt == DT_F32 && (!p.a_kmajor || !p.b_kmajor)) return GPT2_ERR_CONFIG;
     // the fused operator's GELU tiles (and bias) are fp32 whatever the operands
-    const DType out_dt = p.epi == EPI_GELU_PART ? DT_F32 : dt;
+    const DType out_dt = dt;
     const int osz = (int)dtype_size(out_dt);
     if (!al16(p.A) || !al16(p.B) || !al16(p.D) || (p.lda * esz) % 16 || (p.ldb * esz) % 16 ||
-        (p.ldd * osz) % 16 || p.N % (16 / osz) || (dt != DT_F32 && p.N % vec && p.epi != EPI_GELU_PART))
+        (p.ldd * osz) % 16 || p.N % (16 / osz) || (dt != DT_F32 && p.N % vec))
         return GPT2_ERR_ALIGN;
     const bool has_aux = p.epi == EPI_RESID || p.epi == EPI_GELU_BWD;
     if (has_aux && (!p.aux || !al16(p.aux) || (p.ldaux * esz) % 16)) return GPT2_ERR_ALIGN;
@@ -746,7 +714,7 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
         };
         if (cost(192) < 0.92 * cost(256)) BN = 192;
     }
-    if (p.epi != EPI_GELU_PART) {
+    {
         // GPT2_GEMM_BN=128|192|256 overrides the choice (tuning; 192 with K-major B only)
         static const int force_bn = [] {
             const char* e = getenv("GPT2_GEMM_BN");
@@ -754,8 +722,6 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
         }();
         if (force_bn == 128 || force_bn == 256 || (force_bn == 192 && p.b_kmajor && p.epi != EPI_ACCUM))
             BN = force_bn;
-    } else {
-        BN = 256;
     }
     tc::Args a;
     a.M = p.M; a.N = p.N; a.K = p.K;
@@ -766,7 +732,7 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
     a.a_mn = p.a_kmajor ? 0 : 1;
     a.b_mn = p.b_kmajor ? 0 : 1;
     a.D = p.D; a.ldd = p.ldd; a.bias = p.bias; a.aux = p.aux; a.ldaux = p.ldaux; a.D2 = p.D2;
-    a.part = p.part; a.part_ld = p.part_ld; a.err = err;
+    a.err = err;
     a.splits = 1;
     a.kb_per = a.num_kb;
     // Split-K for "+=" products with fewer tiles than CTA slots (the weight

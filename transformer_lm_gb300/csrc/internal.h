@@ -24,9 +24,7 @@ inline int dtype_vec(DType dt) { return dt == DT_F32 ? 4 : 8; }
 //  EPI_RESID     D = acc + bias[n] + aux[m][n]           (residual add)
 //  EPI_GELU_BWD  D = acc * gelu'(aux[m][n])                (GELU backward)
 //  EPI_ACCUM     D = D + acc                               (parameter-gradient +=)
-//  EPI_GELU_PART D = gelu(acc + bias[n]); part[m][tile] = (max, sum exp(D - max)) over the tile
 enum Epi { EPI_STORE = 0, EPI_GELU = 1, EPI_RESID = 2, EPI_GELU_BWD = 3, EPI_ACCUM = 4,
-           EPI_GELU_PART = 5,
            EPI_SPLITK = 6 };  // internal to gemm_tc: fp32 partial sums of one K range
 
 // D[M,N] = A[M,K] . B[N,K]^T with operands given by their storage order:
@@ -40,7 +38,6 @@ struct GemmParams {
     const void* bias;
     const void* aux; long long ldaux;
     void* D2;
-    float* part; int part_ld;  // EPI_GELU_PART: float2 partials, part_ld tiles per row
     float* ws; size_t ws_floats;  // optional fp32 scratch: lets EPI_ACCUM split K (0 = never)
     int M, N, K;
     int epi;
@@ -58,8 +55,6 @@ int gemm_simt(const GemmParams& p, DType dt, cudaStream_t s);
 // DT_F32 -> kind::tf32. err: device error word (bounded waits).
 // Returns 0, or a negative GPT2_ERR_* code for unsupported shapes/alignment.
 int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err);
-// tile width (columns) the tensor-core GEMM uses for EPI_GELU_PART
-int gemm_tc_part_tile_n();
 
 // ---- memory-bound kernels (kernels.cu) ----
 void launch_copy_tokens(const int* src, int* dst, int n, int V, unsigned int* err, cudaStream_t s);
@@ -161,9 +156,6 @@ void launch_init_normal(DType dt, void* p, size_t n, float stddev, unsigned long
 void launch_fill(DType dt, void* p, size_t n, float value, cudaStream_t s);
 void launch_to_f32(DType dt, float* dst, const void* src, size_t n, cudaStream_t s);
 void launch_from_f32(DType dt, void* dst, const float* src, size_t n, cudaStream_t s);
-// fp32 (rows, K) -> bf16 (rows, 3*Kp): [hi | hi | lo] (mode 0) or [hi | lo | hi] (mode 1)
-void launch_split_bf16x3(void* dst, const float* src, int rows, int K, int Kp, int mode,
-                         cudaStream_t s);
 // out = softmax over each row of a (M,N) fp32 tile-partial GELU output (fused operator pass 2)
 void launch_softmax_finish(float* y, const float* part, int M, int N, int tiles, cudaStream_t s);
 

@@ -1769,45 +1769,6 @@ void launch_set_hyper(float* h, float lr, float b1, float b2, float c1, float c2
     launch_pdl(set_hyper_k, 1, 1, 0, s, h, lr, b1, b2, c1, c2, eps, wd, seed);
 }
 
-// ------------------------------------------------------------------ split-precision operands
-// Row r of an fp32 (rows, K) matrix becomes three bf16 segments of Kp >= K
-// columns (zeros past K): hi = bf16(x), lo = bf16(x - hi); mode 0 writes
-// [hi | hi | lo], mode 1 [hi | lo | hi]. A GEMM over the 3*Kp-long rows of a
-// mode-0 left operand and a mode-1 right operand sums hi.hi + hi.lo + lo.hi,
-// which leaves out only lo.lo and the rounding of lo (about 2^-16 of each
-// product).
-__global__ void split_bf16x3_k(bf16* __restrict__ dst, const float* __restrict__ src, int rows,
-                               int K, int Kp, int mode) {
-    pdl_enter();
-    const int g8 = Kp / 8;
-    const long long total = (long long)rows * g8;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        const int r = (int)(i / g8), k0 = (int)(i % g8) * 8;
-        Vec16<bf16> hi, lo;
-#pragma unroll
-        for (int e = 0; e < 8; e++) {
-            const float x = k0 + e < K ? src[(size_t)r * K + k0 + e] : 0.f;
-            hi.v[e] = __float2bfloat16_rn(x);
-            lo.v[e] = __float2bfloat16_rn(x - __bfloat162float(hi.v[e]));
-        }
-        bf16* d = dst + (size_t)r * 3 * Kp + k0;
-        st16(d, hi);
-        st16(d + Kp, mode ? lo : hi);
-        st16(d + 2 * Kp, mode ? hi : lo);
-    }
-}
-
-void launch_split_bf16x3(void* dst, const float* src, int rows, int K, int Kp, int mode,
-                         cudaStream_t s) {
-    note_launch(1);
-    const long long total = (long long)rows * (Kp / 8);
-    long long blocks = (total + 255) / 256;
-    const long long cap = (long long)num_sms() * 8;
-    if (blocks > cap) blocks = cap;
-    launch_pdl(split_bf16x3_k, dim3((unsigned)blocks), dim3(256), 0, s, (bf16*)dst, src, rows, K, Kp, mode);
-}
-
 // ------------------------------------------------------------------ utilities
 __global__ void zero_k(int4* __restrict__ p, size_t n16, char* __restrict__ tail, size_t ntail) {
     pdl_enter();

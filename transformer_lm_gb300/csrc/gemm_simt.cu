@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(256) gemm_simt_k(const GemmParams p) {
 
 int gemm_simt(const GemmParams& p, DType dt, cudaStream_t s) {
     if (p.M <= 0 || p.N <= 0 || p.K <= 0) return GPT2_ERR_ARG;
+    if (p.cs) return GPT2_ERR_CONFIG;  // column sums come with the tensor-core epilogue only
     dim3 grid((p.N + 63) / 64, (p.M + 63) / 64);
     if (grid.y > 65535) return GPT2_ERR_CONFIG;
     note_launch(1);

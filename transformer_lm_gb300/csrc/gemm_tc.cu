@@ -82,6 +82,8 @@ struct Args {
     const void* aux;
     long long ldaux;
     void* D2;
+    float* cs;  // EPI_GELU_BWD, optional: column sums of the output per 32-row group
+    long long ldcs;
     int splits, kb_per;  // split-K: K ranges per tile and k-blocks per range
     unsigned int* err;
 };
@@ -438,6 +440,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if constexpr (EPI == EPI_GELU) tma_store_2d(&tmD2, stg_s + STG_BYTES, nc, m0 + q * 32);
                     bulk_commit();
                 }
+                if constexpr (EPI == EPI_GELU_BWD && sizeof(TO) == 2) {
+                    if (args.cs) {
+                        // column sums of the staged (rounded) chunk over the warp's
+                        // rows, read back from the staging buffer (which the store
+                        // only reads too): lane l adds the column pair 2l, 2l + 1
+                        const int rows = min(32, args.M - (m0 + q * 32));
+                        const int wofs = ((lane >> 2) << 4) | ((lane & 3) << 2);
+                        float2 cs2 = make_float2(0.f, 0.f);
+#pragma unroll 8
+                        for (int rr = 0; rr < rows; rr++) {
+                            const uint32_t u = *reinterpret_cast<const uint32_t*>(
+                                stg + rr * ROWB + (wofs ^ ((rr & 7) << 4)));
+                            cs2 = fadd2(cs2, h2_f2<TO>(u));
+                        }
+                        if (rows > 0 && nc + 2 * lane < args.N)
+                            *reinterpret_cast<float2*>(args.cs + (size_t)((m0 + q * 32) / 32) * args.ldcs + nc +
+                                                       2 * lane) = cs2;
+                    }
+                }
             }
             // this warp's accumulator rows are read: release them to the leader's MMA
             if (!aborted) tc_fence_before();
@@ -688,6 +709,10 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
     if (has_aux && (!p.aux || !al16(p.aux) || (p.ldaux * esz) % 16)) return GPT2_ERR_ALIGN;
     if (p.bias && !al16(p.bias)) return GPT2_ERR_ALIGN;
     if (p.epi == EPI_GELU && (!p.D2 || !al16(p.D2))) return GPT2_ERR_ALIGN;
+    // column sums: the GELU-backward epilogue of 16-bit outputs only
+    if (p.cs && (p.epi != EPI_GELU_BWD || dt == DT_F32 || ((uintptr_t)p.cs & 7u) || (p.ldcs & 1) ||
+                 p.ldcs < p.N))
+        return GPT2_ERR_CONFIG;
 
     const int sms = num_sms();
     const long long nm = (p.M + tc::BM - 1) / tc::BM;
@@ -732,6 +757,7 @@ int gemm_tc(const GemmParams& p, DType dt, cudaStream_t s, unsigned int* err) {
     a.a_mn = p.a_kmajor ? 0 : 1;
     a.b_mn = p.b_kmajor ? 0 : 1;
     a.D = p.D; a.ldd = p.ldd; a.bias = p.bias; a.aux = p.aux; a.ldaux = p.ldaux; a.D2 = p.D2;
+    a.cs = p.cs; a.ldcs = p.ldcs;
     a.err = err;
     a.splits = 1;
     a.kb_per = a.num_kb;

@@ -107,6 +107,11 @@ struct Model {
     float* gpart = nullptr;
     PartialDesc* d_desc = nullptr;
     int ndesc = 0, P_ln = 0, R_cs = 0;
+    // partial rows of the fc bias grad: 32-row groups written by the
+    // GELU-backward GEMM's epilogue where it can (R_fcb = ceil(B T / 32)),
+    // else R_cs slabs of launch_colsum_part (as for the qkv bias grad)
+    int R_fcb = 0;
+    bool cs_gemm = false;
     bool ln_fused = false;
     size_t ln_area = 0, cs_off = 0, fcb_off = 0, qkvb_off = 0;
     // gpt2_train_step: the captured step and what it was captured for
@@ -160,13 +165,14 @@ void tend(Model* m, int i) {
 // ------------------------------------------------------------------ GEMM dispatch
 int gemm(Model* m, int epi, const void* A, long long lda, int a_km, const void* B, long long ldb,
          int b_km, void* D, long long ldd, const void* bias, const void* aux, long long ldaux,
-         void* D2, int M, int N, int K) {
+         void* D2, int M, int N, int K, float* cs = nullptr, long long ldcs = 0) {
     GemmParams p;
     memset(&p, 0, sizeof(p));
     p.A = A; p.lda = lda; p.a_kmajor = a_km;
     p.B = B; p.ldb = ldb; p.b_kmajor = b_km;
     p.D = D; p.ldd = ldd; p.bias = bias; p.aux = aux; p.ldaux = ldaux; p.D2 = D2;
     p.M = M; p.N = N; p.K = K; p.epi = epi;
+    p.cs = cs; p.ldcs = ldcs;
     // each stream has its own split-K scratch, so concurrent products never share one
     if (m->in_side) {
         if (m->gemm_ws) {
@@ -227,7 +233,7 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 float* ln_part(const Model* m, int i) { return m->gpart + (size_t)i * m->ln_area; }
 float* cs_part(const Model* m, int i) { return m->gpart + m->cs_off + (size_t)i * m->R_cs * m->C; }
-float* fcb_part(const Model* m, int l) { return m->gpart + m->fcb_off + (size_t)l * m->R_cs * 4 * m->C; }
+float* fcb_part(const Model* m, int l) { return m->gpart + m->fcb_off + (size_t)l * m->R_fcb * 4 * m->C; }
 float* qkvb_part(const Model* m, int l) { return m->gpart + m->qkvb_off + (size_t)l * m->R_cs * 3 * m->C; }
 
 // partial-row areas and the device table of their reductions (fixed for a B x T)
@@ -238,10 +244,18 @@ int alloc_partials(Model* m) {
     m->ln_fused = layernorm_backward_fuses_colsum(m->dt, C);
     m->P_ln = layernorm_backward_part_rows(m->dt, BT, C);
     m->R_cs = colsum_part_rows(BT);
+    // GPT2_FUSE_COLSUM=0 computes fc's bias grad partials with a separate
+    // column-sum pass instead of in the GELU-backward epilogue (tuning)
+    static const bool fuse = [] {
+        const char* e = getenv("GPT2_FUSE_COLSUM");
+        return e ? atoi(e) != 0 : true;
+    }();
+    m->cs_gemm = fuse && m->tc != 0 && m->dt != DT_F32;
+    m->R_fcb = m->cs_gemm ? (BT + 31) / 32 : m->R_cs;
     m->ln_area = (size_t)m->P_ln * 3 * C;
     m->cs_off = (size_t)(2 * L + 1) * m->ln_area;
     m->fcb_off = m->cs_off + (m->ln_fused ? 0 : (size_t)(2 * L + 1) * m->R_cs * C);
-    m->qkvb_off = m->fcb_off + (size_t)L * m->R_cs * 4 * C;
+    m->qkvb_off = m->fcb_off + (size_t)L * m->R_fcb * 4 * C;
     const size_t total = m->qkvb_off + (size_t)L * m->R_cs * 3 * C;
     CUDA_TRY(cudaMalloc((void**)&m->gpart, total * 4 + 256));
     std::vector<PartialDesc> d;
@@ -264,7 +278,7 @@ int alloc_partials(Model* m) {
         add(ln_part(m, 2 * l), lstride, m->P_ln, C, G(m, 2) + (size_t)l * C * es);
         add(ln_part(m, 2 * l) + C, lstride, m->P_ln, C, G(m, 3) + (size_t)l * C * es);
         if (l > 0) add_cs(2 * l, G(m, 13) + (size_t)(l - 1) * C * es);
-        add(fcb_part(m, l), 4LL * C, m->R_cs, 4 * C, G(m, 11) + (size_t)l * 4 * C * es);
+        add(fcb_part(m, l), 4LL * C, m->R_fcb, 4 * C, G(m, 11) + (size_t)l * 4 * C * es);
         add(qkvb_part(m, l), 3LL * C, m->R_cs, 3 * C, G(m, 5) + (size_t)l * 3 * C * es);
     }
     m->ndesc = (int)d.size();
@@ -540,16 +554,19 @@ int run_backward(Model* m) {
         TRY(mark_side(fcproj_w));
         // dX with the GELU backward fused into its epilogue (overwrites dbt4c)
         TRY(wait_side(qkv_done));
+        // (with the column sums of its output, fc's bias grad, where the epilogue can)
         TRY(gemm(m, EPI_GELU_BWD, m->dresidual, C, 1, P(m, 12) + (size_t)l * 4 * C * C * es, 4 * C, 0,
-                 m->dbt4c, 4 * C, nullptr, fch, 4 * C, nullptr, (int)BT, 4 * C, C));
+                 m->dbt4c, 4 * C, nullptr, fch, 4 * C, nullptr, (int)BT, 4 * C, C,
+                 m->cs_gemm ? fcb_part(m, l) : nullptr, 4LL * C));
         // (fcproj's bias grad: the column sums of the LayerNorm backward above)
         // fc (W: 4C x C): dW and the bias column sums read dbt4c, on the side
         TRY(edge(s, side));
         TRY(on_side([&] {
             TRY(gemm(m, EPI_ACCUM, m->dbt4c, 4 * C, 0, ln2, C, 0, G(m, 10) + (size_t)l * 4 * C * C * es,
                      C, nullptr, nullptr, 0, nullptr, 4 * C, C, (int)BT));
-            TIMED(FAM_OTHER, 4.0 * BT * C * es,
-                  launch_colsum_part(dt, fcb_part(m, l), m->dbt4c, (int)BT, 4 * C, m->stream));
+            if (!m->cs_gemm)
+                TIMED(FAM_OTHER, 4.0 * BT * C * es,
+                      launch_colsum_part(dt, fcb_part(m, l), m->dbt4c, (int)BT, 4 * C, m->stream));
             return GPT2_OK;
         }));
         TRY(mark_side(fc_w));

@@ -39,6 +39,9 @@ struct GemmParams {
     const void* aux; long long ldaux;
     void* D2;
     float* ws; size_t ws_floats;  // optional fp32 scratch: lets EPI_ACCUM split K (0 = never)
+    // optional (EPI_GELU_BWD on the tensor cores only): the column sums of the
+    // rounded output over each 32-row group, cs[(row / 32) * ldcs + col]
+    float* cs; long long ldcs;
     int M, N, K;
     int epi;
 };

@@ -460,57 +460,68 @@ __global__ void layernorm_forward_k(T* __restrict__ out, float* __restrict__ mea
 // and widens them anew in each pass, so the kernel fits in 40 registers and 48
 // one-row warps are resident per SM; the statistics and the affine map use
 // packed fp32 arithmetic.
-template <typename H, int NV>
-__global__ void __launch_bounds__(256, 6) layernorm_forward_bf16_k(H* __restrict__ out, float* __restrict__ mean,
+template <typename H, int NV, int RW>
+__global__ void __launch_bounds__(256, RW == 1 ? 6 : 4) layernorm_forward_bf16_k(H* __restrict__ out, float* __restrict__ mean,
                                                                    float* __restrict__ rstd,
                                                                    const H* __restrict__ inp,
                                                                    const H* __restrict__ w,
                                                                    const H* __restrict__ b, int N) {
     constexpr int C = 256 * NV;
     pdl_enter();
-    const int row = blockIdx.x * 8 + threadIdx.x / 32;
+    // RW rows per warp, rows row0, row0 + 8, ... of the block's 8 RW rows: all
+    // of the warp's loads are issued before the first row's arithmetic
+    const int row0 = blockIdx.x * 8 * RW + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
-    if (row >= N) return;
-    const uint4* x = reinterpret_cast<const uint4*>(inp + (size_t)row * C) + lane;
-    uint4 xv[NV];
+    if (row0 >= N) return;
+    uint4 xv[RW][NV];
 #pragma unroll
-    for (int j = 0; j < NV; j++) xv[j] = x[32 * j];
-    float2 s2 = make_float2(0.f, 0.f);
+    for (int q = 0; q < RW; q++) {
+        const int row = row0 + 8 * q;
+        const uint4* x = reinterpret_cast<const uint4*>(inp + (size_t)row * C) + lane;
 #pragma unroll
-    for (int j = 0; j < NV; j++) {
-        s2 = fadd2(s2, fadd2(h2_f2_v<H>(xv[j].x), h2_f2_v<H>(xv[j].y)));
-        s2 = fadd2(s2, fadd2(h2_f2_v<H>(xv[j].z), h2_f2_v<H>(xv[j].w)));
+        for (int j = 0; j < NV; j++) xv[q][j] = row < N ? x[32 * j] : make_uint4(0u, 0u, 0u, 0u);
     }
-    const float m = warp_sum(s2.x + s2.y) / C;
-    const float2 nm = make_float2(-m, -m);
-    float2 v2 = make_float2(0.f, 0.f);
-    auto sq = [&](uint32_t u) {
-        const float2 d = fadd2(h2_f2_v<H>(u), nm);
-        v2 = ffma2(d, d, v2);
-    };
-#pragma unroll
-    for (int j = 0; j < NV; j++) {
-        sq(xv[j].x); sq(xv[j].y); sq(xv[j].z); sq(xv[j].w);
-    }
-    const float var = warp_sum(v2.x + v2.y) / C;
-    const float r = rsqrtf(var + 1e-5f);
-    // y = (x r - m r) w + b
-    const float2 r2 = make_float2(r, r), nmr = make_float2(-m * r, -m * r);
-    uint4* y = reinterpret_cast<uint4*>(out + (size_t)row * C) + lane;
     const uint4* wp = reinterpret_cast<const uint4*>(w) + lane;
     const uint4* bp = reinterpret_cast<const uint4*>(b) + lane;
-    auto aff = [&](uint32_t xu, uint32_t wu, uint32_t bu) {
-        return f2_h2v<H>(ffma2(ffma2(h2_f2_v<H>(xu), r2, nmr), h2_f2_v<H>(wu), h2_f2_v<H>(bu)));
-    };
 #pragma unroll
-    for (int j = 0; j < NV; j++) {
-        const uint4 wu = __ldg(wp + 32 * j), bu = __ldg(bp + 32 * j);
-        y[32 * j] = make_uint4(aff(xv[j].x, wu.x, bu.x), aff(xv[j].y, wu.y, bu.y), aff(xv[j].z, wu.z, bu.z),
-                               aff(xv[j].w, wu.w, bu.w));
-    }
-    if (lane == 0) {
-        mean[row] = m;
-        rstd[row] = r;
+    for (int q = 0; q < RW; q++) {
+        const int row = row0 + 8 * q;
+        float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < NV; j++) {
+            s2 = fadd2(s2, fadd2(h2_f2_v<H>(xv[q][j].x), h2_f2_v<H>(xv[q][j].y)));
+            s2 = fadd2(s2, fadd2(h2_f2_v<H>(xv[q][j].z), h2_f2_v<H>(xv[q][j].w)));
+        }
+        const float m = warp_sum(s2.x + s2.y) / C;
+        const float2 nm = make_float2(-m, -m);
+        float2 v2 = make_float2(0.f, 0.f);
+        auto sq = [&](uint32_t u) {
+            const float2 d = fadd2(h2_f2_v<H>(u), nm);
+            v2 = ffma2(d, d, v2);
+        };
+#pragma unroll
+        for (int j = 0; j < NV; j++) {
+            sq(xv[q][j].x); sq(xv[q][j].y); sq(xv[q][j].z); sq(xv[q][j].w);
+        }
+        const float var = warp_sum(v2.x + v2.y) / C;
+        const float r = rsqrtf(var + 1e-5f);
+        if (row >= N) break;
+        // y = (x r - m r) w + b
+        const float2 r2 = make_float2(r, r), nmr = make_float2(-m * r, -m * r);
+        uint4* y = reinterpret_cast<uint4*>(out + (size_t)row * C) + lane;
+        auto aff = [&](uint32_t xu, uint32_t wu, uint32_t bu) {
+            return f2_h2v<H>(ffma2(ffma2(h2_f2_v<H>(xu), r2, nmr), h2_f2_v<H>(wu), h2_f2_v<H>(bu)));
+        };
+#pragma unroll
+        for (int j = 0; j < NV; j++) {
+            const uint4 wu = __ldg(wp + 32 * j), bu = __ldg(bp + 32 * j);
+            y[32 * j] = make_uint4(aff(xv[q][j].x, wu.x, bu.x), aff(xv[q][j].y, wu.y, bu.y),
+                                   aff(xv[q][j].z, wu.z, bu.z), aff(xv[q][j].w, wu.w, bu.w));
+        }
+        if (lane == 0) {
+            mean[row] = m;
+            rstd[row] = r;
+        }
     }
 }
 
@@ -528,9 +539,23 @@ void launch_layernorm_forward(DType dt, void* out, float* mean, float* rstd, con
     unsigned g = (unsigned)((N + rows - 1) / rows);
     if (dt != DT_F32 && C % 256 == 0 && C <= 768) {
         const int nv = C / 256;
-#define LNF2(H, NVV)                                                                                 \
-    launch_pdl(layernorm_forward_bf16_k<H, NVV>, g, block, 0, s, (H*)out, mean, rstd, (const H*)inp, \
-               (const H*)w, (const H*)b, N)
+        // two rows per warp while the rows still fill a wave of resident warps
+        // at two per warp, else one
+        static const int rw_env = [] {
+            const char* e = getenv("GPT2_LN_ROWS");
+            return e ? atoi(e) : 0;
+        }();
+        const int rw = rw_env == 1 || rw_env == 2 ? rw_env : 2;
+        const unsigned g2 = (unsigned)((N + rows * rw - 1) / (rows * rw));
+#define LNF2(H, NVV)                                                                                       \
+    do {                                                                                                   \
+        if (rw == 2)                                                                                       \
+            launch_pdl(layernorm_forward_bf16_k<H, NVV, 2>, g2, block, 0, s, (H*)out, mean, rstd,           \
+                       (const H*)inp, (const H*)w, (const H*)b, N);                                        \
+        else                                                                                               \
+            launch_pdl(layernorm_forward_bf16_k<H, NVV, 1>, g2, block, 0, s, (H*)out, mean, rstd,           \
+                       (const H*)inp, (const H*)w, (const H*)b, N);                                        \
+    } while (0)
         if (dt == DT_BF16) {
             if (nv == 1) LNF2(bf16, 1); else if (nv == 2) LNF2(bf16, 2); else LNF2(bf16, 3);
         } else {

@@ -581,16 +581,31 @@ __global__ void __launch_bounds__(256) splitk_reduce_k(H* __restrict__ D, long l
             acc[0] = x0.x; acc[1] = x0.y; acc[2] = x0.z; acc[3] = x0.w;
             acc[4] = x1.x; acc[5] = x1.y; acc[6] = x1.z; acc[7] = x1.w;
         }
-        for (int sp = 1; sp < S; sp++) {
+        H* d = D + (size_t)m * ldd + c;
+        Vec16<H> o;
+        if (accumulate) o = ld16(d);  // in flight with the partials
+        // four ranges' loads in flight at a time, added in range order
+        int sp = 1;
+        for (; sp + 3 < S; sp += 4) {
+            float4 x[4][2];
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                x[j][0] = __ldcs(reinterpret_cast<const float4*>(w + (sp + j) * slice));
+                x[j][1] = __ldcs(reinterpret_cast<const float4*>(w + (sp + j) * slice + 4));
+            }
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                acc[0] += x[j][0].x; acc[1] += x[j][0].y; acc[2] += x[j][0].z; acc[3] += x[j][0].w;
+                acc[4] += x[j][1].x; acc[5] += x[j][1].y; acc[6] += x[j][1].z; acc[7] += x[j][1].w;
+            }
+        }
+        for (; sp < S; sp++) {
             const float4 x0 = __ldcs(reinterpret_cast<const float4*>(w + sp * slice));
             const float4 x1 = __ldcs(reinterpret_cast<const float4*>(w + sp * slice + 4));
             acc[0] += x0.x; acc[1] += x0.y; acc[2] += x0.z; acc[3] += x0.w;
             acc[4] += x1.x; acc[5] += x1.y; acc[6] += x1.z; acc[7] += x1.w;
         }
-        H* d = D + (size_t)m * ldd + c;
-        Vec16<H> o;
         if (accumulate) {
-            o = ld16(d);
 #pragma unroll
             for (int e = 0; e < 8; e++) o.v[e] = from_f<H>(to_f(o.v[e]) + acc[e]);
         } else {

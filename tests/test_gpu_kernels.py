@@ -263,7 +263,7 @@ def test_fused_op_small_shapes_match_oracle():
 
 @pytest.mark.parametrize("N,C,dt", [(1000, 768, "bf16"), (37, 64, "f32"), (8192, 768, "bf16"),
                                     (300, 1024, "bf16"), (129, 1024, "f32"), (515, 640, "bf16"),
-                                    (700, 512, "bf16"), (9, 256, "bf16")])
+                                    (700, 512, "bf16"), (9, 256, "bf16"), (4096, 1024, "bf16")])
 def test_layernorm_forward_backward_match_oracle(N, C, dt):
     import torch
     bf16 = dt == "bf16"

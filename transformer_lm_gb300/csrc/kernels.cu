@@ -455,13 +455,13 @@ __global__ void layernorm_forward_k(T* __restrict__ out, float* __restrict__ mea
     }
 }
 
-// 16-bit rows (bf16 or fp16, H) with C = 256 NV (NV <= 3): lane l keeps the
+// 16-bit rows (bf16 or fp16, H) with C = 256 NV (NV <= 4): lane l keeps the
 // row's 16-byte vectors l, l + 32, ... as packed 16-bit words (4 NV registers)
 // and widens them anew in each pass, so the kernel fits in 40 registers and 48
 // one-row warps are resident per SM; the statistics and the affine map use
 // packed fp32 arithmetic.
 template <typename H, int NV, int RW>
-__global__ void __launch_bounds__(256, RW == 1 ? 6 : 4) layernorm_forward_bf16_k(H* __restrict__ out, float* __restrict__ mean,
+__global__ void __launch_bounds__(256, RW == 1 ? (NV <= 3 ? 6 : 4) : (NV <= 3 ? 4 : 3)) layernorm_forward_bf16_k(H* __restrict__ out, float* __restrict__ mean,
                                                                    float* __restrict__ rstd,
                                                                    const H* __restrict__ inp,
                                                                    const H* __restrict__ w,
@@ -537,7 +537,7 @@ void launch_layernorm_forward(DType dt, void* out, float* mean, float* rstd, con
     const int mv = maxv_for(C / VEC);
     const int block = 256, rows = block / 32;
     unsigned g = (unsigned)((N + rows - 1) / rows);
-    if (dt != DT_F32 && C % 256 == 0 && C <= 768) {
+    if (dt != DT_F32 && C % 256 == 0 && C <= 1024) {
         const int nv = C / 256;
         // two rows per warp while the rows still fill a wave of resident warps
         // at two per warp, else one
@@ -557,9 +557,11 @@ void launch_layernorm_forward(DType dt, void* out, float* mean, float* rstd, con
                        (const H*)inp, (const H*)w, (const H*)b, N);                                        \
     } while (0)
         if (dt == DT_BF16) {
-            if (nv == 1) LNF2(bf16, 1); else if (nv == 2) LNF2(bf16, 2); else LNF2(bf16, 3);
+            if (nv == 1) LNF2(bf16, 1); else if (nv == 2) LNF2(bf16, 2); else if (nv == 3) LNF2(bf16, 3);
+            else LNF2(bf16, 4);
         } else {
-            if (nv == 1) LNF2(f16, 1); else if (nv == 2) LNF2(f16, 2); else LNF2(f16, 3);
+            if (nv == 1) LNF2(f16, 1); else if (nv == 2) LNF2(f16, 2); else if (nv == 3) LNF2(f16, 3);
+            else LNF2(f16, 4);
         }
 #undef LNF2
         return;
@@ -1107,7 +1109,8 @@ void launch_layernorm_backward(DType dt, void* dinp, void* dw, void* db, const v
 
 // ------------------------------------------------------------------ partial-row form
 bool layernorm_backward_fuses_colsum(DType dt, int C) {
-    return dt != DT_F32 && (C / 8 + 31) / 32 <= 3 && (C * 2) % 16 == 0;
+    // the bulk-copy kernel up to 768 columns, the warp-per-row kernel also at 1024
+    return dt != DT_F32 && (C * 2) % 16 == 0 && ((C / 8 + 31) / 32 <= 3 || C == 1024);
 }
 
 int layernorm_backward_part_rows(DType dt, int N, int C) {
@@ -1171,9 +1174,11 @@ int launch_layernorm_backward_part(DType dt, void* dinp, float* part, const void
                    N, C, accumulate, with_colsum);                                                     \
     } while (0)
         if (dt == DT_BF16) {
-            if (nv == 1) LNW(bf16, 1); else if (nv == 2) LNW(bf16, 2); else LNW(bf16, 3);
+            if (nv == 1) LNW(bf16, 1); else if (nv == 2) LNW(bf16, 2); else if (nv == 3) LNW(bf16, 3);
+            else LNW(bf16, 4);
         } else {
-            if (nv == 1) LNW(f16, 1); else if (nv == 2) LNW(f16, 2); else LNW(f16, 3);
+            if (nv == 1) LNW(f16, 1); else if (nv == 2) LNW(f16, 2); else if (nv == 3) LNW(f16, 3);
+            else LNW(f16, 4);
         }
 #undef LNW
         return P;

@@ -274,8 +274,9 @@ long long gpt2_launch_count(void);
  * aligned with K % 4 == 0 and N % 4 == 0 (else GPT2_ERR_ALIGN); M, K, N >= 1
  * (else GPT2_ERR_ARG). Asynchronous on `stream` (a cudaStream_t, NULL = legacy
  * default stream). The first call on a device allocates its scratch (the
- * per-row softmax partials, 8 * M * ceil(N/256) bytes; grown as needed and
- * kept until exit). The output is undefined when gpt2_device_status() then
+ * per-row softmax partials, 8 bytes per row and column tile: tiles of 256
+ * columns, or of 224 where those fill the GPU's CTA pairs better; grown as
+ * needed and kept until exit). The output is undefined when gpt2_device_status() then
  * reports GPT2_ERR_DEVICE_TIMEOUT. */
 int fused_linear_bias_gelu_softmax(const float* x, const float* W, const float* b, float* out,
                                    int M, int K, int N, void* stream);

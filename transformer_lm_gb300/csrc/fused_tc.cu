@@ -9,8 +9,11 @@
 // hi.hi + hi.lo + lo.hi on the bf16 tensor cores with fp32 accumulation: only
 // lo.lo and the rounding of lo are left out (about 2^-16 of each product).
 //
-// A CTA pair computes 256 x 256 output tiles (cta_group::2 MMAs; each CTA
-// holds 128 rows of x and 128 rows of W per stage), persistent over the tiles:
+// A CTA pair computes 256 x BN output tiles (cta_group::2 MMAs; each CTA
+// holds 128 rows of x and BN/2 rows of W per stage), persistent over the
+// tiles; BN is 256, or 224 where 224-wide tiles fill the last round of CTA
+// pairs markedly better (1024 x 8192 outputs: 148 tiles on 76 pairs instead
+// of 128):
 //   warp 0      TMA: per 64-wide k-block, this CTA's 128 x 64 fp32 tile of x
 //               and of W (two 32-column boxes each, 128-byte swizzle) into a
 //               stage of the shared-memory ring, completing on a local barrier;
@@ -46,7 +49,6 @@ namespace fsp {
 using namespace tc;
 
 constexpr int BM = 128;                  // rows of x per CTA
-constexpr int BN = 256;                  // output columns per tile (128 rows of W per CTA)
 constexpr int KB = 64;                   // k-block (fp32 elements per stage)
 constexpr int OPB = BM * KB * 4;         // bytes of one operand's fp32 stage tile (32 KB)
 constexpr int HALF = OPB / 2;            // one 32-column box; later the hi (or lo) tile
@@ -61,7 +63,7 @@ constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * STG;
 constexpr int BAR_BYTES = 256 + 1024;    // barriers and flags, then per-row softmax partials
 constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
-constexpr int TMEM_COLS = 512;           // two 256-column accumulators
+constexpr int TMEM_COLS = 512;           // two accumulators of up to 256 columns
 constexpr int GROUP_M = 8;               // m-block pairs per rasterisation group
 
 struct Args {
@@ -91,9 +93,14 @@ DEVI void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
     lo = f2_h2<bf16>(a - h.x, b - h.y);
 }
 
+// BN: output columns per tile (BN / 2 rows of W per CTA)
+template <int BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fused_split_gemm_k(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                        const __grid_constant__ CUtensorMap tmY, const __grid_constant__ Args a) {
+    static_assert(BN % 32 == 0 && BN <= 256 && BN >= 128, "tile width");
+    constexpr int BNC = BN / 2;                       // rows of W per CTA
+    constexpr int STAGE_TX = OPB + BNC * KB * 4;      // bytes landing per stage
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -154,12 +161,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int st = cid; ok && st < num_tiles; st += ncl) {
                 int mp, nb;
                 tile_coords(st, a.num_mp, a.num_n, mp, nb);
-                const int m0 = (mp * 2 + (int)rank) * BM, n0 = nb * BN + (int)rank * BM;
+                const int m0 = (mp * 2 + (int)rank) * BM, n0 = nb * BN + (int)rank * BNC;
                 for (int kb = 0; kb < a.num_kb; kb++) {
                     if (!mbar_wait(empty(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
                     const uint32_t sx = base + stage * STAGE, sw = sx + OPB;
                     const int k0 = kb * KB;
-                    mbar_expect_tx(full(stage), STAGE);
+                    mbar_expect_tx(full(stage), STAGE_TX);
                     tma_load_2d(sx, &tmX, full(stage), k0, m0);
                     tma_load_2d(sx + HALF, &tmX, full(stage), k0 + 32, m0);
                     tma_load_2d(sw, &tmW, full(stage), k0, n0);
@@ -232,9 +239,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int kb = 0; kb < a.num_kb; kb++) {
                 if (!mbar_wait_warp(full(stage), phase, abort_flag)) { ok = false; break; }
                 uint8_t* sp = base_ptr + stage * STAGE;
-                // 256 rows (x then W) / (8 warps x 16 rows) = 2 passes
+                // 128 + BNC rows (x then W) in groups of 16: 2 passes of 8 warps
 #pragma unroll 1
                 for (int pass = 0; pass < 2; pass++) {
+                    if ((pass * CONV_WARPS + cw) * 16 >= BM + BNC) continue;  // (warp-uniform)
                     const int row = (pass * CONV_WARPS + cw) * 16 + rsub;  // 0..255
                     uint8_t* op = sp + (row >> 7) * OPB;
                     const int r = row & 127;
@@ -405,15 +413,22 @@ static bool make_map_f32(CUtensorMap* m, const void* p, uint64_t cols, uint64_t 
 
 }  // namespace fsp
 
-int fused_split_tile_n() { return fsp::BN; }
+// 224-wide tiles where they take fewer column-tile rounds of the CTA pairs
+// than 256-wide ones (rounds x width) and their M x ceil(N/224) partials fit
+// within max_partials, else 256
+int fused_split_tile_n(int M, int N, long long max_partials) {
+    const long long pairs = num_sms() / 2, mp = ((long long)M + 255) / 256;
+    auto cost = [&](int bn) {
+        const long long tiles = mp * (((long long)N + bn - 1) / bn);
+        return ((tiles + pairs - 1) / pairs) * bn;
+    };
+    const long long parts224 = (long long)M * (((long long)N + 223) / 224);
+    return cost(224) < cost(256) && parts224 <= max_partials ? 224 : 256;
+}
 
-int launch_fused_split_gemm(const float* x, const float* W, const float* b, float* y, float* part,
-                            int part_ld, int M, int K, int N, cudaStream_t s, unsigned int* err) {
-    using namespace fsp;
-    CUtensorMap tx, tw, ty;
-    if (!make_map_f32(&tx, x, K, M, K, BM) || !make_map_f32(&tw, W, K, N, K, BM) ||
-        !make_map_f32(&ty, y, N, M, N, 32))
-        return set_error(GPT2_ERR_CUDA, "fused op: tensor map encoding failed");
+namespace fsp {
+template <int BN>
+static int launch_bn(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty, Args a, cudaStream_t s) {
     static bool attr = false;
     static int max_clusters = 0;
     cudaLaunchConfig_t cfg = {};
@@ -428,37 +443,51 @@ int launch_fused_split_gemm(const float* x, const float* W, const float* b, floa
     cfg.attrs = at;
     cfg.numAttrs = 1;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(fused_split_gemm_k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(fused_split_gemm_k<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              SMEM_BYTES);
         if (e != cudaSuccess)
             return set_error(GPT2_ERR_CUDA, "fused op: shared-memory opt-in failed: %s", cudaGetErrorString(e));
         int n = 0;
         cfg.gridDim = dim3(2 * 64);
-        e = cudaOccupancyMaxActiveClusters(&n, (void*)fused_split_gemm_k, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, (void*)fused_split_gemm_k<BN>, &cfg);
         if (e != cudaSuccess || n < 1)
             return set_error(GPT2_ERR_CUDA, "fused op: no co-resident CTA pair (%s)", cudaGetErrorString(e));
         max_clusters = n;
         attr = true;
     }
-    Args a;
-    a.M = M;
-    a.N = N;
-    a.K = K;
-    a.num_mp = (M + 2 * BM - 1) / (2 * BM);
-    a.num_n = (N + BN - 1) / BN;
-    a.num_kb = (K + KB - 1) / KB;
-    a.bias = b;
-    a.part = reinterpret_cast<float2*>(part);
-    a.part_ld = part_ld;
-    a.err = err;
+    a.num_n = (a.N + BN - 1) / BN;
     const long long tiles = (long long)a.num_mp * a.num_n;
     const long long ncl = tiles < max_clusters ? tiles : max_clusters;
     cfg.gridDim = dim3((unsigned)(2 * ncl));
     cfg.numAttrs += launch_attrs(at + cfg.numAttrs);
     note_launch(1);
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_split_gemm_k, tx, tw, ty, a);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_split_gemm_k<BN>, tx, tw, ty, a);
     if (e != cudaSuccess) return set_error(GPT2_ERR_CUDA, "fused op: launch failed: %s", cudaGetErrorString(e));
     return GPT2_OK;
+}
+}  // namespace fsp
+
+int launch_fused_split_gemm(const float* x, const float* W, const float* b, float* y, float* part,
+                            int part_ld, int M, int K, int N, int tile_n, cudaStream_t s, unsigned int* err) {
+    using namespace fsp;
+    if (tile_n != 256 && tile_n != 224) return set_error(GPT2_ERR_CONFIG, "fused op: tile width %d", tile_n);
+    if (part_ld < (N + tile_n - 1) / tile_n) return set_error(GPT2_ERR_CONFIG, "fused op: partial rows too short");
+    CUtensorMap tx, tw, ty;
+    if (!make_map_f32(&tx, x, K, M, K, BM) || !make_map_f32(&tw, W, K, N, K, (uint32_t)(tile_n / 2)) ||
+        !make_map_f32(&ty, y, N, M, N, 32))
+        return set_error(GPT2_ERR_CUDA, "fused op: tensor map encoding failed");
+    Args a;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.num_mp = (M + 2 * BM - 1) / (2 * BM);
+    a.num_n = 0;
+    a.num_kb = (K + KB - 1) / KB;
+    a.bias = b;
+    a.part = reinterpret_cast<float2*>(part);
+    a.part_ld = part_ld;
+    a.err = err;
+    return tile_n == 224 ? launch_bn<224>(tx, tw, ty, a, s) : launch_bn<256>(tx, tw, ty, a, s);
 }
 
 // the bounded-wait limit of this translation unit's kernels (0: the default)

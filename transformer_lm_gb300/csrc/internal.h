@@ -166,10 +166,13 @@ void launch_softmax_finish(float* y, const float* part, int M, int N, int tiles,
 // y = gelu(x W^T + b) (fp32 x (M,K), W (N,K), b (N), y (M,N), all 16-byte
 // aligned, K % 4 == 0 == N % 4) with the bf16 hi/lo split of x and W done in
 // the kernel; part[row * part_ld + t] = (max, sum exp(y - max)) over the row's
-// 256-column tile t (float2). err: device error word of the bounded waits.
+// column tile t of tile_n (256 or 224) columns (float2; part_ld >= the tile
+// count). err: device error word of the bounded waits.
 int launch_fused_split_gemm(const float* x, const float* W, const float* b, float* y, float* part,
-                            int part_ld, int M, int K, int N, cudaStream_t s, unsigned int* err);
-int fused_split_tile_n();
+                            int part_ld, int M, int K, int N, int tile_n, cudaStream_t s, unsigned int* err);
+// the tile width the fused product takes for an (M, N) output: 224 where it
+// needs fewer rounds of the CTA pairs and M * ceil(N / 224) <= max_partials, else 256
+int fused_split_tile_n(int M, int N, long long max_partials);
 
 // ---- attention (attention.cu) ----
 // qkv (B,T,3C) -> out (B,T,C), lse (B,NH,T) fp32 natural-log sum of exp of the scaled scores

@@ -22,6 +22,11 @@
 
 using namespace gk;
 
+// partials the fused operator's 224-column tiles may need at most: the
+// allocation-free entry point's static array (131072 float2), so that both
+// entry points choose the same tiles for every shape either accepts
+#define FUSED_NARROW_MAX_PARTIALS (1LL << 17)
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -73,7 +78,9 @@ int fused_linear_bias_gelu_softmax(const float* x, const float* W, const float* 
     if (current_device(&dev) != GPT2_OK) return GPT2_ERR_CUDA;
     unsigned int* err = err_word(dev);
     if (!err) return GPT2_ERR_NOMEM;
-    const int tile_n = fused_split_tile_n();
+    // the same tile choice as the allocation-free entry point (whose static
+    // partials bound the narrower tiles), so the two give identical results
+    const int tile_n = fused_split_tile_n(M, N, FUSED_NARROW_MAX_PARTIALS);
     const int tiles = (int)(((long long)N + tile_n - 1) / tile_n);
     // scratch: the row-tile softmax partials
     const size_t need = ((size_t)M * tiles * 2 * sizeof(float) + 255) / 256 * 256;
@@ -91,7 +98,7 @@ int fused_linear_bias_gelu_softmax(const float* x, const float* W, const float* 
     }
     float* part = (float*)scratch;
     cudaStream_t s = (cudaStream_t)stream;
-    const int rc = launch_fused_split_gemm(x, W, b, out, part, tiles, M, K, N, s, err);
+    const int rc = launch_fused_split_gemm(x, W, b, out, part, tiles, M, K, N, tile_n, s, err);
     if (rc != GPT2_OK) return rc;
     launch_softmax_finish(out, part, M, N, tiles, s);
     return launch_status();
@@ -225,8 +232,10 @@ int gpt2_device_status(void) {
 // softmax partials live in the file-scope device array below, reserved when
 // the library is loaded and held by every device that loads it until exit.
 //
-// Limits and sharing: at most NOALLOC_MAX_PARTIALS (row, 256-column tile)
-// pairs, i.e. M * ceil(N / 256) <= 131072 (1 MiB of float2). Every call uses
+// Limits and sharing: at most NOALLOC_MAX_PARTIALS (row, column tile) pairs:
+// calls with M * ceil(N / 256) <= 131072 are accepted (1 MiB of float2), and
+// the product takes its narrower 224-column tiles only where their partials
+// fit the array as well. Every call uses
 // the same array and leaves the previous call's partials in it; nothing needs
 // clearing because the GEMM epilogue writes every partial a call reads.
 // Calls whose GPU work overlaps (different streams, no ordering between them)
@@ -239,6 +248,7 @@ int gpt2_device_status(void) {
 }  // extern "C"
 
 #define NOALLOC_MAX_PARTIALS (1 << 17)
+static_assert(FUSED_NARROW_MAX_PARTIALS <= NOALLOC_MAX_PARTIALS, "224-column tiles fit the static partials");
 
 static __device__ __align__(256) float2 g_noalloc_part[NOALLOC_MAX_PARTIALS];
 // bounded-wait timeout bits of the allocation-free variant (starts at zero)
@@ -298,20 +308,22 @@ extern "C" int fused_linear_bias_gelu_softmax_noalloc(const float* x, const floa
     if (!al16(x) || !al16(W) || !al16(b) || !al16(out) || K % 4 || N % 4)
         return gk::set_error(GPT2_ERR_ALIGN,
                              "fused op (no-alloc): pointers must be 16-byte aligned, K and N multiples of 4");
-    const int tile_n = fused_split_tile_n();
-    const long long tiles = ((long long)N + tile_n - 1) / tile_n;
-    if ((long long)M * tiles > NOALLOC_MAX_PARTIALS)
+    const long long tiles256 = ((long long)N + 255) / 256;
+    if ((long long)M * tiles256 > NOALLOC_MAX_PARTIALS)
         return gk::set_error(GPT2_ERR_ARG,
                              "fused op (no-alloc): M * ceil(N/256) = %lld exceeds the static scratch "
                              "limit of %d",
-                             (long long)M * tiles, NOALLOC_MAX_PARTIALS);
+                             (long long)M * tiles256, NOALLOC_MAX_PARTIALS);
+    // 224-column tiles only where their partials fit the array too
+    const int tile_n = fused_split_tile_n(M, N, FUSED_NARROW_MAX_PARTIALS);
+    const long long tiles = ((long long)N + tile_n - 1) / tile_n;
     int dev;
     if (current_device(&dev) != GPT2_OK) return gk::set_error(GPT2_ERR_CUDA, "no current device");
     NoAllocDevice d;
     if (noalloc_setup(dev, &d) != GPT2_OK)
         return gk::set_error(GPT2_ERR_CUDA, "fused op (no-alloc): cudaGetSymbolAddress failed");
     cudaStream_t s = (cudaStream_t)stream;
-    const int rc = launch_fused_split_gemm(x, W, b, out, d.part, (int)tiles, M, K, N, s, d.err);
+    const int rc = launch_fused_split_gemm(x, W, b, out, d.part, (int)tiles, M, K, N, tile_n, s, d.err);
     if (rc != GPT2_OK) return rc;
     launch_softmax_finish(out, d.part, M, N, (int)tiles, s);
     if (cudaGetLastError() != cudaSuccess)

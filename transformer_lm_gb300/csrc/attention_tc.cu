@@ -22,7 +22,8 @@
 //   warps 2..9   two softmax warpgroups, one per query tile (one TMEM lane =
 //                one query row = one thread): S row from TMEM, row max,
 //                P = exp2(s - m) written back to TMEM as bf16 pairs, and the
-//                item's epilogue O / l and LSE. A row's reference max m moves
+//                item's epilogue O / l (staged per warp in shared memory and
+//                written by TMA stores) and LSE. A row's reference max m moves
 //                only when a block's max exceeds it by more than 8 (so p <=
 //                256); the warp then rescales its O rows in TMEM after the
 //                previous P.V has completed.
@@ -56,8 +57,11 @@ constexpr int TILE_BYTES = 128 * 128;  // 128 rows x 128 bytes (64 bf16)
 constexpr int NUM_THREADS = 64 + NQT * 128;
 constexpr int OFF_Q = 0;                                   // [buf][tile]
 constexpr int OFF_KV = OFF_Q + Q_BUFS * NQT * TILE_BYTES;  // [stage]: K, then V
-constexpr int OFF_BAR = OFF_KV + KV_STAGES * 2 * TILE_BYTES;
+constexpr int STG_BYTES = 32 * 128;  // a softmax warp's output staging: 32 rows x 64 16-bit values
+constexpr int OFF_STG = OFF_KV + KV_STAGES * 2 * TILE_BYTES;
+constexpr int OFF_BAR = OFF_STG + NQT * 4 * STG_BYTES;
 constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 constexpr int TMEM_COLS = 512;
 constexpr int TM_TILE = 256;  // columns per query tile
 constexpr int TM_O = 128;
@@ -102,7 +106,8 @@ DEVI int item_of(int r, int c, int G, int nitems) {
 // KIND 0: bf16 operands and output, 2: fp16 (the tcgen05 kind::f16 operand type)
 template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    flash_fwd_tc_k(const __grid_constant__ CUtensorMap tm, const __grid_constant__ FwdArgs a) {
+    flash_fwd_tc_k(const __grid_constant__ CUtensorMap tm, const __grid_constant__ CUtensorMap tmo,
+                   const __grid_constant__ FwdArgs a) {
     using H = typename std::conditional<KIND == 2, f16, bf16>::type;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -293,6 +298,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t tS = tmem_base + (uint32_t)(t * TM_TILE) + lane_off;
         const uint32_t tO = tS + TM_O;
         const uint32_t tP = tS + TM_P;
+        uint8_t* stg = base_ptr + OFF_STG + (warp - 2) * STG_BYTES;
+        const uint32_t stg_s = base + OFF_STG + (uint32_t)((warp - 2) * STG_BYTES);
         const float sl = a.scale_log2;
         int g = 0, nout = 0;
         bool ok = true;
@@ -387,20 +394,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // O_t is read: the next item's first P.V may overwrite it (it is
             // issued after this warpgroup's next pfull arrival)
             tc_fence_before();
-            if (query < a.T) {
-                const int b = it.bh / a.NH, h = it.bh % a.NH;
-                const float inv = 1.f / l;
-                H* dst = (H*)a.out + ((size_t)b * a.T + query) * C + (size_t)h * HSZ;
+            const int b = it.bh / a.NH, h = it.bh % a.NH;
+            const float inv = 1.f / l;
+            uint32_t pk[HSZ / 2];
 #pragma unroll
-                for (int d = 0; d < HSZ; d += 8) {
-                    *reinterpret_cast<uint4*>(dst + d) =
-                        make_uint4(f2_h2<H>(ov[d] * inv, ov[d + 1] * inv), f2_h2<H>(ov[d + 2] * inv, ov[d + 3] * inv),
-                                   f2_h2<H>(ov[d + 4] * inv, ov[d + 5] * inv),
-                                   f2_h2<H>(ov[d + 6] * inv, ov[d + 7] * inv));
-                }
-                a.lse[(size_t)it.bh * a.T + query] = (m + log2f(l)) * LN2_F;
+            for (int d = 0; d < HSZ / 2; d++) pk[d] = f2_h2<H>(ov[2 * d] * inv, ov[2 * d + 1] * inv);
+            // the warp's 32 output rows through its staging buffer (128-byte
+            // swizzle) and one TMA store, once its previous store has read it;
+            // rows past the sequence end are clipped by the store
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 8; k++)
+                *reinterpret_cast<uint4*>(stg + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+                    make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0 && it.q0 + t * BQ + qq * 32 < a.T) {  // (no store wholly past the end)
+                tma_store_3d(&tmo, stg_s, h * HSZ, it.q0 + t * BQ + qq * 32, b);
+                bulk_commit();
             }
+            if (query < a.T) a.lse[(size_t)it.bh * a.T + query] = (m + log2f(l)) * LN2_F;
         }
+        if (lane == 0) bulk_wait_all();  // the output stores are complete before the CTA exits
     }
 
     __syncthreads();
@@ -461,6 +477,16 @@ int launch_flash_forward_tc(DType dt, void* out, float* lse, const void* qkv, in
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return set_error(GPT2_ERR_CUDA, "flash forward: tensor map encoding failed");
+    // out (B, T, C) as a 3-D tensor (C, T, B); 64 x 32 x 1 boxes (one softmax warp's rows)
+    if ((uintptr_t)out % 16) return set_error(GPT2_ERR_ALIGN, "flash forward: out must be 16-byte aligned");
+    CUtensorMap tmo;
+    cuuint64_t odims[3] = {(cuuint64_t)C, (cuuint64_t)T, (cuuint64_t)B};
+    cuuint64_t ostrides[2] = {(cuuint64_t)C * 2, (cuuint64_t)T * C * 2};
+    cuuint32_t obox[3] = {HSZ, 32, 1};
+    if (fn(&tmo, dt == DT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, odims,
+           ostrides, obox, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return set_error(GPT2_ERR_CUDA, "flash forward: output tensor map encoding failed");
     auto kern = dt == DT_F16 ? flash_fwd_tc_k<2> : flash_fwd_tc_k<0>;
     static bool attr[2] = {false, false};
     if (!attr[dt == DT_F16]) {
@@ -484,7 +510,7 @@ int launch_flash_forward_tc(DType dt, void* out, float* lse, const void* qkv, in
     if (a.nitems == 0) return GPT2_OK;
     dim3 grid(std::min(a.nitems, num_sms()));
     note_launch(1);
-    launch_pdl(kern, grid, dim3(NUM_THREADS), SMEM_BYTES, s, tm, a);
+    launch_pdl(kern, grid, dim3(NUM_THREADS), SMEM_BYTES, s, tm, tmo, a);
     return GPT2_OK;
 }
 

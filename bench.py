@@ -451,7 +451,7 @@ def fused_workload(reps, warmup, peaks):
     peak_tf32 = peaks["bf16_tflops"] * 1.1 / 2.25
     achieved = FUSED_FLOPS / (ms / 1000.0) / 1e12
     traffic = profile_value("fused_op_1024x8192x8192.md", "traffic_bytes_per_call",
-                            ["ops.cu", "gemm_tc.cu", "kernels.cu"])
+                            ["ops.cu", "fused_tc.cu", "kernels.cu"])
     return {
         "workload": (f"fused Linear+bias+GELU(tanh)+row softmax, fp32, x [{M},{K}], W [{N},{K}], "
                      f"b [{N}] (synthetic: x~N(0,1), W~N(0,1/sqrt(K)), b~U(-0.1,0.1))"),

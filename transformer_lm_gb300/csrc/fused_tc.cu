@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // the accumulator rows are read: release them to the leader's MMA
             if (!aborted) tc_fence_before();
             __syncwarp();
-            if (lane == 0 && !aborted) mbar_arrive_cluster(tempty_leader + 8u * (uint32_t)acc);
+            if (lane == 0 && !aborted) mbar_arrive_cluster_relaxed(tempty_leader + 8u * (uint32_t)acc);
             // merge the two chunk parities of each row: one partial per (row, tile)
             if (hh == 1) row_part[rl] = make_float2(pmax, psum);
             epi_bar();

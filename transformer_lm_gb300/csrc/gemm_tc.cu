@@ -465,7 +465,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             __syncwarp();
             if (lane == 0 && !aborted) {
                 if constexpr (CG == 1) mbar_arrive(tempty(acc));
-                else mbar_arrive_cluster(tempty_leader + 8u * (uint32_t)acc);
+                else mbar_arrive_cluster_relaxed(tempty_leader + 8u * (uint32_t)acc);
             }
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }

@@ -148,22 +148,33 @@ DEVI void load_operand(const Args& a, int row, int nc, Vec16<T> (&r)[OC * sizeof
     }
 }
 
+// A chunk's bias (the output's element type, OC columns = 128 bytes) spread
+// over the warp: lane l holds its 4-byte word l (columns 2l, 2l + 1 of a
+// 16-bit output, column l of fp32); 0 past N or without a bias. Read a chunk
+// ahead of its use: every lane needs every column, so the word is broadcast by
+// shuffles at use instead of each thread re-reading the 128 bytes.
+template <typename TO> DEVI uint32_t load_bias_word(const Args& a, int nc, int lane) {
+    constexpr int PER = 4 / (int)sizeof(TO);
+    const int c = nc + lane * PER;
+    if (!a.bias || c >= a.N) return 0u;
+    return __ldg(reinterpret_cast<const unsigned int*>(reinterpret_cast<const TO*>(a.bias) + c));
+}
+
 template <typename T, typename TO, int EPI, int OC>
 DEVI void epilogue_chunk(const Args& a, float (&v)[OC], const Vec16<T> (&r)[OC * sizeof(T) / 16], int row,
-                         int nc, uint32_t (&o)[32], uint32_t (&o2)[32]) {
+                         int nc, uint32_t bw, uint32_t (&o)[32], uint32_t (&o2)[32]) {
     constexpr int VEC = 16 / (int)sizeof(T);
-    // the bias has the output's element type
-    constexpr int BV = 16 / (int)sizeof(TO);
-    const TO* bias = (const TO*)a.bias;
     if constexpr (EPI == EPI_STORE || EPI == EPI_GELU || EPI == EPI_RESID) {
-        if (bias) {
+        if (a.bias) {
 #pragma unroll
-            for (int k = 0; k < OC / BV; k++) {
-                if (nc + k * BV < a.N) {
-                    Vec16<TO> bb;
-                    *reinterpret_cast<int4*>(&bb) = __ldg(reinterpret_cast<const int4*>(bias + nc + k * BV));
-#pragma unroll
-                    for (int e = 0; e < BV; e++) v[k * BV + e] += to_f(bb.v[e]);
+            for (int e2 = 0; e2 < 32; e2++) {
+                const uint32_t w = __shfl_sync(0xffffffffu, bw, e2);
+                if constexpr (sizeof(TO) == 2) {
+                    const float2 f = h2_f2<TO>(w);
+                    v[2 * e2] += f.x;
+                    v[2 * e2 + 1] += f.y;
+                } else {
+                    v[e2] += __uint_as_float(w);
                 }
             }
         }
@@ -406,6 +417,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             constexpr int NV = OC * (int)sizeof(T) / 16;
             Vec16<T> r[NV];
             load_operand<T, EPI, OC>(args, row, n0 + hh * OC, r);
+            uint32_t bw = load_bias_word<TO>(args, n0 + hh * OC, lane);
             int ok = 1;
             if (lane == 0 && !aborted) ok = mbar_wait(tfull(acc), acc_phase, abort_flag) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -423,8 +435,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 else tmem_ld32(taddr, v);
                 Vec16<T> rn[NV];  // the next chunk's operand, in flight during this one
                 if (j + 2 < NCH) load_operand<T, EPI, OC>(args, row, nc + 2 * OC, rn);
+                const uint32_t bwn = j + 2 < NCH ? load_bias_word<TO>(args, nc + 2 * OC, lane) : 0u;
                 uint32_t o[32], o2[32];
-                epilogue_chunk<T, TO, EPI, OC>(args, v, r, row, nc, o, o2);
+                epilogue_chunk<T, TO, EPI, OC>(args, v, r, row, nc, bw, o, o2);
+                bw = bwn;
 #pragma unroll
                 for (int k = 0; k < NV; k++) r[k] = rn[k];
                 // this warp's previous stores have read the staging buffer(s)

@@ -3,7 +3,7 @@
 //
 // y = gelu_tanh(x W^T + b) for fp32 x (M, K) and W (N, K) (POPCORNBENCH
 // "fused Linear + GELU + Softmax": nn.Linear, then GELU), with, per row and
-// 256-column tile, the softmax partials (max, sum exp(y - max)); a second pass
+// column tile, the softmax partials (max, sum exp(y - max)); a second pass
 // (softmax_finish_k) normalises the rows. Each fp32 value v is written as
 // hi + lo with hi = bf16(v) and lo = bf16(v - hi), and x W^T is taken as
 // hi.hi + hi.lo + lo.hi on the bf16 tensor cores with fp32 accumulation: only

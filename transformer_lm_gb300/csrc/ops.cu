@@ -6,8 +6,8 @@
 //    bf16 halves (hi, lo) in shared memory as their fp32 tiles arrive and runs
 //    x W^T as hi.hi + hi.lo + lo.hi on the bf16 tensor cores (about 2^-16
 //    relative per product, fp32 accumulation); its epilogue adds the bias,
-//    applies GELU, stores the row tile and records, per row and 256-column
-//    tile, (max, sum exp(v - max)). The last pass merges the tile partials of
+//    applies GELU, stores the row tile and records, per row and column tile
+//    (256 or 224 columns), (max, sum exp(v - max)). The last pass merges the tile partials of
 //    each row and rewrites the row as exp(v - max) / sum. The allocation-free
 //    variant runs the same two kernels with its partials in a static array.
 //  * gpt2_gemm / gpt2_attention_forward / gpt2_attention_backward: the

@@ -250,7 +250,8 @@ def test_attention_forward_many_items_per_cta(B, T, C, NH):
 
 def test_fused_op_small_shapes_match_oracle():
     import torch
-    for (M, K, N) in [(130, 72, 264), (256, 512, 1000), (1, 4, 4)]:
+    # (1024 x 9728 takes the 256-column tiles, the others the 224-column ones)
+    for (M, K, N) in [(130, 72, 264), (256, 512, 1000), (1, 4, 4), (1024, 64, 9728)]:
         x, W, b = inputs.fused_op_inputs(M, K, N, seed=3)
         ref = oracle.fused_linear_bias_gelu_softmax(x, W, b)
         out = torch.zeros((M, N), dtype=torch.float32, device="cuda")

@@ -306,3 +306,58 @@ def test_layernorm_forward_backward_match_oracle(N, C, dt):
             assert err <= 2.0 ** -8 * np.max(np.abs(want)) + 2e-2 * np.max(np.abs(want - 1.0))
         else:
             assert rel_to_max(got - 1.0, want - 1.0) < 1e-5
+
+
+def test_stand_alone_entry_points_reject_bad_arguments_with_a_message():
+    """Degenerate and misaligned calls are refused on the host, before any
+    launch, with the code the header documents and a description of this call
+    in gpt2_last_error; a valid call afterwards still runs."""
+    import torch
+    f32 = lambda *s: torch.zeros(*s, device="cuda")  # noqa: E731
+    x, W, b, out = f32(8, 8), f32(8, 8), f32(8), f32(8, 8)
+
+    def refused(code, text, fn, *args, **kw):
+        with pytest.raises(G.GPT2Error) as e:
+            fn(*args, **kw)
+        assert e.value.code == code, e.value
+        assert text in G.gpt2_last_error(), G.gpt2_last_error()
+        assert G.lib().gpt2_last_status() == code
+
+    for fused in (G.fused_linear_bias_gelu_softmax, G.fused_linear_bias_gelu_softmax_noalloc):
+        name = fused.__name__
+        refused(-8, name if fused is G.fused_linear_bias_gelu_softmax else "M, K, N", fused,
+                x, W, b, out, 0, 8, 8)  # empty input
+        refused(-8, "NULL", fused, None, W, b, out, 8, 8, 8)
+        refused(-5, "align", fused, x, W, b, out, 8, 6, 8)  # K not a multiple of 4
+        refused(-5, "align", fused, x[:, 1:], W, b, out, 8, 4, 4)  # x not 16-byte aligned
+    A, B, D = (torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda") for _ in range(3))
+    refused(-8, "gpt2_gemm", G.gpt2_gemm, G.GPT2_BF16, 1, "store", A, 64, 1, B, 64, 1, D, 64,
+            M=0, N=64, K=64)
+    refused(-8, "gpt2_gemm", G.gpt2_gemm, G.GPT2_BF16, 1, "store", A, 64, 1, B, 64, 1, D, 64,
+            M=64, N=64, K=0)
+    refused(-5, "gpt2_gemm", G.gpt2_gemm, G.GPT2_BF16, 1, "store", A, 64, 1, B, 64, 1, D, 64,
+            M=64, N=60, K=64)  # N not a multiple of 8 bf16 values
+    refused(-1, "gpt2_gemm", G.gpt2_gemm, 7, 1, "store", A, 64, 1, B, 64, 1, D, 64,
+            M=64, N=64, K=64)  # unknown dtype
+    refused(-8, "gpt2_gemm", G.gpt2_gemm, G.GPT2_BF16, 1, "resid", A, 64, 1, B, 64, 1, D, 64,
+            M=64, N=64, K=64)  # residual epilogue without its operand
+    qkv = torch.zeros(2 * 16 * 3 * 96, dtype=torch.bfloat16, device="cuda")
+    o = torch.zeros(2 * 16 * 96, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(2 * 16 * 2, device="cuda")
+    refused(-8, "gpt2_attention_forward", G.gpt2_attention_forward, G.GPT2_BF16, 1, qkv, o, lse,
+            2, 16, 96, 5)  # C not a multiple of NH
+    refused(-1, "gpt2_attention_forward", G.gpt2_attention_forward, G.GPT2_BF16, 1, qkv, o, lse,
+            2, 16, 96, 2)  # head size 48
+    refused(-8, "gpt2_attention_forward", G.gpt2_attention_forward, G.GPT2_BF16, 1, qkv, o, lse,
+            0, 16, 96, 3)  # empty batch
+    ln_out, mean, rstd = f32(4, 16), f32(4), f32(4)
+    refused(-8, "gpt2_layernorm_forward", G.gpt2_layernorm_forward, G.GPT2_FP32, ln_out, mean, rstd,
+            ln_out, f32(16), f32(16), 4, 12)  # C not a multiple of 8
+    refused(-8, "gpt2_layernorm_forward", G.gpt2_layernorm_forward, G.GPT2_FP32, ln_out, mean, rstd,
+            ln_out, f32(16), f32(16), 0, 16)  # no rows
+    # the library is still usable: a valid product runs and is exact on integers
+    A.copy_(torch.eye(64, dtype=torch.bfloat16, device="cuda") * 2)
+    B.copy_(torch.arange(64 * 64, device="cuda").reshape(64, 64).remainder(7).to(torch.bfloat16))
+    G.gpt2_gemm(G.GPT2_BF16, 1, "store", A, 64, 1, B, 64, 1, D, 64, M=64, N=64, K=64)
+    G.gpt2_device_status()
+    assert torch.equal(D.float(), 2 * B.float().T)

@@ -23,9 +23,11 @@ namespace {
 
 char g_err[512] = "no error";
 int g_status = GPT2_OK;
+unsigned long long g_err_serial = 0;  // counts the errors recorded so far
 
 int fail(int code, const char* fmt, ...) {
     g_status = code;
+    g_err_serial++;
     va_list ap;
     va_start(ap, fmt);
     vsnprintf(g_err, sizeof(g_err), fmt, ap);
@@ -687,12 +689,15 @@ int run_adamw(Model* m, float lr, float beta1, float beta2, float eps, float wei
 
 int gk::set_error(int code, const char* fmt, ...) {
     g_status = code;
+    g_err_serial++;
     va_list ap;
     va_start(ap, fmt);
     vsnprintf(g_err, sizeof(g_err), fmt, ap);
     va_end(ap);
     return code;
 }
+
+unsigned long long gk::error_serial() { return g_err_serial; }
 
 // =================================================================== C ABI
 extern "C" {

@@ -241,6 +241,8 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 }
 // records the library's last error (text and GPT2_ERR_* code); returns code
 int set_error(int code, const char* fmt, ...);
+// number of errors recorded so far (tells whether a callee described its failure)
+unsigned long long error_serial();
 // host-side count of kernel launches made by this library (for benchmark reporting)
 void note_launch(int n);
 long long launch_count();

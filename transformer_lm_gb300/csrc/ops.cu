@@ -63,6 +63,33 @@ bool al16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 bool known_dtype(int dtype) { return dtype == GPT2_FP32 || dtype == GPT2_BF16 || dtype == GPT2_FP16; }
 DType to_dt(int dtype) { return dtype == GPT2_BF16 ? DT_BF16 : dtype == GPT2_FP16 ? DT_F16 : DT_F32; }
 
+const char* code_text(int rc) {
+    switch (rc) {
+        case GPT2_ERR_CONFIG: return "unsupported dtype, epilogue, head size or tile configuration";
+        case GPT2_ERR_ALIGN: return "a pointer, leading dimension or size is not aligned as required";
+        case GPT2_ERR_CUDA: return "a CUDA call failed";
+        case GPT2_ERR_NOMEM: return "a device allocation failed";
+        case GPT2_ERR_ARG: return "NULL pointer or size out of range";
+        case GPT2_ERR_DEVICE_TIMEOUT:
+            return "a bounded in-kernel wait expired; the results of the calls since the last check are invalid";
+        default: return "failed";
+    }
+}
+
+// Every entry point below returns through one of these, so that each failed
+// call leaves a description in gpt2_last_error: a callee's own message
+// stands; an error no callee described gets its code's text, prefixed with
+// the entry point's name.
+struct ErrScope {
+    const char* op;
+    unsigned long long serial;
+    explicit ErrScope(const char* name) : op(name), serial(error_serial()) {}
+    int operator()(int rc) const {
+        if (rc != GPT2_OK && error_serial() == serial) set_error(rc, "%s: %s", op, code_text(rc));
+        return rc;
+    }
+};
+
 }  // namespace
 
 static int noalloc_err_of(int dev, unsigned int* bits);
@@ -71,13 +98,14 @@ extern "C" {
 
 int fused_linear_bias_gelu_softmax(const float* x, const float* W, const float* b, float* out,
                                    int M, int K, int N, void* stream) {
-    if (!x || !W || !b || !out) return GPT2_ERR_ARG;
-    if (M < 1 || K < 1 || N < 1) return GPT2_ERR_ARG;
-    if (!al16(x) || !al16(W) || !al16(b) || !al16(out) || K % 4 || N % 4) return GPT2_ERR_ALIGN;
+    const ErrScope ret("fused_linear_bias_gelu_softmax");
+    if (!x || !W || !b || !out) return ret(GPT2_ERR_ARG);
+    if (M < 1 || K < 1 || N < 1) return ret(GPT2_ERR_ARG);
+    if (!al16(x) || !al16(W) || !al16(b) || !al16(out) || K % 4 || N % 4) return ret(GPT2_ERR_ALIGN);
     int dev;
-    if (current_device(&dev) != GPT2_OK) return GPT2_ERR_CUDA;
+    if (current_device(&dev) != GPT2_OK) return ret(GPT2_ERR_CUDA);
     unsigned int* err = err_word(dev);
-    if (!err) return GPT2_ERR_NOMEM;
+    if (!err) return ret(GPT2_ERR_NOMEM);
     // the same tile choice as the allocation-free entry point (whose static
     // partials bound the narrower tiles), so the two give identical results
     const int tile_n = fused_split_tile_n(M, N, FUSED_NARROW_MAX_PARTIALS);
@@ -91,7 +119,7 @@ int fused_linear_bias_gelu_softmax(const float* x, const float* W, const float* 
             if (dev_part[dev]) cudaFree(dev_part[dev]);
             dev_part[dev] = nullptr;
             dev_part_bytes[dev] = 0;
-            if (cudaMalloc(&dev_part[dev], need) != cudaSuccess) return GPT2_ERR_NOMEM;
+            if (cudaMalloc(&dev_part[dev], need) != cudaSuccess) return ret(GPT2_ERR_NOMEM);
             dev_part_bytes[dev] = need;
         }
         scratch = (char*)dev_part[dev];
@@ -99,86 +127,90 @@ int fused_linear_bias_gelu_softmax(const float* x, const float* W, const float* 
     float* part = (float*)scratch;
     cudaStream_t s = (cudaStream_t)stream;
     const int rc = launch_fused_split_gemm(x, W, b, out, part, tiles, M, K, N, tile_n, s, err);
-    if (rc != GPT2_OK) return rc;
+    if (rc != GPT2_OK) return ret(rc);
     launch_softmax_finish(out, part, M, N, tiles, s);
-    return launch_status();
+    return ret(launch_status());
 }
 
 int gpt2_gemm(int dtype, int tensor_cores, int epilogue, const void* A, long long lda, int a_kmajor,
               const void* B, long long ldb, int b_kmajor, void* D, long long ldd, const void* bias,
               const void* aux, long long ldaux, void* D2, int M, int N, int K, float* ws,
               size_t ws_floats, void* stream) {
-    if (!A || !B || !D) return GPT2_ERR_ARG;
-    if (!known_dtype(dtype)) return GPT2_ERR_CONFIG;
-    if (epilogue < EPI_STORE || epilogue > EPI_ACCUM) return GPT2_ERR_ARG;
-    if ((epilogue == EPI_RESID || epilogue == EPI_GELU_BWD) && !aux) return GPT2_ERR_ARG;
-    if (epilogue == EPI_GELU && !D2) return GPT2_ERR_ARG;
+    const ErrScope ret("gpt2_gemm");
+    if (!A || !B || !D) return ret(GPT2_ERR_ARG);
+    if (!known_dtype(dtype)) return ret(GPT2_ERR_CONFIG);
+    if (epilogue < EPI_STORE || epilogue > EPI_ACCUM) return ret(GPT2_ERR_ARG);
+    if ((epilogue == EPI_RESID || epilogue == EPI_GELU_BWD) && !aux) return ret(GPT2_ERR_ARG);
+    if (epilogue == EPI_GELU && !D2) return ret(GPT2_ERR_ARG);
     GemmParams p = {};
     p.A = A; p.lda = lda; p.a_kmajor = a_kmajor ? 1 : 0;
     p.B = B; p.ldb = ldb; p.b_kmajor = b_kmajor ? 1 : 0;
     p.D = D; p.ldd = ldd; p.bias = bias; p.aux = aux; p.ldaux = ldaux; p.D2 = D2;
     p.M = M; p.N = N; p.K = K; p.epi = epilogue;
-    if (ws && ((uintptr_t)ws & 15u)) return GPT2_ERR_ALIGN;
+    if (ws && ((uintptr_t)ws & 15u)) return ret(GPT2_ERR_ALIGN);
     p.ws = ws; p.ws_floats = ws ? ws_floats : 0;
     const DType dt = to_dt(dtype);
     int rc;
     if (tensor_cores) {
         int dev;
-        if (current_device(&dev) != GPT2_OK) return GPT2_ERR_CUDA;
+        if (current_device(&dev) != GPT2_OK) return ret(GPT2_ERR_CUDA);
         unsigned int* err = err_word(dev);
-        if (!err) return GPT2_ERR_NOMEM;
+        if (!err) return ret(GPT2_ERR_NOMEM);
         rc = gemm_tc(p, dt, (cudaStream_t)stream, err);
     } else {
         rc = gemm_simt(p, dt, (cudaStream_t)stream);
     }
-    if (rc != GPT2_OK) return rc;
-    return launch_status();
+    if (rc != GPT2_OK) return ret(rc);
+    return ret(launch_status());
 }
 
 int gpt2_attention_forward(int dtype, int tensor_cores, const void* qkv, void* out, float* lse,
                            int B, int T, int C, int NH, void* stream) {
-    if (!qkv || !out || !lse) return GPT2_ERR_ARG;
-    if (B < 1 || T < 1 || NH < 1 || C % NH) return GPT2_ERR_ARG;
+    const ErrScope ret("gpt2_attention_forward");
+    if (!qkv || !out || !lse) return ret(GPT2_ERR_ARG);
+    if (B < 1 || T < 1 || NH < 1 || C % NH) return ret(GPT2_ERR_ARG);
     const int HS = C / NH;
-    if (HS != 16 && HS != 32 && HS != 64 && HS != 128) return GPT2_ERR_CONFIG;
-    if (!known_dtype(dtype)) return GPT2_ERR_CONFIG;
+    if (HS != 16 && HS != 32 && HS != 64 && HS != 128) return ret(GPT2_ERR_CONFIG);
+    if (!known_dtype(dtype)) return ret(GPT2_ERR_CONFIG);
     int dev;
-    if (current_device(&dev) != GPT2_OK) return GPT2_ERR_CUDA;
+    if (current_device(&dev) != GPT2_OK) return ret(GPT2_ERR_CUDA);
     unsigned int* err = err_word(dev);
-    if (!err) return GPT2_ERR_NOMEM;
+    if (!err) return ret(GPT2_ERR_NOMEM);
     const int rc = launch_attention_forward(to_dt(dtype), tensor_cores, out,
                                             lse, qkv, B, T, C, NH, (cudaStream_t)stream, err);
-    if (rc != GPT2_OK) return rc;
-    return launch_status();
+    if (rc != GPT2_OK) return ret(rc);
+    return ret(launch_status());
 }
 
 int gpt2_attention_backward(int dtype, int tensor_cores, const void* dout, const void* qkv,
                             const void* out, const float* lse, void* dqkv, float* scratch_D, int B,
                             int T, int C, int NH, void* stream) {
-    if (!dout || !qkv || !out || !lse || !dqkv || !scratch_D) return GPT2_ERR_ARG;
-    if (B < 1 || T < 1 || NH < 1 || C % NH) return GPT2_ERR_ARG;
+    const ErrScope ret("gpt2_attention_backward");
+    if (!dout || !qkv || !out || !lse || !dqkv || !scratch_D) return ret(GPT2_ERR_ARG);
+    if (B < 1 || T < 1 || NH < 1 || C % NH) return ret(GPT2_ERR_ARG);
     const int HS = C / NH;
-    if (HS != 16 && HS != 32 && HS != 64 && HS != 128) return GPT2_ERR_CONFIG;
-    if (!known_dtype(dtype)) return GPT2_ERR_CONFIG;
+    if (HS != 16 && HS != 32 && HS != 64 && HS != 128) return ret(GPT2_ERR_CONFIG);
+    if (!known_dtype(dtype)) return ret(GPT2_ERR_CONFIG);
     int dev;
-    if (current_device(&dev) != GPT2_OK) return GPT2_ERR_CUDA;
+    if (current_device(&dev) != GPT2_OK) return ret(GPT2_ERR_CUDA);
     unsigned int* err = err_word(dev);
-    if (!err) return GPT2_ERR_NOMEM;
+    if (!err) return ret(GPT2_ERR_NOMEM);
     const int rc = launch_attention_backward(to_dt(dtype), tensor_cores, dqkv,
                                              dout, qkv, out, lse, scratch_D, B, T, C, NH,
                                              (cudaStream_t)stream, err);
-    if (rc != GPT2_OK) return rc;
-    return launch_status();
+    if (rc != GPT2_OK) return ret(rc);
+    return ret(launch_status());
 }
 
 int gpt2_layernorm_forward(int dtype, void* out, float* mean, float* rstd, const void* inp,
                            const void* w, const void* b, int N, int C, void* stream) {
-    if (!out || !mean || !rstd || !inp || !w || !b) return GPT2_ERR_ARG;
-    if (!known_dtype(dtype)) return GPT2_ERR_CONFIG;
-    if (N < 1 || C < 8 || C % 8 || C > (dtype == GPT2_FP32 ? 1024 : 2048)) return GPT2_ERR_ARG;
+    const ErrScope ret("gpt2_layernorm_forward");
+    if (!out || !mean || !rstd || !inp || !w || !b) return ret(GPT2_ERR_ARG);
+    if (!known_dtype(dtype)) return ret(GPT2_ERR_CONFIG);
+    if (N < 1 || C < 8 || C % 8 || C > (dtype == GPT2_FP32 ? 1024 : 2048)) return ret(GPT2_ERR_ARG);
     launch_layernorm_forward(to_dt(dtype), out, mean, rstd, inp, w, b, N,
                              C, (cudaStream_t)stream);
-    return launch_status();
+    return ret(launch_status());
 }
 
 size_t gpt2_layernorm_backward_scratch_floats(int C) { return layernorm_backward_ws_floats(C); }
@@ -186,25 +218,27 @@ size_t gpt2_layernorm_backward_scratch_floats(int C) { return layernorm_backward
 int gpt2_layernorm_backward(int dtype, void* dinp, void* dw, void* db, const void* dout,
                             const void* inp, const void* w, const float* mean, const float* rstd,
                             int N, int C, int accumulate, float* scratch, void* stream) {
-    if (!dinp || !dw || !db || !dout || !inp || !w || !mean || !rstd || !scratch) return GPT2_ERR_ARG;
-    if (!known_dtype(dtype)) return GPT2_ERR_CONFIG;
-    if (N < 1 || C < 8 || C % 8 || C > (dtype == GPT2_FP32 ? 1024 : 2048)) return GPT2_ERR_ARG;
+    const ErrScope ret("gpt2_layernorm_backward");
+    if (!dinp || !dw || !db || !dout || !inp || !w || !mean || !rstd || !scratch) return ret(GPT2_ERR_ARG);
+    if (!known_dtype(dtype)) return ret(GPT2_ERR_CONFIG);
+    if (N < 1 || C < 8 || C % 8 || C > (dtype == GPT2_FP32 ? 1024 : 2048)) return ret(GPT2_ERR_ARG);
     int dev;
-    if (current_device(&dev) != GPT2_OK) return GPT2_ERR_CUDA;
+    if (current_device(&dev) != GPT2_OK) return ret(GPT2_ERR_CUDA);
     unsigned int* err = err_word(dev);
-    if (!err) return GPT2_ERR_NOMEM;
+    if (!err) return ret(GPT2_ERR_NOMEM);
     launch_layernorm_backward(to_dt(dtype), dinp, dw, db, dout, inp, w, mean,
                               rstd, N, C, accumulate, scratch, err, (cudaStream_t)stream);
-    return launch_status();
+    return ret(launch_status());
 }
 
 int gpt2_device_status(void) {
+    const ErrScope ret("gpt2_device_status");
     int dev;
-    if (current_device(&dev) != GPT2_OK) return GPT2_ERR_CUDA;
-    if (cudaDeviceSynchronize() != cudaSuccess) return GPT2_ERR_CUDA;
+    if (current_device(&dev) != GPT2_OK) return ret(GPT2_ERR_CUDA);
+    if (cudaDeviceSynchronize() != cudaSuccess) return ret(GPT2_ERR_CUDA);
     unsigned int h = 0;
     // the allocation-free variant's word (only once it has been set up here)
-    if (noalloc_err_of(dev, &h) != GPT2_OK) return GPT2_ERR_CUDA;
+    if (noalloc_err_of(dev, &h) != GPT2_OK) return ret(GPT2_ERR_CUDA);
     // the shared word of the allocating entry points; none exists until one of
     // them ran on this device, and then nothing can have been recorded
     unsigned int* err = nullptr;
@@ -214,11 +248,11 @@ int gpt2_device_status(void) {
     }
     if (err) {
         unsigned int h2 = 0;
-        if (cudaMemcpy(&h2, err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return GPT2_ERR_CUDA;
+        if (cudaMemcpy(&h2, err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return ret(GPT2_ERR_CUDA);
         if (h2) cudaMemset(err, 0, 4);
         h |= h2;
     }
-    if (h & DEVERR_TIMEOUT) return GPT2_ERR_DEVICE_TIMEOUT;
+    if (h & DEVERR_TIMEOUT) return ret(GPT2_ERR_DEVICE_TIMEOUT);
     return GPT2_OK;
 }
 
@@ -302,6 +336,7 @@ static int noalloc_err_of(int dev, unsigned int* bits) {
 extern "C" int fused_linear_bias_gelu_softmax_noalloc(const float* x, const float* W,
                                                       const float* b, float* out, int M, int K,
                                                       int N, void* stream) {
+    const ErrScope ret("fused_linear_bias_gelu_softmax_noalloc");
     if (!x || !W || !b || !out) return gk::set_error(GPT2_ERR_ARG, "fused op (no-alloc): NULL pointer");
     if (M < 1 || K < 1 || N < 1)
         return gk::set_error(GPT2_ERR_ARG, "fused op (no-alloc): M, K, N must be >= 1");
@@ -324,7 +359,7 @@ extern "C" int fused_linear_bias_gelu_softmax_noalloc(const float* x, const floa
         return gk::set_error(GPT2_ERR_CUDA, "fused op (no-alloc): cudaGetSymbolAddress failed");
     cudaStream_t s = (cudaStream_t)stream;
     const int rc = launch_fused_split_gemm(x, W, b, out, d.part, (int)tiles, M, K, N, tile_n, s, d.err);
-    if (rc != GPT2_OK) return rc;
+    if (rc != GPT2_OK) return ret(rc);
     launch_softmax_finish(out, d.part, M, N, (int)tiles, s);
     if (cudaGetLastError() != cudaSuccess)
         return gk::set_error(GPT2_ERR_CUDA, "fused op (no-alloc): launch failed");

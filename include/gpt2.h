@@ -36,7 +36,7 @@ extern "C" {
 #define GPT2_ERR_STATE (-2)          /* call out of order (no model, backward before forward, ...) */
 #define GPT2_ERR_SHAPE (-3)          /* B or T differs from the first forward, or T > maxT */
 #define GPT2_ERR_TOKEN (-4)          /* a token or target id outside [0, V) */
-#define GPT2_ERR_ALIGN (-5)          /* pointer or leading dimension not 16-byte aligned */
+#define GPT2_ERR_ALIGN (-5)          /* pointer, leading dimension or size not aligned as the call requires */
 #define GPT2_ERR_CUDA (-6)           /* a CUDA runtime/driver call failed */
 #define GPT2_ERR_NOMEM (-7)          /* device or pinned-host allocation failed */
 #define GPT2_ERR_ARG (-8)            /* NULL pointer or out-of-range scalar argument */
@@ -315,6 +315,9 @@ int fused_linear_bias_gelu_softmax_noalloc(const float* x, const float* W, const
  *  gelu_backward, residual_forward.) bias may be NULL. Tensor-core path needs
  *  16-byte aligned pointers and leading dimensions and N % (16/elem) == 0, else
  *  GPT2_ERR_ALIGN.
+ *  Errors: GPT2_ERR_ARG for A, B or D NULL, M, N or K < 1, an unknown epilogue,
+ *  epilogues 2 and 3 without aux or 1 without D2; GPT2_ERR_CONFIG for an unknown
+ *  dtype or an fp32 tensor-core product with an MN-major operand.
  *  ws / ws_floats: optional DEVICE fp32 scratch, caller-owned, 16-byte aligned
  *  (NULL or 0 = none). With epilogue 4, bf16 and tensor cores, a product with
  *  fewer output tiles than the GPU has CTA slots (a weight gradient: small
@@ -331,26 +334,31 @@ int gpt2_gemm(int dtype, int tensor_cores, int epilogue, const void* A, long lon
  * lse (B,NH,T) fp32 natural-log sum of exp of the scaled scores (llm.c
  * attention_forward with softmax_forward_kernel5, scale 1/sqrt(HS)).
  * HS = C/NH in {16,32,64,128}; bf16 or fp16 with tensor_cores and HS == 64 uses the
- * tensor-core flash kernel, everything else the SIMT kernel. */
+ * tensor-core flash kernel (operands its tensor maps cannot address take a kernel
+ * without them instead), everything else the SIMT kernel. Errors: GPT2_ERR_ARG for a NULL
+ * pointer, B, T or NH < 1 or C % NH != 0; GPT2_ERR_CONFIG for another head size or an
+ * unknown dtype. */
 int gpt2_attention_forward(int dtype, int tensor_cores, const void* qkv, void* out, float* lse,
                            int B, int T, int C, int NH, void* stream);
 
 /* Its backward: dqkv (B,T,3C) is written (llm.c attention_backward with
- * softmax_autoregressive_backward_kernel); scratch_D is B*NH*T floats. */
+ * softmax_autoregressive_backward_kernel); scratch_D is B*NH*T floats. Same
+ * size rules and errors as the forward. */
 int gpt2_attention_backward(int dtype, int tensor_cores, const void* dout, const void* qkv,
                             const void* out, const float* lse, void* dqkv, float* scratch_D, int B,
                             int T, int C, int NH, void* stream);
 
 /* LayerNorm over the last dimension C of N rows (llm.c "train_gpt2.cu",
  * layernorm_forward_kernel3): biased variance, eps 1e-5; out (N,C), mean and
- * rstd (N) fp32. C % 8 == 0, C <= 2048 (bf16) / 1024 (fp32). */
+ * rstd (N) fp32. N >= 1, C % 8 == 0, 8 <= C <= 2048 (16-bit) / 1024 (fp32), else
+ * GPT2_ERR_ARG (also for a NULL pointer); GPT2_ERR_CONFIG for an unknown dtype. */
 int gpt2_layernorm_forward(int dtype, void* out, float* mean, float* rstd, const void* inp,
                            const void* w, const void* b, int N, int C, void* stream);
 
 /* Its backward (layernorm_backward_kernel6 with += for every output): dinp +=
  * (or = when accumulate == 0), dw += and db += sums over the N rows, computed
  * deterministically through `scratch` (fp32, gpt2_layernorm_backward_scratch_floats(C)
- * floats, caller-owned). */
+ * floats, caller-owned). Same size rules and errors as the forward. */
 size_t gpt2_layernorm_backward_scratch_floats(int C);
 int gpt2_layernorm_backward(int dtype, void* dinp, void* dw, void* db, const void* dout,
                             const void* inp, const void* w, const float* mean, const float* rstd,

@@ -37,3 +37,16 @@ def test_binding_declares_the_same_names():
     from transformer_lm_gb300 import gpt2
     names = set(_declared_functions())
     assert names == set(gpt2._SIGS), names ^ set(gpt2._SIGS)
+    # and a Python function of the same name for each
+    missing = [n for n in names if not callable(getattr(gpt2, n, None))]
+    assert not missing, missing
+
+
+@pytest.mark.skipif(shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                    reason="no CUDA toolkit")
+def test_status_queries_through_the_binding_need_no_gpu():
+    from transformer_lm_gb300 import build, gpt2
+    build.build()
+    assert gpt2.gpt2_last_status() in gpt2.ERRORS
+    assert isinstance(gpt2.gpt2_last_error(), str) and gpt2.gpt2_last_error()
+    assert gpt2.gpt2_launch_count() >= 0

@@ -321,7 +321,7 @@ def test_stand_alone_entry_points_reject_bad_arguments_with_a_message():
             fn(*args, **kw)
         assert e.value.code == code, e.value
         assert text in G.gpt2_last_error(), G.gpt2_last_error()
-        assert G.lib().gpt2_last_status() == code
+        assert G.gpt2_last_status() == code
 
     for fused in (G.fused_linear_bias_gelu_softmax, G.fused_linear_bias_gelu_softmax_noalloc):
         name = fused.__name__

@@ -118,6 +118,10 @@ def gpt2_last_error() -> str:
     return lib().gpt2_last_error().decode()
 
 
+def gpt2_last_status() -> int:
+    return int(lib().gpt2_last_status())
+
+
 def _check(name: str, rc: int) -> None:
     if rc != 0:
         raise GPT2Error(name, rc, gpt2_last_error())
@@ -157,7 +161,7 @@ def gpt2_forward(tokens, targets, B, T) -> float:
     tgt = None if targets is None else _ints(targets)
     loss = lib().gpt2_forward(_as_ip(tok), _as_ip(tgt), B, T)
     if np.isnan(loss):
-        raise GPT2Error("gpt2_forward", int(lib().gpt2_last_status()), gpt2_last_error())
+        raise GPT2Error("gpt2_forward", gpt2_last_status(), gpt2_last_error())
     return float(loss)
 
 

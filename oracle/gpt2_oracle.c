@@ -686,7 +686,8 @@ float oracle_random_f32(unsigned long long* state) {
 /* [P1] SquirrelNoise5 (Squirrel Eiserloh's position hash, version 5): the
  * position times a constant, plus the seed, then four rounds of
  * xorshift-right / add-or-multiply by a constant, and a last xorshift.
- * All arithmetic is modulo 2^32. */
+ * All arithmetic is modulo 2^32. Parity unpinned for the exact values (the
+ * page prints none to check against). */
 unsigned int oracle_squirrel_noise5(unsigned int position, unsigned int seed) {
     unsigned int b = position;
     b *= 0xd2a80a3fu;
